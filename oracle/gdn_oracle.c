@@ -1,0 +1,512 @@
+/*
+ * gdn_oracle.c -- fp64 CPU oracle for the gated delta rule (GatedDeltaNet).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file; only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark use it.  It shares no code, header or constant with the CUDA
+ * library.
+ *
+ * What it computes, and where each step is defined:
+ *
+ *  - Op contract (torch-to-nnef, "custom_extractors/gdn", op contract):
+ *      q, k      [B, T, Hk, Dk]
+ *      v         [B, T, Hv, Dv]     Hv = G * Hk, value head h reads q/k head h / G
+ *      state     [B, Hv, Dk, Dv]
+ *      output    [B, T, Hv, Dv],  final_state [B, Hv, Dk, Dv]
+ *    q and k are L2-normalised with eps 1e-6 and q is scaled by 1/sqrt(Dk)
+ *    inside the op.  The contract states a single width w; this oracle keeps
+ *    Dk and Dv separate (the mlx-lm page's performance section uses Dk=192,
+ *    Dv=128).
+ *  - Gates (mlx-lm PR "Add gated_delta_update VJP", "What this PR adds" and
+ *    "Covered corner cases"): g = exp(-exp(A_log) * softplus(a + dt_bias))
+ *    with the softplus argument clamped, beta = sigmoid(b).  The clamp value
+ *    is not printed; this oracle uses softplus(min(x, 20)) whose derivative is
+ *    sigmoid(x) for x <= 20 and 0 above.
+ *  - Recurrence (the recurrent step that both pages name): per (b, h)
+ *      S <- g S;  delta = beta (v - S^T k);  S <- S + k delta^T;  o = S^T q.
+ *    A masked step leaves S unchanged (mlx-lm page, "Covered corner cases":
+ *    the half-masked final state equals the state after the unmasked prefix);
+ *    the page fixes only the state, so the output of a masked step is read as
+ *    o = S^T q with the unchanged state.
+ *  - VJP (mlx-lm page, "What this PR adds": gradients for q, k, v, a, b,
+ *    A_log, dt_bias and state): plain reverse-mode differentiation of the
+ *    sequential recurrence above, derived by hand, with the state stored
+ *    every 64 steps and recomputed inside each 64-step segment (mlx-lm page,
+ *    "Design notes": CHUNK_SIZE = 64 bounds memory to one chunk).
+ *  - Chunked form (torch-to-nnef page: the chunked rule computes the same
+ *    recurrence with different blocking; mlx-lm page, "Scope and
+ *    follow-ups": chunk-parallel rewrite through a lower-triangular solve):
+ *    an independent fp64 forward in the WY/UT form, used only to check that
+ *    chunked equals sequential up to rounding.
+ *
+ * Everything is fp64.  Parallelism: OpenMP over independent (b, h) pairs;
+ * all cross-pair sums run afterwards in a fixed serial order.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define NORM_EPS 1e-6
+#define SOFTPLUS_CLAMP 20.0
+#define SEGMENT 64
+
+/* ---- scalar helpers ---------------------------------------------------- */
+
+static double sigmoid_d(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* softplus with its argument clamped from above (reading of the clamp). */
+static double softplus_clamped(double x) {
+    double xc = x < SOFTPLUS_CLAMP ? x : SOFTPLUS_CLAMP;
+    return log1p(exp(xc));
+}
+
+/* d/dx softplus(min(x, 20)) */
+static double softplus_clamped_grad(double x) {
+    return x <= SOFTPLUS_CLAMP ? sigmoid_d(x) : 0.0;
+}
+
+/* log-decay l = log g = -exp(A_log) * softplus(min(a + dt_bias, 20)) */
+static double log_decay(double a, double A_log, double dt_bias) {
+    return -exp(A_log) * softplus_clamped(a + dt_bias);
+}
+
+/* 1 / sqrt(sum x^2 + eps) over n entries */
+static double inv_norm(const double* x, int64_t n) {
+    double s = 0.0;
+    for (int64_t i = 0; i < n; ++i) s += x[i] * x[i];
+    return 1.0 / sqrt(s + NORM_EPS);
+}
+
+typedef struct {
+    int64_t B, T, Hk, Hv, Dk, Dv;
+} dims_t;
+
+static int check_dims(const dims_t* d) {
+    if (d->B < 1 || d->T < 0 || d->Hk < 1 || d->Hv < 1 || d->Dk < 1 || d->Dv < 1) return 1;
+    if (d->Hv % d->Hk) return 2;
+    return 0;
+}
+
+/* index helpers (row-major, contiguous) */
+#define IQK(d, b, t, j) ((((b) * (d)->T + (t)) * (d)->Hk + (j)) * (d)->Dk)
+#define IV(d, b, t, h) ((((b) * (d)->T + (t)) * (d)->Hv + (h)) * (d)->Dv)
+#define IG(d, b, t, h) (((b) * (d)->T + (t)) * (d)->Hv + (h))
+#define IS(d, b, h) (((b) * (d)->Hv + (h)) * (d)->Dk * (d)->Dv)
+
+/* Normalised query / key of step t for value head h (GQA: key head h / G). */
+static void load_qk_hat(const dims_t* d, const double* q, const double* k, int64_t b,
+                        int64_t t, int64_t h, double* qh, double* kh) {
+    int64_t G = d->Hv / d->Hk, j = h / G;
+    const double* qp = q + IQK(d, b, t, j);
+    const double* kp = k + IQK(d, b, t, j);
+    double rq = inv_norm(qp, d->Dk) / sqrt((double)d->Dk);
+    double rk = inv_norm(kp, d->Dk);
+    for (int64_t i = 0; i < d->Dk; ++i) {
+        qh[i] = qp[i] * rq;
+        kh[i] = kp[i] * rk;
+    }
+}
+
+/* One applied step of the recurrence on S (Dk x Dv, row-major).
+ * Returns delta in dl, the prediction p = (gS)^T k in p. */
+static void apply_step(int64_t Dk, int64_t Dv, double* S, double g, double beta,
+                       const double* kh, const double* v, double* p, double* dl) {
+    for (int64_t i = 0; i < Dk * Dv; ++i) S[i] *= g;
+    for (int64_t c = 0; c < Dv; ++c) p[c] = 0.0;
+    for (int64_t r = 0; r < Dk; ++r)
+        for (int64_t c = 0; c < Dv; ++c) p[c] += S[r * Dv + c] * kh[r];
+    for (int64_t c = 0; c < Dv; ++c) dl[c] = beta * (v[c] - p[c]);
+    for (int64_t r = 0; r < Dk; ++r)
+        for (int64_t c = 0; c < Dv; ++c) S[r * Dv + c] += kh[r] * dl[c];
+}
+
+/* o = S^T qh */
+static void read_out(int64_t Dk, int64_t Dv, const double* S, const double* qh, double* o) {
+    for (int64_t c = 0; c < Dv; ++c) o[c] = 0.0;
+    for (int64_t r = 0; r < Dk; ++r)
+        for (int64_t c = 0; c < Dv; ++c) o[c] += S[r * Dv + c] * qh[r];
+}
+
+/* ---- sequential forward -------------------------------------------------- */
+
+int gdn_oracle_forward(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk, int64_t Dv,
+                       const double* q, const double* k, const double* v, const double* a,
+                       const double* b, const double* A_log, const double* dt_bias,
+                       const double* state0, const uint8_t* mask, double* o,
+                       double* state_T) {
+    dims_t d = {B, T, Hk, Hv, Dk, Dv};
+    int rc = check_dims(&d);
+    if (rc) return rc;
+    int64_t npairs = B * Hv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t pr = 0; pr < npairs; ++pr) {
+        int64_t bb = pr / Hv, h = pr % Hv;
+        double* S = state_T + IS(&d, bb, h);
+        if (state0)
+            memcpy(S, state0 + IS(&d, bb, h), sizeof(double) * Dk * Dv);
+        else
+            memset(S, 0, sizeof(double) * Dk * Dv);
+        double* qh = malloc(sizeof(double) * Dk);
+        double* kh = malloc(sizeof(double) * Dk);
+        double* p = malloc(sizeof(double) * Dv);
+        double* dl = malloc(sizeof(double) * Dv);
+        for (int64_t t = 0; t < T; ++t) {
+            load_qk_hat(&d, q, k, bb, t, h, qh, kh);
+            int on = mask ? (mask[bb * T + t] != 0) : 1;
+            if (on) {
+                double g = exp(log_decay(a[IG(&d, bb, t, h)], A_log[h], dt_bias[h]));
+                double beta = sigmoid_d(b[IG(&d, bb, t, h)]);
+                apply_step(Dk, Dv, S, g, beta, kh, v + IV(&d, bb, t, h), p, dl);
+            }
+            read_out(Dk, Dv, S, qh, o + IV(&d, bb, t, h));
+        }
+        free(qh); free(kh); free(p); free(dl);
+    }
+    return 0;
+}
+
+/* ---- chunked (WY/UT) forward: second, independent formulation ------------- */
+/*
+ * Inside one chunk of L steps with start state S0 (all quantities local):
+ *   Gam_i = sum_{s<=i} l_s, gam_i = exp(Gam_i), M_ij = exp(Gam_i - Gam_j) (j<=i)
+ *   A_ij  = beta_i M_ij <k_i, k_j>            (j < i, strictly lower)
+ *   (I + A) X = R  solved by forward substitution for
+ *        R = [diag(beta) V | diag(beta gam) K]  ->  X = [U | W]
+ *   Delta = U - W S0
+ *   O     = diag(gam) Q S0 + P Delta,   P_ij = M_ij <q_i, k_j>  (j <= i)
+ *   S     = gam_L S0 + K^T diag(e) Delta,   e_j = exp(Gam_L - Gam_j)
+ * Masked steps enter as l = 0, beta = 0 (an identity step).
+ */
+int gdn_oracle_forward_chunked(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk,
+                               int64_t Dv, int64_t C, const double* q, const double* k,
+                               const double* v, const double* a, const double* b,
+                               const double* A_log, const double* dt_bias,
+                               const double* state0, const uint8_t* mask, double* o,
+                               double* state_T) {
+    dims_t d = {B, T, Hk, Hv, Dk, Dv};
+    int rc = check_dims(&d);
+    if (rc) return rc;
+    if (C < 1) return 1;
+    int64_t npairs = B * Hv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t pr = 0; pr < npairs; ++pr) {
+        int64_t bb = pr / Hv, h = pr % Hv;
+        double* S = state_T + IS(&d, bb, h);
+        if (state0)
+            memcpy(S, state0 + IS(&d, bb, h), sizeof(double) * Dk * Dv);
+        else
+            memset(S, 0, sizeof(double) * Dk * Dv);
+        double* Q = malloc(sizeof(double) * C * Dk);
+        double* K = malloc(sizeof(double) * C * Dk);
+        double* V = malloc(sizeof(double) * C * Dv);
+        double* lg = malloc(sizeof(double) * C);
+        double* bt = malloc(sizeof(double) * C);
+        double* Gm = malloc(sizeof(double) * C);
+        double* A = malloc(sizeof(double) * C * C);
+        double* U = malloc(sizeof(double) * C * Dv);
+        double* W = malloc(sizeof(double) * C * Dk);
+        double* Dl = malloc(sizeof(double) * C * Dv);
+        double* Snew = malloc(sizeof(double) * Dk * Dv);
+        for (int64_t t0 = 0; t0 < T; t0 += C) {
+            int64_t L = (T - t0) < C ? (T - t0) : C;
+            for (int64_t i = 0; i < L; ++i) {
+                int64_t t = t0 + i;
+                load_qk_hat(&d, q, k, bb, t, h, Q + i * Dk, K + i * Dk);
+                memcpy(V + i * Dv, v + IV(&d, bb, t, h), sizeof(double) * Dv);
+                int on = mask ? (mask[bb * T + t] != 0) : 1;
+                lg[i] = on ? log_decay(a[IG(&d, bb, t, h)], A_log[h], dt_bias[h]) : 0.0;
+                bt[i] = on ? sigmoid_d(b[IG(&d, bb, t, h)]) : 0.0;
+                Gm[i] = (i ? Gm[i - 1] : 0.0) + lg[i];
+            }
+            /* A (strictly lower) */
+            for (int64_t i = 0; i < L; ++i)
+                for (int64_t j = 0; j < i; ++j) {
+                    double kk = 0.0;
+                    for (int64_t r = 0; r < Dk; ++r) kk += K[i * Dk + r] * K[j * Dk + r];
+                    A[i * C + j] = bt[i] * exp(Gm[i] - Gm[j]) * kk;
+                }
+            /* forward substitution: (I + A) [U | W] = [diag(beta) V | diag(beta gam) K] */
+            for (int64_t i = 0; i < L; ++i) {
+                double gi = exp(Gm[i]);
+                for (int64_t c = 0; c < Dv; ++c) U[i * Dv + c] = bt[i] * V[i * Dv + c];
+                for (int64_t r = 0; r < Dk; ++r) W[i * Dk + r] = bt[i] * gi * K[i * Dk + r];
+                for (int64_t j = 0; j < i; ++j) {
+                    double aij = A[i * C + j];
+                    for (int64_t c = 0; c < Dv; ++c) U[i * Dv + c] -= aij * U[j * Dv + c];
+                    for (int64_t r = 0; r < Dk; ++r) W[i * Dk + r] -= aij * W[j * Dk + r];
+                }
+            }
+            /* Delta = U - W S0 */
+            for (int64_t i = 0; i < L; ++i)
+                for (int64_t c = 0; c < Dv; ++c) {
+                    double ws = 0.0;
+                    for (int64_t r = 0; r < Dk; ++r) ws += W[i * Dk + r] * S[r * Dv + c];
+                    Dl[i * Dv + c] = U[i * Dv + c] - ws;
+                }
+            /* O = diag(gam) Q S0 + P Delta */
+            for (int64_t i = 0; i < L; ++i) {
+                double* oi = o + IV(&d, bb, t0 + i, h);
+                double gi = exp(Gm[i]);
+                for (int64_t c = 0; c < Dv; ++c) {
+                    double qs = 0.0;
+                    for (int64_t r = 0; r < Dk; ++r) qs += Q[i * Dk + r] * S[r * Dv + c];
+                    oi[c] = gi * qs;
+                }
+                for (int64_t j = 0; j <= i; ++j) {
+                    double qk = 0.0;
+                    for (int64_t r = 0; r < Dk; ++r) qk += Q[i * Dk + r] * K[j * Dk + r];
+                    double pij = exp(Gm[i] - Gm[j]) * qk;
+                    for (int64_t c = 0; c < Dv; ++c) oi[c] += pij * Dl[j * Dv + c];
+                }
+            }
+            /* S = gam_L S0 + K^T diag(e) Delta */
+            double gL = exp(Gm[L - 1]);
+            for (int64_t r = 0; r < Dk; ++r)
+                for (int64_t c = 0; c < Dv; ++c) Snew[r * Dv + c] = gL * S[r * Dv + c];
+            for (int64_t j = 0; j < L; ++j) {
+                double ej = exp(Gm[L - 1] - Gm[j]);
+                for (int64_t r = 0; r < Dk; ++r) {
+                    double kr = ej * K[j * Dk + r];
+                    for (int64_t c = 0; c < Dv; ++c) Snew[r * Dv + c] += kr * Dl[j * Dv + c];
+                }
+            }
+            memcpy(S, Snew, sizeof(double) * Dk * Dv);
+        }
+        free(Q); free(K); free(V); free(lg); free(bt); free(Gm); free(A);
+        free(U); free(W); free(Dl); free(Snew);
+    }
+    return 0;
+}
+
+/* ---- sequential VJP ------------------------------------------------------ */
+/*
+ * Reverse-mode derivative of the sequential recurrence, per (b, h).  For an
+ * applied step with previous state S_prev:
+ *     S_a = g S_prev,  p = S_a^T k,  delta = beta (v - p),
+ *     S   = S_a + k delta^T,  o = S^T q.
+ * With Sbar = dL/dS (from later steps) and obar = dL/do:
+ *     Sbar  += q obar^T;          qbar  = S obar
+ *     kbar   = Sbar delta;        dbar  = Sbar^T k
+ *     vbar   = beta dbar;         betabar = <dbar, v - p>;   pbar = -beta dbar
+ *     Sbar_a = Sbar + k pbar^T;   kbar += S_a pbar
+ *     gbar   = <Sbar_a, S_prev>;  Sbar_prev = g Sbar_a;       lbar = gbar g
+ * A masked step only adds q obar^T to Sbar and gives qbar = S obar.
+ * Then, outside the (b, h) loop, in a fixed order:
+ *   - GQA: dqhat / dkhat of key head j = sum over its G value heads (ascending h)
+ *   - L2 norm: xhat = s x / n, n = sqrt(|x|^2 + eps):
+ *         dx = (s / n) (xhatbar - u <u, xhatbar>),  u = x / n
+ *     (s = 1/sqrt(Dk) for q, 1 for k; written without n^2 or n^3 terms)
+ *   - gates: da = lbar * (-exp(A_log)) * softplus'(a + dt_bias);
+ *            db = betabar * beta (1 - beta);
+ *            dA_log[h] = sum_{b,t} lbar * l;  ddt_bias[h] = sum_{b,t} da
+ */
+int gdn_oracle_backward(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk, int64_t Dv,
+                        const double* q, const double* k, const double* v, const double* a,
+                        const double* b, const double* A_log, const double* dt_bias,
+                        const double* state0, const uint8_t* mask, const double* d_o,
+                        const double* d_state_T, double* dq, double* dk, double* dv,
+                        double* da, double* db, double* dA_log, double* ddt_bias,
+                        double* dstate0) {
+    dims_t d = {B, T, Hk, Hv, Dk, Dv};
+    int rc = check_dims(&d);
+    if (rc) return rc;
+    int64_t G = Hv / Hk;
+    int64_t SS = Dk * Dv;
+    int64_t nseg = (T + SEGMENT - 1) / SEGMENT;
+    /* per value head gradients of the normalised q / k, and of l, beta */
+    double* dqh = calloc((size_t)(B * T * Hv * Dk > 0 ? B * T * Hv * Dk : 1), sizeof(double));
+    double* dkh = calloc((size_t)(B * T * Hv * Dk > 0 ? B * T * Hv * Dk : 1), sizeof(double));
+    double* dlg = calloc((size_t)(B * T * Hv > 0 ? B * T * Hv : 1), sizeof(double));
+    double* dbt = calloc((size_t)(B * T * Hv > 0 ? B * T * Hv : 1), sizeof(double));
+    if (!dqh || !dkh || !dlg || !dbt) { free(dqh); free(dkh); free(dlg); free(dbt); return 3; }
+    int64_t npairs = B * Hv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t pr = 0; pr < npairs; ++pr) {
+        int64_t bb = pr / Hv, h = pr % Hv;
+        /* states at segment starts */
+        double* seg = malloc(sizeof(double) * SS * (nseg > 0 ? nseg : 1));
+        /* states after every step of one segment (index 0 = segment start) */
+        double* hist = malloc(sizeof(double) * SS * (SEGMENT + 1));
+        double* Sb = malloc(sizeof(double) * SS);
+        double* Sa = malloc(sizeof(double) * SS);
+        double* qh = malloc(sizeof(double) * Dk);
+        double* kh = malloc(sizeof(double) * Dk);
+        double* p = malloc(sizeof(double) * Dv);
+        double* dl = malloc(sizeof(double) * Dv);
+        double* dbar = malloc(sizeof(double) * Dv);
+        double* pbar = malloc(sizeof(double) * Dv);
+        double* S = malloc(sizeof(double) * SS);
+        if (state0)
+            memcpy(S, state0 + IS(&d, bb, h), sizeof(double) * SS);
+        else
+            memset(S, 0, sizeof(double) * SS);
+        /* forward pass, keeping only segment-start states */
+        for (int64_t t = 0; t < T; ++t) {
+            if (t % SEGMENT == 0) memcpy(seg + (t / SEGMENT) * SS, S, sizeof(double) * SS);
+            int on = mask ? (mask[bb * T + t] != 0) : 1;
+            if (on) {
+                load_qk_hat(&d, q, k, bb, t, h, qh, kh);
+                double g = exp(log_decay(a[IG(&d, bb, t, h)], A_log[h], dt_bias[h]));
+                double beta = sigmoid_d(b[IG(&d, bb, t, h)]);
+                apply_step(Dk, Dv, S, g, beta, kh, v + IV(&d, bb, t, h), p, dl);
+            }
+        }
+        /* seed: dL/dS_T */
+        if (d_state_T)
+            memcpy(Sb, d_state_T + IS(&d, bb, h), sizeof(double) * SS);
+        else
+            memset(Sb, 0, sizeof(double) * SS);
+        for (int64_t sg = nseg - 1; sg >= 0; --sg) {
+            int64_t t0 = sg * SEGMENT;
+            int64_t L = (T - t0) < SEGMENT ? (T - t0) : SEGMENT;
+            /* recompute states of this segment */
+            memcpy(hist, seg + sg * SS, sizeof(double) * SS);
+            for (int64_t i = 0; i < L; ++i) {
+                int64_t t = t0 + i;
+                double* Sn = hist + (i + 1) * SS;
+                memcpy(Sn, hist + i * SS, sizeof(double) * SS);
+                int on = mask ? (mask[bb * T + t] != 0) : 1;
+                if (on) {
+                    load_qk_hat(&d, q, k, bb, t, h, qh, kh);
+                    double g = exp(log_decay(a[IG(&d, bb, t, h)], A_log[h], dt_bias[h]));
+                    double beta = sigmoid_d(b[IG(&d, bb, t, h)]);
+                    apply_step(Dk, Dv, Sn, g, beta, kh, v + IV(&d, bb, t, h), p, dl);
+                }
+            }
+            /* reverse steps */
+            for (int64_t i = L - 1; i >= 0; --i) {
+                int64_t t = t0 + i;
+                const double* Sprev = hist + i * SS;
+                const double* Scur = hist + (i + 1) * SS;
+                const double* ob = d_o + IV(&d, bb, t, h);
+                double* qbar = dqh + ((bb * T + t) * Hv + h) * Dk;
+                double* kbar = dkh + ((bb * T + t) * Hv + h) * Dk;
+                load_qk_hat(&d, q, k, bb, t, h, qh, kh);
+                /* o = S^T q */
+                for (int64_t r = 0; r < Dk; ++r) {
+                    double acc = 0.0;
+                    for (int64_t c = 0; c < Dv; ++c) {
+                        Sb[r * Dv + c] += qh[r] * ob[c];
+                        acc += Scur[r * Dv + c] * ob[c];
+                    }
+                    qbar[r] = acc;
+                }
+                int on = mask ? (mask[bb * T + t] != 0) : 1;
+                if (!on) continue;
+                double lgv = log_decay(a[IG(&d, bb, t, h)], A_log[h], dt_bias[h]);
+                double g = exp(lgv);
+                double beta = sigmoid_d(b[IG(&d, bb, t, h)]);
+                const double* vt = v + IV(&d, bb, t, h);
+                /* S_a = g S_prev, p = S_a^T k, delta = beta (v - p) */
+                for (int64_t x = 0; x < SS; ++x) Sa[x] = g * Sprev[x];
+                for (int64_t c = 0; c < Dv; ++c) p[c] = 0.0;
+                for (int64_t r = 0; r < Dk; ++r)
+                    for (int64_t c = 0; c < Dv; ++c) p[c] += Sa[r * Dv + c] * kh[r];
+                for (int64_t c = 0; c < Dv; ++c) dl[c] = beta * (vt[c] - p[c]);
+                /* S = S_a + k delta^T */
+                for (int64_t r = 0; r < Dk; ++r) {
+                    double acc = 0.0;
+                    for (int64_t c = 0; c < Dv; ++c) acc += Sb[r * Dv + c] * dl[c];
+                    kbar[r] = acc;
+                }
+                for (int64_t c = 0; c < Dv; ++c) {
+                    double acc = 0.0;
+                    for (int64_t r = 0; r < Dk; ++r) acc += Sb[r * Dv + c] * kh[r];
+                    dbar[c] = acc;
+                }
+                /* delta = beta (v - p) */
+                double betabar = 0.0;
+                double* vbar = dv + IV(&d, bb, t, h);
+                for (int64_t c = 0; c < Dv; ++c) {
+                    vbar[c] = beta * dbar[c];
+                    betabar += dbar[c] * (vt[c] - p[c]);
+                    pbar[c] = -beta * dbar[c];
+                }
+                /* p = S_a^T k */
+                for (int64_t r = 0; r < Dk; ++r) {
+                    double acc = 0.0;
+                    for (int64_t c = 0; c < Dv; ++c) {
+                        Sb[r * Dv + c] += kh[r] * pbar[c];
+                        acc += Sa[r * Dv + c] * pbar[c];
+                    }
+                    kbar[r] += acc;
+                }
+                /* S_a = g S_prev */
+                double gbar = 0.0;
+                for (int64_t x = 0; x < SS; ++x) gbar += Sb[x] * Sprev[x];
+                for (int64_t x = 0; x < SS; ++x) Sb[x] *= g;
+                dlg[IG(&d, bb, t, h)] = gbar * g;
+                dbt[IG(&d, bb, t, h)] = betabar;
+            }
+        }
+        memcpy(dstate0 + IS(&d, bb, h), Sb, sizeof(double) * SS);
+        free(seg); free(hist); free(Sb); free(Sa); free(qh); free(kh);
+        free(p); free(dl); free(dbar); free(pbar); free(S);
+    }
+    /* v gradient is zero on masked steps */
+    if (mask)
+        for (int64_t bb = 0; bb < B; ++bb)
+            for (int64_t t = 0; t < T; ++t)
+                if (!mask[bb * T + t])
+                    for (int64_t h = 0; h < Hv; ++h)
+                        memset(dv + IV(&d, bb, t, h), 0, sizeof(double) * Dv);
+    /* GQA sum + L2-norm backward, per (b, t, key head) */
+    double* acc = malloc(sizeof(double) * Dk);
+    double sq = 1.0 / sqrt((double)Dk);
+    for (int64_t bb = 0; bb < B; ++bb)
+        for (int64_t t = 0; t < T; ++t)
+            for (int64_t j = 0; j < Hk; ++j) {
+                for (int pass = 0; pass < 2; ++pass) {
+                    const double* x = (pass == 0 ? q : k) + IQK(&d, bb, t, j);
+                    const double* src = pass == 0 ? dqh : dkh;
+                    double* dst = (pass == 0 ? dq : dk) + IQK(&d, bb, t, j);
+                    double s = pass == 0 ? sq : 1.0;
+                    for (int64_t r = 0; r < Dk; ++r) acc[r] = 0.0;
+                    for (int64_t h = j * G; h < (j + 1) * G; ++h) {
+                        const double* y = src + ((bb * T + t) * Hv + h) * Dk;
+                        for (int64_t r = 0; r < Dk; ++r) acc[r] += y[r];
+                    }
+                    double rn = inv_norm(x, Dk); /* 1/n */
+                    double uy = 0.0;
+                    for (int64_t r = 0; r < Dk; ++r) uy += x[r] * rn * acc[r];
+                    for (int64_t r = 0; r < Dk; ++r) dst[r] = s * rn * (acc[r] - x[r] * rn * uy);
+                }
+            }
+    free(acc);
+    /* gates and per-head sums (fixed order: b, then t) */
+    for (int64_t h = 0; h < Hv; ++h) {
+        double sA = 0.0, sdt = 0.0;
+        for (int64_t bb = 0; bb < B; ++bb)
+            for (int64_t t = 0; t < T; ++t) {
+                int64_t ix = IG(&d, bb, t, h);
+                int on = mask ? (mask[bb * T + t] != 0) : 1;
+                if (!on) { da[ix] = 0.0; db[ix] = 0.0; continue; }
+                double x = a[ix] + dt_bias[h];
+                double lgv = log_decay(a[ix], A_log[h], dt_bias[h]);
+                double dx = dlg[ix] * (-exp(A_log[h])) * softplus_clamped_grad(x);
+                double beta = sigmoid_d(b[ix]);
+                da[ix] = dx;
+                db[ix] = dbt[ix] * beta * (1.0 - beta);
+                sA += dlg[ix] * lgv;
+                sdt += dx;
+            }
+        dA_log[h] = sA;
+        ddt_bias[h] = sdt;
+    }
+    free(dqh); free(dkh); free(dlg); free(dbt);
+    return 0;
+}
+
+/* ---- threads the OpenMP runtime will use --------------------------------- */
+
+int gdn_oracle_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
