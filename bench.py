@@ -1,0 +1,537 @@
+#!/usr/bin/env python
+"""Benchmark: gated delta rule forward + VJP tokens/s on GB300 (one JSON line).
+
+Default workload: the Qwen3.5-9B GatedDeltaNet layer shape of the mlx-lm
+page's performance table (B=1, T=2048, Hk=16, Hv=64, Dk=192, Dv=128, bf16
+inputs, fp32 state), forward + full backward per step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+One process per GPU (torchrun for N > 1); every rank runs its own replica
+of the workload (weak scaling, no collective on the data path).  Timing:
+W untimed warm-up steps, then K steps each bracketed by CUDA events on the
+launching stream; L2 is flushed (256 MiB write) between timed steps outside
+the events; barrier + synchronize around the timed region; the max over
+ranks is reported.  ``value`` = tokens of all ranks / time.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference
+implementation this method has here) on the host cores, on a bounded sample
+of the same workload, and prints the same JSON line with "impl": "reference".
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from gated_delta_rule_06_gb300 import workloads as wl  # noqa: E402
+
+C = 64
+METRIC = "GDN fwd+bwd tokens/s (Qwen3.5-9B shape, T=2048) and % of TC/HBM roofline"
+DECODE_METRIC = "GDN decode tokens/s (B=256 state step) and % of HBM roofline"
+# the page's own figure for this workload: 149.8 ms fwd+bwd at T=2048 on an
+# M-series Mac (mlx-lm PR performance table) -> 2048 / 0.1498 tokens/s
+PAGE_TOKENS_PER_S = {"qwen35_9b_layer_T2048_bf16": 2048 / 0.1498}
+FP32_ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12  # SMs x FFMA lanes x 2 x max clock
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work model (per launch of each phase)
+# ---------------------------------------------------------------------------
+
+def work_model(w):
+    es = 2 if w.dtype == torch.bfloat16 else 4
+    B, T, Hk, Hv, Dk, Dv = w.B, w.T, w.Hk, w.Hv, w.Dk, w.Dv
+    NC = (T + C - 1) // C
+    Tp = NC * C
+    BH, BHk = B * Hv, B * Hk
+    units = BH * NC  # (b, h, chunk)
+    m = {}
+    m["prep"] = dict(flops=0.0, bytes=2 * B * T * Hv * es + 2 * B * T * Hk * Dk * es
+                     + 2 * BH * Tp * 4 + 2 * BHk * Tp * 4)
+    m["fwd_chunk"] = dict(
+        flops=units * (6 * C * C * Dk + 2 * C * C * Dv + C ** 3 / 3),
+        bytes=units * (2 * C * Dk * es + C * Dv * es + 2 * C * 4 + C * Dk * es + C * Dv * es
+                       + C * C * es + C * C * 4))
+    m["fwd_scan"] = dict(
+        flops=units * (6 * C * Dk * Dv + 2 * C * C * Dv),
+        bytes=units * (3 * C * Dk * es + C * Dv * es + C * C * es + Dk * Dv * 4
+                       + 2 * C * Dv * es) + 2 * BH * Dk * Dv * 4)
+    m["bwd_scan"] = dict(
+        flops=units * (6 * C * Dk * Dv + 2 * C * C * Dv),
+        bytes=units * (C * Dv * es + C * C * es + 3 * C * Dk * es + Dk * Dv * 4 + C * Dv * 4)
+        + BH * Dk * Dv * 4)
+    m["bwd_chunk"] = dict(
+        flops=units * (6 * C * C * Dv + 14 * C * C * Dk + 6 * C * Dk * Dv + 4 * C ** 3),
+        bytes=units * (2 * Dk * Dv * 4 + 3 * C * Dv * es + C * Dv * 4 + 2 * C * Dk * es
+                       + C * C * 4 + 2 * C * Dk * 4 + C * Dv * es + 4 * C * 4))
+    m["bwd_reduce"] = dict(
+        flops=0.0,
+        bytes=2 * BH * T * Dk * 4 + 4 * BHk * T * Dk * es + 2 * BH * T * 4 + 4 * B * T * Hv * es)
+    m["decode"] = dict(flops=BH * (4 * Dk * Dv + 2 * Dk),
+                       bytes=BH * 2 * Dk * Dv * 4 + BHk * 2 * Dk * es + BH * 2 * Dv * es
+                       + BH * 2 * es)
+    # whole step: the bytes any chunked fwd + VJP with fp32 chunk checkpoints
+    # must move (inputs and outputs once, checkpoints written and read once)
+    io_fwd = (2 * B * T * Hk * Dk + B * T * Hv * Dv + 2 * B * T * Hv) * es \
+        + B * T * Hv * Dv * es + 2 * BH * Dk * Dv * 4
+    io_bwd = (2 * B * T * Hk * Dk + 2 * B * T * Hv * Dv + 2 * B * T * Hv) * es \
+        + (2 * B * T * Hk * Dk + B * T * Hv * Dv + 2 * B * T * Hv) * es + 2 * BH * Dk * Dv * 4
+    ckpt = 2 * units * Dk * Dv * 4
+    m["_step"] = dict(bytes=io_fwd + io_bwd + ckpt,
+                      flops=sum(m[k]["flops"] for k in ("fwd_chunk", "fwd_scan", "bwd_scan",
+                                                        "bwd_chunk")))
+    return m
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.lines = []
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            if uuid and not uuid.startswith("GPU-"):
+                uuid = "GPU-" + uuid
+            cmd += ["-i", uuid]
+        except Exception:
+            pass
+        self.cmd = cmd
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU)
+# ---------------------------------------------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle sample (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, key_heads):
+    """Inputs of `w` restricted to the first `key_heads` key-head groups.
+    Returns (inputs, fraction of the workload's (b, h) units)."""
+    x = wl.make_inputs(w)
+    G = w.G
+    nh = key_heads * G
+    sub = {}
+    for n, t in x.items():
+        if t is None:
+            sub[n] = None
+        elif n in ("q", "k"):
+            sub[n] = t[:, :, :key_heads]
+        elif n in ("v", "d_o", "a", "b"):
+            sub[n] = t[:, :, :nh]
+        elif n in ("A_log", "dt_bias"):
+            sub[n] = t[:nh]
+        elif n in ("state0", "d_state_T"):
+            sub[n] = t[:, :nh]
+        else:
+            sub[n] = t
+    return sub, nh / w.Hv
+
+
+def run_oracle_step(sub, backward):
+    import oracle
+
+    args = [sub[n] for n in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "state0", "mask")]
+    t0 = time.perf_counter()
+    oracle.forward(*args)
+    if backward:
+        oracle.backward(*args, sub["d_o"], sub["d_state_T"])
+    return time.perf_counter() - t0
+
+
+def sample_key_heads(w):
+    # a quarter of the key-head groups: a few seconds of fp64 work per step
+    return max(1, w.Hk // 4)
+
+
+def cpu_baseline(w, backward, reps=1):
+    import oracle
+
+    kh = sample_key_heads(w)
+    sub, frac = oracle_sample(w, kh)
+    times = [run_oracle_step(sub, backward) for _ in range(reps)]
+    t = statistics.median(times)
+    tokens = w.B * w.T
+    return {"value": tokens * frac / t, "unit": "tokens/s", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": f"{kh} of {w.Hk} key-head groups ({int(frac * w.Hv)} of {w.Hv} value heads), "
+                      f"all {w.B}x{w.T} tokens, fp64 {'fwd+bwd' if backward else 'fwd'}, "
+                      f"median of {reps}; scaled by the head fraction"}
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    backward = w.backward
+    kh = sample_key_heads(w)
+    sub, frac = oracle_sample(w, kh)
+    for _ in range(args.warmup):
+        run_oracle_step(sub, backward)
+    times = [run_oracle_step(sub, backward) for _ in range(args.steps)]
+    t = sum(times) / len(times)
+    tokens = w.B * w.T
+    value = tokens * frac / t
+    line = {
+        "impl": "reference", "metric": METRIC if backward else DECODE_METRIC,
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t * 1e3 / frac, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(),
+                         "kind": "oracle",
+                         "sample": f"{kh} of {w.Hk} key-head groups per step, all "
+                                   f"{w.B}x{w.T} tokens, scaled by the head fraction"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w):
+    return {"workload": w.name, "B": w.B, "T": w.T, "Hk": w.Hk, "Hv": w.Hv, "Dk": w.Dk,
+            "Dv": w.Dv, "chunk": C, "state": "fp32",
+            "pass": "fwd+bwd" if w.backward else "fwd (decode step)",
+            "l2": "flushed between timed steps (256 MiB write outside the events)"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, w, world, rank, local):
+    from gated_delta_rule_06_gb300 import build as gbuild
+    from gated_delta_rule_06_gb300 import ops
+
+    gbuild.build()
+    lib = ops.load_library()
+    lib.gdn_launch_count.restype = ctypes.c_uint64
+
+    class PhaseTime(ctypes.Structure):
+        _fields_ = [("name", ctypes.c_char_p), ("launches", ctypes.c_int64),
+                    ("total_ms", ctypes.c_double)]
+
+    dev = torch.device("cuda", local)
+    x = wl.make_inputs(w)
+    xd = {k: (None if v is None else v.to(dev)) for k, v in x.items()}
+    backward = w.backward
+    B, T, Hk, Hv, Dk, Dv = w.B, w.T, w.Hk, w.Hv, w.Dk, w.Dv
+    # preallocated outputs / workspaces
+    shape = ops.make_shape(xd["q"], xd["v"], xd["mask"] is not None)
+    fo = {"o": torch.empty((B, T, Hv, Dv), dtype=w.dtype, device=dev),
+          "state_T": torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=dev)}
+    if backward:
+        fo["saved"] = torch.empty(ops.saved_bytes(shape), dtype=torch.uint8, device=dev)
+        fo["ws"] = torch.empty(ops.workspace_bytes(shape, 0), dtype=torch.uint8, device=dev)
+        bo = {"ws": torch.empty(ops.workspace_bytes(shape, 1), dtype=torch.uint8, device=dev)}
+        for n, ref in (("dq", xd["q"]), ("dk", xd["k"]), ("dv", xd["v"]), ("da", xd["a"]),
+                       ("db", xd["b"])):
+            bo[n] = torch.empty_like(ref)
+        bo["dA_log"] = torch.empty((Hv,), dtype=torch.float32, device=dev)
+        bo["ddt_bias"] = torch.empty((Hv,), dtype=torch.float32, device=dev)
+        bo["dstate0"] = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=dev)
+
+    def step(inp):
+        if backward:
+            ops.forward(inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], inp["A_log"],
+                        inp["dt_bias"], inp["state0"], inp["mask"], out=fo)
+            ops.backward(inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], inp["A_log"],
+                         inp["dt_bias"], inp["mask"], fo["saved"], inp["d_o"], inp["d_state_T"],
+                         out=bo)
+        else:
+            ops.forward(inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], inp["A_log"],
+                        inp["dt_bias"], inp["state0"], inp["mask"], keep_saved=False, out=fo)
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step(xd)
+    torch.cuda.synchronize()
+
+    # ---- timed region (device time, CUDA events on the launching stream)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    n0 = lib.gdn_launch_count()
+    lib.gdn_timing_begin()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step(xd)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    launches = int(lib.gdn_launch_count() - n0)
+    phases = (PhaseTime * 16)()
+    cnt = ctypes.c_int(0)
+    lib.gdn_timing_end(phases, 16, ctypes.byref(cnt))
+    barrier(world)
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(step_ms) / len(step_ms)
+    ms_max = max_over_ranks(ms, world)
+    tokens = w.B * w.T
+    value = tokens * world / (ms_max / 1e3)
+
+    # ---- per-phase roofline of the dominant kernel
+    peaks = _peaks()
+    model = work_model(w)
+    ph = {phases[i].name.decode(): (phases[i].launches, phases[i].total_ms)
+          for i in range(cnt.value)}
+    dom = max(ph, key=lambda k: ph[k][1])
+    dl, dms = ph[dom]
+    avg_s = dms / dl / 1e3
+    fl, by = model[dom]["flops"], model[dom]["bytes"]
+    t_hbm = by / (peaks["hbm_gbs"] * 1e9)
+    t_alu = fl / (FP32_ALU_PEAK_TFLOPS * 1e12)
+    traffic = measured_traffic(w.name, dom)
+    if t_alu > t_hbm:
+        roof = {"bound": "alu", "achieved": fl / avg_s / 1e12, "peak": FP32_ALU_PEAK_TFLOPS,
+                "unit": "TFLOP/s", "kernel": dom,
+                "peak_source": "fp32 FFMA: 152 SMs x 128 lanes x 2 flop x 2070 MHz"}
+    else:
+        roof = {"bound": "hbm", "achieved": by / avg_s / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "kernel": dom, "peak_source": f"{peaks['source']} hbm_gbs"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = traffic
+    roof["algorithmic_bytes"] = by
+    roof["algorithmic_flops"] = fl
+    roof["avg_launch_ms"] = avg_s * 1e3
+    roof["share"] = dms / sum(v[1] for v in ph.values())
+
+    step_bytes = model["_step"]["bytes"] if backward else model["decode"]["bytes"]
+    step_roof = {"algorithmic_bytes": step_bytes,
+                 "achieved_gbs": step_bytes / (ms / 1e3) / 1e9,
+                 "frac_of_hbm": step_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                 "peak_source": f"{peaks['source']} hbm_gbs"}
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies timed
+    e2e = run_e2e(args, w, x, xd, fo, bo if backward else None, step, world) \
+        if not args.no_e2e else None
+
+    line = {
+        "metric": METRIC if backward else DECODE_METRIC,
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": (value / PAGE_TOKENS_PER_S[w.name]) if w.name in PAGE_TOKENS_PER_S else None,
+        "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded, shapes and distributions of the workload)",
+        "config": config_of(w),
+        "clocks": clocks,
+        "gpu_launches": launches,
+        "roofline": roof,
+        "step_roofline": step_roof,
+        "phases_ms_per_step": {k: v[1] / args.steps for k, v in ph.items()},
+        "wall_s_timed_region": wall,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        line["cpu_baseline"] = cpu_baseline(w, backward)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measured_traffic(workload, kernel):
+    """DRAM bytes per launch from a committed ncu capture, if one matches."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        return t.get(workload, {}).get(kernel)
+    except Exception:
+        return None
+
+
+def run_e2e(args, w, x, xd, fo, bo, step, world):
+    dev = xd["q"].device
+    names_in = [n for n in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "state0", "mask",
+                            "d_o", "d_state_T") if x[n] is not None]
+    if not w.backward:
+        names_in = [n for n in names_in if n not in ("d_o", "d_state_T")]
+    host = {n: x[n].contiguous().pin_memory() for n in names_in}
+    dev_in = {n: torch.empty_like(xd[n]) for n in names_in}
+    for n in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "state0", "mask", "d_o", "d_state_T"):
+        dev_in.setdefault(n, None)
+    outs = [fo["o"], fo["state_T"]]
+    if bo is not None:
+        outs += [bo[n] for n in ("dq", "dk", "dv", "da", "db", "dA_log", "ddt_bias", "dstate0")]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    stream = torch.cuda.current_stream()
+
+    def e2e_step():
+        for n, t in host.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        step(dev_in)
+        for h, d in zip(host_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / args.steps
+    ms = max_over_ranks(ms, world)
+    return {"value": w.B * w.T * world / (ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen35_9b_layer_T2048_bf16",
+                    choices=[n for n in wl.WORKLOAD_ORDER])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = wl.WORKLOADS[args.workload]
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, w, world, rank)
+    else:
+        run_ours(args, w, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

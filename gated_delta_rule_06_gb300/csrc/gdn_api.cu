@@ -1,0 +1,297 @@
+// gdn_api.cu -- the C ABI of include/gdn.h: argument validation, the layout
+// of the `saved` and workspace buffers, and the launch sequence.
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "../../include/gdn.h"
+#include "gdn_internal.cuh"
+
+namespace {
+
+thread_local char g_cuda_err[256] = "no error";
+
+std::atomic<uint64_t> g_launches{0};
+
+// opt-in per-phase timing (gdn_timing_begin / gdn_timing_end)
+struct PhaseEvent {
+    const char* name;
+    cudaEvent_t start, stop;
+};
+bool g_timing = false;
+std::vector<PhaseEvent> g_events;
+
+template <typename F>
+cudaError_t run_phase(const char* name, cudaStream_t s, F&& launch) {
+    if (!g_timing) return launch();
+    PhaseEvent ev{name, nullptr, nullptr};
+    cudaError_t e = cudaEventCreate(&ev.start);
+    if (e == cudaSuccess) e = cudaEventCreate(&ev.stop);
+    if (e == cudaSuccess) e = cudaEventRecord(ev.start, s);
+    if (e != cudaSuccess) return e;
+    e = launch();
+    if (e != cudaSuccess) return e;
+    e = cudaEventRecord(ev.stop, s);
+    g_events.push_back(ev);
+    return e;
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+    // byte offsets into `saved`
+    size_t ckpt, gam, beta, rq, rk, Tinv, W, P, Delta, saved_total;
+    // byte offsets into the forward workspace
+    size_t U, fwd_total;
+    // byte offsets into the backward workspace
+    size_t dSck, Dbar, dqh, dkh, dl, dbeta, part, bwd_total;
+};
+
+bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+gdn_status validate_shape(const gdn_shape* s, gdn::Dims* d) {
+    if (s == nullptr) return GDN_ERR_INVALID_ARG;
+    if (s->dtype != GDN_DTYPE_F32 && s->dtype != GDN_DTYPE_BF16) return GDN_ERR_INVALID_ARG;
+    if (s->B < 1 || s->T < 1 || s->Hk < 1 || s->Hv < 1) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (s->Hv % s->Hk != 0) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (s->Dk < 8 || s->Dk > 256 || s->Dk % 8 != 0) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (s->Dv < 8 || s->Dv > 256 || s->Dv % 8 != 0) return GDN_ERR_UNSUPPORTED_SHAPE;
+    // grid dimensions: y <= 65535, z <= 65535
+    if (s->Hv > 65535 || s->B > 65535) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (s->T > (int64_t(1) << 40) / 64) return GDN_ERR_UNSUPPORTED_SHAPE;
+    d->B = s->B;
+    d->T = s->T;
+    d->Hk = s->Hk;
+    d->Hv = s->Hv;
+    d->Dk = s->Dk;
+    d->Dv = s->Dv;
+    d->G = s->Hv / s->Hk;
+    d->NC = (s->T + gdn::kChunk - 1) / gdn::kChunk;
+    d->Tp = d->NC * gdn::kChunk;
+    d->dtype = s->dtype;
+    if (d->NC > 2147483647LL) return GDN_ERR_UNSUPPORTED_SHAPE;
+    return GDN_OK;
+}
+
+Layout make_layout(const gdn::Dims& d) {
+    const size_t es = d.dtype == GDN_DTYPE_BF16 ? 2 : 4;
+    const size_t BH = (size_t)d.B * d.Hv;
+    const size_t state_ck = BH * d.NC * d.Dk * d.Dv * sizeof(float);
+    const size_t perstep = BH * d.Tp;
+    Layout L{};
+    size_t o = 0;
+    L.ckpt = o; o = align_up(o + state_ck);
+    L.gam = o; o = align_up(o + perstep * 8);
+    L.beta = o; o = align_up(o + perstep * 4);
+    L.rq = o; o = align_up(o + (size_t)d.B * d.Hk * d.Tp * 4);
+    L.rk = o; o = align_up(o + (size_t)d.B * d.Hk * d.Tp * 4);
+    L.Tinv = o; o = align_up(o + BH * d.NC * gdn::kChunk * gdn::kChunk * 4);
+    L.W = o; o = align_up(o + perstep * d.Dk * es);
+    L.P = o; o = align_up(o + BH * d.NC * gdn::kChunk * gdn::kChunk * es);
+    L.Delta = o; o = align_up(o + perstep * d.Dv * es);
+    L.saved_total = o;
+    o = 0;
+    L.U = o; o = align_up(o + perstep * d.Dv * es);
+    L.fwd_total = o;
+    o = 0;
+    L.dSck = o; o = align_up(o + state_ck);
+    L.Dbar = o; o = align_up(o + perstep * d.Dv * 4);
+    L.dqh = o; o = align_up(o + perstep * d.Dk * 4);
+    L.dkh = o; o = align_up(o + perstep * d.Dk * 4);
+    L.dl = o; o = align_up(o + perstep * 4);
+    L.dbeta = o; o = align_up(o + perstep * 4);
+    L.part = o; o = align_up(o + 2 * (size_t)d.B * d.NC * d.Hv * 4);
+    L.bwd_total = o;
+    return L;
+}
+
+void carve_saved(const Layout& L, void* saved, gdn::Ptrs* p) {
+    char* s = static_cast<char*>(saved);
+    p->ckpt = reinterpret_cast<float*>(s + L.ckpt);
+    p->gam = reinterpret_cast<double*>(s + L.gam);
+    p->beta = reinterpret_cast<float*>(s + L.beta);
+    p->rq = reinterpret_cast<float*>(s + L.rq);
+    p->rk = reinterpret_cast<float*>(s + L.rk);
+    p->Tinv = reinterpret_cast<float*>(s + L.Tinv);
+    p->W = s + L.W;
+    p->P = s + L.P;
+    p->Delta = s + L.Delta;
+}
+
+gdn_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return GDN_OK;
+    std::snprintf(g_cuda_err, sizeof(g_cuda_err), "%s: %s", cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+    return GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+namespace gdn {
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n); }
+}  // namespace gdn
+
+extern "C" {
+
+const char* gdn_status_string(gdn_status status) {
+    switch (status) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: null pointer or bad enum value";
+        case GDN_ERR_UNSUPPORTED_SHAPE: return "GDN_ERR_UNSUPPORTED_SHAPE: shape outside the supported set";
+        case GDN_ERR_WORKSPACE_TOO_SMALL: return "GDN_ERR_WORKSPACE_TOO_SMALL: workspace or saved buffer too small";
+        case GDN_ERR_MISALIGNED: return "GDN_ERR_MISALIGNED: a pointer is not 16-byte aligned";
+        case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a kernel launch failed";
+    }
+    return "unknown gdn_status";
+}
+
+const char* gdn_last_cuda_error(void) { return g_cuda_err; }
+
+gdn_status gdn_workspace_bytes(const gdn_shape* shape, int pass, size_t* bytes) {
+    gdn::Dims d;
+    gdn_status st = validate_shape(shape, &d);
+    if (st != GDN_OK) return st;
+    if (bytes == nullptr || pass < 0 || pass > 2) return GDN_ERR_INVALID_ARG;
+    const Layout L = make_layout(d);
+    if (pass == 0) *bytes = L.fwd_total;
+    else if (pass == 1) *bytes = L.bwd_total;
+    else *bytes = L.fwd_total + L.saved_total;  // inference forward without a saved buffer
+    return GDN_OK;
+}
+
+gdn_status gdn_saved_bytes(const gdn_shape* shape, size_t* bytes) {
+    gdn::Dims d;
+    gdn_status st = validate_shape(shape, &d);
+    if (st != GDN_OK) return st;
+    if (bytes == nullptr) return GDN_ERR_INVALID_ARG;
+    *bytes = make_layout(d).saved_total;
+    return GDN_OK;
+}
+
+gdn_status gdn_forward(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                       const void* a, const void* b, const float* A_log, const float* dt_bias,
+                       const float* state0, const uint8_t* mask, void* o, float* state_T,
+                       void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
+                       void* stream) {
+    gdn::Dims d;
+    gdn_status st = validate_shape(shape, &d);
+    if (st != GDN_OK) return st;
+    if (!q || !k || !v || !a || !b || !A_log || !dt_bias || !o || !state_T) return GDN_ERR_INVALID_ARG;
+    if (shape->has_mask && !mask) return GDN_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, a, b, A_log, dt_bias, state0, mask, o, state_T, saved, ws};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return GDN_ERR_MISALIGNED;
+    gdn::Ptrs p{};
+    p.q = q; p.k = k; p.v = v; p.a = a; p.b = b;
+    p.A_log = A_log; p.dt_bias = dt_bias; p.state0 = state0;
+    p.mask = shape->has_mask ? mask : nullptr;
+    p.o = o; p.state_T = state_T;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Layout L = make_layout(d);
+    if (saved == nullptr && d.T == 1 && gdn::decode_supported(d.Dk, d.Dv))
+        return cuda_status(run_phase("decode", s, [&] { return gdn::launch_decode(d, p, s); }));
+    char* wsb = static_cast<char*>(ws);
+    if (saved != nullptr) {
+        if (saved_bytes < L.saved_total) return GDN_ERR_WORKSPACE_TOO_SMALL;
+        if (ws == nullptr) return GDN_ERR_INVALID_ARG;
+        if (ws_bytes < L.fwd_total) return GDN_ERR_WORKSPACE_TOO_SMALL;
+        carve_saved(L, saved, &p);
+    } else {
+        if (ws == nullptr) return GDN_ERR_INVALID_ARG;
+        if (ws_bytes < L.fwd_total + L.saved_total) return GDN_ERR_WORKSPACE_TOO_SMALL;
+        carve_saved(L, wsb + L.fwd_total, &p);
+    }
+    p.U = wsb + L.U;
+    cudaError_t e = run_phase("prep", s, [&] { return gdn::launch_prep(d, p, s); });
+    if (e == cudaSuccess) e = run_phase("fwd_chunk", s, [&] { return gdn::launch_fwd_chunk(d, p, s); });
+    if (e == cudaSuccess) e = run_phase("fwd_scan", s, [&] { return gdn::launch_fwd_scan(d, p, s); });
+    return cuda_status(e);
+}
+
+gdn_status gdn_backward(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                        const void* a, const void* b, const float* A_log, const float* dt_bias,
+                        const uint8_t* mask, const void* saved, size_t saved_bytes,
+                        const void* d_o, const float* d_state_T, void* dq, void* dk, void* dv,
+                        void* da, void* db, float* dA_log, float* ddt_bias, float* dstate0,
+                        void* ws, size_t ws_bytes, void* stream) {
+    gdn::Dims d;
+    gdn_status st = validate_shape(shape, &d);
+    if (st != GDN_OK) return st;
+    if (!q || !k || !v || !a || !b || !A_log || !dt_bias || !saved || !d_o || !dq || !dk ||
+        !dv || !da || !db || !dA_log || !ddt_bias || !dstate0 || !ws)
+        return GDN_ERR_INVALID_ARG;
+    if (shape->has_mask && !mask) return GDN_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, a, b, A_log, dt_bias, mask, saved, d_o, d_state_T, dq, dk,
+                          dv, da, db, dA_log, ddt_bias, dstate0, ws};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return GDN_ERR_MISALIGNED;
+    const Layout L = make_layout(d);
+    if (saved_bytes < L.saved_total || ws_bytes < L.bwd_total) return GDN_ERR_WORKSPACE_TOO_SMALL;
+    gdn::Ptrs p{};
+    p.q = q; p.k = k; p.v = v; p.a = a; p.b = b;
+    p.A_log = A_log; p.dt_bias = dt_bias;
+    p.mask = shape->has_mask ? mask : nullptr;
+    carve_saved(L, const_cast<void*>(saved), &p);
+    p.d_o = d_o; p.d_state_T = d_state_T;
+    p.dq = dq; p.dk = dk; p.dv = dv; p.da = da; p.db = db;
+    p.dA_log = dA_log; p.ddt_bias = ddt_bias; p.dstate0 = dstate0;
+    char* w = static_cast<char*>(ws);
+    p.dSck = reinterpret_cast<float*>(w + L.dSck);
+    p.Dbar = reinterpret_cast<float*>(w + L.Dbar);
+    p.dqh = reinterpret_cast<float*>(w + L.dqh);
+    p.dkh = reinterpret_cast<float*>(w + L.dkh);
+    p.dl = reinterpret_cast<float*>(w + L.dl);
+    p.dbeta = reinterpret_cast<float*>(w + L.dbeta);
+    p.part = reinterpret_cast<float*>(w + L.part);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = run_phase("bwd_scan", s, [&] { return gdn::launch_bwd_scan(d, p, s); });
+    if (e == cudaSuccess) e = run_phase("bwd_chunk", s, [&] { return gdn::launch_bwd_chunk(d, p, s); });
+    if (e == cudaSuccess) e = run_phase("bwd_reduce", s, [&] { return gdn::launch_bwd_reduce(d, p, s); });
+    return cuda_status(e);
+}
+
+uint64_t gdn_launch_count(void) { return g_launches.load(); }
+
+gdn_status gdn_timing_begin(void) {
+    for (auto& ev : g_events) {
+        cudaEventDestroy(ev.start);
+        cudaEventDestroy(ev.stop);
+    }
+    g_events.clear();
+    g_timing = true;
+    return GDN_OK;
+}
+
+gdn_status gdn_timing_end(gdn_phase_time* out, int max, int* count) {
+    g_timing = false;
+    if (count == nullptr || (out == nullptr && max > 0)) return GDN_ERR_INVALID_ARG;
+    int n = 0;
+    cudaError_t err = cudaSuccess;
+    for (auto& ev : g_events) {
+        float ms = 0.f;
+        cudaError_t e = cudaEventSynchronize(ev.stop);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, ev.start, ev.stop);
+        if (e != cudaSuccess) err = e;
+        int i = 0;
+        while (i < n && std::strcmp(out[i].name, ev.name) != 0) ++i;
+        if (i == n && n < max) {
+            out[n].name = ev.name;
+            out[n].launches = 0;
+            out[n].total_ms = 0.0;
+            ++n;
+        }
+        if (i < n) {
+            out[i].launches += 1;
+            out[i].total_ms += ms;
+        }
+        cudaEventDestroy(ev.start);
+        cudaEventDestroy(ev.stop);
+    }
+    g_events.clear();
+    *count = n;
+    return cuda_status(err);
+}
+
+}  // extern "C"

@@ -1,0 +1,578 @@
+// gdn_bwd.cu -- chunked VJP of the gated delta rule, CUDA-core (FFMA) path.
+//
+// Reverse-mode derivative of the chunk equations (see gdn_fwd.cu), with
+// Obar = dL/dO and Sbar' = dL/dS at the END of the chunk:
+//   bwd_scan   (sequential over chunks, per (b, h, Dv tile); the reverse sweep
+//               of the mlx-lm page's "What this PR adds", recomputing from the
+//               per-chunk checkpoints instead of a saved state history):
+//       Dbar  = P^T Obar + diag(e) K Sbar'
+//       Sbar  = gam_63 Sbar' + Q^T diag(gam) Obar - W^T Dbar
+//   bwd_chunk  (parallel over (b, h, chunk)), with S the chunk-start state:
+//       Xq = Obar S^T, Wbar = -Dbar S^T, Xk = Delta Sbar'^T
+//       Pbar = (Obar Delta^T) o [j <= i]
+//       Y = T^T Dbar -> dV = diag(beta) Y;   Z = T^T Wbar
+//       Tbar = Dbar (diag(beta) V)^T + Wbar (diag(beta gam) K)^T
+//       Abar = -(T^T Tbar T^T) o [j < i]
+//       dQ = diag(gam) Xq + (Pbar o M) K
+//       dK = diag(e) Xk + diag(beta gam) Z + (Pbar o M)^T Q + (Gb + Gb^T) K,
+//            Gb = Abar o beta_i M
+//       betabar_i = <Y_i, V_i> + gam_i <Z_i, K_i> + sum_j Abar_ij M_ij <k_i, k_j>
+//       Gammabar collects M (rows minus columns), gam, e and gam_63 terms and
+//       the log-decay cotangent is its reverse in-chunk cumulative sum.
+//   bwd_reduce: GQA group sums in ascending head order, the L2-norm backward
+//       dx = (s / n) (y - u <u, y>), u = x / n (no n^2 or n^3 terms), the gate
+//       backward and the per-head sums for dA_log / ddt_bias as fixed-order
+//       two-stage sums (mlx-lm page, "Design notes": no atomics, deterministic).
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+// ---------------------------------------------------------------------------
+// bwd_scan: one CTA per (Dv tile, value head, batch), chunks in reverse
+// ---------------------------------------------------------------------------
+template <typename TI, int DVT>
+__global__ void __launch_bounds__(256) bwd_scan_kernel(Dims d, Ptrs p) {
+    extern __shared__ float sm[];
+    const int tile = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
+    const int j = h / (int)d.G;
+    const int Dk = (int)d.Dk, Dv = (int)d.Dv;
+    const int n0 = tile * DVT;
+    float* Sb = sm;                      // [Dk][DVT]
+    float* big = Sb + Dk * DVT;          // [64][Dk]
+    float* Pm = big + kChunk * Dk;       // [64][64]
+    float* Ob = Pm + kChunk * kChunk;    // [64][DVT]
+    float* Db = Ob + kChunk * DVT;       // [64][DVT]
+    float* gm = Db + kChunk * DVT;       // [64]
+    float* ev = gm + kChunk;
+    float* rqv = ev + kChunk;
+    float* rkv = rqv + kChunk;
+
+    const TI* q = (const TI*)p.q;
+    const TI* k = (const TI*)p.k;
+    const TI* W = (const TI*)p.W;
+    const TI* P = (const TI*)p.P;
+    const TI* dO = (const TI*)p.d_o;
+    const float qscale = rsqrtf((float)Dk);
+    const int64_t sbase = ((int64_t)bb * d.Hv + h) * Dk * Dv;
+    for (int idx = threadIdx.x; idx < Dk * DVT; idx += blockDim.x) {
+        const int x = idx / DVT, n = idx % DVT;
+        Sb[idx] = p.d_state_T ? p.d_state_T[sbase + (int64_t)x * Dv + n0 + n] : 0.f;
+    }
+    for (int64_t c = d.NC - 1; c >= 0; --c) {
+        const int64_t t0 = c * kChunk;
+        const int64_t gbase = ((int64_t)bb * d.Hv + h) * d.Tp + t0;
+        const int64_t rbase = ((int64_t)bb * d.Hk + j) * d.Tp + t0;
+        __syncthreads();
+        for (int i = threadIdx.x; i < kChunk; i += blockDim.x) {
+            const double G = p.gam[gbase + i];
+            gm[i] = expf((float)G);
+            ev[i] = expf((float)(p.gam[gbase + kChunk - 1] - G));
+            rqv[i] = p.rq[rbase + i] * qscale;
+            rkv[i] = p.rk[rbase + i];
+        }
+        float* dck = p.dSck + (((int64_t)bb * d.Hv + h) * d.NC + c) * Dk * Dv;
+        for (int idx = threadIdx.x; idx < Dk * DVT; idx += blockDim.x) {
+            const int x = idx / DVT, n = idx % DVT;
+            dck[(int64_t)x * Dv + n0 + n] = Sb[idx];
+        }
+        for (int idx = threadIdx.x; idx < kChunk * DVT; idx += blockDim.x) {
+            const int i = idx / DVT, n = idx % DVT;
+            const int64_t t = t0 + i;
+            Ob[idx] = t < d.T ? ldf(dO + (((int64_t)bb * d.T + t) * d.Hv + h) * Dv + n0 + n) : 0.f;
+        }
+        const TI* Pc = P + (((int64_t)bb * d.Hv + h) * d.NC + c) * kChunk * kChunk;
+        for (int idx = threadIdx.x; idx < kChunk * kChunk; idx += blockDim.x) Pm[idx] = ldf(Pc + idx);
+        for (int idx = threadIdx.x; idx < kChunk * Dk; idx += blockDim.x) {
+            const int i = idx / Dk, x = idx % Dk;
+            const int64_t t = t0 + i;
+            big[idx] = t < d.T ? ldf(k + (((int64_t)bb * d.T + t) * d.Hk + j) * Dk + x) * rkv[i]
+                               : 0.f;
+        }
+        __syncthreads();
+        // Dbar = P^T Obar + diag(e) K Sbar'
+        cta_gemm<2, 4>(kChunk, DVT, kChunk, Pm, 1, kChunk, Ob, DVT, 1, Db, DVT, 1.f, 0.f, nullptr);
+        __syncthreads();
+        cta_gemm<2, 4>(kChunk, DVT, Dk, big, Dk, 1, Sb, DVT, 1, Db, DVT, 1.f, 1.f, ev);
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < kChunk * DVT; idx += blockDim.x) {
+            const int i = idx / DVT, n = idx % DVT;
+            p.Dbar[(gbase + i) * Dv + n0 + n] = Db[idx];
+            Ob[idx] *= gm[i];
+        }
+        for (int idx = threadIdx.x; idx < kChunk * Dk; idx += blockDim.x) {
+            const int i = idx / Dk, x = idx % Dk;
+            const int64_t t = t0 + i;
+            big[idx] = t < d.T ? ldf(q + (((int64_t)bb * d.T + t) * d.Hk + j) * Dk + x) * rqv[i]
+                               : 0.f;
+        }
+        __syncthreads();
+        // Sbar = gam_63 Sbar' + Q^T diag(gam) Obar
+        cta_gemm<2, 4>(Dk, DVT, kChunk, big, 1, Dk, Ob, DVT, 1, Sb, DVT, 1.f, gm[kChunk - 1], nullptr);
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < kChunk * Dk; idx += blockDim.x)
+            big[idx] = ldf(W + gbase * Dk + idx);
+        __syncthreads();
+        // Sbar -= W^T Dbar
+        cta_gemm<2, 4>(Dk, DVT, kChunk, big, 1, Dk, Db, DVT, 1, Sb, DVT, -1.f, 1.f, nullptr);
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < Dk * DVT; idx += blockDim.x) {
+        const int x = idx / DVT, n = idx % DVT;
+        p.dstate0[sbase + (int64_t)x * Dv + n0 + n] = Sb[idx];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// bwd_chunk: one CTA per (chunk, value head, batch)
+// ---------------------------------------------------------------------------
+constexpr int kBlk = 32;  // Dk / Dv streaming block
+
+template <typename TI>
+__global__ void __launch_bounds__(256) bwd_chunk_kernel(Dims d, Ptrs p) {
+    extern __shared__ float sm[];
+    const int c = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
+    const int j = h / (int)d.G;
+    const int Dk = (int)d.Dk, Dv = (int)d.Dv;
+    constexpr int C = kChunk;
+    float* Tm = sm;               // [64][64] T
+    float* Tb = Tm + C * C;       // Tbar, later Abar, later Gb
+    float* Pb = Tb + C * C;       // Pbar, later Pbar o M
+    float* Gkk = Pb + C * C;      // K K^T, later Gb + Gb^T
+    float* Gqk = Gkk + C * C;     // Q K^T
+    float* X = Gqk + C * C;       // scratch 64 x 64
+    float* bO = X + C * C;        // [64][32] blocks
+    float* bD = bO + C * kBlk;
+    float* bDb = bD + C * kBlk;
+    float* bV = bDb + C * kBlk;
+    float* Qb = bV + C * kBlk;
+    float* Kb = Qb + C * kBlk;
+    float* Xq = Kb + C * kBlk;
+    float* Wb = Xq + C * kBlk;
+    float* Xk = Wb + C * kBlk;
+    float* Zb = Xk + C * kBlk;
+    float* Sblk = Zb + C * kBlk;  // [32][32]
+    float* Spblk = Sblk + kBlk * kBlk;
+    float* gm = Spblk + kBlk * kBlk;  // vectors [64]
+    float* ev = gm + C;
+    float* bt = ev + C;
+    float* rqv = bt + C;
+    float* rkv = rqv + C;
+    float* gamb = rkv + C;
+    float* eb = gamb + C;
+    float* betab = eb + C;
+    float* ZK = betab + C;
+    float* red = ZK + C;  // [256] reduction scratch
+    double* Gm = reinterpret_cast<double*>(red + 256);  // [64] Gamma (fp64)
+    double* red2 = Gm + C;                              // [64] fp64 scratch
+
+    const TI* q = (const TI*)p.q;
+    const TI* k = (const TI*)p.k;
+    const TI* v = (const TI*)p.v;
+    const TI* dO = (const TI*)p.d_o;
+    const TI* Delta = (const TI*)p.Delta;
+    TI* dv = (TI*)p.dv;
+    const float qscale = rsqrtf((float)Dk);
+    const int64_t t0 = (int64_t)c * C;
+    const int64_t gbase = ((int64_t)bb * d.Hv + h) * d.Tp + t0;
+    const int64_t rbase = ((int64_t)bb * d.Hk + j) * d.Tp + t0;
+    const int64_t cbase = (((int64_t)bb * d.Hv + h) * d.NC + c) * Dk * Dv;
+    const float* Tg = p.Tinv + (((int64_t)bb * d.Hv + h) * d.NC + c) * C * C;
+    for (int i = threadIdx.x; i < C; i += blockDim.x) {
+        const double G = p.gam[gbase + i];
+        Gm[i] = G;
+        gm[i] = expf((float)G);
+        ev[i] = expf((float)(p.gam[gbase + C - 1] - G));
+        bt[i] = p.beta[gbase + i];
+        rqv[i] = p.rq[rbase + i] * qscale;
+        rkv[i] = p.rk[rbase + i];
+        gamb[i] = 0.f;
+        eb[i] = 0.f;
+        betab[i] = 0.f;
+        ZK[i] = 0.f;
+    }
+    for (int idx = threadIdx.x; idx < C * C; idx += blockDim.x) Tm[idx] = Tg[idx];
+    float gcb = 0.f;  // per-thread partial of <Sbar', S>
+    __syncthreads();
+
+    auto load_rows = [&](float* dst, const TI* src, int64_t row_stride, int64_t col0, int ncol,
+                         bool time_rows, const float* rs) {
+        // dst[i][x] = src[row(i) * row_stride + col0 + x] (* rs[i]) for x < ncol
+        for (int idx = threadIdx.x; idx < C * ncol; idx += blockDim.x) {
+            const int i = idx / ncol, x = idx % ncol;
+            const int64_t t = t0 + i;
+            float val = 0.f;
+            if (!time_rows || t < d.T) val = ldf(src + t * row_stride + col0 + x) * (rs ? rs[i] : 1.f);
+            dst[i * kBlk + x] = val;
+        }
+    };
+
+    // ---- phase 0: Pbar, Y / dV / betabar, Tbar (V part) over Dv blocks
+    for (int dv0 = 0; dv0 < Dv; dv0 += kBlk) {
+        const int nv = min(kBlk, Dv - dv0);
+        const TI* dOb = dO + ((int64_t)bb * d.T * d.Hv + h) * Dv;   // row t at t * Hv * Dv
+        const TI* vb = v + ((int64_t)bb * d.T * d.Hv + h) * Dv;
+        for (int idx = threadIdx.x; idx < C * nv; idx += blockDim.x) {
+            const int i = idx / nv, x = idx % nv;
+            const int64_t t = t0 + i;
+            const bool in = t < d.T;
+            bO[i * kBlk + x] = in ? ldf(dOb + t * d.Hv * Dv + dv0 + x) : 0.f;
+            bV[i * kBlk + x] = in ? ldf(vb + t * d.Hv * Dv + dv0 + x) : 0.f;
+            bD[i * kBlk + x] = ldf(Delta + (gbase + i) * Dv + dv0 + x);
+            bDb[i * kBlk + x] = p.Dbar[(gbase + i) * Dv + dv0 + x];
+        }
+        __syncthreads();
+        const float acc = dv0 ? 1.f : 0.f;
+        cta_gemm<4, 4>(C, C, nv, bO, kBlk, 1, bD, 1, kBlk, Pb, C, 1.f, acc, nullptr);
+        cta_gemm<4, 4>(C, C, nv, bDb, kBlk, 1, bV, 1, kBlk, Tb, C, 1.f, acc, nullptr);
+        cta_gemm<2, 4>(C, nv, C, Tm, 1, C, bDb, kBlk, 1, Xq, kBlk, 1.f, 0.f, nullptr);
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < C * nv; idx += blockDim.x) {
+            const int i = idx / nv, x = idx % nv;
+            const int64_t t = t0 + i;
+            if (t < d.T) stf(dv + (((int64_t)bb * d.T + t) * d.Hv + h) * Dv + dv0 + x, bt[i] * Xq[i * kBlk + x]);
+        }
+        if (threadIdx.x < C) {
+            const int i = threadIdx.x;
+            float s = 0.f;
+            for (int x = 0; x < nv; ++x) s = fmaf(Xq[i * kBlk + x], bV[i * kBlk + x], s);
+            betab[i] += s;
+        }
+        __syncthreads();
+    }
+    for (int idx = threadIdx.x; idx < C * C; idx += blockDim.x) {
+        const int i = idx / C, jj = idx % C;
+        if (jj > i) Pb[idx] = 0.f;
+        Tb[idx] *= bt[jj];
+    }
+    __syncthreads();
+
+    // ---- phase 1: Grams, state products, Wbar / Z, Tbar (K part) over Dk blocks
+    const TI* qrow = q + ((int64_t)bb * d.T * d.Hk + j) * Dk;
+    const TI* krow = k + ((int64_t)bb * d.T * d.Hk + j) * Dk;
+    for (int dk0 = 0; dk0 < Dk; dk0 += kBlk) {
+        const int nk = min(kBlk, Dk - dk0);
+        load_rows(Qb, qrow, d.Hk * Dk, dk0, nk, true, rqv);
+        load_rows(Kb, krow, d.Hk * Dk, dk0, nk, true, rkv);
+        __syncthreads();
+        const float acck = dk0 ? 1.f : 0.f;
+        cta_gemm<4, 4>(C, C, nk, Kb, kBlk, 1, Kb, 1, kBlk, Gkk, C, 1.f, acck, nullptr);
+        cta_gemm<4, 4>(C, C, nk, Qb, kBlk, 1, Kb, 1, kBlk, Gqk, C, 1.f, acck, nullptr);
+        for (int dv0 = 0; dv0 < Dv; dv0 += kBlk) {
+            const int nv = min(kBlk, Dv - dv0);
+            __syncthreads();
+            for (int idx = threadIdx.x; idx < nk * nv; idx += blockDim.x) {
+                const int x = idx / nv, n = idx % nv;
+                const int64_t off = cbase + (int64_t)(dk0 + x) * Dv + dv0 + n;
+                const float s0 = p.ckpt[off], s1 = p.dSck[off];
+                Sblk[x * kBlk + n] = s0;
+                Spblk[x * kBlk + n] = s1;
+                gcb = fmaf(s0, s1, gcb);
+            }
+            const TI* dOb = dO + ((int64_t)bb * d.T * d.Hv + h) * Dv;
+            for (int idx = threadIdx.x; idx < C * nv; idx += blockDim.x) {
+                const int i = idx / nv, x = idx % nv;
+                const int64_t t = t0 + i;
+                bO[i * kBlk + x] = t < d.T ? ldf(dOb + t * d.Hv * Dv + dv0 + x) : 0.f;
+                bD[i * kBlk + x] = ldf(Delta + (gbase + i) * Dv + dv0 + x);
+                bDb[i * kBlk + x] = p.Dbar[(gbase + i) * Dv + dv0 + x];
+            }
+            __syncthreads();
+            const float accv = dv0 ? 1.f : 0.f;
+            cta_gemm<2, 4>(C, nk, nv, bO, kBlk, 1, Sblk, 1, kBlk, Xq, kBlk, 1.f, accv, nullptr);
+            cta_gemm<2, 4>(C, nk, nv, bDb, kBlk, 1, Sblk, 1, kBlk, Wb, kBlk, -1.f, accv, nullptr);
+            cta_gemm<2, 4>(C, nk, nv, bD, kBlk, 1, Spblk, 1, kBlk, Xk, kBlk, 1.f, accv, nullptr);
+        }
+        __syncthreads();
+        if (threadIdx.x < C) {
+            const int i = threadIdx.x;
+            float sq = 0.f, se = 0.f;
+            for (int x = 0; x < nk; ++x) {
+                sq = fmaf(Qb[i * kBlk + x], Xq[i * kBlk + x], sq);
+                se = fmaf(Kb[i * kBlk + x], Xk[i * kBlk + x], se);
+            }
+            gamb[i] += sq;
+            eb[i] += se;
+        }
+        cta_gemm<4, 4>(C, C, nk, Wb, kBlk, 1, Kb, 1, kBlk, X, C, 1.f, acck, nullptr);
+        cta_gemm<2, 4>(C, nk, C, Tm, 1, C, Wb, kBlk, 1, Zb, kBlk, 1.f, 0.f, nullptr);
+        __syncthreads();
+        if (threadIdx.x < C) {
+            const int i = threadIdx.x;
+            float s = 0.f;
+            for (int x = 0; x < nk; ++x) s = fmaf(Zb[i * kBlk + x], Kb[i * kBlk + x], s);
+            ZK[i] += s;
+        }
+        for (int idx = threadIdx.x; idx < C * nk; idx += blockDim.x) {
+            const int i = idx / nk, x = idx % nk;
+            const int64_t off = (gbase + i) * Dk + dk0 + x;
+            p.dqh[off] = gm[i] * Xq[i * kBlk + x];
+            p.dkh[off] = ev[i] * Xk[i * kBlk + x] + bt[i] * gm[i] * Zb[i * kBlk + x];
+        }
+        __syncthreads();
+    }
+    for (int idx = threadIdx.x; idx < C * C; idx += blockDim.x) {
+        const int jj = idx % C;
+        Tb[idx] += bt[jj] * gm[jj] * X[idx];
+    }
+    // <Sbar', S>: fixed-order block reduction of the per-thread partials
+    red[threadIdx.x] = gcb;
+    __syncthreads();
+    for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+        if ((int)threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+        __syncthreads();
+    }
+    const float gCb = red[0];
+
+    // ---- phase 2: Abar = -(T^T Tbar T^T) o [j < i], M / beta / Gamma cotangents
+    cta_gemm<4, 4>(C, C, C, Tb, C, 1, Tm, 1, C, X, C, 1.f, 0.f, nullptr);
+    __syncthreads();
+    cta_gemm<4, 4>(C, C, C, Tm, 1, C, X, C, 1, Tb, C, -1.f, 0.f, nullptr);
+    __syncthreads();
+    if (threadIdx.x < C) {
+        const int i = threadIdx.x;
+        float sb = 0.f;
+        for (int jj = 0; jj < C; ++jj) {
+            const int idx = i * C + jj;
+            const float m = jj <= i ? expf((float)(Gm[i] - Gm[jj])) : 0.f;
+            const float ab = jj < i ? Tb[idx] : 0.f;
+            const float mb = ab * bt[i] * Gkk[idx] + Pb[idx] * Gqk[idx];
+            sb = fmaf(ab * m, Gkk[idx], sb);
+            X[idx] = mb * m;
+            Tb[idx] = ab * bt[i] * m;
+            Pb[idx] *= m;
+        }
+        betab[i] += sb + gm[i] * ZK[i];
+        gamb[i] += bt[i] * ZK[i];
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < C * C; idx += blockDim.x) {
+        const int i = idx / C, jj = idx % C;
+        Gkk[idx] = Tb[idx] + Tb[jj * C + i];
+    }
+    // Gammabar_i = sum_j MM_ij - sum_k MM_ki + gambar_i gam_i - ebar_i e_i (+ chunk-end
+    // terms at i = 63); its reverse cumulative sum is the log-decay cotangent.  The
+    // row-minus-column sums cancel, so they and the scan run in fp64.
+    if (threadIdx.x < C) {
+        const int i = threadIdx.x;
+        double rsum = 0.0, csum = 0.0;
+        for (int jj = 0; jj < C; ++jj) {
+            rsum += (double)X[i * C + jj];
+            csum += (double)X[jj * C + i];
+        }
+        red2[i] = rsum - csum + (double)gamb[i] * gm[i] - (double)eb[i] * ev[i];
+        red[i] = eb[i] * ev[i];
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double se = 0.0;
+        for (int i = 0; i < C; ++i) se += (double)red[i];
+        red2[C - 1] += (double)gCb * gm[C - 1] + se;
+        double run = 0.0;
+        for (int i = C - 1; i >= 0; --i) {
+            run += red2[i];
+            red2[i] = run;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < C) {
+        p.dl[gbase + threadIdx.x] = (float)red2[threadIdx.x];
+        p.dbeta[gbase + threadIdx.x] = betab[threadIdx.x];
+    }
+
+    // ---- phase 3: (Pbar o M) and (Gb + Gb^T) products into dQ / dK
+    for (int dk0 = 0; dk0 < Dk; dk0 += kBlk) {
+        const int nk = min(kBlk, Dk - dk0);
+        __syncthreads();
+        load_rows(Qb, qrow, d.Hk * Dk, dk0, nk, true, rqv);
+        load_rows(Kb, krow, d.Hk * Dk, dk0, nk, true, rkv);
+        __syncthreads();
+        cta_gemm<2, 4>(C, nk, C, Pb, C, 1, Kb, kBlk, 1, Xq, kBlk, 1.f, 0.f, nullptr);
+        cta_gemm<2, 4>(C, nk, C, Pb, 1, C, Qb, kBlk, 1, Xk, kBlk, 1.f, 0.f, nullptr);
+        __syncthreads();
+        cta_gemm<2, 4>(C, nk, C, Gkk, C, 1, Kb, kBlk, 1, Xk, kBlk, 1.f, 1.f, nullptr);
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < C * nk; idx += blockDim.x) {
+            const int i = idx / nk, x = idx % nk;
+            const int64_t off = (gbase + i) * Dk + dk0 + x;
+            p.dqh[off] += Xq[i * kBlk + x];
+            p.dkh[off] += Xk[i * kBlk + x];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// bwd_reduce
+// ---------------------------------------------------------------------------
+// dq / dk: one warp per (b, t, key head); Dk <= 256 -> 8 values per lane
+template <typename TI>
+__global__ void __launch_bounds__(256) bwd_qk_kernel(Dims d, Ptrs p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;  // over (b, t, j)
+    if (row >= d.B * d.T * d.Hk) return;
+    const int64_t j = row % d.Hk;
+    const int64_t t = (row / d.Hk) % d.T;
+    const int64_t bb = row / (d.Hk * d.T);
+    const int Dk = (int)d.Dk;
+    const int64_t xoff = ((bb * d.T + t) * d.Hk + j) * Dk;
+    for (int pass = 0; pass < 2; ++pass) {
+        const TI* x = (const TI*)(pass == 0 ? p.q : p.k) + xoff;
+        const float* src = pass == 0 ? p.dqh : p.dkh;
+        const float r = (pass == 0 ? p.rq : p.rk)[(bb * d.Hk + j) * d.Tp + t];
+        const float s = pass == 0 ? rsqrtf((float)Dk) : 1.f;
+        float y[8], u[8];
+        float dot = 0.f;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int col = lane + 32 * m;
+            y[m] = 0.f;
+            u[m] = 0.f;
+            if (col < Dk) {
+                for (int64_t g = 0; g < d.G; ++g) {
+                    const int64_t h = j * d.G + g;
+                    y[m] += src[((bb * d.Hv + h) * d.Tp + t) * Dk + col];
+                }
+                u[m] = ldf(x + col) * r;
+                dot = fmaf(u[m], y[m], dot);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+        TI* out = (TI*)(pass == 0 ? p.dq : p.dk) + xoff;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int col = lane + 32 * m;
+            if (col < Dk) stf(out + col, s * r * (y[m] - u[m] * dot));
+        }
+    }
+}
+
+// da / db and per-(b, chunk, head) partial sums; grid (NC, B, ceil(Hv / 64))
+template <typename TI>
+__global__ void __launch_bounds__(256) bwd_gate_kernel(Dims d, Ptrs p) {
+    __shared__ float sA[kChunk][65];
+    __shared__ float sD[kChunk][65];
+    const int c = blockIdx.x, bb = blockIdx.y;
+    const int h0 = blockIdx.z * 64;
+    const int nh = (int)(d.Hv - h0 < 64 ? d.Hv - h0 : 64);
+    const int64_t t0 = (int64_t)c * kChunk;
+    const TI* a = (const TI*)p.a;
+    const TI* b = (const TI*)p.b;
+    TI* da = (TI*)p.da;
+    TI* db = (TI*)p.db;
+    for (int idx = threadIdx.x; idx < kChunk * nh; idx += blockDim.x) {
+        const int i = idx / nh, hh = idx % nh, h = h0 + hh;
+        const int64_t t = t0 + i;
+        float vA = 0.f, vD = 0.f;
+        if (t < d.T) {
+            const int64_t ix = ((int64_t)bb * d.T + t) * d.Hv + h;
+            float ga = 0.f, gb = 0.f;
+            if (p.mask == nullptr || p.mask[bb * d.T + t] != 0) {
+                const int64_t gx = ((int64_t)bb * d.Hv + h) * d.Tp + t;
+                const float lb = p.dl[gx];
+                const float x = ldf(a + ix) + p.dt_bias[h];
+                const float xc = fminf(x, kSoftplusClamp);
+                const float eA = expf(p.A_log[h]);
+                const float l = -eA * log1pf(expf(xc));
+                const float sg = x <= kSoftplusClamp ? 1.f / (1.f + expf(-xc)) : 0.f;
+                ga = lb * (-eA) * sg;
+                const float be = p.beta[gx];
+                gb = p.dbeta[gx] * be * (1.f - be);
+                vA = lb * l;
+                vD = ga;
+            }
+            stf(da + ix, ga);
+            stf(db + ix, gb);
+        }
+        sA[i][hh] = vA;
+        sD[i][hh] = vD;
+    }
+    __syncthreads();
+    // fixed-order sum over the 64 steps: one warp per head, pairwise tree
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int hh = warp; hh < nh; hh += blockDim.x >> 5) {
+        float x = sA[2 * lane][hh] + sA[2 * lane + 1][hh];
+        float y = sD[2 * lane][hh] + sD[2 * lane + 1][hh];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            x += __shfl_xor_sync(0xffffffffu, x, off);
+            y += __shfl_xor_sync(0xffffffffu, y, off);
+        }
+        if (lane == 0) {
+            const int64_t pi = ((int64_t)bb * d.NC + c) * d.Hv + h0 + hh;
+            p.part[pi] = x;
+            p.part[d.B * d.NC * d.Hv + pi] = y;
+        }
+    }
+}
+
+// dA_log / ddt_bias: per head, sum of the partials in (b, chunk) order
+__global__ void bwd_head_sum_kernel(Dims d, Ptrs p) {
+    const int64_t h = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (h >= d.Hv) return;
+    float sA = 0.f, sD = 0.f;
+    for (int64_t r = 0; r < d.B * d.NC; ++r) {
+        sA += p.part[r * d.Hv + h];
+        sD += p.part[d.B * d.NC * d.Hv + r * d.Hv + h];
+    }
+    p.dA_log[h] = sA;
+    p.ddt_bias[h] = sD;
+}
+
+template <typename TI, int DVT>
+cudaError_t launch_bscan_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    const size_t smem = sizeof(float) * ((size_t)d.Dk * DVT + (size_t)kChunk * d.Dk +
+                                         kChunk * kChunk + 2 * kChunk * DVT + 4 * kChunk);
+    auto kern = bwd_scan_kernel<TI, DVT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);
+    kern<<<grid, 256, smem, s>>>(d, p);
+    count_launches(1);
+    return cudaPeekAtLastError();
+}
+
+template <typename TI>
+cudaError_t launch_bchunk_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    const size_t smem = sizeof(float) * (6 * kChunk * kChunk + 10 * kChunk * kBlk +
+                                         2 * kBlk * kBlk + 9 * kChunk + 256) +
+                        sizeof(double) * 2 * kChunk;
+    auto kern = bwd_chunk_kernel<TI>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)d.NC, (unsigned)d.Hv, (unsigned)d.B);
+    kern<<<grid, 256, smem, s>>>(d, p);
+    count_launches(1);
+    return cudaPeekAtLastError();
+}
+
+template <typename TI>
+cudaError_t launch_reduce_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    const int64_t rows = d.B * d.T * d.Hk;
+    bwd_qk_kernel<TI><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(d, p);
+    dim3 g((unsigned)d.NC, (unsigned)d.B, (unsigned)((d.Hv + 63) / 64));
+    bwd_gate_kernel<TI><<<g, 256, 0, s>>>(d, p);
+    bwd_head_sum_kernel<<<(unsigned)((d.Hv + 127) / 128), 128, 0, s>>>(d, p);
+    count_launches(3);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_scan(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    if (d.Dv % 32 == 0)
+        return d.dtype == 1 ? launch_bscan_t<__nv_bfloat16, 32>(d, p, s) : launch_bscan_t<float, 32>(d, p, s);
+    if (d.Dv % 16 == 0)
+        return d.dtype == 1 ? launch_bscan_t<__nv_bfloat16, 16>(d, p, s) : launch_bscan_t<float, 16>(d, p, s);
+    return d.dtype == 1 ? launch_bscan_t<__nv_bfloat16, 8>(d, p, s) : launch_bscan_t<float, 8>(d, p, s);
+}
+
+cudaError_t launch_bwd_chunk(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    return d.dtype == 1 ? launch_bchunk_t<__nv_bfloat16>(d, p, s) : launch_bchunk_t<float>(d, p, s);
+}
+
+cudaError_t launch_bwd_reduce(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    return d.dtype == 1 ? launch_reduce_t<__nv_bfloat16>(d, p, s) : launch_reduce_t<float>(d, p, s);
+}
+
+}  // namespace gdn

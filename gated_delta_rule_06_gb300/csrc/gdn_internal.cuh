@@ -1,0 +1,122 @@
+// gdn_internal.cuh -- shapes, buffer layouts and device helpers shared by the
+// CUDA kernels of the gated delta rule library.  Private to libgdn.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+constexpr int kChunk = 64;           // chunk length (mlx-lm page, "Design notes")
+constexpr float kNormEps = 1e-6f;    // L2-norm eps (torch-to-nnef page, op contract)
+constexpr float kSoftplusClamp = 20.f;
+
+struct Dims {
+    int64_t B, T, Hk, Hv, Dk, Dv;
+    int64_t G;   // Hv / Hk
+    int64_t NC;  // number of chunks, ceil(T / 64)
+    int64_t Tp;  // NC * 64 (sequence padded with identity steps)
+    int dtype;   // 0 = fp32, 1 = bf16
+};
+
+// Every device buffer the kernels touch.  Inputs/outputs come from the
+// caller; the rest are carved out of the caller's `saved` and `ws` buffers.
+struct Ptrs {
+    // primal inputs
+    const void *q, *k, *v, *a, *b;
+    const float *A_log, *dt_bias, *state0;
+    const uint8_t* mask;
+    // forward outputs
+    void* o;
+    float* state_T;
+    // saved (forward -> backward)
+    float* ckpt;   // [B, Hv, NC, Dk, Dv] fp32 state at each chunk start
+    double* gam;   // [B, Hv, Tp] in-chunk cumulative log-decay Gamma (fp64: the
+                   // differences Gamma_i - Gamma_j must stay accurate when |Gamma| is large)
+    float* beta;   // [B, Hv, Tp] write strength (0 on masked / padded steps)
+    float* rq;     // [B, Hk, Tp] 1 / sqrt(|q|^2 + eps)   (0 on padded steps)
+    float* rk;     // [B, Hk, Tp] 1 / sqrt(|k|^2 + eps)
+    float* Tinv;   // [B, Hv, NC, 64, 64] fp32 (I + A)^-1 per chunk
+    void* W;       // [B, Hv, Tp, Dk]  T diag(beta gam) K   (input dtype)
+    void* P;       // [B, Hv, NC, 64, 64] (Q K^T) o M, lower incl. diagonal
+    void* Delta;   // [B, Hv, Tp, Dv]  U - W S  per chunk
+    // forward workspace
+    void* U;       // [B, Hv, Tp, Dv]  T diag(beta) V
+    // backward inputs / outputs
+    const void* d_o;
+    const float* d_state_T;
+    void *dq, *dk, *dv, *da, *db;
+    float *dA_log, *ddt_bias, *dstate0;
+    // backward workspace
+    float* dSck;   // [B, Hv, NC, Dk, Dv] state cotangent at each chunk END
+    float* Dbar;   // [B, Hv, Tp, Dv] cotangent of Delta
+    float* dqh;    // [B, Hv, Tp, Dk] cotangent of the normalised q, per value head
+    float* dkh;    // [B, Hv, Tp, Dk]
+    float* dl;     // [B, Hv, Tp] cotangent of the log-decay
+    float* dbeta;  // [B, Hv, Tp]
+    float* part;   // [2, B, NC, Hv] per-chunk partial sums for dA_log, ddt_bias
+};
+
+// ---- scalar load / store in the input dtype ---------------------------------
+__device__ __forceinline__ float ldf(const float* p) { return *p; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void stf(float* p, float x) { *p = x; }
+__device__ __forceinline__ void stf(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + __expf(-x)); }
+
+// ---- CTA-wide fp32 GEMM on shared memory ------------------------------------
+// C[m, n] = beta_c * C[m, n] + alpha * rs[m] * sum_k A(m, k) B(k, n)
+// with A(m, k) = A[m * sam + k * sak] and B(k, n) = B[k * sbk + n * sbn].
+// rs may be nullptr (all ones).  Each thread owns TM x TN output micro tiles;
+// M % TM == 0 and N % TN == 0 are required.  The caller synchronises.
+template <int TM, int TN>
+__device__ __forceinline__ void cta_gemm(int M, int N, int K, const float* A, int sam, int sak,
+                                         const float* Bm, int sbk, int sbn, float* C, int ldc,
+                                         float alpha, float beta_c, const float* rs) {
+    const int tilesN = N / TN;
+    const int ntiles = (M / TM) * tilesN;
+    for (int t = threadIdx.x; t < ntiles; t += blockDim.x) {
+        const int m0 = (t / tilesN) * TM, n0 = (t % tilesN) * TN;
+        float acc[TM][TN];
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+        for (int kk = 0; kk < K; ++kk) {
+            float av[TM], bv[TN];
+#pragma unroll
+            for (int i = 0; i < TM; ++i) av[i] = A[(m0 + i) * sam + kk * sak];
+#pragma unroll
+            for (int j = 0; j < TN; ++j) bv[j] = Bm[kk * sbk + (n0 + j) * sbn];
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const float s = alpha * (rs ? rs[m0 + i] : 1.f);
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                float* c = C + (m0 + i) * ldc + n0 + j;
+                *c = (beta_c != 0.f ? beta_c * *c : 0.f) + s * acc[i][j];
+            }
+        }
+    }
+}
+
+// ---- launchers (defined in the .cu files) -----------------------------------
+cudaError_t launch_prep(const Dims& d, const Ptrs& p, cudaStream_t s);
+cudaError_t launch_fwd_chunk(const Dims& d, const Ptrs& p, cudaStream_t s);
+cudaError_t launch_fwd_scan(const Dims& d, const Ptrs& p, cudaStream_t s);
+cudaError_t launch_bwd_scan(const Dims& d, const Ptrs& p, cudaStream_t s);
+cudaError_t launch_bwd_chunk(const Dims& d, const Ptrs& p, cudaStream_t s);
+cudaError_t launch_bwd_reduce(const Dims& d, const Ptrs& p, cudaStream_t s);
+cudaError_t launch_decode(const Dims& d, const Ptrs& p, cudaStream_t s);
+bool decode_supported(int64_t Dk, int64_t Dv);
+// adds n to the library's launch counter (called by every launcher)
+void count_launches(int n);
+
+}  // namespace gdn

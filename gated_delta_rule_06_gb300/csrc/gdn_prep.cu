@@ -1,0 +1,117 @@
+// gdn_prep.cu -- gate / normalisation prep for the chunked path.
+//
+// Gates (mlx-lm PR "Add gated_delta_update VJP", "What this PR adds" and
+// "Covered corner cases"): per (b, t, h)
+//     l = log g = -exp(A_log[h]) * softplus(min(a + dt_bias[h], 20)),  beta = sigmoid(b)
+// masked and padded steps become identity steps (l = 0, beta = 0), and
+// Gamma = cumulative sum of l inside each 64-step chunk, accumulated and
+// stored in fp64 so that Gamma_i - Gamma_j keeps the accuracy of the steps
+// between i and j however large |Gamma| grows.
+// Norms (torch-to-nnef page, op contract): r = 1 / sqrt(|x|^2 + 1e-6) for
+// every query / key row; padded rows get r = 0.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kGateHeads = 64;  // heads handled per CTA of the gate kernel
+
+template <typename TI>
+__global__ void __launch_bounds__(256) prep_gates_kernel(Dims d, const TI* __restrict__ a,
+                                                         const TI* __restrict__ b,
+                                                         const float* __restrict__ A_log,
+                                                         const float* __restrict__ dt_bias,
+                                                         const uint8_t* __restrict__ mask,
+                                                         double* __restrict__ gam,
+                                                         float* __restrict__ beta) {
+    __shared__ float lg[kChunk][kGateHeads + 1];
+    const int c = blockIdx.x, bb = blockIdx.y;
+    const int h0 = blockIdx.z * kGateHeads;
+    const int nh = (int)(d.Hv - h0 < kGateHeads ? d.Hv - h0 : kGateHeads);
+    const int64_t t0 = (int64_t)c * kChunk;
+    for (int idx = threadIdx.x; idx < kChunk * nh; idx += blockDim.x) {
+        const int i = idx / nh, hh = idx % nh, h = h0 + hh;
+        const int64_t t = t0 + i;
+        float l = 0.f, be = 0.f;
+        if (t < d.T && (mask == nullptr || mask[bb * d.T + t] != 0)) {
+            const int64_t ix = ((int64_t)bb * d.T + t) * d.Hv + h;
+            const float x = ldf(a + ix) + dt_bias[h];
+            const float xc = fminf(x, kSoftplusClamp);
+            l = -expf(A_log[h]) * log1pf(expf(xc));
+            be = 1.f / (1.f + expf(-ldf(b + ix)));
+        }
+        lg[i][hh] = l;
+        beta[((int64_t)bb * d.Hv + h) * d.Tp + t] = be;
+    }
+    __syncthreads();
+    // in-chunk inclusive prefix sum, one warp per head, 2 steps per lane
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int hh = warp; hh < nh; hh += blockDim.x >> 5) {
+        const double x0 = lg[2 * lane][hh], x1 = lg[2 * lane + 1][hh];
+        double s = x0 + x1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const double y = __shfl_up_sync(0xffffffffu, s, off);
+            if (lane >= off) s += y;
+        }
+        const double excl = s - (x0 + x1);
+        double* g = gam + ((int64_t)bb * d.Hv + h0 + hh) * d.Tp + t0;
+        g[2 * lane] = excl + x0;
+        g[2 * lane + 1] = excl + x0 + x1;
+    }
+}
+
+template <typename TI>
+__global__ void __launch_bounds__(256) prep_norms_kernel(Dims d, const TI* __restrict__ q,
+                                                         const TI* __restrict__ k,
+                                                         float* __restrict__ rq,
+                                                         float* __restrict__ rk) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;  // over (b, t, j)
+    const int64_t nrows = d.B * d.Tp * d.Hk;
+    if (row >= nrows) return;
+    const int64_t j = row % d.Hk;
+    const int64_t t = (row / d.Hk) % d.Tp;
+    const int64_t bb = row / (d.Hk * d.Tp);
+    float r_q = 0.f, r_k = 0.f;
+    if (t < d.T) {
+        const int64_t base = ((bb * d.T + t) * d.Hk + j) * d.Dk;
+        float sq = 0.f, sk = 0.f;
+        for (int64_t i = lane; i < d.Dk; i += 32) {
+            const float xq = ldf(q + base + i), xk = ldf(k + base + i);
+            sq = fmaf(xq, xq, sq);
+            sk = fmaf(xk, xk, sk);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            sq += __shfl_xor_sync(0xffffffffu, sq, off);
+            sk += __shfl_xor_sync(0xffffffffu, sk, off);
+        }
+        r_q = 1.f / sqrtf(sq + kNormEps);
+        r_k = 1.f / sqrtf(sk + kNormEps);
+    }
+    if (lane == 0) {
+        rq[(bb * d.Hk + j) * d.Tp + t] = r_q;
+        rk[(bb * d.Hk + j) * d.Tp + t] = r_k;
+    }
+}
+
+template <typename TI>
+cudaError_t launch_prep_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    dim3 g1((unsigned)d.NC, (unsigned)d.B, (unsigned)((d.Hv + kGateHeads - 1) / kGateHeads));
+    prep_gates_kernel<TI><<<g1, 256, 0, s>>>(d, (const TI*)p.a, (const TI*)p.b, p.A_log,
+                                             p.dt_bias, p.mask, p.gam, p.beta);
+    const int64_t rows = d.B * d.Tp * d.Hk;
+    prep_norms_kernel<TI><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(d, (const TI*)p.q,
+                                                                     (const TI*)p.k, p.rq, p.rk);
+    count_launches(2);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    return d.dtype == 1 ? launch_prep_t<__nv_bfloat16>(d, p, s) : launch_prep_t<float>(d, p, s);
+}
+
+}  // namespace gdn

@@ -1,0 +1,266 @@
+"""Thin ctypes binding over libgdn.so (include/gdn.h).
+
+Every step of the computation runs in the library's CUDA kernels; this module
+only checks tensors, allocates outputs/workspaces with PyTorch and passes raw
+device pointers plus the current CUDA stream.  There is no fallback: if the
+library has not been built (``__graft_entry__.build()`` or ``python -m
+gated_delta_rule_06_gb300.build``) every call raises.
+
+Layouts (torch-to-nnef "custom_extractors/gdn", op contract; mlx-lm PR "Add
+gated_delta_update VJP", signature of gated_delta_update_vjp):
+    q, k [B, T, Hk, Dk];  v [B, T, Hv, Dv];  a, b [B, T, Hv];
+    A_log, dt_bias [Hv] fp32;  state [B, Hv, Dk, Dv] fp32;  mask [B, T] bool/uint8.
+q, k, v, a, b share one dtype: float32 or bfloat16.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libgdn.so")
+
+GDN_OK = 0
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+
+
+class GdnError(RuntimeError):
+    pass
+
+
+class GdnShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("T", ctypes.c_int64), ("Hk", ctypes.c_int64),
+                ("Hv", ctypes.c_int64), ("Dk", ctypes.c_int64), ("Dv", ctypes.c_int64),
+                ("dtype", ctypes.c_int32), ("has_mask", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+EXPORTS = ("gdn_status_string", "gdn_last_cuda_error", "gdn_workspace_bytes",
+           "gdn_saved_bytes", "gdn_forward", "gdn_backward")
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libgdn.so (raises if it is missing) and declare its signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise GdnError(f"{path} is missing: build the CUDA library first "
+                           "(python -m gated_delta_rule_06_gb300.build)")
+        lib = ctypes.CDLL(path)
+        vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        shp = ctypes.POINTER(GdnShape)
+        lib.gdn_status_string.argtypes = [i32]
+        lib.gdn_status_string.restype = ctypes.c_char_p
+        lib.gdn_last_cuda_error.argtypes = []
+        lib.gdn_last_cuda_error.restype = ctypes.c_char_p
+        lib.gdn_workspace_bytes.argtypes = [shp, i32, ctypes.POINTER(sz)]
+        lib.gdn_workspace_bytes.restype = i32
+        lib.gdn_saved_bytes.argtypes = [shp, ctypes.POINTER(sz)]
+        lib.gdn_saved_bytes.restype = i32
+        lib.gdn_forward.argtypes = [shp] + [vp] * 11 + [vp, sz, vp, sz, vp]
+        lib.gdn_forward.restype = i32
+        lib.gdn_backward.argtypes = [shp] + [vp] * 9 + [sz] + [vp] * 10 + [vp, sz, vp]
+        lib.gdn_backward.restype = i32
+        _lib = lib
+        return lib
+
+
+def _check(rc: int):
+    if rc != GDN_OK:
+        lib = load_library()
+        msg = lib.gdn_status_string(rc).decode()
+        if "CUDA" in msg:
+            msg += f" ({lib.gdn_last_cuda_error().decode()})"
+        raise GdnError(msg)
+
+
+def make_shape(q: torch.Tensor, v: torch.Tensor, has_mask: bool) -> GdnShape:
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    if q.dtype not in _DTYPES:
+        raise GdnError(f"unsupported dtype {q.dtype}")
+    return GdnShape(B, T, Hk, Hv, Dk, Dv, _DTYPES[q.dtype], int(bool(has_mask)))
+
+
+def saved_bytes(shape: GdnShape) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().gdn_saved_bytes(ctypes.byref(shape), ctypes.byref(n)))
+    return n.value
+
+
+def workspace_bytes(shape: GdnShape, pass_: int) -> int:
+    """pass_ 0: training forward, 1: backward, 2: inference forward (no saved)."""
+    n = ctypes.c_size_t()
+    _check(load_library().gdn_workspace_bytes(ctypes.byref(shape), pass_, ctypes.byref(n)))
+    return n.value
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _cuda(t, name, dtype=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise GdnError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise GdnError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise GdnError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _mask_u8(mask):
+    if mask is None:
+        return None
+    m = mask if mask.dtype == torch.uint8 else mask.to(torch.uint8)
+    return _cuda(m.contiguous(), "mask")
+
+
+def _buf(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
+def forward(q, k, v, a, b, A_log, dt_bias, state0=None, mask=None, *, keep_saved=True,
+            out=None):
+    """Run gdn_forward.  Returns (o, state_T, saved) with saved=None when
+    keep_saved is False (inference).  ``out`` may pass preallocated
+    dict(o=, state_T=, saved=, ws=) buffers."""
+    dt = q.dtype
+    for n, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b)):
+        _cuda(t, n, dt)
+    _cuda(A_log, "A_log", torch.float32)
+    _cuda(dt_bias, "dt_bias", torch.float32)
+    _cuda(state0, "state0", torch.float32)
+    m = _mask_u8(mask)
+    shape = make_shape(q, v, m is not None)
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    out = out or {}
+    o = out.get("o")
+    if o is None:
+        o = torch.empty((B, T, Hv, Dv), dtype=dt, device=q.device)
+    sT = out.get("state_T")
+    if sT is None:
+        sT = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=q.device)
+    saved = None
+    if keep_saved:
+        saved = out.get("saved")
+        if saved is None:
+            saved = _buf(saved_bytes(shape), q.device)
+        ws = out.get("ws")
+        if ws is None:
+            ws = _buf(workspace_bytes(shape, 0), q.device)
+    else:
+        # T == 1 runs the single-step decode kernel, which needs no workspace
+        # (it handles Dk * Dv <= 32768 with Dv % 4 == 0); otherwise the chunked
+        # forward runs with its intermediates in an inference workspace.
+        ws = out.get("ws")
+        if ws is None and not (T == 1 and Dk * Dv <= 32768 and Dv % 4 == 0):
+            ws = _buf(workspace_bytes(shape, 2), q.device)
+    rc = load_library().gdn_forward(
+        ctypes.byref(shape), _p(q), _p(k), _p(v), _p(a), _p(b), _p(A_log), _p(dt_bias),
+        _p(state0), _p(m), _p(o), _p(sT), _p(saved),
+        ctypes.c_size_t(saved.numel() if saved is not None else 0), _p(ws),
+        ctypes.c_size_t(ws.numel() if ws is not None else 0), _stream())
+    _check(rc)
+    return o, sT, saved
+
+
+def decode(q, k, v, a, b, A_log, dt_bias, state, mask=None, *, state_out=None, o=None):
+    """One T = 1 step (inference).  ``state_out`` may be ``state`` (in place)."""
+    if q.shape[1] != 1:
+        raise GdnError("decode takes T == 1")
+    outd = {"state_T": state_out, "o": o, "ws": None}
+    o, sT, _ = forward(q, k, v, a, b, A_log, dt_bias, state, mask, keep_saved=False,
+                       out={k_: v_ for k_, v_ in outd.items() if v_ is not None})
+    return o, sT
+
+
+def backward(q, k, v, a, b, A_log, dt_bias, mask, saved, d_o, d_state_T=None, *, out=None):
+    """Run gdn_backward.  Returns dict(dq, dk, dv, da, db, dA_log, ddt_bias, dstate0)."""
+    dt = q.dtype
+    _cuda(d_o, "d_o", dt)
+    _cuda(d_state_T, "d_state_T", torch.float32)
+    m = _mask_u8(mask)
+    shape = make_shape(q, v, m is not None)
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    out = dict(out or {})
+    dev = q.device
+    g = {
+        "dq": out.get("dq", None), "dk": out.get("dk", None), "dv": out.get("dv", None),
+        "da": out.get("da", None), "db": out.get("db", None),
+        "dA_log": out.get("dA_log", None), "ddt_bias": out.get("ddt_bias", None),
+        "dstate0": out.get("dstate0", None),
+    }
+    if g["dq"] is None:
+        g["dq"] = torch.empty_like(q)
+    if g["dk"] is None:
+        g["dk"] = torch.empty_like(k)
+    if g["dv"] is None:
+        g["dv"] = torch.empty_like(v)
+    if g["da"] is None:
+        g["da"] = torch.empty_like(a)
+    if g["db"] is None:
+        g["db"] = torch.empty_like(b)
+    if g["dA_log"] is None:
+        g["dA_log"] = torch.empty((Hv,), dtype=torch.float32, device=dev)
+    if g["ddt_bias"] is None:
+        g["ddt_bias"] = torch.empty((Hv,), dtype=torch.float32, device=dev)
+    if g["dstate0"] is None:
+        g["dstate0"] = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=dev)
+    ws = out.get("ws")
+    if ws is None:
+        ws = _buf(workspace_bytes(shape, 1), dev)
+    rc = load_library().gdn_backward(
+        ctypes.byref(shape), _p(q), _p(k), _p(v), _p(a), _p(b), _p(A_log), _p(dt_bias),
+        _p(m), _p(saved), ctypes.c_size_t(saved.numel()), _p(d_o), _p(d_state_T),
+        _p(g["dq"]), _p(g["dk"]), _p(g["dv"]), _p(g["da"]), _p(g["db"]), _p(g["dA_log"]),
+        _p(g["ddt_bias"]), _p(g["dstate0"]), _p(ws), ctypes.c_size_t(ws.numel()), _stream())
+    _check(rc)
+    return g
+
+
+class GatedDeltaRule(torch.autograd.Function):
+    """Autograd wrapper: (o, final_state) = gated_delta_rule(q, k, v, a, b,
+    A_log, dt_bias, state0, mask), with gradients for every floating input."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, a, b, A_log, dt_bias, state0, mask):
+        q, k, v, a, b = (t.contiguous() for t in (q, k, v, a, b))
+        o, sT, saved = forward(q, k, v, a, b, A_log.contiguous(), dt_bias.contiguous(),
+                               None if state0 is None else state0.contiguous(), mask)
+        ctx.save_for_backward(q, k, v, a, b, A_log, dt_bias, saved)
+        ctx.mask = mask
+        ctx.has_state0 = state0 is not None
+        return o, sT
+
+    @staticmethod
+    def backward(ctx, d_o, d_sT):
+        q, k, v, a, b, A_log, dt_bias, saved = ctx.saved_tensors
+        if d_o is None:
+            d_o = torch.zeros_like(v)
+        g = backward(q, k, v, a, b, A_log.contiguous(), dt_bias.contiguous(), ctx.mask, saved,
+                     d_o.contiguous(), None if d_sT is None else d_sT.contiguous())
+        return (g["dq"], g["dk"], g["dv"], g["da"], g["db"], g["dA_log"], g["ddt_bias"],
+                g["dstate0"] if ctx.has_state0 else None, None)
+
+
+def gated_delta_rule(q, k, v, a, b, A_log, dt_bias, state0=None, mask=None):
+    """Differentiable gated delta rule (the C-ABI forward + VJP)."""
+    return GatedDeltaRule.apply(q, k, v, a, b, A_log, dt_bias, state0, mask)

@@ -1,0 +1,137 @@
+/*
+ * gdn.h -- C ABI of the GB300 gated delta rule library (libgdn.so).
+ *
+ * The operation (mlx-lm PR "Add gated_delta_update VJP - trainable
+ * GatedDeltaNet on Apple Silicon", "What this PR adds"; torch-to-nnef
+ * "custom_extractors/gdn", op contract):
+ *
+ *   per batch b and value head h (key head j = h / G, G = Hv / Hk):
+ *     qh_t = q_t / sqrt(|q_t|^2 + 1e-6) / sqrt(Dk),  kh_t = k_t / sqrt(|k_t|^2 + 1e-6)
+ *     g_t  = exp(-exp(A_log[h]) * softplus(min(a_t + dt_bias[h], 20)))
+ *     beta_t = sigmoid(b_t)
+ *     if mask[b, t]:  S <- g_t S;  delta = beta_t (v_t - S^T kh_t);  S <- S + kh_t delta^T
+ *     o_t = S^T qh_t                       (a masked step leaves S unchanged)
+ *
+ * gdn_forward returns o and the final state; gdn_backward returns the
+ * gradients of q, k, v, a, b, A_log, dt_bias and the initial state (the VJP
+ * the mlx-lm page adds).  The sequence is processed in chunks of 64 steps
+ * (mlx-lm page, "Design notes": CHUNK_SIZE = 64); the forward keeps the fp32
+ * state at every chunk start in a caller-owned "saved" buffer that the
+ * backward consumes.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library never allocates, frees or synchronises.  All work is enqueued
+ *     on `stream` (a cudaStream_t passed as void*, NULL = legacy stream).
+ *   - Tensors are dense row-major in these layouts:
+ *       q, k, dq, dk        [B, T, Hk, Dk]   dtype
+ *       v, o, d_o, dv       [B, T, Hv, Dv]   dtype
+ *       a, b, da, db        [B, T, Hv]       dtype
+ *       A_log, dt_bias, dA_log, ddt_bias   [Hv]  fp32
+ *       state0, state_T, d_state_T, dstate0 [B, Hv, Dk, Dv] fp32
+ *       mask                [B, T]  uint8, nonzero = step applied
+ *     where dtype is GDN_DTYPE_F32 (float) or GDN_DTYPE_BF16 (bfloat16).
+ *   - Every pointer must be 16-byte aligned (GDN_ERR_MISALIGNED otherwise).
+ *   - Arguments are validated on the host before anything is launched; an
+ *     error returns a status and leaves every output untouched.  A failed
+ *     launch returns GDN_ERR_CUDA (the CUDA error is reported by
+ *     gdn_last_cuda_error()).  Nothing aborts the process or throws.
+ *   - Results are deterministic: no atomics; every reduction has a fixed order.
+ *
+ * Supported shapes: B >= 1, T >= 1, Hk >= 1, Hv % Hk == 0,
+ * 8 <= Dk, Dv <= 256 and both multiples of 8.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,         /* null pointer where one is required, bad enum */
+    GDN_ERR_UNSUPPORTED_SHAPE = 2,   /* shape outside the supported set above */
+    GDN_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes or saved_bytes below the sizing call */
+    GDN_ERR_MISALIGNED = 4,          /* a pointer is not 16-byte aligned */
+    GDN_ERR_CUDA = 5                 /* a kernel launch failed */
+} gdn_status;
+
+typedef enum { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1 } gdn_dtype;
+
+typedef struct {
+    int64_t B, T, Hk, Hv, Dk, Dv;
+    int32_t dtype;    /* gdn_dtype of q, k, v, a, b, o and of their gradients */
+    int32_t has_mask; /* 0: mask pointer ignored (every step applied) */
+} gdn_shape;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* gdn_status_string(gdn_status status);
+
+/* Text of the last CUDA error seen by this thread inside the library. */
+const char* gdn_last_cuda_error(void);
+
+/* Bytes of scratch the caller must pass as `ws` to gdn_forward (pass = 0)
+ * or gdn_backward (pass = 1).  Host-only; launches nothing. */
+gdn_status gdn_workspace_bytes(const gdn_shape* shape, int pass, size_t* bytes);
+
+/* Bytes of the `saved` buffer that gdn_forward fills and gdn_backward reads:
+ * the fp32 state at each of the ceil(T/64) chunk starts plus per-chunk
+ * intermediates of the WY/UT form (mlx-lm page, "Scope and follow-ups":
+ * chunk-parallel form through a lower-triangular solve).  Host-only. */
+gdn_status gdn_saved_bytes(const gdn_shape* shape, size_t* bytes);
+
+/* Forward pass.  state0 may be NULL (zero initial state); mask may be NULL
+ * (every step applied).  state_T may alias state0 (in-place update).
+ * saved may be NULL for inference (nothing kept for the backward); then,
+ * when T == 1, the single-step decode kernel runs and ws may be NULL.
+ * Otherwise ws must hold gdn_workspace_bytes(shape, 0) bytes. */
+gdn_status gdn_forward(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                       const void* a, const void* b, const float* A_log,
+                       const float* dt_bias, const float* state0, const uint8_t* mask,
+                       void* o, float* state_T, void* saved, size_t saved_bytes, void* ws,
+                       size_t ws_bytes, void* stream);
+
+/* Backward pass (VJP).  Takes the same primal inputs and the `saved` buffer
+ * of a gdn_forward call on them, the cotangent d_o of o and d_state_T of the
+ * final state (NULL = zero), and writes dq, dk, dv, da, db (dtype),
+ * dA_log, ddt_bias [Hv] and dstate0 [B, Hv, Dk, Dv] (fp32).  Every output
+ * is written in full (no accumulation into existing contents).  ws must
+ * hold gdn_workspace_bytes(shape, 1) bytes. */
+gdn_status gdn_backward(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                        const void* a, const void* b, const float* A_log,
+                        const float* dt_bias, const uint8_t* mask, const void* saved,
+                        size_t saved_bytes, const void* d_o, const float* d_state_T,
+                        void* dq, void* dk, void* dv, void* da, void* db, float* dA_log,
+                        float* ddt_bias, float* dstate0, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/* ---- instrumentation (host-only bookkeeping, off by default) -------------- */
+
+/* Number of CUDA kernels this library has launched in this process so far. */
+uint64_t gdn_launch_count(void);
+
+/* Per-phase device time.  gdn_timing_begin() makes every later gdn_forward /
+ * gdn_backward record a CUDA event pair around each of its phases, on the
+ * call's stream.  gdn_timing_end() waits for those events, writes up to
+ * `max` entries {phase name, launches, total milliseconds} in first-seen
+ * order, sets *count, and switches recording off.  Returns GDN_ERR_CUDA if an
+ * event failed.  Phases: "prep", "fwd_chunk", "fwd_scan", "bwd_scan",
+ * "bwd_chunk", "bwd_reduce", "decode".  Not thread-safe: one caller at a time. */
+typedef struct {
+    const char* name;
+    int64_t launches;
+    double total_ms;
+} gdn_phase_time;
+
+gdn_status gdn_timing_begin(void);
+gdn_status gdn_timing_end(gdn_phase_time* out, int max, int* count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

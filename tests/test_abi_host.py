@@ -1,0 +1,101 @@
+"""Host-side checks of the C ABI (no GPU needed, nothing is launched).
+
+The library loads, exports every entry point that include/gdn.h declares,
+sizes its buffers, and rejects bad arguments with a status before any launch.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_delta_rule_06_gb300 import build, ops
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return ops.load_library()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(gdn_\w+)\s*\(", src, re.M))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert {"gdn_forward", "gdn_backward", "gdn_workspace_bytes", "gdn_saved_bytes"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _shape(B=1, T=130, Hk=2, Hv=4, Dk=64, Dv=32, dtype=1, has_mask=0):
+    return ops.GdnShape(B, T, Hk, Hv, Dk, Dv, dtype, has_mask)
+
+
+def test_sizes(lib):
+    s = _shape()
+    n = ctypes.c_size_t()
+    assert lib.gdn_saved_bytes(ctypes.byref(s), ctypes.byref(n)) == 0
+    NC = 3
+    assert n.value >= 1 * 4 * NC * 64 * 32 * 4  # fp32 checkpoints
+    for p in (0, 1, 2):
+        assert lib.gdn_workspace_bytes(ctypes.byref(s), p, ctypes.byref(n)) == 0
+        assert n.value > 0 and n.value % 256 == 0
+    assert lib.gdn_workspace_bytes(ctypes.byref(s), 3, ctypes.byref(n)) == 1
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Hv=5), 2), (dict(Dk=12), 2), (dict(Dv=264), 2), (dict(T=0), 2), (dict(B=0), 2),
+    (dict(dtype=7), 1), (dict(Dk=4), 2)])
+def test_bad_shapes(lib, kw, code):
+    s = _shape(**kw)
+    n = ctypes.c_size_t()
+    assert lib.gdn_saved_bytes(ctypes.byref(s), ctypes.byref(n)) == code
+
+
+def _fwd(lib, s, ptr=0x1000, **over):
+    args = dict(q=ptr, k=ptr, v=ptr, a=ptr, b=ptr, A_log=ptr, dt_bias=ptr, state0=None,
+                mask=None, o=ptr, state_T=ptr, saved=ptr, saved_bytes=1 << 40, ws=ptr,
+                ws_bytes=1 << 40)
+    args.update(over)
+    vp = ctypes.c_void_p
+    return lib.gdn_forward(ctypes.byref(s), *[vp(args[n]) if args[n] else None for n in (
+        "q", "k", "v", "a", "b", "A_log", "dt_bias", "state0", "mask", "o", "state_T",
+        "saved")], ctypes.c_size_t(args["saved_bytes"]), vp(args["ws"]),
+        ctypes.c_size_t(args["ws_bytes"]), None)
+
+
+def test_forward_rejects_before_launch(lib):
+    s = _shape()
+    assert _fwd(lib, s, q=None) == 1                       # null input
+    assert _fwd(lib, s, v=0x1008) == 4                     # misaligned
+    assert _fwd(lib, s, saved_bytes=16) == 3               # saved too small
+    assert _fwd(lib, s, ws_bytes=16) == 3                  # workspace too small
+    assert _fwd(lib, _shape(has_mask=1)) == 1              # mask promised, not given
+    assert _fwd(lib, _shape(Hv=3)) == 2                    # Hv % Hk != 0
+
+
+def test_backward_rejects_before_launch(lib):
+    s = _shape()
+    vp = ctypes.c_void_p
+    P = vp(0x1000)
+    args = [P] * 7 + [None, P, ctypes.c_size_t(1 << 40), P, None] + [P] * 8 + [
+        P, ctypes.c_size_t(16), None]
+    assert lib.gdn_backward(ctypes.byref(s), *args) == 3   # workspace too small
+    args2 = list(args)
+    args2[8] = None                                        # no saved buffer
+    assert lib.gdn_backward(ctypes.byref(s), *args2) == 1
+
+
+def test_status_strings(lib):
+    for c in range(6):
+        assert lib.gdn_status_string(c).startswith(b"GDN_")
