@@ -131,6 +131,15 @@ gdn_status cuda_status(cudaError_t e) {
 
 namespace gdn {
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n); }
+unsigned int read_clear_error_all() {
+    const unsigned int words[] = {read_clear_error_selftest()};
+    unsigned int v = 0;
+    for (unsigned int w : words) {
+        if (w == ~0u) return ~0u;
+        v |= w;
+    }
+    return v;
+}
 }  // namespace gdn
 
 extern "C" {

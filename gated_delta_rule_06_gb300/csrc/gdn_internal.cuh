@@ -118,5 +118,9 @@ cudaError_t launch_decode(const Dims& d, const Ptrs& p, cudaStream_t s);
 bool decode_supported(int64_t Dk, int64_t Dv);
 // adds n to the library's launch counter (called by every launcher)
 void count_launches(int n);
+// reads and clears the device error words of every translation unit
+// (~0u if a read failed); defined in gdn_api.cu
+unsigned int read_clear_error_all();
+unsigned int read_clear_error_selftest();
 
 }  // namespace gdn

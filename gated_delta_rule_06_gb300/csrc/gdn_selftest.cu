@@ -1,0 +1,104 @@
+// gdn_selftest.cu -- plain matrix product through the library's tcgen05 path
+// (staging into the canonical shared-memory layout, MMA issue, TMEM read-back).
+#include "../../include/gdn_selftest.h"
+#include "gdn_internal.cuh"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+
+GDN_ERROR_WORD(selftest)
+
+namespace {
+
+__global__ void __launch_bounds__(128) selftest_mma_kernel(int M, int N, int K, int a_mn, int b_mn,
+                                                           const __nv_bfloat16* __restrict__ A,
+                                                           const __nv_bfloat16* __restrict__ B,
+                                                           float* __restrict__ D) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tmem_base;
+    uint8_t* sa = smem;                 // A tile: up to 128 x 256 bf16 = 64 KB
+    uint8_t* sb = smem + 128 * 256 * 2; // B tile: up to 256 x 256 bf16 = 128 KB
+    const int tid = threadIdx.x, warp = tid >> 5;
+    // A: K-major -> x = k, y = m; MN-major -> x = m, y = k.  x groups fastest.
+    tc::Tile ta, tb;
+    ta.base = tc::smem_u32(sa);
+    ta.k_major = !a_mn;
+    const int ax = a_mn ? M : K;
+    ta.xs = 128;
+    ta.ys = (uint32_t)(ax / 8) * 128;
+    tb.base = tc::smem_u32(sb);
+    tb.k_major = !b_mn;
+    const int bx = b_mn ? N : K;
+    tb.xs = 128;
+    tb.ys = (uint32_t)(bx / 8) * 128;
+    for (int e = tid; e < M * K; e += blockDim.x) {
+        const int m = e / K, k = e % K;
+        const uint32_t o = a_mn ? ta.off(m, k) : ta.off(k, m);
+        *reinterpret_cast<__nv_bfloat16*>(sa + o) = A[e];
+    }
+    for (int e = tid; e < K * N; e += blockDim.x) {
+        const int k = e / N, n = e % N;
+        const uint32_t o = b_mn ? tb.off(n, k) : tb.off(k, n);
+        *reinterpret_cast<__nv_bfloat16*>(sb + o) = B[e];
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&tmem_base, 256);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        tc::mbar_init(&bar, 1);
+        tc::fence_mbar_init();
+    }
+    tc::fence_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tbase = tmem_base;
+    if (tid == 0) {
+        tc::mma_tile(tbase, ta, tb, M, N, K, false);
+        tc::mma_commit(&bar);
+    }
+    const bool ok = tc::mbar_wait(&bar, 0, &g_err_selftest);
+    tc::tc_fence_after();
+    if (ok) {
+        for (int c0 = 0; c0 < N; c0 += 16) {
+            float v[16];
+            tc::tmem_ld16(tc::tmem_addr(tbase, 32 * (warp & 3), c0), v);
+            tc::tmem_wait_ld();
+            const int row = 32 * (warp & 3) + (tid & 31);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) D[row * N + c0 + i] = v[i];
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tbase, 256);
+}
+
+}  // namespace
+}  // namespace gdn
+
+extern "C" gdn_status gdn_selftest_mma(int M, int N, int K, int a_mn_major, int b_mn_major,
+                                       const void* A, const void* B, float* D_raw, void* stream) {
+    if (!(M == 64 || M == 128) || N < 16 || N > 256 || N % 16 || K < 16 || K > 256 || K % 16)
+        return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (!A || !B || !D_raw) return GDN_ERR_INVALID_ARG;
+    const size_t smem = (size_t)128 * 256 * 2 + (size_t)256 * 256 * 2;
+    auto kern = gdn::selftest_mma_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    kern<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(
+        M, N, K, a_mn_major, b_mn_major, static_cast<const __nv_bfloat16*>(A),
+        static_cast<const __nv_bfloat16*>(B), D_raw);
+    gdn::count_launches(1);
+    return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+extern "C" gdn_status gdn_device_error(unsigned int* flag) {
+    if (!flag) return GDN_ERR_INVALID_ARG;
+    const unsigned int v = gdn::read_clear_error_all();
+    if (v == ~0u) return GDN_ERR_CUDA;
+    *flag = v;
+    return GDN_OK;
+}

@@ -1,0 +1,190 @@
+// gdn_tc.cuh -- sm_100-family tensor-core primitives (tcgen05, TMEM, mbarrier,
+// bulk/tensor TMA) written as inline PTX, used by the bf16 kernels.
+//
+// Shared-memory operand layout ("canonical, no swizzle"): a tile is stored
+// as 8 x 16-byte core matrices.  For a tile indexed (x, y) where x is the
+// dimension whose 8 consecutive elements share one 16-byte row of a core
+// matrix and y the other dimension:
+//     byte(x, y) = (x / 8) * XS + (y / 8) * YS + (y % 8) * 16 + (x % 8) * 2
+// A K-major operand has x = K (then LBO = XS, SBO = YS); an MN-major operand
+// has x = M or N (then SBO = XS, LBO = YS).  One bf16 MMA consumes K = 16,
+// i.e. two core matrices along K: the next K step starts 2 * LBO further.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+namespace tc {
+
+// Error word bit set when a bounded wait gives up (kernels never trap).  Each
+// translation unit that waits owns one word (GDN_ERROR_WORD) and a host
+// accessor that reads and clears it.
+constexpr unsigned int kErrWaitTimeout = 1u;
+
+#define GDN_ERROR_WORD(tu)                                                       \
+    static __device__ unsigned int g_err_##tu = 0;                                \
+    unsigned int read_clear_error_##tu() {                                       \
+        unsigned int v = 0, z = 0;                                               \
+        if (cudaMemcpyFromSymbol(&v, g_err_##tu, sizeof(v)) != cudaSuccess) return ~0u; \
+        cudaMemcpyToSymbol(g_err_##tu, &z, sizeof(z));                           \
+        return v;                                                                \
+    }
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---- mbarrier ----------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait (about one second of wall time).  On timeout it records
+// kErrWaitTimeout in *err and returns false; callers then skip work.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0 && globaltimer_ns() - t0 > 1000000000ull) {
+            atomicOr(err, kErrWaitTimeout);
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// ---- proxy / ordering fences ----------------------------------------------------
+// generic-proxy shared-memory writes -> visible to the async proxy (tcgen05.mma, TMA)
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ---- TMEM ----------------------------------------------------------------------
+// executed by one full warp; writes the TMEM base address to *dst (shared)
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+// TMEM address of (lane, column)
+__device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
+    return base + (lane << 16) + col;
+}
+
+// 32 lanes x 32 bits, 16 consecutive columns per thread (thread t <-> lane base + t)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---- descriptors -------------------------------------------------------------------
+// shared-memory matrix descriptor, no swizzle, sm_100 version field = 1
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo & 0x3FFFFu) >> 4) << 16;
+    d |= (uint64_t)((sbo & 0x3FFFFu) >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+// instruction descriptor, kind::f16 with bf16 A and B, fp32 accumulator
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+           ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem], one thread issues
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// arrive on *bar once every MMA issued so far by this thread has completed
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+// Operand tile geometry in the canonical layout above.
+struct Tile {
+    uint32_t base;  // shared address of the tile
+    uint32_t xs;    // byte stride between 8-element groups along x
+    uint32_t ys;    // byte stride between 8-row groups along y
+    bool k_major;   // x is the K dimension
+    __device__ __forceinline__ uint32_t off(uint32_t x, uint32_t y) const {
+        return (x >> 3) * xs + (y >> 3) * ys + (y & 7u) * 16u + (x & 7u) * 2u;
+    }
+    // descriptor for the K slice starting at k0 (multiple of 16)
+    __device__ __forceinline__ uint64_t desc(uint32_t k0) const {
+        if (k_major) return sdesc(base + (k0 >> 3) * xs, xs, ys);
+        return sdesc(base + (k0 >> 3) * ys, ys, xs);
+    }
+};
+
+// issue D = A (M x K) * B (K x N) (+ D if accumulate) as K / 16 MMAs
+__device__ __forceinline__ void mma_tile(uint32_t d_tmem, const Tile& A, const Tile& B, int M,
+                                         int N, int K, bool accumulate) {
+    const uint32_t id = idesc_bf16(M, N, !A.k_major, !B.k_major);
+    for (int k = 0; k < K; k += 16)
+        mma_bf16(d_tmem, A.desc(k), B.desc(k), id, (accumulate || k > 0) ? 1u : 0u);
+}
+
+}  // namespace tc
+}  // namespace gdn

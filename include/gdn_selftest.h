@@ -1,0 +1,39 @@
+/*
+ * gdn_selftest.h -- hardware self-check of the tensor-core path of libgdn.so.
+ *
+ * Not an operation of the method (the pages have no counterpart): it runs the
+ * library's own shared-memory staging, tcgen05 MMA issue and TMEM read-back on
+ * a plain matrix product so that tests can check operand layouts and
+ * accumulator lane placement against a reference product.
+ */
+#ifndef GDN_SELFTEST_H
+#define GDN_SELFTEST_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* D_raw = A * B on one CTA with tcgen05.mma (bf16 in, fp32 accumulate).
+ *   A: device bf16 [M][K] row-major, B: device bf16 [K][N] row-major.
+ *   M in {64, 128}; N in 16..256 (multiple of 16); K in 16..256 (multiple of 16).
+ *   a_mn_major / b_mn_major choose the shared-memory operand orientation.
+ *   D_raw: device fp32 [128][N]: every TMEM lane (row) of the accumulator as read
+ *   back by 32x32b loads, so the lane placement of M = 64 results is visible.
+ * Enqueued on `stream`; returns GDN_ERR_UNSUPPORTED_SHAPE for other sizes. */
+gdn_status gdn_selftest_mma(int M, int N, int K, int a_mn_major, int b_mn_major, const void* A,
+                            const void* B, float* D_raw, void* stream);
+
+/* Reads and clears the library's device error word (nonzero after a bounded
+ * wait inside a kernel gave up).  Synchronises the device. */
+gdn_status gdn_device_error(unsigned int* flag);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_SELFTEST_H */

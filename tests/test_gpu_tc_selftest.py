@@ -1,0 +1,66 @@
+"""tcgen05 self-check: the library's shared-memory operand layouts, MMA issue and
+TMEM read-back against a reference matrix product (bf16 in, fp32 out)."""
+
+import ctypes
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from gated_delta_rule_06_gb300 import build, ops
+
+    build.build()
+    L = ops.load_library()
+    L.gdn_selftest_mma.argtypes = [ctypes.c_int] * 5 + [ctypes.c_void_p] * 4
+    L.gdn_selftest_mma.restype = ctypes.c_int
+    L.gdn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+    L.gdn_device_error.restype = ctypes.c_int
+    return L
+
+
+def _run(lib, M, N, K, amn, bmn, seed=0):
+    g = torch.Generator().manual_seed(seed + M + N + K)
+    A = torch.randn((M, K), generator=g).to(torch.bfloat16).cuda()
+    B = torch.randn((K, N), generator=g).to(torch.bfloat16).cuda()
+    D = torch.full((128, N), float("nan"), device="cuda")
+    rc = lib.gdn_selftest_mma(M, N, K, amn, bmn, ctypes.c_void_p(A.data_ptr()),
+                              ctypes.c_void_p(B.data_ptr()), ctypes.c_void_p(D.data_ptr()),
+                              ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    torch.cuda.synchronize()
+    ref = A.float() @ B.float()
+    return D, ref
+
+
+def _lanes_m64():
+    # accumulator row r of an M = 64 MMA sits in TMEM lane 32 * (r // 16) + r % 16
+    return torch.tensor([32 * (r // 16) + r % 16 for r in range(64)])
+
+
+@pytest.mark.parametrize("amn", [0, 1])
+@pytest.mark.parametrize("bmn", [0, 1])
+@pytest.mark.parametrize("N,K", [(64, 16), (64, 192), (128, 64), (192, 128), (256, 32)])
+def test_m128(lib, amn, bmn, N, K):
+    D, ref = _run(lib, 128, N, K, amn, bmn)
+    torch.testing.assert_close(D, ref, rtol=1e-5, atol=1e-4)
+
+
+@pytest.mark.parametrize("amn", [0, 1])
+@pytest.mark.parametrize("bmn", [0, 1])
+@pytest.mark.parametrize("N,K", [(64, 64), (192, 32), (128, 16)])
+def test_m64_lane_placement(lib, amn, bmn, N, K):
+    D, ref = _run(lib, 64, N, K, amn, bmn)
+    got = D[_lanes_m64().cuda()]
+    torch.testing.assert_close(got, ref, rtol=1e-5, atol=1e-4)
+
+
+def test_no_wait_timeouts(lib):
+    flag = ctypes.c_uint(123)
+    assert lib.gdn_device_error(ctypes.byref(flag)) == 0
+    assert flag.value == 0
