@@ -90,10 +90,10 @@ Layout make_layout(const gdn::Dims& d) {
     L.Tinv = o; o = align_up(o + BH * d.NC * gdn::kChunk * gdn::kChunk * 4);
     L.W = o; o = align_up(o + perstep * d.Dk * es);
     L.P = o; o = align_up(o + BH * d.NC * gdn::kChunk * gdn::kChunk * es);
-    L.Delta = o; o = align_up(o + perstep * d.Dv * es);
+    L.Delta = o; o = align_up(o + perstep * d.Dv * 4);
     L.saved_total = o;
     o = 0;
-    L.U = o; o = align_up(o + perstep * d.Dv * es);
+    L.U = o; o = align_up(o + perstep * d.Dv * 4);
     L.fwd_total = o;
     o = 0;
     L.dSck = o; o = align_up(o + state_ck);
@@ -117,7 +117,7 @@ void carve_saved(const Layout& L, void* saved, gdn::Ptrs* p) {
     p->Tinv = reinterpret_cast<float*>(s + L.Tinv);
     p->W = s + L.W;
     p->P = s + L.P;
-    p->Delta = s + L.Delta;
+    p->Delta = reinterpret_cast<float*>(s + L.Delta);
 }
 
 gdn_status cuda_status(cudaError_t e) {
@@ -132,7 +132,8 @@ gdn_status cuda_status(cudaError_t e) {
 namespace gdn {
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n); }
 unsigned int read_clear_error_all() {
-    const unsigned int words[] = {read_clear_error_selftest()};
+    const unsigned int words[] = {read_clear_error_selftest(), read_clear_error_bwdtc(),
+                                  read_clear_error_scantc()};
     unsigned int v = 0;
     for (unsigned int w : words) {
         if (w == ~0u) return ~0u;
@@ -212,7 +213,7 @@ gdn_status gdn_forward(const gdn_shape* shape, const void* q, const void* k, con
         if (ws_bytes < L.fwd_total + L.saved_total) return GDN_ERR_WORKSPACE_TOO_SMALL;
         carve_saved(L, wsb + L.fwd_total, &p);
     }
-    p.U = wsb + L.U;
+    p.U = reinterpret_cast<float*>(wsb + L.U);
     cudaError_t e = run_phase("prep", s, [&] { return gdn::launch_prep(d, p, s); });
     if (e == cudaSuccess) e = run_phase("fwd_chunk", s, [&] { return gdn::launch_fwd_chunk(d, p, s); });
     if (e == cudaSuccess) e = run_phase("fwd_scan", s, [&] { return gdn::launch_fwd_scan(d, p, s); });

@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(256) bwd_chunk_kernel(Dims d, Ptrs p) {
     const TI* k = (const TI*)p.k;
     const TI* v = (const TI*)p.v;
     const TI* dO = (const TI*)p.d_o;
-    const TI* Delta = (const TI*)p.Delta;
+    const float* Delta = p.Delta;
     TI* dv = (TI*)p.dv;
     const float qscale = rsqrtf((float)Dk);
     const int64_t t0 = (int64_t)c * C;
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(256) bwd_chunk_kernel(Dims d, Ptrs p) {
             const bool in = t < d.T;
             bO[i * kBlk + x] = in ? ldf(dOb + t * d.Hv * Dv + dv0 + x) : 0.f;
             bV[i * kBlk + x] = in ? ldf(vb + t * d.Hv * Dv + dv0 + x) : 0.f;
-            bD[i * kBlk + x] = ldf(Delta + (gbase + i) * Dv + dv0 + x);
+            bD[i * kBlk + x] = Delta[(gbase + i) * Dv + dv0 + x];
             bDb[i * kBlk + x] = p.Dbar[(gbase + i) * Dv + dv0 + x];
         }
         __syncthreads();
@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(256) bwd_chunk_kernel(Dims d, Ptrs p) {
                 const int i = idx / nv, x = idx % nv;
                 const int64_t t = t0 + i;
                 bO[i * kBlk + x] = t < d.T ? ldf(dOb + t * d.Hv * Dv + dv0 + x) : 0.f;
-                bD[i * kBlk + x] = ldf(Delta + (gbase + i) * Dv + dv0 + x);
+                bD[i * kBlk + x] = Delta[(gbase + i) * Dv + dv0 + x];
                 bDb[i * kBlk + x] = p.Dbar[(gbase + i) * Dv + dv0 + x];
             }
             __syncthreads();
@@ -560,6 +560,7 @@ cudaError_t launch_reduce_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_bwd_scan(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    if (scan_tc_supported(d)) return launch_bwd_scan_tc(d, p, s);
     if (d.Dv % 32 == 0)
         return d.dtype == 1 ? launch_bscan_t<__nv_bfloat16, 32>(d, p, s) : launch_bscan_t<float, 32>(d, p, s);
     if (d.Dv % 16 == 0)
@@ -568,6 +569,7 @@ cudaError_t launch_bwd_scan(const Dims& d, const Ptrs& p, cudaStream_t s) {
 }
 
 cudaError_t launch_bwd_chunk(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    if (bwd_chunk_tc_supported(d)) return launch_bwd_chunk_tc(d, p, s);
     return d.dtype == 1 ? launch_bchunk_t<__nv_bfloat16>(d, p, s) : launch_bchunk_t<float>(d, p, s);
 }
 

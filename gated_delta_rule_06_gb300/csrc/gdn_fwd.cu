@@ -118,8 +118,8 @@ __global__ void __launch_bounds__(256) fwd_chunk_kernel(Dims d, Ptrs p) {
     __syncthreads();
     cta_gemm<4, 4>(kChunk, Dv, kChunk, Ti, kChunk, 1, X1, Dv, 1, X2, Dv, 1.f, 0.f, nullptr);
     __syncthreads();
-    TI* U = (TI*)p.U + gbase * Dv;
-    for (int idx = threadIdx.x; idx < kChunk * Dv; idx += blockDim.x) stf(U + idx, X2[idx]);
+    float* U = p.U + gbase * Dv;
+    for (int idx = threadIdx.x; idx < kChunk * Dv; idx += blockDim.x) U[idx] = X2[idx];
 }
 
 // ---------------------------------------------------------------------------
@@ -146,9 +146,9 @@ __global__ void __launch_bounds__(256) fwd_scan_kernel(Dims d, Ptrs p) {
     const TI* q = (const TI*)p.q;
     const TI* k = (const TI*)p.k;
     const TI* W = (const TI*)p.W;
-    const TI* U = (const TI*)p.U;
+    const float* U = p.U;
     const TI* P = (const TI*)p.P;
-    TI* Delta = (TI*)p.Delta;
+    float* Delta = p.Delta;
     TI* o = (TI*)p.o;
     const float qscale = rsqrtf((float)Dk);
     const int64_t sbase = ((int64_t)bb * d.Hv + h) * Dk * Dv;
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(256) fwd_scan_kernel(Dims d, Ptrs p) {
             big[idx] = ldf(W + gbase * Dk + idx);
         for (int idx = threadIdx.x; idx < kChunk * DVT; idx += blockDim.x) {
             const int i = idx / DVT, n = idx % DVT;
-            Dl[idx] = ldf(U + (gbase + i) * Dv + n0 + n);
+            Dl[idx] = U[(gbase + i) * Dv + n0 + n];
         }
         __syncthreads();
         // Delta = U - W S
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(256) fwd_scan_kernel(Dims d, Ptrs p) {
         __syncthreads();
         for (int idx = threadIdx.x; idx < kChunk * DVT; idx += blockDim.x) {
             const int i = idx / DVT, n = idx % DVT;
-            stf(Delta + (gbase + i) * Dv + n0 + n, Dl[idx]);
+            Delta[(gbase + i) * Dv + n0 + n] = Dl[idx];
         }
         // O = diag(gam) Q S + P Delta
         for (int idx = threadIdx.x; idx < kChunk * Dk; idx += blockDim.x) {
@@ -259,6 +259,7 @@ cudaError_t launch_fwd_chunk(const Dims& d, const Ptrs& p, cudaStream_t s) {
 }
 
 cudaError_t launch_fwd_scan(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    if (scan_tc_supported(d)) return launch_fwd_scan_tc(d, p, s);
     if (d.Dv % 32 == 0)
         return d.dtype == 1 ? launch_scan_t<__nv_bfloat16, 32>(d, p, s) : launch_scan_t<float, 32>(d, p, s);
     if (d.Dv % 16 == 0)

@@ -40,9 +40,10 @@ struct Ptrs {
     float* Tinv;   // [B, Hv, NC, 64, 64] fp32 (I + A)^-1 per chunk
     void* W;       // [B, Hv, Tp, Dk]  T diag(beta gam) K   (input dtype)
     void* P;       // [B, Hv, NC, 64, 64] (Q K^T) o M, lower incl. diagonal
-    void* Delta;   // [B, Hv, Tp, Dv]  U - W S  per chunk
+    float* Delta;  // [B, Hv, Tp, Dv]  U - W S  per chunk (fp32: Delta cancels, see U)
     // forward workspace
-    void* U;       // [B, Hv, Tp, Dv]  T diag(beta) V
+    float* U;      // [B, Hv, Tp, Dv]  T diag(beta) V (fp32: Delta = U - W S cancels,
+                   // so a rounded U would dominate the error of the log-decay gradient)
     // backward inputs / outputs
     const void* d_o;
     const float* d_state_T;
@@ -116,6 +117,14 @@ cudaError_t launch_bwd_chunk(const Dims& d, const Ptrs& p, cudaStream_t s);
 cudaError_t launch_bwd_reduce(const Dims& d, const Ptrs& p, cudaStream_t s);
 cudaError_t launch_decode(const Dims& d, const Ptrs& p, cudaStream_t s);
 bool decode_supported(int64_t Dk, int64_t Dv);
+// tensor-core (tcgen05) variants for bf16 inputs
+bool bwd_chunk_tc_supported(const Dims& d);
+cudaError_t launch_bwd_chunk_tc(const Dims& d, const Ptrs& p, cudaStream_t s);
+unsigned int read_clear_error_bwdtc();
+bool scan_tc_supported(const Dims& d);
+cudaError_t launch_fwd_scan_tc(const Dims& d, const Ptrs& p, cudaStream_t s);
+cudaError_t launch_bwd_scan_tc(const Dims& d, const Ptrs& p, cudaStream_t s);
+unsigned int read_clear_error_scantc();
 // adds n to the library's launch counter (called by every launcher)
 void count_launches(int n);
 // reads and clears the device error words of every translation unit

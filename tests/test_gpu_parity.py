@@ -77,6 +77,16 @@ def test_head_dims(Dk, Dv, Hk, Hv, dtype):
     _full_parity(w)
 
 
+@pytest.mark.parametrize("T", [1, 64, 65, 130, 200])
+@pytest.mark.parametrize("Dk,Dv", [(64, 64), (128, 128), (192, 128), (96, 192)])
+def test_tensor_core_paths_bf16(T, Dk, Dv):
+    """bf16 shapes that take the tcgen05 kernels (Dk % 32 == 0, Dv % 64 == 0):
+    ragged tails, half masking, the clamp head and GQA."""
+    w = wl.custom("tc", 2, T, 2, 4, Dk, Dv, dtype=torch.bfloat16, seed=7 * T + Dk + Dv,
+                  mask="half_second_batch" if T > 65 else "none", clamp_head=True)
+    _full_parity(w)
+
+
 def test_zero_initial_state_and_no_state_cotangent():
     w = wl.custom("zs", 2, 70, 2, 4, 32, 32, dtype=torch.float32, seed=5, state_sigma=0.0,
                   d_state=False)
@@ -99,7 +109,7 @@ def test_all_true_mask_equals_no_mask():
 
 def test_deterministic_bitwise():
     """Two runs give byte-identical outputs and gradients (no atomics anywhere)."""
-    w = wl.custom("det", 2, 150, 2, 4, 64, 32, dtype=torch.bfloat16, seed=9,
+    w = wl.custom("det", 2, 150, 2, 4, 64, 64, dtype=torch.bfloat16, seed=9,
                   mask="half_second_batch")
     xd = to_dev(wl.make_inputs(w))
     outs = []
