@@ -109,6 +109,33 @@ gdn_status gdn_backward(const gdn_shape* shape, const void* q, const void* k, co
                         float* ddt_bias, float* dstate0, void* ws, size_t ws_bytes,
                         void* stream);
 
+/* ---- forward without any allocation -------------------------------------- */
+
+/* Inference forward (no saved buffer) that allocates nothing and takes no
+ * workspace: for callers that cannot allocate device memory where they run the
+ * op (an inference runtime or plugin host that forbids allocation while work
+ * is enqueued, code inside a CUDA stream capture, a host whose device memory
+ * is fixed up front).  The pages have no counterpart: it is a packaging of
+ * gdn_forward (saved = NULL) whose scratch lives in a fixed device array owned
+ * by the library.
+ *   - Inputs, outputs, layouts and results are those of gdn_forward with
+ *     saved = NULL; the caller passes only inputs and outputs.
+ *   - The scratch is a static device array of gdn_noalloc_scratch_bytes()
+ *     bytes (64 MiB) that every GPU which loads the library holds until the
+ *     process exits.  Shapes whose gdn_workspace_bytes(shape, 2) exceeds it are
+ *     rejected with GDN_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the one array and leave their intermediates in it:
+ *     calls whose work overlaps on the GPU (other streams, other threads)
+ *     race; serialise them.  Nothing in it needs to start at zero.
+ *   - Returns GDN_ERR_CUDA if the address lookup or a launch fails. */
+size_t gdn_noalloc_scratch_bytes(void);
+gdn_status gdn_forward_noalloc(const gdn_shape* shape, const void* q, const void* k,
+                               const void* v, const void* a, const void* b, const float* A_log,
+                               const float* dt_bias, const float* state0, const uint8_t* mask,
+                               void* o, float* state_T, void* stream);
+
 /* ---- instrumentation (host-only bookkeeping, off by default) -------------- */
 
 /* Number of CUDA kernels this library has launched in this process so far. */
