@@ -108,43 +108,52 @@ __device__ __forceinline__ void ld8(const float* p, float (&v)[8]) {
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-// Stage a [64 rows x ncols] block into a canonical tile (x = column, y = row):
-// value = src[row * ld + col] * rs[row] * sign, rows >= nvalid are zero.
-template <typename TS>
-__device__ __forceinline__ void stage(uint8_t* tile, const TS* src, int64_t ld, int ncols,
-                                      int nvalid, const float* rs, float sign) {
+// 64-row bf16 tile (x = column) fetched with 16-byte cp.async; rows >= nvalid zero
+__device__ __forceinline__ void cpa_tile(uint8_t* tile, const __nv_bfloat16* src, int64_t ld,
+                                         int ncols, int nvalid) {
     const int cpr = ncols / 8;
+    const uint32_t base = tc::smem_u32(tile);
     const uint32_t ys = (uint32_t)ncols * 16u;
     for (int e = threadIdx.x; e < C * cpr; e += blockDim.x) {
         const int row = e / cpr, cc = e % cpr;
-        float v[8];
-        if (row < nvalid) {
-            ld8(src + row * ld + cc * 8, v);
-            const float s = sign * (rs ? rs[row] : 1.f);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] *= s;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = 0.f;
-        }
-        st_bf16x8(tile + cc * 128u + (row >> 3) * ys + (row & 7) * 16u, v);
+        const bool in = row < nvalid;
+        tc::cp_async16(base + cc * 128u + (row >> 3) * ys + (row & 7) * 16u,
+                       src + (in ? row : 0) * ld + cc * 8, in ? 16u : 0u);
     }
 }
 
-// Stage a [64 x ncols] fp32 block as two bf16 tiles hi + lo (lo = v - hi).
-__device__ __forceinline__ void stage_split(uint8_t* hi, uint8_t* lo, const float* src, int64_t ld,
-                                            int ncols) {
+// Stage 64 rows x ncols of an fp32 matrix as bf16 tiles (x = column).  With lo
+// != nullptr the value is split into hi + lo (lo = v - bf16(v)).  Loads are
+// issued four 8-element chunks deep per thread before any is stored.
+__device__ __forceinline__ void stage_f32(uint8_t* hi, uint8_t* lo, const float* src, int64_t ld,
+                                          int ncols, float sign) {
+    constexpr int U = 4;
     const int cpr = ncols / 8;
+    const int total = C * cpr;
     const uint32_t ys = (uint32_t)ncols * 16u;
-    for (int e = threadIdx.x; e < C * cpr; e += blockDim.x) {
-        const int row = e / cpr, cc = e % cpr;
-        float v[8], l[8];
-        ld8(src + row * ld + cc * 8, v);
+    for (int base = threadIdx.x; base < total; base += U * blockDim.x) {
+        float v[U][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) l[i] = v[i] - __bfloat162float(__float2bfloat16_rn(v[i]));
-        const uint32_t o = cc * 128u + (row >> 3) * ys + (row & 7) * 16u;
-        st_bf16x8(hi + o, v);
-        st_bf16x8(lo + o, l);
+        for (int u = 0; u < U; ++u) {
+            const int e = base + u * blockDim.x;
+            if (e < total) ld8(src + (e / cpr) * ld + (e % cpr) * 8, v[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = base + u * blockDim.x;
+            if (e < total) {
+                const int row = e / cpr, cc = e % cpr;
+                const uint32_t o = cc * 128u + (row >> 3) * ys + (row & 7) * 16u;
+                float l[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    v[u][i] *= sign;
+                    l[i] = v[u][i] - __bfloat162float(__float2bfloat16_rn(v[u][i]));
+                }
+                st_bf16x8(hi + o, v[u]);
+                if (lo) st_bf16x8(lo + o, l);
+            }
+        }
     }
 }
 
@@ -253,13 +262,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     const int64_t ldq = d.Hk * Dk, ldv = d.Hv * Dv;
     // q and k enter as the exact bf16 inputs; their normalisations are applied
     // in fp32 to the other operand or in the epilogues
-    stage(sm + L.K, k + ((int64_t)bb * d.T + t0) * ldq + (int64_t)j * Dk, ldq, Dk, nvalid, nullptr, 1.f);
-    stage(sm + L.Q, q + ((int64_t)bb * d.T + t0) * ldq + (int64_t)j * Dk, ldq, Dk, nvalid, nullptr, 1.f);
-    stage(sm + L.O, dO + ((int64_t)bb * d.T + t0) * ldv + (int64_t)h * Dv, ldv, Dv, nvalid, nullptr, 1.f);
-    stage(sm + L.V, v + ((int64_t)bb * d.T + t0) * ldv + (int64_t)h * Dv, ldv, Dv, nvalid, nullptr, 1.f);
-    stage_split(sm + L.D, sm + L.Dlo, Delta + gbase * Dv, Dv, Dv);
-    stage(sm + L.NB, p.Dbar + gbase * Dv, Dv, Dv, C, nullptr, -1.f);
-    stage(sm + L.Tt, p.Tinv + (((int64_t)bb * d.Hv + h) * d.NC + c) * C * C, C, C, C, nullptr, 1.f);
+    cpa_tile(sm + L.K, k + ((int64_t)bb * d.T + t0) * ldq + (int64_t)j * Dk, ldq, Dk, nvalid);
+    cpa_tile(sm + L.Q, q + ((int64_t)bb * d.T + t0) * ldq + (int64_t)j * Dk, ldq, Dk, nvalid);
+    cpa_tile(sm + L.O, dO + ((int64_t)bb * d.T + t0) * ldv + (int64_t)h * Dv, ldv, Dv, nvalid);
+    cpa_tile(sm + L.V, v + ((int64_t)bb * d.T + t0) * ldv + (int64_t)h * Dv, ldv, Dv, nvalid);
+    tc::cp_async_commit();
+    stage_f32(sm + L.D, sm + L.Dlo, Delta + gbase * Dv, Dv, Dv, 1.f);
+    stage_f32(sm + L.NB, nullptr, p.Dbar + gbase * Dv, Dv, Dv, -1.f);
+    stage_f32(sm + L.Tt, nullptr, p.Tinv + (((int64_t)bb * d.Hv + h) * d.NC + c) * C * C, C, C, 1.f);
+    tc::cp_async_wait_all();
     tc::fence_async_smem();
     tc::tc_fence_before();
     __syncthreads();
@@ -311,27 +322,42 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
         });
     }
 
-    // ---- phase 1: state products per 64-wide block of Dk
+    // ---- phase 1: state products per kBlkK-wide block of Dk.  The fp32 S and
+    // Sbar' rows of the next block are loaded into registers while the current
+    // block's MMAs run.
     float gcb = 0.f;
+    constexpr int kPer = (kBlkK * 256 / 8 + kThreads - 1) / kThreads;  // chunks per thread (Dv <= 256)
+    float pre_s[kPer][8], pre_p[kPer][8];
+    const int cpr_s = Dv / 8;
+    auto load_blk = [&](int dk0, int nk) {
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int e = tid + u * kThreads;
+            if (e < nk * cpr_s) {
+                const int64_t off = cbase + (int64_t)(dk0 + e / cpr_s) * Dv + (e % cpr_s) * 8;
+                ld8(p.ckpt + off, pre_s[u]);
+                ld8(p.dSck + off, pre_p[u]);
+            }
+        }
+    };
+    load_blk(0, Dk < kBlkK ? Dk : kBlkK);
     for (int dk0 = 0; dk0 < Dk; dk0 += kBlkK) {
         const int nk = Dk - dk0 < kBlkK ? Dk - dk0 : kBlkK;
         tc::tc_fence_before();
         __syncthreads();  // previous block's TMEM reads and MMAs are done
-        // S and Sbar' rows dk0 .. dk0 + nk (x = dv, y = dk - dk0)
         {
-            const int cpr = Dv / 8;
             const uint32_t ys = (uint32_t)Dv * 16u;
-            for (int e = tid; e < nk * cpr; e += blockDim.x) {
-                const int row = e / cpr, cc = e % cpr;
-                float a[8], b2[8];
-                const int64_t off = cbase + (int64_t)(dk0 + row) * Dv + cc * 8;
-                ld8(p.ckpt + off, a);
-                ld8(p.dSck + off, b2);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) gcb = fmaf(a[i], b2[i], gcb);
-                const uint32_t o = cc * 128u + (row >> 3) * ys + (row & 7) * 16u;
-                st_bf16x8(sm + L.S + o, a);
-                st_bf16x8(sm + L.Sp + o, b2);
+            for (int u = 0; u < kPer; ++u) {
+                const int e = tid + u * kThreads;
+                if (e < nk * cpr_s) {
+                    const int row = e / cpr_s, cc = e % cpr_s;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) gcb = fmaf(pre_s[u][i], pre_p[u][i], gcb);
+                    const uint32_t o = cc * 128u + (row >> 3) * ys + (row & 7) * 16u;
+                    st_bf16x8(sm + L.S + o, pre_s[u]);
+                    st_bf16x8(sm + L.Sp + o, pre_p[u]);
+                }
             }
         }
         tc::fence_async_smem();
@@ -346,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
             tc::mma_tile(tb + 128, tDlo, tSp, C, nk, Dv, true);
             tc::mma_commit(&bar);
         }
+        if (dk0 + kBlkK < Dk) load_blk(dk0 + kBlkK, Dk - dk0 - kBlkK < kBlkK ? Dk - dk0 - kBlkK : kBlkK);
         sync_after_mma(&bar, phase, ok);
         if (ok) {
             const int g = warp >> 2;
@@ -430,7 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
         });
     }
     const float* Tg = p.Tinv + (((int64_t)bb * d.Hv + h) * d.NC + c) * C * C;
-    for (int i = tid; i < C * C; i += blockDim.x) Tf[i] = Tg[i];
+    for (int i = tid; i < C * C / 4; i += blockDim.x)
+        reinterpret_cast<float4*>(Tf)[i] = reinterpret_cast<const float4*>(Tg)[i];
     __syncthreads();
     if (tid < C) {
         const int i = tid;

@@ -254,6 +254,7 @@ cudaError_t launch_fwd_chunk_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_fwd_chunk(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    if (fwd_chunk_tc_supported(d)) return launch_fwd_chunk_tc(d, p, s);
     return d.dtype == 1 ? launch_fwd_chunk_t<__nv_bfloat16>(d, p, s)
                         : launch_fwd_chunk_t<float>(d, p, s);
 }

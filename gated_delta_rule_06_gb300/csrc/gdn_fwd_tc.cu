@@ -1,0 +1,329 @@
+// gdn_fwd_tc.cu -- chunk-local WY/UT products of the forward on the tensor
+// cores (tcgen05, bf16 operands, fp32 accumulators in TMEM) for bf16 inputs.
+//
+// Per (chunk, value head, batch), with raw q, k, v (mlx-lm PR "Add
+// gated_delta_update VJP", "Scope and follow-ups": chunk-parallel form through a
+// lower-triangular solve; torch-to-nnef "custom_extractors/gdn": the chunked
+// rule equals the recurrent one):
+//   K K^T, Q K^T                 (M = 64 MMAs; norms and 1/sqrt(Dk) applied in fp32)
+//   A_ij = beta_i M_ij <k_i, k_j>  (j < i),   P_ij = M_ij <q_i, k_j>  (j <= i)
+//   T = (I + A)^-1               blocked forward substitution in fp32 (16 x 16 blocks)
+//   W = T diag(beta gam r_k) K,   U = T diag(beta) V
+// T enters the W / U products as two bf16 terms (hi + lo) so that U keeps fp32
+// accuracy (the forward state update subtracts W S from U).  Outputs: T (fp32),
+// P, W (bf16), U (fp32).
+#include "gdn_internal.cuh"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+
+GDN_ERROR_WORD(fwdtc)
+
+namespace {
+
+constexpr int C = kChunk;
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ uint32_t canon(int x, int y, int ncols) {
+    return (uint32_t)(x >> 3) * 128u + (uint32_t)(y >> 3) * (uint32_t)ncols * 16u +
+           (uint32_t)(y & 7) * 16u + (uint32_t)(x & 7) * 2u;
+}
+
+__device__ __forceinline__ void st_bf16x8(uint8_t* dst, const float* v) {
+    uint4 u;
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]);
+    __nv_bfloat162 h1 = __floats2bfloat162_rn(v[2], v[3]);
+    __nv_bfloat162 h2 = __floats2bfloat162_rn(v[4], v[5]);
+    __nv_bfloat162 h3 = __floats2bfloat162_rn(v[6], v[7]);
+    u.x = *reinterpret_cast<uint32_t*>(&h0);
+    u.y = *reinterpret_cast<uint32_t*>(&h1);
+    u.z = *reinterpret_cast<uint32_t*>(&h2);
+    u.w = *reinterpret_cast<uint32_t*>(&h3);
+    *reinterpret_cast<uint4*>(dst) = u;
+}
+
+__device__ __forceinline__ void cpa_tile(uint8_t* tile, const __nv_bfloat16* src, int64_t ld,
+                                         int ncols, int nvalid) {
+    const int cpr = ncols / 8;
+    const uint32_t base = tc::smem_u32(tile);
+    for (int e = threadIdx.x; e < C * cpr; e += blockDim.x) {
+        const int row = e / cpr, cc = e % cpr;
+        const bool in = row < nvalid;
+        tc::cp_async16(base + canon(cc * 8, row, ncols), src + (in ? row : 0) * ld + cc * 8,
+                       in ? 16u : 0u);
+    }
+}
+
+__device__ __forceinline__ tc::Tile tile_of(uint8_t* p, int ncols, bool k_major) {
+    tc::Tile t;
+    t.base = tc::smem_u32(p);
+    t.xs = 128;
+    t.ys = (uint32_t)ncols * 16u;
+    t.k_major = k_major;
+    return t;
+}
+
+// M = 64 accumulator walk: warp w reads rows 16 (w % 4) .. +15, column half w / 4
+template <typename F>
+__device__ __forceinline__ void acc_rows(uint32_t tbase, uint32_t col0, int ncols, F&& f) {
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    const int sp = w & 3, g = w >> 2;
+    const int half = ncols / 2;
+    for (int c = g * half; c < (g + 1) * half; c += 16) {
+        float v[16];
+        tc::tmem_ld16(tc::tmem_addr(tbase, 32 * sp, col0 + c), v);
+        tc::tmem_wait_ld();
+        if (l < 16) f(16 * sp + l, c, v);
+    }
+}
+
+// T = (I + A)^-1 for a 64 x 64 strictly lower A (fp32, row-major in shared
+// memory), by forward substitution on 16 x 16 blocks: the four diagonal blocks
+// first, then the block sub-diagonals d = 1, 2, 3 with
+//   T_ij = -T_ii * sum_{k=j}^{i-1} A_ik T_kj.
+// X is 64 x 64 scratch.  All threads of the CTA take part; ends synchronised.
+__device__ void tri_inverse64(const float* A, float* T, float* X) {
+    const int tid = threadIdx.x;
+    for (int e = tid; e < C * C; e += blockDim.x) T[e] = 0.f;
+    __syncthreads();
+    if (tid < C) {
+        const int blk = tid >> 4, c = tid & 15, o = 16 * blk;
+        float col[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float v = (i == c) ? 1.f : 0.f;
+#pragma unroll
+            for (int jj = 0; jj < i; ++jj) v = fmaf(-A[(o + i) * C + o + jj], col[jj], v);
+            col[i] = (i < c) ? 0.f : v;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) T[(o + i) * C + o + c] = col[i];
+    }
+    __syncthreads();
+    for (int dlt = 1; dlt < 4; ++dlt) {
+        const int nb = 4 - dlt;  // blocks (bi, bj = bi - dlt), bi = dlt .. 3
+        for (int e = tid; e < nb * 256; e += blockDim.x) {
+            const int b = e >> 8, r = (e >> 4) & 15, c = e & 15;
+            const int bi = dlt + b, bj = b;
+            float s = 0.f;
+            for (int k = 16 * bj; k < 16 * bi; ++k) s = fmaf(A[(16 * bi + r) * C + k], T[k * C + 16 * bj + c], s);
+            X[(16 * bi + r) * C + 16 * bj + c] = s;
+        }
+        __syncthreads();
+        for (int e = tid; e < nb * 256; e += blockDim.x) {
+            const int b = e >> 8, r = (e >> 4) & 15, c = e & 15;
+            const int bi = dlt + b, bj = b;
+            float s = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                s = fmaf(T[(16 * bi + r) * C + 16 * bi + k], X[(16 * bi + k) * C + 16 * bj + c], s);
+            T[(16 * bi + r) * C + 16 * bj + c] = -s;
+        }
+        __syncthreads();
+    }
+}
+
+struct F1Smem {
+    uint32_t K, Q, V, A, T, X, Tw, Twl, Tu, Tul, vec, total;
+};
+
+__host__ __device__ inline F1Smem f1_plan(int Dk, int Dv) {
+    F1Smem s{};
+    uint32_t o = 0;
+    auto take = [&](uint32_t bytes) {
+        const uint32_t r = o;
+        o += (bytes + 1023u) & ~1023u;
+        return r;
+    };
+    s.K = take(C * Dk * 2);
+    s.Q = take(C * Dk * 2);
+    s.V = take(C * Dv * 2);
+    s.A = take(C * C * 4);
+    s.T = take(C * C * 4);
+    s.X = take(C * C * 4);
+    s.Tw = take(C * C * 2);
+    s.Twl = take(C * C * 2);
+    s.Tu = take(C * C * 2);
+    s.Tul = take(C * C * 2);
+    s.vec = take(8 * C * 4 + C * 8);
+    s.total = o;
+    return s;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) fwd_chunk_tc_kernel(Dims d, Ptrs p) {
+    extern __shared__ __align__(1024) uint8_t sm[];
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tmem_sh;
+    const int c = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
+    const int j = h / (int)d.G;
+    const int Dk = (int)d.Dk, Dv = (int)d.Dv;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const F1Smem L = f1_plan(Dk, Dv);
+    float* vec = reinterpret_cast<float*>(sm + L.vec);
+    float* bt = vec;            // beta
+    float* gm = bt + C;         // exp(Gamma)
+    float* rqv = gm + C;        // r_q / sqrt(Dk)
+    float* rkv = rqv + C;       // r_k
+    double* Gm = reinterpret_cast<double*>(vec + 8 * C);
+    float* A = reinterpret_cast<float*>(sm + L.A);
+    float* Tm = reinterpret_cast<float*>(sm + L.T);
+    float* X = reinterpret_cast<float*>(sm + L.X);
+
+    const int64_t t0 = (int64_t)c * C;
+    const int nvalid = (int)(d.T - t0 < C ? d.T - t0 : C);
+    const int64_t bh = (int64_t)bb * d.Hv + h;
+    const int64_t gbase = bh * d.Tp + t0;
+    const int64_t rbase = ((int64_t)bb * d.Hk + j) * d.Tp + t0;
+    const int64_t ldq = d.Hk * Dk, ldv = d.Hv * Dv;
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
+    const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(p.k);
+    const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(p.v);
+
+    cpa_tile(sm + L.K, k + ((int64_t)bb * d.T + t0) * ldq + (int64_t)j * Dk, ldq, Dk, nvalid);
+    cpa_tile(sm + L.Q, q + ((int64_t)bb * d.T + t0) * ldq + (int64_t)j * Dk, ldq, Dk, nvalid);
+    cpa_tile(sm + L.V, v + ((int64_t)bb * d.T + t0) * ldv + (int64_t)h * Dv, ldv, Dv, nvalid);
+    tc::cp_async_commit();
+    if (warp == 0) {
+        tc::tmem_alloc(&tmem_sh, 512);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        tc::mbar_init(&bar, 1);
+        tc::fence_mbar_init();
+    }
+    if (tid < C) {
+        const double G = p.gam[gbase + tid];
+        Gm[tid] = G;
+        gm[tid] = expf((float)G);
+        bt[tid] = p.beta[gbase + tid];
+        rqv[tid] = p.rq[rbase + tid] * rsqrtf((float)Dk);
+        rkv[tid] = p.rk[rbase + tid];
+    }
+    tc::cp_async_wait_all();
+    tc::fence_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tb = tmem_sh;
+    uint32_t phase = 0;
+    bool ok = true;
+    const tc::Tile tK = tile_of(sm + L.K, Dk, true), tQ = tile_of(sm + L.Q, Dk, true);
+    const tc::Tile tKmn = tile_of(sm + L.K, Dk, false), tVmn = tile_of(sm + L.V, Dv, false);
+
+    // ---- Grams of the raw rows
+    if (tid == 0) {
+        tc::mma_tile(tb + 0, tK, tK, C, C, Dk, false);
+        tc::mma_tile(tb + 64, tQ, tK, C, C, Dk, false);
+        tc::mma_commit(&bar);
+    }
+    ok = tc::mbar_wait(&bar, phase, &g_err_fwdtc) && ok;
+    phase ^= 1u;
+    tc::tc_fence_after();
+    __nv_bfloat16* P = static_cast<__nv_bfloat16*>(p.P) + (bh * d.NC + c) * C * C;
+    if (ok) {
+        acc_rows(tb, 0, C, [&](int r, int c0, const float (&x)[16]) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int jj = c0 + i;
+                const float m = jj < r ? expf((float)(Gm[r] - Gm[jj])) : 0.f;
+                A[r * C + jj] = bt[r] * m * rkv[r] * rkv[jj] * x[i];
+            }
+        });
+        acc_rows(tb, 64, C, [&](int r, int c0, const float (&x)[16]) {
+            float pv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int jj = c0 + i;
+                const float m = jj <= r ? expf((float)(Gm[r] - Gm[jj])) : 0.f;
+                pv[i] = m * rqv[r] * rkv[jj] * x[i];
+            }
+            uint8_t* dst = reinterpret_cast<uint8_t*>(P + r * C + c0);
+            st_bf16x8(dst, pv);
+            st_bf16x8(dst + 16, pv + 8);
+        });
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+
+    // ---- T = (I + A)^-1 (fp32)
+    tri_inverse64(A, Tm, X);
+    float* Tg = p.Tinv + (bh * d.NC + c) * C * C;
+    for (int e = tid; e < C * C / 4; e += blockDim.x)
+        reinterpret_cast<float4*>(Tg)[e] = reinterpret_cast<const float4*>(Tm)[e];
+    // A operands T diag(beta gam r_k) and T diag(beta), each as hi + lo bf16 (x = j, y = i)
+    for (int e = tid; e < C * (C / 8); e += blockDim.x) {
+        const int i = e / (C / 8), j0 = (e % (C / 8)) * 8;
+        float w8[8], wl[8], u8[8], ul[8];
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const int jj = j0 + s;
+            const float t = Tm[i * C + jj];
+            w8[s] = t * bt[jj] * gm[jj] * rkv[jj];
+            u8[s] = t * bt[jj];
+            wl[s] = w8[s] - __bfloat162float(__float2bfloat16_rn(w8[s]));
+            ul[s] = u8[s] - __bfloat162float(__float2bfloat16_rn(u8[s]));
+        }
+        const uint32_t o = canon(j0, i, C);
+        st_bf16x8(sm + L.Tw + o, w8);
+        st_bf16x8(sm + L.Twl + o, wl);
+        st_bf16x8(sm + L.Tu + o, u8);
+        st_bf16x8(sm + L.Tul + o, ul);
+    }
+    tc::fence_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+
+    // ---- W = T diag(beta gam r_k) K,  U = T diag(beta) V
+    const tc::Tile tTw = tile_of(sm + L.Tw, C, true), tTwl = tile_of(sm + L.Twl, C, true);
+    const tc::Tile tTu = tile_of(sm + L.Tu, C, true), tTul = tile_of(sm + L.Tul, C, true);
+    if (tid == 0) {
+        tc::mma_tile(tb + 0, tTw, tKmn, C, Dk, C, false);
+        tc::mma_tile(tb + 0, tTwl, tKmn, C, Dk, C, true);
+        tc::mma_tile(tb + Dk, tTu, tVmn, C, Dv, C, false);
+        tc::mma_tile(tb + Dk, tTul, tVmn, C, Dv, C, true);
+        tc::mma_commit(&bar);
+    }
+    ok = tc::mbar_wait(&bar, phase, &g_err_fwdtc) && ok;
+    phase ^= 1u;
+    tc::tc_fence_after();
+    if (ok) {
+        __nv_bfloat16* W = static_cast<__nv_bfloat16*>(p.W) + gbase * Dk;
+        float* U = p.U + gbase * Dv;
+        acc_rows(tb, 0, Dk, [&](int r, int c0, const float (&x)[16]) {
+            uint8_t* dst = reinterpret_cast<uint8_t*>(W + (int64_t)r * Dk + c0);
+            st_bf16x8(dst, x);
+            st_bf16x8(dst + 16, x + 8);
+        });
+        acc_rows(tb, Dk, Dv, [&](int r, int c0, const float (&x)[16]) {
+            float4* dst = reinterpret_cast<float4*>(U + (int64_t)r * Dv + c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+        });
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tb, 512);
+}
+
+}  // namespace
+
+bool fwd_chunk_tc_supported(const Dims& d) {
+    if (d.dtype != 1) return false;
+    if (d.Dk % 32 || d.Dv % 32 || d.Dk > 256 || d.Dv > 256) return false;
+    return f1_plan((int)d.Dk, (int)d.Dv).total + 2048 <= 227u * 1024u;
+}
+
+cudaError_t launch_fwd_chunk_tc(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    const size_t smem = f1_plan((int)d.Dk, (int)d.Dv).total + 1024;
+    auto kern = fwd_chunk_tc_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)d.NC, (unsigned)d.Hv, (unsigned)d.B);
+    kern<<<grid, kThreads, smem, s>>>(d, p);
+    count_launches(1);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace gdn

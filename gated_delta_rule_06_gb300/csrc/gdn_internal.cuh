@@ -125,6 +125,9 @@ bool scan_tc_supported(const Dims& d);
 cudaError_t launch_fwd_scan_tc(const Dims& d, const Ptrs& p, cudaStream_t s);
 cudaError_t launch_bwd_scan_tc(const Dims& d, const Ptrs& p, cudaStream_t s);
 unsigned int read_clear_error_scantc();
+bool fwd_chunk_tc_supported(const Dims& d);
+cudaError_t launch_fwd_chunk_tc(const Dims& d, const Ptrs& p, cudaStream_t s);
+unsigned int read_clear_error_fwdtc();
 // adds n to the library's launch counter (called by every launcher)
 void count_launches(int n);
 // reads and clears the device error words of every translation unit
