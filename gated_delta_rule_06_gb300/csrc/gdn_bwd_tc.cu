@@ -4,22 +4,18 @@
 // Same equations as the CUDA-core version in gdn_bwd.cu (reverse-mode
 // derivative of the chunked WY/UT form; mlx-lm PR "Add gated_delta_update
 // VJP", "What this PR adds" and "Scope and follow-ups").  One CTA per
-// (chunk, value head, batch); every product has the chunk's 64 time rows as
-// its M dimension (M = 64 MMAs, accumulator row r in TMEM lane
-// 32 (r / 16) + r % 16):
-//   phase 0:  Pbar = Obar Delta^T,  Dbar V^T,  Y = T^T Dbar
+// (chunk, value head, batch); every product has 64 rows as its M dimension
+// (M = 64 MMAs, accumulator row r in TMEM lane 32 (r / 16) + r % 16):
+//   phase 0:  Pbar = Obar Delta^T,  Dbar V^T,  Y = T^T Dbar,  K K^T,  Q K^T
 //   phase 1:  per 32-wide block of Dk:  Obar S^T,  Wbar = -Dbar S^T,  Delta Sbar'^T
-//   (Delta, a cancelling difference stored in fp32, enters as two bf16 terms)
-//   phase 1b: K K^T, Q K^T, Wbar K^T, Z = T^T Wbar
-//   phase 2:  Abar = -(T^T Tbar T^T) and the gate / log-decay cotangents on CUDA
-//             cores in fp32 (fp64 for the cancelling row-minus-column sums)
+//   phase 1b: Wbar K^T,  Z = T^T Wbar
+//   phase 2:  X = Tbar T^T,  Abar = -T^T X,  then the gate / log-decay cotangents
+//             element-wise in fp32 (fp64 for the cancelling row / column sums)
 //   phase 3:  (Pbar o M) K  and  (Pbar o M)^T Q + (Gb + Gb^T) K
-// q and k are staged as the exact bf16 inputs; the normalisations r_q, r_k
+// Delta (a cancelling difference, stored in fp32) enters as two bf16 terms
+// (hi + lo).  q and k are staged as the exact bf16 inputs; the norms r_q, r_k
 // (and 1/sqrt(Dk)) are applied in fp32 in the epilogues or folded into the
 // other operand, so the normalised rows are never rounded.
-// Operands are staged from global memory into the canonical no-swizzle
-// shared-memory layout (see gdn_tc.cuh); results leave TMEM through 32x32b
-// loads, eight warps splitting the columns.
 #include "gdn_internal.cuh"
 #include "gdn_tc.cuh"
 
@@ -32,11 +28,13 @@ namespace {
 constexpr int C = kChunk;
 constexpr int kThreads = 256;
 constexpr int kBlkK = 32;  // Dk block of the state products
+// TMEM column map
+constexpr uint32_t kColGkk = 384, kColGqk = 448;
 
 struct Smem {
     // byte offsets inside dynamic shared memory
-    uint32_t K, Q, W, R1, O, D, Dlo, NB, V, S, Sp, Tt, PMk, PMq, Hk, Pf, Tbf, Gkk, Gqk, Tf, Xf, vec,
-        total;
+    uint32_t K, Q, W, R1, O, D, Dlo, NB, V, S, Sp, Gkk, Gqk, Tbh, Xh, PMk, PMq, Hk, Tt, Pf, Tbf,
+        vec, total;
 };
 
 __host__ __device__ inline Smem smem_plan(int Dk, int Dv) {
@@ -47,38 +45,37 @@ __host__ __device__ inline Smem smem_plan(int Dk, int Dv) {
         o += (bytes + 1023u) & ~1023u;
         return r;
     };
-    const uint32_t tk = C * Dk * 2, tv = C * Dv * 2;
+    const uint32_t tk = C * Dk * 2, tv = C * Dv * 2, t64 = C * C * 2, f64x64 = C * C * 4;
     s.K = take(tk);
     s.Q = take(tk);
     s.W = take(tk);
-    // region R1: Dv-wide operands of phases 0-1, then fp32 scratch of phase 2 and
-    // the phase-3 operands
-    const uint32_t r1_ops = 6 * tv;
-    const uint32_t r1_late = 4 * C * C * 4 + 3 * C * C * 2;
+    // region R1: Dv-wide operands of phases 0-1, then phase-2/3 scratch
+    const uint32_t r1_ops = 5 * tv + 2 * (tv / 2);
+    const uint32_t r1_late = 2 * f64x64 + 5 * t64;
     s.R1 = take(r1_ops > r1_late ? r1_ops : r1_late);
     s.O = s.R1;
     s.D = s.O + tv;
     s.Dlo = s.D + tv;
     s.NB = s.Dlo + tv;
     s.V = s.NB + tv;
-    s.S = s.V + tv;              // kBlkK x Dv
+    s.S = s.V + tv;  // kBlkK x Dv
     s.Sp = s.S + tv / 2;
-    s.Gkk = s.R1;
-    s.Gqk = s.Gkk + C * C * 4;
-    s.Tf = s.Gqk + C * C * 4;
-    s.Xf = s.Tf + C * C * 4;
-    s.PMk = s.Xf + C * C * 4;
-    s.PMq = s.PMk + C * C * 2;
-    s.Hk = s.PMq + C * C * 2;
-    s.Tt = take(C * C * 2);
-    s.Pf = take(C * C * 4);
-    s.Tbf = take(C * C * 4);
-    s.vec = take(24 * C * 4 + 4 * C * 8 + 256);
+    s.Gkk = s.R1;            // fp32, later Mbar o M in place
+    s.Gqk = s.Gkk + f64x64;  // fp32, later Gb in place
+    s.Tbh = s.Gqk + f64x64;
+    s.Xh = s.Tbh + t64;
+    s.PMk = s.Xh + t64;
+    s.PMq = s.PMk + t64;
+    s.Hk = s.PMq + t64;
+    s.Tt = take(t64);
+    s.Pf = take(f64x64);
+    s.Tbf = take(f64x64);
+    s.vec = take(24 * C * 4 + 8 * C * 8 + 1024);
     s.total = o;
     return s;
 }
 
-__device__ __forceinline__ void st_bf16x8(uint8_t* dst, const float (&v)[8]) {
+__device__ __forceinline__ void st_bf16x8(uint8_t* dst, const float* v) {
     uint4 u;
     __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]);
     __nv_bfloat162 h1 = __floats2bfloat162_rn(v[2], v[3]);
@@ -90,9 +87,8 @@ __device__ __forceinline__ void st_bf16x8(uint8_t* dst, const float (&v)[8]) {
     u.w = *reinterpret_cast<uint32_t*>(&h3);
     *reinterpret_cast<uint4*>(dst) = u;
 }
-
-__device__ __forceinline__ void ld8(const __nv_bfloat16* p, float (&v)[8]) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
+__device__ __forceinline__ void ld_bf16x8(const uint8_t* src, float* v) {
+    const uint4 u = *reinterpret_cast<const uint4*>(src);
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -101,11 +97,40 @@ __device__ __forceinline__ void ld8(const __nv_bfloat16* p, float (&v)[8]) {
         v[2 * i + 1] = f.y;
     }
 }
-__device__ __forceinline__ void ld8(const float* p, float (&v)[8]) {
+__device__ __forceinline__ void ld8(const float* p, float* v) {
     const float4 a = *reinterpret_cast<const float4*>(p);
     const float4 b = *reinterpret_cast<const float4*>(p + 4);
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void st16f(float* dst, const float* v) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        reinterpret_cast<float4*>(dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+__device__ __forceinline__ void add16f(float* dst, const float* v) {
+    float4* p4 = reinterpret_cast<float4*>(dst);
+    float4 a[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = p4[i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        p4[i] = make_float4(a[i].x + v[4 * i], a[i].y + v[4 * i + 1], a[i].z + v[4 * i + 2],
+                            a[i].w + v[4 * i + 3]);
+}
+
+__device__ __forceinline__ uint32_t canon(int x, int y, int ncols) {
+    return (uint32_t)(x >> 3) * 128u + (uint32_t)(y >> 3) * (uint32_t)ncols * 16u +
+           (uint32_t)(y & 7) * 16u + (uint32_t)(x & 7) * 2u;
+}
+// 16 consecutive elements (x0 multiple of 8) of row y of a canonical bf16 tile
+__device__ __forceinline__ void tile_row16(const uint8_t* tile, int ncols, int x0, int y, float* v) {
+    ld_bf16x8(tile + canon(x0, y, ncols), v);
+    ld_bf16x8(tile + canon(x0 + 8, y, ncols), v + 8);
+}
+__device__ __forceinline__ void tile_put16(uint8_t* tile, int ncols, int x0, int y, const float* v) {
+    st_bf16x8(tile + canon(x0, y, ncols), v);
+    st_bf16x8(tile + canon(x0 + 8, y, ncols), v + 8);
 }
 
 // 64-row bf16 tile (x = column) fetched with 16-byte cp.async; rows >= nvalid zero
@@ -113,12 +138,11 @@ __device__ __forceinline__ void cpa_tile(uint8_t* tile, const __nv_bfloat16* src
                                          int ncols, int nvalid) {
     const int cpr = ncols / 8;
     const uint32_t base = tc::smem_u32(tile);
-    const uint32_t ys = (uint32_t)ncols * 16u;
     for (int e = threadIdx.x; e < C * cpr; e += blockDim.x) {
         const int row = e / cpr, cc = e % cpr;
         const bool in = row < nvalid;
-        tc::cp_async16(base + cc * 128u + (row >> 3) * ys + (row & 7) * 16u,
-                       src + (in ? row : 0) * ld + cc * 8, in ? 16u : 0u);
+        tc::cp_async16(base + canon(cc * 8, row, ncols), src + (in ? row : 0) * ld + cc * 8,
+                       in ? 16u : 0u);
     }
 }
 
@@ -130,7 +154,6 @@ __device__ __forceinline__ void stage_f32(uint8_t* hi, uint8_t* lo, const float*
     constexpr int U = 4;
     const int cpr = ncols / 8;
     const int total = C * cpr;
-    const uint32_t ys = (uint32_t)ncols * 16u;
     for (int base = threadIdx.x; base < total; base += U * blockDim.x) {
         float v[U][8];
 #pragma unroll
@@ -142,8 +165,7 @@ __device__ __forceinline__ void stage_f32(uint8_t* hi, uint8_t* lo, const float*
         for (int u = 0; u < U; ++u) {
             const int e = base + u * blockDim.x;
             if (e < total) {
-                const int row = e / cpr, cc = e % cpr;
-                const uint32_t o = cc * 128u + (row >> 3) * ys + (row & 7) * 16u;
+                const uint32_t o = canon((e % cpr) * 8, e / cpr, ncols);
                 float l[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -155,16 +177,6 @@ __device__ __forceinline__ void stage_f32(uint8_t* hi, uint8_t* lo, const float*
             }
         }
     }
-}
-
-// read one bf16 element of a canonical tile (x = column)
-__device__ __forceinline__ float tile_at(const uint8_t* tile, int ncols, int x, int y) {
-    const uint32_t off = (x >> 3) * 128u + (y >> 3) * (uint32_t)ncols * 16u + (y & 7) * 16u + (x & 7) * 2u;
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + off));
-}
-__device__ __forceinline__ void tile_put(uint8_t* tile, int ncols, int x, int y, float v) {
-    const uint32_t off = (x >> 3) * 128u + (y >> 3) * (uint32_t)ncols * 16u + (y & 7) * 16u + (x & 7) * 2u;
-    *reinterpret_cast<__nv_bfloat16*>(tile + off) = __float2bfloat16_rn(v);
 }
 
 __device__ __forceinline__ tc::Tile kmaj(uint8_t* smem, uint32_t off, int ncols) {
@@ -201,6 +213,11 @@ __device__ __forceinline__ void sync_after_mma(uint64_t* bar, uint32_t& phase, b
     phase ^= 1u;
     tc::tc_fence_after();
 }
+__device__ __forceinline__ void cta_sync_tc() {
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+}
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs p) {
     extern __shared__ __align__(1024) uint8_t sm[];
@@ -210,21 +227,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     const int j = h / (int)d.G;
     const int Dk = (int)d.Dk, Dv = (int)d.Dv;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = warp >> 2;  // column half walked by this warp in acc_rows
     const Smem L = smem_plan(Dk, Dv);
     float* vec = reinterpret_cast<float*>(sm + L.vec);
-    float* gm = vec;            // exp(Gamma)
-    float* ev = gm + C;         // exp(Gamma_63 - Gamma)
-    float* bt = ev + C;         // beta
-    float* rqv = bt + C;        // r_q / sqrt(Dk)
-    float* rkv = rqv + C;       // r_k
-    float* gq = rkv + C;        // [2][64] row-dot partials: gambar * gam
-    float* ee = gq + 2 * C;     // [2][64] ebar * e
-    float* bb0 = ee + 2 * C;    // [2][64] betabar (Y . V)
-    float* zk = bb0 + 2 * C;    // [2][64] Z . K
-    float* betab = zk + 2 * C;  // [64]
-    float* red = betab + C;     // [256]
+    float* gm = vec;             // exp(Gamma)
+    float* ev = gm + C;          // exp(Gamma_63 - Gamma)
+    float* bt = ev + C;          // beta
+    float* rqv = bt + C;         // r_q / sqrt(Dk)
+    float* rkv = rqv + C;        // r_k
+    float* gq = rkv + C;         // [2][64] row-dot partials: gambar * gam
+    float* ee = gq + 2 * C;      // [2][64] ebar * e
+    float* bb0 = ee + 2 * C;     // [2][64] betabar (Y . V)
+    float* zk = bb0 + 2 * C;     // [2][64] Z . K
+    float* sbp = zk + 2 * C;     // [2][64] sum_j Abar M Gkk
+    float* betab = sbp + 2 * C;  // [64]
+    float* red = betab + C;      // [256]
     double* Gm = reinterpret_cast<double*>(red + 256);  // [64]
-    double* red2 = Gm + C;                              // [64]
+    double* rsp = Gm + C;                               // [2][64] row sums of Mbar o M
+    double* csp = rsp + 2 * C;                          // [4][64] column sums
+    double* gam_bar = csp + 4 * C;                      // [64]
 
     const int64_t t0 = (int64_t)c * C;
     const int nvalid = (int)(d.T - t0 < C ? d.T - t0 : C);
@@ -235,9 +256,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(p.k);
     const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(p.v);
     const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(p.d_o);
-    const float* Delta = p.Delta;
     __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(p.dv);
+    const int64_t ldq = d.Hk * Dk, ldv = d.Hv * Dv;
 
+    // ---- operands: raw q, k, dO, v by cp.async; Delta (hi + lo), -Dbar, T as bf16
+    cpa_tile(sm + L.K, k + ((int64_t)bb * d.T + t0) * ldq + (int64_t)j * Dk, ldq, Dk, nvalid);
+    cpa_tile(sm + L.Q, q + ((int64_t)bb * d.T + t0) * ldq + (int64_t)j * Dk, ldq, Dk, nvalid);
+    cpa_tile(sm + L.O, dO + ((int64_t)bb * d.T + t0) * ldv + (int64_t)h * Dv, ldv, Dv, nvalid);
+    cpa_tile(sm + L.V, v + ((int64_t)bb * d.T + t0) * ldv + (int64_t)h * Dv, ldv, Dv, nvalid);
+    tc::cp_async_commit();
     if (warp == 0) {
         tc::tmem_alloc(&tmem_base_sh, 512);
         tc::tmem_relinquish();
@@ -246,35 +273,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
         tc::mbar_init(&bar, 1);
         tc::fence_mbar_init();
     }
-    for (int i = tid; i < C; i += blockDim.x) {
-        const double G = p.gam[gbase + i];
-        Gm[i] = G;
-        gm[i] = expf((float)G);
-        ev[i] = expf((float)(p.gam[gbase + C - 1] - G));
-        bt[i] = p.beta[gbase + i];
-        rqv[i] = p.rq[rbase + i] * rsqrtf((float)Dk);
-        rkv[i] = p.rk[rbase + i];
+    if (tid < C) {
+        const double G = p.gam[gbase + tid];
+        Gm[tid] = G;
+        gm[tid] = expf((float)G);
+        ev[tid] = expf((float)(p.gam[gbase + C - 1] - G));
+        bt[tid] = p.beta[gbase + tid];
+        rqv[tid] = p.rq[rbase + tid] * rsqrtf((float)Dk);
+        rkv[tid] = p.rk[rbase + tid];
     }
-    for (int i = tid; i < 8 * C; i += blockDim.x) gq[i] = 0.f;  // gq, ee, bb0, zk
-    __syncthreads();
-
-    // ---- stage the phase-0/1 operands
-    const int64_t ldq = d.Hk * Dk, ldv = d.Hv * Dv;
-    // q and k enter as the exact bf16 inputs; their normalisations are applied
-    // in fp32 to the other operand or in the epilogues
-    cpa_tile(sm + L.K, k + ((int64_t)bb * d.T + t0) * ldq + (int64_t)j * Dk, ldq, Dk, nvalid);
-    cpa_tile(sm + L.Q, q + ((int64_t)bb * d.T + t0) * ldq + (int64_t)j * Dk, ldq, Dk, nvalid);
-    cpa_tile(sm + L.O, dO + ((int64_t)bb * d.T + t0) * ldv + (int64_t)h * Dv, ldv, Dv, nvalid);
-    cpa_tile(sm + L.V, v + ((int64_t)bb * d.T + t0) * ldv + (int64_t)h * Dv, ldv, Dv, nvalid);
-    tc::cp_async_commit();
-    stage_f32(sm + L.D, sm + L.Dlo, Delta + gbase * Dv, Dv, Dv, 1.f);
+    for (int i = tid; i < 10 * C; i += blockDim.x) gq[i] = 0.f;  // gq, ee, bb0, zk, sbp
+    for (int i = tid; i < 2 * C; i += blockDim.x) rsp[i] = 0.0;
+    stage_f32(sm + L.D, sm + L.Dlo, p.Delta + gbase * Dv, Dv, Dv, 1.f);
     stage_f32(sm + L.NB, nullptr, p.Dbar + gbase * Dv, Dv, Dv, -1.f);
     stage_f32(sm + L.Tt, nullptr, p.Tinv + (((int64_t)bb * d.Hv + h) * d.NC + c) * C * C, C, C, 1.f);
     tc::cp_async_wait_all();
     tc::fence_async_smem();
-    tc::tc_fence_before();
-    __syncthreads();
-    tc::tc_fence_after();
+    cta_sync_tc();
     const uint32_t tb = tmem_base_sh;
     uint32_t phase = 0;
     bool ok = true;
@@ -284,47 +299,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     const tc::Tile tO = kmaj(sm, L.O, Dv), tD = kmaj(sm, L.D, Dv), tNB = kmaj(sm, L.NB, Dv);
     const tc::Tile tDlo = kmaj(sm, L.Dlo, Dv);
     const tc::Tile tV = kmaj(sm, L.V, Dv), tNBmn = mnmaj(sm, L.NB, Dv);
-    const tc::Tile tTmn = mnmaj(sm, L.Tt, C);
+    const tc::Tile tTt = kmaj(sm, L.Tt, C), tTmn = mnmaj(sm, L.Tt, C);
 
-    // ---- phase 0: Pbar = Obar Delta^T | -Dbar V^T | -T^T Dbar
+    // ---- phase 0: Pbar = Obar Delta^T | -Dbar V^T | -T^T Dbar | K K^T | Q K^T
     if (tid == 0) {
         tc::mma_tile(tb + 0, tO, tD, C, C, Dv, false);
         tc::mma_tile(tb + 0, tO, tDlo, C, C, Dv, true);
         tc::mma_tile(tb + 64, tNB, tV, C, C, Dv, false);
         tc::mma_tile(tb + 128, tTmn, tNBmn, C, Dv, C, false);
+        tc::mma_tile(tb + kColGkk, tK, tK, C, C, Dk, false);
+        tc::mma_tile(tb + kColGqk, tQ, tK, C, C, Dk, false);
         tc::mma_commit(&bar);
     }
-    sync_after_mma(&bar, phase, ok);
-    float* Pf = reinterpret_cast<float*>(sm + L.Pf);
-    float* Tbf = reinterpret_cast<float*>(sm + L.Tbf);
-    if (ok) {
-        acc_rows(tb, 0, C, [&](int r, int c0, const float (&x)[16]) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) Pf[r * C + c0 + i] = (c0 + i <= r) ? x[i] : 0.f;
-        });
-        acc_rows(tb, 64, C, [&](int r, int c0, const float (&x)[16]) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) Tbf[r * C + c0 + i] = -bt[c0 + i] * x[i];
-        });
-        acc_rows(tb, 128, Dv, [&](int r, int c0, const float (&x)[16]) {
-            const int g = warp >> 2;
-            float s = 0.f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) s = fmaf(-x[i], tile_at(sm + L.V, Dv, c0 + i, r), s);
-            bb0[g * C + r] += s;
-            if (r < nvalid) {
-                __nv_bfloat16* dst = dv + ((int64_t)bb * d.T + t0 + r) * ldv + (int64_t)h * Dv + c0;
-#pragma unroll
-                for (int i = 0; i < 16; i += 2)
-                    *reinterpret_cast<__nv_bfloat162*>(dst + i) =
-                        __floats2bfloat162_rn(-bt[r] * x[i], -bt[r] * x[i + 1]);
-            }
-        });
-    }
-
-    // ---- phase 1: state products per kBlkK-wide block of Dk.  The fp32 S and
-    // Sbar' rows of the next block are loaded into registers while the current
-    // block's MMAs run.
+    // the first block of S / Sbar' rows, into registers while phase 0 runs
     float gcb = 0.f;
     constexpr int kPer = (kBlkK * 256 / 8 + kThreads - 1) / kThreads;  // chunks per thread (Dv <= 256)
     float pre_s[kPer][8], pre_p[kPer][8];
@@ -341,10 +328,46 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
         }
     };
     load_blk(0, Dk < kBlkK ? Dk : kBlkK);
+    sync_after_mma(&bar, phase, ok);
+    float* Pf = reinterpret_cast<float*>(sm + L.Pf);
+    float* Tbf = reinterpret_cast<float*>(sm + L.Tbf);
+    if (ok) {
+        acc_rows(tb, 0, C, [&](int r, int c0, const float (&x)[16]) {
+            float m[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) m[i] = (c0 + i <= r) ? x[i] : 0.f;
+            st16f(Pf + r * C + c0, m);
+        });
+        acc_rows(tb, 64, C, [&](int r, int c0, const float (&x)[16]) {
+            float m[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) m[i] = -bt[c0 + i] * x[i];
+            st16f(Tbf + r * C + c0, m);
+        });
+        acc_rows(tb, 128, Dv, [&](int r, int c0, const float (&x)[16]) {
+            float vv[16], y[16];
+            tile_row16(sm + L.V, Dv, c0, r, vv);
+            float s = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                s = fmaf(-x[i], vv[i], s);
+                y[i] = -bt[r] * x[i];
+            }
+            bb0[g * C + r] += s;
+            if (r < nvalid) {
+                uint8_t* dst = reinterpret_cast<uint8_t*>(dv + ((int64_t)bb * d.T + t0 + r) * ldv +
+                                                          (int64_t)h * Dv + c0);
+                st_bf16x8(dst, y);
+                st_bf16x8(dst + 16, y + 8);
+            }
+        });
+    }
+
+    // ---- phase 1: state products per kBlkK-wide block of Dk; the next block's
+    // fp32 S / Sbar' rows load into registers while the current block's MMAs run
     for (int dk0 = 0; dk0 < Dk; dk0 += kBlkK) {
         const int nk = Dk - dk0 < kBlkK ? Dk - dk0 : kBlkK;
-        tc::tc_fence_before();
-        __syncthreads();  // previous block's TMEM reads and MMAs are done
+        cta_sync_tc();  // previous block's TMEM reads and MMAs are done
         {
             const uint32_t ys = (uint32_t)Dv * 16u;
 #pragma unroll
@@ -361,9 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
             }
         }
         tc::fence_async_smem();
-        tc::tc_fence_before();
-        __syncthreads();
-        tc::tc_fence_after();
+        cta_sync_tc();
         const tc::Tile tS = kmaj(sm, L.S, Dv), tSp = kmaj(sm, L.Sp, Dv);
         if (tid == 0) {
             tc::mma_tile(tb + 0, tO, tS, C, nk, Dv, false);
@@ -375,51 +396,46 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
         if (dk0 + kBlkK < Dk) load_blk(dk0 + kBlkK, Dk - dk0 - kBlkK < kBlkK ? Dk - dk0 - kBlkK : kBlkK);
         sync_after_mma(&bar, phase, ok);
         if (ok) {
-            const int g = warp >> 2;
             acc_rows(tb, 0, nk, [&](int r, int c0, const float (&x)[16]) {
-                float* dst = p.dqh + (gbase + r) * Dk + dk0 + c0;
+                float y[16], qq[16];
+                tile_row16(sm + L.Q, Dk, dk0 + c0, r, qq);
                 float s = 0.f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float y = gm[r] * x[i];
-                    dst[i] = y;
-                    s = fmaf(y, tile_at(sm + L.Q, Dk, dk0 + c0 + i, r), s);
+                    y[i] = gm[r] * x[i];
+                    s = fmaf(y[i], qq[i], s);
                 }
+                st16f(p.dqh + (gbase + r) * Dk + dk0 + c0, y);
                 gq[g * C + r] += s;
             });
             acc_rows(tb, 64, nk, [&](int r, int c0, const float (&x)[16]) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) tile_put(sm + L.W, Dk, dk0 + c0 + i, r, x[i]);
+                tile_put16(sm + L.W, Dk, dk0 + c0, r, x);
             });
             acc_rows(tb, 128, nk, [&](int r, int c0, const float (&x)[16]) {
-                float* dst = p.dkh + (gbase + r) * Dk + dk0 + c0;
+                float y[16], kk[16];
+                tile_row16(sm + L.K, Dk, dk0 + c0, r, kk);
                 float s = 0.f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float y = ev[r] * x[i];
-                    dst[i] = y;
-                    s = fmaf(y, tile_at(sm + L.K, Dk, dk0 + c0 + i, r), s);
+                    y[i] = ev[r] * x[i];
+                    s = fmaf(y[i], kk[i], s);
                 }
+                st16f(p.dkh + (gbase + r) * Dk + dk0 + c0, y);
                 ee[g * C + r] += s;
             });
         }
     }
-    // <Sbar', S> over the whole state: fixed-order block reduction
     red[tid] = gcb;
     tc::fence_async_smem();  // Wbar tile written by generic stores -> MMA operand
-    tc::tc_fence_before();
-    __syncthreads();
-    tc::tc_fence_after();
+    cta_sync_tc();
 
-    // ---- phase 1b: K K^T | Q K^T | Wbar K^T | Z = T^T Wbar
+    // ---- phase 1b: Wbar K^T | Z = T^T Wbar
     if (tid == 0) {
-        tc::mma_tile(tb + 0, tK, tK, C, C, Dk, false);
-        tc::mma_tile(tb + 64, tQ, tK, C, C, Dk, false);
-        tc::mma_tile(tb + 128, tW, tK, C, C, Dk, false);
-        tc::mma_tile(tb + 192, tTmn, tWmn, C, Dk, C, false);
+        tc::mma_tile(tb + 0, tW, tK, C, C, Dk, false);
+        tc::mma_tile(tb + 64, tTmn, tWmn, C, Dk, C, false);
         tc::mma_commit(&bar);
     }
-    for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+    for (int s = blockDim.x / 2; s > 0; s >>= 1) {  // <Sbar', S>, fixed-order tree
         if (tid < s) red[tid] += red[tid + s];
         __syncthreads();
     }
@@ -427,130 +443,170 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     sync_after_mma(&bar, phase, ok);
     float* Gkk = reinterpret_cast<float*>(sm + L.Gkk);
     float* Gqk = reinterpret_cast<float*>(sm + L.Gqk);
-    float* Tf = reinterpret_cast<float*>(sm + L.Tf);
-    float* Xf = reinterpret_cast<float*>(sm + L.Xf);
     if (ok) {
+        acc_rows(tb, kColGkk, C, [&](int r, int c0, const float (&x)[16]) {
+            float y[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) y[i] = rkv[r] * rkv[c0 + i] * x[i];
+            st16f(Gkk + r * C + c0, y);
+        });
+        acc_rows(tb, kColGqk, C, [&](int r, int c0, const float (&x)[16]) {
+            float y[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) y[i] = rqv[r] * rkv[c0 + i] * x[i];
+            st16f(Gqk + r * C + c0, y);
+        });
         acc_rows(tb, 0, C, [&](int r, int c0, const float (&x)[16]) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) Gkk[r * C + c0 + i] = rkv[r] * rkv[c0 + i] * x[i];
-        });
-        acc_rows(tb, 64, C, [&](int r, int c0, const float (&x)[16]) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) Gqk[r * C + c0 + i] = rqv[r] * rkv[c0 + i] * x[i];
-        });
-        acc_rows(tb, 128, C, [&](int r, int c0, const float (&x)[16]) {
 #pragma unroll
             for (int i = 0; i < 16; ++i)
                 Tbf[r * C + c0 + i] += bt[c0 + i] * gm[c0 + i] * rkv[c0 + i] * x[i];
         });
-        acc_rows(tb, 192, Dk, [&](int r, int c0, const float (&x)[16]) {
-            const int g = warp >> 2;
-            float* dst = p.dkh + (gbase + r) * Dk + c0;
+        acc_rows(tb, 64, Dk, [&](int r, int c0, const float (&x)[16]) {
+            float y[16], kk[16];
+            tile_row16(sm + L.K, Dk, c0, r, kk);
             const float sc = bt[r] * gm[r];
             float s = 0.f;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                dst[i] += sc * x[i];
-                s = fmaf(x[i], tile_at(sm + L.K, Dk, c0 + i, r), s);
+                y[i] = sc * x[i];
+                s = fmaf(x[i], kk[i], s);
             }
+            add16f(p.dkh + (gbase + r) * Dk + c0, y);
             zk[g * C + r] += s;
         });
     }
-    const float* Tg = p.Tinv + (((int64_t)bb * d.Hv + h) * d.NC + c) * C * C;
-    for (int i = tid; i < C * C / 4; i += blockDim.x)
-        reinterpret_cast<float4*>(Tf)[i] = reinterpret_cast<const float4*>(Tg)[i];
     __syncthreads();
     if (tid < C) {
         const int i = tid;
-        betab[i] = bb0[i] + bb0[C + i];
         const float z = rkv[i] * (zk[i] + zk[C + i]);  // <Z_i, k_hat_i>
-        betab[i] += gm[i] * z;
+        betab[i] = bb0[i] + bb0[C + i] + gm[i] * z;
         gq[i] = rqv[i] * (gq[i] + gq[C + i]) + bt[i] * z * gm[i];  // gambar * gam
         ee[i] = rkv[i] * (ee[i] + ee[C + i]);                      // ebar * e
     }
+    // Tbar as a bf16 operand (x = j, y = i)
+    for (int e = tid; e < C * (C / 8); e += blockDim.x) {
+        const int i = e / (C / 8), j0 = (e % (C / 8)) * 8;
+        st_bf16x8(sm + L.Tbh + canon(j0, i, C), Tbf + i * C + j0);
+    }
+    tc::fence_async_smem();
+    cta_sync_tc();
 
-    // ---- phase 2: Abar = -(T^T Tbar T^T), gate / log-decay cotangents
-    cta_gemm<4, 4>(C, C, C, Tbf, C, 1, Tf, 1, C, Xf, C, 1.f, 0.f, nullptr);
-    __syncthreads();
-    cta_gemm<4, 4>(C, C, C, Tf, 1, C, Xf, C, 1, Tbf, C, -1.f, 0.f, nullptr);
-    __syncthreads();
-    if (tid < C) {
-        const int i = tid;
-        float sb = 0.f;
-        for (int jj = 0; jj < C; ++jj) {
-            const int idx = i * C + jj;
-            const float m = jj <= i ? expf((float)(Gm[i] - Gm[jj])) : 0.f;
-            const float ab = jj < i ? Tbf[idx] : 0.f;
-            const float mb = ab * bt[i] * Gkk[idx] + Pf[idx] * Gqk[idx];
-            sb = fmaf(ab * m, Gkk[idx], sb);
-            Xf[idx] = mb * m;
-            Tbf[idx] = ab * bt[i] * m;
-            const float pm = Pf[idx] * m;
-            Pf[idx] = pm;
-            tile_put(sm + L.PMk, C, jj, i, pm * rkv[jj]);
-            tile_put(sm + L.PMq, C, jj, i, pm * rqv[i]);
-        }
-        betab[i] += sb;
-    }
-    __syncthreads();
-    for (int idx = tid; idx < C * C; idx += blockDim.x) {
-        const int i = idx / C, jj = idx % C;
-        tile_put(sm + L.Hk, C, jj, i, (Tbf[idx] + Tbf[jj * C + i]) * rkv[jj]);
-    }
-    if (tid < C) {
-        const int i = tid;
-        double rsum = 0.0, csum = 0.0;
-        for (int jj = 0; jj < C; ++jj) {
-            rsum += (double)Xf[i * C + jj];
-            csum += (double)Xf[jj * C + i];
-        }
-        red2[i] = rsum - csum + (double)gq[i] - (double)ee[i];
-    }
-    tc::fence_async_smem();  // PM / H tiles -> MMA operands
-    tc::tc_fence_before();
-    __syncthreads();
-    tc::tc_fence_after();
-
-    // ---- phase 3: dQ += (Pbar o M) K;  dK += (Pbar o M)^T Q + (Gb + Gb^T) K
-    const tc::Tile tPMk = kmaj(sm, L.PMk, C), tPMqmn = mnmaj(sm, L.PMq, C), tHk = kmaj(sm, L.Hk, C);
+    // ---- phase 2: X = Tbar T^T, then Abar' = T^T X (Abar = -Abar')
     if (tid == 0) {
-        tc::mma_tile(tb + 0, tPMk, tKmn, C, Dk, C, false);
-        tc::mma_tile(tb + Dk, tPMqmn, tQmn, C, Dk, C, false);
-        tc::mma_tile(tb + Dk, tHk, tKmn, C, Dk, C, true);
+        tc::mma_tile(tb + 0, kmaj(sm, L.Tbh, C), tTt, C, C, C, false);
         tc::mma_commit(&bar);
     }
+    sync_after_mma(&bar, phase, ok);
+    if (ok) {
+        acc_rows(tb, 0, C, [&](int r, int c0, const float (&x)[16]) {
+            tile_put16(sm + L.Xh, C, c0, r, x);  // X row-major (x = l, y = j)
+        });
+    }
+    tc::fence_async_smem();
+    cta_sync_tc();
     if (tid == 0) {
-        double se = 0.0;
-        for (int i = 0; i < C; ++i) se += (double)ee[i];
-        red2[C - 1] += (double)gCb * gm[C - 1] + se;
-        double run = 0.0;
-        for (int i = C - 1; i >= 0; --i) {
-            run += red2[i];
-            red2[i] = run;
-        }
+        tc::mma_tile(tb + 64, tTmn, mnmaj(sm, L.Xh, C), C, C, C, false);
+        tc::mma_commit(&bar);
+    }
+    sync_after_mma(&bar, phase, ok);
+    if (ok) {
+        // element-wise: M, Abar, Mbar o M (in place of Gkk), Gb (in place of Gqk),
+        // Pbar o M scaled by r_k (columns) and by r_q (rows) as bf16 operands
+        acc_rows(tb, 64, C, [&](int r, int c0, const float (&x)[16]) {
+            float sb = 0.f;
+            double rs = 0.0;
+            float pk[16], pq[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int jj = c0 + i;
+                const int idx = r * C + jj;
+                const float m = jj <= r ? expf((float)(Gm[r] - Gm[jj])) : 0.f;
+                const float ab = jj < r ? -x[i] : 0.f;
+                const float gk = Gkk[idx];
+                const float mb = ab * bt[r] * gk + Pf[idx] * Gqk[idx];
+                sb = fmaf(ab * m, gk, sb);
+                const float mm = mb * m;
+                Gkk[idx] = mm;
+                Gqk[idx] = ab * bt[r] * m;
+                rs += (double)mm;
+                const float pm = Pf[idx] * m;
+                pk[i] = pm * rkv[jj];
+                pq[i] = pm * rqv[r];
+            }
+            tile_put16(sm + L.PMk, C, c0, r, pk);
+            tile_put16(sm + L.PMq, C, c0, r, pq);
+            sbp[g * C + r] += sb;  // two 16-column chunks per thread
+            rsp[g * C + r] += rs;
+        });
     }
     __syncthreads();
+    // H = (Gb + Gb^T) diag(r_k) as a bf16 operand; column sums of Mbar o M (fp64)
+    for (int e = tid; e < C * (C / 8); e += blockDim.x) {
+        const int i = e / (C / 8), j0 = (e % (C / 8)) * 8;
+        float h8[8];
+#pragma unroll
+        for (int s = 0; s < 8; ++s) h8[s] = (Gqk[i * C + j0 + s] + Gqk[(j0 + s) * C + i]) * rkv[j0 + s];
+        st_bf16x8(sm + L.Hk + canon(j0, i, C), h8);
+    }
+    {
+        const int i = tid & (C - 1), qd = tid >> 6;
+        double cs = 0.0;
+#pragma unroll 4
+        for (int kk = 16 * qd; kk < 16 * qd + 16; ++kk) cs += (double)Gkk[kk * C + i];
+        csp[qd * C + i] = cs;
+    }
+    tc::fence_async_smem();
+    cta_sync_tc();
+
+    // ---- phase 3: dQ += (Pbar o M) K;  dK += (Pbar o M)^T Q + (Gb + Gb^T) K
+    if (tid == 0) {
+        tc::mma_tile(tb + 0, kmaj(sm, L.PMk, C), tKmn, C, Dk, C, false);
+        tc::mma_tile(tb + Dk, mnmaj(sm, L.PMq, C), tQmn, C, Dk, C, false);
+        tc::mma_tile(tb + Dk, kmaj(sm, L.Hk, C), tKmn, C, Dk, C, true);
+        tc::mma_commit(&bar);
+    }
+    // Gammabar_i = sum_j (Mbar o M)_ij - sum_k (Mbar o M)_ki + gambar_i gam_i - ebar_i e_i,
+    // plus the chunk-end terms at i = 63; the log-decay cotangent is its reverse
+    // cumulative sum (one warp, fp64, two steps per lane)
     if (tid < C) {
-        p.dl[gbase + tid] = (float)red2[tid];
-        p.dbeta[gbase + tid] = betab[tid];
+        const int i = tid;
+        betab[i] += sbp[i] + sbp[C + i];
+        gam_bar[i] = (rsp[i] + rsp[C + i]) - (csp[i] + csp[C + i] + csp[2 * C + i] + csp[3 * C + i]) +
+                     (double)gq[i] - (double)ee[i];
+    }
+    __syncthreads();
+    if (warp == 0) {
+        double se = (double)ee[2 * lane] + (double)ee[2 * lane + 1];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) se += __shfl_xor_sync(0xffffffffu, se, off);
+        double x0 = gam_bar[2 * lane], x1 = gam_bar[2 * lane + 1];
+        if (lane == 31) x1 += (double)gCb * gm[C - 1] + se;
+        // suffix sums: element i gets sum_{k >= i}
+        const double tot = x0 + x1;
+        double suf = tot;  // inclusive suffix over lanes >= lane
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const double y = __shfl_down_sync(0xffffffffu, suf, off);
+            if (lane + off < 32) suf += y;
+        }
+        const double after = suf - tot;  // lanes > lane
+        p.dl[gbase + 2 * lane + 1] = (float)(x1 + after);
+        p.dl[gbase + 2 * lane] = (float)(x0 + x1 + after);
+        p.dbeta[gbase + 2 * lane] = betab[2 * lane];
+        p.dbeta[gbase + 2 * lane + 1] = betab[2 * lane + 1];
     }
     sync_after_mma(&bar, phase, ok);
     if (ok) {
         acc_rows(tb, 0, Dk, [&](int r, int c0, const float (&x)[16]) {
-            float* dst = p.dqh + (gbase + r) * Dk + c0;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) dst[i] += x[i];
+            add16f(p.dqh + (gbase + r) * Dk + c0, x);
         });
         acc_rows(tb, Dk, Dk, [&](int r, int c0, const float (&x)[16]) {
-            float* dst = p.dkh + (gbase + r) * Dk + c0;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) dst[i] += x[i];
+            add16f(p.dkh + (gbase + r) * Dk + c0, x);
         });
     }
     tc::tc_fence_before();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tb, 512);
-    (void)lane;
 }
 
 }  // namespace
