@@ -11,7 +11,9 @@
 //   phase 1b: Wbar K^T,  Z = T^T Wbar
 //   phase 2:  X = Tbar T^T,  Abar = -T^T X,  then the gate / log-decay cotangents
 //             element-wise in fp32 (fp64 for the cancelling row / column sums)
-//   phase 3:  (Pbar o M) K  and  (Pbar o M)^T Q + (Gb + Gb^T) K
+//   phase 3:  (Pbar o M) K  and  diag(beta gam) Z + (Pbar o M)^T Q + (Gb + Gb^T) K,
+//             accumulated in TMEM and stored to second dq / dk buffers that the
+//             reduction adds (no read-modify-write of global memory)
 // Delta (a cancelling difference, stored in fp32) enters as two bf16 terms
 // (hi + lo).  q and k are staged as the exact bf16 inputs; the norms r_q, r_k
 // (and 1/sqrt(Dk)) are applied in fp32 in the epilogues or folded into the
@@ -30,6 +32,9 @@ constexpr int kThreads = 256;
 constexpr int kBlkK = 32;  // Dk block of the state products
 // TMEM column map
 constexpr uint32_t kColGkk = 384, kColGqk = 448;
+// fp32 64 x 64 scratch matrices are row-padded to 65 floats: epilogue lanes own
+// rows, and an unpadded 256-byte row stride puts every lane in one bank
+constexpr int LDM = C + 1;
 
 struct Smem {
     // byte offsets inside dynamic shared memory
@@ -45,7 +50,7 @@ __host__ __device__ inline Smem smem_plan(int Dk, int Dv) {
         o += (bytes + 1023u) & ~1023u;
         return r;
     };
-    const uint32_t tk = C * Dk * 2, tv = C * Dv * 2, t64 = C * C * 2, f64x64 = C * C * 4;
+    const uint32_t tk = C * Dk * 2, tv = C * Dv * 2, t64 = C * C * 2, f64x64 = C * LDM * 4;
     s.K = take(tk);
     s.Q = take(tk);
     s.W = take(tk);
@@ -70,7 +75,7 @@ __host__ __device__ inline Smem smem_plan(int Dk, int Dv) {
     s.Tt = take(t64);
     s.Pf = take(f64x64);
     s.Tbf = take(f64x64);
-    s.vec = take(24 * C * 4 + 8 * C * 8 + 1024);
+    s.vec = take(40 * C * 4 + 2 * C * 8 + 1024);
     s.total = o;
     return s;
 }
@@ -139,7 +144,8 @@ __device__ __forceinline__ void cpa_tile(uint8_t* tile, const __nv_bfloat16* src
     const int cpr = ncols / 8;
     const uint32_t base = tc::smem_u32(tile);
     for (int e = threadIdx.x; e < C * cpr; e += blockDim.x) {
-        const int row = e / cpr, cc = e % cpr;
+        int row, cc;
+        chunk_rc(e, cpr, row, cc);
         const bool in = row < nvalid;
         tc::cp_async16(base + canon(cc * 8, row, ncols), src + (in ? row : 0) * ld + cc * 8,
                        in ? 16u : 0u);
@@ -159,13 +165,19 @@ __device__ __forceinline__ void stage_f32(uint8_t* hi, uint8_t* lo, const float*
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int e = base + u * blockDim.x;
-            if (e < total) ld8(src + (e / cpr) * ld + (e % cpr) * 8, v[u]);
+            if (e < total) {
+                int row, cc;
+                chunk_rc(e, cpr, row, cc);
+                ld8(src + row * ld + cc * 8, v[u]);
+            }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int e = base + u * blockDim.x;
             if (e < total) {
-                const uint32_t o = canon((e % cpr) * 8, e / cpr, ncols);
+                int row, cc;
+                chunk_rc(e, cpr, row, cc);
+                const uint32_t o = canon(cc * 8, row, ncols);
                 float l[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -242,10 +254,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     float* sbp = zk + 2 * C;     // [2][64] sum_j Abar M Gkk
     float* betab = sbp + 2 * C;  // [64]
     float* red = betab + C;      // [256]
-    double* Gm = reinterpret_cast<double*>(red + 256);  // [64]
-    double* rsp = Gm + C;                               // [2][64] row sums of Mbar o M
-    double* csp = rsp + 2 * C;                          // [4][64] column sums
-    double* gam_bar = csp + 4 * C;                      // [64]
+    // Gamma as an unevaluated sum hi + lo of two floats: for steps i, j whose
+    // Gamma are within a factor of two (the only case where exp(Gamma_i - Gamma_j)
+    // is not negligible), (hi_i - hi_j) is exact and the difference keeps fp64
+    // accuracy without fp64 arithmetic
+    float* Ghi = red + 256;     // [64]
+    float* Glo = Ghi + C;       // [64]
+    float* rsp = Glo + C;       // [2][64] row sums of Mbar o M (compensated)
+    float* rsc = rsp + 2 * C;   // [2][64] their compensation terms
+    float* csp = rsc + 2 * C;   // [4][64] column sums (compensated, folded)
+    double* gam_bar = reinterpret_cast<double*>(csp + 4 * C);  // [64]
 
     const int64_t t0 = (int64_t)c * C;
     const int nvalid = (int)(d.T - t0 < C ? d.T - t0 : C);
@@ -259,6 +277,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(p.dv);
     const int64_t ldq = d.Hk * Dk, ldv = d.Hv * Dv;
 
+    // S / Sbar' rows of a Dk block, loaded into registers ahead of use
+    float gcb = 0.f;
+    constexpr int kPer = (kBlkK * 256 / 8 + kThreads - 1) / kThreads;  // chunks per thread (Dv <= 256)
+    float pre_s[kPer][8], pre_p[kPer][8];
+    const int cpr_s = Dv / 8;
+    auto load_blk = [&](int dk0, int nk) {
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int e = tid + u * kThreads;
+            if (e < nk * cpr_s) {
+                int row, cc;
+                chunk_rc(e, cpr_s, row, cc);
+                const int64_t off = cbase + (int64_t)(dk0 + row) * Dv + cc * 8;
+                ld8(p.ckpt + off, pre_s[u]);
+                ld8(p.dSck + off, pre_p[u]);
+            }
+        }
+    };
     // ---- operands: raw q, k, dO, v by cp.async; Delta (hi + lo), -Dbar, T as bf16
     cpa_tile(sm + L.K, k + ((int64_t)bb * d.T + t0) * ldq + (int64_t)j * Dk, ldq, Dk, nvalid);
     cpa_tile(sm + L.Q, q + ((int64_t)bb * d.T + t0) * ldq + (int64_t)j * Dk, ldq, Dk, nvalid);
@@ -275,7 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     }
     if (tid < C) {
         const double G = p.gam[gbase + tid];
-        Gm[tid] = G;
+        const float ghi = (float)G;
+        Ghi[tid] = ghi;
+        Glo[tid] = (float)(G - (double)ghi);
         gm[tid] = expf((float)G);
         ev[tid] = expf((float)(p.gam[gbase + C - 1] - G));
         bt[tid] = p.beta[gbase + tid];
@@ -283,7 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
         rkv[tid] = p.rk[rbase + tid];
     }
     for (int i = tid; i < 10 * C; i += blockDim.x) gq[i] = 0.f;  // gq, ee, bb0, zk, sbp
-    for (int i = tid; i < 2 * C; i += blockDim.x) rsp[i] = 0.0;
+    for (int i = tid; i < 4 * C; i += blockDim.x) rsp[i] = 0.f;  // rsp, rsc
+    load_blk(0, Dk < kBlkK ? Dk : kBlkK);
     stage_f32(sm + L.D, sm + L.Dlo, p.Delta + gbase * Dv, Dv, Dv, 1.f);
     stage_f32(sm + L.NB, nullptr, p.Dbar + gbase * Dv, Dv, Dv, -1.f);
     stage_f32(sm + L.Tt, nullptr, p.Tinv + (((int64_t)bb * d.Hv + h) * d.NC + c) * C * C, C, C, 1.f);
@@ -311,23 +350,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
         tc::mma_tile(tb + kColGqk, tQ, tK, C, C, Dk, false);
         tc::mma_commit(&bar);
     }
-    // the first block of S / Sbar' rows, into registers while phase 0 runs
-    float gcb = 0.f;
-    constexpr int kPer = (kBlkK * 256 / 8 + kThreads - 1) / kThreads;  // chunks per thread (Dv <= 256)
-    float pre_s[kPer][8], pre_p[kPer][8];
-    const int cpr_s = Dv / 8;
-    auto load_blk = [&](int dk0, int nk) {
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int e = tid + u * kThreads;
-            if (e < nk * cpr_s) {
-                const int64_t off = cbase + (int64_t)(dk0 + e / cpr_s) * Dv + (e % cpr_s) * 8;
-                ld8(p.ckpt + off, pre_s[u]);
-                ld8(p.dSck + off, pre_p[u]);
-            }
-        }
-    };
-    load_blk(0, Dk < kBlkK ? Dk : kBlkK);
     sync_after_mma(&bar, phase, ok);
     float* Pf = reinterpret_cast<float*>(sm + L.Pf);
     float* Tbf = reinterpret_cast<float*>(sm + L.Tbf);
@@ -336,13 +358,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
             float m[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) m[i] = (c0 + i <= r) ? x[i] : 0.f;
-            st16f(Pf + r * C + c0, m);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Pf[r * LDM + c0 + i] = m[i];
         });
         acc_rows(tb, 64, C, [&](int r, int c0, const float (&x)[16]) {
             float m[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) m[i] = -bt[c0 + i] * x[i];
-            st16f(Tbf + r * C + c0, m);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Tbf[r * LDM + c0 + i] = m[i];
         });
         acc_rows(tb, 128, Dv, [&](int r, int c0, const float (&x)[16]) {
             float vv[16], y[16];
@@ -374,7 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
             for (int u = 0; u < kPer; ++u) {
                 const int e = tid + u * kThreads;
                 if (e < nk * cpr_s) {
-                    const int row = e / cpr_s, cc = e % cpr_s;
+                    int row, cc;
+                    chunk_rc(e, cpr_s, row, cc);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) gcb = fmaf(pre_s[u][i], pre_p[u][i], gcb);
                     const uint32_t o = cc * 128u + (row >> 3) * ys + (row & 7) * 16u;
@@ -448,32 +473,47 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
             float y[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) y[i] = rkv[r] * rkv[c0 + i] * x[i];
-            st16f(Gkk + r * C + c0, y);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Gkk[r * LDM + c0 + i] = y[i];
         });
         acc_rows(tb, kColGqk, C, [&](int r, int c0, const float (&x)[16]) {
             float y[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) y[i] = rqv[r] * rkv[c0 + i] * x[i];
-            st16f(Gqk + r * C + c0, y);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Gqk[r * LDM + c0 + i] = y[i];
         });
         acc_rows(tb, 0, C, [&](int r, int c0, const float (&x)[16]) {
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-                Tbf[r * C + c0 + i] += bt[c0 + i] * gm[c0 + i] * rkv[c0 + i] * x[i];
+                Tbf[r * LDM + c0 + i] += bt[c0 + i] * gm[c0 + i] * rkv[c0 + i] * x[i];
         });
-        acc_rows(tb, 64, Dk, [&](int r, int c0, const float (&x)[16]) {
-            float y[16], kk[16];
-            tile_row16(sm + L.K, Dk, c0, r, kk);
-            const float sc = bt[r] * gm[r];
-            float s = 0.f;
+        // Z stays in TMEM, rescaled in place to diag(beta gam) Z: the phase-3
+        // products for dK accumulate on top of it
+        {
+            const int sp = warp & 3, half = Dk / 2;
+            const int r = 16 * sp + lane;
+            for (int c0 = g * half; c0 < (g + 1) * half; c0 += 16) {
+                float x[16];
+                const uint32_t ta = tc::tmem_addr(tb, 32 * sp, 64 + c0);
+                tc::tmem_ld16(ta, x);
+                tc::tmem_wait_ld();
+                if (lane < 16) {
+                    float kk[16];
+                    tile_row16(sm + L.K, Dk, c0, r, kk);
+                    const float sc = bt[r] * gm[r];
+                    float s = 0.f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                y[i] = sc * x[i];
-                s = fmaf(x[i], kk[i], s);
+                    for (int i = 0; i < 16; ++i) {
+                        s = fmaf(x[i], kk[i], s);
+                        x[i] *= sc;
+                    }
+                    zk[g * C + r] += s;
+                }
+                tc::tmem_st16(ta, x);
             }
-            add16f(p.dkh + (gbase + r) * Dk + c0, y);
-            zk[g * C + r] += s;
-        });
+            tc::tmem_wait_st();
+        }
     }
     __syncthreads();
     if (tid < C) {
@@ -486,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     // Tbar as a bf16 operand (x = j, y = i)
     for (int e = tid; e < C * (C / 8); e += blockDim.x) {
         const int i = e / (C / 8), j0 = (e % (C / 8)) * 8;
-        st_bf16x8(sm + L.Tbh + canon(j0, i, C), Tbf + i * C + j0);
+        st_bf16x8(sm + L.Tbh + canon(j0, i, C), Tbf + i * LDM + j0);
     }
     tc::fence_async_smem();
     cta_sync_tc();
@@ -504,23 +544,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     }
     tc::fence_async_smem();
     cta_sync_tc();
-    if (tid == 0) {
-        tc::mma_tile(tb + 64, tTmn, mnmaj(sm, L.Xh, C), C, C, C, false);
+    if (tid == 0) {  // columns 0..63 again: X has been read; 64.. hold diag(beta gam) Z
+        tc::mma_tile(tb + 0, tTmn, mnmaj(sm, L.Xh, C), C, C, C, false);
         tc::mma_commit(&bar);
     }
     sync_after_mma(&bar, phase, ok);
     if (ok) {
         // element-wise: M, Abar, Mbar o M (in place of Gkk), Gb (in place of Gqk),
         // Pbar o M scaled by r_k (columns) and by r_q (rows) as bf16 operands
-        acc_rows(tb, 64, C, [&](int r, int c0, const float (&x)[16]) {
+        acc_rows(tb, 0, C, [&](int r, int c0, const float (&x)[16]) {
             float sb = 0.f;
-            double rs = 0.0;
+            float rs = rsp[g * C + r], rc = rsc[g * C + r];  // Kahan-compensated row sum
             float pk[16], pq[16];
+            const float ghr = Ghi[r], glr = Glo[r];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int jj = c0 + i;
-                const int idx = r * C + jj;
-                const float m = jj <= r ? expf((float)(Gm[r] - Gm[jj])) : 0.f;
+                const int idx = r * LDM + jj;
+                const float m = jj <= r ? expf((ghr - Ghi[jj]) + (glr - Glo[jj])) : 0.f;
                 const float ab = jj < r ? -x[i] : 0.f;
                 const float gk = Gkk[idx];
                 const float mb = ab * bt[r] * gk + Pf[idx] * Gqk[idx];
@@ -528,7 +569,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
                 const float mm = mb * m;
                 Gkk[idx] = mm;
                 Gqk[idx] = ab * bt[r] * m;
-                rs += (double)mm;
+                const float yk = mm - rc;
+                const float tk = rs + yk;
+                rc = (tk - rs) - yk;
+                rs = tk;
                 const float pm = Pf[idx] * m;
                 pk[i] = pm * rkv[jj];
                 pq[i] = pm * rqv[r];
@@ -536,7 +580,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
             tile_put16(sm + L.PMk, C, c0, r, pk);
             tile_put16(sm + L.PMq, C, c0, r, pq);
             sbp[g * C + r] += sb;  // two 16-column chunks per thread
-            rsp[g * C + r] += rs;
+            rsp[g * C + r] = rs;
+            rsc[g * C + r] = rc;
         });
     }
     __syncthreads();
@@ -545,24 +590,29 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
         const int i = e / (C / 8), j0 = (e % (C / 8)) * 8;
         float h8[8];
 #pragma unroll
-        for (int s = 0; s < 8; ++s) h8[s] = (Gqk[i * C + j0 + s] + Gqk[(j0 + s) * C + i]) * rkv[j0 + s];
+        for (int s = 0; s < 8; ++s) h8[s] = (Gqk[i * LDM + j0 + s] + Gqk[(j0 + s) * LDM + i]) * rkv[j0 + s];
         st_bf16x8(sm + L.Hk + canon(j0, i, C), h8);
     }
     {
         const int i = tid & (C - 1), qd = tid >> 6;
-        double cs = 0.0;
+        float cs = 0.f, cc = 0.f;  // Kahan-compensated column sum
 #pragma unroll 4
-        for (int kk = 16 * qd; kk < 16 * qd + 16; ++kk) cs += (double)Gkk[kk * C + i];
-        csp[qd * C + i] = cs;
+        for (int kk = 16 * qd; kk < 16 * qd + 16; ++kk) {
+            const float yk = Gkk[kk * LDM + i] - cc;
+            const float tk = cs + yk;
+            cc = (tk - cs) - yk;
+            cs = tk;
+        }
+        csp[qd * C + i] = cs - cc;
     }
     tc::fence_async_smem();
     cta_sync_tc();
 
     // ---- phase 3: dQ += (Pbar o M) K;  dK += (Pbar o M)^T Q + (Gb + Gb^T) K
     if (tid == 0) {
-        tc::mma_tile(tb + 0, kmaj(sm, L.PMk, C), tKmn, C, Dk, C, false);
-        tc::mma_tile(tb + Dk, mnmaj(sm, L.PMq, C), tQmn, C, Dk, C, false);
-        tc::mma_tile(tb + Dk, kmaj(sm, L.Hk, C), tKmn, C, Dk, C, true);
+        tc::mma_tile(tb + 64 + Dk, kmaj(sm, L.PMk, C), tKmn, C, Dk, C, false);
+        tc::mma_tile(tb + 64, mnmaj(sm, L.PMq, C), tQmn, C, Dk, C, true);
+        tc::mma_tile(tb + 64, kmaj(sm, L.Hk, C), tKmn, C, Dk, C, true);
         tc::mma_commit(&bar);
     }
     // Gammabar_i = sum_j (Mbar o M)_ij - sum_k (Mbar o M)_ki + gambar_i gam_i - ebar_i e_i,
@@ -571,8 +621,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     if (tid < C) {
         const int i = tid;
         betab[i] += sbp[i] + sbp[C + i];
-        gam_bar[i] = (rsp[i] + rsp[C + i]) - (csp[i] + csp[C + i] + csp[2 * C + i] + csp[3 * C + i]) +
-                     (double)gq[i] - (double)ee[i];
+        const double rows = ((double)rsp[i] - (double)rsc[i]) + ((double)rsp[C + i] - (double)rsc[C + i]);
+        const double cols = (double)csp[i] + (double)csp[C + i] + (double)csp[2 * C + i] + (double)csp[3 * C + i];
+        gam_bar[i] = rows - cols + (double)gq[i] - (double)ee[i];
     }
     __syncthreads();
     if (warp == 0) {
@@ -597,11 +648,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     }
     sync_after_mma(&bar, phase, ok);
     if (ok) {
-        acc_rows(tb, 0, Dk, [&](int r, int c0, const float (&x)[16]) {
-            add16f(p.dqh + (gbase + r) * Dk + c0, x);
+        acc_rows(tb, 64 + Dk, Dk, [&](int r, int c0, const float (&x)[16]) {
+            st16f(p.dqh2 + (gbase + r) * Dk + c0, x);
         });
-        acc_rows(tb, Dk, Dk, [&](int r, int c0, const float (&x)[16]) {
-            add16f(p.dkh + (gbase + r) * Dk + c0, x);
+        acc_rows(tb, 64, Dk, [&](int r, int c0, const float (&x)[16]) {
+            st16f(p.dkh2 + (gbase + r) * Dk + c0, x);
         });
     }
     tc::tc_fence_before();
@@ -613,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
 
 bool bwd_chunk_tc_supported(const Dims& d) {
     if (d.dtype != 1) return false;
-    if (d.Dk % 32 || d.Dv % 32 || d.Dk > 256 || d.Dv > 256) return false;
+    if (d.Dk % 32 || d.Dv % 32 || d.Dk > 224 || d.Dv > 256) return false;  // TMEM: 2 Dk + 64 <= 512
     return smem_plan((int)d.Dk, (int)d.Dv).total + 2048 <= 227u * 1024u;
 }
 

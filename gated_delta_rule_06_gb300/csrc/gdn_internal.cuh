@@ -54,6 +54,9 @@ struct Ptrs {
     float* Dbar;   // [B, Hv, Tp, Dv] cotangent of Delta
     float* dqh;    // [B, Hv, Tp, Dk] cotangent of the normalised q, per value head
     float* dkh;    // [B, Hv, Tp, Dk]
+    float* dqh2;   // [B, Hv, Tp, Dk] second part of dqh (tensor-core path), summed by bwd_reduce
+    float* dkh2;   // [B, Hv, Tp, Dk]
+    int dq_parts;  // 1: dqh / dkh hold the full cotangents; 2: add dqh2 / dkh2
     float* dl;     // [B, Hv, Tp] cotangent of the log-decay
     float* dbeta;  // [B, Hv, Tp]
     float* part;   // [2, B, NC, Hv] per-chunk partial sums for dA_log, ddt_bias
@@ -130,6 +133,15 @@ cudaError_t launch_fwd_chunk_tc(const Dims& d, const Ptrs& p, cudaStream_t s);
 unsigned int read_clear_error_fwdtc();
 // adds n to the library's launch counter (called by every launcher)
 void count_launches(int n);
+// chunk index e of a 64-row (or 8k-row) canonical-tile copy -> (row, 8-column
+// group) with row % 8 fastest: eight consecutive chunks fill one 128-byte core
+// matrix (conflict-free shared-memory stores) and a warp covers 8 rows x 4
+// column groups (whole 32-byte sectors of the global rows)
+__device__ __forceinline__ void chunk_rc(int e, int cpr, int& row, int& cc) {
+    const int t = e >> 3;
+    cc = t % cpr;
+    row = (t / cpr) * 8 + (e & 7);
+}
 // reads and clears the device error words of every translation unit
 // (~0u if a read failed); defined in gdn_api.cu
 unsigned int read_clear_error_all();

@@ -63,7 +63,8 @@ __device__ __forceinline__ void cpa_tile(uint8_t* tile, const __nv_bfloat16* src
     const int cpr = ncols / 8;
     const uint32_t base = tc::smem_u32(tile);
     for (int e = threadIdx.x; e < C * cpr; e += blockDim.x) {
-        const int row = e / cpr, cc = e % cpr;
+        int row, cc;
+        chunk_rc(e, cpr, row, cc);
         const bool in = row < nvalid;
         tc::cp_async16(base + canon(cc * 8, row, ncols), src + (in ? row : 0) * ld + cc * 8,
                        in ? 16u : 0u);
