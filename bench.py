@@ -463,12 +463,21 @@ def run_ours(args, w, world, rank, local):
 
 
 def measured_traffic(workload, kernel):
-    """DRAM bytes per launch from a committed ncu capture, if one matches."""
+    """DRAM bytes per launch from a committed ncu capture of this workload, or
+    None when there is none or the kernel's sources changed since it was taken."""
+    import hashlib
+
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            t = json.load(f)
-        return t.get(workload, {}).get(kernel)
+            ent = json.load(f).get(workload, {}).get(kernel)
+        if not ent:
+            return None
+        h = hashlib.sha256()
+        for src in ent["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        return ent["bytes"] if h.hexdigest()[:16] == ent["source_sha256_16"] else None
     except Exception:
         return None
 
