@@ -77,8 +77,11 @@ gdn_status validate_shape(const gdn_shape* s, gdn::Dims* d) {
 
 Layout make_layout(const gdn::Dims& d) {
     const size_t es = d.dtype == GDN_DTYPE_BF16 ? 2 : 4;
+    // the tensor-core path keeps checkpoints, T, the state cotangents and Dbar
+    // as bf16 operand images (half the fp32 size)
+    const size_t img = gdn::tc_path(d) ? 2 : 4;
     const size_t BH = (size_t)d.B * d.Hv;
-    const size_t state_ck = BH * d.NC * d.Dk * d.Dv * sizeof(float);
+    const size_t state_ck = BH * d.NC * d.Dk * d.Dv * img;
     const size_t perstep = BH * d.Tp;
     Layout L{};
     size_t o = 0;
@@ -87,7 +90,7 @@ Layout make_layout(const gdn::Dims& d) {
     L.beta = o; o = align_up(o + perstep * 4);
     L.rq = o; o = align_up(o + (size_t)d.B * d.Hk * d.Tp * 4);
     L.rk = o; o = align_up(o + (size_t)d.B * d.Hk * d.Tp * 4);
-    L.Tinv = o; o = align_up(o + BH * d.NC * gdn::kChunk * gdn::kChunk * 4);
+    L.Tinv = o; o = align_up(o + BH * d.NC * gdn::kChunk * gdn::kChunk * img);
     L.W = o; o = align_up(o + perstep * d.Dk * es);
     L.P = o; o = align_up(o + BH * d.NC * gdn::kChunk * gdn::kChunk * es);
     L.Delta = o; o = align_up(o + perstep * d.Dv * 4);
@@ -97,7 +100,7 @@ Layout make_layout(const gdn::Dims& d) {
     L.fwd_total = o;
     o = 0;
     L.dSck = o; o = align_up(o + state_ck);
-    L.Dbar = o; o = align_up(o + perstep * d.Dv * 4);
+    L.Dbar = o; o = align_up(o + perstep * d.Dv * img);
     L.dqh = o; o = align_up(o + perstep * d.Dk * 4);
     L.dkh = o; o = align_up(o + perstep * d.Dk * 4);
     L.dqh2 = o; o = align_up(o + perstep * d.Dk * 4);
@@ -132,6 +135,10 @@ gdn_status cuda_status(cudaError_t e) {
 }  // namespace
 
 namespace gdn {
+bool tc_path(const Dims& d) {
+    return d.dtype == GDN_DTYPE_BF16 && fwd_chunk_tc_supported(d) && scan_tc_supported(d) &&
+           bwd_chunk_tc_supported(d);
+}
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n); }
 unsigned int read_clear_error_all() {
     const unsigned int words[] = {read_clear_error_selftest(), read_clear_error_bwdtc(),
@@ -256,7 +263,7 @@ gdn_status gdn_backward(const gdn_shape* shape, const void* q, const void* k, co
     p.dkh = reinterpret_cast<float*>(w + L.dkh);
     p.dqh2 = reinterpret_cast<float*>(w + L.dqh2);
     p.dkh2 = reinterpret_cast<float*>(w + L.dkh2);
-    p.dq_parts = gdn::bwd_chunk_tc_supported(d) ? 2 : 1;
+    p.dq_parts = gdn::tc_path(d) ? 2 : 1;
     p.dl = reinterpret_cast<float*>(w + L.dl);
     p.dbeta = reinterpret_cast<float*>(w + L.dbeta);
     p.part = reinterpret_cast<float*>(w + L.part);

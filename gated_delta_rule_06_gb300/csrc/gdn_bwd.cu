@@ -563,7 +563,7 @@ cudaError_t launch_reduce_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_bwd_scan(const Dims& d, const Ptrs& p, cudaStream_t s) {
-    if (scan_tc_supported(d)) return launch_bwd_scan_tc(d, p, s);
+    if (tc_path(d)) return launch_bwd_scan_tc(d, p, s);
     if (d.Dv % 32 == 0)
         return d.dtype == 1 ? launch_bscan_t<__nv_bfloat16, 32>(d, p, s) : launch_bscan_t<float, 32>(d, p, s);
     if (d.Dv % 16 == 0)
@@ -572,7 +572,7 @@ cudaError_t launch_bwd_scan(const Dims& d, const Ptrs& p, cudaStream_t s) {
 }
 
 cudaError_t launch_bwd_chunk(const Dims& d, const Ptrs& p, cudaStream_t s) {
-    if (bwd_chunk_tc_supported(d)) return launch_bwd_chunk_tc(d, p, s);
+    if (tc_path(d)) return launch_bwd_chunk_tc(d, p, s);
     return d.dtype == 1 ? launch_bchunk_t<__nv_bfloat16>(d, p, s) : launch_bchunk_t<float>(d, p, s);
 }
 

@@ -14,10 +14,14 @@
 //   phase 3:  (Pbar o M) K  and  diag(beta gam) Z + (Pbar o M)^T Q + (Gb + Gb^T) K,
 //             accumulated in TMEM and stored to second dq / dk buffers that the
 //             reduction adds (no read-modify-write of global memory)
-// Delta (a cancelling difference, stored in fp32) enters as two bf16 terms
-// (hi + lo).  q and k are staged as the exact bf16 inputs; the norms r_q, r_k
-// (and 1/sqrt(Dk)) are applied in fp32 in the epilogues or folded into the
-// other operand, so the normalised rows are never rounded.
+// Delta (a cancelling difference) enters as two bf16 terms (hi + lo).  q and k
+// are staged as the exact bf16 inputs; the norms r_q, r_k (and 1/sqrt(Dk)) are
+// applied in fp32 in the epilogues or folded into the other operand, so the
+// normalised rows are never rounded.  The saved intermediates (Delta hi / lo,
+// -Dbar, T, the state checkpoints S and the chunk-end cotangents Sbar') are
+// bf16 operand images written by the earlier kernels; each arrives with one
+// bulk copy, and the 32-wide Dk blocks of S / Sbar' are double-buffered so the
+// next block streams in while the current block's products run.
 #include "gdn_internal.cuh"
 #include "gdn_tc.cuh"
 
@@ -102,28 +106,11 @@ __device__ __forceinline__ void ld_bf16x8(const uint8_t* src, float* v) {
         v[2 * i + 1] = f.y;
     }
 }
-__device__ __forceinline__ void ld8(const float* p, float* v) {
-    const float4 a = *reinterpret_cast<const float4*>(p);
-    const float4 b = *reinterpret_cast<const float4*>(p + 4);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
 __device__ __forceinline__ void st16f(float* dst, const float* v) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         reinterpret_cast<float4*>(dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
-__device__ __forceinline__ void add16f(float* dst, const float* v) {
-    float4* p4 = reinterpret_cast<float4*>(dst);
-    float4 a[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) a[i] = p4[i];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        p4[i] = make_float4(a[i].x + v[4 * i], a[i].y + v[4 * i + 1], a[i].z + v[4 * i + 2],
-                            a[i].w + v[4 * i + 3]);
-}
-
 __device__ __forceinline__ uint32_t canon(int x, int y, int ncols) {
     return (uint32_t)(x >> 3) * 128u + (uint32_t)(y >> 3) * (uint32_t)ncols * 16u +
            (uint32_t)(y & 7) * 16u + (uint32_t)(x & 7) * 2u;
@@ -149,45 +136,6 @@ __device__ __forceinline__ void cpa_tile(uint8_t* tile, const __nv_bfloat16* src
         const bool in = row < nvalid;
         tc::cp_async16(base + canon(cc * 8, row, ncols), src + (in ? row : 0) * ld + cc * 8,
                        in ? 16u : 0u);
-    }
-}
-
-// Stage 64 rows x ncols of an fp32 matrix as bf16 tiles (x = column).  With lo
-// != nullptr the value is split into hi + lo (lo = v - bf16(v)).  Loads are
-// issued four 8-element chunks deep per thread before any is stored.
-__device__ __forceinline__ void stage_f32(uint8_t* hi, uint8_t* lo, const float* src, int64_t ld,
-                                          int ncols, float sign) {
-    constexpr int U = 4;
-    const int cpr = ncols / 8;
-    const int total = C * cpr;
-    for (int base = threadIdx.x; base < total; base += U * blockDim.x) {
-        float v[U][8];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int e = base + u * blockDim.x;
-            if (e < total) {
-                int row, cc;
-                chunk_rc(e, cpr, row, cc);
-                ld8(src + row * ld + cc * 8, v[u]);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int e = base + u * blockDim.x;
-            if (e < total) {
-                int row, cc;
-                chunk_rc(e, cpr, row, cc);
-                const uint32_t o = canon(cc * 8, row, ncols);
-                float l[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    v[u][i] *= sign;
-                    l[i] = v[u][i] - __bfloat162float(__float2bfloat16_rn(v[u][i]));
-                }
-                st_bf16x8(hi + o, v[u]);
-                if (lo) st_bf16x8(lo + o, l);
-            }
-        }
     }
 }
 
@@ -233,7 +181,7 @@ __device__ __forceinline__ void cta_sync_tc() {
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs p) {
     extern __shared__ __align__(1024) uint8_t sm[];
-    __shared__ uint64_t bar;
+    __shared__ uint64_t bar, barL, barS[2];
     __shared__ uint32_t tmem_base_sh;
     const int c = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
     const int j = h / (int)d.G;
@@ -269,33 +217,28 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     const int nvalid = (int)(d.T - t0 < C ? d.T - t0 : C);
     const int64_t gbase = ((int64_t)bb * d.Hv + h) * d.Tp + t0;
     const int64_t rbase = ((int64_t)bb * d.Hk + j) * d.Tp + t0;
-    const int64_t cbase = (((int64_t)bb * d.Hv + h) * d.NC + c) * Dk * Dv;
+    const int64_t ci = ((int64_t)bb * d.Hv + h) * d.NC + c;  // chunk image index
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
     const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(p.k);
     const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(p.v);
     const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(p.d_o);
     __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(p.dv);
     const int64_t ldq = d.Hk * Dk, ldv = d.Hv * Dv;
-
-    // S / Sbar' rows of a Dk block, loaded into registers ahead of use
-    float gcb = 0.f;
-    constexpr int kPer = (kBlkK * 256 / 8 + kThreads - 1) / kThreads;  // chunks per thread (Dv <= 256)
-    float pre_s[kPer][8], pre_p[kPer][8];
-    const int cpr_s = Dv / 8;
-    auto load_blk = [&](int dk0, int nk) {
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int e = tid + u * kThreads;
-            if (e < nk * cpr_s) {
-                int row, cc;
-                chunk_rc(e, cpr_s, row, cc);
-                const int64_t off = cbase + (int64_t)(dk0 + row) * Dv + cc * 8;
-                ld8(p.ckpt + off, pre_s[u]);
-                ld8(p.dSck + off, pre_p[u]);
-            }
-        }
+    const uint32_t tv = (uint32_t)(C * Dv * 2);         // one 64 x Dv bf16 tile
+    const uint32_t blk = (uint32_t)(kBlkK * Dv * 2);    // one Dk block of S (or Sbar')
+    const uint8_t* ck_img = reinterpret_cast<const uint8_t*>(p.ckpt) + ci * (int64_t)Dk * Dv * 2;
+    const uint8_t* ds_img = reinterpret_cast<const uint8_t*>(p.dSck) + ci * (int64_t)Dk * Dv * 2;
+    // Dk block b of S / Sbar' (panels 4b .. 4b + 3 of the images) -> buffer b & 1
+    // (buffer 1 is the V tile's space, free once phase 0 is done)
+    auto sbuf = [&](int b) { return (b & 1) ? L.V : L.S; };
+    auto load_blk = [&](int b) {
+        const uint32_t dst = sbuf(b);
+        tc::mbar_arrive_expect_tx(&barS[b & 1], 2 * blk);
+        tc::bulk_g2s(sm + dst, ck_img + (int64_t)b * blk, blk, &barS[b & 1]);
+        tc::bulk_g2s(sm + dst + blk, ds_img + (int64_t)b * blk, blk, &barS[b & 1]);
     };
-    // ---- operands: raw q, k, dO, v by cp.async; Delta (hi + lo), -Dbar, T as bf16
+    // ---- operands: raw q, k, dO, v by cp.async; Delta (hi + lo), -Dbar, T and
+    // the first Dk block of S / Sbar' as bf16 images by bulk copies
     cpa_tile(sm + L.K, k + ((int64_t)bb * d.T + t0) * ldq + (int64_t)j * Dk, ldq, Dk, nvalid);
     cpa_tile(sm + L.Q, q + ((int64_t)bb * d.T + t0) * ldq + (int64_t)j * Dk, ldq, Dk, nvalid);
     cpa_tile(sm + L.O, dO + ((int64_t)bb * d.T + t0) * ldv + (int64_t)h * Dv, ldv, Dv, nvalid);
@@ -307,7 +250,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     }
     if (tid == 0) {
         tc::mbar_init(&bar, 1);
+        tc::mbar_init(&barL, 1);
+        tc::mbar_init(&barS[0], 1);
+        tc::mbar_init(&barS[1], 1);
         tc::fence_mbar_init();
+        const uint8_t* dl_img = reinterpret_cast<const uint8_t*>(p.Delta) + ci * (int64_t)C * Dv * 4;
+        tc::mbar_arrive_expect_tx(&barL, 3 * tv + C * C * 2);
+        tc::bulk_g2s(sm + L.D, dl_img, tv, &barL);
+        tc::bulk_g2s(sm + L.Dlo, dl_img + tv, tv, &barL);
+        tc::bulk_g2s(sm + L.NB, reinterpret_cast<const uint8_t*>(p.Dbar) + ci * (int64_t)tv, tv, &barL);
+        tc::bulk_g2s(sm + L.Tt, reinterpret_cast<const uint8_t*>(p.Tinv) + ci * (int64_t)C * C * 2,
+                     C * C * 2, &barL);
+        load_blk(0);
     }
     if (tid < C) {
         const double G = p.gam[gbase + tid];
@@ -322,30 +276,28 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     }
     for (int i = tid; i < 10 * C; i += blockDim.x) gq[i] = 0.f;  // gq, ee, bb0, zk, sbp
     for (int i = tid; i < 4 * C; i += blockDim.x) rsp[i] = 0.f;  // rsp, rsc
-    load_blk(0, Dk < kBlkK ? Dk : kBlkK);
-    stage_f32(sm + L.D, sm + L.Dlo, p.Delta + gbase * Dv, Dv, Dv, 1.f);
-    stage_f32(sm + L.NB, nullptr, p.Dbar + gbase * Dv, Dv, Dv, -1.f);
-    stage_f32(sm + L.Tt, nullptr, p.Tinv + (((int64_t)bb * d.Hv + h) * d.NC + c) * C * C, C, C, 1.f);
     tc::cp_async_wait_all();
     tc::fence_async_smem();
     cta_sync_tc();
     const uint32_t tb = tmem_base_sh;
     uint32_t phase = 0;
-    bool ok = true;
+    bool ok = tc::mbar_wait(&barL, 0, &g_err_bwdtc);
 
     const tc::Tile tK = kmaj(sm, L.K, Dk), tQ = kmaj(sm, L.Q, Dk), tW = kmaj(sm, L.W, Dk);
     const tc::Tile tKmn = mnmaj(sm, L.K, Dk), tQmn = mnmaj(sm, L.Q, Dk), tWmn = mnmaj(sm, L.W, Dk);
-    const tc::Tile tO = kmaj(sm, L.O, Dv), tD = kmaj(sm, L.D, Dv), tNB = kmaj(sm, L.NB, Dv);
-    const tc::Tile tDlo = kmaj(sm, L.Dlo, Dv);
-    const tc::Tile tV = kmaj(sm, L.V, Dv), tNBmn = mnmaj(sm, L.NB, Dv);
-    const tc::Tile tTt = kmaj(sm, L.Tt, C), tTmn = mnmaj(sm, L.Tt, C);
+    const tc::Tile tO = kmaj(sm, L.O, Dv), tV = kmaj(sm, L.V, Dv);
+    // Delta / -Dbar images: x = step t (canonical, 8-row groups of Dv 1024 bytes apart)
+    const tc::Tile tDmn = mnmaj(sm, L.D, C), tDlomn = mnmaj(sm, L.Dlo, C);
+    const tc::Tile tNB = kmaj(sm, L.NB, C), tNBmn = mnmaj(sm, L.NB, C);
+    // T image: panel layout, x = column j
+    const tc::Tile tTt = tc::panel_tile(sm + L.Tt, C, true), tTmn = tc::panel_tile(sm + L.Tt, C, false);
 
     // ---- phase 0: Pbar = Obar Delta^T | -Dbar V^T | -T^T Dbar | K K^T | Q K^T
     if (tid == 0) {
-        tc::mma_tile(tb + 0, tO, tD, C, C, Dv, false);
-        tc::mma_tile(tb + 0, tO, tDlo, C, C, Dv, true);
-        tc::mma_tile(tb + 64, tNB, tV, C, C, Dv, false);
-        tc::mma_tile(tb + 128, tTmn, tNBmn, C, Dv, C, false);
+        tc::mma_tile(tb + 0, tO, tDmn, C, C, Dv, false);
+        tc::mma_tile(tb + 0, tO, tDlomn, C, C, Dv, true);
+        tc::mma_tile(tb + 64, tNBmn, tV, C, C, Dv, false);
+        tc::mma_tile(tb + 128, tTmn, tNB, C, Dv, C, false);
         tc::mma_tile(tb + kColGkk, tK, tK, C, C, Dk, false);
         tc::mma_tile(tb + kColGqk, tQ, tK, C, C, Dk, false);
         tc::mma_commit(&bar);
@@ -387,38 +339,33 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
         });
     }
 
-    // ---- phase 1: state products per kBlkK-wide block of Dk; the next block's
-    // fp32 S / Sbar' rows load into registers while the current block's MMAs run
-    for (int dk0 = 0; dk0 < Dk; dk0 += kBlkK) {
-        const int nk = Dk - dk0 < kBlkK ? Dk - dk0 : kBlkK;
-        cta_sync_tc();  // previous block's TMEM reads and MMAs are done
-        {
-            const uint32_t ys = (uint32_t)Dv * 16u;
+    // ---- phase 1: state products per kBlkK-wide block of Dk; block b + 1 streams
+    // into the other buffer while block b's products and epilogues run.  <S, Sbar'>
+    // (the chunk-end term of the log-decay cotangent) is summed from the same tiles.
+    float gcb = 0.f;
+    const int nblk = Dk / kBlkK;
+    for (int b = 0; b < nblk; ++b) {
+        const int dk0 = b * kBlkK, nk = kBlkK;
+        cta_sync_tc();  // previous block's TMEM reads and MMAs are done; its buffer is free
+        if (tid == 0 && b + 1 < nblk) load_blk(b + 1);
+        ok = tc::mbar_wait(&barS[b & 1], (uint32_t)(b >> 1) & 1u, &g_err_bwdtc) && ok;
+        const uint8_t* sS = sm + sbuf(b);
+        for (int e = tid; e < (int)(blk / 16); e += kThreads) {
+            float a8[8], b8[8];
+            ld_bf16x8(sS + 16 * e, a8);
+            ld_bf16x8(sS + blk + 16 * e, b8);
 #pragma unroll
-            for (int u = 0; u < kPer; ++u) {
-                const int e = tid + u * kThreads;
-                if (e < nk * cpr_s) {
-                    int row, cc;
-                    chunk_rc(e, cpr_s, row, cc);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) gcb = fmaf(pre_s[u][i], pre_p[u][i], gcb);
-                    const uint32_t o = cc * 128u + (row >> 3) * ys + (row & 7) * 16u;
-                    st_bf16x8(sm + L.S + o, pre_s[u]);
-                    st_bf16x8(sm + L.Sp + o, pre_p[u]);
-                }
-            }
+            for (int i = 0; i < 8; ++i) gcb = fmaf(a8[i], b8[i], gcb);
         }
-        tc::fence_async_smem();
-        cta_sync_tc();
-        const tc::Tile tS = kmaj(sm, L.S, Dv), tSp = kmaj(sm, L.Sp, Dv);
+        // S / Sbar' blocks: panel layout over Dv rows, x = dk (the N dimension)
+        const tc::Tile tS = tc::panel_tile(sS, Dv, false), tSp = tc::panel_tile(sS + blk, Dv, false);
         if (tid == 0) {
             tc::mma_tile(tb + 0, tO, tS, C, nk, Dv, false);
-            tc::mma_tile(tb + 64, tNB, tS, C, nk, Dv, false);
-            tc::mma_tile(tb + 128, tD, tSp, C, nk, Dv, false);
-            tc::mma_tile(tb + 128, tDlo, tSp, C, nk, Dv, true);
+            tc::mma_tile(tb + 64, tNBmn, tS, C, nk, Dv, false);
+            tc::mma_tile(tb + 128, tDmn, tSp, C, nk, Dv, false);
+            tc::mma_tile(tb + 128, tDlomn, tSp, C, nk, Dv, true);
             tc::mma_commit(&bar);
         }
-        if (dk0 + kBlkK < Dk) load_blk(dk0 + kBlkK, Dk - dk0 - kBlkK < kBlkK ? Dk - dk0 - kBlkK : kBlkK);
         sync_after_mma(&bar, phase, ok);
         if (ok) {
             acc_rows(tb, 0, nk, [&](int r, int c0, const float (&x)[16]) {

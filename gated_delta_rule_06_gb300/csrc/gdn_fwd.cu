@@ -254,13 +254,13 @@ cudaError_t launch_fwd_chunk_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_fwd_chunk(const Dims& d, const Ptrs& p, cudaStream_t s) {
-    if (fwd_chunk_tc_supported(d)) return launch_fwd_chunk_tc(d, p, s);
+    if (tc_path(d)) return launch_fwd_chunk_tc(d, p, s);
     return d.dtype == 1 ? launch_fwd_chunk_t<__nv_bfloat16>(d, p, s)
                         : launch_fwd_chunk_t<float>(d, p, s);
 }
 
 cudaError_t launch_fwd_scan(const Dims& d, const Ptrs& p, cudaStream_t s) {
-    if (scan_tc_supported(d)) return launch_fwd_scan_tc(d, p, s);
+    if (tc_path(d)) return launch_fwd_scan_tc(d, p, s);
     if (d.Dv % 32 == 0)
         return d.dtype == 1 ? launch_scan_t<__nv_bfloat16, 32>(d, p, s) : launch_scan_t<float, 32>(d, p, s);
     if (d.Dv % 16 == 0)

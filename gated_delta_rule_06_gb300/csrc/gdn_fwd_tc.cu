@@ -10,8 +10,9 @@
 //   T = (I + A)^-1               blocked forward substitution in fp32 (16 x 16 blocks)
 //   W = T diag(beta gam r_k) K,   U = T diag(beta) V
 // T enters the W / U products as two bf16 terms (hi + lo) so that U keeps fp32
-// accuracy (the forward state update subtracts W S from U).  Outputs: T (fp32),
-// P, W (bf16), U (fp32).
+// accuracy (the forward state update subtracts W S from U).  Outputs: T, P and
+// W as bf16 panel images (the operand layout of the scans and the gradient
+// kernel), U row-major in fp32.
 #include "gdn_internal.cuh"
 #include "gdn_tc.cuh"
 
@@ -220,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_chunk_tc_kernel(Dims d, Ptrs 
     ok = tc::mbar_wait(&bar, phase, &g_err_fwdtc) && ok;
     phase ^= 1u;
     tc::tc_fence_after();
-    __nv_bfloat16* P = static_cast<__nv_bfloat16*>(p.P) + (bh * d.NC + c) * C * C;
+    uint8_t* Pimg = static_cast<uint8_t*>(p.P) + (bh * d.NC + c) * C * C * 2;
     if (ok) {
         acc_rows(tb, 0, C, [&](int r, int c0, const float (&x)[16]) {
 #pragma unroll
@@ -238,9 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_chunk_tc_kernel(Dims d, Ptrs 
                 const float m = jj <= r ? expf((float)(Gm[r] - Gm[jj])) : 0.f;
                 pv[i] = m * rqv[r] * rkv[jj] * x[i];
             }
-            uint8_t* dst = reinterpret_cast<uint8_t*>(P + r * C + c0);
-            st_bf16x8(dst, pv);
-            st_bf16x8(dst + 16, pv + 8);
+            st_bf16x8(Pimg + tc::panel_off(c0, r, C), pv);
+            st_bf16x8(Pimg + tc::panel_off(c0 + 8, r, C), pv + 8);
         });
     }
     tc::tc_fence_before();
@@ -249,9 +249,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_chunk_tc_kernel(Dims d, Ptrs 
 
     // ---- T = (I + A)^-1 (fp32)
     tri_inverse64(A, Tm, X);
-    float* Tg = p.Tinv + (bh * d.NC + c) * C * C;
-    for (int e = tid; e < C * C / 4; e += blockDim.x)
-        reinterpret_cast<float4*>(Tg)[e] = reinterpret_cast<const float4*>(Tm)[e];
+    // T as a bf16 panel image: 16-byte chunk e holds row e % 64, columns 8 (e / 64) ..
+    uint8_t* Timg = reinterpret_cast<uint8_t*>(p.Tinv) + (bh * d.NC + c) * C * C * 2;
+    for (int e = tid; e < C * (C / 8); e += blockDim.x)
+        st_bf16x8(Timg + 16 * e, Tm + (e % C) * C + (e / C) * 8);
     // A operands T diag(beta gam r_k) and T diag(beta), each as hi + lo bf16 (x = j, y = i)
     for (int e = tid; e < C * (C / 8); e += blockDim.x) {
         const int i = e / (C / 8), j0 = (e % (C / 8)) * 8;
@@ -290,12 +291,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_chunk_tc_kernel(Dims d, Ptrs 
     phase ^= 1u;
     tc::tc_fence_after();
     if (ok) {
-        __nv_bfloat16* W = static_cast<__nv_bfloat16*>(p.W) + gbase * Dk;
+        uint8_t* Wimg = static_cast<uint8_t*>(p.W) + gbase * Dk * 2;
         float* U = p.U + gbase * Dv;
         acc_rows(tb, 0, Dk, [&](int r, int c0, const float (&x)[16]) {
-            uint8_t* dst = reinterpret_cast<uint8_t*>(W + (int64_t)r * Dk + c0);
-            st_bf16x8(dst, x);
-            st_bf16x8(dst + 16, x + 8);
+            st_bf16x8(Wimg + tc::panel_off(c0, r, C), x);
+            st_bf16x8(Wimg + tc::panel_off(c0 + 8, r, C), x + 8);
         });
         acc_rows(tb, Dk, Dv, [&](int r, int c0, const float (&x)[16]) {
             float4* dst = reinterpret_cast<float4*>(U + (int64_t)r * Dv + c0);

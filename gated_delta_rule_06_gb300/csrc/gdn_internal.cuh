@@ -22,6 +22,21 @@ struct Dims {
 
 // Every device buffer the kernels touch.  Inputs/outputs come from the
 // caller; the rest are carved out of the caller's `saved` and `ws` buffers.
+//
+// Two storage formats exist for the saved intermediates.  The CUDA-core path
+// (fp32 inputs, and shapes outside the tensor-core kernels' range) stores them
+// row-major as annotated.  The tensor-core path (tc_path) stores every one of
+// them as bf16 operand images per chunk, in the exact shared-memory layout the
+// consuming MMA reads, so each is moved by one bulk copy:
+//   ckpt   [B, Hv, NC] images of S^T (Dv rows x Dk, panel layout), bf16
+//   Tinv   [B, Hv, NC] images of T (64 rows x 64, panel), bf16
+//   W      [B, Hv, NC] images of W (64 rows x Dk, panel)
+//   P      [B, Hv, NC] images of P (64 rows x 64, panel)
+//   Delta  [B, Hv, NC] pairs {hi, lo} of images of Delta^T (Dv rows x 64,
+//          canonical x = step, 8-row groups 1024 bytes apart), Delta = hi + lo
+//   dSck   [B, Hv, NC] images of Sbar'^T (Dv rows x Dk, panel), bf16
+//   Dbar   [B, Hv, NC] images of -Dbar^T (Dv rows x 64, as Delta), bf16
+// U, gam, beta, rq, rk and the backward partials keep the row-major fp32 form.
 struct Ptrs {
     // primal inputs
     const void *q, *k, *v, *a, *b;
@@ -131,6 +146,9 @@ unsigned int read_clear_error_scantc();
 bool fwd_chunk_tc_supported(const Dims& d);
 cudaError_t launch_fwd_chunk_tc(const Dims& d, const Ptrs& p, cudaStream_t s);
 unsigned int read_clear_error_fwdtc();
+// bf16 inputs whose shape every tensor-core kernel supports: the whole forward
+// and backward run on the tensor-core kernels with the image formats above
+bool tc_path(const Dims& d);
 // adds n to the library's launch counter (called by every launcher)
 void count_launches(int n);
 // chunk index e of a 64-row (or 8k-row) canonical-tile copy -> (row, 8-column

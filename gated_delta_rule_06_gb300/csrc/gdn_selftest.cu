@@ -76,6 +76,77 @@ __global__ void __launch_bounds__(128) selftest_mma_kernel(int M, int N, int K, 
     if (warp == 0) tc::tmem_dealloc(tbase, 256);
 }
 
+// Same product with A held in TMEM (the form the scans use for the state):
+// thread m writes row m of A as packed bf16 pairs into columns 256 .. 256 + K/2.
+__global__ void __launch_bounds__(128) selftest_mma_ta_kernel(int N, int K, int b_mn,
+                                                              const __nv_bfloat16* __restrict__ A,
+                                                              const __nv_bfloat16* __restrict__ B,
+                                                              float* __restrict__ D) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tmem_base;
+    uint8_t* sb = smem;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    tc::Tile tb;
+    tb.base = tc::smem_u32(sb);
+    tb.k_major = !b_mn;
+    const int bx = b_mn ? N : K;
+    tb.xs = 128;
+    tb.ys = (uint32_t)(bx / 8) * 128;
+    for (int e = tid; e < K * N; e += blockDim.x) {
+        const int k = e / N, n = e % N;
+        const uint32_t o = b_mn ? tb.off(n, k) : tb.off(k, n);
+        *reinterpret_cast<__nv_bfloat16*>(sb + o) = B[e];
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(&tmem_base, 512);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        tc::mbar_init(&bar, 1);
+        tc::fence_mbar_init();
+    }
+    tc::fence_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tbase = tmem_base;
+    const uint32_t acol = 256;
+    for (int k0 = 0; k0 < K; k0 += 32) {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int k = k0 + 2 * i;
+            const float x = k < K ? __bfloat162float(A[tid * K + k]) : 0.f;
+            const float y = k + 1 < K ? __bfloat162float(A[tid * K + k + 1]) : 0.f;
+            w[i] = tc::pack_bf16(x, y);
+        }
+        tc::tmem_st16u(tc::tmem_addr(tbase, 32 * warp, acol + k0 / 2), w);
+    }
+    tc::tmem_wait_st();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (tid == 0) {
+        tc::mma_tile_ta(tbase, tbase + acol, tb, 128, N, K, false);
+        tc::mma_commit(&bar);
+    }
+    const bool ok = tc::mbar_wait(&bar, 0, &g_err_selftest);
+    tc::tc_fence_after();
+    if (ok) {
+        for (int c0 = 0; c0 < N; c0 += 16) {
+            float v[16];
+            tc::tmem_ld16(tc::tmem_addr(tbase, 32 * warp, c0), v);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) D[tid * N + c0 + i] = v[i];
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tbase, 512);
+}
+
 }  // namespace
 }  // namespace gdn
 
@@ -91,6 +162,20 @@ extern "C" gdn_status gdn_selftest_mma(int M, int N, int K, int a_mn_major, int 
     kern<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(
         M, N, K, a_mn_major, b_mn_major, static_cast<const __nv_bfloat16*>(A),
         static_cast<const __nv_bfloat16*>(B), D_raw);
+    gdn::count_launches(1);
+    return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+extern "C" gdn_status gdn_selftest_mma_tmem_a(int N, int K, int b_mn_major, const void* A,
+                                              const void* B, float* D, void* stream) {
+    if (N < 16 || N > 256 || N % 16 || K < 16 || K > 256 || K % 32) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (!A || !B || !D) return GDN_ERR_INVALID_ARG;
+    const size_t smem = (size_t)256 * 256 * 2;
+    auto kern = gdn::selftest_mma_ta_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    kern<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(
+        N, K, b_mn_major, static_cast<const __nv_bfloat16*>(A), static_cast<const __nv_bfloat16*>(B), D);
     gdn::count_launches(1);
     return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

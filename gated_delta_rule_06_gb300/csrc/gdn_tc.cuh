@@ -11,6 +11,7 @@
 // i.e. two core matrices along K: the next K step starts 2 * LBO further.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -156,6 +157,31 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
+// ---- bulk (non-tensor) asynchronous copies through the async proxy ------------------
+// Addresses 16-byte aligned, size a multiple of 16.  global -> shared completes
+// `bytes` of transaction count on *bar (the issuer arms it with arrive_expect_tx);
+// shared -> global is tracked in the issuing thread's bulk groups.
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst_smem)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_u32(src_smem)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// this thread's bulk stores have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// this thread's bulk stores are complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ---- descriptors -------------------------------------------------------------------
 // shared-memory matrix descriptor, no swizzle, sm_100 version field = 1
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -183,6 +209,18 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]: A (M x K, bf16) held in TMEM, row m in the
+// accumulator's lane for row m, K elements packed two per 32-bit column
+// (element 2i in the low half of column i)
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // arrive on *bar once every MMA issued so far by this thread has completed
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile(
@@ -207,12 +245,62 @@ struct Tile {
     }
 };
 
+// "Panel" image of a bf16 operand with `rows` rows (y) and 8-column groups (x):
+// the canonical layout with XS = rows * 16 and YS = 128, so every 8-column group
+// is one contiguous panel of rows x 16 bytes and a run of groups is one block.
+// Saved intermediates are stored in global memory in this form and moved with a
+// single bulk copy.
+__host__ __device__ __forceinline__ uint32_t panel_off(uint32_t x, uint32_t y, uint32_t rows) {
+    return (x >> 3) * rows * 16u + y * 16u + (x & 7u) * 2u;
+}
+__device__ __forceinline__ Tile panel_tile(const void* smem, uint32_t rows, bool k_major) {
+    Tile t;
+    t.base = smem_u32(smem);
+    t.xs = rows * 16u;
+    t.ys = 128u;
+    t.k_major = k_major;
+    return t;
+}
+
 // issue D = A (M x K) * B (K x N) (+ D if accumulate) as K / 16 MMAs
 __device__ __forceinline__ void mma_tile(uint32_t d_tmem, const Tile& A, const Tile& B, int M,
                                          int N, int K, bool accumulate) {
     const uint32_t id = idesc_bf16(M, N, !A.k_major, !B.k_major);
     for (int k = 0; k < K; k += 16)
         mma_bf16(d_tmem, A.desc(k), B.desc(k), id, (accumulate || k > 0) ? 1u : 0u);
+}
+
+// issue D = A (M x K, in TMEM at column a_col) * B (K x N) (+ D) as K / 16 MMAs
+__device__ __forceinline__ void mma_tile_ta(uint32_t d_tmem, uint32_t a_tmem, const Tile& B, int M,
+                                            int N, int K, bool accumulate) {
+    const uint32_t id = idesc_bf16(M, N, false, !B.k_major);
+    for (int k = 0; k < K; k += 16)
+        mma_bf16_ta(d_tmem, a_tmem + (uint32_t)(k >> 1), B.desc(k), id,
+                    (accumulate || k > 0) ? 1u : 0u);
+}
+// 32 lanes x 32 bits, 16 consecutive columns per thread, raw 32-bit words
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld16u(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+// two floats -> packed bf16 pair (x in the low half), round to nearest even
+__device__ __forceinline__ uint32_t pack_bf16(float x, float y) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    return *reinterpret_cast<uint32_t*>(&h);
 }
 
 }  // namespace tc

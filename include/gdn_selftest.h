@@ -28,6 +28,17 @@ extern "C" {
 gdn_status gdn_selftest_mma(int M, int N, int K, int a_mn_major, int b_mn_major, const void* A,
                             const void* B, float* D_raw, void* stream);
 
+/* D = A * B on one CTA with tcgen05.mma taking A from tensor memory (the form
+ * the scans use for the state operand), M = 128.
+ *   A: device bf16 [128][K] row-major, written by its 128 threads into TMEM
+ *   (row m in lane m, two elements per 32-bit column); B: device bf16 [K][N]
+ *   row-major, staged in shared memory in the orientation b_mn_major selects.
+ *   N in 16..256 (multiple of 16); K in 32..256 (multiple of 32).
+ *   D: device fp32 [128][N].
+ * Enqueued on `stream`; returns GDN_ERR_UNSUPPORTED_SHAPE for other sizes. */
+gdn_status gdn_selftest_mma_tmem_a(int N, int K, int b_mn_major, const void* A, const void* B,
+                                   float* D, void* stream);
+
 /* Reads and clears the library's device error word (nonzero after a bounded
  * wait inside a kernel gave up).  Synchronises the device. */
 gdn_status gdn_device_error(unsigned int* flag);

@@ -19,6 +19,8 @@ def lib():
     L = ops.load_library()
     L.gdn_selftest_mma.argtypes = [ctypes.c_int] * 5 + [ctypes.c_void_p] * 4
     L.gdn_selftest_mma.restype = ctypes.c_int
+    L.gdn_selftest_mma_tmem_a.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p] * 4
+    L.gdn_selftest_mma_tmem_a.restype = ctypes.c_int
     L.gdn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     L.gdn_device_error.restype = ctypes.c_int
     return L
@@ -58,6 +60,21 @@ def test_m64_lane_placement(lib, amn, bmn, N, K):
     D, ref = _run(lib, 64, N, K, amn, bmn)
     got = D[_lanes_m64().cuda()]
     torch.testing.assert_close(got, ref, rtol=1e-5, atol=1e-4)
+
+
+@pytest.mark.parametrize("bmn", [0, 1])
+@pytest.mark.parametrize("N,K", [(64, 32), (64, 192), (192, 64), (128, 256)])
+def test_a_from_tmem(lib, bmn, N, K):
+    g = torch.Generator().manual_seed(7 + N + K)
+    A = torch.randn((128, K), generator=g).to(torch.bfloat16).cuda()
+    B = torch.randn((K, N), generator=g).to(torch.bfloat16).cuda()
+    D = torch.full((128, N), float("nan"), device="cuda")
+    rc = lib.gdn_selftest_mma_tmem_a(N, K, bmn, ctypes.c_void_p(A.data_ptr()),
+                                     ctypes.c_void_p(B.data_ptr()), ctypes.c_void_p(D.data_ptr()),
+                                     ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    torch.cuda.synchronize()
+    torch.testing.assert_close(D, A.float() @ B.float(), rtol=1e-5, atol=1e-4)
 
 
 def test_no_wait_timeouts(lib):
