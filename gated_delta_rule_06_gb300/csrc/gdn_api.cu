@@ -1,8 +1,11 @@
 // gdn_api.cu -- the C ABI of include/gdn.h: argument validation, the layout
 // of the `saved` and workspace buffers, and the launch sequence.
+#include <cudaTypedefs.h>
+
 #include <atomic>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "../../include/gdn.h"
@@ -125,6 +128,25 @@ void carve_saved(const Layout& L, void* saved, gdn::Ptrs* p) {
     p->Delta = reinterpret_cast<float*>(s + L.Delta);
 }
 
+// tensor maps of q, k, v (and dO) for the tensor-core kernels: full-width
+// 64-row tiles, dO in tiles of at most 128 columns (the scans' value tile)
+bool make_tmaps(const gdn::Dims& d, const void* q, const void* k, const void* v, const void* dO,
+                const void* o, gdn::Tmaps* m) {
+    std::memset(m, 0, sizeof(*m));
+    const int vt = (int)(d.Dv < 128 ? d.Dv : 128);
+    bool ok = gdn::encode_row_tile_map(&m->q, q, d.B, d.T, d.Hk, d.Dk, (int)d.Dk) &&
+              gdn::encode_row_tile_map(&m->k, k, d.B, d.T, d.Hk, d.Dk, (int)d.Dk) &&
+              gdn::encode_row_tile_map(&m->v, v, d.B, d.T, d.Hv, d.Dv, (int)d.Dv);
+    if (ok && dO) ok = gdn::encode_row_tile_map(&m->dO, dO, d.B, d.T, d.Hv, d.Dv, vt);
+    if (ok && o) ok = gdn::encode_row_major_map(&m->o, o, d.B, d.T, d.Hv * d.Dv, vt);
+    return ok;
+}
+
+gdn_status tmap_error() {
+    std::snprintf(g_cuda_err, sizeof(g_cuda_err), "cuTensorMapEncodeTiled refused a tensor map");
+    return GDN_ERR_CUDA;
+}
+
 gdn_status cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return GDN_OK;
     std::snprintf(g_cuda_err, sizeof(g_cuda_err), "%s: %s", cudaGetErrorName(e),
@@ -135,6 +157,49 @@ gdn_status cuda_status(cudaError_t e) {
 }  // namespace
 
 namespace gdn {
+// the driver's tensor-map encoder, resolved once through the runtime
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return encode;
+}
+
+bool encode_row_tile_map(CUtensorMap* m, const void* base, int64_t B, int64_t T, int64_t H,
+                         int64_t D, int cols) {
+    const auto encode = tensor_map_encoder();
+    if (encode == nullptr || cols % 8 || cols < 8 || cols > 256 || D % 8) return false;
+    const cuuint64_t dims[5] = {8, (cuuint64_t)T, (cuuint64_t)(D / 8), (cuuint64_t)H, (cuuint64_t)B};
+    // byte strides of dims 1..4: row, 8-column group, head, batch
+    const cuuint64_t strides[4] = {(cuuint64_t)(H * D * 2), 16, (cuuint64_t)(D * 2),
+                                   (cuuint64_t)(T * H * D * 2)};
+    const cuuint32_t box[5] = {8, (cuuint32_t)kChunk, (cuuint32_t)(cols / 8), 1, 1};
+    const cuuint32_t unit[5] = {1, 1, 1, 1, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
+                  unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_row_major_map(CUtensorMap* m, const void* base, int64_t B, int64_t T, int64_t rowlen,
+                          int cols) {
+    const auto encode = tensor_map_encoder();
+    if (encode == nullptr || cols % 8 || cols < 8 || cols > 256 || rowlen % 8) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)rowlen, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t strides[2] = {(cuuint64_t)(rowlen * 2), (cuuint64_t)(T * rowlen * 2)};
+    const cuuint32_t box[3] = {(cuuint32_t)cols, (cuuint32_t)kChunk, 1};
+    const cuuint32_t unit[3] = {1, 1, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                  unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool tc_path(const Dims& d) {
     return d.dtype == GDN_DTYPE_BF16 && fwd_chunk_tc_supported(d) && scan_tc_supported(d) &&
            bwd_chunk_tc_supported(d);
@@ -142,7 +207,8 @@ bool tc_path(const Dims& d) {
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n); }
 unsigned int read_clear_error_all() {
     const unsigned int words[] = {read_clear_error_selftest(), read_clear_error_bwdtc(),
-                                  read_clear_error_scantc(), read_clear_error_fwdtc()};
+                                  read_clear_error_scantc(), read_clear_error_fwdtc(),
+                                  read_clear_error_scanta()};
     unsigned int v = 0;
     for (unsigned int w : words) {
         if (w == ~0u) return ~0u;
@@ -223,6 +289,11 @@ gdn_status gdn_forward(const gdn_shape* shape, const void* q, const void* k, con
         carve_saved(L, wsb + L.fwd_total, &p);
     }
     p.U = reinterpret_cast<float*>(wsb + L.U);
+    gdn::Tmaps maps;
+    if (gdn::tc_path(d)) {
+        if (!make_tmaps(d, q, k, v, nullptr, o, &maps)) return tmap_error();
+        p.tmaps = &maps;
+    }
     cudaError_t e = run_phase("prep", s, [&] { return gdn::launch_prep(d, p, s); });
     if (e == cudaSuccess) e = run_phase("fwd_chunk", s, [&] { return gdn::launch_fwd_chunk(d, p, s); });
     if (e == cudaSuccess) e = run_phase("fwd_scan", s, [&] { return gdn::launch_fwd_scan(d, p, s); });
@@ -268,6 +339,11 @@ gdn_status gdn_backward(const gdn_shape* shape, const void* q, const void* k, co
     p.dbeta = reinterpret_cast<float*>(w + L.dbeta);
     p.part = reinterpret_cast<float*>(w + L.part);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    gdn::Tmaps maps;
+    if (gdn::tc_path(d)) {
+        if (!make_tmaps(d, q, k, v, d_o, nullptr, &maps)) return tmap_error();
+        p.tmaps = &maps;
+    }
     cudaError_t e = run_phase("bwd_scan", s, [&] { return gdn::launch_bwd_scan(d, p, s); });
     if (e == cudaSuccess) e = run_phase("bwd_chunk", s, [&] { return gdn::launch_bwd_chunk(d, p, s); });
     if (e == cudaSuccess) e = run_phase("bwd_reduce", s, [&] { return gdn::launch_bwd_reduce(d, p, s); });

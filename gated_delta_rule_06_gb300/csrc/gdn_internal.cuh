@@ -2,6 +2,7 @@
 // CUDA kernels of the gated delta rule library.  Private to libgdn.so.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (type only; the library links the runtime alone)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -19,6 +20,24 @@ struct Dims {
     int64_t Tp;  // NC * 64 (sequence padded with identity steps)
     int dtype;   // 0 = fp32, 1 = bf16
 };
+
+// TMA descriptors of the raw bf16 inputs, encoded on the host for each call of
+// the tensor-core path and handed to the kernels as __grid_constant__ params.
+// Each describes a [B, T, H, D] tensor (row t of head h of batch b at
+// ((b T + t) H + h) D) as 5-d {8, T, D / 8, H, B} with a box of 64 rows: one
+// load brings a 64-row tile in the panel layout (8-column groups of 64 x 16
+// bytes); rows past T arrive as zeros.
+// `o` is the output [B, T, Hv, Dv] as 3-d {Hv Dv, T, B} with a row-major box of
+// 64 rows x min(Dv, 128) columns, for TMA stores of staged output rows (rows past
+// T are not written).
+struct Tmaps {
+    CUtensorMap q, k, v, dO, o;
+};
+// box `cols` columns wide (multiple of 8, <= 256); false if the driver refuses
+bool encode_row_tile_map(CUtensorMap* m, const void* base, int64_t B, int64_t T, int64_t H,
+                         int64_t D, int cols);
+bool encode_row_major_map(CUtensorMap* m, const void* base, int64_t B, int64_t T, int64_t rowlen,
+                          int cols);
 
 // Every device buffer the kernels touch.  Inputs/outputs come from the
 // caller; the rest are carved out of the caller's `saved` and `ws` buffers.
@@ -75,6 +94,8 @@ struct Ptrs {
     float* dl;     // [B, Hv, Tp] cotangent of the log-decay
     float* dbeta;  // [B, Hv, Tp]
     float* part;   // [2, B, NC, Hv] per-chunk partial sums for dA_log, ddt_bias
+    // host copy of the tensor maps (tensor-core path; read by the launchers only)
+    const Tmaps* tmaps;
 };
 
 // ---- scalar load / store in the input dtype ---------------------------------
@@ -143,6 +164,9 @@ bool scan_tc_supported(const Dims& d);
 cudaError_t launch_fwd_scan_tc(const Dims& d, const Ptrs& p, cudaStream_t s);
 cudaError_t launch_bwd_scan_tc(const Dims& d, const Ptrs& p, cudaStream_t s);
 unsigned int read_clear_error_scantc();
+bool scan_ta_supported(const Dims& d);
+cudaError_t launch_fwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s);
+unsigned int read_clear_error_scanta();
 bool fwd_chunk_tc_supported(const Dims& d);
 cudaError_t launch_fwd_chunk_tc(const Dims& d, const Ptrs& p, cudaStream_t s);
 unsigned int read_clear_error_fwdtc();

@@ -1,0 +1,460 @@
+// gdn_scan_ta.cu -- the forward chunk scan for 128-row value tiles (M = 128
+// tcgen05 MMAs) with its A operands held in tensor memory.
+//
+// Same recurrence as gdn_scan_tc.cu (mlx-lm PR "Add gated_delta_update VJP",
+// "What this PR adds" and "Design notes": chunk 64, sequential over chunks):
+//   Delta^T = U^T - S^T W^T,   O^T = S^T Qs^T + Delta^T P^T,
+//   S^T <- gam_63 S^T + (Delta^T diag(e r_k)) K
+// with Qs = diag(gam r_q / sqrt(Dk)) Q.  The products with N = 64 (one chunk of
+// steps) would be bound by shared-memory bandwidth if their 128-row A operand
+// were read from shared memory, so S^T (as bf16 pairs) and Delta^T (hi + lo, and
+// diag(e r_k)-scaled hi + lo) are written by the epilogue threads straight into
+// TMEM, each thread its own accumulator row, and the MMAs take A from there.
+// B operands: the W and P images by bulk copy, raw q and k tiles by TMA (q is
+// scaled by gam r_q / sqrt(Dk) in place); the per-chunk gate and norm vectors
+// by bulk copy two chunks ahead.  Output rows are accumulated in two TMEM
+// buffers so the epilogue of chunk c runs while the products of chunk c + 1 do.
+//
+// TMEM columns: [0, Dk) the fp32 state S^T; [Dk, Dk + 128) A operands (S^T as
+// bf16 pairs during step 2, then Delta^T hi | lo | e-scaled hi | lo, 32 each);
+// [Dk + 128, +64) the Delta^T accumulator; then two 64-column output buffers.
+#include "gdn_internal.cuh"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+
+GDN_ERROR_WORD(scanta)
+
+namespace {
+
+constexpr int C = kChunk;
+constexpr int kThreads = 256;
+constexpr int DVT = 128;
+constexpr int kStoreWarp = 1;
+constexpr uint32_t kRawBytes = C * 8 + 2 * C * 4;  // gam (fp64) | r_q | r_k of one chunk
+
+__device__ __forceinline__ uint32_t canon(int x, int y, int ncols) {
+    return (uint32_t)(x >> 3) * 128u + (uint32_t)(y >> 3) * (uint32_t)ncols * 16u +
+           (uint32_t)(y & 7) * 16u + (uint32_t)(x & 7) * 2u;
+}
+
+struct TaSmem {
+    uint32_t W, Q, K, P, St, Dt, Dlo, Ob, raw, vec, total;
+};
+
+__host__ __device__ inline TaSmem ta_plan(int Dk) {
+    TaSmem s{};
+    uint32_t o = 0;
+    auto take = [&](uint32_t bytes) {
+        const uint32_t r = o;
+        o += (bytes + 1023u) & ~1023u;
+        return r;
+    };
+    s.W = take(C * Dk * 2);     // panel images (64 rows)
+    s.Q = take(C * Dk * 2);
+    s.K = take(C * Dk * 2);
+    s.P = take(C * C * 2);
+    s.St = take(DVT * Dk * 2);  // checkpoint image staging (panel, 128 rows)
+    s.Dt = take(DVT * C * 2);   // Delta^T hi / lo image staging (canonical, x = step)
+    s.Dlo = take(DVT * C * 2);
+    s.Ob = take(C * DVT * 2);   // output rows [t][dv]
+    s.raw = take(2 * kRawBytes);
+    s.vec = take(2 * 4 * C * 4);
+    s.total = o;
+    return s;
+}
+
+struct TaCols {
+    uint32_t aop, dacc, o0;
+};
+__host__ __device__ inline TaCols ta_cols(int Dk) {
+    TaCols t;
+    t.aop = (uint32_t)Dk;
+    t.dacc = (uint32_t)Dk + 128;
+    t.o0 = (uint32_t)Dk + 192;
+    return t;
+}
+
+// gam, e, gam r_q / sqrt(Dk), e r_k of one chunk from its raw block
+__device__ __forceinline__ void vectors_from_raw(const uint8_t* raw, float* v, int Dk) {
+    const int i = threadIdx.x;
+    if (i < C) {
+        const double* G = reinterpret_cast<const double*>(raw);
+        const float* rq = reinterpret_cast<const float*>(raw + C * 8);
+        const float* rk = reinterpret_cast<const float*>(raw + C * 12);
+        const float gm = expf((float)G[i]);
+        const float e = expf((float)(G[C - 1] - G[i]));
+        v[i] = gm;
+        v[C + i] = e;
+        v[2 * C + i] = gm * rq[i] * rsqrtf((float)Dk);
+        v[3 * C + i] = e * rk[i];
+    }
+}
+
+// q tile (panel layout, 16-byte chunk e holds step e % 64) scaled in place by
+// gam r_q / sqrt(Dk) of its step; each thread keeps one step
+__device__ __forceinline__ void scale_q(uint8_t* Q, const uint8_t* raw, int Dk) {
+    const int t = threadIdx.x & (C - 1);
+    const double* G = reinterpret_cast<const double*>(raw);
+    const float* rq = reinterpret_cast<const float*>(raw + C * 8);
+    const float s = expf((float)G[t]) * rq[t] * rsqrtf((float)Dk);
+    for (int e = threadIdx.x; e < C * Dk / 8; e += kThreads) {
+        uint4 u = reinterpret_cast<const uint4*>(Q)[e];
+        uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+            w[i] = tc::pack_bf16(f.x * s, f.y * s);
+        }
+        reinterpret_cast<uint4*>(Q)[e] = u;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads + 32, 1)
+    fwd_scan_ta_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm) {
+    extern __shared__ __align__(1024) uint8_t sm[];
+    __shared__ uint64_t bar, barW, barQ, barK, barP, barR[2];
+    __shared__ uint32_t tmem_sh;
+    const int tile = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
+    const int j = h / (int)d.G;
+    const int Dk = (int)d.Dk, Dv = (int)d.Dv;
+    const int n0 = tile * DVT;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // warps 0-7: epilogues (accumulator row r, column half g); warp 8: loads and MMA issue
+    const bool epi = tid < kThreads;
+    const bool prod = warp == kThreads / 32 && lane == 0;
+    const int r = 32 * (warp & 3) + lane;
+    const int g = (tid >> 7) & 1;
+    const uint32_t lb = 32u * (uint32_t)(warp & 3);
+    const TaSmem L = ta_plan(Dk);
+    const TaCols TC = ta_cols(Dk);
+    const int64_t bh = (int64_t)bb * d.Hv + h;
+    const uint32_t wbytes = (uint32_t)(C * Dk * 2), pbytes = (uint32_t)(C * C * 2);
+    const uint8_t* Wimg = static_cast<const uint8_t*>(p.W);
+    const uint8_t* Pimg = static_cast<const uint8_t*>(p.P);
+    uint8_t* ckimg = reinterpret_cast<uint8_t*>(p.ckpt);
+    uint8_t* dlimg = reinterpret_cast<uint8_t*>(p.Delta);
+    __nv_bfloat16* Ob = reinterpret_cast<__nv_bfloat16*>(sm + L.Ob);
+    const float* U = p.U;
+
+    // loads (producer)
+    auto load_w = [&](int64_t c) {
+        tc::mbar_arrive_expect_tx(&barW, wbytes);
+        tc::bulk_g2s(sm + L.W, Wimg + (bh * d.NC + c) * wbytes, wbytes, &barW);
+    };
+    auto load_p = [&](int64_t c) {
+        tc::mbar_arrive_expect_tx(&barP, pbytes);
+        tc::bulk_g2s(sm + L.P, Pimg + (bh * d.NC + c) * pbytes, pbytes, &barP);
+    };
+    auto load_q = [&](int64_t c) {
+        tc::mbar_arrive_expect_tx(&barQ, wbytes);
+        tc::tma_load_5d(sm + L.Q, &tm.q, 0, (int)(c * C), 0, j, bb, &barQ);
+    };
+    auto load_k = [&](int64_t c) {
+        tc::mbar_arrive_expect_tx(&barK, wbytes);
+        tc::tma_load_5d(sm + L.K, &tm.k, 0, (int)(c * C), 0, j, bb, &barK);
+    };
+    auto load_raw = [&](int64_t c) {
+        const int s = (int)(c & 1);
+        uint8_t* dst = sm + L.raw + s * kRawBytes;
+        tc::mbar_arrive_expect_tx(&barR[s], kRawBytes);
+        tc::bulk_g2s(dst, p.gam + bh * d.Tp + c * C, C * 8, &barR[s]);
+        tc::bulk_g2s(dst + C * 8, p.rq + ((int64_t)bb * d.Hk + j) * d.Tp + c * C, C * 4, &barR[s]);
+        tc::bulk_g2s(dst + C * 12, p.rk + ((int64_t)bb * d.Hk + j) * d.Tp + c * C, C * 4, &barR[s]);
+    };
+    // stores (lane 0 of the store warp; the caller commits)
+    auto store_o = [&](int64_t c) { tc::tma_store_3d(&tm.o, Ob, h * Dv + n0, (int)(c * C), bb); };
+    auto store_ck = [&](int64_t c) {
+        uint8_t* img = ckimg + (bh * d.NC + c) * (int64_t)Dk * Dv * 2;
+        if (DVT == Dv) {
+            tc::bulk_s2g(img, sm + L.St, (uint32_t)(DVT * Dk * 2));
+        } else {
+            for (int gi = 0; gi < Dk / 8; ++gi)
+                tc::bulk_s2g(img + (size_t)gi * Dv * 16 + (size_t)n0 * 16, sm + L.St + gi * DVT * 16,
+                             (uint32_t)(DVT * 16));
+        }
+    };
+    auto store_delta = [&](int64_t c) {
+        uint8_t* base = dlimg + (bh * d.NC + c) * (int64_t)C * Dv * 4 + (int64_t)n0 * 128;
+        tc::bulk_s2g(base, sm + L.Dt, (uint32_t)(DVT * 128));
+        tc::bulk_s2g(base + (int64_t)C * Dv * 2, sm + L.Dlo, (uint32_t)(DVT * 128));
+    };
+    const bool storer = warp == kStoreWarp && lane == 0;
+    // output rows of chunk c (buffer c & 1) -> staging
+    auto step5 = [&](uint32_t tb, int64_t c) {
+        float a[2][16];
+        const uint32_t col = TC.o0 + (uint32_t)(c & 1) * 64u + 32u * g;
+        tc::tmem_ld16(tc::tmem_addr(tb, lb, col), a[0]);
+        tc::tmem_ld16(tc::tmem_addr(tb, lb, col + 16), a[1]);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Ob[(32 * g + 16 * u + i) * DVT + r] = __float2bfloat16_rn(a[u][i]);
+    };
+
+    if (warp == 0) {
+        tc::tmem_alloc(&tmem_sh, 512);
+        tc::tmem_relinquish();
+    }
+    if (prod) {
+        tc::mbar_init(&bar, 1);
+        tc::mbar_init(&barW, 1);
+        tc::mbar_init(&barQ, 1);
+        tc::mbar_init(&barK, 1);
+        tc::mbar_init(&barP, 1);
+        tc::mbar_init(&barR[0], 1);
+        tc::mbar_init(&barR[1], 1);
+        tc::fence_mbar_init();
+    }
+    __syncthreads();  // barriers initialised
+    if (prod) {
+        load_w(0);
+        load_q(0);
+        load_k(0);
+        load_p(0);
+        load_raw(0);
+        if (d.NC > 1) load_raw(1);
+    }
+    // this thread's U^T values of the current chunk (steps 32 g .. 32 g + 31)
+    float ureg[C / 2];
+    if (epi) {
+        const float* up = U + (bh * d.Tp + g * (C / 2)) * Dv + n0 + r;
+#pragma unroll
+        for (int i = 0; i < C / 2; ++i) ureg[i] = up[(int64_t)i * Dv];
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tb = tmem_sh;
+    const int halfk = Dk / 2;
+    const int64_t sbase = bh * Dk * Dv + n0;
+    bool ok = true;
+    if (epi) {
+        for (int cc = g * halfk; cc < (g + 1) * halfk; cc += 16) {  // initial state -> TMEM
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = p.state0 ? p.state0[sbase + (int64_t)(cc + i) * Dv + r] : 0.f;
+            tc::tmem_st16(tc::tmem_addr(tb, lb, cc), v);
+        }
+        tc::tmem_wait_st();
+        ok = tc::mbar_wait(&barR[0], 0, &g_err_scanta);
+        ok = tc::mbar_wait(&barQ, 0, &g_err_scanta) && ok;
+        vectors_from_raw(sm + L.raw, reinterpret_cast<float*>(sm + L.vec), Dk);
+        scale_q(sm + L.Q, sm + L.raw, Dk);
+        tc::fence_async_smem();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+
+    const tc::Tile tW = tc::panel_tile(sm + L.W, C, true);     // B = W^T: x = dk = K
+    const tc::Tile tQ = tc::panel_tile(sm + L.Q, C, true);     // B = Qs^T
+    const tc::Tile tP = tc::panel_tile(sm + L.P, C, true);     // B = P^T: x = s = K
+    const tc::Tile tKmn = tc::panel_tile(sm + L.K, C, false);  // B = K: x = dk = N
+    uint32_t phase = 0;
+
+    for (int64_t c = 0; c < d.NC; ++c) {
+        const float* vb = reinterpret_cast<const float*>(sm + L.vec) + (c & 1) * 4 * C;
+        const float* kev = vb + 3 * C;
+        const float gC = vb[C - 1];
+        const uint32_t ocol = TC.o0 + (uint32_t)(c & 1) * 64u;
+        if (storer) {  // Delta images of chunk c - 1, staged before the barrier above
+            if (c > 0) store_delta(c - 1);
+            tc::bulk_commit();
+        }
+        // step 1: S^T -> A operand (bf16 pairs in TMEM); S^T *= gam_63
+        if (epi) {
+            for (int cb = g * halfk; cb < (g + 1) * halfk; cb += 32) {
+                float v[2][16];
+                tc::tmem_ld16(tc::tmem_addr(tb, lb, cb), v[0]);
+                tc::tmem_ld16(tc::tmem_addr(tb, lb, cb + 16), v[1]);
+                tc::tmem_wait_ld();
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    w[i] = tc::pack_bf16(v[0][2 * i], v[0][2 * i + 1]);
+                    w[8 + i] = tc::pack_bf16(v[1][2 * i], v[1][2 * i + 1]);
+                }
+                tc::tmem_st16u(tc::tmem_addr(tb, lb, TC.aop + cb / 2), w);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    v[0][i] *= gC;
+                    v[1][i] *= gC;
+                }
+                tc::tmem_st16(tc::tmem_addr(tb, lb, cb), v[0]);
+                tc::tmem_st16(tc::tmem_addr(tb, lb, cb + 16), v[1]);
+            }
+            tc::tmem_wait_st();
+        }
+        if (storer) tc::bulk_wait_read_but1();  // checkpoint / output staging read out
+        tc::tc_fence_before();
+        __syncthreads();  // (B)
+        tc::tc_fence_after();
+        uint32_t hiw[16], low[16];
+        if (prod) {
+            // step 2: Delta^T acc = S^T W^T and O^T = S^T Qs^T, two independent
+            // accumulation chains interleaved
+            ok = tc::mbar_wait(&barW, (uint32_t)(c & 1), &g_err_scanta) && ok;
+            const uint32_t id = tc::idesc_bf16(DVT, C, false, false);
+            for (int k = 0; k < Dk; k += 16) {
+                tc::mma_bf16_ta(tb + TC.dacc, tb + TC.aop + k / 2, tW.desc(k), id, k > 0);
+                tc::mma_bf16_ta(tb + ocol, tb + TC.aop + k / 2, tQ.desc(k), id, k > 0);
+            }
+            tc::mma_commit(&bar);
+            ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
+            phase ^= 1u;
+            if (c + 1 < d.NC) {
+                load_w(c + 1);
+                load_q(c + 1);
+            }
+        } else if (epi) {
+            // meanwhile: the checkpoint image (S^T bf16, from the A operand) and
+            // the output rows of chunk c - 1
+            for (int cb = g * (Dk / 4); cb < (g + 1) * (Dk / 4); cb += 16) {
+                uint32_t w[16];
+                tc::tmem_ld16u(tc::tmem_addr(tb, lb, TC.aop + cb), w);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    *reinterpret_cast<uint4*>(sm + L.St + tc::panel_off(2 * cb + 8 * q4, r, DVT)) =
+                        make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+            }
+            if (c > 0) step5(tb, c - 1);
+            tc::fence_async_smem();
+            ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
+            phase ^= 1u;
+            tc::tc_fence_after();
+            // step 3: Delta^T = U^T - acc -> A operands hi, lo and (diag(e r_k)) hi, lo
+            float a[2][16];
+            tc::tmem_ld16(tc::tmem_addr(tb, lb, TC.dacc + 32 * g), a[0]);
+            tc::tmem_ld16(tc::tmem_addr(tb, lb, TC.dacc + 32 * g + 16), a[1]);
+            tc::tmem_wait_ld();
+            uint32_t dew[16], delw[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float dl[2], lo[2], de[2], dlo[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int ti = 2 * i + u;  // step 32 g + ti
+                    dl[u] = ureg[ti] - a[ti >> 4][ti & 15];
+                    lo[u] = dl[u] - __bfloat162float(__float2bfloat16_rn(dl[u]));
+                    de[u] = dl[u] * kev[32 * g + ti];
+                    dlo[u] = de[u] - __bfloat162float(__float2bfloat16_rn(de[u]));
+                }
+                hiw[i] = tc::pack_bf16(dl[0], dl[1]);
+                low[i] = tc::pack_bf16(lo[0], lo[1]);
+                dew[i] = tc::pack_bf16(de[0], de[1]);
+                delw[i] = tc::pack_bf16(dlo[0], dlo[1]);
+            }
+            tc::tmem_st16u(tc::tmem_addr(tb, lb, TC.aop + 16 * g), hiw);
+            tc::tmem_st16u(tc::tmem_addr(tb, lb, TC.aop + 32 + 16 * g), low);
+            tc::tmem_st16u(tc::tmem_addr(tb, lb, TC.aop + 64 + 16 * g), dew);
+            tc::tmem_st16u(tc::tmem_addr(tb, lb, TC.aop + 96 + 16 * g), delw);
+            tc::tmem_wait_st();
+        }
+        if (storer) tc::bulk_wait_read_all();  // Delta staging of c - 1 read out
+        tc::tc_fence_before();
+        __syncthreads();  // (C)
+        tc::tc_fence_after();
+        if (prod) {
+            // step 4: O^T += Delta^T P^T (hi, lo);  S^T += (Delta^T diag(e r_k)) K (hi, lo)
+            ok = tc::mbar_wait(&barP, (uint32_t)(c & 1), &g_err_scanta) && ok;
+            ok = tc::mbar_wait(&barK, (uint32_t)(c & 1), &g_err_scanta) && ok;
+            const uint32_t idp = tc::idesc_bf16(DVT, C, false, false);
+            const uint32_t idk = tc::idesc_bf16(DVT, Dk, false, true);
+            for (int i = 0; i < 8; ++i) {
+                const int k = (i & 3) * 16;
+                const uint32_t hl = (uint32_t)(i >> 2) * 32u;
+                tc::mma_bf16_ta(tb + ocol, tb + TC.aop + hl + k / 2, tP.desc(k), idp, 1u);
+                tc::mma_bf16_ta(tb, tb + TC.aop + 64 + hl + k / 2, tKmn.desc(k), idk, 1u);
+            }
+            tc::mma_commit(&bar);
+            ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
+            phase ^= 1u;
+            if (c + 1 < d.NC) {
+                load_k(c + 1);
+                load_p(c + 1);
+            }
+            if (c + 2 < d.NC) load_raw(c + 2);
+        } else if (epi) {
+            if (storer) {
+                store_ck(c);
+                if (c > 0) store_o(c - 1);
+                tc::bulk_commit();
+            }
+            // meanwhile: Delta image staging, U / vectors / scaled q of chunk c + 1
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const uint32_t off = canon(32 * g + 8 * q4, r, C);
+                *reinterpret_cast<uint4*>(sm + L.Dt + off) =
+                    make_uint4(hiw[4 * q4], hiw[4 * q4 + 1], hiw[4 * q4 + 2], hiw[4 * q4 + 3]);
+                *reinterpret_cast<uint4*>(sm + L.Dlo + off) =
+                    make_uint4(low[4 * q4], low[4 * q4 + 1], low[4 * q4 + 2], low[4 * q4 + 3]);
+            }
+            if (c + 1 < d.NC) {
+                const float* up = U + (bh * d.Tp + (c + 1) * C + g * (C / 2)) * Dv + n0 + r;
+#pragma unroll
+                for (int i = 0; i < C / 2; ++i) ureg[i] = up[(int64_t)i * Dv];
+                const uint8_t* raw = sm + L.raw + ((c + 1) & 1) * kRawBytes;
+                ok = tc::mbar_wait(&barR[(c + 1) & 1], (uint32_t)(((c + 1) >> 1) & 1), &g_err_scanta) && ok;
+                vectors_from_raw(raw, reinterpret_cast<float*>(sm + L.vec) + ((c + 1) & 1) * 4 * C, Dk);
+                ok = tc::mbar_wait(&barQ, (uint32_t)((c + 1) & 1), &g_err_scanta) && ok;
+                scale_q(sm + L.Q, raw, Dk);
+            }
+            tc::fence_async_smem();
+            ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
+            phase ^= 1u;
+            tc::tc_fence_after();
+        }
+        // before the last chunk's output rows are staged: all stores have read out
+        if (storer && c + 1 == d.NC) tc::bulk_wait_read_all();
+        tc::tc_fence_before();
+        __syncthreads();  // (A) of chunk c + 1
+        tc::tc_fence_after();
+    }
+    // the last chunk's output rows and Delta images
+    if (epi) step5(tb, d.NC - 1);
+    tc::fence_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (storer) {
+        store_delta(d.NC - 1);
+        store_o(d.NC - 1);
+        tc::bulk_commit();
+    }
+    if (epi) {
+        for (int cc = g * halfk; cc < (g + 1) * halfk; cc += 16) {
+            float v[16];
+            tc::tmem_ld16(tc::tmem_addr(tb, lb, cc), v);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) p.state_T[sbase + (int64_t)(cc + i) * Dv + r] = v[i];
+        }
+    }
+    if (storer) tc::bulk_wait_all();
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tb, 512);
+}
+
+}  // namespace
+
+bool scan_ta_supported(const Dims& d) {
+    return d.dtype == 1 && d.Dv % DVT == 0 && d.Dk % 64 == 0 && d.Dk >= 64 && d.Dk <= 192 &&
+           ta_plan((int)d.Dk).total + 2048 <= 227u * 1024u;
+}
+
+cudaError_t launch_fwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    const size_t smem = ta_plan((int)d.Dk).total + 1024;
+    auto kern = fwd_scan_ta_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);
+    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps);
+    count_launches(1);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace gdn

@@ -692,6 +692,7 @@ bool scan_tc_supported(const Dims& d) {
 }
 
 cudaError_t launch_fwd_scan_tc(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    if (scan_ta_supported(d) && p.tmaps) return launch_fwd_scan_ta(d, p, s);
     return scan_dvt(d) == 128 ? launch_scan<128>(d, p, s, true) : launch_scan<64>(d, p, s, true);
 }
 

@@ -147,6 +147,29 @@ __global__ void __launch_bounds__(128) selftest_mma_ta_kernel(int N, int K, int 
     if (warp == 0) tc::tmem_dealloc(tbase, 512);
 }
 
+// One TMA tile load through a row-tile tensor map, copied back verbatim.
+__global__ void __launch_bounds__(128) selftest_tma_kernel(const __grid_constant__ CUtensorMap map,
+                                                           int b, int t0, int h, int xg0, int cols,
+                                                           uint8_t* __restrict__ out) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ uint64_t bar;
+    const int tid = threadIdx.x;
+    const uint32_t bytes = (uint32_t)(kChunk * cols * 2);
+    if (tid == 0) {
+        tc::mbar_init(&bar, 1);
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        tc::mbar_arrive_expect_tx(&bar, bytes);
+        tc::tma_load_5d(smem, &map, 0, t0, xg0, h, b, &bar);
+    }
+    const bool ok = tc::mbar_wait(&bar, 0, &g_err_selftest);
+    if (ok)
+        for (uint32_t e = tid; e < bytes / 16; e += blockDim.x)
+            reinterpret_cast<uint4*>(out)[e] = reinterpret_cast<const uint4*>(smem)[e];
+}
+
 }  // namespace
 }  // namespace gdn
 
@@ -176,6 +199,24 @@ extern "C" gdn_status gdn_selftest_mma_tmem_a(int N, int K, int b_mn_major, cons
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     kern<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(
         N, K, b_mn_major, static_cast<const __nv_bfloat16*>(A), static_cast<const __nv_bfloat16*>(B), D);
+    gdn::count_launches(1);
+    return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+extern "C" gdn_status gdn_selftest_tma_tile(int64_t B, int64_t T, int64_t H, int64_t D, int cols,
+                                            int b, int t0, int h, int xg0, const void* src,
+                                            void* out, void* stream) {
+    if (!src || !out) return GDN_ERR_INVALID_ARG;
+    if (cols % 8 || cols < 8 || cols > 256 || D % 8 || xg0 < 0 || xg0 * 8 + cols > D)
+        return GDN_ERR_UNSUPPORTED_SHAPE;
+    CUtensorMap m;
+    if (!gdn::encode_row_tile_map(&m, src, B, T, H, D, cols)) return GDN_ERR_CUDA;
+    const size_t smem = (size_t)gdn::kChunk * cols * 2;
+    auto kern = gdn::selftest_tma_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    kern<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(m, b, t0, h, xg0, cols,
+                                                              static_cast<uint8_t*>(out));
     gdn::count_launches(1);
     return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -179,8 +179,36 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// ... all but the most recent committed group
+__device__ __forceinline__ void bulk_wait_read_but1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 // this thread's bulk stores are complete
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// ---- tensor (TMA) loads -----------------------------------------------------------
+// 5-d tiled load of the box at coordinates c0..c4 of the tensor map `map` (the
+// address of a __grid_constant__ kernel parameter) into shared memory; the box
+// bytes complete on *bar (armed by the issuer with arrive_expect_tx)
+__device__ __forceinline__ void tma_load_5d(void* dst, const void* map, int c0, int c1, int c2,
+                                            int c3, int c4, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 3-d tiled store of a box from shared memory to the tensor map's tensor at
+// coordinates c0..c2 (all non-negative; elements past the tensor's extent are
+// not written), tracked in this thread's bulk groups
+__device__ __forceinline__ void tma_store_3d(const void* map, const void* src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
+                 : "memory");
+}
 
 // ---- descriptors -------------------------------------------------------------------
 // shared-memory matrix descriptor, no swizzle, sm_100 version field = 1

@@ -39,6 +39,16 @@ gdn_status gdn_selftest_mma(int M, int N, int K, int a_mn_major, int b_mn_major,
 gdn_status gdn_selftest_mma_tmem_a(int N, int K, int b_mn_major, const void* A, const void* B,
                                    float* D, void* stream);
 
+/* One 64-row tile of a bf16 [B][T][H][D] tensor loaded by TMA through the
+ * library's row-tile tensor map (the path the scans and the gradient kernel use
+ * for q, k, v and dO), copied back verbatim: out receives 64 * cols * 2 bytes in
+ * the panel layout, byte (g * 64 + r) * 16 + 2 i = element (b, t0 + r, h,
+ * 8 (xg0 + g) + i), zero where t0 + r >= T.  cols: multiple of 8 in 8..256.
+ * Enqueued on `stream`. */
+gdn_status gdn_selftest_tma_tile(int64_t B, int64_t T, int64_t H, int64_t D, int cols, int b,
+                                 int t0, int h, int xg0, const void* src, void* out,
+                                 void* stream);
+
 /* Reads and clears the library's device error word (nonzero after a bounded
  * wait inside a kernel gave up).  Synchronises the device. */
 gdn_status gdn_device_error(unsigned int* flag);

@@ -21,6 +21,8 @@ def lib():
     L.gdn_selftest_mma.restype = ctypes.c_int
     L.gdn_selftest_mma_tmem_a.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p] * 4
     L.gdn_selftest_mma_tmem_a.restype = ctypes.c_int
+    L.gdn_selftest_tma_tile.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int] * 5 + [ctypes.c_void_p] * 3
+    L.gdn_selftest_tma_tile.restype = ctypes.c_int
     L.gdn_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     L.gdn_device_error.restype = ctypes.c_int
     return L
@@ -75,6 +77,29 @@ def test_a_from_tmem(lib, bmn, N, K):
     assert rc == 0
     torch.cuda.synchronize()
     torch.testing.assert_close(D, A.float() @ B.float(), rtol=1e-5, atol=1e-4)
+
+
+@pytest.mark.parametrize("B,T,H,D,cols,b,t0,h,xg0", [
+    (2, 200, 3, 192, 192, 1, 128, 2, 0),   # full width, ragged last tile (rows 200.. zero)
+    (1, 64, 1, 64, 64, 0, 0, 0, 0),
+    (2, 130, 4, 256, 128, 0, 64, 3, 16),   # column sub-tile starting at column 128
+    (1, 300, 2, 128, 128, 0, 256, 1, 0),   # 44 valid rows
+])
+def test_tma_row_tile(lib, B, T, H, D, cols, b, t0, h, xg0):
+    g = torch.Generator().manual_seed(B * T + D)
+    x = torch.randn((B, T, H, D), generator=g).to(torch.bfloat16).cuda()
+    out = torch.full((64 * cols,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    rc = lib.gdn_selftest_tma_tile(B, T, H, D, cols, b, t0, h, xg0, ctypes.c_void_p(x.data_ptr()),
+                                   ctypes.c_void_p(out.data_ptr()),
+                                   ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    torch.cuda.synchronize()
+    rows = torch.zeros((64, cols), dtype=torch.bfloat16)
+    nv = max(0, min(64, T - t0))
+    rows[:nv] = x[b, t0:t0 + nv, h, 8 * xg0:8 * xg0 + cols].cpu()
+    # panel layout: [column group][row][8 elements]
+    want = rows.reshape(64, cols // 8, 8).permute(1, 0, 2).reshape(-1)
+    assert torch.equal(out.cpu(), want)
 
 
 def test_no_wait_timeouts(lib):
