@@ -166,6 +166,7 @@ cudaError_t launch_bwd_scan_tc(const Dims& d, const Ptrs& p, cudaStream_t s);
 unsigned int read_clear_error_scantc();
 bool scan_ta_supported(const Dims& d);
 cudaError_t launch_fwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s);
+cudaError_t launch_bwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s);
 unsigned int read_clear_error_scanta();
 bool fwd_chunk_tc_supported(const Dims& d);
 cudaError_t launch_fwd_chunk_tc(const Dims& d, const Ptrs& p, cudaStream_t s);

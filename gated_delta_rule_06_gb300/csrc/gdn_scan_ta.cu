@@ -1,5 +1,5 @@
-// gdn_scan_ta.cu -- the forward chunk scan for 128-row value tiles (M = 128
-// tcgen05 MMAs) with its A operands held in tensor memory.
+// gdn_scan_ta.cu -- the forward and backward chunk scans for 128-row value
+// tiles (M = 128 tcgen05 MMAs) with the state operand held in tensor memory.
 //
 // Same recurrence as gdn_scan_tc.cu (mlx-lm PR "Add gated_delta_update VJP",
 // "What this PR adds" and "Design notes": chunk 64, sequential over chunks):
@@ -18,6 +18,14 @@
 // TMEM columns: [0, Dk) the fp32 state S^T; [Dk, Dk + 128) A operands (S^T as
 // bf16 pairs during step 2, then Delta^T hi | lo | e-scaled hi | lo, 32 each);
 // [Dk + 128, +64) the Delta^T accumulator; then two 64-column output buffers.
+//
+// Backward (reverse over chunks), per chunk with Sbar^T the state cotangent:
+//   A1 = Obar^T P,  A2 = Sbar^T K^T  (Sbar^T as bf16 pairs in TMEM),
+//   Sbar^T <- gam_63 Sbar^T + (Obar^T diag(gam r_q / sqrt(Dk))) Q   (hi + lo),
+//   -Dbar^T = -(A1 + A2 diag(e r_k)),   Sbar^T += (-Dbar^T) W.
+// Obar, q, k tiles by TMA; P and W images by bulk copy; the Sbar'^T and -Dbar^T
+// images written back with bulk stores.  TMEM: [0, Dk) state, [Dk, Dk + 128)
+// Sbar^T bf16 pairs, then A1 and A2 (64 columns each).
 #include "gdn_internal.cuh"
 #include "gdn_tc.cuh"
 
@@ -439,11 +447,337 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
 
+struct TbSmem {
+    uint32_t P, K, Q, W, O, Os, Oslo, St, ND, raw, vec, total;
+};
+
+__host__ __device__ inline TbSmem tb_plan(int Dk) {
+    TbSmem s{};
+    uint32_t o = 0;
+    auto take = [&](uint32_t bytes) {
+        const uint32_t r = o;
+        o += (bytes + 1023u) & ~1023u;
+        return r;
+    };
+    s.P = take(C * C * 2);      // panel images / TMA panel tiles (64 rows)
+    s.K = take(C * Dk * 2);
+    s.Q = take(C * Dk * 2);
+    s.W = take(C * Dk * 2);
+    s.O = take(C * DVT * 2);    // Obar tile, panel (x = value column)
+    s.Os = take(C * DVT * 2);   // Obar diag(gam r_q / sqrt(Dk)), hi and lo, same layout
+    s.Oslo = take(C * DVT * 2);
+    s.St = take(DVT * Dk * 2);  // Sbar'^T image staging (panel, 128 rows)
+    s.ND = take(DVT * C * 2);   // -Dbar^T (canonical, x = step): operand and image
+    s.raw = take(2 * kRawBytes);
+    s.vec = take(2 * 4 * C * 4);
+    s.total = o;
+    return s;
+}
+
+// Obar tile (panel layout, chunk e holds step e % 64) -> Os, Oslo: the tile
+// scaled by gam r_q / sqrt(Dk) of its step, as hi + lo bf16
+__device__ __forceinline__ void build_os(const uint8_t* O, uint8_t* Os, uint8_t* Oslo,
+                                         const uint8_t* raw, int Dk) {
+    const int t = threadIdx.x & (C - 1);
+    const double* G = reinterpret_cast<const double*>(raw);
+    const float* rq = reinterpret_cast<const float*>(raw + C * 8);
+    const float s = expf((float)G[t]) * rq[t] * rsqrtf((float)Dk);
+    for (int e = threadIdx.x; e < C * DVT / 8; e += kThreads) {
+        uint4 u = reinterpret_cast<const uint4*>(O)[e];
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(&u);
+        uint4 hi, lo;
+        uint32_t* hw = reinterpret_cast<uint32_t*>(&hi);
+        uint32_t* lw = reinterpret_cast<uint32_t*>(&lo);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+            const float x = f.x * s, y = f.y * s;
+            hw[i] = tc::pack_bf16(x, y);
+            const float2 hf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hw[i]));
+            lw[i] = tc::pack_bf16(x - hf.x, y - hf.y);
+        }
+        reinterpret_cast<uint4*>(Os)[e] = hi;
+        reinterpret_cast<uint4*>(Oslo)[e] = lo;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads + 32, 1)
+    bwd_scan_ta_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm) {
+    extern __shared__ __align__(1024) uint8_t sm[];
+    __shared__ uint64_t bar, barW, barQ, barK, barP, barO, barR[2];
+    __shared__ uint32_t tmem_sh;
+    const int tile = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
+    const int j = h / (int)d.G;
+    const int Dk = (int)d.Dk, Dv = (int)d.Dv;
+    const int n0 = tile * DVT;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool epi = tid < kThreads;
+    const bool prod = warp == kThreads / 32 && lane == 0;
+    const bool storer = warp == kStoreWarp && lane == 0;
+    const int r = 32 * (warp & 3) + lane;
+    const int g = (tid >> 7) & 1;
+    const uint32_t lb = 32u * (uint32_t)(warp & 3);
+    const TbSmem L = tb_plan(Dk);
+    const uint32_t aop = (uint32_t)Dk, kA1 = (uint32_t)Dk + 128, kA2 = (uint32_t)Dk + 192;
+    const int64_t bh = (int64_t)bb * d.Hv + h;
+    const uint32_t kbytes = (uint32_t)(C * Dk * 2), pbytes = (uint32_t)(C * C * 2);
+    const uint32_t obytes = (uint32_t)(C * DVT * 2);
+    const uint8_t* Wimg = static_cast<const uint8_t*>(p.W);
+    const uint8_t* Pimg = static_cast<const uint8_t*>(p.P);
+    uint8_t* dsimg = reinterpret_cast<uint8_t*>(p.dSck);
+    uint8_t* dbimg = reinterpret_cast<uint8_t*>(p.Dbar);
+    const int64_t NC = d.NC;
+
+    // m = NC - 1 - c counts processed chunks: ring slots and mbarrier parities follow it
+    auto load_w = [&](int64_t c) {
+        tc::mbar_arrive_expect_tx(&barW, kbytes);
+        tc::bulk_g2s(sm + L.W, Wimg + (bh * NC + c) * kbytes, kbytes, &barW);
+    };
+    auto load_p = [&](int64_t c) {
+        tc::mbar_arrive_expect_tx(&barP, pbytes);
+        tc::bulk_g2s(sm + L.P, Pimg + (bh * NC + c) * pbytes, pbytes, &barP);
+    };
+    auto load_kq = [&](int64_t c) {
+        tc::mbar_arrive_expect_tx(&barK, kbytes);
+        tc::tma_load_5d(sm + L.K, &tm.k, 0, (int)(c * C), 0, j, bb, &barK);
+        tc::mbar_arrive_expect_tx(&barQ, kbytes);
+        tc::tma_load_5d(sm + L.Q, &tm.q, 0, (int)(c * C), 0, j, bb, &barQ);
+    };
+    auto load_o = [&](int64_t c) {
+        tc::mbar_arrive_expect_tx(&barO, obytes);
+        tc::tma_load_5d(sm + L.O, &tm.dO, 0, (int)(c * C), n0 / 8, h, bb, &barO);
+    };
+    auto load_raw = [&](int64_t c) {
+        const int s = (int)((NC - 1 - c) & 1);
+        uint8_t* dst = sm + L.raw + s * kRawBytes;
+        tc::mbar_arrive_expect_tx(&barR[s], kRawBytes);
+        tc::bulk_g2s(dst, p.gam + bh * d.Tp + c * C, C * 8, &barR[s]);
+        tc::bulk_g2s(dst + C * 8, p.rq + ((int64_t)bb * d.Hk + j) * d.Tp + c * C, C * 4, &barR[s]);
+        tc::bulk_g2s(dst + C * 12, p.rk + ((int64_t)bb * d.Hk + j) * d.Tp + c * C, C * 4, &barR[s]);
+    };
+    auto store_images = [&](int64_t c) {  // storer; the caller commits
+        uint8_t* img = dsimg + (bh * NC + c) * (int64_t)Dk * Dv * 2;
+        if (DVT == Dv) {
+            tc::bulk_s2g(img, sm + L.St, (uint32_t)(DVT * Dk * 2));
+        } else {
+            for (int gi = 0; gi < Dk / 8; ++gi)
+                tc::bulk_s2g(img + (size_t)gi * Dv * 16 + (size_t)n0 * 16, sm + L.St + gi * DVT * 16,
+                             (uint32_t)(DVT * 16));
+        }
+        tc::bulk_s2g(dbimg + (bh * NC + c) * (int64_t)C * Dv * 2 + (int64_t)n0 * 128, sm + L.ND,
+                     (uint32_t)(DVT * 128));
+    };
+
+    if (warp == 0) {
+        tc::tmem_alloc(&tmem_sh, 512);
+        tc::tmem_relinquish();
+    }
+    if (prod) {
+        tc::mbar_init(&bar, 1);
+        tc::mbar_init(&barW, 1);
+        tc::mbar_init(&barQ, 1);
+        tc::mbar_init(&barK, 1);
+        tc::mbar_init(&barP, 1);
+        tc::mbar_init(&barO, 1);
+        tc::mbar_init(&barR[0], 1);
+        tc::mbar_init(&barR[1], 1);
+        tc::fence_mbar_init();
+    }
+    __syncthreads();  // barriers initialised
+    if (prod) {
+        load_w(NC - 1);
+        load_kq(NC - 1);
+        load_p(NC - 1);
+        load_o(NC - 1);
+        load_raw(NC - 1);
+        if (NC > 1) load_raw(NC - 2);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tb = tmem_sh;
+    const int halfk = Dk / 2;
+    const int64_t sbase = bh * Dk * Dv + n0;
+    bool ok = true;
+    if (epi) {
+        for (int cc = g * halfk; cc < (g + 1) * halfk; cc += 16) {  // final cotangent -> TMEM
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = p.d_state_T ? p.d_state_T[sbase + (int64_t)(cc + i) * Dv + r] : 0.f;
+            tc::tmem_st16(tc::tmem_addr(tb, lb, cc), v);
+        }
+        tc::tmem_wait_st();
+        ok = tc::mbar_wait(&barR[0], 0, &g_err_scanta);
+        ok = tc::mbar_wait(&barO, 0, &g_err_scanta) && ok;
+        vectors_from_raw(sm + L.raw, reinterpret_cast<float*>(sm + L.vec), Dk);
+        build_os(sm + L.O, sm + L.Os, sm + L.Oslo, sm + L.raw, Dk);
+        tc::fence_async_smem();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+
+    const tc::Tile tOmn = tc::panel_tile(sm + L.O, C, false);      // A = Obar^T: x = dv = M
+    const tc::Tile tOsmn = tc::panel_tile(sm + L.Os, C, false);
+    const tc::Tile tOslomn = tc::panel_tile(sm + L.Oslo, C, false);
+    const tc::Tile tPmn = tc::panel_tile(sm + L.P, C, false);      // B = P: x = s = N
+    const tc::Tile tK = tc::panel_tile(sm + L.K, C, true);         // B = K^T: x = dk = K
+    const tc::Tile tQmn = tc::panel_tile(sm + L.Q, C, false);      // B = Q: x = dk = N
+    const tc::Tile tWmn = tc::panel_tile(sm + L.W, C, false);      // B = W: x = dk = N
+    tc::Tile tND;                                                  // A = -Dbar^T: x = t = K
+    tND.base = tc::smem_u32(sm + L.ND);
+    tND.xs = 128;
+    tND.ys = (uint32_t)C * 16u;
+    tND.k_major = true;
+    uint32_t phase = 0;
+
+    for (int64_t c = NC - 1; c >= 0; --c) {
+        const int64_t m = NC - 1 - c;
+        const float* vb = reinterpret_cast<const float*>(sm + L.vec) + (m & 1) * 4 * C;
+        const float* kev = vb + 3 * C;
+        const float gC = vb[C - 1];
+        // step 1: Sbar^T -> A operand (bf16 pairs in TMEM); Sbar^T *= gam_63
+        if (epi) {
+            for (int cb = g * halfk; cb < (g + 1) * halfk; cb += 32) {
+                float v[2][16];
+                tc::tmem_ld16(tc::tmem_addr(tb, lb, cb), v[0]);
+                tc::tmem_ld16(tc::tmem_addr(tb, lb, cb + 16), v[1]);
+                tc::tmem_wait_ld();
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    w[i] = tc::pack_bf16(v[0][2 * i], v[0][2 * i + 1]);
+                    w[8 + i] = tc::pack_bf16(v[1][2 * i], v[1][2 * i + 1]);
+                }
+                tc::tmem_st16u(tc::tmem_addr(tb, lb, aop + cb / 2), w);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    v[0][i] *= gC;
+                    v[1][i] *= gC;
+                }
+                tc::tmem_st16(tc::tmem_addr(tb, lb, cb), v[0]);
+                tc::tmem_st16(tc::tmem_addr(tb, lb, cb + 16), v[1]);
+            }
+            tc::tmem_wait_st();
+        }
+        if (storer) tc::bulk_wait_read_all();  // images of chunk c + 1 read out of St / ND
+        tc::tc_fence_before();
+        __syncthreads();  // (B)
+        tc::tc_fence_after();
+        if (prod) {
+            // step 2: A1 = Obar^T P, A2 = Sbar^T K^T, Sbar^T += Os Q + Oslo Q, with the
+            // three accumulation chains interleaved
+            ok = tc::mbar_wait(&barP, (uint32_t)(m & 1), &g_err_scanta) && ok;
+            ok = tc::mbar_wait(&barK, (uint32_t)(m & 1), &g_err_scanta) && ok;
+            ok = tc::mbar_wait(&barQ, (uint32_t)(m & 1), &g_err_scanta) && ok;
+            const uint32_t id64 = tc::idesc_bf16(DVT, C, true, true);
+            const uint32_t id2 = tc::idesc_bf16(DVT, C, false, false);
+            const uint32_t idq = tc::idesc_bf16(DVT, Dk, true, true);
+            for (int k = 0; k < Dk; k += 16) {
+                tc::mma_bf16_ta(tb + kA2, tb + aop + k / 2, tK.desc(k), id2, k > 0);
+                if (k < C) {
+                    tc::mma_bf16(tb + kA1, tOmn.desc(k), tPmn.desc(k), id64, k > 0);
+                    tc::mma_bf16(tb, tOsmn.desc(k), tQmn.desc(k), idq, 1u);
+                    tc::mma_bf16(tb, tOslomn.desc(k), tQmn.desc(k), idq, 1u);
+                }
+            }
+            tc::mma_commit(&bar);
+            ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
+            phase ^= 1u;
+            if (c > 0) {  // Obar, P, K, Q tiles are free
+                load_o(c - 1);
+                load_p(c - 1);
+                load_kq(c - 1);
+            }
+        } else if (epi) {
+            // meanwhile: the Sbar'^T image (from the A operand)
+            for (int cb = g * (Dk / 4); cb < (g + 1) * (Dk / 4); cb += 16) {
+                uint32_t w[16];
+                tc::tmem_ld16u(tc::tmem_addr(tb, lb, aop + cb), w);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    *reinterpret_cast<uint4*>(sm + L.St + tc::panel_off(2 * cb + 8 * q4, r, DVT)) =
+                        make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
+            }
+            ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
+            phase ^= 1u;
+            tc::tc_fence_after();
+            // step 3: -Dbar^T = -(A1 + A2 diag(e r_k)) -> operand / image tile
+            float a1[2][16], a2[2][16];
+            tc::tmem_ld16(tc::tmem_addr(tb, lb, kA1 + 32 * g), a1[0]);
+            tc::tmem_ld16(tc::tmem_addr(tb, lb, kA1 + 32 * g + 16), a1[1]);
+            tc::tmem_ld16(tc::tmem_addr(tb, lb, kA2 + 32 * g), a2[0]);
+            tc::tmem_ld16(tc::tmem_addr(tb, lb, kA2 + 32 * g + 16), a2[1]);
+            tc::tmem_wait_ld();
+            uint32_t nd[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int t0 = 32 * g + 2 * i;
+                const float x = -(a1[(2 * i) >> 4][(2 * i) & 15] + kev[t0] * a2[(2 * i) >> 4][(2 * i) & 15]);
+                const float y = -(a1[(2 * i + 1) >> 4][(2 * i + 1) & 15] +
+                                  kev[t0 + 1] * a2[(2 * i + 1) >> 4][(2 * i + 1) & 15]);
+                nd[i] = tc::pack_bf16(x, y);
+            }
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+                *reinterpret_cast<uint4*>(sm + L.ND + canon(32 * g + 8 * q4, r, C)) =
+                    make_uint4(nd[4 * q4], nd[4 * q4 + 1], nd[4 * q4 + 2], nd[4 * q4 + 3]);
+            tc::fence_async_smem();
+        }
+        tc::tc_fence_before();
+        __syncthreads();  // (C)
+        tc::tc_fence_after();
+        if (prod) {
+            // step 4: Sbar^T += (-Dbar^T) W
+            ok = tc::mbar_wait(&barW, (uint32_t)(m & 1), &g_err_scanta) && ok;
+            tc::mma_tile(tb, tND, tWmn, DVT, Dk, C, true);
+            tc::mma_commit(&bar);
+            ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
+            phase ^= 1u;
+            if (c > 0) load_w(c - 1);
+            if (c > 1) load_raw(c - 2);
+        } else if (epi) {
+            if (storer) {
+                store_images(c);
+                tc::bulk_commit();
+            }
+            if (c > 0) {  // vectors and the scaled Obar operands of chunk c - 1
+                const uint8_t* raw = sm + L.raw + ((m + 1) & 1) * kRawBytes;
+                ok = tc::mbar_wait(&barR[(m + 1) & 1], (uint32_t)(((m + 1) >> 1) & 1), &g_err_scanta) && ok;
+                vectors_from_raw(raw, reinterpret_cast<float*>(sm + L.vec) + ((m + 1) & 1) * 4 * C, Dk);
+                ok = tc::mbar_wait(&barO, (uint32_t)((m + 1) & 1), &g_err_scanta) && ok;
+                build_os(sm + L.O, sm + L.Os, sm + L.Oslo, raw, Dk);
+                tc::fence_async_smem();
+            }
+            ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
+            phase ^= 1u;
+            tc::tc_fence_after();
+        }
+        tc::tc_fence_before();
+        __syncthreads();  // (A) of chunk c - 1
+        tc::tc_fence_after();
+    }
+    if (epi) {
+        for (int cc = g * halfk; cc < (g + 1) * halfk; cc += 16) {
+            float v[16];
+            tc::tmem_ld16(tc::tmem_addr(tb, lb, cc), v);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) p.dstate0[sbase + (int64_t)(cc + i) * Dv + r] = v[i];
+        }
+    }
+    if (storer) tc::bulk_wait_all();
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tb, 512);
+}
+
 }  // namespace
 
 bool scan_ta_supported(const Dims& d) {
     return d.dtype == 1 && d.Dv % DVT == 0 && d.Dk % 64 == 0 && d.Dk >= 64 && d.Dk <= 192 &&
-           ta_plan((int)d.Dk).total + 2048 <= 227u * 1024u;
+           ta_plan((int)d.Dk).total + 2048 <= 227u * 1024u && tb_plan((int)d.Dk).total + 2048 <= 227u * 1024u;
 }
 
 cudaError_t launch_fwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s) {
@@ -457,4 +791,17 @@ cudaError_t launch_fwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s) {
     return cudaPeekAtLastError();
 }
 
+}  // namespace gdn
+
+namespace gdn {
+cudaError_t launch_bwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    const size_t smem = tb_plan((int)d.Dk).total + 1024;
+    auto kern = bwd_scan_ta_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);
+    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps);
+    count_launches(1);
+    return cudaPeekAtLastError();
+}
 }  // namespace gdn

@@ -697,6 +697,7 @@ cudaError_t launch_fwd_scan_tc(const Dims& d, const Ptrs& p, cudaStream_t s) {
 }
 
 cudaError_t launch_bwd_scan_tc(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    if (scan_ta_supported(d) && p.tmaps) return launch_bwd_scan_ta(d, p, s);
     return scan_dvt(d) == 128 ? launch_scan<128>(d, p, s, false) : launch_scan<64>(d, p, s, false);
 }
 
