@@ -49,7 +49,7 @@ struct Layout {
     // byte offsets into the forward workspace
     size_t U, fwd_total;
     // byte offsets into the backward workspace
-    size_t dSck, Dbar, dqh, dkh, dqh2, dkh2, dl, dbeta, part, bwd_total;
+    size_t dSck, Dbar, dqh, dkh, dl, dbeta, part, bwd_total;
 };
 
 bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -106,8 +106,6 @@ Layout make_layout(const gdn::Dims& d) {
     L.Dbar = o; o = align_up(o + perstep * d.Dv * img);
     L.dqh = o; o = align_up(o + perstep * d.Dk * 4);
     L.dkh = o; o = align_up(o + perstep * d.Dk * 4);
-    L.dqh2 = o; o = align_up(o + perstep * d.Dk * 4);
-    L.dkh2 = o; o = align_up(o + perstep * d.Dk * 4);
     L.dl = o; o = align_up(o + perstep * 4);
     L.dbeta = o; o = align_up(o + perstep * 4);
     L.part = o; o = align_up(o + 2 * (size_t)d.B * d.NC * d.Hv * 4);
@@ -332,9 +330,6 @@ gdn_status gdn_backward(const gdn_shape* shape, const void* q, const void* k, co
     p.Dbar = reinterpret_cast<float*>(w + L.Dbar);
     p.dqh = reinterpret_cast<float*>(w + L.dqh);
     p.dkh = reinterpret_cast<float*>(w + L.dkh);
-    p.dqh2 = reinterpret_cast<float*>(w + L.dqh2);
-    p.dkh2 = reinterpret_cast<float*>(w + L.dkh2);
-    p.dq_parts = gdn::tc_path(d) ? 2 : 1;
     p.dl = reinterpret_cast<float*>(w + L.dl);
     p.dbeta = reinterpret_cast<float*>(w + L.dbeta);
     p.part = reinterpret_cast<float*>(w + L.part);

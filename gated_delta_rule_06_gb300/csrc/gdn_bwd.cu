@@ -418,7 +418,6 @@ __global__ void __launch_bounds__(256) bwd_qk_kernel(Dims d, Ptrs p) {
     for (int pass = 0; pass < 2; ++pass) {
         const TI* x = (const TI*)(pass == 0 ? p.q : p.k) + xoff;
         const float* src = pass == 0 ? p.dqh : p.dkh;
-        const float* src2 = pass == 0 ? p.dqh2 : p.dkh2;
         const float r = (pass == 0 ? p.rq : p.rk)[(bb * d.Hk + j) * d.Tp + t];
         const float s = pass == 0 ? rsqrtf((float)Dk) : 1.f;
         float y[8], u[8];
@@ -433,7 +432,6 @@ __global__ void __launch_bounds__(256) bwd_qk_kernel(Dims d, Ptrs p) {
                     const int64_t h = j * d.G + g;
                     const int64_t off = ((bb * d.Hv + h) * d.Tp + t) * Dk + col;
                     y[m] += src[off];
-                    if (p.dq_parts == 2) y[m] += src2[off];
                 }
                 u[m] = ldf(x + col) * r;
                 dot = fmaf(u[m], y[m], dot);

@@ -6,14 +6,15 @@
 // VJP", "What this PR adds" and "Scope and follow-ups").  One CTA per
 // (chunk, value head, batch); every product has 64 rows as its M dimension
 // (M = 64 MMAs, accumulator row r in TMEM lane 32 (r / 16) + r % 16):
-//   phase 0:  Pbar = Obar Delta^T,  Dbar V^T,  Y = T^T Dbar,  K K^T,  Q K^T
+//   phase 0:  Pbar = Obar Delta^T,  Dbar V^T,  Y = T^T Dbar
 //   phase 1:  per 32-wide block of Dk:  Obar S^T,  Wbar = -Dbar S^T,  Delta Sbar'^T
-//   phase 1b: Wbar K^T,  Z = T^T Wbar
-//   phase 2:  X = Tbar T^T,  Abar = -T^T X,  then the gate / log-decay cotangents
-//             element-wise in fp32 (fp64 for the cancelling row / column sums)
-//   phase 3:  (Pbar o M) K  and  diag(beta gam) Z + (Pbar o M)^T Q + (Gb + Gb^T) K,
-//             accumulated in TMEM and stored to second dq / dk buffers that the
-//             reduction adds (no read-modify-write of global memory)
+//   phase 1b: Wbar K^T,  diag(beta gam) T^T Wbar,  K K^T
+//   phase 2:  X = Tbar T^T,  Q K^T,  Abar = -T^T X,  then the gate / log-decay
+//             cotangents element-wise in fp32 (fp64 for the cancelling sums)
+//   phase 3:  (Pbar o M) K  and  (Pbar o M)^T Q + (Gb + Gb^T) K
+// The cotangents of the normalised q and k rows accumulate in TMEM from
+// phase 1 on (the state products of phase 1, rescaled in place, then Z and
+// the phase-3 products on top) and are stored once at the end.
 // Delta (a cancelling difference) enters as two bf16 terms (hi + lo).  q and k
 // are staged as the exact bf16 inputs; the norms r_q, r_k (and 1/sqrt(Dk)) are
 // applied in fp32 in the epilogues or folded into the other operand, so the
@@ -34,16 +35,19 @@ namespace {
 constexpr int C = kChunk;
 constexpr int kThreads = 256;
 constexpr int kBlkK = 32;  // Dk block of the state products
-// TMEM column map
-constexpr uint32_t kColGkk = 384, kColGqk = 448;
+// TMEM column map (Dk <= 192): scratch S1 = [0, 64); dk accumulator AK = [64, 64 + Dk);
+// dq accumulator AQ = [64 + Dk, 64 + 2 Dk); scratch S2 = 64 columns from
+// 64 + max(2 Dk, Dv).  Phase 0 parks Y (Dv <= 256 columns) at 64, before AK /
+// AQ are live.
+constexpr uint32_t kS1 = 0, kAK = 64;
 // fp32 64 x 64 scratch matrices are row-padded to 65 floats: epilogue lanes own
 // rows, and an unpadded 256-byte row stride puts every lane in one bank
 constexpr int LDM = C + 1;
 
 struct Smem {
     // byte offsets inside dynamic shared memory
-    uint32_t K, Q, W, R1, O, D, Dlo, NB, V, S, Sp, Gkk, Gqk, Tbh, Xh, PMk, PMq, Hk, Tt, Pf, Tbf,
-        vec, total;
+    uint32_t K, Q, W, R1, O, D, Dlo, NB, V, S, Sp, Gkk, Gqk, Tbh, Xh, PMk, PMq, Hk, Tsc, Tt, Pf,
+        Tbf, vec, total;
 };
 
 __host__ __device__ inline Smem smem_plan(int Dk, int Dv) {
@@ -60,7 +64,7 @@ __host__ __device__ inline Smem smem_plan(int Dk, int Dv) {
     s.W = take(tk);
     // region R1: Dv-wide operands of phases 0-1, then phase-2/3 scratch
     const uint32_t r1_ops = 5 * tv + 2 * (tv / 2);
-    const uint32_t r1_late = 2 * f64x64 + 5 * t64;
+    const uint32_t r1_late = 2 * f64x64 + 6 * t64;
     s.R1 = take(r1_ops > r1_late ? r1_ops : r1_late);
     s.O = s.R1;
     s.D = s.O + tv;
@@ -76,6 +80,7 @@ __host__ __device__ inline Smem smem_plan(int Dk, int Dv) {
     s.PMk = s.Xh + t64;
     s.PMq = s.PMk + t64;
     s.Hk = s.PMq + t64;
+    s.Tsc = s.Hk + t64;      // diag(beta gam)-scaled T image
     s.Tt = take(t64);
     s.Pf = take(f64x64);
     s.Tbf = take(f64x64);
@@ -168,6 +173,45 @@ __device__ __forceinline__ void acc_rows(uint32_t tbase, uint32_t col0, int ncol
     }
 }
 
+// As acc_rows, and the (modified) values are written back in place.  Lanes
+// 16..31 write TMEM lanes that an M = 64 accumulator does not use.
+template <typename F>
+__device__ __forceinline__ void acc_rows_rw(uint32_t tbase, uint32_t col0, int ncols, F&& f) {
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    const int sp = w & 3, g = w >> 2;
+    const int half = ncols / 2;
+    for (int c = g * half; c < (g + 1) * half; c += 16) {
+        float v[16];
+        const uint32_t ta = tc::tmem_addr(tbase, 32 * sp, col0 + c);
+        tc::tmem_ld16(ta, v);
+        tc::tmem_wait_ld();
+        if (l < 16) f(16 * sp + l, c, v);
+        tc::tmem_st16(ta, v);
+    }
+    tc::tmem_wait_st();
+}
+// M = 64 accumulator walk with all 32 lanes: lane l < 16 takes columns c .. c + 7
+// of row 16 (w % 4) + l, lane l + 16 columns c + 8 .. c + 15 of the same row
+// (handed over by shuffles); f(row, first column, 8 values, lane half)
+template <typename F>
+__device__ __forceinline__ void acc_rows_all(uint32_t tbase, uint32_t col0, int ncols, F&& f) {
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    const int sp = w & 3, g = w >> 2, hl = l >> 4;
+    const int half = ncols / 2;
+    for (int c = g * half; c < (g + 1) * half; c += 16) {
+        float v[16];
+        tc::tmem_ld16(tc::tmem_addr(tbase, 32 * sp, col0 + c), v);
+        tc::tmem_wait_ld();
+        float x[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float up = __shfl_sync(0xffffffffu, v[8 + i], l & 15);
+            x[i] = hl ? up : v[i];
+        }
+        f(16 * sp + (l & 15), c + 8 * hl, x, hl);
+    }
+}
+
 __device__ __forceinline__ void sync_after_mma(uint64_t* bar, uint32_t& phase, bool& ok) {
     ok = tc::mbar_wait(bar, phase, &g_err_bwdtc) && ok;
     phase ^= 1u;
@@ -199,8 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     float* ee = gq + 2 * C;      // [2][64] ebar * e
     float* bb0 = ee + 2 * C;     // [2][64] betabar (Y . V)
     float* zk = bb0 + 2 * C;     // [2][64] Z . K
-    float* sbp = zk + 2 * C;     // [2][64] sum_j Abar M Gkk
-    float* betab = sbp + 2 * C;  // [64]
+    float* sbp = zk + 2 * C;     // [4][64] sum_j Abar M Gkk
+    float* betab = sbp + 4 * C;  // [64]
     float* red = betab + C;      // [256]
     // Gamma as an unevaluated sum hi + lo of two floats: for steps i, j whose
     // Gamma are within a factor of two (the only case where exp(Gamma_i - Gamma_j)
@@ -208,9 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     // accuracy without fp64 arithmetic
     float* Ghi = red + 256;     // [64]
     float* Glo = Ghi + C;       // [64]
-    float* rsp = Glo + C;       // [2][64] row sums of Mbar o M (compensated)
-    float* rsc = rsp + 2 * C;   // [2][64] their compensation terms
-    float* csp = rsc + 2 * C;   // [4][64] column sums (compensated, folded)
+    float* rsp = Glo + C;       // [4][64] row sums of Mbar o M (compensated)
+    float* rsc = rsp + 4 * C;   // [4][64] their compensation terms
+    float* csp = rsc + 4 * C;   // [4][64] column sums (compensated, folded)
     double* gam_bar = reinterpret_cast<double*>(csp + 4 * C);  // [64]
 
     const int64_t t0 = (int64_t)c * C;
@@ -274,8 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
         rqv[tid] = p.rq[rbase + tid] * rsqrtf((float)Dk);
         rkv[tid] = p.rk[rbase + tid];
     }
-    for (int i = tid; i < 10 * C; i += blockDim.x) gq[i] = 0.f;  // gq, ee, bb0, zk, sbp
-    for (int i = tid; i < 4 * C; i += blockDim.x) rsp[i] = 0.f;  // rsp, rsc
+    for (int i = tid; i < 12 * C; i += blockDim.x) gq[i] = 0.f;  // gq, ee, bb0, zk, sbp
+    for (int i = tid; i < 8 * C; i += blockDim.x) rsp[i] = 0.f;  // rsp, rsc
     tc::cp_async_wait_all();
     tc::fence_async_smem();
     cta_sync_tc();
@@ -292,35 +336,36 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     // T image: panel layout, x = column j
     const tc::Tile tTt = tc::panel_tile(sm + L.Tt, C, true), tTmn = tc::panel_tile(sm + L.Tt, C, false);
 
-    // ---- phase 0: Pbar = Obar Delta^T | -Dbar V^T | -T^T Dbar | K K^T | Q K^T
+    // S2 also clears Y (Dv columns from kAK) of phase 0
+    const uint32_t kAQ = kAK + (uint32_t)Dk, kS2 = kAK + (uint32_t)(2 * Dk > Dv ? 2 * Dk : Dv);
+
+    // ---- phase 0: Pbar = Obar Delta^T | -Dbar V^T | -T^T Dbar
     if (tid == 0) {
-        tc::mma_tile(tb + 0, tO, tDmn, C, C, Dv, false);
-        tc::mma_tile(tb + 0, tO, tDlomn, C, C, Dv, true);
-        tc::mma_tile(tb + 64, tNBmn, tV, C, C, Dv, false);
-        tc::mma_tile(tb + 128, tTmn, tNB, C, Dv, C, false);
-        tc::mma_tile(tb + kColGkk, tK, tK, C, C, Dk, false);
-        tc::mma_tile(tb + kColGqk, tQ, tK, C, C, Dk, false);
+        tc::mma_tile(tb + kS1, tO, tDmn, C, C, Dv, false);
+        tc::mma_tile(tb + kS1, tO, tDlomn, C, C, Dv, true);
+        tc::mma_tile(tb + kS2, tNBmn, tV, C, C, Dv, false);
+        tc::mma_tile(tb + kAK, tTmn, tNB, C, Dv, C, false);
         tc::mma_commit(&bar);
     }
     sync_after_mma(&bar, phase, ok);
     float* Pf = reinterpret_cast<float*>(sm + L.Pf);
     float* Tbf = reinterpret_cast<float*>(sm + L.Tbf);
     if (ok) {
-        acc_rows(tb, 0, C, [&](int r, int c0, const float (&x)[16]) {
+        acc_rows(tb, kS1, C, [&](int r, int c0, const float (&x)[16]) {
             float m[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) m[i] = (c0 + i <= r) ? x[i] : 0.f;
 #pragma unroll
             for (int i = 0; i < 16; ++i) Pf[r * LDM + c0 + i] = m[i];
         });
-        acc_rows(tb, 64, C, [&](int r, int c0, const float (&x)[16]) {
+        acc_rows(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
             float m[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) m[i] = -bt[c0 + i] * x[i];
 #pragma unroll
             for (int i = 0; i < 16; ++i) Tbf[r * LDM + c0 + i] = m[i];
         });
-        acc_rows(tb, 128, Dv, [&](int r, int c0, const float (&x)[16]) {
+        acc_rows(tb, kAK, Dv, [&](int r, int c0, const float (&x)[16]) {
             float vv[16], y[16];
             tile_row16(sm + L.V, Dv, c0, r, vv);
             float s = 0.f;
@@ -340,8 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     }
 
     // ---- phase 1: state products per kBlkK-wide block of Dk; block b + 1 streams
-    // into the other buffer while block b's products and epilogues run.  <S, Sbar'>
-    // (the chunk-end term of the log-decay cotangent) is summed from the same tiles.
+    // into the other buffer while block b's products and epilogues run.  Obar S^T
+    // and Delta Sbar'^T land in the dq / dk accumulators and are rescaled there by
+    // gam and e.  <S, Sbar'> (the chunk-end term of the log-decay cotangent) is
+    // summed from the same tiles.
     float gcb = 0.f;
     const int nblk = Dk / kBlkK;
     for (int b = 0; b < nblk; ++b) {
@@ -360,51 +407,59 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
         // S / Sbar' blocks: panel layout over Dv rows, x = dk (the N dimension)
         const tc::Tile tS = tc::panel_tile(sS, Dv, false), tSp = tc::panel_tile(sS + blk, Dv, false);
         if (tid == 0) {
-            tc::mma_tile(tb + 0, tO, tS, C, nk, Dv, false);
-            tc::mma_tile(tb + 64, tNBmn, tS, C, nk, Dv, false);
-            tc::mma_tile(tb + 128, tDmn, tSp, C, nk, Dv, false);
-            tc::mma_tile(tb + 128, tDlomn, tSp, C, nk, Dv, true);
+            tc::mma_tile(tb + kAQ + dk0, tO, tS, C, nk, Dv, false);
+            tc::mma_tile(tb + kS1, tNBmn, tS, C, nk, Dv, false);
+            tc::mma_tile(tb + kAK + dk0, tDmn, tSp, C, nk, Dv, false);
+            tc::mma_tile(tb + kAK + dk0, tDlomn, tSp, C, nk, Dv, true);
             tc::mma_commit(&bar);
         }
         sync_after_mma(&bar, phase, ok);
         if (ok) {
-            acc_rows(tb, 0, nk, [&](int r, int c0, const float (&x)[16]) {
-                float y[16], qq[16];
+            acc_rows_rw(tb, kAQ + dk0, nk, [&](int r, int c0, float (&x)[16]) {
+                float qq[16];
                 tile_row16(sm + L.Q, Dk, dk0 + c0, r, qq);
                 float s = 0.f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    y[i] = gm[r] * x[i];
-                    s = fmaf(y[i], qq[i], s);
+                    x[i] *= gm[r];
+                    s = fmaf(x[i], qq[i], s);
                 }
-                st16f(p.dqh + (gbase + r) * Dk + dk0 + c0, y);
                 gq[g * C + r] += s;
             });
-            acc_rows(tb, 64, nk, [&](int r, int c0, const float (&x)[16]) {
+            acc_rows(tb, kS1, nk, [&](int r, int c0, const float (&x)[16]) {
                 tile_put16(sm + L.W, Dk, dk0 + c0, r, x);
             });
-            acc_rows(tb, 128, nk, [&](int r, int c0, const float (&x)[16]) {
-                float y[16], kk[16];
+            acc_rows_rw(tb, kAK + dk0, nk, [&](int r, int c0, float (&x)[16]) {
+                float kk[16];
                 tile_row16(sm + L.K, Dk, dk0 + c0, r, kk);
                 float s = 0.f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    y[i] = ev[r] * x[i];
-                    s = fmaf(y[i], kk[i], s);
+                    x[i] *= ev[r];
+                    s = fmaf(x[i], kk[i], s);
                 }
-                st16f(p.dkh + (gbase + r) * Dk + dk0 + c0, y);
                 ee[g * C + r] += s;
             });
         }
     }
     red[tid] = gcb;
-    tc::fence_async_smem();  // Wbar tile written by generic stores -> MMA operand
+    // diag(beta gam) T^T as an operand: T image columns scaled by beta gam
+    for (int e = tid; e < C * (C / 8); e += kThreads) {
+        const int j0 = (e / C) * 8;  // panel chunk e: row e % 64, columns j0 .. j0 + 7
+        float t8[8];
+        ld_bf16x8(sm + L.Tt + 16 * e, t8);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t8[i] *= bt[j0 + i] * gm[j0 + i];
+        st_bf16x8(sm + L.Tsc + 16 * e, t8);
+    }
+    tc::fence_async_smem();  // Wbar and scaled-T tiles written by generic stores -> MMA operands
     cta_sync_tc();
 
-    // ---- phase 1b: Wbar K^T | Z = T^T Wbar
+    // ---- phase 1b: Wbar K^T | dk += diag(beta gam) T^T Wbar | K K^T
     if (tid == 0) {
-        tc::mma_tile(tb + 0, tW, tK, C, C, Dk, false);
-        tc::mma_tile(tb + 64, tTmn, tWmn, C, Dk, C, false);
+        tc::mma_tile(tb + kS1, tW, tK, C, C, Dk, false);
+        tc::mma_tile(tb + kAK, tc::panel_tile(sm + L.Tsc, C, false), tWmn, C, Dk, C, true);
+        tc::mma_tile(tb + kS2, tK, tK, C, C, Dk, false);
         tc::mma_commit(&bar);
     }
     for (int s = blockDim.x / 2; s > 0; s >>= 1) {  // <Sbar', S>, fixed-order tree
@@ -415,57 +470,33 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     sync_after_mma(&bar, phase, ok);
     float* Gkk = reinterpret_cast<float*>(sm + L.Gkk);
     float* Gqk = reinterpret_cast<float*>(sm + L.Gqk);
+    float* ZP = Gqk;  // T o (Wbar K^T), until Gqk is formed in phase 2
     if (ok) {
-        acc_rows(tb, kColGkk, C, [&](int r, int c0, const float (&x)[16]) {
-            float y[16];
+        acc_rows(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) y[i] = rkv[r] * rkv[c0 + i] * x[i];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) Gkk[r * LDM + c0 + i] = y[i];
+            for (int i = 0; i < 16; ++i) Gkk[r * LDM + c0 + i] = rkv[r] * rkv[c0 + i] * x[i];
         });
-        acc_rows(tb, kColGqk, C, [&](int r, int c0, const float (&x)[16]) {
-            float y[16];
+        acc_rows(tb, kS1, C, [&](int r, int c0, const float (&x)[16]) {
+            float tt[16];
+            ld_bf16x8(sm + L.Tt + tc::panel_off(c0, r, C), tt);
+            ld_bf16x8(sm + L.Tt + tc::panel_off(c0 + 8, r, C), tt + 8);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) y[i] = rqv[r] * rkv[c0 + i] * x[i];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) Gqk[r * LDM + c0 + i] = y[i];
-        });
-        acc_rows(tb, 0, C, [&](int r, int c0, const float (&x)[16]) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
+            for (int i = 0; i < 16; ++i) {
                 Tbf[r * LDM + c0 + i] += bt[c0 + i] * gm[c0 + i] * rkv[c0 + i] * x[i];
-        });
-        // Z stays in TMEM, rescaled in place to diag(beta gam) Z: the phase-3
-        // products for dK accumulate on top of it
-        {
-            const int sp = warp & 3, half = Dk / 2;
-            const int r = 16 * sp + lane;
-            for (int c0 = g * half; c0 < (g + 1) * half; c0 += 16) {
-                float x[16];
-                const uint32_t ta = tc::tmem_addr(tb, 32 * sp, 64 + c0);
-                tc::tmem_ld16(ta, x);
-                tc::tmem_wait_ld();
-                if (lane < 16) {
-                    float kk[16];
-                    tile_row16(sm + L.K, Dk, c0, r, kk);
-                    const float sc = bt[r] * gm[r];
-                    float s = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        s = fmaf(x[i], kk[i], s);
-                        x[i] *= sc;
-                    }
-                    zk[g * C + r] += s;
-                }
-                tc::tmem_st16(ta, x);
+                ZP[r * LDM + c0 + i] = tt[i] * x[i];
             }
-            tc::tmem_wait_st();
-        }
+        });
+    }
+    __syncthreads();
+    if (tid < C) {  // <Z_i, k_i> = sum_m T_mi (Wbar K^T)_mi, Z = T^T Wbar (fixed order)
+        float z = 0.f;
+        for (int m = 0; m < C; ++m) z += ZP[m * LDM + tid];
+        zk[tid] = z;
     }
     __syncthreads();
     if (tid < C) {
         const int i = tid;
-        const float z = rkv[i] * (zk[i] + zk[C + i]);  // <Z_i, k_hat_i>
+        const float z = rkv[i] * zk[i];  // <Z_i, k_hat_i>
         betab[i] = bb0[i] + bb0[C + i] + gm[i] * z;
         gq[i] = rqv[i] * (gq[i] + gq[C + i]) + bt[i] * z * gm[i];  // gambar * gam
         ee[i] = rkv[i] * (ee[i] + ee[C + i]);                      // ebar * e
@@ -478,34 +509,41 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     tc::fence_async_smem();
     cta_sync_tc();
 
-    // ---- phase 2: X = Tbar T^T, then Abar' = T^T X (Abar = -Abar')
+    // ---- phase 2: X = Tbar T^T | Q K^T, then Abar' = T^T X (Abar = -Abar')
     if (tid == 0) {
-        tc::mma_tile(tb + 0, kmaj(sm, L.Tbh, C), tTt, C, C, C, false);
+        tc::mma_tile(tb + kS1, kmaj(sm, L.Tbh, C), tTt, C, C, C, false);
+        tc::mma_tile(tb + kS2, tQ, tK, C, C, Dk, false);
         tc::mma_commit(&bar);
     }
     sync_after_mma(&bar, phase, ok);
     if (ok) {
-        acc_rows(tb, 0, C, [&](int r, int c0, const float (&x)[16]) {
+        acc_rows(tb, kS1, C, [&](int r, int c0, const float (&x)[16]) {
             tile_put16(sm + L.Xh, C, c0, r, x);  // X row-major (x = l, y = j)
+        });
+        acc_rows(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Gqk[r * LDM + c0 + i] = rqv[r] * rkv[c0 + i] * x[i];
         });
     }
     tc::fence_async_smem();
     cta_sync_tc();
-    if (tid == 0) {  // columns 0..63 again: X has been read; 64.. hold diag(beta gam) Z
-        tc::mma_tile(tb + 0, tTmn, mnmaj(sm, L.Xh, C), C, C, C, false);
+    if (tid == 0) {
+        tc::mma_tile(tb + kS1, tTmn, mnmaj(sm, L.Xh, C), C, C, C, false);
         tc::mma_commit(&bar);
     }
     sync_after_mma(&bar, phase, ok);
     if (ok) {
         // element-wise: M, Abar, Mbar o M (in place of Gkk), Gb (in place of Gqk),
-        // Pbar o M scaled by r_k (columns) and by r_q (rows) as bf16 operands
-        acc_rows(tb, 0, C, [&](int r, int c0, const float (&x)[16]) {
+        // Pbar o M scaled by r_k (columns) and by r_q (rows) as bf16 operands;
+        // every lane takes 8 columns of a row
+        acc_rows_all(tb, kS1, C, [&](int r, int c0, const float (&x)[8], int hl) {
+            const int pi = 2 * g + hl;
             float sb = 0.f;
-            float rs = rsp[g * C + r], rc = rsc[g * C + r];  // Kahan-compensated row sum
-            float pk[16], pq[16];
+            float rs = rsp[pi * C + r], rc = rsc[pi * C + r];  // Kahan-compensated row sum
+            float pk[8], pq[8];
             const float ghr = Ghi[r], glr = Glo[r];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < 8; ++i) {
                 const int jj = c0 + i;
                 const int idx = r * LDM + jj;
                 const float m = jj <= r ? expf((ghr - Ghi[jj]) + (glr - Glo[jj])) : 0.f;
@@ -524,11 +562,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
                 pk[i] = pm * rkv[jj];
                 pq[i] = pm * rqv[r];
             }
-            tile_put16(sm + L.PMk, C, c0, r, pk);
-            tile_put16(sm + L.PMq, C, c0, r, pq);
-            sbp[g * C + r] += sb;  // two 16-column chunks per thread
-            rsp[g * C + r] = rs;
-            rsc[g * C + r] = rc;
+            st_bf16x8(sm + L.PMk + canon(c0, r, C), pk);
+            st_bf16x8(sm + L.PMq + canon(c0, r, C), pq);
+            sbp[pi * C + r] += sb;  // two 8-column pieces per lane
+            rsp[pi * C + r] = rs;
+            rsc[pi * C + r] = rc;
         });
     }
     __syncthreads();
@@ -555,11 +593,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     tc::fence_async_smem();
     cta_sync_tc();
 
-    // ---- phase 3: dQ += (Pbar o M) K;  dK += (Pbar o M)^T Q + (Gb + Gb^T) K
+    // ---- phase 3: dq += (Pbar o M) K;  dk += (Pbar o M)^T Q + (Gb + Gb^T) K
     if (tid == 0) {
-        tc::mma_tile(tb + 64 + Dk, kmaj(sm, L.PMk, C), tKmn, C, Dk, C, false);
-        tc::mma_tile(tb + 64, mnmaj(sm, L.PMq, C), tQmn, C, Dk, C, true);
-        tc::mma_tile(tb + 64, kmaj(sm, L.Hk, C), tKmn, C, Dk, C, true);
+        tc::mma_tile(tb + kAQ, kmaj(sm, L.PMk, C), tKmn, C, Dk, C, true);
+        tc::mma_tile(tb + kAK, mnmaj(sm, L.PMq, C), tQmn, C, Dk, C, true);
+        tc::mma_tile(tb + kAK, kmaj(sm, L.Hk, C), tKmn, C, Dk, C, true);
         tc::mma_commit(&bar);
     }
     // Gammabar_i = sum_j (Mbar o M)_ij - sum_k (Mbar o M)_ki + gambar_i gam_i - ebar_i e_i,
@@ -567,8 +605,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     // cumulative sum (one warp, fp64, two steps per lane)
     if (tid < C) {
         const int i = tid;
-        betab[i] += sbp[i] + sbp[C + i];
-        const double rows = ((double)rsp[i] - (double)rsc[i]) + ((double)rsp[C + i] - (double)rsc[C + i]);
+        betab[i] += sbp[i] + sbp[C + i] + sbp[2 * C + i] + sbp[3 * C + i];
+        double rows = 0.0;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) rows += (double)rsp[q4 * C + i] - (double)rsc[q4 * C + i];
         const double cols = (double)csp[i] + (double)csp[C + i] + (double)csp[2 * C + i] + (double)csp[3 * C + i];
         gam_bar[i] = rows - cols + (double)gq[i] - (double)ee[i];
     }
@@ -595,11 +635,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     }
     sync_after_mma(&bar, phase, ok);
     if (ok) {
-        acc_rows(tb, 64 + Dk, Dk, [&](int r, int c0, const float (&x)[16]) {
-            st16f(p.dqh2 + (gbase + r) * Dk + c0, x);
+        acc_rows(tb, kAQ, Dk, [&](int r, int c0, const float (&x)[16]) {
+            st16f(p.dqh + (gbase + r) * Dk + c0, x);
         });
-        acc_rows(tb, 64, Dk, [&](int r, int c0, const float (&x)[16]) {
-            st16f(p.dkh2 + (gbase + r) * Dk + c0, x);
+        acc_rows(tb, kAK, Dk, [&](int r, int c0, const float (&x)[16]) {
+            st16f(p.dkh + (gbase + r) * Dk + c0, x);
         });
     }
     tc::tc_fence_before();
@@ -611,7 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
 
 bool bwd_chunk_tc_supported(const Dims& d) {
     if (d.dtype != 1) return false;
-    if (d.Dk % 32 || d.Dv % 32 || d.Dk > 224 || d.Dv > 256) return false;  // TMEM: 2 Dk + 64 <= 512
+    // TMEM: scratch 64 + dk and dq accumulators 2 Dk + scratch 64 <= 512
+    if (d.Dk % 32 || d.Dv % 32 || d.Dk > 192 || d.Dv > 256) return false;
     return smem_plan((int)d.Dk, (int)d.Dv).total + 2048 <= 227u * 1024u;
 }
 

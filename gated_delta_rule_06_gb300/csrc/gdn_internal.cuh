@@ -88,9 +88,6 @@ struct Ptrs {
     float* Dbar;   // [B, Hv, Tp, Dv] cotangent of Delta
     float* dqh;    // [B, Hv, Tp, Dk] cotangent of the normalised q, per value head
     float* dkh;    // [B, Hv, Tp, Dk]
-    float* dqh2;   // [B, Hv, Tp, Dk] second part of dqh (tensor-core path), summed by bwd_reduce
-    float* dkh2;   // [B, Hv, Tp, Dk]
-    int dq_parts;  // 1: dqh / dkh hold the full cotangents; 2: add dqh2 / dkh2
     float* dl;     // [B, Hv, Tp] cotangent of the log-decay
     float* dbeta;  // [B, Hv, Tp]
     float* part;   // [2, B, NC, Hv] per-chunk partial sums for dA_log, ddt_bias
