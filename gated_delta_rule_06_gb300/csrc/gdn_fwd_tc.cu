@@ -24,6 +24,7 @@ namespace {
 
 constexpr int C = kChunk;
 constexpr int kThreads = 256;
+constexpr int kTmemCols = 256;  // half the TMEM: two CTAs per SM
 
 __device__ __forceinline__ uint32_t canon(int x, int y, int ncols) {
     return (uint32_t)(x >> 3) * 128u + (uint32_t)(y >> 3) * (uint32_t)ncols * 16u +
@@ -79,14 +80,18 @@ __device__ __forceinline__ void acc_rows(uint32_t tbase, uint32_t col0, int ncol
     }
 }
 
-// T = (I + A)^-1 for a 64 x 64 strictly lower A (fp32, row-major in shared
+// fp32 64 x 64 matrices in shared memory have rows of LDT floats: 68 keeps
+// rows 16-byte aligned and moves consecutive rows four banks apart
+constexpr int LDT = C + 4;
+
+// T = (I + A)^-1 for a 64 x 64 strictly lower A (fp32, row stride LDT in shared
 // memory), by forward substitution on 16 x 16 blocks: the four diagonal blocks
 // first, then the block sub-diagonals d = 1, 2, 3 with
 //   T_ij = -T_ii * sum_{k=j}^{i-1} A_ik T_kj.
 // X is 64 x 64 scratch.  All threads of the CTA take part; ends synchronised.
 __device__ void tri_inverse64(const float* A, float* T, float* X) {
     const int tid = threadIdx.x;
-    for (int e = tid; e < C * C; e += blockDim.x) T[e] = 0.f;
+    for (int e = tid; e < C * C; e += blockDim.x) T[(e >> 6) * LDT + (e & 63)] = 0.f;
     __syncthreads();
     if (tid < C) {
         const int blk = tid >> 4, c = tid & 15, o = 16 * blk;
@@ -95,11 +100,11 @@ __device__ void tri_inverse64(const float* A, float* T, float* X) {
         for (int i = 0; i < 16; ++i) {
             float v = (i == c) ? 1.f : 0.f;
 #pragma unroll
-            for (int jj = 0; jj < i; ++jj) v = fmaf(-A[(o + i) * C + o + jj], col[jj], v);
+            for (int jj = 0; jj < i; ++jj) v = fmaf(-A[(o + i) * LDT + o + jj], col[jj], v);
             col[i] = (i < c) ? 0.f : v;
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) T[(o + i) * C + o + c] = col[i];
+        for (int i = 0; i < 16; ++i) T[(o + i) * LDT + o + c] = col[i];
     }
     __syncthreads();
     for (int dlt = 1; dlt < 4; ++dlt) {
@@ -108,8 +113,8 @@ __device__ void tri_inverse64(const float* A, float* T, float* X) {
             const int b = e >> 8, r = (e >> 4) & 15, c = e & 15;
             const int bi = dlt + b, bj = b;
             float s = 0.f;
-            for (int k = 16 * bj; k < 16 * bi; ++k) s = fmaf(A[(16 * bi + r) * C + k], T[k * C + 16 * bj + c], s);
-            X[(16 * bi + r) * C + 16 * bj + c] = s;
+            for (int k = 16 * bj; k < 16 * bi; ++k) s = fmaf(A[(16 * bi + r) * LDT + k], T[k * LDT + 16 * bj + c], s);
+            X[(16 * bi + r) * LDT + 16 * bj + c] = s;
         }
         __syncthreads();
         for (int e = tid; e < nb * 256; e += blockDim.x) {
@@ -118,8 +123,8 @@ __device__ void tri_inverse64(const float* A, float* T, float* X) {
             float s = 0.f;
 #pragma unroll
             for (int k = 0; k < 16; ++k)
-                s = fmaf(T[(16 * bi + r) * C + 16 * bi + k], X[(16 * bi + k) * C + 16 * bj + c], s);
-            T[(16 * bi + r) * C + 16 * bj + c] = -s;
+                s = fmaf(T[(16 * bi + r) * LDT + 16 * bi + k], X[(16 * bi + k) * LDT + 16 * bj + c], s);
+            T[(16 * bi + r) * LDT + 16 * bj + c] = -s;
         }
         __syncthreads();
     }
@@ -129,6 +134,9 @@ struct F1Smem {
     uint32_t K, Q, V, A, T, X, Tw, Twl, Tu, Tul, vec, total;
 };
 
+// Sized for two CTAs per SM: T takes the space of the q tile (dead after the
+// Grams) when it fits, and the four bf16 T-operand tiles that of A and X (dead
+// after the solve).
 __host__ __device__ inline F1Smem f1_plan(int Dk, int Dv) {
     F1Smem s{};
     uint32_t o = 0;
@@ -137,22 +145,23 @@ __host__ __device__ inline F1Smem f1_plan(int Dk, int Dv) {
         o += (bytes + 1023u) & ~1023u;
         return r;
     };
+    const uint32_t fm = C * LDT * 4;  // one padded fp32 64 x 64 matrix
     s.K = take(C * Dk * 2);
     s.Q = take(C * Dk * 2);
     s.V = take(C * Dv * 2);
-    s.A = take(C * C * 4);
-    s.T = take(C * C * 4);
-    s.X = take(C * C * 4);
-    s.Tw = take(C * C * 2);
-    s.Twl = take(C * C * 2);
-    s.Tu = take(C * C * 2);
-    s.Tul = take(C * C * 2);
+    s.A = take(2 * fm);               // A, then X right after it
+    s.X = s.A + fm;
+    s.T = (uint32_t)(C * Dk * 2) >= fm ? s.Q : take(fm);
+    s.Tw = s.A;
+    s.Twl = s.A + C * C * 2;
+    s.Tu = s.A + 2 * C * C * 2;
+    s.Tul = s.A + 3 * C * C * 2;
     s.vec = take(8 * C * 4 + C * 8);
     s.total = o;
     return s;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) fwd_chunk_tc_kernel(Dims d, Ptrs p) {
+__global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs p) {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ uint64_t bar;
     __shared__ uint32_t tmem_sh;
@@ -166,7 +175,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_chunk_tc_kernel(Dims d, Ptrs 
     float* gm = bt + C;         // exp(Gamma)
     float* rqv = gm + C;        // r_q / sqrt(Dk)
     float* rkv = rqv + C;       // r_k
-    double* Gm = reinterpret_cast<double*>(vec + 8 * C);
+    // Gamma as an unevaluated sum hi + lo of two floats: for steps whose Gamma are
+    // within a factor of two (the only case where exp(Gamma_i - Gamma_j) is not
+    // negligible) hi_i - hi_j is exact, so differences keep fp64 accuracy
+    float* Ghi = rkv + C;
+    float* Glo = Ghi + C;
     float* A = reinterpret_cast<float*>(sm + L.A);
     float* Tm = reinterpret_cast<float*>(sm + L.T);
     float* X = reinterpret_cast<float*>(sm + L.X);
@@ -186,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_chunk_tc_kernel(Dims d, Ptrs 
     cpa_tile(sm + L.V, v + ((int64_t)bb * d.T + t0) * ldv + (int64_t)h * Dv, ldv, Dv, nvalid);
     tc::cp_async_commit();
     if (warp == 0) {
-        tc::tmem_alloc(&tmem_sh, 512);
+        tc::tmem_alloc(&tmem_sh, kTmemCols);
         tc::tmem_relinquish();
     }
     if (tid == 0) {
@@ -195,7 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_chunk_tc_kernel(Dims d, Ptrs 
     }
     if (tid < C) {
         const double G = p.gam[gbase + tid];
-        Gm[tid] = G;
+        const float gh = (float)G;
+        Ghi[tid] = gh;
+        Glo[tid] = (float)(G - (double)gh);
         gm[tid] = expf((float)G);
         bt[tid] = p.beta[gbase + tid];
         rqv[tid] = p.rq[rbase + tid] * rsqrtf((float)Dk);
@@ -227,8 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_chunk_tc_kernel(Dims d, Ptrs 
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int jj = c0 + i;
-                const float m = jj < r ? expf((float)(Gm[r] - Gm[jj])) : 0.f;
-                A[r * C + jj] = bt[r] * m * rkv[r] * rkv[jj] * x[i];
+                const float m = jj < r ? expf((Ghi[r] - Ghi[jj]) + (Glo[r] - Glo[jj])) : 0.f;
+                A[r * LDT + jj] = bt[r] * m * rkv[r] * rkv[jj] * x[i];
             }
         });
         acc_rows(tb, 64, C, [&](int r, int c0, const float (&x)[16]) {
@@ -236,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_chunk_tc_kernel(Dims d, Ptrs 
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int jj = c0 + i;
-                const float m = jj <= r ? expf((float)(Gm[r] - Gm[jj])) : 0.f;
+                const float m = jj <= r ? expf((Ghi[r] - Ghi[jj]) + (Glo[r] - Glo[jj])) : 0.f;
                 pv[i] = m * rqv[r] * rkv[jj] * x[i];
             }
             st_bf16x8(Pimg + tc::panel_off(c0, r, C), pv);
@@ -252,15 +267,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_chunk_tc_kernel(Dims d, Ptrs 
     // T as a bf16 panel image: 16-byte chunk e holds row e % 64, columns 8 (e / 64) ..
     uint8_t* Timg = reinterpret_cast<uint8_t*>(p.Tinv) + (bh * d.NC + c) * C * C * 2;
     for (int e = tid; e < C * (C / 8); e += blockDim.x)
-        st_bf16x8(Timg + 16 * e, Tm + (e % C) * C + (e / C) * 8);
+        st_bf16x8(Timg + 16 * e, Tm + (e % C) * LDT + (e / C) * 8);
     // A operands T diag(beta gam r_k) and T diag(beta), each as hi + lo bf16 (x = j, y = i)
     for (int e = tid; e < C * (C / 8); e += blockDim.x) {
-        const int i = e / (C / 8), j0 = (e % (C / 8)) * 8;
+        int i, jg;
+        chunk_rc(e, C / 8, i, jg);  // eight consecutive rows per 8-lane group
+        const int j0 = 8 * jg;
         float w8[8], wl[8], u8[8], ul[8];
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
             const int jj = j0 + s;
-            const float t = Tm[i * C + jj];
+            const float t = Tm[i * LDT + jj];
             w8[s] = t * bt[jj] * gm[jj] * rkv[jj];
             u8[s] = t * bt[jj];
             wl[s] = w8[s] - __bfloat162float(__float2bfloat16_rn(w8[s]));
@@ -277,27 +294,48 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_chunk_tc_kernel(Dims d, Ptrs 
     __syncthreads();
     tc::tc_fence_after();
 
-    // ---- W = T diag(beta gam r_k) K,  U = T diag(beta) V
+    // ---- W = T diag(beta gam r_k) K,  U = T diag(beta) V: one round of MMAs
+    // when both fit in the 256 TMEM columns, else W first, then U
     const tc::Tile tTw = tile_of(sm + L.Tw, C, true), tTwl = tile_of(sm + L.Twl, C, true);
     const tc::Tile tTu = tile_of(sm + L.Tu, C, true), tTul = tile_of(sm + L.Tul, C, true);
+    const bool one_round = Dk + Dv <= kTmemCols;
     if (tid == 0) {
         tc::mma_tile(tb + 0, tTw, tKmn, C, Dk, C, false);
         tc::mma_tile(tb + 0, tTwl, tKmn, C, Dk, C, true);
-        tc::mma_tile(tb + Dk, tTu, tVmn, C, Dv, C, false);
-        tc::mma_tile(tb + Dk, tTul, tVmn, C, Dv, C, true);
+        if (one_round) {
+            tc::mma_tile(tb + Dk, tTu, tVmn, C, Dv, C, false);
+            tc::mma_tile(tb + Dk, tTul, tVmn, C, Dv, C, true);
+        }
         tc::mma_commit(&bar);
     }
     ok = tc::mbar_wait(&bar, phase, &g_err_fwdtc) && ok;
     phase ^= 1u;
     tc::tc_fence_after();
+    uint8_t* Wimg = static_cast<uint8_t*>(p.W) + gbase * Dk * 2;
     if (ok) {
-        uint8_t* Wimg = static_cast<uint8_t*>(p.W) + gbase * Dk * 2;
-        float* U = p.U + gbase * Dv;
         acc_rows(tb, 0, Dk, [&](int r, int c0, const float (&x)[16]) {
             st_bf16x8(Wimg + tc::panel_off(c0, r, C), x);
             st_bf16x8(Wimg + tc::panel_off(c0 + 8, r, C), x + 8);
         });
-        acc_rows(tb, Dk, Dv, [&](int r, int c0, const float (&x)[16]) {
+    }
+    uint32_t ucol = (uint32_t)Dk;
+    if (!one_round) {
+        tc::tc_fence_before();
+        __syncthreads();  // W read out of TMEM
+        tc::tc_fence_after();
+        if (tid == 0) {
+            tc::mma_tile(tb + 0, tTu, tVmn, C, Dv, C, false);
+            tc::mma_tile(tb + 0, tTul, tVmn, C, Dv, C, true);
+            tc::mma_commit(&bar);
+        }
+        ok = tc::mbar_wait(&bar, phase, &g_err_fwdtc) && ok;
+        phase ^= 1u;
+        tc::tc_fence_after();
+        ucol = 0;
+    }
+    if (ok) {
+        float* U = p.U + gbase * Dv;
+        acc_rows(tb, ucol, Dv, [&](int r, int c0, const float (&x)[16]) {
             float4* dst = reinterpret_cast<float4*>(U + (int64_t)r * Dv + c0);
 #pragma unroll
             for (int i = 0; i < 4; ++i) dst[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
@@ -305,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_chunk_tc_kernel(Dims d, Ptrs 
     }
     tc::tc_fence_before();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tb, 512);
+    if (warp == 0) tc::tmem_dealloc(tb, kTmemCols);
 }
 
 }  // namespace
