@@ -135,7 +135,9 @@ bool make_tmaps(const gdn::Dims& d, const void* q, const void* k, const void* v,
     bool ok = gdn::encode_row_tile_map(&m->q, q, d.B, d.T, d.Hk, d.Dk, (int)d.Dk) &&
               gdn::encode_row_tile_map(&m->k, k, d.B, d.T, d.Hk, d.Dk, (int)d.Dk) &&
               gdn::encode_row_tile_map(&m->v, v, d.B, d.T, d.Hv, d.Dv, (int)d.Dv);
-    if (ok && dO) ok = gdn::encode_row_tile_map(&m->dO, dO, d.B, d.T, d.Hv, d.Dv, vt);
+    if (ok && dO)
+        ok = gdn::encode_row_tile_map(&m->dO, dO, d.B, d.T, d.Hv, d.Dv, vt) &&
+             gdn::encode_row_tile_map(&m->dOf, dO, d.B, d.T, d.Hv, d.Dv, (int)d.Dv);
     if (ok && o) ok = gdn::encode_row_major_map(&m->o, o, d.B, d.T, d.Hv * d.Dv, vt);
     return ok;
 }

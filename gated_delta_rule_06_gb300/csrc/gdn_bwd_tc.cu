@@ -125,23 +125,14 @@ __device__ __forceinline__ void tile_row16(const uint8_t* tile, int ncols, int x
     ld_bf16x8(tile + canon(x0, y, ncols), v);
     ld_bf16x8(tile + canon(x0 + 8, y, ncols), v + 8);
 }
+// 16 consecutive elements (x0 multiple of 8) of row y of a 64-row panel tile
+__device__ __forceinline__ void panel_row16(const uint8_t* tile, int x0, int y, float* v) {
+    ld_bf16x8(tile + tc::panel_off(x0, y, C), v);
+    ld_bf16x8(tile + tc::panel_off(x0 + 8, y, C), v + 8);
+}
 __device__ __forceinline__ void tile_put16(uint8_t* tile, int ncols, int x0, int y, const float* v) {
     st_bf16x8(tile + canon(x0, y, ncols), v);
     st_bf16x8(tile + canon(x0 + 8, y, ncols), v + 8);
-}
-
-// 64-row bf16 tile (x = column) fetched with 16-byte cp.async; rows >= nvalid zero
-__device__ __forceinline__ void cpa_tile(uint8_t* tile, const __nv_bfloat16* src, int64_t ld,
-                                         int ncols, int nvalid) {
-    const int cpr = ncols / 8;
-    const uint32_t base = tc::smem_u32(tile);
-    for (int e = threadIdx.x; e < C * cpr; e += blockDim.x) {
-        int row, cc;
-        chunk_rc(e, cpr, row, cc);
-        const bool in = row < nvalid;
-        tc::cp_async16(base + canon(cc * 8, row, ncols), src + (in ? row : 0) * ld + cc * 8,
-                       in ? 16u : 0u);
-    }
 }
 
 __device__ __forceinline__ tc::Tile kmaj(uint8_t* smem, uint32_t off, int ncols) {
@@ -212,6 +203,43 @@ __device__ __forceinline__ void acc_rows_all(uint32_t tbase, uint32_t col0, int 
     }
 }
 
+// Unevaluated sums hi + lo of two floats (Knuth's two-sum, Dekker's fast
+// two-sum): ~48-bit sums in fp32 arithmetic, for the cancelling log-decay sums
+struct f2 {
+    float hi, lo;
+};
+__device__ __forceinline__ f2 two_sum(float a, float b) {
+    const float s = a + b;
+    const float bb = s - a;
+    return {s, (a - (s - bb)) + (b - bb)};
+}
+__device__ __forceinline__ f2 f2_add(f2 x, f2 y) {
+    const f2 s = two_sum(x.hi, y.hi);
+    const float lo = s.lo + (x.lo + y.lo);
+    const float h = s.hi + lo;
+    return {h, lo - (h - s.hi)};
+}
+
+// As acc_rows with up to four 16-column loads in flight per wait
+template <typename F>
+__device__ __forceinline__ void acc_rows4(uint32_t tbase, uint32_t col0, int ncols, F&& f) {
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    const int sp = w & 3, g = w >> 2;
+    const int half = ncols / 2, end = (g + 1) * half;
+    for (int cb = g * half; cb < end; cb += 64) {
+        float v[4][16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (cb + 16 * u < end) tc::tmem_ld16(tc::tmem_addr(tbase, 32 * sp, col0 + cb + 16 * u), v[u]);
+        tc::tmem_wait_ld();
+        if (l < 16) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (cb + 16 * u < end) f(16 * sp + l, cb + 16 * u, v[u]);
+        }
+    }
+}
+
 __device__ __forceinline__ void sync_after_mma(uint64_t* bar, uint32_t& phase, bool& ok) {
     ok = tc::mbar_wait(bar, phase, &g_err_bwdtc) && ok;
     phase ^= 1u;
@@ -223,15 +251,22 @@ __device__ __forceinline__ void cta_sync_tc() {
     tc::tc_fence_after();
 }
 
-__global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs p) {
+__global__ void __launch_bounds__(kThreads + 32, 1)
+    bwd_chunk_tc_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm) {
     extern __shared__ __align__(1024) uint8_t sm[];
-    __shared__ uint64_t bar, barL, barS[2];
+    // bar: MMA rounds outside phase 1; barM / barE: phase-1 products of block b
+    // done / block b's epilogue done (two of each, by block parity); barOV, barL,
+    // barKQ, barS: operand arrivals
+    __shared__ uint64_t bar, barOV, barL, barKQ, barS[2], barM[2], barE[2];
     __shared__ uint32_t tmem_base_sh;
     const int c = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
     const int j = h / (int)d.G;
     const int Dk = (int)d.Dk, Dv = (int)d.Dv;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = warp >> 2;  // column half walked by this warp in acc_rows
+    // warps 0-7: epilogues (row quarter warp % 4, column half g); warp 8: loads and MMA issue
+    const bool epi = tid < kThreads;
+    const bool prod = tid == kThreads;
+    const int g = (warp >> 2) & 1;
     const Smem L = smem_plan(Dk, Dv);
     float* vec = reinterpret_cast<float*>(sm + L.vec);
     float* gm = vec;             // exp(Gamma)
@@ -255,20 +290,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     float* rsp = Glo + C;       // [4][64] row sums of Mbar o M (compensated)
     float* rsc = rsp + 4 * C;   // [4][64] their compensation terms
     float* csp = rsc + 4 * C;   // [4][64] column sums (compensated, folded)
-    double* gam_bar = reinterpret_cast<double*>(csp + 4 * C);  // [64]
+    float* gbh = csp + 4 * C;   // [64] Gammabar as hi + lo
+    float* gbl = gbh + C;       // [64]
 
     const int64_t t0 = (int64_t)c * C;
     const int nvalid = (int)(d.T - t0 < C ? d.T - t0 : C);
     const int64_t gbase = ((int64_t)bb * d.Hv + h) * d.Tp + t0;
     const int64_t rbase = ((int64_t)bb * d.Hk + j) * d.Tp + t0;
     const int64_t ci = ((int64_t)bb * d.Hv + h) * d.NC + c;  // chunk image index
-    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
-    const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(p.k);
-    const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(p.v);
-    const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(p.d_o);
     __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(p.dv);
-    const int64_t ldq = d.Hk * Dk, ldv = d.Hv * Dv;
+    const int64_t ldv = d.Hv * Dv;
     const uint32_t tv = (uint32_t)(C * Dv * 2);         // one 64 x Dv bf16 tile
+    const uint32_t tk = (uint32_t)(C * Dk * 2);         // one 64 x Dk bf16 tile
     const uint32_t blk = (uint32_t)(kBlkK * Dv * 2);    // one Dk block of S (or Sbar')
     const uint8_t* ck_img = reinterpret_cast<const uint8_t*>(p.ckpt) + ci * (int64_t)Dk * Dv * 2;
     const uint8_t* ds_img = reinterpret_cast<const uint8_t*>(p.dSck) + ci * (int64_t)Dk * Dv * 2;
@@ -281,23 +314,27 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
         tc::bulk_g2s(sm + dst, ck_img + (int64_t)b * blk, blk, &barS[b & 1]);
         tc::bulk_g2s(sm + dst + blk, ds_img + (int64_t)b * blk, blk, &barS[b & 1]);
     };
-    // ---- operands: raw q, k, dO, v by cp.async; Delta (hi + lo), -Dbar, T and
-    // the first Dk block of S / Sbar' as bf16 images by bulk copies
-    cpa_tile(sm + L.K, k + ((int64_t)bb * d.T + t0) * ldq + (int64_t)j * Dk, ldq, Dk, nvalid);
-    cpa_tile(sm + L.Q, q + ((int64_t)bb * d.T + t0) * ldq + (int64_t)j * Dk, ldq, Dk, nvalid);
-    cpa_tile(sm + L.O, dO + ((int64_t)bb * d.T + t0) * ldv + (int64_t)h * Dv, ldv, Dv, nvalid);
-    cpa_tile(sm + L.V, v + ((int64_t)bb * d.T + t0) * ldv + (int64_t)h * Dv, ldv, Dv, nvalid);
-    tc::cp_async_commit();
+    // ---- operands, all issued by the producer: raw dO, v (phase 0) and k, q by
+    // TMA in the panel layout; Delta (hi + lo), -Dbar, T and the first Dk block of
+    // S / Sbar' as bf16 images by bulk copies
     if (warp == 0) {
         tc::tmem_alloc(&tmem_base_sh, 512);
         tc::tmem_relinquish();
     }
-    if (tid == 0) {
+    if (prod) {
         tc::mbar_init(&bar, 1);
+        tc::mbar_init(&barOV, 1);
         tc::mbar_init(&barL, 1);
-        tc::mbar_init(&barS[0], 1);
-        tc::mbar_init(&barS[1], 1);
+        tc::mbar_init(&barKQ, 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&barS[i], 1);
+            tc::mbar_init(&barM[i], 1);
+            tc::mbar_init(&barE[i], kThreads);
+        }
         tc::fence_mbar_init();
+        tc::mbar_arrive_expect_tx(&barOV, 2 * tv);
+        tc::tma_load_5d(sm + L.O, &tm.dOf, 0, (int)t0, 0, h, bb, &barOV);
+        tc::tma_load_5d(sm + L.V, &tm.v, 0, (int)t0, 0, h, bb, &barOV);
         const uint8_t* dl_img = reinterpret_cast<const uint8_t*>(p.Delta) + ci * (int64_t)C * Dv * 4;
         tc::mbar_arrive_expect_tx(&barL, 3 * tv + C * C * 2);
         tc::bulk_g2s(sm + L.D, dl_img, tv, &barL);
@@ -305,6 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
         tc::bulk_g2s(sm + L.NB, reinterpret_cast<const uint8_t*>(p.Dbar) + ci * (int64_t)tv, tv, &barL);
         tc::bulk_g2s(sm + L.Tt, reinterpret_cast<const uint8_t*>(p.Tinv) + ci * (int64_t)C * C * 2,
                      C * C * 2, &barL);
+        tc::mbar_arrive_expect_tx(&barKQ, 2 * tk);
+        tc::tma_load_5d(sm + L.K, &tm.k, 0, (int)t0, 0, j, bb, &barKQ);
+        tc::tma_load_5d(sm + L.Q, &tm.q, 0, (int)t0, 0, j, bb, &barKQ);
         load_blk(0);
     }
     if (tid < C) {
@@ -320,16 +360,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     }
     for (int i = tid; i < 12 * C; i += blockDim.x) gq[i] = 0.f;  // gq, ee, bb0, zk, sbp
     for (int i = tid; i < 8 * C; i += blockDim.x) rsp[i] = 0.f;  // rsp, rsc
-    tc::cp_async_wait_all();
-    tc::fence_async_smem();
     cta_sync_tc();
     const uint32_t tb = tmem_base_sh;
     uint32_t phase = 0;
-    bool ok = tc::mbar_wait(&barL, 0, &g_err_bwdtc);
+    bool ok = tc::mbar_wait(&barOV, 0, &g_err_bwdtc);
+    ok = tc::mbar_wait(&barL, 0, &g_err_bwdtc) && ok;
 
-    const tc::Tile tK = kmaj(sm, L.K, Dk), tQ = kmaj(sm, L.Q, Dk), tW = kmaj(sm, L.W, Dk);
-    const tc::Tile tKmn = mnmaj(sm, L.K, Dk), tQmn = mnmaj(sm, L.Q, Dk), tWmn = mnmaj(sm, L.W, Dk);
-    const tc::Tile tO = kmaj(sm, L.O, Dv), tV = kmaj(sm, L.V, Dv);
+    // k, q, dO, v tiles: panel layout (x = column, 64 rows); Wbar tile: canonical
+    const tc::Tile tK = tc::panel_tile(sm + L.K, C, true), tQ = tc::panel_tile(sm + L.Q, C, true);
+    const tc::Tile tKmn = tc::panel_tile(sm + L.K, C, false), tQmn = tc::panel_tile(sm + L.Q, C, false);
+    const tc::Tile tW = kmaj(sm, L.W, Dk), tWmn = mnmaj(sm, L.W, Dk);
+    const tc::Tile tO = tc::panel_tile(sm + L.O, C, true), tV = tc::panel_tile(sm + L.V, C, true);
     // Delta / -Dbar images: x = step t (canonical, 8-row groups of Dv 1024 bytes apart)
     const tc::Tile tDmn = mnmaj(sm, L.D, C), tDlomn = mnmaj(sm, L.Dlo, C);
     const tc::Tile tNB = kmaj(sm, L.NB, C), tNBmn = mnmaj(sm, L.NB, C);
@@ -340,111 +381,133 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     const uint32_t kAQ = kAK + (uint32_t)Dk, kS2 = kAK + (uint32_t)(2 * Dk > Dv ? 2 * Dk : Dv);
 
     // ---- phase 0: Pbar = Obar Delta^T | -Dbar V^T | -T^T Dbar
-    if (tid == 0) {
+    if (prod) {
         tc::mma_tile(tb + kS1, tO, tDmn, C, C, Dv, false);
         tc::mma_tile(tb + kS1, tO, tDlomn, C, C, Dv, true);
         tc::mma_tile(tb + kS2, tNBmn, tV, C, C, Dv, false);
         tc::mma_tile(tb + kAK, tTmn, tNB, C, Dv, C, false);
         tc::mma_commit(&bar);
     }
-    sync_after_mma(&bar, phase, ok);
     float* Pf = reinterpret_cast<float*>(sm + L.Pf);
     float* Tbf = reinterpret_cast<float*>(sm + L.Tbf);
-    if (ok) {
-        acc_rows(tb, kS1, C, [&](int r, int c0, const float (&x)[16]) {
-            float m[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) m[i] = (c0 + i <= r) ? x[i] : 0.f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) Pf[r * LDM + c0 + i] = m[i];
-        });
-        acc_rows(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
-            float m[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) m[i] = -bt[c0 + i] * x[i];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) Tbf[r * LDM + c0 + i] = m[i];
-        });
-        acc_rows(tb, kAK, Dv, [&](int r, int c0, const float (&x)[16]) {
-            float vv[16], y[16];
-            tile_row16(sm + L.V, Dv, c0, r, vv);
-            float s = 0.f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                s = fmaf(-x[i], vv[i], s);
-                y[i] = -bt[r] * x[i];
-            }
-            bb0[g * C + r] += s;
-            if (r < nvalid) {
-                uint8_t* dst = reinterpret_cast<uint8_t*>(dv + ((int64_t)bb * d.T + t0 + r) * ldv +
-                                                          (int64_t)h * Dv + c0);
-                st_bf16x8(dst, y);
-                st_bf16x8(dst + 16, y + 8);
-            }
-        });
-    }
-
-    // ---- phase 1: state products per kBlkK-wide block of Dk; block b + 1 streams
-    // into the other buffer while block b's products and epilogues run.  Obar S^T
-    // and Delta Sbar'^T land in the dq / dk accumulators and are rescaled there by
-    // gam and e.  <S, Sbar'> (the chunk-end term of the log-decay cotangent) is
-    // summed from the same tiles.
-    float gcb = 0.f;
-    const int nblk = Dk / kBlkK;
-    for (int b = 0; b < nblk; ++b) {
-        const int dk0 = b * kBlkK, nk = kBlkK;
-        cta_sync_tc();  // previous block's TMEM reads and MMAs are done; its buffer is free
-        if (tid == 0 && b + 1 < nblk) load_blk(b + 1);
-        ok = tc::mbar_wait(&barS[b & 1], (uint32_t)(b >> 1) & 1u, &g_err_bwdtc) && ok;
-        const uint8_t* sS = sm + sbuf(b);
-        for (int e = tid; e < (int)(blk / 16); e += kThreads) {
-            float a8[8], b8[8];
-            ld_bf16x8(sS + 16 * e, a8);
-            ld_bf16x8(sS + blk + 16 * e, b8);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) gcb = fmaf(a8[i], b8[i], gcb);
-        }
-        // S / Sbar' blocks: panel layout over Dv rows, x = dk (the N dimension)
-        const tc::Tile tS = tc::panel_tile(sS, Dv, false), tSp = tc::panel_tile(sS + blk, Dv, false);
-        if (tid == 0) {
-            tc::mma_tile(tb + kAQ + dk0, tO, tS, C, nk, Dv, false);
-            tc::mma_tile(tb + kS1, tNBmn, tS, C, nk, Dv, false);
-            tc::mma_tile(tb + kAK + dk0, tDmn, tSp, C, nk, Dv, false);
-            tc::mma_tile(tb + kAK + dk0, tDlomn, tSp, C, nk, Dv, true);
-            tc::mma_commit(&bar);
-        }
+    if (epi) {
         sync_after_mma(&bar, phase, ok);
         if (ok) {
-            acc_rows_rw(tb, kAQ + dk0, nk, [&](int r, int c0, float (&x)[16]) {
-                float qq[16];
-                tile_row16(sm + L.Q, Dk, dk0 + c0, r, qq);
+            acc_rows(tb, kS1, C, [&](int r, int c0, const float (&x)[16]) {
+                float m[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) m[i] = (c0 + i <= r) ? x[i] : 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) Pf[r * LDM + c0 + i] = m[i];
+            });
+            acc_rows(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
+                float m[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) m[i] = -bt[c0 + i] * x[i];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) Tbf[r * LDM + c0 + i] = m[i];
+            });
+            acc_rows(tb, kAK, Dv, [&](int r, int c0, const float (&x)[16]) {
+                float vv[16], y[16];
+                panel_row16(sm + L.V, c0, r, vv);
                 float s = 0.f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    x[i] *= gm[r];
-                    s = fmaf(x[i], qq[i], s);
+                    s = fmaf(-x[i], vv[i], s);
+                    y[i] = -bt[r] * x[i];
                 }
-                gq[g * C + r] += s;
-            });
-            acc_rows(tb, kS1, nk, [&](int r, int c0, const float (&x)[16]) {
-                tile_put16(sm + L.W, Dk, dk0 + c0, r, x);
-            });
-            acc_rows_rw(tb, kAK + dk0, nk, [&](int r, int c0, float (&x)[16]) {
-                float kk[16];
-                tile_row16(sm + L.K, Dk, dk0 + c0, r, kk);
-                float s = 0.f;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    x[i] *= ev[r];
-                    s = fmaf(x[i], kk[i], s);
+                bb0[g * C + r] += s;
+                if (r < nvalid) {
+                    uint8_t* dst = reinterpret_cast<uint8_t*>(dv + ((int64_t)bb * d.T + t0 + r) * ldv +
+                                                              (int64_t)h * Dv + c0);
+                    st_bf16x8(dst, y);
+                    st_bf16x8(dst + 16, y + 8);
                 }
-                ee[g * C + r] += s;
             });
         }
     }
-    red[tid] = gcb;
+    cta_sync_tc();  // phase-0 reads of TMEM and of the V tile are done
+
+    // ---- phase 1: state products per kBlkK-wide block of Dk.  The producer
+    // issues block b's products as soon as its S / Sbar' block has landed and the
+    // epilogue of block b - 2 has released the Wbar scratch half, so block b + 1
+    // multiplies while block b's epilogue runs; Obar S^T and Delta Sbar'^T land in
+    // the dq / dk accumulators and are rescaled there by gam and e.  <S, Sbar'>
+    // (the chunk-end term of the log-decay cotangent) is summed from the tiles.
+    float gcb = 0.f;
+    const int nblk = Dk / kBlkK;
+    constexpr int nk = kBlkK;
+    if (prod) {
+        if (nblk > 1) load_blk(1);
+        for (int b = 0; b < nblk; ++b) {
+            const int dk0 = b * kBlkK;
+            ok = tc::mbar_wait(&barS[b & 1], (uint32_t)(b >> 1) & 1u, &g_err_bwdtc) && ok;
+            const uint8_t* sS = sm + sbuf(b);
+            const tc::Tile tS = tc::panel_tile(sS, Dv, false), tSp = tc::panel_tile(sS + blk, Dv, false);
+            const uint32_t wcol = kS1 + 32u * (uint32_t)(b & 1);
+            tc::mma_tile(tb + kAQ + dk0, tO, tS, C, nk, Dv, false);
+            tc::mma_tile(tb + wcol, tNBmn, tS, C, nk, Dv, false);
+            tc::mma_tile(tb + kAK + dk0, tDmn, tSp, C, nk, Dv, false);
+            tc::mma_tile(tb + kAK + dk0, tDlomn, tSp, C, nk, Dv, true);
+            tc::mma_commit(&barM[b & 1]);
+            if (b >= 1 && b + 1 < nblk) {
+                // block b + 1 into the buffer of block b - 1 once that block's epilogue
+                // (and so its products) is done; this also frees the Wbar half of b + 1
+                ok = tc::mbar_wait(&barE[(b - 1) & 1], (uint32_t)((b - 1) >> 1) & 1u, &g_err_bwdtc) && ok;
+                load_blk(b + 1);
+            }
+        }
+    } else if (epi) {
+        ok = tc::mbar_wait(&barKQ, 0, &g_err_bwdtc) && ok;
+        for (int b = 0; b < nblk; ++b) {
+            const int dk0 = b * kBlkK;
+            const uint32_t par = (uint32_t)(b >> 1) & 1u;
+            ok = tc::mbar_wait(&barS[b & 1], par, &g_err_bwdtc) && ok;
+            const uint8_t* sS = sm + sbuf(b);
+            for (int e = tid; e < (int)(blk / 16); e += kThreads) {
+                float a8[8], b8[8];
+                ld_bf16x8(sS + 16 * e, a8);
+                ld_bf16x8(sS + blk + 16 * e, b8);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) gcb = fmaf(a8[i], b8[i], gcb);
+            }
+            ok = tc::mbar_wait(&barM[b & 1], par, &g_err_bwdtc) && ok;
+            tc::tc_fence_after();
+            if (ok) {
+                acc_rows_rw(tb, kAQ + dk0, nk, [&](int r, int c0, float (&x)[16]) {
+                    float qq[16];
+                    panel_row16(sm + L.Q, dk0 + c0, r, qq);
+                    float s = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        x[i] *= gm[r];
+                        s = fmaf(x[i], qq[i], s);
+                    }
+                    gq[g * C + r] += s;
+                });
+                acc_rows(tb, kS1 + 32u * (uint32_t)(b & 1), nk, [&](int r, int c0, const float (&x)[16]) {
+                    tile_put16(sm + L.W, Dk, dk0 + c0, r, x);
+                });
+                acc_rows_rw(tb, kAK + dk0, nk, [&](int r, int c0, float (&x)[16]) {
+                    float kk[16];
+                    panel_row16(sm + L.K, dk0 + c0, r, kk);
+                    float s = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        x[i] *= ev[r];
+                        s = fmaf(x[i], kk[i], s);
+                    }
+                    ee[g * C + r] += s;
+                });
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(&barE[b & 1]);
+        }
+        red[tid] = gcb;
+    }
+    cta_sync_tc();  // phase 1 done: its operand space (under the phase-2/3 scratch) is free
     // diag(beta gam) T^T as an operand: T image columns scaled by beta gam
-    for (int e = tid; e < C * (C / 8); e += kThreads) {
+    for (int e = tid; e < C * (C / 8); e += blockDim.x) {
         const int j0 = (e / C) * 8;  // panel chunk e: row e % 64, columns j0 .. j0 + 7
         float t8[8];
         ld_bf16x8(sm + L.Tt + 16 * e, t8);
@@ -456,22 +519,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     cta_sync_tc();
 
     // ---- phase 1b: Wbar K^T | dk += diag(beta gam) T^T Wbar | K K^T
-    if (tid == 0) {
+    if (prod) {
+        ok = tc::mbar_wait(&barKQ, 0, &g_err_bwdtc) && ok;
         tc::mma_tile(tb + kS1, tW, tK, C, C, Dk, false);
         tc::mma_tile(tb + kAK, tc::panel_tile(sm + L.Tsc, C, false), tWmn, C, Dk, C, true);
         tc::mma_tile(tb + kS2, tK, tK, C, C, Dk, false);
         tc::mma_commit(&bar);
     }
-    for (int s = blockDim.x / 2; s > 0; s >>= 1) {  // <Sbar', S>, fixed-order tree
+    for (int s = kThreads / 2; s > 0; s >>= 1) {  // <Sbar', S>, fixed-order tree
         if (tid < s) red[tid] += red[tid + s];
         __syncthreads();
     }
     const float gCb = red[0];
-    sync_after_mma(&bar, phase, ok);
     float* Gkk = reinterpret_cast<float*>(sm + L.Gkk);
     float* Gqk = reinterpret_cast<float*>(sm + L.Gqk);
     float* ZP = Gqk;  // T o (Wbar K^T), until Gqk is formed in phase 2
-    if (ok) {
+    if (epi) sync_after_mma(&bar, phase, ok);
+    if (epi && ok) {
         acc_rows(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) Gkk[r * LDM + c0 + i] = rkv[r] * rkv[c0 + i] * x[i];
@@ -510,13 +574,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     cta_sync_tc();
 
     // ---- phase 2: X = Tbar T^T | Q K^T, then Abar' = T^T X (Abar = -Abar')
-    if (tid == 0) {
+    if (prod) {
         tc::mma_tile(tb + kS1, kmaj(sm, L.Tbh, C), tTt, C, C, C, false);
         tc::mma_tile(tb + kS2, tQ, tK, C, C, Dk, false);
         tc::mma_commit(&bar);
     }
-    sync_after_mma(&bar, phase, ok);
-    if (ok) {
+    if (epi) sync_after_mma(&bar, phase, ok);
+    if (epi && ok) {
         acc_rows(tb, kS1, C, [&](int r, int c0, const float (&x)[16]) {
             tile_put16(sm + L.Xh, C, c0, r, x);  // X row-major (x = l, y = j)
         });
@@ -527,12 +591,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     }
     tc::fence_async_smem();
     cta_sync_tc();
-    if (tid == 0) {
+    if (prod) {
         tc::mma_tile(tb + kS1, tTmn, mnmaj(sm, L.Xh, C), C, C, C, false);
         tc::mma_commit(&bar);
     }
-    sync_after_mma(&bar, phase, ok);
-    if (ok) {
+    if (epi) sync_after_mma(&bar, phase, ok);
+    if (epi && ok) {
         // element-wise: M, Abar, Mbar o M (in place of Gkk), Gb (in place of Gqk),
         // Pbar o M scaled by r_k (columns) and by r_q (rows) as bf16 operands;
         // every lane takes 8 columns of a row
@@ -578,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
         for (int s = 0; s < 8; ++s) h8[s] = (Gqk[i * LDM + j0 + s] + Gqk[(j0 + s) * LDM + i]) * rkv[j0 + s];
         st_bf16x8(sm + L.Hk + canon(j0, i, C), h8);
     }
-    {
+    if (epi) {
         const int i = tid & (C - 1), qd = tid >> 6;
         float cs = 0.f, cc = 0.f;  // Kahan-compensated column sum
 #pragma unroll 4
@@ -594,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     cta_sync_tc();
 
     // ---- phase 3: dq += (Pbar o M) K;  dk += (Pbar o M)^T Q + (Gb + Gb^T) K
-    if (tid == 0) {
+    if (prod) {
         tc::mma_tile(tb + kAQ, kmaj(sm, L.PMk, C), tKmn, C, Dk, C, true);
         tc::mma_tile(tb + kAK, mnmaj(sm, L.PMq, C), tQmn, C, Dk, C, true);
         tc::mma_tile(tb + kAK, kmaj(sm, L.Hk, C), tKmn, C, Dk, C, true);
@@ -602,43 +666,53 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_tc_kernel(Dims d, Ptrs 
     }
     // Gammabar_i = sum_j (Mbar o M)_ij - sum_k (Mbar o M)_ki + gambar_i gam_i - ebar_i e_i,
     // plus the chunk-end terms at i = 63; the log-decay cotangent is its reverse
-    // cumulative sum (one warp, fp64, two steps per lane)
+    // cumulative sum (one warp, two-float sums, two steps per lane)
     if (tid < C) {
         const int i = tid;
         betab[i] += sbp[i] + sbp[C + i] + sbp[2 * C + i] + sbp[3 * C + i];
-        double rows = 0.0;
+        f2 gb{0.f, 0.f};
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) rows += (double)rsp[q4 * C + i] - (double)rsc[q4 * C + i];
-        const double cols = (double)csp[i] + (double)csp[C + i] + (double)csp[2 * C + i] + (double)csp[3 * C + i];
-        gam_bar[i] = rows - cols + (double)gq[i] - (double)ee[i];
+        for (int q4 = 0; q4 < 4; ++q4) {
+            gb = f2_add(gb, f2{rsp[q4 * C + i], -rsc[q4 * C + i]});
+            gb = f2_add(gb, f2{-csp[q4 * C + i], 0.f});
+        }
+        gb = f2_add(gb, f2{gq[i], 0.f});
+        gb = f2_add(gb, f2{-ee[i], 0.f});
+        gbh[i] = gb.hi;
+        gbl[i] = gb.lo;
     }
     __syncthreads();
     if (warp == 0) {
-        double se = (double)ee[2 * lane] + (double)ee[2 * lane + 1];
+        // chunk-end terms at i = 63: <S, Sbar'> gam_63 + sum_j ebar_j e_j
+        f2 se = f2_add(f2{ee[2 * lane], 0.f}, f2{ee[2 * lane + 1], 0.f});
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) se += __shfl_xor_sync(0xffffffffu, se, off);
-        double x0 = gam_bar[2 * lane], x1 = gam_bar[2 * lane + 1];
-        if (lane == 31) x1 += (double)gCb * gm[C - 1] + se;
+        for (int off = 16; off > 0; off >>= 1)
+            se = f2_add(se, f2{__shfl_xor_sync(0xffffffffu, se.hi, off), __shfl_xor_sync(0xffffffffu, se.lo, off)});
+        const f2 x0{gbh[2 * lane], gbl[2 * lane]};
+        f2 x1{gbh[2 * lane + 1], gbl[2 * lane + 1]};
+        if (lane == 31) x1 = f2_add(f2_add(x1, two_sum(gCb * gm[C - 1], 0.f)), se);
         // suffix sums: element i gets sum_{k >= i}
-        const double tot = x0 + x1;
-        double suf = tot;  // inclusive suffix over lanes >= lane
+        const f2 tot = f2_add(x0, x1);
+        f2 suf = tot;  // inclusive suffix over lanes >= lane
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const double y = __shfl_down_sync(0xffffffffu, suf, off);
-            if (lane + off < 32) suf += y;
+            const f2 y{__shfl_down_sync(0xffffffffu, suf.hi, off), __shfl_down_sync(0xffffffffu, suf.lo, off)};
+            if (lane + off < 32) suf = f2_add(suf, y);
         }
-        const double after = suf - tot;  // lanes > lane
-        p.dl[gbase + 2 * lane + 1] = (float)(x1 + after);
-        p.dl[gbase + 2 * lane] = (float)(x0 + x1 + after);
+        const f2 after = f2_add(suf, f2{-tot.hi, -tot.lo});  // lanes > lane
+        const f2 d1 = f2_add(x1, after);
+        const f2 d0 = f2_add(x0, d1);
+        p.dl[gbase + 2 * lane + 1] = d1.hi + d1.lo;
+        p.dl[gbase + 2 * lane] = d0.hi + d0.lo;
         p.dbeta[gbase + 2 * lane] = betab[2 * lane];
         p.dbeta[gbase + 2 * lane + 1] = betab[2 * lane + 1];
     }
-    sync_after_mma(&bar, phase, ok);
-    if (ok) {
-        acc_rows(tb, kAQ, Dk, [&](int r, int c0, const float (&x)[16]) {
+    if (epi) sync_after_mma(&bar, phase, ok);
+    if (epi && ok) {
+        acc_rows4(tb, kAQ, Dk, [&](int r, int c0, const float (&x)[16]) {
             st16f(p.dqh + (gbase + r) * Dk + c0, x);
         });
-        acc_rows(tb, kAK, Dk, [&](int r, int c0, const float (&x)[16]) {
+        acc_rows4(tb, kAK, Dk, [&](int r, int c0, const float (&x)[16]) {
             st16f(p.dkh + (gbase + r) * Dk + c0, x);
         });
     }
@@ -663,7 +737,7 @@ cudaError_t launch_bwd_chunk_tc(const Dims& d, const Ptrs& p, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)d.NC, (unsigned)d.Hv, (unsigned)d.B);
-    kern<<<grid, kThreads, smem, s>>>(d, p);
+    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps);
     count_launches(1);
     return cudaPeekAtLastError();
 }

@@ -31,7 +31,7 @@ struct Dims {
 // 64 rows x min(Dv, 128) columns, for TMA stores of staged output rows (rows past
 // T are not written).
 struct Tmaps {
-    CUtensorMap q, k, v, dO, o;
+    CUtensorMap q, k, v, dO, dOf, o;  // dO: boxes min(Dv, 128) wide; dOf: Dv wide
 };
 // box `cols` columns wide (multiple of 8, <= 256); false if the driver refuses
 bool encode_row_tile_map(CUtensorMap* m, const void* base, int64_t B, int64_t T, int64_t H,
