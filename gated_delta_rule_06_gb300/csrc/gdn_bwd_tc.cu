@@ -22,7 +22,7 @@
 // -Dbar, T, the state checkpoints S and the chunk-end cotangents Sbar') are
 // bf16 operand images written by the earlier kernels; each arrives with one
 // bulk copy, and the 32-wide Dk blocks of S / Sbar' are double-buffered so the
-// next block streams in while the current block's products run.
+// next block streams in while the current block's epilogue runs.
 #include "gdn_internal.cuh"
 #include "gdn_tc.cuh"
 
@@ -34,7 +34,7 @@ namespace {
 
 constexpr int C = kChunk;
 constexpr int kThreads = 256;
-constexpr int kBlkK = 32;  // Dk block of the state products
+constexpr int kBlkK = 64;  // Dk block of the state products (the last one may be 32)
 // TMEM column map (Dk <= 192): scratch S1 = [0, 64); dk accumulator AK = [64, 64 + Dk);
 // dq accumulator AQ = [64 + Dk, 64 + 2 Dk); scratch S2 = 64 columns from
 // 64 + max(2 Dk, Dv).  Phase 0 parks Y (Dv <= 256 columns) at 64, before AK /
@@ -71,7 +71,7 @@ __host__ __device__ inline Smem smem_plan(int Dk, int Dv) {
     s.Dlo = s.D + tv;
     s.NB = s.Dlo + tv;
     s.V = s.NB + tv;
-    s.S = s.V + tv;  // kBlkK x Dv
+    s.S = s.V + tv;  // with V: one Dk block of S and of Sbar' (2 x 64 x Dv bf16)
     s.Sp = s.S + tv / 2;
     s.Gkk = s.R1;            // fp32, later Mbar o M in place
     s.Gqk = s.Gkk + f64x64;  // fp32, later Gb in place
@@ -255,9 +255,9 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     bwd_chunk_tc_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm) {
     extern __shared__ __align__(1024) uint8_t sm[];
     // bar: MMA rounds outside phase 1; barM / barE: phase-1 products of block b
-    // done / block b's epilogue done (two of each, by block parity); barOV, barL,
-    // barKQ, barS: operand arrivals
-    __shared__ uint64_t bar, barOV, barL, barKQ, barS[2], barM[2], barE[2];
+    // done / block b's epilogue done (two of each, by block parity); barG: block
+    // b's tiles read by the <S, Sbar'> sums; barOV, barL, barKQ, barS: arrivals
+    __shared__ uint64_t bar, barOV, barL, barKQ, barS, barG, barM[2], barE[2];
     __shared__ uint32_t tmem_base_sh;
     const int c = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
     const int j = h / (int)d.G;
@@ -302,17 +302,18 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     const int64_t ldv = d.Hv * Dv;
     const uint32_t tv = (uint32_t)(C * Dv * 2);         // one 64 x Dv bf16 tile
     const uint32_t tk = (uint32_t)(C * Dk * 2);         // one 64 x Dk bf16 tile
-    const uint32_t blk = (uint32_t)(kBlkK * Dv * 2);    // one Dk block of S (or Sbar')
+    const uint32_t blk = (uint32_t)(kBlkK * Dv * 2);    // one full Dk block of S (or Sbar')
     const uint8_t* ck_img = reinterpret_cast<const uint8_t*>(p.ckpt) + ci * (int64_t)Dk * Dv * 2;
     const uint8_t* ds_img = reinterpret_cast<const uint8_t*>(p.dSck) + ci * (int64_t)Dk * Dv * 2;
-    // Dk block b of S / Sbar' (panels 4b .. 4b + 3 of the images) -> buffer b & 1
-    // (buffer 1 is the V tile's space, free once phase 0 is done)
-    auto sbuf = [&](int b) { return (b & 1) ? L.V : L.S; };
+    // Dk block b of S / Sbar' (panels 8b .. 8b + nk(b) / 8 - 1 of the images, one
+    // buffer in the space of the V tile, free once phase 0 is done)
+    const int nblk = (Dk + kBlkK - 1) / kBlkK;
+    auto nkb = [&](int b) { return Dk - b * kBlkK < kBlkK ? Dk - b * kBlkK : kBlkK; };
     auto load_blk = [&](int b) {
-        const uint32_t dst = sbuf(b);
-        tc::mbar_arrive_expect_tx(&barS[b & 1], 2 * blk);
-        tc::bulk_g2s(sm + dst, ck_img + (int64_t)b * blk, blk, &barS[b & 1]);
-        tc::bulk_g2s(sm + dst + blk, ds_img + (int64_t)b * blk, blk, &barS[b & 1]);
+        const uint32_t bytes = (uint32_t)(nkb(b) * Dv * 2);
+        tc::mbar_arrive_expect_tx(&barS, 2 * bytes);
+        tc::bulk_g2s(sm + L.V, ck_img + (int64_t)b * blk, bytes, &barS);
+        tc::bulk_g2s(sm + L.V + bytes, ds_img + (int64_t)b * blk, bytes, &barS);
     };
     // ---- operands, all issued by the producer: raw dO, v (phase 0) and k, q by
     // TMA in the panel layout; Delta (hi + lo), -Dbar, T and the first Dk block of
@@ -326,8 +327,9 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::mbar_init(&barOV, 1);
         tc::mbar_init(&barL, 1);
         tc::mbar_init(&barKQ, 1);
+        tc::mbar_init(&barS, 1);
+        tc::mbar_init(&barG, kThreads);
         for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&barS[i], 1);
             tc::mbar_init(&barM[i], 1);
             tc::mbar_init(&barE[i], kThreads);
         }
@@ -345,7 +347,6 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::mbar_arrive_expect_tx(&barKQ, 2 * tk);
         tc::tma_load_5d(sm + L.K, &tm.k, 0, (int)t0, 0, j, bb, &barKQ);
         tc::tma_load_5d(sm + L.Q, &tm.q, 0, (int)t0, 0, j, bb, &barKQ);
-        load_blk(0);
     }
     if (tid < C) {
         const double G = p.gam[gbase + tid];
@@ -428,50 +429,51 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     }
     cta_sync_tc();  // phase-0 reads of TMEM and of the V tile are done
 
-    // ---- phase 1: state products per kBlkK-wide block of Dk.  The producer
-    // issues block b's products as soon as its S / Sbar' block has landed and the
-    // epilogue of block b - 2 has released the Wbar scratch half, so block b + 1
-    // multiplies while block b's epilogue runs; Obar S^T and Delta Sbar'^T land in
-    // the dq / dk accumulators and are rescaled there by gam and e.  <S, Sbar'>
-    // (the chunk-end term of the log-decay cotangent) is summed from the tiles.
+    // ---- phase 1: state products per kBlkK-wide block of Dk through one buffer:
+    // the producer issues block b's products once its S / Sbar' block has landed
+    // (and the epilogue of block b - 2 has released its Wbar scratch: S1 for even,
+    // S2 for odd blocks), and loads block b + 1 as soon as block b's products and
+    // <S, Sbar'> sums have read the buffer, so the load overlaps block b's
+    // epilogue.  Obar S^T and Delta Sbar'^T land in the dq / dk accumulators and
+    // are rescaled there by gam and e.
     float gcb = 0.f;
-    const int nblk = Dk / kBlkK;
-    constexpr int nk = kBlkK;
     if (prod) {
-        if (nblk > 1) load_blk(1);
+        load_blk(0);
         for (int b = 0; b < nblk; ++b) {
-            const int dk0 = b * kBlkK;
-            ok = tc::mbar_wait(&barS[b & 1], (uint32_t)(b >> 1) & 1u, &g_err_bwdtc) && ok;
-            const uint8_t* sS = sm + sbuf(b);
-            const tc::Tile tS = tc::panel_tile(sS, Dv, false), tSp = tc::panel_tile(sS + blk, Dv, false);
-            const uint32_t wcol = kS1 + 32u * (uint32_t)(b & 1);
+            const int dk0 = b * kBlkK, nk = nkb(b);
+            const uint32_t par = (uint32_t)b & 1u;
+            ok = tc::mbar_wait(&barS, par, &g_err_bwdtc) && ok;
+            if (b >= 2) ok = tc::mbar_wait(&barE[b & 1], (uint32_t)((b - 2) >> 1) & 1u, &g_err_bwdtc) && ok;
+            const tc::Tile tS = tc::panel_tile(sm + L.V, Dv, false);
+            const tc::Tile tSp = tc::panel_tile(sm + L.V + nk * Dv * 2, Dv, false);
+            const uint32_t wcol = (b & 1) ? kS2 : kS1;
             tc::mma_tile(tb + kAQ + dk0, tO, tS, C, nk, Dv, false);
             tc::mma_tile(tb + wcol, tNBmn, tS, C, nk, Dv, false);
             tc::mma_tile(tb + kAK + dk0, tDmn, tSp, C, nk, Dv, false);
             tc::mma_tile(tb + kAK + dk0, tDlomn, tSp, C, nk, Dv, true);
             tc::mma_commit(&barM[b & 1]);
-            if (b >= 1 && b + 1 < nblk) {
-                // block b + 1 into the buffer of block b - 1 once that block's epilogue
-                // (and so its products) is done; this also frees the Wbar half of b + 1
-                ok = tc::mbar_wait(&barE[(b - 1) & 1], (uint32_t)((b - 1) >> 1) & 1u, &g_err_bwdtc) && ok;
+            if (b + 1 < nblk) {  // the buffer is free once the products and the sums have read it
+                ok = tc::mbar_wait(&barM[b & 1], (uint32_t)(b >> 1) & 1u, &g_err_bwdtc) && ok;
+                ok = tc::mbar_wait(&barG, par, &g_err_bwdtc) && ok;
                 load_blk(b + 1);
             }
         }
     } else if (epi) {
         ok = tc::mbar_wait(&barKQ, 0, &g_err_bwdtc) && ok;
         for (int b = 0; b < nblk; ++b) {
-            const int dk0 = b * kBlkK;
-            const uint32_t par = (uint32_t)(b >> 1) & 1u;
-            ok = tc::mbar_wait(&barS[b & 1], par, &g_err_bwdtc) && ok;
-            const uint8_t* sS = sm + sbuf(b);
-            for (int e = tid; e < (int)(blk / 16); e += kThreads) {
+            const int dk0 = b * kBlkK, nk = nkb(b);
+            ok = tc::mbar_wait(&barS, (uint32_t)b & 1u, &g_err_bwdtc) && ok;
+            const uint8_t* sS = sm + L.V;
+            const int bytes = nk * Dv * 2;
+            for (int e = tid; e < bytes / 16; e += kThreads) {
                 float a8[8], b8[8];
                 ld_bf16x8(sS + 16 * e, a8);
-                ld_bf16x8(sS + blk + 16 * e, b8);
+                ld_bf16x8(sS + bytes + 16 * e, b8);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) gcb = fmaf(a8[i], b8[i], gcb);
             }
-            ok = tc::mbar_wait(&barM[b & 1], par, &g_err_bwdtc) && ok;
+            tc::mbar_arrive(&barG);
+            ok = tc::mbar_wait(&barM[b & 1], (uint32_t)(b >> 1) & 1u, &g_err_bwdtc) && ok;
             tc::tc_fence_after();
             if (ok) {
                 acc_rows_rw(tb, kAQ + dk0, nk, [&](int r, int c0, float (&x)[16]) {
@@ -485,7 +487,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
                     }
                     gq[g * C + r] += s;
                 });
-                acc_rows(tb, kS1 + 32u * (uint32_t)(b & 1), nk, [&](int r, int c0, const float (&x)[16]) {
+                acc_rows(tb, (b & 1) ? kS2 : kS1, nk, [&](int r, int c0, const float (&x)[16]) {
                     tile_put16(sm + L.W, Dk, dk0 + c0, r, x);
                 });
                 acc_rows_rw(tb, kAK + dk0, nk, [&](int r, int c0, float (&x)[16]) {
