@@ -404,7 +404,36 @@ __global__ void __launch_bounds__(256) bwd_chunk_kernel(Dims d, Ptrs p) {
 // ---------------------------------------------------------------------------
 // bwd_reduce
 // ---------------------------------------------------------------------------
-// dq / dk: one warp per (b, t, key head); Dk <= 256 -> 8 values per lane
+// dq / dk: one warp per (b, t, key head).  Lane l takes the 4-column groups l
+// and l + 32 (Dk <= 256); the per-head rows of both cotangents are loaded as
+// float4 before any is used, so a warp keeps up to 4 G loads in flight.
+__device__ __forceinline__ void add4(float4& a, const float4 b) {
+    a.x += b.x;
+    a.y += b.y;
+    a.z += b.z;
+    a.w += b.w;
+}
+__device__ __forceinline__ void ld4x(const float* x, float* v) {
+    const float4 a = *reinterpret_cast<const float4*>(x);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+}
+__device__ __forceinline__ void ld4x(const __nv_bfloat16* x, float* v) {
+    const uint2 u = *reinterpret_cast<const uint2*>(x);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+__device__ __forceinline__ void st4x(float* o, const float* v) {
+    *reinterpret_cast<float4*>(o) = make_float4(v[0], v[1], v[2], v[3]);
+}
+__device__ __forceinline__ void st4x(__nv_bfloat16* o, const float* v) {
+    uint2 u;
+    __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(o) = u;
+}
+
 template <typename TI>
 __global__ void __launch_bounds__(256) bwd_qk_kernel(Dims d, Ptrs p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -413,37 +442,60 @@ __global__ void __launch_bounds__(256) bwd_qk_kernel(Dims d, Ptrs p) {
     const int64_t j = row % d.Hk;
     const int64_t t = (row / d.Hk) % d.T;
     const int64_t bb = row / (d.Hk * d.T);
-    const int Dk = (int)d.Dk;
+    const int Dk = (int)d.Dk, Dk4 = Dk / 4;
     const int64_t xoff = ((bb * d.T + t) * d.Hk + j) * Dk;
-    for (int pass = 0; pass < 2; ++pass) {
-        const TI* x = (const TI*)(pass == 0 ? p.q : p.k) + xoff;
-        const float* src = pass == 0 ? p.dqh : p.dkh;
-        const float r = (pass == 0 ? p.rq : p.rk)[(bb * d.Hk + j) * d.Tp + t];
-        const float s = pass == 0 ? rsqrtf((float)Dk) : 1.f;
-        float y[8], u[8];
+    const int64_t hstride = d.Tp * Dk;  // next value head of the group
+    const int64_t off0 = ((bb * d.Hv + j * d.G) * d.Tp + t) * Dk;
+    float4 y[2][2];  // [pass][group]
+#pragma unroll
+    for (int ps = 0; ps < 2; ++ps)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) y[ps][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t g = 0; g < d.G; ++g) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int q4 = lane + 32 * i;
+            if (q4 < Dk4) {
+                const int64_t off = off0 + g * hstride + 4 * q4;
+                add4(y[0][i], *reinterpret_cast<const float4*>(p.dqh + off));
+                add4(y[1][i], *reinterpret_cast<const float4*>(p.dkh + off));
+            }
+        }
+    }
+#pragma unroll
+    for (int ps = 0; ps < 2; ++ps) {
+        const TI* x = (const TI*)(ps == 0 ? p.q : p.k) + xoff;
+        const float r = (ps == 0 ? p.rq : p.rk)[(bb * d.Hk + j) * d.Tp + t];
+        const float s = ps == 0 ? rsqrtf((float)Dk) : 1.f;
+        float u[2][4], yv[2][4];
         float dot = 0.f;
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const int col = lane + 32 * m;
-            y[m] = 0.f;
-            u[m] = 0.f;
-            if (col < Dk) {
-                for (int64_t g = 0; g < d.G; ++g) {
-                    const int64_t h = j * d.G + g;
-                    const int64_t off = ((bb * d.Hv + h) * d.Tp + t) * Dk + col;
-                    y[m] += src[off];
+        for (int i = 0; i < 2; ++i) {
+            const int q4 = lane + 32 * i;
+            yv[i][0] = y[ps][i].x; yv[i][1] = y[ps][i].y; yv[i][2] = y[ps][i].z; yv[i][3] = y[ps][i].w;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) u[i][c] = 0.f;
+            if (q4 < Dk4) {
+                ld4x(x + 4 * q4, u[i]);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    u[i][c] *= r;
+                    dot = fmaf(u[i][c], yv[i][c], dot);
                 }
-                u[m] = ldf(x + col) * r;
-                dot = fmaf(u[m], y[m], dot);
             }
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-        TI* out = (TI*)(pass == 0 ? p.dq : p.dk) + xoff;
+        TI* out = (TI*)(ps == 0 ? p.dq : p.dk) + xoff;
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const int col = lane + 32 * m;
-            if (col < Dk) stf(out + col, s * r * (y[m] - u[m] * dot));
+        for (int i = 0; i < 2; ++i) {
+            const int q4 = lane + 32 * i;
+            if (q4 < Dk4) {
+                float o[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) o[c] = s * r * (yv[i][c] - u[i][c] * dot);
+                st4x(out + 4 * q4, o);
+            }
         }
     }
 }
