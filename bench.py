@@ -67,44 +67,56 @@ def _peaks():
 # ---------------------------------------------------------------------------
 
 def work_model(w):
+    """Per-phase algorithmic flops and bytes of one fwd+bwd step, in the storage
+    formats the kernels use: bf16 inputs keep the saved intermediates as bf16
+    operand images (checkpoints, T, W, P, Delta as hi + lo, state cotangents,
+    -Dbar), fp32 inputs as fp32 arrays."""
     es = 2 if w.dtype == torch.bfloat16 else 4
+    img = 2 if w.dtype == torch.bfloat16 else 4  # checkpoint / T / cotangent images
     B, T, Hk, Hv, Dk, Dv = w.B, w.T, w.Hk, w.Hv, w.Dk, w.Dv
     NC = (T + C - 1) // C
     Tp = NC * C
     BH, BHk = B * Hv, B * Hk
     units = BH * NC  # (b, h, chunk)
+    qk = BHk * NC * 2 * C * Dk * es  # q and k tiles, read once per key head
     m = {}
     m["prep"] = dict(flops=0.0, bytes=2 * B * T * Hv * es + 2 * B * T * Hk * Dk * es
-                     + 2 * BH * Tp * 4 + 2 * BHk * Tp * 4)
+                     + 2 * BH * Tp * 4 + BH * Tp * 8 + 2 * BHk * Tp * 4)
+    # q, k, v tiles in; W, P, T images and U (fp32) out
     m["fwd_chunk"] = dict(
         flops=units * (6 * C * C * Dk + 2 * C * C * Dv + C ** 3 / 3),
-        bytes=units * (2 * C * Dk * es + C * Dv * es + 2 * C * 4 + C * Dk * es + C * Dv * es
-                       + C * C * es + C * C * 4))
+        bytes=qk + units * (C * Dv * es + 2 * C * 4 + C * 8
+                            + C * Dk * es + C * C * es + C * C * img + C * Dv * 4))
+    # W, P, q, k, U in; checkpoint image, Delta (hi + lo) and o out
     m["fwd_scan"] = dict(
         flops=units * (6 * C * Dk * Dv + 2 * C * C * Dv),
-        bytes=units * (3 * C * Dk * es + C * Dv * es + C * C * es + Dk * Dv * 4
-                       + 2 * C * Dv * es) + 2 * BH * Dk * Dv * 4)
+        bytes=qk + units * (C * Dk * es + C * C * es + C * Dv * 4 + Dk * Dv * img
+                            + C * Dv * 4 + C * Dv * es) + 2 * BH * Dk * Dv * 4)
+    # dO, P, k, q, W in; chunk-end cotangent and -Dbar images out
     m["bwd_scan"] = dict(
         flops=units * (6 * C * Dk * Dv + 2 * C * C * Dv),
-        bytes=units * (C * Dv * es + C * C * es + 3 * C * Dk * es + Dk * Dv * 4 + C * Dv * 4)
+        bytes=qk + units * (C * Dv * es + C * C * es + C * Dk * es + Dk * Dv * img + C * Dv * img)
         + BH * Dk * Dv * 4)
+    # checkpoint and cotangent images, Delta, -Dbar, T, q, k, dO, v in;
+    # dq, dk per value head (fp32), dv, log-decay and beta cotangents out
     m["bwd_chunk"] = dict(
         flops=units * (6 * C * C * Dv + 14 * C * C * Dk + 6 * C * Dk * Dv + 4 * C ** 3),
-        bytes=units * (2 * Dk * Dv * 4 + 3 * C * Dv * es + C * Dv * 4 + 2 * C * Dk * es
-                       + C * C * 4 + 2 * C * Dk * 4 + C * Dv * es + 4 * C * 4))
+        bytes=qk + units * (2 * Dk * Dv * img + C * Dv * 4 + C * Dv * img + C * C * img
+                            + 2 * C * Dv * es + 4 * C * 4
+                            + 2 * C * Dk * 4 + C * Dv * es + 2 * C * 4))
     m["bwd_reduce"] = dict(
         flops=0.0,
         bytes=2 * BH * T * Dk * 4 + 4 * BHk * T * Dk * es + 2 * BH * T * 4 + 4 * B * T * Hv * es)
     m["decode"] = dict(flops=BH * (4 * Dk * Dv + 2 * Dk),
                        bytes=BH * 2 * Dk * Dv * 4 + BHk * 2 * Dk * es + BH * 2 * Dv * es
                        + BH * 2 * es)
-    # whole step: the bytes any chunked fwd + VJP with fp32 chunk checkpoints
-    # must move (inputs and outputs once, checkpoints written and read once)
+    # whole step: inputs and outputs once, plus the chunk checkpoints (in the
+    # format stored) written once and read once
     io_fwd = (2 * B * T * Hk * Dk + B * T * Hv * Dv + 2 * B * T * Hv) * es \
         + B * T * Hv * Dv * es + 2 * BH * Dk * Dv * 4
     io_bwd = (2 * B * T * Hk * Dk + 2 * B * T * Hv * Dv + 2 * B * T * Hv) * es \
         + (2 * B * T * Hk * Dk + B * T * Hv * Dv + 2 * B * T * Hv) * es + 2 * BH * Dk * Dv * 4
-    ckpt = 2 * units * Dk * Dv * 4
+    ckpt = 2 * units * Dk * Dv * img
     m["_step"] = dict(bytes=io_fwd + io_bwd + ckpt,
                       flops=sum(m[k]["flops"] for k in ("fwd_chunk", "fwd_scan", "bwd_scan",
                                                         "bwd_chunk")))
