@@ -129,7 +129,7 @@ void carve_saved(const Layout& L, void* saved, gdn::Ptrs* p) {
 // tensor maps of q, k, v (and dO) for the tensor-core kernels: full-width
 // 64-row tiles, dO in tiles of at most 128 columns (the scans' value tile)
 bool make_tmaps(const gdn::Dims& d, const void* q, const void* k, const void* v, const void* dO,
-                const void* o, gdn::Tmaps* m) {
+                const void* o, const void* U, gdn::Tmaps* m) {
     std::memset(m, 0, sizeof(*m));
     const int vt = (int)(d.Dv < 128 ? d.Dv : 128);
     bool ok = gdn::encode_row_tile_map(&m->q, q, d.B, d.T, d.Hk, d.Dk, (int)d.Dk) &&
@@ -139,6 +139,7 @@ bool make_tmaps(const gdn::Dims& d, const void* q, const void* k, const void* v,
         ok = gdn::encode_row_tile_map(&m->dO, dO, d.B, d.T, d.Hv, d.Dv, vt) &&
              gdn::encode_row_tile_map(&m->dOf, dO, d.B, d.T, d.Hv, d.Dv, (int)d.Dv);
     if (ok && o) ok = gdn::encode_row_major_map(&m->o, o, d.B, d.T, d.Hv * d.Dv, vt);
+    if (ok && U) ok = gdn::encode_f32_rows_map(&m->U, U, d.B * d.Hv * d.Tp, d.Dv, vt);
     return ok;
 }
 
@@ -196,6 +197,18 @@ bool encode_row_major_map(CUtensorMap* m, const void* base, int64_t B, int64_t T
     const cuuint32_t box[3] = {(cuuint32_t)cols, (cuuint32_t)kChunk, 1};
     const cuuint32_t unit[3] = {1, 1, 1};
     return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                  unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_f32_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols_total, int cols) {
+    const auto encode = tensor_map_encoder();
+    if (encode == nullptr || cols % 4 || cols < 4 || cols > 256 || cols_total % 4) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols_total, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(cols_total * 4)};
+    const cuuint32_t box[2] = {(cuuint32_t)cols, (cuuint32_t)kChunk};
+    const cuuint32_t unit[2] = {1, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
                   unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -291,7 +304,7 @@ gdn_status gdn_forward(const gdn_shape* shape, const void* q, const void* k, con
     p.U = reinterpret_cast<float*>(wsb + L.U);
     gdn::Tmaps maps;
     if (gdn::tc_path(d)) {
-        if (!make_tmaps(d, q, k, v, nullptr, o, &maps)) return tmap_error();
+        if (!make_tmaps(d, q, k, v, nullptr, o, p.U, &maps)) return tmap_error();
         p.tmaps = &maps;
     }
     cudaError_t e = run_phase("prep", s, [&] { return gdn::launch_prep(d, p, s); });
@@ -338,7 +351,7 @@ gdn_status gdn_backward(const gdn_shape* shape, const void* q, const void* k, co
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     gdn::Tmaps maps;
     if (gdn::tc_path(d)) {
-        if (!make_tmaps(d, q, k, v, d_o, nullptr, &maps)) return tmap_error();
+        if (!make_tmaps(d, q, k, v, d_o, nullptr, nullptr, &maps)) return tmap_error();
         p.tmaps = &maps;
     }
     cudaError_t e = run_phase("bwd_scan", s, [&] { return gdn::launch_bwd_scan(d, p, s); });

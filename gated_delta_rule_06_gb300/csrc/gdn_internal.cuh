@@ -30,14 +30,18 @@ struct Dims {
 // `o` is the output [B, T, Hv, Dv] as 3-d {Hv Dv, T, B} with a row-major box of
 // 64 rows x min(Dv, 128) columns, for TMA stores of staged output rows (rows past
 // T are not written).
+// `U` is the forward workspace U [B Hv Tp, Dv] fp32 with a box of 64 rows x
+// min(Dv, 128) columns (row-major), for the forward scan.
 struct Tmaps {
-    CUtensorMap q, k, v, dO, dOf, o;  // dO: boxes min(Dv, 128) wide; dOf: Dv wide
+    CUtensorMap q, k, v, dO, dOf, o, U;  // dO: boxes min(Dv, 128) wide; dOf: Dv wide
 };
 // box `cols` columns wide (multiple of 8, <= 256); false if the driver refuses
 bool encode_row_tile_map(CUtensorMap* m, const void* base, int64_t B, int64_t T, int64_t H,
                          int64_t D, int cols);
 bool encode_row_major_map(CUtensorMap* m, const void* base, int64_t B, int64_t T, int64_t rowlen,
                           int cols);
+// fp32 [rows, cols_total] row-major, box of 64 rows x `cols` columns
+bool encode_f32_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols_total, int cols);
 
 // Every device buffer the kernels touch.  Inputs/outputs come from the
 // caller; the rest are carved out of the caller's `saved` and `ws` buffers.

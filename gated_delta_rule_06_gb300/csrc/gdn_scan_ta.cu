@@ -11,8 +11,8 @@
 // diag(e r_k)-scaled hi + lo) are written by the epilogue threads straight into
 // TMEM, each thread its own accumulator row, and the MMAs take A from there.
 // B operands: the W and P images by bulk copy, raw q and k tiles by TMA (q is
-// scaled by gam r_q / sqrt(Dk) in place); the per-chunk gate and norm vectors
-// by bulk copy two chunks ahead.  Output rows are accumulated in two TMEM
+// scaled by gam r_q / sqrt(Dk) in place); U rows by TMA; the per-chunk gate
+// and norm vectors by bulk copy two chunks ahead.  Output rows are accumulated in two TMEM
 // buffers so the epilogue of chunk c runs while the products of chunk c + 1 do.
 //
 // TMEM columns: [0, Dk) the fp32 state S^T; [Dk, Dk + 128) A operands (S^T as
@@ -47,7 +47,7 @@ __device__ __forceinline__ uint32_t canon(int x, int y, int ncols) {
 }
 
 struct TaSmem {
-    uint32_t W, Q, K, P, St, Dt, Dlo, Ob, raw, vec, total;
+    uint32_t W, Q, K, P, Ub, St, Dt, Dlo, Ob, raw, vec, total;
 };
 
 __host__ __device__ inline TaSmem ta_plan(int Dk) {
@@ -62,6 +62,7 @@ __host__ __device__ inline TaSmem ta_plan(int Dk) {
     s.Q = take(C * Dk * 2);
     s.K = take(C * Dk * 2);
     s.P = take(C * C * 2);
+    s.Ub = take(C * DVT * 4);   // U rows of the value tile [t][dv], fp32, by TMA
     s.St = take(DVT * Dk * 2);  // checkpoint image staging (panel, 128 rows)
     s.Dt = take(DVT * C * 2);   // Delta^T hi / lo image staging (canonical, x = step)
     s.Dlo = take(DVT * C * 2);
@@ -121,7 +122,7 @@ __device__ __forceinline__ void scale_q(uint8_t* Q, const uint8_t* raw, int Dk) 
 __global__ void __launch_bounds__(kThreads + 32, 1)
     fwd_scan_ta_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm) {
     extern __shared__ __align__(1024) uint8_t sm[];
-    __shared__ uint64_t bar, barW, barQ, barK, barP, barR[2];
+    __shared__ uint64_t bar, barW, barQ, barK, barP, barU, barR[2];
     __shared__ uint32_t tmem_sh;
     const int tile = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
     const int j = h / (int)d.G;
@@ -143,7 +144,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     uint8_t* ckimg = reinterpret_cast<uint8_t*>(p.ckpt);
     uint8_t* dlimg = reinterpret_cast<uint8_t*>(p.Delta);
     __nv_bfloat16* Ob = reinterpret_cast<__nv_bfloat16*>(sm + L.Ob);
-    const float* U = p.U;
+    const float* Ub = reinterpret_cast<const float*>(sm + L.Ub);
 
     // loads (producer)
     auto load_w = [&](int64_t c) {
@@ -169,6 +170,10 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::bulk_g2s(dst, p.gam + bh * d.Tp + c * C, C * 8, &barR[s]);
         tc::bulk_g2s(dst + C * 8, p.rq + ((int64_t)bb * d.Hk + j) * d.Tp + c * C, C * 4, &barR[s]);
         tc::bulk_g2s(dst + C * 12, p.rk + ((int64_t)bb * d.Hk + j) * d.Tp + c * C, C * 4, &barR[s]);
+    };
+    auto load_u = [&](int64_t c) {  // U rows of chunk c, value columns n0 .. n0 + 127
+        tc::mbar_arrive_expect_tx(&barU, (uint32_t)(C * DVT * 4));
+        tc::tma_load_2d(sm + L.Ub, &tm.U, n0, (int)(bh * d.Tp + c * C), &barU);
     };
     // stores (lane 0 of the store warp; the caller commits)
     auto store_o = [&](int64_t c) { tc::tma_store_3d(&tm.o, Ob, h * Dv + n0, (int)(c * C), bb); };
@@ -211,6 +216,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::mbar_init(&barQ, 1);
         tc::mbar_init(&barK, 1);
         tc::mbar_init(&barP, 1);
+        tc::mbar_init(&barU, 1);
         tc::mbar_init(&barR[0], 1);
         tc::mbar_init(&barR[1], 1);
         tc::fence_mbar_init();
@@ -221,15 +227,9 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         load_q(0);
         load_k(0);
         load_p(0);
+        load_u(0);
         load_raw(0);
         if (d.NC > 1) load_raw(1);
-    }
-    // this thread's U^T values of the current chunk (steps 32 g .. 32 g + 31)
-    float ureg[C / 2];
-    if (epi) {
-        const float* up = U + (bh * d.Tp + g * (C / 2)) * Dv + n0 + r;
-#pragma unroll
-        for (int i = 0; i < C / 2; ++i) ureg[i] = up[(int64_t)i * Dv];
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -334,6 +334,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             phase ^= 1u;
             tc::tc_fence_after();
             // step 3: Delta^T = U^T - acc -> A operands hi, lo and (diag(e r_k)) hi, lo
+            ok = tc::mbar_wait(&barU, (uint32_t)(c & 1), &g_err_scanta) && ok;
             float a[2][16];
             tc::tmem_ld16(tc::tmem_addr(tb, lb, TC.dacc + 32 * g), a[0]);
             tc::tmem_ld16(tc::tmem_addr(tb, lb, TC.dacc + 32 * g + 16), a[1]);
@@ -345,7 +346,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const int ti = 2 * i + u;  // step 32 g + ti
-                    dl[u] = ureg[ti] - a[ti >> 4][ti & 15];
+                    dl[u] = Ub[(32 * g + ti) * DVT + r] - a[ti >> 4][ti & 15];
                     lo[u] = dl[u] - __bfloat162float(__float2bfloat16_rn(dl[u]));
                     de[u] = dl[u] * kev[32 * g + ti];
                     dlo[u] = de[u] - __bfloat162float(__float2bfloat16_rn(de[u]));
@@ -378,6 +379,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
                 tc::mma_bf16_ta(tb, tb + TC.aop + 64 + hl + k / 2, tKmn.desc(k), idk, 1u);
             }
             tc::mma_commit(&bar);
+            if (c + 1 < d.NC) load_u(c + 1);  // step 3 of chunk c has read U
             ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
             phase ^= 1u;
             if (c + 1 < d.NC) {
@@ -401,9 +403,6 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
                     make_uint4(low[4 * q4], low[4 * q4 + 1], low[4 * q4 + 2], low[4 * q4 + 3]);
             }
             if (c + 1 < d.NC) {
-                const float* up = U + (bh * d.Tp + (c + 1) * C + g * (C / 2)) * Dv + n0 + r;
-#pragma unroll
-                for (int i = 0; i < C / 2; ++i) ureg[i] = up[(int64_t)i * Dv];
                 const uint8_t* raw = sm + L.raw + ((c + 1) & 1) * kRawBytes;
                 ok = tc::mbar_wait(&barR[(c + 1) & 1], (uint32_t)(((c + 1) >> 1) & 1), &g_err_scanta) && ok;
                 vectors_from_raw(raw, reinterpret_cast<float*>(sm + L.vec) + ((c + 1) & 1) * 4 * C, Dk);

@@ -203,6 +203,14 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const void* map, int c0, 
         : "memory");
 }
 
+// 2-d tiled load (coordinates c0 = innermost, c1) into shared memory
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int c0, int c1, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
 // 3-d tiled store of a box from shared memory to the tensor map's tensor at
 // coordinates c0..c2 (all non-negative; elements past the tensor's extent are
 // not written), tracked in this thread's bulk groups
