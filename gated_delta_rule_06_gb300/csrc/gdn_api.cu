@@ -45,7 +45,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
     // byte offsets into `saved`
-    size_t ckpt, gam, beta, rq, rk, Tinv, W, P, Delta, saved_total;
+    size_t ckpt, gam, beta, rq, rk, Tinv, W, P, Delta, kimg, qimg, saved_total;
     // byte offsets into the forward workspace
     size_t U, fwd_total;
     // byte offsets into the backward workspace
@@ -97,6 +97,9 @@ Layout make_layout(const gdn::Dims& d) {
     L.W = o; o = align_up(o + perstep * d.Dk * es);
     L.P = o; o = align_up(o + BH * d.NC * gdn::kChunk * gdn::kChunk * es);
     L.Delta = o; o = align_up(o + perstep * d.Dv * 4);
+    const size_t qk_img = img == 2 ? (size_t)d.B * d.Hk * d.Tp * d.Dk * 2 : 0;
+    L.kimg = o; o = align_up(o + qk_img);
+    L.qimg = o; o = align_up(o + qk_img);
     L.saved_total = o;
     o = 0;
     L.U = o; o = align_up(o + perstep * d.Dv * 4);
@@ -124,17 +127,17 @@ void carve_saved(const Layout& L, void* saved, gdn::Ptrs* p) {
     p->W = s + L.W;
     p->P = s + L.P;
     p->Delta = reinterpret_cast<float*>(s + L.Delta);
+    p->kimg = s + L.kimg;
+    p->qimg = s + L.qimg;
 }
 
-// tensor maps of q, k, v (and dO) for the tensor-core kernels: full-width
+// tensor maps of v (and dO, o, U) for the tensor-core kernels: full-width
 // 64-row tiles, dO in tiles of at most 128 columns (the scans' value tile)
-bool make_tmaps(const gdn::Dims& d, const void* q, const void* k, const void* v, const void* dO,
-                const void* o, const void* U, gdn::Tmaps* m) {
+bool make_tmaps(const gdn::Dims& d, const void* v, const void* dO, const void* o, const void* U,
+                gdn::Tmaps* m) {
     std::memset(m, 0, sizeof(*m));
     const int vt = (int)(d.Dv < 128 ? d.Dv : 128);
-    bool ok = gdn::encode_row_tile_map(&m->q, q, d.B, d.T, d.Hk, d.Dk, (int)d.Dk) &&
-              gdn::encode_row_tile_map(&m->k, k, d.B, d.T, d.Hk, d.Dk, (int)d.Dk) &&
-              gdn::encode_row_tile_map(&m->v, v, d.B, d.T, d.Hv, d.Dv, (int)d.Dv);
+    bool ok = gdn::encode_row_tile_map(&m->v, v, d.B, d.T, d.Hv, d.Dv, (int)d.Dv);
     if (ok && dO)
         ok = gdn::encode_row_tile_map(&m->dO, dO, d.B, d.T, d.Hv, d.Dv, vt) &&
              gdn::encode_row_tile_map(&m->dOf, dO, d.B, d.T, d.Hv, d.Dv, (int)d.Dv);
@@ -304,7 +307,7 @@ gdn_status gdn_forward(const gdn_shape* shape, const void* q, const void* k, con
     p.U = reinterpret_cast<float*>(wsb + L.U);
     gdn::Tmaps maps;
     if (gdn::tc_path(d)) {
-        if (!make_tmaps(d, q, k, v, nullptr, o, p.U, &maps)) return tmap_error();
+        if (!make_tmaps(d, v, nullptr, o, p.U, &maps)) return tmap_error();
         p.tmaps = &maps;
     }
     cudaError_t e = run_phase("prep", s, [&] { return gdn::launch_prep(d, p, s); });
@@ -351,7 +354,7 @@ gdn_status gdn_backward(const gdn_shape* shape, const void* q, const void* k, co
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     gdn::Tmaps maps;
     if (gdn::tc_path(d)) {
-        if (!make_tmaps(d, q, k, v, d_o, nullptr, nullptr, &maps)) return tmap_error();
+        if (!make_tmaps(d, v, d_o, nullptr, nullptr, &maps)) return tmap_error();
         p.tmaps = &maps;
     }
     cudaError_t e = run_phase("bwd_scan", s, [&] { return gdn::launch_bwd_scan(d, p, s); });

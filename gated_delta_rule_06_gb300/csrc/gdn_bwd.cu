@@ -510,7 +510,6 @@ __global__ void __launch_bounds__(256) bwd_gate_kernel(Dims d, Ptrs p) {
     const int nh = (int)(d.Hv - h0 < 64 ? d.Hv - h0 : 64);
     const int64_t t0 = (int64_t)c * kChunk;
     const TI* a = (const TI*)p.a;
-    const TI* b = (const TI*)p.b;
     TI* da = (TI*)p.da;
     TI* db = (TI*)p.db;
     for (int idx = threadIdx.x; idx < kChunk * nh; idx += blockDim.x) {

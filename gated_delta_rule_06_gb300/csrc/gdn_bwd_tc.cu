@@ -315,9 +315,8 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::bulk_g2s(sm + L.V, ck_img + (int64_t)b * blk, bytes, &barS);
         tc::bulk_g2s(sm + L.V + bytes, ds_img + (int64_t)b * blk, bytes, &barS);
     };
-    // ---- operands, all issued by the producer: raw dO, v (phase 0) and k, q by
-    // TMA in the panel layout; Delta (hi + lo), -Dbar, T and the first Dk block of
-    // S / Sbar' as bf16 images by bulk copies
+    // ---- operands, all issued by the producer: raw dO, v (phase 0) by TMA in the
+    // panel layout; the k, q images, Delta (hi + lo), -Dbar and T by bulk copies
     if (warp == 0) {
         tc::tmem_alloc(&tmem_base_sh, 512);
         tc::tmem_relinquish();
@@ -344,9 +343,10 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::bulk_g2s(sm + L.NB, reinterpret_cast<const uint8_t*>(p.Dbar) + ci * (int64_t)tv, tv, &barL);
         tc::bulk_g2s(sm + L.Tt, reinterpret_cast<const uint8_t*>(p.Tinv) + ci * (int64_t)C * C * 2,
                      C * C * 2, &barL);
+        const int64_t kqi = ((int64_t)bb * d.Hk + j) * d.NC + c;  // q / k images of this chunk
         tc::mbar_arrive_expect_tx(&barKQ, 2 * tk);
-        tc::tma_load_5d(sm + L.K, &tm.k, 0, (int)t0, 0, j, bb, &barKQ);
-        tc::tma_load_5d(sm + L.Q, &tm.q, 0, (int)t0, 0, j, bb, &barKQ);
+        tc::bulk_g2s(sm + L.K, static_cast<const uint8_t*>(p.kimg) + kqi * tk, tk, &barKQ);
+        tc::bulk_g2s(sm + L.Q, static_cast<const uint8_t*>(p.qimg) + kqi * tk, tk, &barKQ);
     }
     if (tid < C) {
         const double G = p.gam[gbase + tid];

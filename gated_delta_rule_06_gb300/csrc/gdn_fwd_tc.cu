@@ -1,7 +1,7 @@
 // gdn_fwd_tc.cu -- chunk-local WY/UT products of the forward on the tensor
 // cores (tcgen05, bf16 operands, fp32 accumulators in TMEM) for bf16 inputs.
 //
-// Per (chunk, value head, batch), with raw q, k, v (mlx-lm PR "Add
+// Per (chunk, value head, batch), with raw q, k (panel images written by prep), v (mlx-lm PR "Add
 // gated_delta_update VJP", "Scope and follow-ups": chunk-parallel form through a
 // lower-triangular solve; torch-to-nnef "custom_extractors/gdn": the chunked
 // rule equals the recurrent one):
@@ -163,7 +163,7 @@ __host__ __device__ inline F1Smem f1_plan(int Dk, int Dv) {
 
 __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs p) {
     extern __shared__ __align__(1024) uint8_t sm[];
-    __shared__ uint64_t bar;
+    __shared__ uint64_t bar, barKQ;
     __shared__ uint32_t tmem_sh;
     const int c = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
     const int j = h / (int)d.G;
@@ -189,13 +189,9 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs 
     const int64_t bh = (int64_t)bb * d.Hv + h;
     const int64_t gbase = bh * d.Tp + t0;
     const int64_t rbase = ((int64_t)bb * d.Hk + j) * d.Tp + t0;
-    const int64_t ldq = d.Hk * Dk, ldv = d.Hv * Dv;
-    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
-    const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(p.k);
+    const int64_t ldv = d.Hv * Dv;
     const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(p.v);
 
-    cpa_tile(sm + L.K, k + ((int64_t)bb * d.T + t0) * ldq + (int64_t)j * Dk, ldq, Dk, nvalid);
-    cpa_tile(sm + L.Q, q + ((int64_t)bb * d.T + t0) * ldq + (int64_t)j * Dk, ldq, Dk, nvalid);
     cpa_tile(sm + L.V, v + ((int64_t)bb * d.T + t0) * ldv + (int64_t)h * Dv, ldv, Dv, nvalid);
     tc::cp_async_commit();
     if (warp == 0) {
@@ -204,7 +200,14 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs 
     }
     if (tid == 0) {
         tc::mbar_init(&bar, 1);
+        tc::mbar_init(&barKQ, 1);
         tc::fence_mbar_init();
+        // raw k and q rows of this chunk: panel images written by prep
+        const uint32_t tk = (uint32_t)(C * Dk * 2);
+        const int64_t kqi = ((int64_t)bb * d.Hk + j) * d.NC + c;
+        tc::mbar_arrive_expect_tx(&barKQ, 2 * tk);
+        tc::bulk_g2s(sm + L.K, static_cast<const uint8_t*>(p.kimg) + kqi * tk, tk, &barKQ);
+        tc::bulk_g2s(sm + L.Q, static_cast<const uint8_t*>(p.qimg) + kqi * tk, tk, &barKQ);
     }
     if (tid < C) {
         const double G = p.gam[gbase + tid];
@@ -223,9 +226,9 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs 
     tc::tc_fence_after();
     const uint32_t tb = tmem_sh;
     uint32_t phase = 0;
-    bool ok = true;
-    const tc::Tile tK = tile_of(sm + L.K, Dk, true), tQ = tile_of(sm + L.Q, Dk, true);
-    const tc::Tile tKmn = tile_of(sm + L.K, Dk, false), tVmn = tile_of(sm + L.V, Dv, false);
+    bool ok = tc::mbar_wait(&barKQ, 0, &g_err_fwdtc);
+    const tc::Tile tK = tc::panel_tile(sm + L.K, C, true), tQ = tc::panel_tile(sm + L.Q, C, true);
+    const tc::Tile tKmn = tc::panel_tile(sm + L.K, C, false), tVmn = tile_of(sm + L.V, Dv, false);
 
     // ---- Grams of the raw rows
     if (tid == 0) {

@@ -21,7 +21,8 @@ struct Dims {
     int dtype;   // 0 = fp32, 1 = bf16
 };
 
-// TMA descriptors of the raw bf16 inputs, encoded on the host for each call of
+// TMA descriptors of the raw bf16 inputs v and dO (q and k reach the kernels as
+// panel images written by prep) and of the output, encoded on the host for each call of
 // the tensor-core path and handed to the kernels as __grid_constant__ params.
 // Each describes a [B, T, H, D] tensor (row t of head h of batch b at
 // ((b T + t) H + h) D) as 5-d {8, T, D / 8, H, B} with a box of 64 rows: one
@@ -33,7 +34,7 @@ struct Dims {
 // `U` is the forward workspace U [B Hv Tp, Dv] fp32 with a box of 64 rows x
 // min(Dv, 128) columns (row-major), for the forward scan.
 struct Tmaps {
-    CUtensorMap q, k, v, dO, dOf, o, U;  // dO: boxes min(Dv, 128) wide; dOf: Dv wide
+    CUtensorMap v, dO, dOf, o, U;  // dO: boxes min(Dv, 128) wide; dOf: Dv wide
 };
 // box `cols` columns wide (multiple of 8, <= 256); false if the driver refuses
 bool encode_row_tile_map(CUtensorMap* m, const void* base, int64_t B, int64_t T, int64_t H,
@@ -58,6 +59,7 @@ bool encode_f32_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t
 //   Delta  [B, Hv, NC] pairs {hi, lo} of images of Delta^T (Dv rows x 64,
 //          canonical x = step, 8-row groups 1024 bytes apart), Delta = hi + lo
 //   dSck   [B, Hv, NC] images of Sbar'^T (Dv rows x Dk, panel), bf16
+//   kimg, qimg  [B, Hk, NC] images of the raw k / q rows (64 x Dk, panel)
 //   Dbar   [B, Hv, NC] images of -Dbar^T (Dv rows x 64, as Delta), bf16
 // U, gam, beta, rq, rk and the backward partials keep the row-major fp32 form.
 struct Ptrs {
@@ -79,6 +81,8 @@ struct Ptrs {
     void* W;       // [B, Hv, Tp, Dk]  T diag(beta gam) K   (input dtype)
     void* P;       // [B, Hv, NC, 64, 64] (Q K^T) o M, lower incl. diagonal
     float* Delta;  // [B, Hv, Tp, Dv]  U - W S  per chunk (fp32: Delta cancels, see U)
+    void* kimg;    // tensor-core path: [B, Hk, NC] images of the raw k rows of each
+    void* qimg;    // chunk (64 rows x Dk, panel; rows past T zero), written by prep
     // forward workspace
     float* U;      // [B, Hv, Tp, Dv]  T diag(beta) V (fp32: Delta = U - W S cancels,
                    // so a rounded U would dominate the error of the log-decay gradient)

@@ -96,14 +96,72 @@ __global__ void __launch_bounds__(256) prep_norms_kernel(Dims d, const TI* __res
     }
 }
 
+// Tensor-core path: the same norms from 16-byte row pieces, and the raw bf16
+// rows copied into the per-chunk panel images (piece g of row t of chunk c at
+// byte g * 1024 + (t % 64) * 16 of image (b, j, c); rows past T are zero).
+__global__ void __launch_bounds__(256) prep_norms_img_kernel(Dims d, const __nv_bfloat16* __restrict__ q,
+                                                             const __nv_bfloat16* __restrict__ k,
+                                                             float* __restrict__ rq,
+                                                             float* __restrict__ rk,
+                                                             uint8_t* __restrict__ qimg,
+                                                             uint8_t* __restrict__ kimg) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;  // over (b, t, j)
+    const int64_t nrows = d.B * d.Tp * d.Hk;
+    if (row >= nrows) return;
+    const int64_t j = row % d.Hk;
+    const int64_t t = (row / d.Hk) % d.Tp;
+    const int64_t bb = row / (d.Hk * d.Tp);
+    const int ng = (int)(d.Dk / 8);  // 16-byte pieces per row (<= 32)
+    const bool in = t < d.T;
+    uint4 uq = make_uint4(0u, 0u, 0u, 0u), uk = uq;
+    float sq = 0.f, sk = 0.f;
+    if (lane < ng && in) {
+        const int64_t base = ((bb * d.T + t) * d.Hk + j) * d.Dk + 8 * lane;
+        uq = *reinterpret_cast<const uint4*>(q + base);
+        uk = *reinterpret_cast<const uint4*>(k + base);
+        const __nv_bfloat162* hq = reinterpret_cast<const __nv_bfloat162*>(&uq);
+        const __nv_bfloat162* hk = reinterpret_cast<const __nv_bfloat162*>(&uk);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 fq = __bfloat1622float2(hq[i]), fk = __bfloat1622float2(hk[i]);
+            sq = fmaf(fq.x, fq.x, sq);
+            sq = fmaf(fq.y, fq.y, sq);
+            sk = fmaf(fk.x, fk.x, sk);
+            sk = fmaf(fk.y, fk.y, sk);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, off);
+        sk += __shfl_xor_sync(0xffffffffu, sk, off);
+    }
+    if (lane < ng) {
+        const int64_t c = t / kChunk;
+        const int64_t off = ((bb * d.Hk + j) * d.NC + c) * kChunk * d.Dk * 2 + (int64_t)lane * kChunk * 16 +
+                            (t % kChunk) * 16;
+        *reinterpret_cast<uint4*>(qimg + off) = uq;
+        *reinterpret_cast<uint4*>(kimg + off) = uk;
+    }
+    if (lane == 0) {
+        rq[(bb * d.Hk + j) * d.Tp + t] = in ? 1.f / sqrtf(sq + kNormEps) : 0.f;
+        rk[(bb * d.Hk + j) * d.Tp + t] = in ? 1.f / sqrtf(sk + kNormEps) : 0.f;
+    }
+}
+
 template <typename TI>
 cudaError_t launch_prep_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
     dim3 g1((unsigned)d.NC, (unsigned)d.B, (unsigned)((d.Hv + kGateHeads - 1) / kGateHeads));
     prep_gates_kernel<TI><<<g1, 256, 0, s>>>(d, (const TI*)p.a, (const TI*)p.b, p.A_log,
                                              p.dt_bias, p.mask, p.gam, p.beta);
     const int64_t rows = d.B * d.Tp * d.Hk;
-    prep_norms_kernel<TI><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(d, (const TI*)p.q,
-                                                                     (const TI*)p.k, p.rq, p.rk);
+    if (tc_path(d))
+        prep_norms_img_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
+            d, (const __nv_bfloat16*)p.q, (const __nv_bfloat16*)p.k, p.rq, p.rk,
+            static_cast<uint8_t*>(p.qimg), static_cast<uint8_t*>(p.kimg));
+    else
+        prep_norms_kernel<TI><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(d, (const TI*)p.q,
+                                                                         (const TI*)p.k, p.rq, p.rk);
     count_launches(2);
     return cudaPeekAtLastError();
 }

@@ -10,7 +10,7 @@
 // were read from shared memory, so S^T (as bf16 pairs) and Delta^T (hi + lo, and
 // diag(e r_k)-scaled hi + lo) are written by the epilogue threads straight into
 // TMEM, each thread its own accumulator row, and the MMAs take A from there.
-// B operands: the W and P images by bulk copy, raw q and k tiles by TMA (q is
+// B operands: the W and P images and the raw q and k images by bulk copy (q is
 // scaled by gam r_q / sqrt(Dk) in place); U rows by TMA; the per-chunk gate
 // and norm vectors by bulk copy two chunks ahead.  Output rows are accumulated in two TMEM
 // buffers so the epilogue of chunk c runs while the products of chunk c + 1 do.
@@ -23,8 +23,9 @@
 //   A1 = Obar^T P,  A2 = Sbar^T K^T  (Sbar^T as bf16 pairs in TMEM),
 //   Sbar^T <- gam_63 Sbar^T + (Obar^T diag(gam r_q / sqrt(Dk))) Q   (hi + lo),
 //   -Dbar^T = -(A1 + A2 diag(e r_k)),   Sbar^T += (-Dbar^T) W.
-// Obar, q, k tiles by TMA; P and W images by bulk copy; the Sbar'^T and -Dbar^T
-// images written back with bulk stores.  TMEM: [0, Dk) state, [Dk, Dk + 128)
+// Obar tiles by TMA two chunks ahead (double-buffered); q, k, P and W images by
+// bulk copy; the Sbar'^T image stored from registers, the -Dbar^T
+// image (double-buffered, it is also the step-4 operand) by bulk stores.  TMEM: [0, Dk) state, [Dk, Dk + 128)
 // Sbar^T bf16 pairs, then A1 and A2 (64 columns each).
 #include "gdn_internal.cuh"
 #include "gdn_tc.cuh"
@@ -155,13 +156,14 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::mbar_arrive_expect_tx(&barP, pbytes);
         tc::bulk_g2s(sm + L.P, Pimg + (bh * d.NC + c) * pbytes, pbytes, &barP);
     };
+    const int64_t kq = (int64_t)bb * d.Hk + j;  // (b, key head): q / k images of its chunks
     auto load_q = [&](int64_t c) {
         tc::mbar_arrive_expect_tx(&barQ, wbytes);
-        tc::tma_load_5d(sm + L.Q, &tm.q, 0, (int)(c * C), 0, j, bb, &barQ);
+        tc::bulk_g2s(sm + L.Q, static_cast<const uint8_t*>(p.qimg) + (kq * d.NC + c) * wbytes, wbytes, &barQ);
     };
     auto load_k = [&](int64_t c) {
         tc::mbar_arrive_expect_tx(&barK, wbytes);
-        tc::tma_load_5d(sm + L.K, &tm.k, 0, (int)(c * C), 0, j, bb, &barK);
+        tc::bulk_g2s(sm + L.K, static_cast<const uint8_t*>(p.kimg) + (kq * d.NC + c) * wbytes, wbytes, &barK);
     };
     auto load_raw = [&](int64_t c) {
         const int s = (int)(c & 1);
@@ -447,7 +449,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
 }
 
 struct TbSmem {
-    uint32_t P, K, Q, W, O, Os, Oslo, St, ND, raw, vec, total;
+    uint32_t P, K, Q, W, O, Os, Oslo, ND, raw, vec, total;
 };
 
 __host__ __device__ inline TbSmem tb_plan(int Dk) {
@@ -462,11 +464,10 @@ __host__ __device__ inline TbSmem tb_plan(int Dk) {
     s.K = take(C * Dk * 2);
     s.Q = take(C * Dk * 2);
     s.W = take(C * Dk * 2);
-    s.O = take(C * DVT * 2);    // Obar tile, panel (x = value column)
+    s.O = take(2 * C * DVT * 2);  // Obar tiles of two chunks, panel (x = value column)
     s.Os = take(C * DVT * 2);   // Obar diag(gam r_q / sqrt(Dk)), hi and lo, same layout
     s.Oslo = take(C * DVT * 2);
-    s.St = take(DVT * Dk * 2);  // Sbar'^T image staging (panel, 128 rows)
-    s.ND = take(DVT * C * 2);   // -Dbar^T (canonical, x = step): operand and image
+    s.ND = take(2 * DVT * C * 2);  // -Dbar^T of two chunks (canonical, x = step): operand and image
     s.raw = take(2 * kRawBytes);
     s.vec = take(2 * 4 * C * 4);
     s.total = o;
@@ -503,7 +504,7 @@ __device__ __forceinline__ void build_os(const uint8_t* O, uint8_t* Os, uint8_t*
 __global__ void __launch_bounds__(kThreads + 32, 1)
     bwd_scan_ta_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm) {
     extern __shared__ __align__(1024) uint8_t sm[];
-    __shared__ uint64_t bar, barW, barQ, barK, barP, barO, barR[2];
+    __shared__ uint64_t bar, barW, barQ, barK, barP, barO[2], barR[2];
     __shared__ uint32_t tmem_sh;
     const int tile = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
     const int j = h / (int)d.G;
@@ -536,15 +537,19 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::mbar_arrive_expect_tx(&barP, pbytes);
         tc::bulk_g2s(sm + L.P, Pimg + (bh * NC + c) * pbytes, pbytes, &barP);
     };
+    const int64_t kq = (int64_t)bb * d.Hk + j;  // (b, key head): q / k images of its chunks
     auto load_kq = [&](int64_t c) {
         tc::mbar_arrive_expect_tx(&barK, kbytes);
-        tc::tma_load_5d(sm + L.K, &tm.k, 0, (int)(c * C), 0, j, bb, &barK);
+        tc::bulk_g2s(sm + L.K, static_cast<const uint8_t*>(p.kimg) + (kq * NC + c) * kbytes, kbytes, &barK);
         tc::mbar_arrive_expect_tx(&barQ, kbytes);
-        tc::tma_load_5d(sm + L.Q, &tm.q, 0, (int)(c * C), 0, j, bb, &barQ);
+        tc::bulk_g2s(sm + L.Q, static_cast<const uint8_t*>(p.qimg) + (kq * NC + c) * kbytes, kbytes, &barQ);
     };
+    // Obar tile of chunk c -> buffer (NC - 1 - c) & 1
+    auto obuf = [&](int64_t c) { return sm + L.O + ((NC - 1 - c) & 1) * obytes; };
     auto load_o = [&](int64_t c) {
-        tc::mbar_arrive_expect_tx(&barO, obytes);
-        tc::tma_load_5d(sm + L.O, &tm.dO, 0, (int)(c * C), n0 / 8, h, bb, &barO);
+        uint64_t* b = &barO[(NC - 1 - c) & 1];
+        tc::mbar_arrive_expect_tx(b, obytes);
+        tc::tma_load_5d(obuf(c), &tm.dO, 0, (int)(c * C), n0 / 8, h, bb, b);
     };
     auto load_raw = [&](int64_t c) {
         const int s = (int)((NC - 1 - c) & 1);
@@ -554,16 +559,10 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::bulk_g2s(dst + C * 8, p.rq + ((int64_t)bb * d.Hk + j) * d.Tp + c * C, C * 4, &barR[s]);
         tc::bulk_g2s(dst + C * 12, p.rk + ((int64_t)bb * d.Hk + j) * d.Tp + c * C, C * 4, &barR[s]);
     };
-    auto store_images = [&](int64_t c) {  // storer; the caller commits
-        uint8_t* img = dsimg + (bh * NC + c) * (int64_t)Dk * Dv * 2;
-        if (DVT == Dv) {
-            tc::bulk_s2g(img, sm + L.St, (uint32_t)(DVT * Dk * 2));
-        } else {
-            for (int gi = 0; gi < Dk / 8; ++gi)
-                tc::bulk_s2g(img + (size_t)gi * Dv * 16 + (size_t)n0 * 16, sm + L.St + gi * DVT * 16,
-                             (uint32_t)(DVT * 16));
-        }
-        tc::bulk_s2g(dbimg + (bh * NC + c) * (int64_t)C * Dv * 2 + (int64_t)n0 * 128, sm + L.ND,
+    // -Dbar^T tile of chunk c (and its image source) -> buffer (NC - 1 - c) & 1
+    auto ndbuf = [&](int64_t c) { return sm + L.ND + ((NC - 1 - c) & 1) * (uint32_t)(DVT * C * 2); };
+    auto store_dbar = [&](int64_t c) {  // storer; the caller commits
+        tc::bulk_s2g(dbimg + (bh * NC + c) * (int64_t)C * Dv * 2 + (int64_t)n0 * 128, ndbuf(c),
                      (uint32_t)(DVT * 128));
     };
 
@@ -577,7 +576,8 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::mbar_init(&barQ, 1);
         tc::mbar_init(&barK, 1);
         tc::mbar_init(&barP, 1);
-        tc::mbar_init(&barO, 1);
+        tc::mbar_init(&barO[0], 1);
+        tc::mbar_init(&barO[1], 1);
         tc::mbar_init(&barR[0], 1);
         tc::mbar_init(&barR[1], 1);
         tc::fence_mbar_init();
@@ -588,6 +588,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         load_kq(NC - 1);
         load_p(NC - 1);
         load_o(NC - 1);
+        if (NC > 1) load_o(NC - 2);
         load_raw(NC - 1);
         if (NC > 1) load_raw(NC - 2);
     }
@@ -607,16 +608,16 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         }
         tc::tmem_wait_st();
         ok = tc::mbar_wait(&barR[0], 0, &g_err_scanta);
-        ok = tc::mbar_wait(&barO, 0, &g_err_scanta) && ok;
+        ok = tc::mbar_wait(&barO[0], 0, &g_err_scanta) && ok;
         vectors_from_raw(sm + L.raw, reinterpret_cast<float*>(sm + L.vec), Dk);
-        build_os(sm + L.O, sm + L.Os, sm + L.Oslo, sm + L.raw, Dk);
+        build_os(obuf(NC - 1), sm + L.Os, sm + L.Oslo, sm + L.raw, Dk);
         tc::fence_async_smem();
     }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
 
-    const tc::Tile tOmn = tc::panel_tile(sm + L.O, C, false);      // A = Obar^T: x = dv = M
+    // A = Obar^T: x = dv = M (tile of the current chunk's buffer, below)
     const tc::Tile tOsmn = tc::panel_tile(sm + L.Os, C, false);
     const tc::Tile tOslomn = tc::panel_tile(sm + L.Oslo, C, false);
     const tc::Tile tPmn = tc::panel_tile(sm + L.P, C, false);      // B = P: x = s = N
@@ -624,7 +625,6 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     const tc::Tile tQmn = tc::panel_tile(sm + L.Q, C, false);      // B = Q: x = dk = N
     const tc::Tile tWmn = tc::panel_tile(sm + L.W, C, false);      // B = W: x = dk = N
     tc::Tile tND;                                                  // A = -Dbar^T: x = t = K
-    tND.base = tc::smem_u32(sm + L.ND);
     tND.xs = 128;
     tND.ys = (uint32_t)C * 16u;
     tND.k_major = true;
@@ -659,10 +659,12 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             }
             tc::tmem_wait_st();
         }
-        if (storer) tc::bulk_wait_read_all();  // images of chunk c + 1 read out of St / ND
+        if (storer) tc::bulk_wait_read_but1();  // -Dbar image of chunk c + 2 read out of its buffer
         tc::tc_fence_before();
         __syncthreads();  // (B)
         tc::tc_fence_after();
+        const tc::Tile tOmn = tc::panel_tile(obuf(c), C, false);
+        tND.base = tc::smem_u32(ndbuf(c));
         if (prod) {
             // step 2: A1 = Obar^T P, A2 = Sbar^T K^T, Sbar^T += Os Q + Oslo Q, with the
             // three accumulation chains interleaved
@@ -683,20 +685,22 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             tc::mma_commit(&bar);
             ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
             phase ^= 1u;
-            if (c > 0) {  // Obar, P, K, Q tiles are free
-                load_o(c - 1);
+            if (c > 0) {  // P, K, Q tiles (and this chunk's Obar buffer) are free
+                if (c > 1) load_o(c - 2);
                 load_p(c - 1);
                 load_kq(c - 1);
             }
         } else if (epi) {
-            // meanwhile: the Sbar'^T image (from the A operand)
+            // meanwhile: the Sbar'^T image, straight from the A operand to global
+            // memory (each warp store covers 32 consecutive 16-byte rows of a panel)
+            uint8_t* img = dsimg + (bh * NC + c) * (int64_t)Dk * Dv * 2;
             for (int cb = g * (Dk / 4); cb < (g + 1) * (Dk / 4); cb += 16) {
                 uint32_t w[16];
                 tc::tmem_ld16u(tc::tmem_addr(tb, lb, aop + cb), w);
                 tc::tmem_wait_ld();
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4)
-                    *reinterpret_cast<uint4*>(sm + L.St + tc::panel_off(2 * cb + 8 * q4, r, DVT)) =
+                    *reinterpret_cast<uint4*>(img + tc::panel_off(2 * cb + 8 * q4, n0 + r, Dv)) =
                         make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
             }
             ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
@@ -720,7 +724,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             }
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4)
-                *reinterpret_cast<uint4*>(sm + L.ND + canon(32 * g + 8 * q4, r, C)) =
+                *reinterpret_cast<uint4*>(ndbuf(c) + canon(32 * g + 8 * q4, r, C)) =
                     make_uint4(nd[4 * q4], nd[4 * q4 + 1], nd[4 * q4 + 2], nd[4 * q4 + 3]);
             tc::fence_async_smem();
         }
@@ -738,15 +742,15 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             if (c > 1) load_raw(c - 2);
         } else if (epi) {
             if (storer) {
-                store_images(c);
+                store_dbar(c);
                 tc::bulk_commit();
             }
             if (c > 0) {  // vectors and the scaled Obar operands of chunk c - 1
                 const uint8_t* raw = sm + L.raw + ((m + 1) & 1) * kRawBytes;
                 ok = tc::mbar_wait(&barR[(m + 1) & 1], (uint32_t)(((m + 1) >> 1) & 1), &g_err_scanta) && ok;
                 vectors_from_raw(raw, reinterpret_cast<float*>(sm + L.vec) + ((m + 1) & 1) * 4 * C, Dk);
-                ok = tc::mbar_wait(&barO, (uint32_t)((m + 1) & 1), &g_err_scanta) && ok;
-                build_os(sm + L.O, sm + L.Os, sm + L.Oslo, raw, Dk);
+                ok = tc::mbar_wait(&barO[(m + 1) & 1], (uint32_t)(((m + 1) >> 1) & 1), &g_err_scanta) && ok;
+                build_os(obuf(c - 1), sm + L.Os, sm + L.Oslo, raw, Dk);
                 tc::fence_async_smem();
             }
             ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
