@@ -120,11 +120,6 @@ __device__ __forceinline__ uint32_t canon(int x, int y, int ncols) {
     return (uint32_t)(x >> 3) * 128u + (uint32_t)(y >> 3) * (uint32_t)ncols * 16u +
            (uint32_t)(y & 7) * 16u + (uint32_t)(x & 7) * 2u;
 }
-// 16 consecutive elements (x0 multiple of 8) of row y of a canonical bf16 tile
-__device__ __forceinline__ void tile_row16(const uint8_t* tile, int ncols, int x0, int y, float* v) {
-    ld_bf16x8(tile + canon(x0, y, ncols), v);
-    ld_bf16x8(tile + canon(x0 + 8, y, ncols), v + 8);
-}
 // 16 consecutive elements (x0 multiple of 8) of row y of a 64-row panel tile
 __device__ __forceinline__ void panel_row16(const uint8_t* tile, int x0, int y, float* v) {
     ld_bf16x8(tile + tc::panel_off(x0, y, C), v);
