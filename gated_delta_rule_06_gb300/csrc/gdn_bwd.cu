@@ -500,14 +500,16 @@ __global__ void __launch_bounds__(256) bwd_qk_kernel(Dims d, Ptrs p) {
     }
 }
 
-// da / db and per-(b, chunk, head) partial sums; grid (NC, B, ceil(Hv / 64))
+// da / db and per-(b, chunk, head) partial sums; grid (NC, B, ceil(Hv / 8)),
+// one warp per head in the sums
+constexpr int kGateHeadsB = 8;
 template <typename TI>
 __global__ void __launch_bounds__(256) bwd_gate_kernel(Dims d, Ptrs p) {
-    __shared__ float sA[kChunk][65];
-    __shared__ float sD[kChunk][65];
+    __shared__ float sA[kChunk][kGateHeadsB + 1];
+    __shared__ float sD[kChunk][kGateHeadsB + 1];
     const int c = blockIdx.x, bb = blockIdx.y;
-    const int h0 = blockIdx.z * 64;
-    const int nh = (int)(d.Hv - h0 < 64 ? d.Hv - h0 : 64);
+    const int h0 = blockIdx.z * kGateHeadsB;
+    const int nh = (int)(d.Hv - h0 < kGateHeadsB ? d.Hv - h0 : kGateHeadsB);
     const int64_t t0 = (int64_t)c * kChunk;
     const TI* a = (const TI*)p.a;
     TI* da = (TI*)p.da;
@@ -602,7 +604,7 @@ template <typename TI>
 cudaError_t launch_reduce_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
     const int64_t rows = d.B * d.T * d.Hk;
     bwd_qk_kernel<TI><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(d, p);
-    dim3 g((unsigned)d.NC, (unsigned)d.B, (unsigned)((d.Hv + 63) / 64));
+    dim3 g((unsigned)d.NC, (unsigned)d.B, (unsigned)((d.Hv + kGateHeadsB - 1) / kGateHeadsB));
     bwd_gate_kernel<TI><<<g, 256, 0, s>>>(d, p);
     bwd_head_sum_kernel<<<(unsigned)((d.Hv + 127) / 128), 128, 0, s>>>(d, p);
     count_launches(3);

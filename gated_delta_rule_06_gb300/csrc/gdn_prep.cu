@@ -14,7 +14,7 @@
 namespace gdn {
 namespace {
 
-constexpr int kGateHeads = 64;  // heads handled per CTA of the gate kernel
+constexpr int kGateHeads = 8;  // heads per CTA of the gate kernel: one warp each, many CTAs
 
 template <typename TI>
 __global__ void __launch_bounds__(256) prep_gates_kernel(Dims d, const TI* __restrict__ a,
