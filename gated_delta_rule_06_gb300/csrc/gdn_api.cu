@@ -107,8 +107,9 @@ Layout make_layout(const gdn::Dims& d) {
     o = 0;
     L.dSck = o; o = align_up(o + state_ck);
     L.Dbar = o; o = align_up(o + perstep * d.Dv * img);
-    L.dqh = o; o = align_up(o + perstep * d.Dk * 4);
-    L.dkh = o; o = align_up(o + perstep * d.Dk * 4);
+    // per-value-head q / k cotangents: bf16 on the tensor-core path, else fp32
+    L.dqh = o; o = align_up(o + perstep * d.Dk * img);
+    L.dkh = o; o = align_up(o + perstep * d.Dk * img);
     L.dl = o; o = align_up(o + perstep * 4);
     L.dbeta = o; o = align_up(o + perstep * 4);
     L.part = o; o = align_up(o + 2 * (size_t)d.B * d.NC * d.Hv * 4);

@@ -434,7 +434,15 @@ __device__ __forceinline__ void st4x(__nv_bfloat16* o, const float* v) {
     *reinterpret_cast<uint2*>(o) = u;
 }
 
-template <typename TI>
+__device__ __forceinline__ float4 ldp4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ldp4(const __nv_bfloat16* p) {
+    float v[4];
+    ld4x(p, v);
+    return make_float4(v[0], v[1], v[2], v[3]);
+}
+
+// TI: input dtype; PT: dtype of the per-value-head partials
+template <typename TI, typename PT>
 __global__ void __launch_bounds__(256) bwd_qk_kernel(Dims d, Ptrs p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;  // over (b, t, j)
@@ -457,8 +465,8 @@ __global__ void __launch_bounds__(256) bwd_qk_kernel(Dims d, Ptrs p) {
             const int q4 = lane + 32 * i;
             if (q4 < Dk4) {
                 const int64_t off = off0 + g * hstride + 4 * q4;
-                add4(y[0][i], *reinterpret_cast<const float4*>(p.dqh + off));
-                add4(y[1][i], *reinterpret_cast<const float4*>(p.dkh + off));
+                add4(y[0][i], ldp4(reinterpret_cast<const PT*>(p.dqh) + off));
+                add4(y[1][i], ldp4(reinterpret_cast<const PT*>(p.dkh) + off));
             }
         }
     }
@@ -603,7 +611,10 @@ cudaError_t launch_bchunk_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
 template <typename TI>
 cudaError_t launch_reduce_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
     const int64_t rows = d.B * d.T * d.Hk;
-    bwd_qk_kernel<TI><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(d, p);
+    if (tc_path(d))
+        bwd_qk_kernel<TI, __nv_bfloat16><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(d, p);
+    else
+        bwd_qk_kernel<TI, float><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(d, p);
     dim3 g((unsigned)d.NC, (unsigned)d.B, (unsigned)((d.Hv + kGateHeadsB - 1) / kGateHeadsB));
     bwd_gate_kernel<TI><<<g, 256, 0, s>>>(d, p);
     bwd_head_sum_kernel<<<(unsigned)((d.Hv + 127) / 128), 128, 0, s>>>(d, p);

@@ -706,11 +706,16 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     }
     if (epi) sync_after_mma(&bar, phase, ok);
     if (epi && ok) {
+        // per-value-head partials as bf16 (summed over the group and normalised in fp32)
+        uint8_t* dqh = reinterpret_cast<uint8_t*>(p.dqh) + (gbase * Dk) * 2;
+        uint8_t* dkh = reinterpret_cast<uint8_t*>(p.dkh) + (gbase * Dk) * 2;
         acc_rows4(tb, kAQ, Dk, [&](int r, int c0, const float (&x)[16]) {
-            st16f(p.dqh + (gbase + r) * Dk + c0, x);
+            st_bf16x8(dqh + ((int64_t)r * Dk + c0) * 2, x);
+            st_bf16x8(dqh + ((int64_t)r * Dk + c0 + 8) * 2, x + 8);
         });
         acc_rows4(tb, kAK, Dk, [&](int r, int c0, const float (&x)[16]) {
-            st16f(p.dkh + (gbase + r) * Dk + c0, x);
+            st_bf16x8(dkh + ((int64_t)r * Dk + c0) * 2, x);
+            st_bf16x8(dkh + ((int64_t)r * Dk + c0 + 8) * 2, x + 8);
         });
     }
     tc::tc_fence_before();
