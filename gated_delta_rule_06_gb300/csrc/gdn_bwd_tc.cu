@@ -250,9 +250,10 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     bwd_chunk_tc_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm) {
     extern __shared__ __align__(1024) uint8_t sm[];
     // bar: MMA rounds outside phase 1; barM / barE: phase-1 products of block b
-    // done / block b's epilogue done (two of each, by block parity); barG: block
-    // b's tiles read by the <S, Sbar'> sums; barOV, barL, barKQ, barS: arrivals
-    __shared__ uint64_t bar, barOV, barL, barKQ, barS, barG, barM[2], barE[2];
+    // done / block b's epilogue done (two of each, by block parity); barMa: block
+    // b's products with S done; barG: block b's tiles read by the <S, Sbar'> sums;
+    // barOV, barL, barKQ, barSa / barSb (S / Sbar' halves of a block): arrivals
+    __shared__ uint64_t bar, barOV, barL, barKQ, barSa, barSb, barMa, barG, barM[2], barE[2];
     __shared__ uint32_t tmem_base_sh;
     const int c = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
     const int j = h / (int)d.G;
@@ -304,11 +305,16 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     // buffer in the space of the V tile, free once phase 0 is done)
     const int nblk = (Dk + kBlkK - 1) / kBlkK;
     auto nkb = [&](int b) { return Dk - b * kBlkK < kBlkK ? Dk - b * kBlkK : kBlkK; };
-    auto load_blk = [&](int b) {
+    // the S half of the buffer at L.V, the Sbar' half one full block further
+    auto load_s = [&](int b) {
         const uint32_t bytes = (uint32_t)(nkb(b) * Dv * 2);
-        tc::mbar_arrive_expect_tx(&barS, 2 * bytes);
-        tc::bulk_g2s(sm + L.V, ck_img + (int64_t)b * blk, bytes, &barS);
-        tc::bulk_g2s(sm + L.V + bytes, ds_img + (int64_t)b * blk, bytes, &barS);
+        tc::mbar_arrive_expect_tx(&barSa, bytes);
+        tc::bulk_g2s(sm + L.V, ck_img + (int64_t)b * blk, bytes, &barSa);
+    };
+    auto load_sp = [&](int b) {
+        const uint32_t bytes = (uint32_t)(nkb(b) * Dv * 2);
+        tc::mbar_arrive_expect_tx(&barSb, bytes);
+        tc::bulk_g2s(sm + L.V + blk, ds_img + (int64_t)b * blk, bytes, &barSb);
     };
     // ---- operands, all issued by the producer: raw dO, v (phase 0) by TMA in the
     // panel layout; the k, q images, Delta (hi + lo), -Dbar and T by bulk copies
@@ -321,7 +327,9 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::mbar_init(&barOV, 1);
         tc::mbar_init(&barL, 1);
         tc::mbar_init(&barKQ, 1);
-        tc::mbar_init(&barS, 1);
+        tc::mbar_init(&barSa, 1);
+        tc::mbar_init(&barSb, 1);
+        tc::mbar_init(&barMa, 1);
         tc::mbar_init(&barG, kThreads);
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&barM[i], 1);
@@ -424,46 +432,53 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     }
     cta_sync_tc();  // phase-0 reads of TMEM and of the V tile are done
 
-    // ---- phase 1: state products per kBlkK-wide block of Dk through one buffer:
-    // the producer issues block b's products once its S / Sbar' block has landed
-    // (and the epilogue of block b - 2 has released its Wbar scratch: S1 for even,
-    // S2 for odd blocks), and loads block b + 1 as soon as block b's products and
-    // <S, Sbar'> sums have read the buffer, so the load overlaps block b's
-    // epilogue.  Obar S^T and Delta Sbar'^T land in the dq / dk accumulators and
-    // are rescaled there by gam and e.
+    // ---- phase 1: state products per kBlkK-wide block of Dk through one buffer
+    // of two halves, S and Sbar'.  The producer issues block b's products with S
+    // (Obar S^T, -Dbar S^T) as soon as its S half has landed (and the epilogue of
+    // block b - 2 has released its Wbar scratch: S1 for even, S2 for odd blocks),
+    // then those with Sbar' (Delta Sbar'^T); each half of block b + 1 loads as
+    // soon as the products (and the <S, Sbar'> sums) that read it are done, so
+    // the loads overlap the other half's products and the epilogues.  Obar S^T and
+    // Delta Sbar'^T land in the dq / dk accumulators, rescaled there by gam and e.
     float gcb = 0.f;
     if (prod) {
-        load_blk(0);
+        load_s(0);
+        load_sp(0);
         for (int b = 0; b < nblk; ++b) {
             const int dk0 = b * kBlkK, nk = nkb(b);
             const uint32_t par = (uint32_t)b & 1u;
-            ok = tc::mbar_wait(&barS, par, &g_err_bwdtc) && ok;
+            ok = tc::mbar_wait(&barSa, par, &g_err_bwdtc) && ok;
             if (b >= 2) ok = tc::mbar_wait(&barE[b & 1], (uint32_t)((b - 2) >> 1) & 1u, &g_err_bwdtc) && ok;
             const tc::Tile tS = tc::panel_tile(sm + L.V, Dv, false);
-            const tc::Tile tSp = tc::panel_tile(sm + L.V + nk * Dv * 2, Dv, false);
+            const tc::Tile tSp = tc::panel_tile(sm + L.V + blk, Dv, false);
             const uint32_t wcol = (b & 1) ? kS2 : kS1;
             tc::mma_tile(tb + kAQ + dk0, tO, tS, C, nk, Dv, false);
             tc::mma_tile(tb + wcol, tNBmn, tS, C, nk, Dv, false);
+            tc::mma_commit(&barMa);
+            ok = tc::mbar_wait(&barSb, par, &g_err_bwdtc) && ok;
             tc::mma_tile(tb + kAK + dk0, tDmn, tSp, C, nk, Dv, false);
             tc::mma_tile(tb + kAK + dk0, tDlomn, tSp, C, nk, Dv, true);
             tc::mma_commit(&barM[b & 1]);
-            if (b + 1 < nblk) {  // the buffer is free once the products and the sums have read it
-                ok = tc::mbar_wait(&barM[b & 1], (uint32_t)(b >> 1) & 1u, &g_err_bwdtc) && ok;
+            if (b + 1 < nblk) {
+                ok = tc::mbar_wait(&barMa, par, &g_err_bwdtc) && ok;
                 ok = tc::mbar_wait(&barG, par, &g_err_bwdtc) && ok;
-                load_blk(b + 1);
+                load_s(b + 1);
+                ok = tc::mbar_wait(&barM[b & 1], (uint32_t)(b >> 1) & 1u, &g_err_bwdtc) && ok;
+                load_sp(b + 1);
             }
         }
     } else if (epi) {
         ok = tc::mbar_wait(&barKQ, 0, &g_err_bwdtc) && ok;
         for (int b = 0; b < nblk; ++b) {
             const int dk0 = b * kBlkK, nk = nkb(b);
-            ok = tc::mbar_wait(&barS, (uint32_t)b & 1u, &g_err_bwdtc) && ok;
+            ok = tc::mbar_wait(&barSa, (uint32_t)b & 1u, &g_err_bwdtc) && ok;
+            ok = tc::mbar_wait(&barSb, (uint32_t)b & 1u, &g_err_bwdtc) && ok;
             const uint8_t* sS = sm + L.V;
             const int bytes = nk * Dv * 2;
             for (int e = tid; e < bytes / 16; e += kThreads) {
                 float a8[8], b8[8];
                 ld_bf16x8(sS + 16 * e, a8);
-                ld_bf16x8(sS + bytes + 16 * e, b8);
+                ld_bf16x8(sS + blk + 16 * e, b8);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) gcb = fmaf(a8[i], b8[i], gcb);
             }
@@ -500,7 +515,10 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             tc::tc_fence_before();
             tc::mbar_arrive(&barE[b & 1]);
         }
-        red[tid] = gcb;
+        // <S, Sbar'> of this CTA: warp sums by a fixed shuffle tree, then in warp order
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) gcb += __shfl_xor_sync(0xffffffffu, gcb, off);
+        if (lane == 0) red[warp] = gcb;
     }
     cta_sync_tc();  // phase 1 done: its operand space (under the phase-2/3 scratch) is free
     // diag(beta gam) T^T as an operand: T image columns scaled by beta gam
@@ -523,11 +541,9 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::mma_tile(tb + kS2, tK, tK, C, C, Dk, false);
         tc::mma_commit(&bar);
     }
-    for (int s = kThreads / 2; s > 0; s >>= 1) {  // <Sbar', S>, fixed-order tree
-        if (tid < s) red[tid] += red[tid + s];
-        __syncthreads();
-    }
-    const float gCb = red[0];
+    float gCb = 0.f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) gCb += red[w];
     float* Gkk = reinterpret_cast<float*>(sm + L.Gkk);
     float* Gqk = reinterpret_cast<float*>(sm + L.Gqk);
     float* ZP = Gqk;  // T o (Wbar K^T), until Gqk is formed in phase 2
