@@ -9,35 +9,79 @@
 //     o = g r + delta <kh, qh>                      (= S'^T qh)
 //     S' = g S + kh delta^T                         (written once)
 // A masked step is the identity (g = 1, beta = 0).  The kernel is bound by
-// HBM traffic (2 Dk Dv 4 bytes per head); it uses 16-byte vector loads and
-// stores, warp shuffles and one shared-memory exchange, no tensor cores.
+// HBM traffic (2 Dk Dv 4 bytes per head).  One CTA per (b, h): a single bulk
+// copy brings the head's state into shared memory while the norms and gates
+// are computed, the step runs out of shared memory (16-byte accesses, warp
+// shuffles), and a single bulk store writes the new state back.  Shared
+// memory, not registers, holds the state, so several CTAs share an SM and
+// keep enough bytes in flight.
 #include "gdn_internal.cuh"
+#include "gdn_tc.cuh"
 
 namespace gdn {
+
+GDN_ERROR_WORD(decode)
+
 namespace {
 
-constexpr int kDecodeThreads = 512;
-constexpr int kDecodeRows = 16;  // max state rows per thread (held in registers)
+constexpr int kDecThreads = 256;
+
+struct DecPlan {
+    int ncg, R;           // float4 column groups, row groups
+    size_t S, qh, kh, pr, rr, red, total;
+};
+__host__ __device__ inline DecPlan dec_plan(int Dk, int Dv) {
+    DecPlan pl{};
+    pl.ncg = Dv / 4;
+    pl.R = kDecThreads / pl.ncg;
+    size_t o = 0;
+    pl.S = o;   o += (size_t)Dk * Dv * 4;
+    pl.qh = o;  o += (size_t)Dk * 4;
+    pl.kh = o;  o += (size_t)Dk * 4;
+    pl.pr = o;  o += (size_t)pl.R * Dv * 4;  // partial S^T kh per row group
+    pl.rr = o;  o += (size_t)pl.R * Dv * 4;  // partial S^T qh per row group
+    pl.red = o; o += 64 * 4;
+    pl.total = o;
+    return pl;
+}
 
 template <typename TI>
-__global__ void __launch_bounds__(kDecodeThreads) decode_kernel(Dims d, Ptrs p) {
-    extern __shared__ float sm[];
+__global__ void __launch_bounds__(kDecThreads) decode_kernel(Dims d, Ptrs p) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ uint64_t bar;
     const int h = blockIdx.x, bb = blockIdx.y;
     const int j = h / (int)d.G;
     const int Dk = (int)d.Dk, Dv = (int)d.Dv;
-    const int ncg = Dv / 4;                   // float4 column groups
-    const int R = kDecodeThreads / ncg;       // row groups
-    float* qh = sm;                           // [Dk]
-    float* kh = qh + Dk;                      // [Dk]
-    float* pr = kh + Dk;                      // [R][Dv] partial S^T k
-    float* rr = pr + R * Dv;                  // [R][Dv] partial S^T q
-    float* red = rr + R * Dv;                 // [64] scalars
-
+    const DecPlan pl = dec_plan(Dk, Dv);
+    const int ncg = pl.ncg, R = pl.R;
+    float* S = reinterpret_cast<float*>(dsm + pl.S);
+    float* qh = reinterpret_cast<float*>(dsm + pl.qh);
+    float* kh = reinterpret_cast<float*>(dsm + pl.kh);
+    float* pr = reinterpret_cast<float*>(dsm + pl.pr);
+    float* rr = reinterpret_cast<float*>(dsm + pl.rr);
+    float* red = reinterpret_cast<float*>(dsm + pl.red);
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
+    const int64_t sbase = ((int64_t)bb * d.Hv + h) * Dk * Dv;
+    const uint32_t sbytes = (uint32_t)Dk * (uint32_t)Dv * 4u;
+
+    if (tid == 0) {
+        tc::mbar_init(&bar, 1);
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    if (p.state0) {
+        if (tid == 0) {  // the whole state of the head, in flight during the prelude
+            tc::mbar_arrive_expect_tx(&bar, sbytes);
+            tc::bulk_g2s(S, p.state0 + sbase, sbytes, &bar);
+        }
+    } else {
+        for (int i = tid; i < Dk * Dv / 4; i += kDecThreads)
+            reinterpret_cast<float4*>(S)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     const TI* q = (const TI*)p.q + ((int64_t)bb * d.Hk + j) * Dk;
     const TI* k = (const TI*)p.k + ((int64_t)bb * d.Hk + j) * Dk;
-    // L2 norms of q and k (warp 0 and warp 1), gates (warp 2)
+    // L2 norms of q and k (warps 0 and 1), gates (warp 2)
     if (warp < 2) {
         const TI* x = warp == 0 ? q : k;
         float s = 0.f;
@@ -62,31 +106,26 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(Dims d, Ptrs p) 
     }
     __syncthreads();
     const float qs = red[0] * rsqrtf((float)Dk), ks = red[1];
-    for (int i = tid; i < Dk; i += blockDim.x) {
+    for (int i = tid; i < Dk; i += kDecThreads) {
         qh[i] = ldf(q + i) * qs;
         kh[i] = ldf(k + i) * ks;
     }
     __syncthreads();
     const float g = red[2], be = red[3];
+    bool ok = true;
+    if (p.state0) ok = tc::mbar_wait(&bar, 0, &g_err_decode);
     const int cg = tid % ncg, rg = tid / ncg;
     const bool active = rg < R;
-    const int64_t sbase = ((int64_t)bb * d.Hv + h) * Dk * Dv;
-    const float4* S4 = reinterpret_cast<const float4*>(p.state0 ? p.state0 + sbase : nullptr);
-    float4 Sreg[kDecodeRows];
+    float4* S4 = reinterpret_cast<float4*>(S);
     float4 pp = make_float4(0.f, 0.f, 0.f, 0.f), rp = pp;
     if (active) {
-#pragma unroll
-        for (int m = 0; m < kDecodeRows; ++m) {
-            const int x = rg + m * R;
-            if (x < Dk) {
-                const float4 s = p.state0 ? S4[(int64_t)x * ncg + cg] : make_float4(0.f, 0.f, 0.f, 0.f);
-                Sreg[m] = s;
-                const float kx = kh[x], qx = qh[x];
-                pp.x = fmaf(s.x, kx, pp.x); pp.y = fmaf(s.y, kx, pp.y);
-                pp.z = fmaf(s.z, kx, pp.z); pp.w = fmaf(s.w, kx, pp.w);
-                rp.x = fmaf(s.x, qx, rp.x); rp.y = fmaf(s.y, qx, rp.y);
-                rp.z = fmaf(s.z, qx, rp.z); rp.w = fmaf(s.w, qx, rp.w);
-            }
+        for (int x = rg; x < Dk; x += R) {
+            const float4 s = S4[x * ncg + cg];
+            const float kx = kh[x], qx = qh[x];
+            pp.x = fmaf(s.x, kx, pp.x); pp.y = fmaf(s.y, kx, pp.y);
+            pp.z = fmaf(s.z, kx, pp.z); pp.w = fmaf(s.w, kx, pp.w);
+            rp.x = fmaf(s.x, qx, rp.x); rp.y = fmaf(s.y, qx, rp.y);
+            rp.z = fmaf(s.z, qx, rp.z); rp.w = fmaf(s.w, qx, rp.w);
         }
         reinterpret_cast<float4*>(pr + rg * Dv)[cg] = pp;
         reinterpret_cast<float4*>(rr + rg * Dv)[cg] = rp;
@@ -101,7 +140,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(Dims d, Ptrs p) 
     }
     __syncthreads();
     // column sums over the row groups in fixed order -> delta, o
-    for (int c = tid; c < Dv; c += blockDim.x) {
+    for (int c = tid; c < Dv; c += kDecThreads) {
         float ps = 0.f, rs = 0.f;
         for (int r = 0; r < R; ++r) {
             ps += pr[r * Dv + c];
@@ -110,51 +149,48 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(Dims d, Ptrs p) 
         const int64_t vo = ((int64_t)bb * d.Hv + h) * Dv + c;
         const float dlt = be * (ldf((const TI*)p.v + vo) - g * ps);
         stf((TI*)p.o + vo, g * rs + dlt * red[4]);
-        rr[c] = dlt;  // row 0 of rr is free once every thread has summed it
+        rr[c] = dlt;  // row 0 of rr: only this thread reads column c
     }
     __syncthreads();
     if (active) {
         const float4 dv4 = reinterpret_cast<const float4*>(rr)[cg];
-        float4* O4 = reinterpret_cast<float4*>(p.state_T + sbase);
-#pragma unroll
-        for (int m = 0; m < kDecodeRows; ++m) {
-            const int x = rg + m * R;
-            if (x < Dk) {
-                const float kx = kh[x];
-                float4 s = Sreg[m];
-                s.x = fmaf(g, s.x, kx * dv4.x); s.y = fmaf(g, s.y, kx * dv4.y);
-                s.z = fmaf(g, s.z, kx * dv4.z); s.w = fmaf(g, s.w, kx * dv4.w);
-                O4[(int64_t)x * ncg + cg] = s;
-            }
+        for (int x = rg; x < Dk; x += R) {
+            const float kx = kh[x];
+            float4 s = S4[x * ncg + cg];
+            s.x = fmaf(g, s.x, kx * dv4.x); s.y = fmaf(g, s.y, kx * dv4.y);
+            s.z = fmaf(g, s.z, kx * dv4.z); s.w = fmaf(g, s.w, kx * dv4.w);
+            S4[x * ncg + cg] = s;
         }
+    }
+    tc::fence_async_smem();  // the new state, written by plain stores -> the bulk store
+    __syncthreads();
+    if (tid == 0 && ok) {
+        tc::bulk_s2g(p.state_T + sbase, S, sbytes);
+        tc::bulk_commit();
+        tc::bulk_wait_all();
     }
 }
 
 }  // namespace
 
 bool decode_supported(int64_t Dk, int64_t Dv) {
-    if (Dv % 4 != 0) return false;
-    const int64_t ncg = Dv / 4;
-    if (ncg > kDecodeThreads) return false;
-    const int64_t R = kDecodeThreads / ncg;
-    return (Dk + R - 1) / R <= kDecodeRows;
+    if (Dv % 4 != 0 || Dv / 4 > kDecThreads || kDecThreads % (Dv / 4) != 0) return false;
+    return dec_plan((int)Dk, (int)Dv).total + 1024 <= 227u * 1024u;
 }
 
 cudaError_t launch_decode(const Dims& d, const Ptrs& p, cudaStream_t s) {
-    const int ncg = (int)(d.Dv / 4);
-    const int R = kDecodeThreads / ncg;
-    const size_t smem = sizeof(float) * (2 * d.Dk + 2 * (size_t)R * d.Dv + 64);
+    const size_t smem = dec_plan((int)d.Dk, (int)d.Dv).total;
     dim3 grid((unsigned)d.Hv, (unsigned)d.B);
     if (d.dtype == 1) {
         auto kern = decode_kernel<__nv_bfloat16>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        kern<<<grid, kDecodeThreads, smem, s>>>(d, p);
+        kern<<<grid, kDecThreads, smem, s>>>(d, p);
     } else {
         auto kern = decode_kernel<float>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        kern<<<grid, kDecodeThreads, smem, s>>>(d, p);
+        kern<<<grid, kDecThreads, smem, s>>>(d, p);
     }
     count_launches(1);
     return cudaPeekAtLastError();
