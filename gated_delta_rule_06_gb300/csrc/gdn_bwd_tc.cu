@@ -111,11 +111,6 @@ __device__ __forceinline__ void ld_bf16x8(const uint8_t* src, float* v) {
         v[2 * i + 1] = f.y;
     }
 }
-__device__ __forceinline__ void st16f(float* dst, const float* v) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        reinterpret_cast<float4*>(dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-}
 __device__ __forceinline__ uint32_t canon(int x, int y, int ncols) {
     return (uint32_t)(x >> 3) * 128u + (uint32_t)(y >> 3) * (uint32_t)ncols * 16u +
            (uint32_t)(y & 7) * 16u + (uint32_t)(x & 7) * 2u;

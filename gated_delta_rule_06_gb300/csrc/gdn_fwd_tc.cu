@@ -66,17 +66,26 @@ __device__ __forceinline__ tc::Tile tile_of(uint8_t* p, int ncols, bool k_major)
     return t;
 }
 
-// M = 64 accumulator walk: warp w reads rows 16 (w % 4) .. +15, column half w / 4
+// M = 64 accumulator walk (rows 16 (w % 4) .. +15 in warp w, column half w / 4)
+// with all 32 lanes: lane l < 16 takes columns c .. c + 7 of row
+// 16 (w % 4) + l, lane l + 16 columns c + 8 .. c + 15 of that row (handed over
+// by shuffles); f(row, first column, 8 values)
 template <typename F>
-__device__ __forceinline__ void acc_rows(uint32_t tbase, uint32_t col0, int ncols, F&& f) {
+__device__ __forceinline__ void acc_rows_all(uint32_t tbase, uint32_t col0, int ncols, F&& f) {
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    const int sp = w & 3, g = w >> 2;
+    const int sp = w & 3, g = w >> 2, hl = l >> 4;
     const int half = ncols / 2;
     for (int c = g * half; c < (g + 1) * half; c += 16) {
         float v[16];
         tc::tmem_ld16(tc::tmem_addr(tbase, 32 * sp, col0 + c), v);
         tc::tmem_wait_ld();
-        if (l < 16) f(16 * sp + l, c, v);
+        float x[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float up = __shfl_sync(0xffffffffu, v[8 + i], l & 15);
+            x[i] = hl ? up : v[i];
+        }
+        f(16 * sp + (l & 15), c + 8 * hl, x);
     }
 }
 
@@ -89,10 +98,10 @@ constexpr int LDT = C + 4;
 // first, then the block sub-diagonals d = 1, 2, 3 with
 //   T_ij = -T_ii * sum_{k=j}^{i-1} A_ik T_kj.
 // X is 64 x 64 scratch.  All threads of the CTA take part; ends synchronised.
+// Only the blocks on and below the diagonal of T are written (the diagonal
+// blocks in full, zeros above their diagonal); the solve reads no other.
 __device__ void tri_inverse64(const float* A, float* T, float* X) {
     const int tid = threadIdx.x;
-    for (int e = tid; e < C * C; e += blockDim.x) T[(e >> 6) * LDT + (e & 63)] = 0.f;
-    __syncthreads();
     if (tid < C) {
         const int blk = tid >> 4, c = tid & 15, o = 16 * blk;
         float col[16];
@@ -156,7 +165,7 @@ __host__ __device__ inline F1Smem f1_plan(int Dk, int Dv) {
     s.Twl = s.A + C * C * 2;
     s.Tu = s.A + 2 * C * C * 2;
     s.Tul = s.A + 3 * C * C * 2;
-    s.vec = take(8 * C * 4 + C * 8);
+    s.vec = take(14 * C * 4 + C * 8);
     s.total = o;
     return s;
 }
@@ -180,6 +189,13 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs 
     // negligible) hi_i - hi_j is exact, so differences keep fp64 accuracy
     float* Ghi = rkv + C;
     float* Glo = Ghi + C;
+    // Off the diagonal 16 x 16 blocks, M_ij = exp(Gamma_i - Gamma_j) is the
+    // product of two factors through the last step b = 16 J + 15 of the column
+    // block J of j: uf[J][i] = exp(Gamma_i - Gamma_b) (i > b) and wf[J][j] =
+    // exp(Gamma_b - Gamma_j) (j <= b).  Gamma does not increase, so both lie in
+    // (0, 1]: neither overflows, and one underflows only where M_ij does.
+    float* uf = Glo + C;      // [3][64]
+    float* wf = uf + 3 * C;   // [3][64]
     float* A = reinterpret_cast<float*>(sm + L.A);
     float* Tm = reinterpret_cast<float*>(sm + L.T);
     float* X = reinterpret_cast<float*>(sm + L.X);
@@ -236,30 +252,66 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs 
         tc::mma_tile(tb + 64, tQ, tK, C, C, Dk, false);
         tc::mma_commit(&bar);
     }
+    if (tid < 3 * C) {  // decay factors, while the Grams run
+        const int J = tid / C, i = tid % C, b = 16 * J + 15;
+        const float dg = (Ghi[i] - Ghi[b]) + (Glo[i] - Glo[b]);
+        uf[tid] = i > b ? expf(dg) : 0.f;
+        wf[tid] = i <= b ? expf(-dg) : 0.f;
+    }
+    __syncthreads();
     ok = tc::mbar_wait(&bar, phase, &g_err_fwdtc) && ok;
     phase ^= 1u;
     tc::tc_fence_after();
     uint8_t* Pimg = static_cast<uint8_t*>(p.P) + (bh * d.NC + c) * C * C * 2;
     if (ok) {
-        acc_rows(tb, 0, C, [&](int r, int c0, const float (&x)[16]) {
+        // A and P in one pass over both Grams, all 32 lanes: row r, 8 columns from
+        // c0.  The 16-column block J of a piece and the row block of a warp are
+        // warp-uniform, so is the choice between the factored and the direct decay.
+        const int l = tid & 31, sp = warp & 3, g = warp >> 2, hl = l >> 4;
+        const int r = 16 * sp + (l & 15);
+        const float ra = bt[r] * rkv[r], rp = rqv[r], ghr = Ghi[r], glr = Glo[r];
+        for (int cp = 32 * g; cp < 32 * g + 32; cp += 16) {
+            float va[16], vp[16];
+            tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, cp), va);
+            tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, 64 + cp), vp);
+            tc::tmem_wait_ld();
+            float xa[8], xp[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int jj = c0 + i;
-                const float m = jj < r ? expf((Ghi[r] - Ghi[jj]) + (Glo[r] - Glo[jj])) : 0.f;
-                A[r * LDT + jj] = bt[r] * m * rkv[r] * rkv[jj] * x[i];
+            for (int i = 0; i < 8; ++i) {
+                const float ua = __shfl_sync(0xffffffffu, va[8 + i], l & 15);
+                const float up = __shfl_sync(0xffffffffu, vp[8 + i], l & 15);
+                xa[i] = hl ? ua : va[i];
+                xp[i] = hl ? up : vp[i];
             }
-        });
-        acc_rows(tb, 64, C, [&](int r, int c0, const float (&x)[16]) {
-            float pv[16];
+            const int c0 = cp + 8 * hl, J = cp >> 4;
+            float m[8];
+            if (J < sp) {
+                const float u = uf[J * C + r];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int jj = c0 + i;
-                const float m = jj <= r ? expf((Ghi[r] - Ghi[jj]) + (Glo[r] - Glo[jj])) : 0.f;
-                pv[i] = m * rqv[r] * rkv[jj] * x[i];
+                for (int i = 0; i < 8; ++i) m[i] = u * wf[J * C + c0 + i];
+            } else if (J == sp) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int jj = c0 + i;
+                    m[i] = jj <= r ? expf((ghr - Ghi[jj]) + (glr - Glo[jj])) : 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) m[i] = 0.f;
             }
-            st_bf16x8(Pimg + tc::panel_off(c0, r, C), pv);
-            st_bf16x8(Pimg + tc::panel_off(c0 + 8, r, C), pv + 8);
-        });
+            float a8[8], p8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int jj = c0 + i;
+                const float mk = m[i] * rkv[jj];
+                a8[i] = jj < r ? ra * mk * xa[i] : 0.f;
+                p8[i] = rp * mk * xp[i];
+            }
+            float4* arow = reinterpret_cast<float4*>(A + r * LDT + c0);
+            arow[0] = make_float4(a8[0], a8[1], a8[2], a8[3]);
+            arow[1] = make_float4(a8[4], a8[5], a8[6], a8[7]);
+            st_bf16x8(Pimg + tc::panel_off(c0, r, C), p8);
+        }
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -269,8 +321,13 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs 
     tri_inverse64(A, Tm, X);
     // T as a bf16 panel image: 16-byte chunk e holds row e % 64, columns 8 (e / 64) ..
     uint8_t* Timg = reinterpret_cast<uint8_t*>(p.Tinv) + (bh * d.NC + c) * C * C * 2;
-    for (int e = tid; e < C * (C / 8); e += blockDim.x)
-        st_bf16x8(Timg + 16 * e, Tm + (e % C) * LDT + (e / C) * 8);
+    for (int e = tid; e < C * (C / 8); e += blockDim.x) {
+        const int i = e % C, j0 = (e / C) * 8;
+        float t8[8];
+#pragma unroll
+        for (int s = 0; s < 8; ++s) t8[s] = (j0 >> 4) > (i >> 4) ? 0.f : Tm[i * LDT + j0 + s];
+        st_bf16x8(Timg + 16 * e, t8);
+    }
     // A operands T diag(beta gam r_k) and T diag(beta), each as hi + lo bf16 (x = j, y = i)
     for (int e = tid; e < C * (C / 8); e += blockDim.x) {
         int i, jg;
@@ -280,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs 
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
             const int jj = j0 + s;
-            const float t = Tm[i * LDT + jj];
+            const float t = (jj >> 4) > (i >> 4) ? 0.f : Tm[i * LDT + jj];
             w8[s] = t * bt[jj] * gm[jj] * rkv[jj];
             u8[s] = t * bt[jj];
             wl[s] = w8[s] - __bfloat162float(__float2bfloat16_rn(w8[s]));
@@ -316,9 +373,8 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs 
     tc::tc_fence_after();
     uint8_t* Wimg = static_cast<uint8_t*>(p.W) + gbase * Dk * 2;
     if (ok) {
-        acc_rows(tb, 0, Dk, [&](int r, int c0, const float (&x)[16]) {
+        acc_rows_all(tb, 0, Dk, [&](int r, int c0, const float (&x)[8]) {
             st_bf16x8(Wimg + tc::panel_off(c0, r, C), x);
-            st_bf16x8(Wimg + tc::panel_off(c0 + 8, r, C), x + 8);
         });
     }
     uint32_t ucol = (uint32_t)Dk;
@@ -338,10 +394,10 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs 
     }
     if (ok) {
         float* U = p.U + gbase * Dv;
-        acc_rows(tb, ucol, Dv, [&](int r, int c0, const float (&x)[16]) {
+        acc_rows_all(tb, ucol, Dv, [&](int r, int c0, const float (&x)[8]) {
             float4* dst = reinterpret_cast<float4*>(U + (int64_t)r * Dv + c0);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+            dst[0] = make_float4(x[0], x[1], x[2], x[3]);
+            dst[1] = make_float4(x[4], x[5], x[6], x[7]);
         });
     }
     tc::tc_fence_before();
