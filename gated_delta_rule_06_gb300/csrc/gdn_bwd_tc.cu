@@ -283,6 +283,12 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     float* csp = rsc + 4 * C;   // [4][64] column sums (compensated, folded)
     float* gbh = csp + 4 * C;   // [64] Gammabar as hi + lo
     float* gbl = gbh + C;       // [64]
+    // Off the diagonal 16 x 16 blocks, M_ij = exp(Gamma_i - Gamma_j) is the
+    // product of two factors through the last step b = 16 J + 15 of the column
+    // block J of j: uf[J][i] = exp(Gamma_i - Gamma_b) (i > b) and wf[J][j] =
+    // exp(Gamma_b - Gamma_j) (j <= b), both in (0, 1] since Gamma does not increase
+    float* uf = gbl + C;        // [3][64]
+    float* wf = uf + 3 * C;     // [3][64]
 
     const int64_t t0 = (int64_t)c * C;
     const int nvalid = (int)(d.T - t0 < C ? d.T - t0 : C);
@@ -360,6 +366,12 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     for (int i = tid; i < 12 * C; i += blockDim.x) gq[i] = 0.f;  // gq, ee, bb0, zk, sbp
     for (int i = tid; i < 8 * C; i += blockDim.x) rsp[i] = 0.f;  // rsp, rsc
     cta_sync_tc();
+    if (tid < 3 * C) {  // decay factors (read first by the element-wise phase)
+        const int J = tid / C, i = tid % C, b = 16 * J + 15;
+        const float dg = (Ghi[i] - Ghi[b]) + (Glo[i] - Glo[b]);
+        uf[tid] = i > b ? expf(dg) : 0.f;
+        wf[tid] = i <= b ? expf(-dg) : 0.f;
+    }
     const uint32_t tb = tmem_base_sh;
     uint32_t phase = 0;
     bool ok = tc::mbar_wait(&barOV, 0, &g_err_bwdtc);
@@ -612,13 +624,30 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             const int pi = 2 * g + hl;
             float sb = 0.f;
             float rs = rsp[pi * C + r], rc = rsc[pi * C + r];  // Kahan-compensated row sum
-            float pk[8], pq[8];
-            const float ghr = Ghi[r], glr = Glo[r];
+            float pk[8], pq[8], mv[8];
+            // the column block of the piece and the row block of the warp are
+            // warp-uniform, so is the choice between factored and direct decay
+            const int J = c0 >> 4, I = r >> 4;
+            if (J < I) {
+                const float u = uf[J * C + r];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mv[i] = u * wf[J * C + c0 + i];
+            } else if (J == I) {
+                const float ghr = Ghi[r], glr = Glo[r];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int jj = c0 + i;
+                    mv[i] = jj <= r ? expf((ghr - Ghi[jj]) + (glr - Glo[jj])) : 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mv[i] = 0.f;
+            }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int jj = c0 + i;
                 const int idx = r * LDM + jj;
-                const float m = jj <= r ? expf((ghr - Ghi[jj]) + (glr - Glo[jj])) : 0.f;
+                const float m = mv[i];
                 const float ab = jj < r ? -x[i] : 0.f;
                 const float gk = Gkk[idx];
                 const float mb = ab * bt[r] * gk + Pf[idx] * Gqk[idx];
