@@ -7,7 +7,7 @@
 // (chunk, value head, batch); every product has 64 rows as its M dimension
 // (M = 64 MMAs, accumulator row r in TMEM lane 32 (r / 16) + r % 16):
 //   phase 0:  Pbar = Obar Delta^T,  Dbar V^T,  Y = T^T Dbar
-//   phase 1:  per 32-wide block of Dk:  Obar S^T,  Wbar = -Dbar S^T,  Delta Sbar'^T
+//   phase 1:  per 64-wide block of Dk:  Delta Sbar'^T,  Obar S^T,  Wbar = -Dbar S^T
 //   phase 1b: Wbar K^T,  diag(beta gam) T^T Wbar,  K K^T
 //   phase 2:  X = Tbar T^T,  Q K^T,  Abar = -T^T X,  then the gate / log-decay
 //             cotangents element-wise in fp32 (fp64 for the cancelling sums)
@@ -21,7 +21,7 @@
 // normalised rows are never rounded.  The saved intermediates (Delta hi / lo,
 // -Dbar, T, the state checkpoints S and the chunk-end cotangents Sbar') are
 // bf16 operand images written by the earlier kernels; each arrives with one
-// bulk copy, and the 32-wide Dk blocks of S / Sbar' are double-buffered so the
+// bulk copy, and the 64-wide Dk blocks of S / Sbar' stream through one buffer so the
 // next block streams in while the current block's epilogue runs.
 #include "gdn_internal.cuh"
 #include "gdn_tc.cuh"
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     extern __shared__ __align__(1024) uint8_t sm[];
     // bar: MMA rounds outside phase 1; barM / barE: phase-1 products of block b
     // done / block b's epilogue done (two of each, by block parity); barMa: block
-    // b's products with S done; barG: block b's tiles read by the <S, Sbar'> sums;
+    // b's products with Sbar' done; barG: block b's tiles read by the <S, Sbar'> sums;
     // barOV, barL, barKQ, barSa / barSb (S / Sbar' halves of a block): arrivals
     __shared__ uint64_t bar, barOV, barL, barKQ, barSa, barSb, barMa, barG, barM[2], barE[2];
     __shared__ uint32_t tmem_base_sh;
@@ -351,6 +351,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::mbar_arrive_expect_tx(&barKQ, 2 * tk);
         tc::bulk_g2s(sm + L.K, static_cast<const uint8_t*>(p.kimg) + kqi * tk, tk, &barKQ);
         tc::bulk_g2s(sm + L.Q, static_cast<const uint8_t*>(p.qimg) + kqi * tk, tk, &barKQ);
+        load_sp(0);  // its half of the block buffer is not used by phase 0
     }
     if (tid < C) {
         const double G = p.gam[gbase + tid];
@@ -440,42 +441,44 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     cta_sync_tc();  // phase-0 reads of TMEM and of the V tile are done
 
     // ---- phase 1: state products per kBlkK-wide block of Dk through one buffer
-    // of two halves, S and Sbar'.  The producer issues block b's products with S
-    // (Obar S^T, -Dbar S^T) as soon as its S half has landed (and the epilogue of
-    // block b - 2 has released its Wbar scratch: S1 for even, S2 for odd blocks),
-    // then those with Sbar' (Delta Sbar'^T); each half of block b + 1 loads as
-    // soon as the products (and the <S, Sbar'> sums) that read it are done, so
-    // the loads overlap the other half's products and the epilogues.  Obar S^T and
-    // Delta Sbar'^T land in the dq / dk accumulators, rescaled there by gam and e.
+    // of two halves, S and Sbar'.  The producer issues block b's products with
+    // Sbar' (Delta Sbar'^T) as soon as its half has landed, then those with S
+    // (Obar S^T, -Dbar S^T) once the S half has landed and the epilogue of block
+    // b - 2 has released its Wbar scratch (S1 for even, S2 for odd blocks); each
+    // half of block b + 1 loads as soon as the products (and the <S, Sbar'> sums)
+    // that read it are done, so the loads overlap the other half's products and
+    // the epilogues.  The first Sbar' half arrives with the phase-0 operands.
+    // Obar S^T and Delta Sbar'^T land in the dq / dk accumulators, rescaled there
+    // by gam and e.
     float gcb = 0.f;
     if (prod) {
         load_s(0);
-        load_sp(0);
         for (int b = 0; b < nblk; ++b) {
             const int dk0 = b * kBlkK, nk = nkb(b);
             const uint32_t par = (uint32_t)b & 1u;
-            ok = tc::mbar_wait(&barSa, par, &g_err_bwdtc) && ok;
-            if (b >= 2) ok = tc::mbar_wait(&barE[b & 1], (uint32_t)((b - 2) >> 1) & 1u, &g_err_bwdtc) && ok;
             const tc::Tile tS = tc::panel_tile(sm + L.V, Dv, false);
             const tc::Tile tSp = tc::panel_tile(sm + L.V + blk, Dv, false);
             const uint32_t wcol = (b & 1) ? kS2 : kS1;
-            tc::mma_tile(tb + kAQ + dk0, tO, tS, C, nk, Dv, false);
-            tc::mma_tile(tb + wcol, tNBmn, tS, C, nk, Dv, false);
-            tc::mma_commit(&barMa);
             ok = tc::mbar_wait(&barSb, par, &g_err_bwdtc) && ok;
             tc::mma_tile(tb + kAK + dk0, tDmn, tSp, C, nk, Dv, false);
             tc::mma_tile(tb + kAK + dk0, tDlomn, tSp, C, nk, Dv, true);
+            tc::mma_commit(&barMa);
+            ok = tc::mbar_wait(&barSa, par, &g_err_bwdtc) && ok;
+            if (b >= 2) ok = tc::mbar_wait(&barE[b & 1], (uint32_t)((b - 2) >> 1) & 1u, &g_err_bwdtc) && ok;
+            tc::mma_tile(tb + kAQ + dk0, tO, tS, C, nk, Dv, false);
+            tc::mma_tile(tb + wcol, tNBmn, tS, C, nk, Dv, false);
             tc::mma_commit(&barM[b & 1]);
             if (b + 1 < nblk) {
                 ok = tc::mbar_wait(&barMa, par, &g_err_bwdtc) && ok;
                 ok = tc::mbar_wait(&barG, par, &g_err_bwdtc) && ok;
-                load_s(b + 1);
-                ok = tc::mbar_wait(&barM[b & 1], (uint32_t)(b >> 1) & 1u, &g_err_bwdtc) && ok;
                 load_sp(b + 1);
+                ok = tc::mbar_wait(&barM[b & 1], (uint32_t)(b >> 1) & 1u, &g_err_bwdtc) && ok;
+                load_s(b + 1);
             }
         }
     } else if (epi) {
         ok = tc::mbar_wait(&barKQ, 0, &g_err_bwdtc) && ok;
+        const int sp = warp & 3;
         for (int b = 0; b < nblk; ++b) {
             const int dk0 = b * kBlkK, nk = nkb(b);
             ok = tc::mbar_wait(&barSa, (uint32_t)b & 1u, &g_err_bwdtc) && ok;
@@ -493,31 +496,52 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             ok = tc::mbar_wait(&barM[b & 1], (uint32_t)(b >> 1) & 1u, &g_err_bwdtc) && ok;
             tc::tc_fence_after();
             if (ok) {
-                acc_rows_rw(tb, kAQ + dk0, nk, [&](int r, int c0, float (&x)[16]) {
-                    float qq[16];
-                    panel_row16(sm + L.Q, dk0 + c0, r, qq);
-                    float s = 0.f;
+                // the block's three accumulators in one batch of TMEM loads: warp
+                // columns g nk / 2 .. + nk / 2 (one or two 16-column pieces)
+                const int half = nk / 2, np = half / 16;
+                const uint32_t wcol = (b & 1) ? kS2 : kS1;
+                float aq[2][16], wv[2][16], ak[2][16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        x[i] *= gm[r];
-                        s = fmaf(x[i], qq[i], s);
+                for (int u = 0; u < 2; ++u)
+                    if (u < np) {
+                        const int cc = g * half + 16 * u;
+                        tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, kAQ + dk0 + cc), aq[u]);
+                        tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, wcol + cc), wv[u]);
+                        tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, kAK + dk0 + cc), ak[u]);
                     }
-                    gq[g * C + r] += s;
-                });
-                acc_rows(tb, (b & 1) ? kS2 : kS1, nk, [&](int r, int c0, const float (&x)[16]) {
-                    tile_put16(sm + L.W, Dk, dk0 + c0, r, x);
-                });
-                acc_rows_rw(tb, kAK + dk0, nk, [&](int r, int c0, float (&x)[16]) {
-                    float kk[16];
-                    panel_row16(sm + L.K, dk0 + c0, r, kk);
-                    float s = 0.f;
+                tc::tmem_wait_ld();
+                if (lane < 16) {
+                    const int r = 16 * sp + lane;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        x[i] *= ev[r];
-                        s = fmaf(x[i], kk[i], s);
+                    for (int u = 0; u < 2; ++u)
+                        if (u < np) {
+                            const int cc = g * half + 16 * u;
+                            float qq[16], kk[16];
+                            panel_row16(sm + L.Q, dk0 + cc, r, qq);
+                            panel_row16(sm + L.K, dk0 + cc, r, kk);
+                            float sq = 0.f, sk = 0.f;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                aq[u][i] *= gm[r];
+                                sq = fmaf(aq[u][i], qq[i], sq);
+                                ak[u][i] *= ev[r];
+                                sk = fmaf(ak[u][i], kk[i], sk);
+                            }
+                            gq[g * C + r] += sq;
+                            ee[g * C + r] += sk;
+                            tile_put16(sm + L.W, Dk, dk0 + cc, r, wv[u]);
+                        }
+                }
+                // rescaled values back in place (lanes 16..31 write TMEM lanes that
+                // an M = 64 accumulator does not use)
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+                    if (u < np) {
+                        const int cc = g * half + 16 * u;
+                        tc::tmem_st16(tc::tmem_addr(tb, 32 * sp, kAQ + dk0 + cc), aq[u]);
+                        tc::tmem_st16(tc::tmem_addr(tb, 32 * sp, kAK + dk0 + cc), ak[u]);
                     }
-                    ee[g * C + r] += s;
-                });
+                tc::tmem_wait_st();
             }
             tc::tc_fence_before();
             tc::mbar_arrive(&barE[b & 1]);
