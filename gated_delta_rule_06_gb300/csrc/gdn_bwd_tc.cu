@@ -3,8 +3,10 @@
 //
 // Same equations as the CUDA-core version in gdn_bwd.cu (reverse-mode
 // derivative of the chunked WY/UT form; mlx-lm PR "Add gated_delta_update
-// VJP", "What this PR adds" and "Scope and follow-ups").  One CTA per
-// (chunk, value head, batch); every product has 64 rows as its M dimension
+// VJP", "What this PR adds" and "Scope and follow-ups").  One persistent CTA
+// per SM walks the work items (chunk, value head, batch), loading the next
+// item's operands while it stores the current one's results; every product
+// has 64 rows as its M dimension
 // (M = 64 MMAs, accumulator row r in TMEM lane 32 (r / 16) + r % 16):
 //   phase 0:  Pbar = Obar Delta^T,  Dbar V^T,  Y = T^T Dbar
 //   phase 1:  per 64-wide block of Dk:  Delta Sbar'^T,  Obar S^T,  Wbar = -Dbar S^T
@@ -210,30 +212,34 @@ __device__ __forceinline__ f2 f2_add(f2 x, f2 y) {
     return {h, lo - (h - s.hi)};
 }
 
-// As acc_rows with up to four 16-column loads in flight per wait
+// As acc_rows with two 16-column loads in flight per wait
 template <typename F>
-__device__ __forceinline__ void acc_rows4(uint32_t tbase, uint32_t col0, int ncols, F&& f) {
+__device__ __forceinline__ void acc_rows2(uint32_t tbase, uint32_t col0, int ncols, F&& f) {
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
     const int sp = w & 3, g = w >> 2;
     const int half = ncols / 2, end = (g + 1) * half;
-    for (int cb = g * half; cb < end; cb += 64) {
-        float v[4][16];
+    for (int cb = g * half; cb < end; cb += 32) {
+        float v[2][16];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < 2; ++u)
             if (cb + 16 * u < end) tc::tmem_ld16(tc::tmem_addr(tbase, 32 * sp, col0 + cb + 16 * u), v[u]);
         tc::tmem_wait_ld();
         if (l < 16) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < 2; ++u)
                 if (cb + 16 * u < end) f(16 * sp + l, cb + 16 * u, v[u]);
         }
     }
 }
 
-__device__ __forceinline__ void sync_after_mma(uint64_t* bar, uint32_t& phase, bool& ok) {
-    ok = tc::mbar_wait(bar, phase, &g_err_bwdtc) && ok;
+// Completion of an MMA round on `bar`: waiting threads wait for it; every thread
+// advances its copy of the barrier's phase
+__device__ __forceinline__ void sync_after_mma(uint64_t* bar, uint32_t& phase, bool& ok, bool wait) {
+    if (wait) {
+        ok = tc::mbar_wait(bar, phase, &g_err_bwdtc) && ok;
+        tc::tc_fence_after();
+    }
     phase ^= 1u;
-    tc::tc_fence_after();
 }
 __device__ __forceinline__ void cta_sync_tc() {
     tc::tc_fence_before();
@@ -250,8 +256,6 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     // barOV, barL, barKQ, barSa / barSb (S / Sbar' halves of a block): arrivals
     __shared__ uint64_t bar, barOV, barL, barKQ, barSa, barSb, barMa, barG, barM[2], barE[2];
     __shared__ uint32_t tmem_base_sh;
-    const int c = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
-    const int j = h / (int)d.G;
     const int Dk = (int)d.Dk, Dv = (int)d.Dv;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // warps 0-7: epilogues (row quarter warp % 4, column half g); warp 8: loads and MMA issue
@@ -290,35 +294,61 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     float* uf = gbl + C;        // [3][64]
     float* wf = uf + 3 * C;     // [3][64]
 
-    const int64_t t0 = (int64_t)c * C;
-    const int nvalid = (int)(d.T - t0 < C ? d.T - t0 : C);
-    const int64_t gbase = ((int64_t)bb * d.Hv + h) * d.Tp + t0;
-    const int64_t rbase = ((int64_t)bb * d.Hk + j) * d.Tp + t0;
-    const int64_t ci = ((int64_t)bb * d.Hv + h) * d.NC + c;  // chunk image index
+    // Persistent: CTA k takes the work items (chunk, value head, batch) k, k + grid,
+    // ... (chunk fastest); the next item's operands load while the current one ends.
+    const int nitems = (int)(d.NC * d.Hv * d.B);
     __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(p.dv);
     const int64_t ldv = d.Hv * Dv;
     const uint32_t tv = (uint32_t)(C * Dv * 2);         // one 64 x Dv bf16 tile
     const uint32_t tk = (uint32_t)(C * Dk * 2);         // one 64 x Dk bf16 tile
     const uint32_t blk = (uint32_t)(kBlkK * Dv * 2);    // one full Dk block of S (or Sbar')
-    const uint8_t* ck_img = reinterpret_cast<const uint8_t*>(p.ckpt) + ci * (int64_t)Dk * Dv * 2;
-    const uint8_t* ds_img = reinterpret_cast<const uint8_t*>(p.dSck) + ci * (int64_t)Dk * Dv * 2;
-    // Dk block b of S / Sbar' (panels 8b .. 8b + nk(b) / 8 - 1 of the images, one
-    // buffer in the space of the V tile, free once phase 0 is done)
+    // Dk block b of S / Sbar' (panels 8b .. 8b + nk(b) / 8 - 1 of the images of
+    // chunk image ci, one buffer in the space of the V tile, free once phase 0 is
+    // done): the S half at L.V, the Sbar' half one full block further
     const int nblk = (Dk + kBlkK - 1) / kBlkK;
     auto nkb = [&](int b) { return Dk - b * kBlkK < kBlkK ? Dk - b * kBlkK : kBlkK; };
-    // the S half of the buffer at L.V, the Sbar' half one full block further
-    auto load_s = [&](int b) {
+    auto load_s = [&](int64_t ci, int b) {
         const uint32_t bytes = (uint32_t)(nkb(b) * Dv * 2);
         tc::mbar_arrive_expect_tx(&barSa, bytes);
-        tc::bulk_g2s(sm + L.V, ck_img + (int64_t)b * blk, bytes, &barSa);
+        tc::bulk_g2s(sm + L.V, reinterpret_cast<const uint8_t*>(p.ckpt) + ci * (int64_t)Dk * Dv * 2 + (int64_t)b * blk,
+                     bytes, &barSa);
     };
-    auto load_sp = [&](int b) {
+    auto load_sp = [&](int64_t ci, int b) {
         const uint32_t bytes = (uint32_t)(nkb(b) * Dv * 2);
         tc::mbar_arrive_expect_tx(&barSb, bytes);
-        tc::bulk_g2s(sm + L.V + blk, ds_img + (int64_t)b * blk, bytes, &barSb);
+        tc::bulk_g2s(sm + L.V + blk, reinterpret_cast<const uint8_t*>(p.dSck) + ci * (int64_t)Dk * Dv * 2 + (int64_t)b * blk,
+                     bytes, &barSb);
     };
-    // ---- operands, all issued by the producer: raw dO, v (phase 0) by TMA in the
-    // panel layout; the k, q images, Delta (hi + lo), -Dbar and T by bulk copies
+    // ---- operands of item it, all issued by the producer, in two groups.  Phase 0:
+    // raw dO, v by TMA in the panel layout, Delta (hi + lo), -Dbar and T by bulk
+    // copies.  Phase 1 (issued once the phase-0 products are, so that the first
+    // group, which every SM wants at about the same time, is smaller): the k, q
+    // images and the first Sbar' block (its half of the block buffer is not used
+    // by phase 0).
+    auto issue_loads = [&](int it) {
+        const int c = it % (int)d.NC, h = (it / (int)d.NC) % (int)d.Hv, bb = it / (int)(d.NC * d.Hv);
+        const int64_t ci = ((int64_t)bb * d.Hv + h) * d.NC + c;
+        tc::mbar_arrive_expect_tx(&barOV, 2 * tv);
+        tc::tma_load_5d(sm + L.O, &tm.dOf, 0, c * C, 0, h, bb, &barOV);
+        tc::tma_load_5d(sm + L.V, &tm.v, 0, c * C, 0, h, bb, &barOV);
+        const uint8_t* dl_img = reinterpret_cast<const uint8_t*>(p.Delta) + ci * (int64_t)C * Dv * 4;
+        tc::mbar_arrive_expect_tx(&barL, 3 * tv + C * C * 2);
+        tc::bulk_g2s(sm + L.D, dl_img, tv, &barL);
+        tc::bulk_g2s(sm + L.Dlo, dl_img + tv, tv, &barL);
+        tc::bulk_g2s(sm + L.NB, reinterpret_cast<const uint8_t*>(p.Dbar) + ci * (int64_t)tv, tv, &barL);
+        tc::bulk_g2s(sm + L.Tt, reinterpret_cast<const uint8_t*>(p.Tinv) + ci * (int64_t)C * C * 2,
+                     C * C * 2, &barL);
+    };
+    auto issue_loads_kq = [&](int it) {
+        const int c = it % (int)d.NC, h = (it / (int)d.NC) % (int)d.Hv, bb = it / (int)(d.NC * d.Hv);
+        const int j = h / (int)d.G;
+        const int64_t ci = ((int64_t)bb * d.Hv + h) * d.NC + c;
+        const int64_t kqi = ((int64_t)bb * d.Hk + j) * d.NC + c;  // q / k images of this chunk
+        tc::mbar_arrive_expect_tx(&barKQ, 2 * tk);
+        tc::bulk_g2s(sm + L.K, static_cast<const uint8_t*>(p.kimg) + kqi * tk, tk, &barKQ);
+        tc::bulk_g2s(sm + L.Q, static_cast<const uint8_t*>(p.qimg) + kqi * tk, tk, &barKQ);
+        load_sp(ci, 0);
+    };
     if (warp == 0) {
         tc::tmem_alloc(&tmem_base_sh, 512);
         tc::tmem_relinquish();
@@ -337,22 +367,26 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             tc::mbar_init(&barE[i], kThreads);
         }
         tc::fence_mbar_init();
-        tc::mbar_arrive_expect_tx(&barOV, 2 * tv);
-        tc::tma_load_5d(sm + L.O, &tm.dOf, 0, (int)t0, 0, h, bb, &barOV);
-        tc::tma_load_5d(sm + L.V, &tm.v, 0, (int)t0, 0, h, bb, &barOV);
-        const uint8_t* dl_img = reinterpret_cast<const uint8_t*>(p.Delta) + ci * (int64_t)C * Dv * 4;
-        tc::mbar_arrive_expect_tx(&barL, 3 * tv + C * C * 2);
-        tc::bulk_g2s(sm + L.D, dl_img, tv, &barL);
-        tc::bulk_g2s(sm + L.Dlo, dl_img + tv, tv, &barL);
-        tc::bulk_g2s(sm + L.NB, reinterpret_cast<const uint8_t*>(p.Dbar) + ci * (int64_t)tv, tv, &barL);
-        tc::bulk_g2s(sm + L.Tt, reinterpret_cast<const uint8_t*>(p.Tinv) + ci * (int64_t)C * C * 2,
-                     C * C * 2, &barL);
-        const int64_t kqi = ((int64_t)bb * d.Hk + j) * d.NC + c;  // q / k images of this chunk
-        tc::mbar_arrive_expect_tx(&barKQ, 2 * tk);
-        tc::bulk_g2s(sm + L.K, static_cast<const uint8_t*>(p.kimg) + kqi * tk, tk, &barKQ);
-        tc::bulk_g2s(sm + L.Q, static_cast<const uint8_t*>(p.qimg) + kqi * tk, tk, &barKQ);
-        load_sp(0);  // its half of the block buffer is not used by phase 0
+        if ((int)blockIdx.x < nitems) issue_loads((int)blockIdx.x);
     }
+    cta_sync_tc();
+    const uint32_t tb = tmem_base_sh;
+    uint32_t phase = 0;        // parity of the next completion of bar (MMA rounds)
+    uint32_t pit = 0;          // parity of the per-item arrivals (barOV, barL, barKQ)
+    uint32_t B0 = 0;           // Dk blocks of the earlier items (parities of the block barriers)
+    bool ok = true;
+    // producer: an item whose operands are in flight but not yet waited for
+    bool pending = false;
+    uint32_t pend_pit = 0;
+    for (int it = (int)blockIdx.x; it < nitems; it += (int)gridDim.x, pit ^= 1u, B0 += (uint32_t)nblk) {
+    pending = false;
+    const int c = it % (int)d.NC, h = (it / (int)d.NC) % (int)d.Hv, bb = it / (int)(d.NC * d.Hv);
+    const int j = h / (int)d.G;
+    const int64_t t0 = (int64_t)c * C;
+    const int nvalid = (int)(d.T - t0 < C ? d.T - t0 : C);
+    const int64_t gbase = ((int64_t)bb * d.Hv + h) * d.Tp + t0;
+    const int64_t rbase = ((int64_t)bb * d.Hk + j) * d.Tp + t0;
+    const int64_t ci = ((int64_t)bb * d.Hv + h) * d.NC + c;  // chunk image index
     if (tid < C) {
         const double G = p.gam[gbase + tid];
         const float ghi = (float)G;
@@ -373,10 +407,8 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         uf[tid] = i > b ? expf(dg) : 0.f;
         wf[tid] = i <= b ? expf(-dg) : 0.f;
     }
-    const uint32_t tb = tmem_base_sh;
-    uint32_t phase = 0;
-    bool ok = tc::mbar_wait(&barOV, 0, &g_err_bwdtc);
-    ok = tc::mbar_wait(&barL, 0, &g_err_bwdtc) && ok;
+    ok = tc::mbar_wait(&barOV, pit, &g_err_bwdtc) && ok;
+    ok = tc::mbar_wait(&barL, pit, &g_err_bwdtc) && ok;
 
     // k, q, dO, v tiles: panel layout (x = column, 64 rows); Wbar tile: canonical
     const tc::Tile tK = tc::panel_tile(sm + L.K, C, true), tQ = tc::panel_tile(sm + L.Q, C, true);
@@ -399,11 +431,12 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::mma_tile(tb + kS2, tNBmn, tV, C, C, Dv, false);
         tc::mma_tile(tb + kAK, tTmn, tNB, C, Dv, C, false);
         tc::mma_commit(&bar);
+        issue_loads_kq(it);
     }
     float* Pf = reinterpret_cast<float*>(sm + L.Pf);
     float* Tbf = reinterpret_cast<float*>(sm + L.Tbf);
+    sync_after_mma(&bar, phase, ok, epi);
     if (epi) {
-        sync_after_mma(&bar, phase, ok);
         if (ok) {
             acc_rows(tb, kS1, C, [&](int r, int c0, const float (&x)[16]) {
                 float m[16];
@@ -452,10 +485,10 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     // by gam and e.
     float gcb = 0.f;
     if (prod) {
-        load_s(0);
+        load_s(ci, 0);
         for (int b = 0; b < nblk; ++b) {
             const int dk0 = b * kBlkK, nk = nkb(b);
-            const uint32_t par = (uint32_t)b & 1u;
+            const uint32_t B = B0 + (uint32_t)b, par = B & 1u;
             const tc::Tile tS = tc::panel_tile(sm + L.V, Dv, false);
             const tc::Tile tSp = tc::panel_tile(sm + L.V + blk, Dv, false);
             const uint32_t wcol = (b & 1) ? kS2 : kS1;
@@ -464,25 +497,26 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             tc::mma_tile(tb + kAK + dk0, tDlomn, tSp, C, nk, Dv, true);
             tc::mma_commit(&barMa);
             ok = tc::mbar_wait(&barSa, par, &g_err_bwdtc) && ok;
-            if (b >= 2) ok = tc::mbar_wait(&barE[b & 1], (uint32_t)((b - 2) >> 1) & 1u, &g_err_bwdtc) && ok;
+            if (b >= 2) ok = tc::mbar_wait(&barE[B & 1], ((B - 2) >> 1) & 1u, &g_err_bwdtc) && ok;
             tc::mma_tile(tb + kAQ + dk0, tO, tS, C, nk, Dv, false);
             tc::mma_tile(tb + wcol, tNBmn, tS, C, nk, Dv, false);
-            tc::mma_commit(&barM[b & 1]);
+            tc::mma_commit(&barM[B & 1]);
             if (b + 1 < nblk) {
                 ok = tc::mbar_wait(&barMa, par, &g_err_bwdtc) && ok;
                 ok = tc::mbar_wait(&barG, par, &g_err_bwdtc) && ok;
-                load_sp(b + 1);
-                ok = tc::mbar_wait(&barM[b & 1], (uint32_t)(b >> 1) & 1u, &g_err_bwdtc) && ok;
-                load_s(b + 1);
+                load_sp(ci, b + 1);
+                ok = tc::mbar_wait(&barM[B & 1], (B >> 1) & 1u, &g_err_bwdtc) && ok;
+                load_s(ci, b + 1);
             }
         }
     } else if (epi) {
-        ok = tc::mbar_wait(&barKQ, 0, &g_err_bwdtc) && ok;
+        ok = tc::mbar_wait(&barKQ, pit, &g_err_bwdtc) && ok;
         const int sp = warp & 3;
         for (int b = 0; b < nblk; ++b) {
             const int dk0 = b * kBlkK, nk = nkb(b);
-            ok = tc::mbar_wait(&barSa, (uint32_t)b & 1u, &g_err_bwdtc) && ok;
-            ok = tc::mbar_wait(&barSb, (uint32_t)b & 1u, &g_err_bwdtc) && ok;
+            const uint32_t B = B0 + (uint32_t)b;
+            ok = tc::mbar_wait(&barSa, B & 1u, &g_err_bwdtc) && ok;
+            ok = tc::mbar_wait(&barSb, B & 1u, &g_err_bwdtc) && ok;
             const uint8_t* sS = sm + L.V;
             const int bytes = nk * Dv * 2;
             for (int e = tid; e < bytes / 16; e += kThreads) {
@@ -493,58 +527,46 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
                 for (int i = 0; i < 8; ++i) gcb = fmaf(a8[i], b8[i], gcb);
             }
             tc::mbar_arrive(&barG);
-            ok = tc::mbar_wait(&barM[b & 1], (uint32_t)(b >> 1) & 1u, &g_err_bwdtc) && ok;
+            ok = tc::mbar_wait(&barM[B & 1], (B >> 1) & 1u, &g_err_bwdtc) && ok;
             tc::tc_fence_after();
             if (ok) {
-                // the block's three accumulators in one batch of TMEM loads: warp
-                // columns g nk / 2 .. + nk / 2 (one or two 16-column pieces)
+                // warp columns g nk / 2 .. + nk / 2 in one or two 16-column pieces; the
+                // three accumulators of a piece in one batch of TMEM loads
                 const int half = nk / 2, np = half / 16;
                 const uint32_t wcol = (b & 1) ? kS2 : kS1;
-                float aq[2][16], wv[2][16], ak[2][16];
+                for (int u = 0; u < np; ++u) {
+                    const int cc = g * half + 16 * u;
+                    float aq[16], wv[16], ak[16];
+                    tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, kAQ + dk0 + cc), aq);
+                    tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, wcol + cc), wv);
+                    tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, kAK + dk0 + cc), ak);
+                    tc::tmem_wait_ld();
+                    if (lane < 16) {
+                        const int r = 16 * sp + lane;
+                        float qq[16], kk[16];
+                        panel_row16(sm + L.Q, dk0 + cc, r, qq);
+                        panel_row16(sm + L.K, dk0 + cc, r, kk);
+                        float sq = 0.f, sk = 0.f;
 #pragma unroll
-                for (int u = 0; u < 2; ++u)
-                    if (u < np) {
-                        const int cc = g * half + 16 * u;
-                        tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, kAQ + dk0 + cc), aq[u]);
-                        tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, wcol + cc), wv[u]);
-                        tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, kAK + dk0 + cc), ak[u]);
-                    }
-                tc::tmem_wait_ld();
-                if (lane < 16) {
-                    const int r = 16 * sp + lane;
-#pragma unroll
-                    for (int u = 0; u < 2; ++u)
-                        if (u < np) {
-                            const int cc = g * half + 16 * u;
-                            float qq[16], kk[16];
-                            panel_row16(sm + L.Q, dk0 + cc, r, qq);
-                            panel_row16(sm + L.K, dk0 + cc, r, kk);
-                            float sq = 0.f, sk = 0.f;
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                aq[u][i] *= gm[r];
-                                sq = fmaf(aq[u][i], qq[i], sq);
-                                ak[u][i] *= ev[r];
-                                sk = fmaf(ak[u][i], kk[i], sk);
-                            }
-                            gq[g * C + r] += sq;
-                            ee[g * C + r] += sk;
-                            tile_put16(sm + L.W, Dk, dk0 + cc, r, wv[u]);
+                        for (int i = 0; i < 16; ++i) {
+                            aq[i] *= gm[r];
+                            sq = fmaf(aq[i], qq[i], sq);
+                            ak[i] *= ev[r];
+                            sk = fmaf(ak[i], kk[i], sk);
                         }
-                }
-                // rescaled values back in place (lanes 16..31 write TMEM lanes that
-                // an M = 64 accumulator does not use)
-#pragma unroll
-                for (int u = 0; u < 2; ++u)
-                    if (u < np) {
-                        const int cc = g * half + 16 * u;
-                        tc::tmem_st16(tc::tmem_addr(tb, 32 * sp, kAQ + dk0 + cc), aq[u]);
-                        tc::tmem_st16(tc::tmem_addr(tb, 32 * sp, kAK + dk0 + cc), ak[u]);
+                        gq[g * C + r] += sq;
+                        ee[g * C + r] += sk;
+                        tile_put16(sm + L.W, Dk, dk0 + cc, r, wv);
                     }
+                    // rescaled values back in place (lanes 16..31 write TMEM lanes
+                    // that an M = 64 accumulator does not use)
+                    tc::tmem_st16(tc::tmem_addr(tb, 32 * sp, kAQ + dk0 + cc), aq);
+                    tc::tmem_st16(tc::tmem_addr(tb, 32 * sp, kAK + dk0 + cc), ak);
+                }
                 tc::tmem_wait_st();
             }
             tc::tc_fence_before();
-            tc::mbar_arrive(&barE[b & 1]);
+            tc::mbar_arrive(&barE[B & 1]);
         }
         // <S, Sbar'> of this CTA: warp sums by a fixed shuffle tree, then in warp order
 #pragma unroll
@@ -566,7 +588,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
 
     // ---- phase 1b: Wbar K^T | dk += diag(beta gam) T^T Wbar | K K^T
     if (prod) {
-        ok = tc::mbar_wait(&barKQ, 0, &g_err_bwdtc) && ok;
+        ok = tc::mbar_wait(&barKQ, pit, &g_err_bwdtc) && ok;
         tc::mma_tile(tb + kS1, tW, tK, C, C, Dk, false);
         tc::mma_tile(tb + kAK, tc::panel_tile(sm + L.Tsc, C, false), tWmn, C, Dk, C, true);
         tc::mma_tile(tb + kS2, tK, tK, C, C, Dk, false);
@@ -578,7 +600,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     float* Gkk = reinterpret_cast<float*>(sm + L.Gkk);
     float* Gqk = reinterpret_cast<float*>(sm + L.Gqk);
     float* ZP = Gqk;  // T o (Wbar K^T), until Gqk is formed in phase 2
-    if (epi) sync_after_mma(&bar, phase, ok);
+    sync_after_mma(&bar, phase, ok, epi);
     if (epi && ok) {
         acc_rows(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
 #pragma unroll
@@ -623,7 +645,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::mma_tile(tb + kS2, tQ, tK, C, C, Dk, false);
         tc::mma_commit(&bar);
     }
-    if (epi) sync_after_mma(&bar, phase, ok);
+    sync_after_mma(&bar, phase, ok, epi);
     if (epi && ok) {
         acc_rows(tb, kS1, C, [&](int r, int c0, const float (&x)[16]) {
             tile_put16(sm + L.Xh, C, c0, r, x);  // X row-major (x = l, y = j)
@@ -639,7 +661,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::mma_tile(tb + kS1, tTmn, mnmaj(sm, L.Xh, C), C, C, C, false);
         tc::mma_commit(&bar);
     }
-    if (epi) sync_after_mma(&bar, phase, ok);
+    sync_after_mma(&bar, phase, ok, epi);
     if (epi && ok) {
         // element-wise: M, Abar, Mbar o M (in place of Gkk), Gb (in place of Gqk),
         // Pbar o M scaled by r_k (columns) and by r_q (rows) as bf16 operands;
@@ -768,19 +790,41 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         p.dbeta[gbase + 2 * lane] = betab[2 * lane];
         p.dbeta[gbase + 2 * lane + 1] = betab[2 * lane + 1];
     }
-    if (epi) sync_after_mma(&bar, phase, ok);
+    // the producer waits too: once the phase-3 products are done, every operand
+    // tile of this item is dead and the next item's loads go out, under the
+    // final stores below
+    sync_after_mma(&bar, phase, ok, epi || prod);
+    if (prod && ok) {
+        const int next = it + (int)gridDim.x;
+        if (next < nitems) {
+            issue_loads(next);
+            pending = true;
+            pend_pit = pit ^ 1u;
+        }
+    }
     if (epi && ok) {
         // per-value-head partials as bf16 (summed over the group and normalised in fp32)
         uint8_t* dqh = reinterpret_cast<uint8_t*>(p.dqh) + (gbase * Dk) * 2;
         uint8_t* dkh = reinterpret_cast<uint8_t*>(p.dkh) + (gbase * Dk) * 2;
-        acc_rows4(tb, kAQ, Dk, [&](int r, int c0, const float (&x)[16]) {
+        acc_rows2(tb, kAQ, Dk, [&](int r, int c0, const float (&x)[16]) {
             st_bf16x8(dqh + ((int64_t)r * Dk + c0) * 2, x);
             st_bf16x8(dqh + ((int64_t)r * Dk + c0 + 8) * 2, x + 8);
         });
-        acc_rows4(tb, kAK, Dk, [&](int r, int c0, const float (&x)[16]) {
+        acc_rows2(tb, kAK, Dk, [&](int r, int c0, const float (&x)[16]) {
             st_bf16x8(dkh + ((int64_t)r * Dk + c0) * 2, x);
             st_bf16x8(dkh + ((int64_t)r * Dk + c0 + 8) * 2, x + 8);
         });
+    }
+    tc::tc_fence_before();
+    const int failed = __syncthreads_or(!ok);  // a bounded wait gave up: stop here
+    tc::tc_fence_after();
+    if (failed) break;
+    }  // items
+    if (prod && pending) {
+        // only after a failed wait: the copies of an item that will not run land
+        // before the CTA exits (each wait bounded)
+        tc::mbar_wait(&barOV, pend_pit, &g_err_bwdtc);
+        tc::mbar_wait(&barL, pend_pit, &g_err_bwdtc);
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -802,7 +846,9 @@ cudaError_t launch_bwd_chunk_tc(const Dims& d, const Ptrs& p, cudaStream_t s) {
     auto kern = bwd_chunk_tc_kernel;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)d.NC, (unsigned)d.Hv, (unsigned)d.B);
+    // persistent: one CTA per SM (the shared memory allows no second one)
+    const int64_t nitems = d.NC * d.Hv * d.B;
+    const int grid = (int)(nitems < sm_count() ? nitems : sm_count());
     kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps);
     count_launches(1);
     return cudaPeekAtLastError();

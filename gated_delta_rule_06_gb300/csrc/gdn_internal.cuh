@@ -161,6 +161,8 @@ cudaError_t launch_bwd_chunk(const Dims& d, const Ptrs& p, cudaStream_t s);
 cudaError_t launch_bwd_reduce(const Dims& d, const Ptrs& p, cudaStream_t s);
 cudaError_t launch_decode(const Dims& d, const Ptrs& p, cudaStream_t s);
 bool decode_supported(int64_t Dk, int64_t Dv);
+// streaming multiprocessors of the current device (cached per device)
+int sm_count();
 unsigned int read_clear_error_decode();
 // tensor-core (tcgen05) variants for bf16 inputs
 bool bwd_chunk_tc_supported(const Dims& d);
