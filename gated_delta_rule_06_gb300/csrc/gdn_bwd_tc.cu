@@ -438,14 +438,14 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     sync_after_mma(&bar, phase, ok, epi);
     if (epi) {
         if (ok) {
-            acc_rows(tb, kS1, C, [&](int r, int c0, const float (&x)[16]) {
+            acc_rows2(tb, kS1, C, [&](int r, int c0, const float (&x)[16]) {
                 float m[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) m[i] = (c0 + i <= r) ? x[i] : 0.f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) Pf[r * LDM + c0 + i] = m[i];
             });
-            acc_rows(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
+            acc_rows2(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
                 float m[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) m[i] = -bt[c0 + i] * x[i];
@@ -602,11 +602,11 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     float* ZP = Gqk;  // T o (Wbar K^T), until Gqk is formed in phase 2
     sync_after_mma(&bar, phase, ok, epi);
     if (epi && ok) {
-        acc_rows(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
+        acc_rows2(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) Gkk[r * LDM + c0 + i] = rkv[r] * rkv[c0 + i] * x[i];
         });
-        acc_rows(tb, kS1, C, [&](int r, int c0, const float (&x)[16]) {
+        acc_rows2(tb, kS1, C, [&](int r, int c0, const float (&x)[16]) {
             float tt[16];
             ld_bf16x8(sm + L.Tt + tc::panel_off(c0, r, C), tt);
             ld_bf16x8(sm + L.Tt + tc::panel_off(c0 + 8, r, C), tt + 8);
@@ -647,10 +647,10 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     }
     sync_after_mma(&bar, phase, ok, epi);
     if (epi && ok) {
-        acc_rows(tb, kS1, C, [&](int r, int c0, const float (&x)[16]) {
+        acc_rows2(tb, kS1, C, [&](int r, int c0, const float (&x)[16]) {
             tile_put16(sm + L.Xh, C, c0, r, x);  // X row-major (x = l, y = j)
         });
-        acc_rows(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
+        acc_rows2(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) Gqk[r * LDM + c0 + i] = rqv[r] * rkv[c0 + i] * x[i];
         });
