@@ -70,7 +70,8 @@ def work_model(w):
     """Per-phase algorithmic flops and bytes of one fwd+bwd step, in the storage
     formats the kernels use: bf16 inputs keep the saved intermediates as bf16
     operand images (checkpoints, T, W, P, Delta as hi + lo, state cotangents,
-    -Dbar), fp32 inputs as fp32 arrays."""
+    -Dbar, the q / k rows of each chunk) and the per-value-head q / k
+    cotangents in bf16, fp32 inputs all of them as fp32 arrays."""
     es = 2 if w.dtype == torch.bfloat16 else 4
     img = 2 if w.dtype == torch.bfloat16 else 4  # checkpoint / T / cotangent images
     B, T, Hk, Hv, Dk, Dv = w.B, w.T, w.Hk, w.Hv, w.Dk, w.Dv
@@ -80,8 +81,11 @@ def work_model(w):
     units = BH * NC  # (b, h, chunk)
     qk = BHk * NC * 2 * C * Dk * es  # q and k tiles, read once per key head
     m = {}
+    # a, b, q, k in; Gamma (fp64), beta, r_q, r_k out, and on the tensor-core
+    # path the q / k chunk images
     m["prep"] = dict(flops=0.0, bytes=2 * B * T * Hv * es + 2 * B * T * Hk * Dk * es
-                     + 2 * BH * Tp * 4 + BH * Tp * 8 + 2 * BHk * Tp * 4)
+                     + 2 * BH * Tp * 4 + BH * Tp * 8 + 2 * BHk * Tp * 4
+                     + (qk if w.dtype == torch.bfloat16 else 0))
     # q, k, v tiles in; W, P, T images and U (fp32) out
     m["fwd_chunk"] = dict(
         flops=units * (6 * C * C * Dk + 2 * C * C * Dv + C ** 3 / 3),
@@ -98,15 +102,15 @@ def work_model(w):
         bytes=qk + units * (C * Dv * es + C * C * es + C * Dk * es + Dk * Dv * img + C * Dv * img)
         + BH * Dk * Dv * 4)
     # checkpoint and cotangent images, Delta, -Dbar, T, q, k, dO, v in;
-    # dq, dk per value head (fp32), dv, log-decay and beta cotangents out
+    # dq, dk per value head, dv, log-decay and beta cotangents out
     m["bwd_chunk"] = dict(
         flops=units * (6 * C * C * Dv + 14 * C * C * Dk + 6 * C * Dk * Dv + 4 * C ** 3),
         bytes=qk + units * (2 * Dk * Dv * img + C * Dv * 4 + C * Dv * img + C * C * img
                             + 2 * C * Dv * es + 4 * C * 4
-                            + 2 * C * Dk * 4 + C * Dv * es + 2 * C * 4))
+                            + 2 * C * Dk * img + C * Dv * es + 2 * C * 4))
     m["bwd_reduce"] = dict(
         flops=0.0,
-        bytes=2 * BH * T * Dk * 4 + 4 * BHk * T * Dk * es + 2 * BH * T * 4 + 4 * B * T * Hv * es)
+        bytes=2 * BH * T * Dk * img + 4 * BHk * T * Dk * es + 2 * BH * T * 4 + 4 * B * T * Hv * es)
     m["decode"] = dict(flops=BH * (4 * Dk * Dv + 2 * Dk),
                        bytes=BH * 2 * Dk * Dv * 4 + BHk * 2 * Dk * es + BH * 2 * Dv * es
                        + BH * 2 * es)
