@@ -404,41 +404,38 @@ __global__ void __launch_bounds__(256) bwd_chunk_kernel(Dims d, Ptrs p) {
 // ---------------------------------------------------------------------------
 // bwd_reduce
 // ---------------------------------------------------------------------------
-// dq / dk: one warp per (b, t, key head).  Lane l takes the 4-column groups l
-// and l + 32 (Dk <= 256); the per-head rows of both cotangents are loaded as
-// float4 before any is used, so a warp keeps up to 4 G loads in flight.
-__device__ __forceinline__ void add4(float4& a, const float4 b) {
-    a.x += b.x;
-    a.y += b.y;
-    a.z += b.z;
-    a.w += b.w;
-}
-__device__ __forceinline__ void ld4x(const float* x, float* v) {
-    const float4 a = *reinterpret_cast<const float4*>(x);
+// dq / dk: one warp per (b, t, key head).  Lane l takes the eight columns
+// 8l .. 8l + 7 (Dk <= 256, a multiple of 8): one 16-byte load per bf16 row
+// piece.  The q / k rows load first, then the per-value-head partials of the
+// group four heads at a time (all eight loads in flight before any is added);
+// the group sum runs in ascending head order.
+__device__ __forceinline__ void ld8(const float* x, float* v) {
+    const float4 a = reinterpret_cast<const float4*>(x)[0], b = reinterpret_cast<const float4*>(x)[1];
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
-__device__ __forceinline__ void ld4x(const __nv_bfloat16* x, float* v) {
-    const uint2 u = *reinterpret_cast<const uint2*>(x);
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+__device__ __forceinline__ void ld8(const __nv_bfloat16* x, float* v) {
+    const uint4 u = *reinterpret_cast<const uint4*>(x);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
 }
-__device__ __forceinline__ void st4x(float* o, const float* v) {
-    *reinterpret_cast<float4*>(o) = make_float4(v[0], v[1], v[2], v[3]);
+__device__ __forceinline__ void st8(float* o, const float* v) {
+    reinterpret_cast<float4*>(o)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(o)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
-__device__ __forceinline__ void st4x(__nv_bfloat16* o, const float* v) {
-    uint2 u;
-    __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
-    u.x = *reinterpret_cast<uint32_t*>(&a);
-    u.y = *reinterpret_cast<uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(o) = u;
-}
-
-__device__ __forceinline__ float4 ldp4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-__device__ __forceinline__ float4 ldp4(const __nv_bfloat16* p) {
-    float v[4];
-    ld4x(p, v);
-    return make_float4(v[0], v[1], v[2], v[3]);
+__device__ __forceinline__ void st8(__nv_bfloat16* o, const float* v) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(o) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // TI: input dtype; PT: dtype of the per-value-head partials
@@ -450,60 +447,64 @@ __global__ void __launch_bounds__(256) bwd_qk_kernel(Dims d, Ptrs p) {
     const int64_t j = row % d.Hk;
     const int64_t t = (row / d.Hk) % d.T;
     const int64_t bb = row / (d.Hk * d.T);
-    const int Dk = (int)d.Dk, Dk4 = Dk / 4;
-    const int64_t xoff = ((bb * d.T + t) * d.Hk + j) * Dk;
+    const int Dk = (int)d.Dk, G = (int)d.G;
+    const bool act = 8 * lane < Dk;
+    const int c0 = act ? 8 * lane : 0;
+    const int64_t xoff = ((bb * d.T + t) * d.Hk + j) * Dk + c0;
     const int64_t hstride = d.Tp * Dk;  // next value head of the group
-    const int64_t off0 = ((bb * d.Hv + j * d.G) * d.Tp + t) * Dk;
-    float4 y[2][2];  // [pass][group]
+    const int64_t off0 = ((bb * d.Hv + j * d.G) * d.Tp + t) * Dk + c0;
+    const PT* dqh = reinterpret_cast<const PT*>(p.dqh) + off0;
+    const PT* dkh = reinterpret_cast<const PT*>(p.dkh) + off0;
+    float u[2][8], y[2][8];
 #pragma unroll
-    for (int ps = 0; ps < 2; ++ps)
+    for (int c = 0; c < 8; ++c) u[0][c] = u[1][c] = y[0][c] = y[1][c] = 0.f;
+    if (act) {
+        ld8((const TI*)p.q + xoff, u[0]);
+        ld8((const TI*)p.k + xoff, u[1]);
+        int g = 0;
+        for (; g + 4 <= G; g += 4) {
+            float a[4][8], b[4][8];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) y[ps][i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t g = 0; g < d.G; ++g) {
+            for (int e = 0; e < 4; ++e) {
+                ld8(dqh + (int64_t)(g + e) * hstride, a[e]);
+                ld8(dkh + (int64_t)(g + e) * hstride, b[e]);
+            }
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int q4 = lane + 32 * i;
-            if (q4 < Dk4) {
-                const int64_t off = off0 + g * hstride + 4 * q4;
-                add4(y[0][i], ldp4(reinterpret_cast<const PT*>(p.dqh) + off));
-                add4(y[1][i], ldp4(reinterpret_cast<const PT*>(p.dkh) + off));
+            for (int e = 0; e < 4; ++e)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    y[0][c] += a[e][c];
+                    y[1][c] += b[e][c];
+                }
+        }
+        for (; g < G; ++g) {
+            float a[8], b[8];
+            ld8(dqh + (int64_t)g * hstride, a);
+            ld8(dkh + (int64_t)g * hstride, b);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                y[0][c] += a[c];
+                y[1][c] += b[c];
             }
         }
     }
 #pragma unroll
     for (int ps = 0; ps < 2; ++ps) {
-        const TI* x = (const TI*)(ps == 0 ? p.q : p.k) + xoff;
         const float r = (ps == 0 ? p.rq : p.rk)[(bb * d.Hk + j) * d.Tp + t];
         const float s = ps == 0 ? rsqrtf((float)Dk) : 1.f;
-        float u[2][4], yv[2][4];
         float dot = 0.f;
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int q4 = lane + 32 * i;
-            yv[i][0] = y[ps][i].x; yv[i][1] = y[ps][i].y; yv[i][2] = y[ps][i].z; yv[i][3] = y[ps][i].w;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) u[i][c] = 0.f;
-            if (q4 < Dk4) {
-                ld4x(x + 4 * q4, u[i]);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    u[i][c] *= r;
-                    dot = fmaf(u[i][c], yv[i][c], dot);
-                }
-            }
+        for (int c = 0; c < 8; ++c) {
+            u[ps][c] *= r;
+            dot = fmaf(u[ps][c], y[ps][c], dot);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-        TI* out = (TI*)(ps == 0 ? p.dq : p.dk) + xoff;
+        if (act) {
+            float o[8];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int q4 = lane + 32 * i;
-            if (q4 < Dk4) {
-                float o[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) o[c] = s * r * (yv[i][c] - u[i][c] * dot);
-                st4x(out + 4 * q4, o);
-            }
+            for (int c = 0; c < 8; ++c) o[c] = s * r * (y[ps][c] - u[ps][c] * dot);
+            st8((TI*)(ps == 0 ? p.dq : p.dk) + xoff, o);
         }
     }
 }
