@@ -15,6 +15,9 @@ float64 numpy arrays in the op contract's layouts (torch-to-nnef page,
     A_log, dt_bias [Hv];  state [B, Hv, Dk, Dv];  mask [B, T] (bool / uint8);
     o [B, T, Hv, Dv].
 
+The ``*_lb`` functions take the op contract's other gate form instead of
+(a, b, A_log, dt_bias): log_decay = log g and beta, both [B, T, Hv].
+
 Inputs may be any real dtype; they are upcast exactly to float64 (bf16 and
 fp32 values are representable in fp64), so input rounding is not counted as
 oracle error.
@@ -66,6 +69,10 @@ def _load():
         lib.gdn_oracle_forward_chunked.restype = ctypes.c_int
         lib.gdn_oracle_backward.argtypes = [i64] * 6 + [dp] * 19
         lib.gdn_oracle_backward.restype = ctypes.c_int
+        lib.gdn_oracle_forward_lb.argtypes = [i64] * 6 + [dp] * 9
+        lib.gdn_oracle_forward_lb.restype = ctypes.c_int
+        lib.gdn_oracle_backward_lb.argtypes = [i64] * 6 + [dp] * 15
+        lib.gdn_oracle_backward_lb.restype = ctypes.c_int
         lib.gdn_oracle_threads.argtypes = []
         lib.gdn_oracle_threads.restype = ctypes.c_int
         _lib = lib
@@ -158,3 +165,40 @@ def backward(q, k, v, a, b, A_log, dt_bias, state0, mask, d_o, d_state_T=None):
 
 
 GRAD_NAMES = ("dq", "dk", "dv", "da", "db", "dA_log", "ddt_bias", "dstate0")
+
+
+def forward_lb(q, k, v, log_decay, beta, state0=None, mask=None):
+    """Sequential recurrence with the gates given as log_decay = log g and beta
+    ([B, T, Hv]).  Returns (o, state_T)."""
+    q, k, v, log_decay, beta, state0 = map(_f64, (q, k, v, log_decay, beta, state0))
+    mask = _u8(mask)
+    B, T, Hk, Hv, Dk, Dv = _dims(q, v)
+    o = np.zeros((B, T, Hv, Dv))
+    sT = np.zeros((B, Hv, Dk, Dv))
+    rc = _load().gdn_oracle_forward_lb(B, T, Hk, Hv, Dk, Dv, *map(_ptr, (
+        q, k, v, log_decay, beta, state0, mask, o, sT)))
+    if rc:
+        raise ValueError(f"oracle forward_lb rejected the shapes (code {rc})")
+    return o, sT
+
+
+def backward_lb(q, k, v, log_decay, beta, state0, mask, d_o, d_state_T=None):
+    """VJP of forward_lb.  Returns a dict with dq, dk, dv, d_log_decay, d_beta,
+    dstate0 (the gate cotangents [B, T, Hv], zero on masked steps)."""
+    q, k, v, log_decay, beta, state0, d_o, d_state_T = map(
+        _f64, (q, k, v, log_decay, beta, state0, d_o, d_state_T))
+    mask = _u8(mask)
+    B, T, Hk, Hv, Dk, Dv = _dims(q, v)
+    out = dict(
+        dq=np.zeros(q.shape), dk=np.zeros(k.shape), dv=np.zeros(v.shape),
+        d_log_decay=np.zeros(log_decay.shape), d_beta=np.zeros(beta.shape),
+        dstate0=np.zeros((B, Hv, Dk, Dv)))
+    rc = _load().gdn_oracle_backward_lb(B, T, Hk, Hv, Dk, Dv, *map(_ptr, (
+        q, k, v, log_decay, beta, state0, mask, d_o, d_state_T,
+        out["dq"], out["dk"], out["dv"], out["d_log_decay"], out["d_beta"], out["dstate0"])))
+    if rc:
+        raise ValueError(f"oracle backward_lb rejected the shapes (code {rc})")
+    return out
+
+
+GRAD_NAMES_LB = ("dq", "dk", "dv", "d_log_decay", "d_beta", "dstate0")

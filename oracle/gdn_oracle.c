@@ -22,6 +22,10 @@
  *    with the softplus argument clamped, beta = sigmoid(b).  The clamp value
  *    is not printed; this oracle uses softplus(min(x, 20)) whose derivative is
  *    sigmoid(x) for x <= 20 and 0 above.
+ *  - Second input form (torch-to-nnef page, op contract: log_decay and beta
+ *    [b, S, hv]): the per-step log-decay l = log g and beta are given
+ *    directly; its VJP returns their cotangents.  Both forms run one fp64
+ *    core that takes (l, beta) per step; the a / b form computes them first.
  *  - Recurrence (the recurrent step that both pages name): per (b, h)
  *      S <- g S;  delta = beta (v - S^T k);  S <- S + k delta^T;  o = S^T q.
  *    A masked step leaves S unchanged (mlx-lm page, "Covered corner cases":
@@ -131,16 +135,31 @@ static void read_out(int64_t Dk, int64_t Dv, const double* S, const double* qh, 
         for (int64_t c = 0; c < Dv; ++c) o[c] += S[r * Dv + c] * qh[r];
 }
 
+/* Per-step gates of the a / b form in fp64: lg = log g, bt = beta ([B, T, Hv]).
+ * Returns 0, or 3 when memory runs out (both arrays then NULL). */
+static int gates_ab(const dims_t* d, const double* a, const double* b, const double* A_log,
+                    const double* dt_bias, double** lg, double** bt) {
+    int64_t n = d->B * d->T * d->Hv;
+    *lg = malloc(sizeof(double) * (n > 0 ? n : 1));
+    *bt = malloc(sizeof(double) * (n > 0 ? n : 1));
+    if (!*lg || !*bt) { free(*lg); free(*bt); *lg = *bt = NULL; return 3; }
+    for (int64_t bb = 0; bb < d->B; ++bb)
+        for (int64_t t = 0; t < d->T; ++t)
+            for (int64_t h = 0; h < d->Hv; ++h) {
+                int64_t ix = IG(d, bb, t, h);
+                (*lg)[ix] = log_decay(a[ix], A_log[h], dt_bias[h]);
+                (*bt)[ix] = sigmoid_d(b[ix]);
+            }
+    return 0;
+}
+
 /* ---- sequential forward -------------------------------------------------- */
 
-int gdn_oracle_forward(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk, int64_t Dv,
-                       const double* q, const double* k, const double* v, const double* a,
-                       const double* b, const double* A_log, const double* dt_bias,
-                       const double* state0, const uint8_t* mask, double* o,
-                       double* state_T) {
-    dims_t d = {B, T, Hk, Hv, Dk, Dv};
-    int rc = check_dims(&d);
-    if (rc) return rc;
+static int forward_core(const dims_t* dd, const double* q, const double* k, const double* v,
+                        const double* lg, const double* bt, const double* state0,
+                        const uint8_t* mask, double* o, double* state_T) {
+    const dims_t d = *dd;
+    const int64_t B = d.B, T = d.T, Hv = d.Hv, Dk = d.Dk, Dv = d.Dv;
     int64_t npairs = B * Hv;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t pr = 0; pr < npairs; ++pr) {
@@ -158,8 +177,8 @@ int gdn_oracle_forward(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk,
             load_qk_hat(&d, q, k, bb, t, h, qh, kh);
             int on = mask ? (mask[bb * T + t] != 0) : 1;
             if (on) {
-                double g = exp(log_decay(a[IG(&d, bb, t, h)], A_log[h], dt_bias[h]));
-                double beta = sigmoid_d(b[IG(&d, bb, t, h)]);
+                double g = exp(lg[IG(&d, bb, t, h)]);
+                double beta = bt[IG(&d, bb, t, h)];
                 apply_step(Dk, Dv, S, g, beta, kh, v + IV(&d, bb, t, h), p, dl);
             }
             read_out(Dk, Dv, S, qh, o + IV(&d, bb, t, h));
@@ -167,6 +186,32 @@ int gdn_oracle_forward(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk,
         free(qh); free(kh); free(p); free(dl);
     }
     return 0;
+}
+
+int gdn_oracle_forward(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk, int64_t Dv,
+                       const double* q, const double* k, const double* v, const double* a,
+                       const double* b, const double* A_log, const double* dt_bias,
+                       const double* state0, const uint8_t* mask, double* o,
+                       double* state_T) {
+    dims_t d = {B, T, Hk, Hv, Dk, Dv};
+    int rc = check_dims(&d);
+    if (rc) return rc;
+    double *lg, *bt;
+    if (gates_ab(&d, a, b, A_log, dt_bias, &lg, &bt)) return 3;
+    rc = forward_core(&d, q, k, v, lg, bt, state0, mask, o, state_T);
+    free(lg); free(bt);
+    return rc;
+}
+
+/* log_decay / beta form: l and beta per step, [B, T, Hv] */
+int gdn_oracle_forward_lb(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk, int64_t Dv,
+                          const double* q, const double* k, const double* v,
+                          const double* log_decay_, const double* beta, const double* state0,
+                          const uint8_t* mask, double* o, double* state_T) {
+    dims_t d = {B, T, Hk, Hv, Dk, Dv};
+    int rc = check_dims(&d);
+    if (rc) return rc;
+    return forward_core(&d, q, k, v, log_decay_, beta, state0, mask, o, state_T);
 }
 
 /* ---- chunked (WY/UT) forward: second, independent formulation ------------- */
@@ -304,25 +349,24 @@ int gdn_oracle_forward_chunked(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int
  *            db = betabar * beta (1 - beta);
  *            dA_log[h] = sum_{b,t} lbar * l;  ddt_bias[h] = sum_{b,t} da
  */
-int gdn_oracle_backward(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk, int64_t Dv,
-                        const double* q, const double* k, const double* v, const double* a,
-                        const double* b, const double* A_log, const double* dt_bias,
-                        const double* state0, const uint8_t* mask, const double* d_o,
-                        const double* d_state_T, double* dq, double* dk, double* dv,
-                        double* da, double* db, double* dA_log, double* ddt_bias,
-                        double* dstate0) {
-    dims_t d = {B, T, Hk, Hv, Dk, Dv};
-    int rc = check_dims(&d);
-    if (rc) return rc;
+/* The VJP up to the gates: dq, dk, dv, dstate0 and the per-step cotangents
+ * dlg of l = log g and dbt of beta ([B, T, Hv], zero on masked steps). */
+static int backward_core(const dims_t* dd, const double* q, const double* k, const double* v,
+                         const double* lg, const double* bt, const double* state0,
+                         const uint8_t* mask, const double* d_o, const double* d_state_T,
+                         double* dq, double* dk, double* dv, double* dlg, double* dbt,
+                         double* dstate0) {
+    const dims_t d = *dd;
+    const int64_t B = d.B, T = d.T, Hk = d.Hk, Hv = d.Hv, Dk = d.Dk, Dv = d.Dv;
     int64_t G = Hv / Hk;
     int64_t SS = Dk * Dv;
     int64_t nseg = (T + SEGMENT - 1) / SEGMENT;
-    /* per value head gradients of the normalised q / k, and of l, beta */
+    /* per value head gradients of the normalised q / k */
     double* dqh = calloc((size_t)(B * T * Hv * Dk > 0 ? B * T * Hv * Dk : 1), sizeof(double));
     double* dkh = calloc((size_t)(B * T * Hv * Dk > 0 ? B * T * Hv * Dk : 1), sizeof(double));
-    double* dlg = calloc((size_t)(B * T * Hv > 0 ? B * T * Hv : 1), sizeof(double));
-    double* dbt = calloc((size_t)(B * T * Hv > 0 ? B * T * Hv : 1), sizeof(double));
-    if (!dqh || !dkh || !dlg || !dbt) { free(dqh); free(dkh); free(dlg); free(dbt); return 3; }
+    if (!dqh || !dkh) { free(dqh); free(dkh); return 3; }
+    memset(dlg, 0, sizeof(double) * B * T * Hv);
+    memset(dbt, 0, sizeof(double) * B * T * Hv);
     int64_t npairs = B * Hv;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t pr = 0; pr < npairs; ++pr) {
@@ -350,8 +394,8 @@ int gdn_oracle_backward(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk
             int on = mask ? (mask[bb * T + t] != 0) : 1;
             if (on) {
                 load_qk_hat(&d, q, k, bb, t, h, qh, kh);
-                double g = exp(log_decay(a[IG(&d, bb, t, h)], A_log[h], dt_bias[h]));
-                double beta = sigmoid_d(b[IG(&d, bb, t, h)]);
+                double g = exp(lg[IG(&d, bb, t, h)]);
+                double beta = bt[IG(&d, bb, t, h)];
                 apply_step(Dk, Dv, S, g, beta, kh, v + IV(&d, bb, t, h), p, dl);
             }
         }
@@ -372,8 +416,8 @@ int gdn_oracle_backward(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk
                 int on = mask ? (mask[bb * T + t] != 0) : 1;
                 if (on) {
                     load_qk_hat(&d, q, k, bb, t, h, qh, kh);
-                    double g = exp(log_decay(a[IG(&d, bb, t, h)], A_log[h], dt_bias[h]));
-                    double beta = sigmoid_d(b[IG(&d, bb, t, h)]);
+                    double g = exp(lg[IG(&d, bb, t, h)]);
+                    double beta = bt[IG(&d, bb, t, h)];
                     apply_step(Dk, Dv, Sn, g, beta, kh, v + IV(&d, bb, t, h), p, dl);
                 }
             }
@@ -397,9 +441,8 @@ int gdn_oracle_backward(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk
                 }
                 int on = mask ? (mask[bb * T + t] != 0) : 1;
                 if (!on) continue;
-                double lgv = log_decay(a[IG(&d, bb, t, h)], A_log[h], dt_bias[h]);
-                double g = exp(lgv);
-                double beta = sigmoid_d(b[IG(&d, bb, t, h)]);
+                double g = exp(lg[IG(&d, bb, t, h)]);
+                double beta = bt[IG(&d, bb, t, h)];
                 const double* vt = v + IV(&d, bb, t, h);
                 /* S_a = g S_prev, p = S_a^T k, delta = beta (v - p) */
                 for (int64_t x = 0; x < SS; ++x) Sa[x] = g * Sprev[x];
@@ -477,6 +520,28 @@ int gdn_oracle_backward(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk
                 }
             }
     free(acc);
+    free(dqh); free(dkh);
+    return 0;
+}
+
+int gdn_oracle_backward(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk, int64_t Dv,
+                        const double* q, const double* k, const double* v, const double* a,
+                        const double* b, const double* A_log, const double* dt_bias,
+                        const double* state0, const uint8_t* mask, const double* d_o,
+                        const double* d_state_T, double* dq, double* dk, double* dv,
+                        double* da, double* db, double* dA_log, double* ddt_bias,
+                        double* dstate0) {
+    dims_t d = {B, T, Hk, Hv, Dk, Dv};
+    int rc = check_dims(&d);
+    if (rc) return rc;
+    double *lg, *bt;
+    if (gates_ab(&d, a, b, A_log, dt_bias, &lg, &bt)) return 3;
+    double* dlg = malloc(sizeof(double) * (B * T * Hv > 0 ? B * T * Hv : 1));
+    double* dbt = malloc(sizeof(double) * (B * T * Hv > 0 ? B * T * Hv : 1));
+    if (!dlg || !dbt) { free(lg); free(bt); free(dlg); free(dbt); return 3; }
+    rc = backward_core(&d, q, k, v, lg, bt, state0, mask, d_o, d_state_T, dq, dk, dv, dlg, dbt,
+                       dstate0);
+    if (rc) { free(lg); free(bt); free(dlg); free(dbt); return rc; }
     /* gates and per-head sums (fixed order: b, then t) */
     for (int64_t h = 0; h < Hv; ++h) {
         double sA = 0.0, sdt = 0.0;
@@ -497,8 +562,23 @@ int gdn_oracle_backward(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk
         dA_log[h] = sA;
         ddt_bias[h] = sdt;
     }
-    free(dqh); free(dkh); free(dlg); free(dbt);
+    free(lg); free(bt); free(dlg); free(dbt);
     return 0;
+}
+
+/* log_decay / beta form: returns d_log_decay and d_beta ([B, T, Hv], zero on
+ * masked steps) in place of the gate-parameter cotangents */
+int gdn_oracle_backward_lb(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk, int64_t Dv,
+                           const double* q, const double* k, const double* v,
+                           const double* log_decay_, const double* beta, const double* state0,
+                           const uint8_t* mask, const double* d_o, const double* d_state_T,
+                           double* dq, double* dk, double* dv, double* d_log_decay,
+                           double* d_beta, double* dstate0) {
+    dims_t d = {B, T, Hk, Hv, Dk, Dv};
+    int rc = check_dims(&d);
+    if (rc) return rc;
+    return backward_core(&d, q, k, v, log_decay_, beta, state0, mask, d_o, d_state_T, dq, dk,
+                         dv, d_log_decay, d_beta, dstate0);
 }
 
 /* ---- threads the OpenMP runtime will use --------------------------------- */

@@ -323,3 +323,113 @@ def test_chunked_catches_planted_slip():
     y["v"][0, 64, 0] += 1e-3
     o2, _ = oracle.forward_chunked(*[y[n] for n in args], chunk=64)
     assert np.abs(o1 - o2).max() > 1e-8
+
+
+# -- the log_decay / beta input form (torch-to-nnef page, op contract) ----------
+
+def _lb_inputs(B, T, Hk, Hv, Dk, Dv, seed, masked=False):
+    r = np.random.default_rng(seed)
+    x = dict(q=r.standard_normal((B, T, Hk, Dk)), k=r.standard_normal((B, T, Hk, Dk)),
+             v=r.standard_normal((B, T, Hv, Dv)),
+             log_decay=-r.uniform(0.0, 2.0, (B, T, Hv)), beta=r.uniform(0.0, 1.0, (B, T, Hv)),
+             state0=0.1 * r.standard_normal((B, Hv, Dk, Dv)), mask=None,
+             d_o=r.standard_normal((B, T, Hv, Dv)), d_state_T=r.standard_normal((B, Hv, Dk, Dv)))
+    if masked:
+        m = np.ones((B, T), dtype=np.uint8)
+        m[-1, T // 2:] = 0
+        x["mask"] = m
+    return x
+
+
+def _lb_loss(x):
+    o, sT = oracle.forward_lb(x["q"], x["k"], x["v"], x["log_decay"], x["beta"], x["state0"],
+                              x["mask"])
+    return float((o * x["d_o"]).sum() + (sT * x["d_state_T"]).sum())
+
+
+@pytest.mark.parametrize("masked", [False, True])
+def test_lb_fd_all_grads(masked):
+    """Central differences of L = <o, dO> + <S_T, dS_T> through the log_decay /
+    beta form (GQA G = 2, T = 67 over two 64-step segments, optional mask)."""
+    x = _lb_inputs(2, 67, 1, 2, 6, 4, seed=21 + masked, masked=masked)
+    g = oracle.backward_lb(x["q"], x["k"], x["v"], x["log_decay"], x["beta"], x["state0"],
+                           x["mask"], x["d_o"], x["d_state_T"])
+    h = 2.0 ** -17
+    rng = np.random.default_rng(5)
+    names = dict(q="dq", k="dk", v="dv", log_decay="d_log_decay", beta="d_beta",
+                 state0="dstate0")
+    for name, gname in names.items():
+        flat = x[name].reshape(-1)
+        idx = rng.choice(flat.size, min(flat.size, 24), replace=False)
+        if masked and name in ("log_decay", "beta"):  # include masked steps
+            idx = np.concatenate([idx, [flat.size - 1, flat.size - 3]])
+        fd = np.zeros(len(idx))
+        for n, i in enumerate(idx):
+            old = flat[i]
+            flat[i] = old + h
+            lp = _lb_loss(x)
+            flat[i] = old - h
+            lm = _lb_loss(x)
+            flat[i] = old
+            fd[n] = (lp - lm) / (2 * h)
+        an = g[gname].reshape(-1)[idx]
+        assert np.abs(an - fd).max() <= 1e-7 * max(np.abs(fd).max(), 1.0), name
+
+
+def test_lb_identity_and_reset_closed_forms():
+    """log_decay = 0, beta = 0 is the identity step (S_T = S_0, o_t = S_0^T q_t);
+    log_decay = -800 (g = 0 in fp64) resets the state each step, so
+    S_t = k_t (beta_t v_t)^T and o_t = <q_t, k_t> beta_t v_t (normalised q, k)."""
+    x = _lb_inputs(1, 9, 1, 2, 5, 3, seed=31)
+    q, k, v, s0 = x["q"], x["k"], x["v"], x["state0"]
+    qh = q / np.sqrt((q * q).sum(-1, keepdims=True) + 1e-6) / np.sqrt(q.shape[-1])
+    kh = k / np.sqrt((k * k).sum(-1, keepdims=True) + 1e-6)
+    zero = np.zeros_like(x["beta"])
+    o, sT = oracle.forward_lb(q, k, v, zero, zero, s0)
+    np.testing.assert_array_equal(sT, s0)
+    for h in range(2):
+        np.testing.assert_allclose(o[0, :, h], qh[0, :, 0] @ s0[0, h], rtol=0, atol=1e-13)
+    reset = np.full_like(x["beta"], -800.0)
+    o, sT = oracle.forward_lb(q, k, v, reset, x["beta"], s0)
+    for h in range(2):
+        qk = (qh[0, :, 0] * kh[0, :, 0]).sum(-1)
+        want = (qk * x["beta"][0, :, h])[:, None] * v[0, :, h]
+        np.testing.assert_allclose(o[0, :, h], want, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(sT[0, h], np.outer(kh[0, -1, 0], x["beta"][0, -1, h] * v[0, -1, h]),
+                                   rtol=0, atol=1e-13)
+    g = oracle.backward_lb(q, k, v, reset, x["beta"], s0, None, x["d_o"], x["d_state_T"])
+    assert np.all(g["d_log_decay"] == 0.0)   # d/dl = gbar * g with g = 0
+    assert np.all(g["dstate0"] == 0.0)       # the first step erases S_0
+
+
+def test_lb_matches_gate_form_and_chain_rule():
+    """The two gate forms describe one recurrence: with l = -exp(A_log)
+    softplus(min(a + dt_bias, 20)) and beta = sigmoid(b), the log_decay / beta
+    form gives the same o and S_T, and the gate cotangents of the a / b form are
+    its d_log_decay, d_beta through that map (clamp head included)."""
+    w = wl.custom("lbmap", 2, 70, 1, 2, 6, 4, seed=41, mask="half_second_batch",
+                  clamp_head=True)
+    x = _inputs(w)
+    xc = x["a"] + x["dt_bias"][None, None, :]
+    l = -np.exp(x["A_log"])[None, None, :] * np.log1p(np.exp(np.minimum(xc, 20.0)))
+    beta = 1.0 / (1.0 + np.exp(-x["b"]))
+    o1, s1 = oracle.forward(x["q"], x["k"], x["v"], x["a"], x["b"], x["A_log"], x["dt_bias"],
+                            x["state0"], x["mask"])
+    o2, s2 = oracle.forward_lb(x["q"], x["k"], x["v"], l, beta, x["state0"], x["mask"])
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(s2, s1, rtol=0, atol=1e-12)
+    g1 = oracle.backward(x["q"], x["k"], x["v"], x["a"], x["b"], x["A_log"], x["dt_bias"],
+                         x["state0"], x["mask"], x["d_o"], x["d_state_T"])
+    g2 = oracle.backward_lb(x["q"], x["k"], x["v"], l, beta, x["state0"], x["mask"], x["d_o"],
+                            x["d_state_T"])
+    for n in ("dq", "dk", "dv", "dstate0"):
+        np.testing.assert_allclose(g2[n], g1[n], rtol=0, atol=1e-10 * max(1.0, np.abs(g1[n]).max()))
+    sig = 1.0 / (1.0 + np.exp(-xc))
+    da = g2["d_log_decay"] * (-np.exp(x["A_log"]))[None, None, :] * np.where(xc <= 20.0, sig, 0.0)
+    np.testing.assert_allclose(g1["da"], da, rtol=0, atol=1e-10 * max(1.0, np.abs(da).max()))
+    np.testing.assert_allclose(g1["db"], g2["d_beta"] * beta * (1 - beta), rtol=0, atol=1e-10)
+    np.testing.assert_allclose(g1["dA_log"], (g2["d_log_decay"] * l).sum((0, 1)), rtol=1e-10,
+                               atol=1e-10)
+    if x["mask"] is not None:
+        off = x["mask"] == 0
+        assert np.all(g2["d_log_decay"][off] == 0) and np.all(g2["d_beta"][off] == 0)
