@@ -287,15 +287,20 @@ gdn_status gdn_saved_bytes(const gdn_shape* shape, size_t* bytes) {
     return GDN_OK;
 }
 
-gdn_status gdn_forward(const gdn_shape* shape, const void* q, const void* k, const void* v,
-                       const void* a, const void* b, const float* A_log, const float* dt_bias,
-                       const float* state0, const uint8_t* mask, void* o, float* state_T,
-                       void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
-                       void* stream) {
+namespace {
+// gdn_forward and gdn_forward_lb: gates = 0 takes (a, b, A_log, dt_bias), 1 takes
+// (log_decay, beta) in a, b
+gdn_status forward_impl(const gdn_shape* shape, int gates, const void* q, const void* k,
+                        const void* v, const void* a, const void* b, const float* A_log,
+                        const float* dt_bias, const float* state0, const uint8_t* mask, void* o,
+                        float* state_T, void* saved, size_t saved_bytes, void* ws,
+                        size_t ws_bytes, void* stream) {
     gdn::Dims d;
     gdn_status st = validate_shape(shape, &d);
     if (st != GDN_OK) return st;
-    if (!q || !k || !v || !a || !b || !A_log || !dt_bias || !o || !state_T) return GDN_ERR_INVALID_ARG;
+    d.gates = gates;
+    if (!q || !k || !v || !a || !b || !o || !state_T) return GDN_ERR_INVALID_ARG;
+    if (gates == 0 && (!A_log || !dt_bias)) return GDN_ERR_INVALID_ARG;
     if (shape->has_mask && !mask) return GDN_ERR_INVALID_ARG;
     const void* ptrs[] = {q, k, v, a, b, A_log, dt_bias, state0, mask, o, state_T, saved, ws};
     for (const void* p : ptrs)
@@ -332,18 +337,22 @@ gdn_status gdn_forward(const gdn_shape* shape, const void* q, const void* k, con
     return cuda_status(e);
 }
 
-gdn_status gdn_backward(const gdn_shape* shape, const void* q, const void* k, const void* v,
-                        const void* a, const void* b, const float* A_log, const float* dt_bias,
-                        const uint8_t* mask, const void* saved, size_t saved_bytes,
-                        const void* d_o, const float* d_state_T, void* dq, void* dk, void* dv,
-                        void* da, void* db, float* dA_log, float* ddt_bias, float* dstate0,
-                        void* ws, size_t ws_bytes, void* stream) {
+// gdn_backward and gdn_backward_lb (gates as in forward_impl; with gates = 1, da
+// and db receive the log_decay and beta cotangents and dA_log, ddt_bias are unused)
+gdn_status backward_impl(const gdn_shape* shape, int gates, const void* q, const void* k,
+                         const void* v, const void* a, const void* b, const float* A_log,
+                         const float* dt_bias, const uint8_t* mask, const void* saved,
+                         size_t saved_bytes, const void* d_o, const float* d_state_T, void* dq,
+                         void* dk, void* dv, void* da, void* db, float* dA_log, float* ddt_bias,
+                         float* dstate0, void* ws, size_t ws_bytes, void* stream) {
     gdn::Dims d;
     gdn_status st = validate_shape(shape, &d);
     if (st != GDN_OK) return st;
-    if (!q || !k || !v || !a || !b || !A_log || !dt_bias || !saved || !d_o || !dq || !dk ||
-        !dv || !da || !db || !dA_log || !ddt_bias || !dstate0 || !ws)
+    d.gates = gates;
+    if (!q || !k || !v || !a || !b || !saved || !d_o || !dq || !dk || !dv || !da || !db ||
+        !dstate0 || !ws)
         return GDN_ERR_INVALID_ARG;
+    if (gates == 0 && (!A_log || !dt_bias || !dA_log || !ddt_bias)) return GDN_ERR_INVALID_ARG;
     if (shape->has_mask && !mask) return GDN_ERR_INVALID_ARG;
     const void* ptrs[] = {q, k, v, a, b, A_log, dt_bias, mask, saved, d_o, d_state_T, dq, dk,
                           dv, da, db, dA_log, ddt_bias, dstate0, ws};
@@ -377,6 +386,46 @@ gdn_status gdn_backward(const gdn_shape* shape, const void* q, const void* k, co
     if (e == cudaSuccess) e = run_phase("bwd_chunk", s, [&] { return gdn::launch_bwd_chunk(d, p, s); });
     if (e == cudaSuccess) e = run_phase("bwd_reduce", s, [&] { return gdn::launch_bwd_reduce(d, p, s); });
     return cuda_status(e);
+}
+}  // namespace
+
+gdn_status gdn_forward(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                       const void* a, const void* b, const float* A_log, const float* dt_bias,
+                       const float* state0, const uint8_t* mask, void* o, float* state_T,
+                       void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
+                       void* stream) {
+    return forward_impl(shape, 0, q, k, v, a, b, A_log, dt_bias, state0, mask, o, state_T, saved,
+                        saved_bytes, ws, ws_bytes, stream);
+}
+
+gdn_status gdn_forward_lb(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                          const void* log_decay, const void* beta, const float* state0,
+                          const uint8_t* mask, void* o, float* state_T, void* saved,
+                          size_t saved_bytes, void* ws, size_t ws_bytes, void* stream) {
+    return forward_impl(shape, 1, q, k, v, log_decay, beta, nullptr, nullptr, state0, mask, o,
+                        state_T, saved, saved_bytes, ws, ws_bytes, stream);
+}
+
+gdn_status gdn_backward(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                        const void* a, const void* b, const float* A_log, const float* dt_bias,
+                        const uint8_t* mask, const void* saved, size_t saved_bytes,
+                        const void* d_o, const float* d_state_T, void* dq, void* dk, void* dv,
+                        void* da, void* db, float* dA_log, float* ddt_bias, float* dstate0,
+                        void* ws, size_t ws_bytes, void* stream) {
+    return backward_impl(shape, 0, q, k, v, a, b, A_log, dt_bias, mask, saved, saved_bytes, d_o,
+                         d_state_T, dq, dk, dv, da, db, dA_log, ddt_bias, dstate0, ws, ws_bytes,
+                         stream);
+}
+
+gdn_status gdn_backward_lb(const gdn_shape* shape, const void* q, const void* k,
+                           const void* v, const void* log_decay, const void* beta,
+                           const uint8_t* mask, const void* saved, size_t saved_bytes,
+                           const void* d_o, const float* d_state_T, void* dq, void* dk,
+                           void* dv, void* d_log_decay, void* d_beta, float* dstate0,
+                           void* ws, size_t ws_bytes, void* stream) {
+    return backward_impl(shape, 1, q, k, v, log_decay, beta, nullptr, nullptr, mask, saved,
+                         saved_bytes, d_o, d_state_T, dq, dk, dv, d_log_decay, d_beta, nullptr,
+                         nullptr, dstate0, ws, ws_bytes, stream);
 }
 
 uint64_t gdn_launch_count(void) { return g_launches.load(); }

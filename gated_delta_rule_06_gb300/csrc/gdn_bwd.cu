@@ -530,7 +530,13 @@ __global__ void __launch_bounds__(256) bwd_gate_kernel(Dims d, Ptrs p) {
         if (t < d.T) {
             const int64_t ix = ((int64_t)bb * d.T + t) * d.Hv + h;
             float ga = 0.f, gb = 0.f;
-            if (p.mask == nullptr || p.mask[bb * d.T + t] != 0) {
+            if (d.gates == 1) {  // cotangents of the given log_decay and beta
+                if (p.mask == nullptr || p.mask[bb * d.T + t] != 0) {
+                    const int64_t gx = ((int64_t)bb * d.Hv + h) * d.Tp + t;
+                    ga = p.dl[gx];
+                    gb = p.dbeta[gx];
+                }
+            } else if (p.mask == nullptr || p.mask[bb * d.T + t] != 0) {
                 const int64_t gx = ((int64_t)bb * d.Hv + h) * d.Tp + t;
                 const float lb = p.dl[gx];
                 const float x = ldf(a + ix) + p.dt_bias[h];
@@ -550,6 +556,7 @@ __global__ void __launch_bounds__(256) bwd_gate_kernel(Dims d, Ptrs p) {
         sA[i][hh] = vA;
         sD[i][hh] = vD;
     }
+    if (d.gates == 1) return;  // no per-head gate parameters
     __syncthreads();
     // fixed-order sum over the 64 steps: one warp per head, pairwise tree
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -618,6 +625,10 @@ cudaError_t launch_reduce_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
         bwd_qk_kernel<TI, float><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(d, p);
     dim3 g((unsigned)d.NC, (unsigned)d.B, (unsigned)((d.Hv + kGateHeadsB - 1) / kGateHeadsB));
     bwd_gate_kernel<TI><<<g, 256, 0, s>>>(d, p);
+    if (d.gates == 1) {  // log_decay / beta inputs: no per-head parameters to sum
+        count_launches(2);
+        return cudaPeekAtLastError();
+    }
     bwd_head_sum_kernel<<<(unsigned)((d.Hv + 127) / 128), 128, 0, s>>>(d, p);
     count_launches(3);
     return cudaPeekAtLastError();

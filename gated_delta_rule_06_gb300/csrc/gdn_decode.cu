@@ -97,9 +97,14 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Dims d, Ptrs p) {
         float g = 1.f, be = 0.f;
         if (on) {
             const int64_t ix = (int64_t)bb * d.Hv + h;
-            const float x = ldf((const TI*)p.a + ix) + p.dt_bias[h];
-            g = expf(-expf(p.A_log[h]) * log1pf(expf(fminf(x, kSoftplusClamp))));
-            be = 1.f / (1.f + expf(-ldf((const TI*)p.b + ix)));
+            if (d.gates == 1) {  // given log_decay and beta
+                g = expf(ldf((const TI*)p.a + ix));
+                be = ldf((const TI*)p.b + ix);
+            } else {
+                const float x = ldf((const TI*)p.a + ix) + p.dt_bias[h];
+                g = expf(-expf(p.A_log[h]) * log1pf(expf(fminf(x, kSoftplusClamp))));
+                be = 1.f / (1.f + expf(-ldf((const TI*)p.b + ix)));
+            }
         }
         red[2] = g;
         red[3] = be;

@@ -19,6 +19,11 @@ struct Dims {
     int64_t NC;  // number of chunks, ceil(T / 64)
     int64_t Tp;  // NC * 64 (sequence padded with identity steps)
     int dtype;   // 0 = fp32, 1 = bf16
+    // gate inputs: 0 = (a, b, A_log, dt_bias), from which the kernels form
+    // l = -exp(A_log) softplus(min(a + dt_bias, 20)) and beta = sigmoid(b);
+    // 1 = the per-step log_decay l and beta themselves (in Ptrs::a, Ptrs::b;
+    // A_log, dt_bias unused), whose cotangents the backward returns in da, db
+    int gates = 0;
 };
 
 // TMA descriptors of the raw bf16 inputs v and dO (q and k reach the kernels as

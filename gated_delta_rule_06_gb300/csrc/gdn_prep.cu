@@ -35,10 +35,15 @@ __global__ void __launch_bounds__(256) prep_gates_kernel(Dims d, const TI* __res
         float l = 0.f, be = 0.f;
         if (t < d.T && (mask == nullptr || mask[bb * d.T + t] != 0)) {
             const int64_t ix = ((int64_t)bb * d.T + t) * d.Hv + h;
-            const float x = ldf(a + ix) + dt_bias[h];
-            const float xc = fminf(x, kSoftplusClamp);
-            l = -expf(A_log[h]) * log1pf(expf(xc));
-            be = 1.f / (1.f + expf(-ldf(b + ix)));
+            if (d.gates == 1) {  // given log_decay and beta
+                l = ldf(a + ix);
+                be = ldf(b + ix);
+            } else {
+                const float x = ldf(a + ix) + dt_bias[h];
+                const float xc = fminf(x, kSoftplusClamp);
+                l = -expf(A_log[h]) * log1pf(expf(xc));
+                be = 1.f / (1.f + expf(-ldf(b + ix)));
+            }
         }
         lg[i][hh] = l;
         beta[((int64_t)bb * d.Hv + h) * d.Tp + t] = be;

@@ -70,6 +70,10 @@ def load_library(path: str = LIB_PATH):
         lib.gdn_forward.restype = i32
         lib.gdn_backward.argtypes = [shp] + [vp] * 9 + [sz] + [vp] * 10 + [vp, sz, vp]
         lib.gdn_backward.restype = i32
+        lib.gdn_forward_lb.argtypes = [shp] + [vp] * 9 + [vp, sz, vp, sz, vp]
+        lib.gdn_forward_lb.restype = i32
+        lib.gdn_backward_lb.argtypes = [shp] + [vp] * 7 + [sz] + [vp] * 8 + [vp, sz, vp]
+        lib.gdn_backward_lb.restype = i32
         _lib = lib
         return lib
 
@@ -264,3 +268,101 @@ class GatedDeltaRule(torch.autograd.Function):
 def gated_delta_rule(q, k, v, a, b, A_log, dt_bias, state0=None, mask=None):
     """Differentiable gated delta rule (the C-ABI forward + VJP)."""
     return GatedDeltaRule.apply(q, k, v, a, b, A_log, dt_bias, state0, mask)
+
+
+# ---- log_decay / beta gate form ----------------------------------------------
+
+def forward_lb(q, k, v, log_decay, beta, state0=None, mask=None, *, keep_saved=True, out=None):
+    """Run gdn_forward_lb: the gates given as log_decay = log g (finite, <= 0)
+    and beta, both [B, T, Hv] in the dtype of q.  Returns (o, state_T, saved)
+    as forward does."""
+    dt = q.dtype
+    for n, t in (("q", q), ("k", k), ("v", v), ("log_decay", log_decay), ("beta", beta)):
+        _cuda(t, n, dt)
+    _cuda(state0, "state0", torch.float32)
+    m = _mask_u8(mask)
+    shape = make_shape(q, v, m is not None)
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    out = out or {}
+    o = out.get("o")
+    if o is None:
+        o = torch.empty((B, T, Hv, Dv), dtype=dt, device=q.device)
+    sT = out.get("state_T")
+    if sT is None:
+        sT = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=q.device)
+    saved = None
+    ws = out.get("ws")
+    if keep_saved:
+        saved = out.get("saved")
+        if saved is None:
+            saved = _buf(saved_bytes(shape), q.device)
+        if ws is None:
+            ws = _buf(workspace_bytes(shape, 0), q.device)
+    elif ws is None and not (T == 1 and Dk * Dv <= 32768 and Dv % 4 == 0):
+        ws = _buf(workspace_bytes(shape, 2), q.device)
+    rc = load_library().gdn_forward_lb(
+        ctypes.byref(shape), _p(q), _p(k), _p(v), _p(log_decay), _p(beta), _p(state0), _p(m),
+        _p(o), _p(sT), _p(saved), ctypes.c_size_t(saved.numel() if saved is not None else 0),
+        _p(ws), ctypes.c_size_t(ws.numel() if ws is not None else 0), _stream())
+    _check(rc)
+    return o, sT, saved
+
+
+def backward_lb(q, k, v, log_decay, beta, mask, saved, d_o, d_state_T=None, *, out=None):
+    """Run gdn_backward_lb.  Returns dict(dq, dk, dv, d_log_decay, d_beta, dstate0)."""
+    dt = q.dtype
+    _cuda(d_o, "d_o", dt)
+    _cuda(d_state_T, "d_state_T", torch.float32)
+    m = _mask_u8(mask)
+    shape = make_shape(q, v, m is not None)
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    out = dict(out or {})
+    dev = q.device
+    g = {n: out.get(n) for n in ("dq", "dk", "dv", "d_log_decay", "d_beta", "dstate0")}
+    for n, ref in (("dq", q), ("dk", k), ("dv", v), ("d_log_decay", log_decay), ("d_beta", beta)):
+        if g[n] is None:
+            g[n] = torch.empty_like(ref)
+    if g["dstate0"] is None:
+        g["dstate0"] = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=dev)
+    ws = out.get("ws")
+    if ws is None:
+        ws = _buf(workspace_bytes(shape, 1), dev)
+    rc = load_library().gdn_backward_lb(
+        ctypes.byref(shape), _p(q), _p(k), _p(v), _p(log_decay), _p(beta), _p(m), _p(saved),
+        ctypes.c_size_t(saved.numel()), _p(d_o), _p(d_state_T), _p(g["dq"]), _p(g["dk"]),
+        _p(g["dv"]), _p(g["d_log_decay"]), _p(g["d_beta"]), _p(g["dstate0"]), _p(ws),
+        ctypes.c_size_t(ws.numel()), _stream())
+    _check(rc)
+    return g
+
+
+class GatedDeltaRuleLB(torch.autograd.Function):
+    """Autograd wrapper of the log_decay / beta form: (o, final_state) =
+    gated_delta_rule_lb(q, k, v, log_decay, beta, state0, mask)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, log_decay, beta, state0, mask):
+        q, k, v, log_decay, beta = (t.contiguous() for t in (q, k, v, log_decay, beta))
+        o, sT, saved = forward_lb(q, k, v, log_decay, beta,
+                                  None if state0 is None else state0.contiguous(), mask)
+        ctx.save_for_backward(q, k, v, log_decay, beta, saved)
+        ctx.mask = mask
+        ctx.has_state0 = state0 is not None
+        return o, sT
+
+    @staticmethod
+    def backward(ctx, d_o, d_sT):
+        q, k, v, log_decay, beta, saved = ctx.saved_tensors
+        if d_o is None:
+            d_o = torch.zeros_like(v)
+        g = backward_lb(q, k, v, log_decay, beta, ctx.mask, saved, d_o.contiguous(),
+                        None if d_sT is None else d_sT.contiguous())
+        return (g["dq"], g["dk"], g["dv"], g["d_log_decay"], g["d_beta"],
+                g["dstate0"] if ctx.has_state0 else None, None)
+
+
+def gated_delta_rule_lb(q, k, v, log_decay, beta, state0=None, mask=None):
+    """Differentiable gated delta rule with the gates given as log_decay, beta."""
+    return GatedDeltaRuleLB.apply(q, k, v, log_decay, beta, state0, mask)

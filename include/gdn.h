@@ -109,6 +109,33 @@ gdn_status gdn_backward(const gdn_shape* shape, const void* q, const void* k, co
                         float* ddt_bias, float* dstate0, void* ws, size_t ws_bytes,
                         void* stream);
 
+/* ---- log_decay / beta gate form --------------------------------------------- */
+
+/* The op contract's other gate input (torch-to-nnef "custom_extractors/gdn",
+ * op contract: log_decay and beta [b, S, hv]): the per-step log-decay
+ * l_t = log g_t and beta_t are given directly instead of (a, b, A_log,
+ * dt_bias); the recurrence is the one above with g_t = exp(l_t).
+ *   - log_decay, beta, d_log_decay, d_beta: [B, T, Hv] in the shape's dtype.
+ *   - log_decay must be finite and <= 0 (g in (0, 1], a decay), and beta
+ *     finite; the chunked kernels rely on the cumulative log-decay not
+ *     increasing within a chunk.  Values are not checked (they live on the
+ *     device): outside that range results are unspecified.
+ *   - Sizing, `saved`, `ws`, masking, decode (T == 1, saved == NULL) and every
+ *     other convention are those of gdn_forward / gdn_backward, and a saved
+ *     buffer from gdn_forward_lb is consumed by gdn_backward_lb.
+ *   - gdn_backward_lb writes d_log_decay and d_beta (zero on masked steps) in
+ *     place of da, db, dA_log and ddt_bias. */
+gdn_status gdn_forward_lb(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                          const void* log_decay, const void* beta, const float* state0,
+                          const uint8_t* mask, void* o, float* state_T, void* saved,
+                          size_t saved_bytes, void* ws, size_t ws_bytes, void* stream);
+gdn_status gdn_backward_lb(const gdn_shape* shape, const void* q, const void* k,
+                           const void* v, const void* log_decay, const void* beta,
+                           const uint8_t* mask, const void* saved, size_t saved_bytes,
+                           const void* d_o, const float* d_state_T, void* dq, void* dk,
+                           void* dv, void* d_log_decay, void* d_beta, float* dstate0,
+                           void* ws, size_t ws_bytes, void* stream);
+
 /* ---- forward without any allocation -------------------------------------- */
 
 /* Inference forward (no saved buffer) that allocates nothing and takes no
