@@ -233,10 +233,22 @@ def max_over_ranks(x, world):
 # CPU oracle sample (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(w, key_heads):
+def make_inputs(w, gates="ab"):
+    """The workload's seeded inputs; with gates == "lb" the gates are the
+    per-step log_decay and beta (torch-to-nnef page, op contract) instead of
+    a, b, A_log, dt_bias."""
+    x = wl.make_inputs(w)
+    if gates == "lb":
+        x.update(wl.make_lb_gates(w))
+        for n in ("a", "b", "A_log", "dt_bias"):
+            x.pop(n)
+    return x
+
+
+def oracle_sample(w, key_heads, gates="ab"):
     """Inputs of `w` restricted to the first `key_heads` key-head groups.
     Returns (inputs, fraction of the workload's (b, h) units)."""
-    x = wl.make_inputs(w)
+    x = make_inputs(w, gates)
     G = w.G
     nh = key_heads * G
     sub = {}
@@ -245,7 +257,7 @@ def oracle_sample(w, key_heads):
             sub[n] = None
         elif n in ("q", "k"):
             sub[n] = t[:, :, :key_heads]
-        elif n in ("v", "d_o", "a", "b"):
+        elif n in ("v", "d_o", "a", "b", "log_decay", "beta"):
             sub[n] = t[:, :, :nh]
         elif n in ("A_log", "dt_bias"):
             sub[n] = t[:nh]
@@ -259,11 +271,17 @@ def oracle_sample(w, key_heads):
 def run_oracle_step(sub, backward):
     import oracle
 
-    args = [sub[n] for n in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "state0", "mask")]
     t0 = time.perf_counter()
-    oracle.forward(*args)
-    if backward:
-        oracle.backward(*args, sub["d_o"], sub["d_state_T"])
+    if "log_decay" in sub:
+        args = [sub[n] for n in ("q", "k", "v", "log_decay", "beta", "state0", "mask")]
+        oracle.forward_lb(*args)
+        if backward:
+            oracle.backward_lb(*args, sub["d_o"], sub["d_state_T"])
+    else:
+        args = [sub[n] for n in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "state0", "mask")]
+        oracle.forward(*args)
+        if backward:
+            oracle.backward(*args, sub["d_o"], sub["d_state_T"])
     return time.perf_counter() - t0
 
 
@@ -272,11 +290,11 @@ def sample_key_heads(w):
     return max(1, w.Hk // 4)
 
 
-def cpu_baseline(w, backward, reps=1):
+def cpu_baseline(w, backward, reps=1, gates="ab"):
     import oracle
 
     kh = sample_key_heads(w)
-    sub, frac = oracle_sample(w, kh)
+    sub, frac = oracle_sample(w, kh, gates)
     times = [run_oracle_step(sub, backward) for _ in range(reps)]
     t = statistics.median(times)
     tokens = w.B * w.T
@@ -295,7 +313,7 @@ def run_reference(args, w, world, rank):
     oracle.build()
     backward = w.backward
     kh = sample_key_heads(w)
-    sub, frac = oracle_sample(w, kh)
+    sub, frac = oracle_sample(w, kh, args.gates)
     for _ in range(args.warmup):
         run_oracle_step(sub, backward)
     times = [run_oracle_step(sub, backward) for _ in range(args.steps)]
@@ -307,7 +325,7 @@ def run_reference(args, w, world, rank):
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t * 1e3 / frac, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w),
+        "config": config_of(w, args.gates),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(),
                          "kind": "oracle",
                          "sample": f"{kh} of {w.Hk} key-head groups per step, all "
@@ -318,10 +336,12 @@ def run_reference(args, w, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def config_of(w):
+def config_of(w, gates="ab"):
     return {"workload": w.name, "B": w.B, "T": w.T, "Hk": w.Hk, "Hv": w.Hv, "Dk": w.Dk,
             "Dv": w.Dv, "chunk": C, "state": "fp32",
             "pass": "fwd+bwd" if w.backward else "fwd (decode step)",
+            "gates": ("log_decay, beta (gdn_forward_lb / gdn_backward_lb)" if gates == "lb"
+                      else "a, b, A_log, dt_bias"),
             "l2": "flushed between timed steps (256 MiB write outside the events)"}
 
 
@@ -342,7 +362,8 @@ def run_ours(args, w, world, rank, local):
                     ("total_ms", ctypes.c_double)]
 
     dev = torch.device("cuda", local)
-    x = wl.make_inputs(w)
+    lb = args.gates == "lb"
+    x = make_inputs(w, args.gates)
     xd = {k: (None if v is None else v.to(dev)) for k, v in x.items()}
     backward = w.backward
     B, T, Hk, Hv, Dk, Dv = w.B, w.T, w.Hk, w.Hv, w.Dk, w.Dv
@@ -354,29 +375,42 @@ def run_ours(args, w, world, rank, local):
         fo["saved"] = torch.empty(ops.saved_bytes(shape), dtype=torch.uint8, device=dev)
         fo["ws"] = torch.empty(ops.workspace_bytes(shape, 0), dtype=torch.uint8, device=dev)
         bo = {"ws": torch.empty(ops.workspace_bytes(shape, 1), dtype=torch.uint8, device=dev)}
-        for n, ref in (("dq", xd["q"]), ("dk", xd["k"]), ("dv", xd["v"]), ("da", xd["a"]),
-                       ("db", xd["b"])):
+        gate_grads = ((("d_log_decay", xd["log_decay"]), ("d_beta", xd["beta"])) if lb else
+                      (("da", xd["a"]), ("db", xd["b"])))
+        for n, ref in (("dq", xd["q"]), ("dk", xd["k"]), ("dv", xd["v"])) + gate_grads:
             bo[n] = torch.empty_like(ref)
-        bo["dA_log"] = torch.empty((Hv,), dtype=torch.float32, device=dev)
-        bo["ddt_bias"] = torch.empty((Hv,), dtype=torch.float32, device=dev)
+        if not lb:
+            bo["dA_log"] = torch.empty((Hv,), dtype=torch.float32, device=dev)
+            bo["ddt_bias"] = torch.empty((Hv,), dtype=torch.float32, device=dev)
         bo["dstate0"] = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=dev)
 
+    def fwd_call(inp, keep_saved):
+        if lb:
+            ops.forward_lb(inp["q"], inp["k"], inp["v"], inp["log_decay"], inp["beta"],
+                           inp["state0"], inp["mask"], keep_saved=keep_saved, out=fo)
+        else:
+            ops.forward(inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], inp["A_log"],
+                        inp["dt_bias"], inp["state0"], inp["mask"], keep_saved=keep_saved,
+                        out=fo)
+
     def step_fwd(inp):
-        ops.forward(inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], inp["A_log"],
-                    inp["dt_bias"], inp["state0"], inp["mask"], out=fo)
+        fwd_call(inp, True)
 
     def step_bwd(inp):
-        ops.backward(inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], inp["A_log"],
-                     inp["dt_bias"], inp["mask"], fo["saved"], inp["d_o"], inp["d_state_T"],
-                     out=bo)
+        if lb:
+            ops.backward_lb(inp["q"], inp["k"], inp["v"], inp["log_decay"], inp["beta"],
+                            inp["mask"], fo["saved"], inp["d_o"], inp["d_state_T"], out=bo)
+        else:
+            ops.backward(inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], inp["A_log"],
+                         inp["dt_bias"], inp["mask"], fo["saved"], inp["d_o"],
+                         inp["d_state_T"], out=bo)
 
     def step(inp):
         if backward:
             step_fwd(inp)
             step_bwd(inp)
         else:
-            ops.forward(inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], inp["A_log"],
-                        inp["dt_bias"], inp["state0"], inp["mask"], keep_saved=False, out=fo)
+            fwd_call(inp, False)
     step.parts = (step_fwd, step_bwd)
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -466,7 +500,7 @@ def run_ours(args, w, world, rank, local):
         "vs_baseline": (value / PAGE_TOKENS_PER_S[w.name]) if w.name in PAGE_TOKENS_PER_S else None,
         "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded, shapes and distributions of the workload)",
-        "config": config_of(w),
+        "config": config_of(w, args.gates),
         "clocks": clocks,
         "gpu_launches": launches,
         "roofline": roof,
@@ -480,7 +514,7 @@ def run_ours(args, w, world, rank, local):
         import oracle
 
         oracle.build()
-        line["cpu_baseline"] = cpu_baseline(w, backward)
+        line["cpu_baseline"] = cpu_baseline(w, backward, gates=args.gates)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -507,17 +541,19 @@ def measured_traffic(workload, kernel):
 
 def run_e2e(args, w, x, xd, fo, bo, step, world):
     dev = xd["q"].device
-    names_in = [n for n in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "state0", "mask",
-                            "d_o", "d_state_T") if x[n] is not None]
+    names_in = [n for n in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "log_decay", "beta",
+                            "state0", "mask", "d_o", "d_state_T") if x.get(n) is not None]
     if not w.backward:
         names_in = [n for n in names_in if n not in ("d_o", "d_state_T")]
     host = {n: x[n].contiguous().pin_memory() for n in names_in}
     dev_in = {n: torch.empty_like(xd[n]) for n in names_in}
-    for n in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "state0", "mask", "d_o", "d_state_T"):
+    for n in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "log_decay", "beta", "state0",
+              "mask", "d_o", "d_state_T"):
         dev_in.setdefault(n, None)
     outs = [fo["o"], fo["state_T"]]
     if bo is not None:
-        outs += [bo[n] for n in ("dq", "dk", "dv", "da", "db", "dA_log", "ddt_bias", "dstate0")]
+        outs += [bo[n] for n in ("dq", "dk", "dv", "da", "db", "d_log_decay", "d_beta", "dA_log",
+                                 "ddt_bias", "dstate0") if n in bo]
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in outs)
@@ -591,6 +627,9 @@ def main():
                     choices=[n for n in wl.WORKLOAD_ORDER])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gates", choices=["ab", "lb"], default="ab",
+                    help="gate inputs: a, b, A_log, dt_bias (default) or the per-step "
+                         "log_decay and beta")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

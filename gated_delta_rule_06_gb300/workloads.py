@@ -17,6 +17,12 @@ the workload, not drawn):
 * d_o ~ N(0, 1) in the input dtype; d_state_T ~ N(0, 1) fp32 for the fp32
   workloads, absent (zero) for the bf16 ones.
 
+The log_decay / beta gate form (torch-to-nnef page, op contract) draws its
+gates with ``make_lb_gates``: log_decay = -exp(u), u ~ U(ln 0.01, ln 4) (a
+decay g between 0.018 and 0.99), value head 0 at -50 (a near-reset every
+step), beta ~ U(0, 1), both in the input dtype, from a generator seeded
+separately (seed + 7919).
+
 Workload shapes follow the mlx-lm page's toy gradient-check shape and its
 Qwen3.5-9B GatedDeltaNet performance shape, and the torch-to-nnef page's
 square-width GQA layout.
@@ -140,3 +146,16 @@ def make_inputs(w: Workload, seed: Optional[int] = None) -> dict:
     else:
         raise ValueError(w.mask)
     return x
+
+
+def make_lb_gates(w: Workload, seed: Optional[int] = None) -> dict:
+    """Draw log_decay and beta ([B, T, Hv], input dtype) for the log_decay /
+    beta gate form; the recipe is in the module docstring."""
+    gen = torch.Generator().manual_seed((w.seed if seed is None else seed) + 7919)
+    shape = (w.B, w.T, w.Hv)
+    u = torch.rand(shape, generator=gen, dtype=torch.float64)
+    lo, hi = math.log(0.01), math.log(4.0)
+    ld = -torch.exp(lo + u * (hi - lo))
+    ld[:, :, 0] = -50.0
+    beta = torch.rand(shape, generator=gen, dtype=torch.float64)
+    return {"log_decay": ld.to(w.dtype), "beta": beta.to(w.dtype)}

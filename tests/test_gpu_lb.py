@@ -4,9 +4,9 @@ against the fp64 oracle's forward_lb / backward_lb, element by element.
 
 Tolerances are those of the a / b form: per tensor max|x - y| / max|y|, 1e-4
 for fp32 inputs and 2e-2 for bf16 inputs.  q, k, v, the state, the
-cotangents and the mask come from the shared seeded generator; log_decay and
-beta are drawn here: log_decay = -exp(u), u ~ U(ln 0.01, ln 4) (g between
-0.018 and 0.99), value head 0 at -50 (a near-reset every step), beta ~ U(0, 1).
+cotangents, the mask and the gates (``make_lb_gates``: log_decay = -exp(u),
+u ~ U(ln 0.01, ln 4), value head 0 at -50, beta ~ U(0, 1)) come from the
+shared seeded generator.
 """
 
 import numpy as np
@@ -31,14 +31,7 @@ def _cuda():
 
 def _lb_inputs(w, seed):
     x = wl.make_inputs(w)
-    gen = torch.Generator().manual_seed(seed)
-    B, T, Hv = w.B, w.T, w.Hv
-    u = torch.rand((B, T, Hv), generator=gen, dtype=torch.float64)
-    ld = -torch.exp(np.log(0.01) + u * (np.log(4.0) - np.log(0.01)))
-    ld[:, :, 0] = -50.0
-    beta = torch.rand((B, T, Hv), generator=gen, dtype=torch.float64)
-    x["log_decay"] = ld.to(w.dtype)
-    x["beta"] = beta.to(w.dtype)
+    x.update(wl.make_lb_gates(w, seed))
     for n in ("a", "b", "A_log", "dt_bias"):
         x.pop(n)
     return x
@@ -148,32 +141,3 @@ def test_lb_autograd_function():
                      ("beta", "d_beta"), ("state0", "dstate0")):
         check(gname, leaves[n].grad, gr[gname], 1e-4)
 
-
-def test_lb_agrees_with_gate_form_on_the_same_gates():
-    """The same recurrence through both entry points: log_decay and beta formed
-    (in fp64 on the host) from a, b, A_log, dt_bias.  The outputs agree to
-    within the fp32 rounding of the gates, and the gate-form cotangents are
-    the log_decay / beta ones through the chain rule."""
-    ops = _ops()
-    w = wl.custom("lbeq", 1, 130, 2, 4, 32, 32, seed=111)
-    x = wl.make_inputs(w)
-    xd = to_dev(x)
-    xc = x["a"].double() + x["dt_bias"].double()
-    ld = -torch.exp(x["A_log"].double()) * torch.log1p(torch.exp(torch.clamp(xc, max=20.0)))
-    be = torch.sigmoid(x["b"].double())
-    ldd, bed = ld.float().cuda(), be.float().cuda()
-    o1, s1, sv1 = ops.forward(xd["q"], xd["k"], xd["v"], xd["a"], xd["b"], xd["A_log"],
-                              xd["dt_bias"], xd["state0"], None)
-    o2, s2, sv2 = ops.forward_lb(xd["q"], xd["k"], xd["v"], ldd, bed, xd["state0"], None)
-    check("o", o2, np64(o1), 1e-5)
-    check("state_T", s2, np64(s1), 1e-5)
-    g1 = ops.backward(xd["q"], xd["k"], xd["v"], xd["a"], xd["b"], xd["A_log"], xd["dt_bias"],
-                      None, sv1, xd["d_o"], xd["d_state_T"])
-    g2 = ops.backward_lb(xd["q"], xd["k"], xd["v"], ldd, bed, None, sv2, xd["d_o"],
-                         xd["d_state_T"])
-    for n in ("dq", "dk", "dv", "dstate0"):
-        check(n, g2[n], np64(g1[n]), 1e-5)
-    sig = torch.sigmoid(xc) * (xc <= 20.0)
-    da = np64(g2["d_log_decay"]) * (-np.exp(np64(x["A_log"])))[None, None, :] * sig.numpy()
-    check("da", g1["da"], da, 1e-5)
-    check("db", g1["db"], np64(g2["d_beta"]) * (be * (1 - be)).numpy(), 1e-5)
