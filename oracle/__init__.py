@@ -73,6 +73,8 @@ def _load():
         lib.gdn_oracle_forward_lb.restype = ctypes.c_int
         lib.gdn_oracle_backward_lb.argtypes = [i64] * 6 + [dp] * 15
         lib.gdn_oracle_backward_lb.restype = ctypes.c_int
+        lib.gdn_oracle_causal_conv1d_update.argtypes = [i64] * 4 + [dp] * 5
+        lib.gdn_oracle_causal_conv1d_update.restype = ctypes.c_int
         lib.gdn_oracle_threads.argtypes = []
         lib.gdn_oracle_threads.restype = ctypes.c_int
         _lib = lib
@@ -202,3 +204,19 @@ def backward_lb(q, k, v, log_decay, beta, state0, mask, d_o, d_state_T=None):
 
 
 GRAD_NAMES_LB = ("dq", "dk", "dv", "d_log_decay", "d_beta", "dstate0")
+
+
+def causal_conv1d_update(hidden, conv_state, weight):
+    """Depthwise causal conv1d + SiLU with a K-sample carry state (torch-to-nnef
+    page, CausalConvUpdateReified).  hidden [B, C, S], conv_state [B, C, K],
+    weight [C, K].  Returns (out [B, C, S], final_state [B, C, K])."""
+    hidden, conv_state, weight = map(_f64, (hidden, conv_state, weight))
+    B, C, S = hidden.shape
+    K = weight.shape[1]
+    out = np.zeros((B, C, S))
+    fs = np.zeros((B, C, K))
+    rc = _load().gdn_oracle_causal_conv1d_update(B, C, S, K, *map(_ptr, (
+        hidden, conv_state, weight, out, fs)))
+    if rc:
+        raise ValueError(f"oracle causal_conv1d_update rejected the shapes (code {rc})")
+    return out, fs

@@ -37,6 +37,14 @@
  *    sequential recurrence above, derived by hand, with the state stored
  *    every 64 steps and recomputed inside each 64-step segment (mlx-lm page,
  *    "Design notes": CHUNK_SIZE = 64 bounds memory to one chunk).
+ *  - Causal conv1d update (torch-to-nnef page, CausalConvUpdateReified: a
+ *    depthwise causal conv1d + SiLU with a k-sample carry state; hidden
+ *    [b, C, S], conv_state [b, C, k], weight [C, k] -> out [b, C, S],
+ *    final_state [b, C, k]).  Reading: per channel the k carried samples and
+ *    the S new ones form one sequence x; out_t = SiLU(sum_i w_i x_{t+1+i}), the
+ *    correlation of the k taps with the window that ends at new sample t (the
+ *    oldest carried sample falls outside every window); final_state = the last
+ *    k samples of x; no bias.
  *  - Chunked form (torch-to-nnef page: the chunked rule computes the same
  *    recurrence with different blocking; mlx-lm page, "Scope and
  *    follow-ups": chunk-parallel rewrite through a lower-triangular solve):
@@ -579,6 +587,30 @@ int gdn_oracle_backward_lb(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t
     if (rc) return rc;
     return backward_core(&d, q, k, v, log_decay_, beta, state0, mask, d_o, d_state_T, dq, dk,
                          dv, d_log_decay, d_beta, dstate0);
+}
+
+/* ---- causal conv1d update ------------------------------------------------ */
+
+int gdn_oracle_causal_conv1d_update(int64_t B, int64_t C, int64_t S, int64_t K,
+                                    const double* hidden, const double* conv_state,
+                                    const double* weight, double* out, double* final_state) {
+    if (B < 1 || C < 1 || S < 0 || K < 1) return 1;
+    double* x = malloc(sizeof(double) * (size_t)(K + S));
+    if (!x) return 3;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t c = 0; c < C; ++c) {
+            const int64_t bc = b * C + c;
+            for (int64_t i = 0; i < K; ++i) x[i] = conv_state[bc * K + i];
+            for (int64_t t = 0; t < S; ++t) x[K + t] = hidden[bc * S + t];
+            for (int64_t t = 0; t < S; ++t) {
+                double acc = 0.0;
+                for (int64_t i = 0; i < K; ++i) acc += weight[c * K + i] * x[t + 1 + i];
+                out[bc * S + t] = acc / (1.0 + exp(-acc));
+            }
+            for (int64_t i = 0; i < K; ++i) final_state[bc * K + i] = x[S + i];
+        }
+    free(x);
+    return 0;
 }
 
 /* ---- threads the OpenMP runtime will use --------------------------------- */

@@ -433,3 +433,51 @@ def test_lb_matches_gate_form_and_chain_rule():
     if x["mask"] is not None:
         off = x["mask"] == 0
         assert np.all(g2["d_log_decay"][off] == 0) and np.all(g2["d_beta"][off] == 0)
+
+
+# -- the causal conv1d update (torch-to-nnef page, CausalConvUpdateReified) -----
+
+def _silu(x):
+    return x / (1.0 + np.exp(-x))
+
+
+@pytest.mark.parametrize("S,K", [(1, 4), (5, 4), (9, 3), (2, 1)])
+def test_conv1d_matches_numpy_correlation(S, K):
+    """out = SiLU of the valid correlation of the k taps with [state, hidden],
+    first window dropped (numpy's convolve with the taps reversed);
+    final_state = the last k samples."""
+    r = np.random.default_rng(100 + S * 10 + K)
+    B, C = 2, 5
+    hid = r.standard_normal((B, C, S))
+    st = r.standard_normal((B, C, K))
+    w = r.standard_normal((C, K))
+    out, fs = oracle.causal_conv1d_update(hid, st, w)
+    for b in range(B):
+        for c in range(C):
+            x = np.concatenate([st[b, c], hid[b, c]])
+            corr = np.convolve(x, w[c][::-1], mode="valid")  # length S + 1
+            np.testing.assert_allclose(out[b, c], _silu(corr[1:]), rtol=1e-14, atol=1e-14)
+            np.testing.assert_array_equal(fs[b, c], x[-K:])
+
+
+def test_conv1d_delta_taps_and_split_carry():
+    """A tap on the newest sample gives out_t = SiLU(x_t); a tap on the oldest
+    in the window gives SiLU(x_{t-k+1}) (a k-1 step delay through the state);
+    running S1 + S2 samples at once equals two calls with the state carried."""
+    r = np.random.default_rng(7)
+    B, C, K = 1, 3, 4
+    hid = r.standard_normal((B, C, 10))
+    st = r.standard_normal((B, C, K))
+    last = np.zeros((C, K)); last[:, -1] = 1.0
+    out, _ = oracle.causal_conv1d_update(hid, st, last)
+    np.testing.assert_allclose(out, _silu(hid), rtol=1e-15, atol=0)
+    first = np.zeros((C, K)); first[:, 0] = 1.0
+    out, _ = oracle.causal_conv1d_update(hid, st, first)
+    delayed = np.concatenate([st[:, :, 1:], hid], axis=-1)[:, :, :10]
+    np.testing.assert_allclose(out, _silu(delayed), rtol=1e-15, atol=0)
+    w = r.standard_normal((C, K))
+    o_all, f_all = oracle.causal_conv1d_update(hid, st, w)
+    o1, f1 = oracle.causal_conv1d_update(hid[:, :, :6], st, w)
+    o2, f2 = oracle.causal_conv1d_update(hid[:, :, 6:], f1, w)
+    np.testing.assert_array_equal(np.concatenate([o1, o2], axis=-1), o_all)
+    np.testing.assert_array_equal(f2, f_all)
