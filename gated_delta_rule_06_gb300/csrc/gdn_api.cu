@@ -428,6 +428,24 @@ gdn_status gdn_backward_lb(const gdn_shape* shape, const void* q, const void* k,
                          nullptr, dstate0, ws, ws_bytes, stream);
 }
 
+gdn_status gdn_causal_conv1d_update(int64_t B, int64_t C, int64_t S, int64_t K, int32_t dtype,
+                                    const void* hidden, const void* conv_state,
+                                    const void* weight, void* out, void* final_state,
+                                    void* stream) {
+    if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16) return GDN_ERR_INVALID_ARG;
+    if (B < 1 || C < 1 || S < 1 || K < 1 || K > gdn::kConvMaxK) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (B * C > (int64_t(1) << 40) || B * C * S > (int64_t(1) << 46)) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (!hidden || !conv_state || !weight || !out || !final_state) return GDN_ERR_INVALID_ARG;
+    const void* ptrs[] = {hidden, conv_state, weight, out, final_state};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return GDN_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return cuda_status(run_phase("conv1d", s, [&] {
+        return gdn::launch_causal_conv1d_update(B, C, S, (int)K, dtype, hidden, conv_state, weight,
+                                                out, final_state, s);
+    }));
+}
+
 uint64_t gdn_launch_count(void) { return g_launches.load(); }
 
 gdn_status gdn_timing_begin(void) {

@@ -10,6 +10,7 @@
 namespace gdn {
 
 constexpr int kChunk = 64;           // chunk length (mlx-lm page, "Design notes")
+constexpr int kConvMaxK = 16;        // longest causal conv1d kernel supported
 constexpr float kNormEps = 1e-6f;    // L2-norm eps (torch-to-nnef page, op contract)
 constexpr float kSoftplusClamp = 20.f;
 
@@ -166,6 +167,11 @@ cudaError_t launch_bwd_chunk(const Dims& d, const Ptrs& p, cudaStream_t s);
 cudaError_t launch_bwd_reduce(const Dims& d, const Ptrs& p, cudaStream_t s);
 cudaError_t launch_decode(const Dims& d, const Ptrs& p, cudaStream_t s);
 bool decode_supported(int64_t Dk, int64_t Dv);
+// depthwise causal conv1d + SiLU with a K-sample carry state (K <= kConvMaxK)
+cudaError_t launch_causal_conv1d_update(int64_t B, int64_t C, int64_t S, int K, int dtype,
+                                        const void* hidden, const void* conv_state,
+                                        const void* weight, void* out, void* final_state,
+                                        cudaStream_t s);
 // streaming multiprocessors of the current device (cached per device)
 int sm_count();
 unsigned int read_clear_error_decode();

@@ -74,6 +74,8 @@ def load_library(path: str = LIB_PATH):
         lib.gdn_forward_lb.restype = i32
         lib.gdn_backward_lb.argtypes = [shp] + [vp] * 7 + [sz] + [vp] * 8 + [vp, sz, vp]
         lib.gdn_backward_lb.restype = i32
+        lib.gdn_causal_conv1d_update.argtypes = [ctypes.c_int64] * 4 + [i32] + [vp] * 6
+        lib.gdn_causal_conv1d_update.restype = i32
         _lib = lib
         return lib
 
@@ -366,3 +368,28 @@ class GatedDeltaRuleLB(torch.autograd.Function):
 def gated_delta_rule_lb(q, k, v, log_decay, beta, state0=None, mask=None):
     """Differentiable gated delta rule with the gates given as log_decay, beta."""
     return GatedDeltaRuleLB.apply(q, k, v, log_decay, beta, state0, mask)
+
+
+# ---- causal conv1d update ----------------------------------------------------
+
+def causal_conv1d_update(hidden, conv_state, weight, *, out=None, final_state=None):
+    """Depthwise causal conv1d + SiLU with a K-sample carry state
+    (gdn_causal_conv1d_update): hidden [B, C, S], conv_state [B, C, K], weight
+    [C, K], all of one dtype.  Returns (out [B, C, S], final_state [B, C, K]);
+    pass final_state=conv_state to update the state in place."""
+    dt = hidden.dtype
+    for n, t in (("hidden", hidden), ("conv_state", conv_state), ("weight", weight)):
+        _cuda(t, n, dt)
+    B, C, S = hidden.shape
+    K = weight.shape[1]
+    if tuple(conv_state.shape) != (B, C, K) or tuple(weight.shape) != (C, K):
+        raise GdnError("causal_conv1d_update: conv_state must be [B, C, K], weight [C, K]")
+    if out is None:
+        out = torch.empty_like(hidden)
+    if final_state is None:
+        final_state = torch.empty_like(conv_state)
+    rc = load_library().gdn_causal_conv1d_update(
+        B, C, S, K, 1 if dt == torch.bfloat16 else 0, _p(hidden), _p(conv_state), _p(weight),
+        _p(out), _p(final_state), _stream())
+    _check(rc)
+    return out, final_state

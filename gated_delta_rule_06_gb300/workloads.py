@@ -159,3 +159,14 @@ def make_lb_gates(w: Workload, seed: Optional[int] = None) -> dict:
     ld[:, :, 0] = -50.0
     beta = torch.rand(shape, generator=gen, dtype=torch.float64)
     return {"log_decay": ld.to(w.dtype), "beta": beta.to(w.dtype)}
+
+
+def make_conv_inputs(B: int, C: int, S: int, K: int, dtype: torch.dtype = torch.float32,
+                     seed: int = 0) -> dict:
+    """Inputs of the causal conv1d update: hidden [B, C, S] ~ N(0, 1), conv_state
+    [B, C, K] ~ N(0, 1), weight [C, K] ~ N(0, 1/K), in this draw order, in the
+    input dtype."""
+    gen = torch.Generator().manual_seed(seed)
+    return {"hidden": _normal(gen, (B, C, S), dtype),
+            "conv_state": _normal(gen, (B, C, K), dtype),
+            "weight": _normal(gen, (C, K), dtype, sigma=1.0 / math.sqrt(K))}

@@ -136,6 +136,26 @@ gdn_status gdn_backward_lb(const gdn_shape* shape, const void* q, const void* k,
                            void* dv, void* d_log_decay, void* d_beta, float* dstate0,
                            void* ws, size_t ws_bytes, void* stream);
 
+/* ---- causal conv1d update ------------------------------------------------- */
+
+/* Depthwise causal conv1d + SiLU with a K-sample carry state, the short
+ * convolution in front of the recurrence (torch-to-nnef "custom_extractors/gdn",
+ * CausalConvUpdateReified: hidden [b, C, S], conv_state [b, C, k], weight
+ * [C, k] -> out [b, C, S], final_state [b, C, k]).  Per (b, c), the K carried
+ * samples followed by the S new ones form one sequence x, and
+ *     out_t = SiLU(sum_{i<K} weight[c, i] x_{t+1+i}),   t = 0 .. S-1
+ *     final_state = the last K samples of x
+ * (no bias; the oldest carried sample lies outside every window).
+ *   - hidden, out [B, C, S]; conv_state, final_state [B, C, K]; weight [C, K];
+ *     all in `dtype` (gdn_dtype), fp32 arithmetic.  final_state may alias
+ *     conv_state (in-place update); out must not alias an input.
+ *   - B, C, S >= 1 and 1 <= K <= 16 (GDN_ERR_UNSUPPORTED_SHAPE otherwise);
+ *     pointers 16-byte aligned; device pointers; enqueued on `stream`. */
+gdn_status gdn_causal_conv1d_update(int64_t B, int64_t C, int64_t S, int64_t K, int32_t dtype,
+                                    const void* hidden, const void* conv_state,
+                                    const void* weight, void* out, void* final_state,
+                                    void* stream);
+
 /* ---- forward without any allocation -------------------------------------- */
 
 /* Inference forward (no saved buffer) that allocates nothing and takes no
