@@ -66,7 +66,7 @@ def _peaks():
 # algorithmic work model (per launch of each phase)
 # ---------------------------------------------------------------------------
 
-def work_model(w):
+def work_model(w, conv_k=0):
     """Per-phase algorithmic flops and bytes of one fwd+bwd step, in the storage
     formats the kernels use: bf16 inputs keep the saved intermediates as bf16
     operand images (checkpoints, T, W, P, Delta as hi + lo, state cotangents,
@@ -114,6 +114,13 @@ def work_model(w):
     m["decode"] = dict(flops=BH * (4 * Dk * Dv + 2 * Dk),
                        bytes=BH * 2 * Dk * Dv * 4 + BHk * 2 * Dk * es + BH * 2 * Dv * es
                        + BH * 2 * es)
+    if conv_k:
+        # fused short convolution: the mixed projection, the carried windows in and
+        # out and the taps replace the q / k / v reads
+        Cm = 2 * Hk * Dk + Hv * Dv
+        m["decode"]["flops"] += B * Cm * 2 * conv_k
+        m["decode"]["bytes"] += (B * Cm * (1 + 2 * conv_k) + Cm * conv_k) * es \
+            - (BHk * 2 * Dk + BH * Dv) * es
     # whole step: inputs and outputs once, plus the chunk checkpoints (in the
     # format stored) written once and read once
     io_fwd = (2 * B * T * Hk * Dk + B * T * Hv * Dv + 2 * B * T * Hv) * es \
@@ -245,8 +252,9 @@ def make_inputs(w, gates="ab"):
     return x
 
 
-def oracle_sample(w, key_heads, gates="ab"):
-    """Inputs of `w` restricted to the first `key_heads` key-head groups.
+def oracle_sample(w, key_heads, gates="ab", conv_k=0):
+    """Inputs of `w` restricted to the first `key_heads` key-head groups (with
+    conv_k, plus the whole mixed projection and its convolution inputs).
     Returns (inputs, fraction of the workload's (b, h) units)."""
     x = make_inputs(w, gates)
     G = w.G
@@ -265,6 +273,11 @@ def oracle_sample(w, key_heads, gates="ab"):
             sub[n] = t[:, :nh]
         else:
             sub[n] = t
+    if conv_k:
+        cvi = wl.make_conv_inputs(w.B, 2 * w.Hk * w.Dk + w.Hv * w.Dv, 1, conv_k, w.dtype,
+                                  w.seed + 1)
+        sub["hidden"], sub["conv_state"], sub["conv_weight"] = (cvi["hidden"], cvi["conv_state"],
+                                                               cvi["weight"])
     return sub, nh / w.Hv
 
 
@@ -272,6 +285,8 @@ def run_oracle_step(sub, backward):
     import oracle
 
     t0 = time.perf_counter()
+    if "hidden" in sub:  # the fused decode's convolution (all channels)
+        oracle.causal_conv1d_update(sub["hidden"], sub["conv_state"], sub["conv_weight"])
     if "log_decay" in sub:
         args = [sub[n] for n in ("q", "k", "v", "log_decay", "beta", "state0", "mask")]
         oracle.forward_lb(*args)
@@ -290,11 +305,11 @@ def sample_key_heads(w):
     return max(1, w.Hk // 4)
 
 
-def cpu_baseline(w, backward, reps=1, gates="ab"):
+def cpu_baseline(w, backward, reps=1, gates="ab", conv_k=0):
     import oracle
 
     kh = sample_key_heads(w)
-    sub, frac = oracle_sample(w, kh, gates)
+    sub, frac = oracle_sample(w, kh, gates, conv_k)
     times = [run_oracle_step(sub, backward) for _ in range(reps)]
     t = statistics.median(times)
     tokens = w.B * w.T
@@ -313,7 +328,7 @@ def run_reference(args, w, world, rank):
     oracle.build()
     backward = w.backward
     kh = sample_key_heads(w)
-    sub, frac = oracle_sample(w, kh, args.gates)
+    sub, frac = oracle_sample(w, kh, args.gates, args.fused_conv)
     for _ in range(args.warmup):
         run_oracle_step(sub, backward)
     times = [run_oracle_step(sub, backward) for _ in range(args.steps)]
@@ -325,7 +340,7 @@ def run_reference(args, w, world, rank):
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t * 1e3 / frac, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w, args.gates),
+        "config": config_of(w, args.gates, args.fused_conv),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(),
                          "kind": "oracle",
                          "sample": f"{kh} of {w.Hk} key-head groups per step, all "
@@ -336,10 +351,12 @@ def run_reference(args, w, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def config_of(w, gates="ab"):
+def config_of(w, gates="ab", conv_k=0):
     return {"workload": w.name, "B": w.B, "T": w.T, "Hk": w.Hk, "Hv": w.Hv, "Dk": w.Dk,
             "Dv": w.Dv, "chunk": C, "state": "fp32",
-            "pass": "fwd+bwd" if w.backward else "fwd (decode step)",
+            "pass": ("fwd+bwd" if w.backward else
+                     f"fwd (decode step, {conv_k}-tap short convolution fused in front)" if conv_k
+                     else "fwd (decode step)"),
             "gates": ("log_decay, beta (gdn_forward_lb / gdn_backward_lb)" if gates == "lb"
                       else "a, b, A_log, dt_bias"),
             "l2": "flushed between timed steps (256 MiB write outside the events)"}
@@ -364,13 +381,27 @@ def run_ours(args, w, world, rank, local):
     dev = torch.device("cuda", local)
     lb = args.gates == "lb"
     x = make_inputs(w, args.gates)
+    conv_k = args.fused_conv
+    if conv_k:  # the mixed projection and its convolution replace q, k, v
+        Cm = w.Hk * w.Dk * 2 + w.Hv * w.Dv
+        cvi = wl.make_conv_inputs(w.B, Cm, 1, conv_k, w.dtype, w.seed + 1)
+        x["hidden"] = cvi["hidden"][:, :, 0].contiguous()
+        x["conv_state"] = cvi["conv_state"]
+        x["conv_weight"] = cvi["weight"]
+        for n in ("q", "k", "v"):
+            x.pop(n)
+        for n in ("a", "b", "log_decay", "beta"):
+            if n in x:
+                x[n] = x[n][:, 0].contiguous()
     xd = {k: (None if v is None else v.to(dev)) for k, v in x.items()}
     backward = w.backward
     B, T, Hk, Hv, Dk, Dv = w.B, w.T, w.Hk, w.Hv, w.Dk, w.Dv
     # preallocated outputs / workspaces
-    shape = ops.make_shape(xd["q"], xd["v"], xd["mask"] is not None)
+    shape = None if conv_k else ops.make_shape(xd["q"], xd["v"], xd["mask"] is not None)
     fo = {"o": torch.empty((B, T, Hv, Dv), dtype=w.dtype, device=dev),
           "state_T": torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=dev)}
+    if conv_k:
+        fo["final_conv_state"] = torch.empty_like(xd["conv_state"])
     if backward:
         fo["saved"] = torch.empty(ops.saved_bytes(shape), dtype=torch.uint8, device=dev)
         fo["ws"] = torch.empty(ops.workspace_bytes(shape, 0), dtype=torch.uint8, device=dev)
@@ -385,7 +416,14 @@ def run_ours(args, w, world, rank, local):
         bo["dstate0"] = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=dev)
 
     def fwd_call(inp, keep_saved):
-        if lb:
+        if conv_k:
+            gates = ({"log_decay": inp["log_decay"], "beta": inp["beta"]} if lb else
+                     {"a": inp["a"], "b": inp["b"], "A_log": inp["A_log"],
+                      "dt_bias": inp["dt_bias"]})
+            ops.decode_conv(inp["hidden"], inp["conv_state"], inp["conv_weight"], inp["state0"],
+                            mask=inp["mask"], final_conv_state=fo["final_conv_state"],
+                            state_out=fo["state_T"], o=fo["o"], **gates)
+        elif lb:
             ops.forward_lb(inp["q"], inp["k"], inp["v"], inp["log_decay"], inp["beta"],
                            inp["state0"], inp["mask"], keep_saved=keep_saved, out=fo)
         else:
@@ -451,7 +489,7 @@ def run_ours(args, w, world, rank, local):
 
     # ---- per-phase roofline of the dominant kernel
     peaks = _peaks()
-    model = work_model(w)
+    model = work_model(w, args.fused_conv)
     ph = {phases[i].name.decode(): (phases[i].launches, phases[i].total_ms)
           for i in range(cnt.value)}
     dom = max(ph, key=lambda k: ph[k][1])
@@ -500,7 +538,7 @@ def run_ours(args, w, world, rank, local):
         "vs_baseline": (value / PAGE_TOKENS_PER_S[w.name]) if w.name in PAGE_TOKENS_PER_S else None,
         "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded, shapes and distributions of the workload)",
-        "config": config_of(w, args.gates),
+        "config": config_of(w, args.gates, args.fused_conv),
         "clocks": clocks,
         "gpu_launches": launches,
         "roofline": roof,
@@ -514,7 +552,8 @@ def run_ours(args, w, world, rank, local):
         import oracle
 
         oracle.build()
-        line["cpu_baseline"] = cpu_baseline(w, backward, gates=args.gates)
+        line["cpu_baseline"] = cpu_baseline(w, backward, gates=args.gates,
+                                            conv_k=args.fused_conv)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -540,17 +579,20 @@ def measured_traffic(workload, kernel):
 
 
 def run_e2e(args, w, x, xd, fo, bo, step, world):
-    dev = xd["q"].device
-    names_in = [n for n in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "log_decay", "beta",
-                            "state0", "mask", "d_o", "d_state_T") if x.get(n) is not None]
+    dev = fo["o"].device
+    names_in = [n for n in ("q", "k", "v", "hidden", "conv_state", "conv_weight", "a", "b",
+                            "A_log", "dt_bias", "log_decay", "beta", "state0", "mask", "d_o",
+                            "d_state_T") if x.get(n) is not None]
     if not w.backward:
         names_in = [n for n in names_in if n not in ("d_o", "d_state_T")]
     host = {n: x[n].contiguous().pin_memory() for n in names_in}
     dev_in = {n: torch.empty_like(xd[n]) for n in names_in}
-    for n in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "log_decay", "beta", "state0",
-              "mask", "d_o", "d_state_T"):
+    for n in ("q", "k", "v", "hidden", "conv_state", "conv_weight", "a", "b", "A_log",
+              "dt_bias", "log_decay", "beta", "state0", "mask", "d_o", "d_state_T"):
         dev_in.setdefault(n, None)
     outs = [fo["o"], fo["state_T"]]
+    if "final_conv_state" in fo:
+        outs.append(fo["final_conv_state"])
     if bo is not None:
         outs += [bo[n] for n in ("dq", "dk", "dv", "da", "db", "d_log_decay", "d_beta", "dA_log",
                                  "ddt_bias", "dstate0") if n in bo]
@@ -627,12 +669,17 @@ def main():
                     choices=[n for n in wl.WORKLOAD_ORDER])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused-conv", type=int, default=0, metavar="K",
+                    help="decode workloads: run the step with a K-tap short convolution "
+                         "fused in front (gdn_decode_conv); 0 = plain decode")
     ap.add_argument("--gates", choices=["ab", "lb"], default="ab",
                     help="gate inputs: a, b, A_log, dt_bias (default) or the per-step "
                          "log_decay and beta")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.fused_conv and (wl.WORKLOADS[args.workload].backward or not 1 <= args.fused_conv <= 16):
+        ap.error("--fused-conv K takes 1 <= K <= 16 and a decode workload")
     w = wl.WORKLOADS[args.workload]
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -446,6 +446,42 @@ gdn_status gdn_causal_conv1d_update(int64_t B, int64_t C, int64_t S, int64_t K, 
     }));
 }
 
+gdn_status gdn_decode_conv(const gdn_shape* shape, int32_t gates, int64_t K, const void* hidden,
+                           const void* conv_state, const void* conv_weight,
+                           void* final_conv_state, const void* a, const void* b,
+                           const float* A_log, const float* dt_bias, const float* state0,
+                           const uint8_t* mask, void* o, float* state_T, void* stream) {
+    gdn::Dims d;
+    gdn_status st = validate_shape(shape, &d);
+    if (st != GDN_OK) return st;
+    if (gates != 0 && gates != 1) return GDN_ERR_INVALID_ARG;
+    d.gates = gates;
+    if (d.T != 1 || K < 1 || K > gdn::kConvMaxK || !gdn::decode_supported(d.Dk, d.Dv))
+        return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (!hidden || !conv_state || !conv_weight || !final_conv_state || !a || !b || !o || !state_T)
+        return GDN_ERR_INVALID_ARG;
+    if (gates == 0 && (!A_log || !dt_bias)) return GDN_ERR_INVALID_ARG;
+    if (shape->has_mask && !mask) return GDN_ERR_INVALID_ARG;
+    const void* ptrs[] = {hidden, conv_state, conv_weight, final_conv_state, a, b, A_log,
+                          dt_bias, state0, mask, o, state_T};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return GDN_ERR_MISALIGNED;
+    const size_t es = d.dtype == GDN_DTYPE_BF16 ? 2 : 4;
+    const size_t cs_bytes = (size_t)d.B * (2 * d.Hk * d.Dk + d.Hv * d.Dv) * K * es;
+    const char* c0 = static_cast<const char*>(conv_state);
+    const char* f0 = static_cast<const char*>(final_conv_state);
+    if (f0 < c0 + cs_bytes && c0 < f0 + cs_bytes) return GDN_ERR_INVALID_ARG;  // overlap
+    gdn::Ptrs p{};
+    p.a = a; p.b = b; p.A_log = A_log; p.dt_bias = dt_bias; p.state0 = state0;
+    p.mask = shape->has_mask ? mask : nullptr;
+    p.o = o; p.state_T = state_T;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return cuda_status(run_phase("decode", s, [&] {
+        return gdn::launch_decode_conv(d, p, hidden, conv_state, conv_weight, final_conv_state,
+                                       (int)K, s);
+    }));
+}
+
 uint64_t gdn_launch_count(void) { return g_launches.load(); }
 
 gdn_status gdn_timing_begin(void) {

@@ -166,6 +166,11 @@ cudaError_t launch_bwd_scan(const Dims& d, const Ptrs& p, cudaStream_t s);
 cudaError_t launch_bwd_chunk(const Dims& d, const Ptrs& p, cudaStream_t s);
 cudaError_t launch_bwd_reduce(const Dims& d, const Ptrs& p, cudaStream_t s);
 cudaError_t launch_decode(const Dims& d, const Ptrs& p, cudaStream_t s);
+// the decode step with the short convolution fused in front (q, k, v come from
+// `hidden` [B, 2 Hk Dk + Hv Dv] through the K-tap convolution; p.q, p.k, p.v unused)
+cudaError_t launch_decode_conv(const Dims& d, const Ptrs& p, const void* hidden,
+                               const void* conv_state, const void* weight, void* final_state,
+                               int K, cudaStream_t s);
 bool decode_supported(int64_t Dk, int64_t Dv);
 // depthwise causal conv1d + SiLU with a K-sample carry state (K <= kConvMaxK)
 cudaError_t launch_causal_conv1d_update(int64_t B, int64_t C, int64_t S, int K, int dtype,

@@ -76,6 +76,8 @@ def load_library(path: str = LIB_PATH):
         lib.gdn_backward_lb.restype = i32
         lib.gdn_causal_conv1d_update.argtypes = [ctypes.c_int64] * 4 + [i32] + [vp] * 6
         lib.gdn_causal_conv1d_update.restype = i32
+        lib.gdn_decode_conv.argtypes = [shp, i32, ctypes.c_int64] + [vp] * 13
+        lib.gdn_decode_conv.restype = i32
         _lib = lib
         return lib
 
@@ -393,3 +395,56 @@ def causal_conv1d_update(hidden, conv_state, weight, *, out=None, final_state=No
         _p(out), _p(final_state), _stream())
     _check(rc)
     return out, final_state
+
+
+def decode_conv(hidden, conv_state, conv_weight, state, *, a=None, b=None, A_log=None,
+                dt_bias=None, log_decay=None, beta=None, mask=None, final_conv_state=None,
+                state_out=None, o=None):
+    """One T = 1 step with the short convolution fused in front (gdn_decode_conv).
+
+    hidden [B, C] or [B, C, 1] is the mixed projection q | k | v (C = 2 Hk Dk +
+    Hv Dv), conv_state [B, C, K], conv_weight [C, K], state [B, Hv, Dk, Dv]
+    (fp32 or None for zeros).  Gates: a, b, A_log, dt_bias, or log_decay, beta
+    ([B, Hv] or [B, 1, Hv]).  Returns (o [B, 1, Hv, Dv], state_T,
+    final_conv_state); state_out may be state (in place), final_conv_state
+    must be a separate buffer."""
+    dt = hidden.dtype
+    if hidden.dim() == 3:
+        hidden = hidden[:, :, 0]
+    hidden = hidden.contiguous()
+    for n, t in (("hidden", hidden), ("conv_state", conv_state), ("conv_weight", conv_weight)):
+        _cuda(t, n, dt)
+    lb = log_decay is not None
+    ga, gb = (log_decay, beta) if lb else (a, b)
+    if ga is None or gb is None:
+        raise GdnError("decode_conv: pass a, b, A_log, dt_bias or log_decay, beta")
+    _cuda(ga, "a / log_decay", dt)
+    _cuda(gb, "b / beta", dt)
+    if not lb:
+        _cuda(A_log, "A_log", torch.float32)
+        _cuda(dt_bias, "dt_bias", torch.float32)
+    _cuda(state, "state", torch.float32)
+    B, C = hidden.shape
+    K = conv_weight.shape[1]
+    Hv = ga.shape[-1]
+    if state is None and state_out is None:
+        raise GdnError("decode_conv: pass state or state_out to give Dk, Dv")
+    ref = state if state is not None else state_out
+    Dk, Dv = ref.shape[2], ref.shape[3]
+    if (C - Hv * Dv) % (2 * Dk) or C <= Hv * Dv:
+        raise GdnError("decode_conv: hidden width must be 2 Hk Dk + Hv Dv")
+    Hk = (C - Hv * Dv) // (2 * Dk)
+    m = _mask_u8(mask)
+    shape = GdnShape(B, 1, Hk, Hv, Dk, Dv, _DTYPES[dt], int(m is not None))
+    if o is None:
+        o = torch.empty((B, 1, Hv, Dv), dtype=dt, device=hidden.device)
+    if state_out is None:
+        state_out = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=hidden.device)
+    if final_conv_state is None:
+        final_conv_state = torch.empty_like(conv_state)
+    rc = load_library().gdn_decode_conv(
+        ctypes.byref(shape), 1 if lb else 0, K, _p(hidden), _p(conv_state), _p(conv_weight),
+        _p(final_conv_state), _p(ga), _p(gb), _p(A_log), _p(dt_bias), _p(state), _p(m), _p(o),
+        _p(state_out), _stream())
+    _check(rc)
+    return o, state_out, final_conv_state

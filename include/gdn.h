@@ -156,6 +156,33 @@ gdn_status gdn_causal_conv1d_update(int64_t B, int64_t C, int64_t S, int64_t K, 
                                     const void* weight, void* out, void* final_state,
                                     void* stream);
 
+/* ---- decode step with the convolution fused in front ----------------------- */
+
+/* One T = 1 step of the recurrence whose q, k, v come from the short
+ * convolution (gdn_causal_conv1d_update) of the layer's mixed projection, in
+ * one kernel (mlx-lm page, "Scope and follow-ups": a mega-fused T = 1 kernel;
+ * torch-to-nnef page: the conv update and the recurrence as the two ops of the
+ * decode path).
+ *   - hidden [B, C] (the S = 1 column of [B, C, 1]), C = 2 Hk Dk + Hv Dv,
+ *     holding q | k | v along C, each head-major (q channel j Dk + i, k channel
+ *     Hk Dk + j Dk + i, v channel 2 Hk Dk + h Dv + i); conv_state,
+ *     final_conv_state [B, C, K]; conv_weight [C, K]; all in shape->dtype.
+ *   - final_conv_state receives the shifted windows and must not overlap
+ *     conv_state (the G value heads of a key head read the same q / k channels).
+ *   - gates = 0: a, b [B, Hv] with A_log, dt_bias [Hv] as in gdn_forward;
+ *     gates = 1: a = log_decay, b = beta [B, Hv] as in gdn_forward_lb (A_log,
+ *     dt_bias ignored).
+ *   - state0 [B, Hv, Dk, Dv] (NULL = zeros), state_T may alias it; o
+ *     [B, 1, Hv, Dv].  A masked row (mask[b] == 0) keeps both its carried
+ *     conv state and its recurrent state; its o reads the unchanged state.
+ *   - Requires shape->T == 1, 1 <= K <= 16, Dv % 4 == 0 and the state of one
+ *     head within shared memory (Dk * Dv <= 32768 at Dv = 128). */
+gdn_status gdn_decode_conv(const gdn_shape* shape, int32_t gates, int64_t K, const void* hidden,
+                           const void* conv_state, const void* conv_weight,
+                           void* final_conv_state, const void* a, const void* b,
+                           const float* A_log, const float* dt_bias, const float* state0,
+                           const uint8_t* mask, void* o, float* state_T, void* stream);
+
 /* ---- forward without any allocation -------------------------------------- */
 
 /* Inference forward (no saved buffer) that allocates nothing and takes no
