@@ -307,9 +307,13 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             // accumulation chains interleaved
             ok = tc::mbar_wait(&barW, (uint32_t)(c & 1), &g_err_scanta) && ok;
             const uint32_t id = tc::idesc_bf16(DVT, C, false, false);
+            uint64_t dw = tW.desc(0), dq = tQ.desc(0);
+            const uint64_t iw = tW.desc_step(), iq = tQ.desc_step();
             for (int k = 0; k < Dk; k += 16) {
-                tc::mma_bf16_ta(tb + TC.dacc, tb + TC.aop + k / 2, tW.desc(k), id, k > 0);
-                tc::mma_bf16_ta(tb + ocol, tb + TC.aop + k / 2, tQ.desc(k), id, k > 0);
+                tc::mma_bf16_ta(tb + TC.dacc, tb + TC.aop + k / 2, dw, id, k > 0);
+                tc::mma_bf16_ta(tb + ocol, tb + TC.aop + k / 2, dq, id, k > 0);
+                dw += iw;
+                dq += iq;
             }
             tc::mma_commit(&bar);
             ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
@@ -374,11 +378,14 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             ok = tc::mbar_wait(&barK, (uint32_t)(c & 1), &g_err_scanta) && ok;
             const uint32_t idp = tc::idesc_bf16(DVT, C, false, false);
             const uint32_t idk = tc::idesc_bf16(DVT, Dk, false, true);
+            const uint64_t dp0 = tP.desc(0), ip = tP.desc_step();
+            const uint64_t dk0 = tKmn.desc(0), ik = tKmn.desc_step();
+#pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int k = (i & 3) * 16;
                 const uint32_t hl = (uint32_t)(i >> 2) * 32u;
-                tc::mma_bf16_ta(tb + ocol, tb + TC.aop + hl + k / 2, tP.desc(k), idp, 1u);
-                tc::mma_bf16_ta(tb, tb + TC.aop + 64 + hl + k / 2, tKmn.desc(k), idk, 1u);
+                tc::mma_bf16_ta(tb + ocol, tb + TC.aop + hl + k / 2, dp0 + (uint64_t)(i & 3) * ip, idp, 1u);
+                tc::mma_bf16_ta(tb, tb + TC.aop + 64 + hl + k / 2, dk0 + (uint64_t)(i & 3) * ik, idk, 1u);
             }
             tc::mma_commit(&bar);
             if (c + 1 < d.NC) load_u(c + 1);  // step 3 of chunk c has read U
@@ -674,12 +681,18 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             const uint32_t id64 = tc::idesc_bf16(DVT, C, true, true);
             const uint32_t id2 = tc::idesc_bf16(DVT, C, false, false);
             const uint32_t idq = tc::idesc_bf16(DVT, Dk, true, true);
+            uint64_t dK = tK.desc(0), dO = tOmn.desc(0), dP = tPmn.desc(0), dOs = tOsmn.desc(0),
+                     dQ = tQmn.desc(0), dOl = tOslomn.desc(0);
+            const uint64_t iK = tK.desc_step(), iO = tOmn.desc_step(), iP = tPmn.desc_step(),
+                           iOs = tOsmn.desc_step(), iQ = tQmn.desc_step(), iOl = tOslomn.desc_step();
             for (int k = 0; k < Dk; k += 16) {
-                tc::mma_bf16_ta(tb + kA2, tb + aop + k / 2, tK.desc(k), id2, k > 0);
+                tc::mma_bf16_ta(tb + kA2, tb + aop + k / 2, dK, id2, k > 0);
+                dK += iK;
                 if (k < C) {
-                    tc::mma_bf16(tb + kA1, tOmn.desc(k), tPmn.desc(k), id64, k > 0);
-                    tc::mma_bf16(tb, tOsmn.desc(k), tQmn.desc(k), idq, 1u);
-                    tc::mma_bf16(tb, tOslomn.desc(k), tQmn.desc(k), idq, 1u);
+                    tc::mma_bf16(tb + kA1, dO, dP, id64, k > 0);
+                    tc::mma_bf16(tb, dOs, dQ, idq, 1u);
+                    tc::mma_bf16(tb, dOl, dQ, idq, 1u);
+                    dO += iO; dP += iP; dOs += iOs; dQ += iQ; dOl += iOl;
                 }
             }
             tc::mma_commit(&bar);

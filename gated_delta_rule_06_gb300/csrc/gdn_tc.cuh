@@ -282,6 +282,13 @@ struct Tile {
         if (k_major) return sdesc(base + (k0 >> 3) * xs, xs, ys);
         return sdesc(base + (k0 >> 3) * ys, ys, xs);
     }
+    // desc(k0 + 16) - desc(k0): the next K slice moves only the start-address
+    // field (addresses below 256 KB never carry into the next field).  Issuing
+    // loops add it instead of rebuilding the descriptor, which keeps the single
+    // issuing thread from becoming the bottleneck of small MMAs.
+    __device__ __forceinline__ uint64_t desc_step() const {
+        return (uint64_t)((2u * (k_major ? xs : ys)) >> 4);
+    }
 };
 
 // "Panel" image of a bf16 operand with `rows` rows (y) and 8-column groups (x):
@@ -305,17 +312,25 @@ __device__ __forceinline__ Tile panel_tile(const void* smem, uint32_t rows, bool
 __device__ __forceinline__ void mma_tile(uint32_t d_tmem, const Tile& A, const Tile& B, int M,
                                          int N, int K, bool accumulate) {
     const uint32_t id = idesc_bf16(M, N, !A.k_major, !B.k_major);
-    for (int k = 0; k < K; k += 16)
-        mma_bf16(d_tmem, A.desc(k), B.desc(k), id, (accumulate || k > 0) ? 1u : 0u);
+    uint64_t da = A.desc(0), db = B.desc(0);
+    const uint64_t ia = A.desc_step(), ib = B.desc_step();
+    for (int k = 0; k < K; k += 16) {
+        mma_bf16(d_tmem, da, db, id, (accumulate || k > 0) ? 1u : 0u);
+        da += ia;
+        db += ib;
+    }
 }
 
 // issue D = A (M x K, in TMEM at column a_col) * B (K x N) (+ D) as K / 16 MMAs
 __device__ __forceinline__ void mma_tile_ta(uint32_t d_tmem, uint32_t a_tmem, const Tile& B, int M,
                                             int N, int K, bool accumulate) {
     const uint32_t id = idesc_bf16(M, N, false, !B.k_major);
-    for (int k = 0; k < K; k += 16)
-        mma_bf16_ta(d_tmem, a_tmem + (uint32_t)(k >> 1), B.desc(k), id,
-                    (accumulate || k > 0) ? 1u : 0u);
+    uint64_t db = B.desc(0);
+    const uint64_t ib = B.desc_step();
+    for (int k = 0; k < K; k += 16) {
+        mma_bf16_ta(d_tmem, a_tmem + (uint32_t)(k >> 1), db, id, (accumulate || k > 0) ? 1u : 0u);
+        db += ib;
+    }
 }
 // 32 lanes x 32 bits, 16 consecutive columns per thread, raw 32-bit words
 __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
