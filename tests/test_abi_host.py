@@ -99,3 +99,54 @@ def test_backward_rejects_before_launch(lib):
 def test_status_strings(lib):
     for c in range(6):
         assert lib.gdn_status_string(c).startswith(b"GDN_")
+
+
+def test_lb_entry_points_reject_before_launch(lib):
+    """gdn_forward_lb / gdn_backward_lb: the same host checks as the a / b form."""
+    s = _shape()
+    vp = ctypes.c_void_p
+    P = vp(0x1000)
+    big = ctypes.c_size_t(1 << 40)
+    fwd = [P, P, P, P, P, None, None, P, P, P, big, P, big, None]
+    assert lib.gdn_forward_lb(ctypes.byref(s), *fwd[:4], None, *fwd[5:]) == 1      # no beta
+    assert lib.gdn_forward_lb(ctypes.byref(s), *fwd[:3], vp(0x1004), *fwd[4:]) == 4  # misaligned
+    small = list(fwd)
+    small[12] = ctypes.c_size_t(16)
+    assert lib.gdn_forward_lb(ctypes.byref(s), *small) == 3                          # ws too small
+    assert lib.gdn_forward_lb(ctypes.byref(_shape(Dv=12)), *fwd) == 2               # shape
+    bwd = [P] * 5 + [None, P, big, P, None] + [P] * 6 + [P, ctypes.c_size_t(16), None]
+    assert lib.gdn_backward_lb(ctypes.byref(s), *bwd) == 3                           # ws too small
+    bwd2 = list(bwd)
+    bwd2[13] = None                                                                  # no d_log_decay
+    assert lib.gdn_backward_lb(ctypes.byref(s), *bwd2) == 1
+
+
+def test_conv1d_update_rejects_before_launch(lib):
+    vp = ctypes.c_void_p
+    P = vp(0x1000)
+    ok = (2, 64, 1, 4, 1)
+    assert lib.gdn_causal_conv1d_update(*ok[:3], 0, ok[4], P, P, P, P, P, None) == 2  # K = 0
+    assert lib.gdn_causal_conv1d_update(*ok[:3], 17, ok[4], P, P, P, P, P, None) == 2  # K > 16
+    assert lib.gdn_causal_conv1d_update(0, 64, 1, 4, 1, P, P, P, P, P, None) == 2     # B = 0
+    assert lib.gdn_causal_conv1d_update(*ok[:4], 9, P, P, P, P, P, None) == 1         # dtype
+    assert lib.gdn_causal_conv1d_update(*ok, P, None, P, P, P, None) == 1             # null state
+    assert lib.gdn_causal_conv1d_update(*ok, P, P, vp(0x1002), P, P, None) == 4       # misaligned
+
+
+def test_decode_conv_rejects_before_launch(lib):
+    vp = ctypes.c_void_p
+    s = _shape(T=1, Dk=64, Dv=64)
+    A, B_ = vp(0x100000), vp(0x200000)  # two separate conv-state buffers
+
+    def call(shape=s, gates=1, K=4, conv_state=A, final=B_, hidden=vp(0x1000)):
+        return lib.gdn_decode_conv(ctypes.byref(shape), gates, K, hidden, conv_state,
+                                   vp(0x3000), final, vp(0x4000), vp(0x5000), None, None, None,
+                                   None, vp(0x6000), vp(0x7000), None)
+
+    assert call(shape=_shape(T=2, Dk=64, Dv=64)) == 2   # decode takes T == 1
+    assert call(K=0) == 2 and call(K=17) == 2            # kernel length
+    assert call(gates=2) == 1                            # gate form
+    assert call(gates=0) == 1                            # a / b form needs A_log, dt_bias
+    assert call(final=A) == 1                            # final conv state overlaps the input
+    assert call(hidden=None) == 1
+    assert call(hidden=vp(0x1004)) == 4                  # misaligned
