@@ -6,14 +6,16 @@ page's performance table (B=1, T=2048, Hk=16, Hv=64, Dk=192, Dv=128, bf16
 inputs, fp32 state), forward + full backward per step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME]
+                  [--workload NAME] [--gates ab|lb] [--fused-conv K]
 
 One process per GPU (torchrun for N > 1); every rank runs its own replica
 of the workload (weak scaling, no collective on the data path).  Timing:
 W untimed warm-up steps, then K steps each bracketed by CUDA events on the
 launching stream; L2 is flushed (256 MiB write) between timed steps outside
 the events; barrier + synchronize around the timed region; the max over
-ranks is reported.  ``value`` = tokens of all ranks / time.
+ranks is reported.  ``value`` = tokens of all ranks / time.  The per-phase
+kernel times behind the roofline come from a second pass over the same K
+steps with the library's phase events (the timed steps carry none).
 
 ``--impl reference`` times the fp64 CPU oracle (the only reference
 implementation this method has here) on the host cores, on a bounded sample
@@ -359,7 +361,9 @@ def config_of(w, gates="ab", conv_k=0):
                      else "fwd (decode step)"),
             "gates": ("log_decay, beta (gdn_forward_lb / gdn_backward_lb)" if gates == "lb"
                       else "a, b, A_log, dt_bias"),
-            "l2": "flushed between timed steps (256 MiB write outside the events)"}
+            "l2": "flushed between timed steps (256 MiB write outside the events)",
+            "phase_times": "a second pass over the same steps with per-phase CUDA events "
+                           "(the timed steps carry none)"}
 
 
 # ---------------------------------------------------------------------------
@@ -457,7 +461,10 @@ def run_ours(args, w, world, rank, local):
         step(xd)
     torch.cuda.synchronize()
 
-    # ---- timed region (device time, CUDA events on the launching stream)
+    # ---- timed region (device time, CUDA events on the launching stream).  The
+    # step time carries no per-phase events: recording them between the kernels
+    # costs 10 - 30 us a step.  The per-phase times come from a second pass over
+    # the same K steps (L2 flushed the same way) with the library's phase events.
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     sampler = ClockSampler(local)
@@ -466,7 +473,6 @@ def run_ours(args, w, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     n0 = lib.gdn_launch_count()
-    lib.gdn_timing_begin()
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
@@ -476,6 +482,13 @@ def run_ours(args, w, world, rank, local):
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     launches = int(lib.gdn_launch_count() - n0)
+    barrier(world)
+    # phase pass
+    lib.gdn_timing_begin()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        step(xd)
+    torch.cuda.synchronize()
     phases = (PhaseTime * 16)()
     cnt = ctypes.c_int(0)
     lib.gdn_timing_end(phases, 16, ctypes.byref(cnt))
