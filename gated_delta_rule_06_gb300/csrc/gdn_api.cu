@@ -389,6 +389,10 @@ gdn_status backward_impl(const gdn_shape* shape, int gates, const void* q, const
 }
 }  // namespace
 
+gdn_status gdn_checkpoint_bytes(const gdn_shape* shape, size_t* bytes) {
+    return gdn_saved_bytes(shape, bytes);
+}
+
 gdn_status gdn_forward(const gdn_shape* shape, const void* q, const void* k, const void* v,
                        const void* a, const void* b, const float* A_log, const float* dt_bias,
                        const float* state0, const uint8_t* mask, void* o, float* state_T,

@@ -84,6 +84,13 @@ gdn_status gdn_workspace_bytes(const gdn_shape* shape, int pass, size_t* bytes);
  * chunk-parallel form through a lower-triangular solve).  Host-only. */
 gdn_status gdn_saved_bytes(const gdn_shape* shape, size_t* bytes);
 
+/* The same number under the name the checkpoint sizing call also goes by: the
+ * saved buffer is where the forward keeps the chunk-start states (the
+ * checkpoints) together with the per-chunk intermediates the backward reads.
+ * On the tensor-core path the checkpoints are stored as bf16 operand images,
+ * so the buffer is not B*Hv*NC*Dk*Dv*4 bytes of fp32 states. */
+gdn_status gdn_checkpoint_bytes(const gdn_shape* shape, size_t* bytes);
+
 /* Forward pass.  state0 may be NULL (zero initial state); mask may be NULL
  * (every step applied).  state_T may alias state0 (in-place update).
  * saved may be NULL for inference (nothing kept for the backward); then,
