@@ -101,56 +101,65 @@ __global__ void __launch_bounds__(256) prep_norms_kernel(Dims d, const TI* __res
     }
 }
 
-// Tensor-core path: the same norms from 16-byte row pieces, and the raw bf16
-// rows copied into the per-chunk panel images (piece g of row t of chunk c at
-// byte g * 1024 + (t % 64) * 16 of image (b, j, c); rows past T are zero).
+// Tensor-core path: the same norms, and the raw bf16 rows copied into the
+// per-chunk panel images (piece g of row t of chunk c at byte g * 1024 +
+// (t % 64) * 16 of image (b, j, c); rows past T are zero).  One CTA per (chunk,
+// key head, batch): the chunk's q and k rows load with row-contiguous 16-byte
+// reads into shared memory in the images' panel order, each 64-row panel padded
+// by 16 bytes so that the staging writes and the reads below are conflict-free;
+// the norms come from shared memory; each image leaves with contiguous stores.
+constexpr int kPanelPad = kChunk * 16 + 16;  // bytes per staged 64-row panel
+
 __global__ void __launch_bounds__(256) prep_norms_img_kernel(Dims d, const __nv_bfloat16* __restrict__ q,
                                                              const __nv_bfloat16* __restrict__ k,
                                                              float* __restrict__ rq,
                                                              float* __restrict__ rk,
                                                              uint8_t* __restrict__ qimg,
                                                              uint8_t* __restrict__ kimg) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;  // over (b, t, j)
-    const int64_t nrows = d.B * d.Tp * d.Hk;
-    if (row >= nrows) return;
-    const int64_t j = row % d.Hk;
-    const int64_t t = (row / d.Hk) % d.Tp;
-    const int64_t bb = row / (d.Hk * d.Tp);
-    const int ng = (int)(d.Dk / 8);  // 16-byte pieces per row (<= 32)
-    const bool in = t < d.T;
-    uint4 uq = make_uint4(0u, 0u, 0u, 0u), uk = uq;
-    float sq = 0.f, sk = 0.f;
-    if (lane < ng && in) {
-        const int64_t base = ((bb * d.T + t) * d.Hk + j) * d.Dk + 8 * lane;
-        uq = *reinterpret_cast<const uint4*>(q + base);
-        uk = *reinterpret_cast<const uint4*>(k + base);
-        const __nv_bfloat162* hq = reinterpret_cast<const __nv_bfloat162*>(&uq);
-        const __nv_bfloat162* hk = reinterpret_cast<const __nv_bfloat162*>(&uk);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 fq = __bfloat1622float2(hq[i]), fk = __bfloat1622float2(hk[i]);
-            sq = fmaf(fq.x, fq.x, sq);
-            sq = fmaf(fq.y, fq.y, sq);
-            sk = fmaf(fk.x, fk.x, sk);
-            sk = fmaf(fk.y, fk.y, sk);
+    extern __shared__ __align__(16) uint8_t stage[];  // 2 * (Dk / 8) panels
+    const int c = blockIdx.x, j = blockIdx.y, bb = blockIdx.z;
+    const int tid = threadIdx.x;
+    const int ng = (int)(d.Dk / 8);  // 16-byte pieces per row
+    uint8_t* sq = stage;
+    uint8_t* sk = stage + ng * kPanelPad;
+    const int64_t t0 = (int64_t)c * kChunk;
+    for (int e = tid; e < kChunk * ng; e += blockDim.x) {  // row r = e / ng, piece g = e % ng
+        const int r = e / ng, g = e - (e / ng) * ng;
+        const int64_t t = t0 + r;
+        uint4 uq = make_uint4(0u, 0u, 0u, 0u), uk = uq;
+        if (t < d.T) {
+            const int64_t base = (((int64_t)bb * d.T + t) * d.Hk + j) * d.Dk + 8 * g;
+            uq = *reinterpret_cast<const uint4*>(q + base);
+            uk = *reinterpret_cast<const uint4*>(k + base);
         }
+        *reinterpret_cast<uint4*>(sq + g * kPanelPad + r * 16) = uq;
+        *reinterpret_cast<uint4*>(sk + g * kPanelPad + r * 16) = uk;
     }
+    __syncthreads();
+    if (tid < 2 * kChunk) {  // thread r: row r of q; thread 64 + r: row r of k
+        const int r = tid & (kChunk - 1);
+        const uint8_t* src = tid < kChunk ? sq : sk;
+        float sum = 0.f;
+        for (int g = 0; g < ng; ++g) {
+            const uint4 u = *reinterpret_cast<const uint4*>(src + g * kPanelPad + r * 16);
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        sq += __shfl_xor_sync(0xffffffffu, sq, off);
-        sk += __shfl_xor_sync(0xffffffffu, sk, off);
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(h2[i]);
+                sum = fmaf(f.x, f.x, sum);
+                sum = fmaf(f.y, f.y, sum);
+            }
+        }
+        const int64_t t = t0 + r;
+        (tid < kChunk ? rq : rk)[((int64_t)bb * d.Hk + j) * d.Tp + t] = t < d.T ? 1.f / sqrtf(sum + kNormEps) : 0.f;
     }
-    if (lane < ng) {
-        const int64_t c = t / kChunk;
-        const int64_t off = ((bb * d.Hk + j) * d.NC + c) * kChunk * d.Dk * 2 + (int64_t)lane * kChunk * 16 +
-                            (t % kChunk) * 16;
-        *reinterpret_cast<uint4*>(qimg + off) = uq;
-        *reinterpret_cast<uint4*>(kimg + off) = uk;
-    }
-    if (lane == 0) {
-        rq[(bb * d.Hk + j) * d.Tp + t] = in ? 1.f / sqrtf(sq + kNormEps) : 0.f;
-        rk[(bb * d.Hk + j) * d.Tp + t] = in ? 1.f / sqrtf(sk + kNormEps) : 0.f;
+    const int64_t ioff = (((int64_t)bb * d.Hk + j) * d.NC + c) * kChunk * d.Dk * 2;
+    for (int e = tid; e < kChunk * ng; e += blockDim.x) {  // piece g = e / 64, row r = e % 64
+        const int g = e >> 6, r = e & (kChunk - 1);
+        *reinterpret_cast<uint4*>(qimg + ioff + (int64_t)e * 16) =
+            *reinterpret_cast<const uint4*>(sq + g * kPanelPad + r * 16);
+        *reinterpret_cast<uint4*>(kimg + ioff + (int64_t)e * 16) =
+            *reinterpret_cast<const uint4*>(sk + g * kPanelPad + r * 16);
     }
 }
 
@@ -160,11 +169,15 @@ cudaError_t launch_prep_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
     prep_gates_kernel<TI><<<g1, 256, 0, s>>>(d, (const TI*)p.a, (const TI*)p.b, p.A_log,
                                              p.dt_bias, p.mask, p.gam, p.beta);
     const int64_t rows = d.B * d.Tp * d.Hk;
-    if (tc_path(d))
-        prep_norms_img_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
+    if (tc_path(d)) {
+        const int smem = (int)(2 * (d.Dk / 8) * kPanelPad);
+        cudaError_t e = cudaFuncSetAttribute(prep_norms_img_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        prep_norms_img_kernel<<<dim3((unsigned)d.NC, (unsigned)d.Hk, (unsigned)d.B), 256, smem, s>>>(
             d, (const __nv_bfloat16*)p.q, (const __nv_bfloat16*)p.k, p.rq, p.rk,
             static_cast<uint8_t*>(p.qimg), static_cast<uint8_t*>(p.kimg));
-    else
+    } else
         prep_norms_kernel<TI><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(d, (const TI*)p.q,
                                                                          (const TI*)p.k, p.rq, p.rk);
     count_launches(2);
