@@ -42,9 +42,21 @@ constexpr int kBlkK = 64;  // Dk block of the state products (the last one may b
 // 64 + max(2 Dk, Dv).  Phase 0 parks Y (Dv <= 256 columns) at 64, before AK /
 // AQ are live.
 constexpr uint32_t kS1 = 0, kAK = 64;
-// fp32 64 x 64 scratch matrices are row-padded to 65 floats: epilogue lanes own
-// rows, and an unpadded 256-byte row stride puts every lane in one bank
-constexpr int LDM = C + 1;
+// fp32 64 x 64 scratch matrices have rows of 68 floats: 16-byte aligned rows
+// (row-wise runs move as float4) four banks apart, so eight lanes that own eight
+// rows touch 32 distinct banks; an unpadded 256-byte row stride would put every
+// lane in one bank
+constexpr int LDM = C + 4;
+
+__device__ __forceinline__ void ld_row8(const float* src, float* v) {
+    const float4 a = reinterpret_cast<const float4*>(src)[0], b = reinterpret_cast<const float4*>(src)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void st_row8(float* dst, const float* v) {
+    reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
 
 struct Smem {
     // byte offsets inside dynamic shared memory
@@ -442,15 +454,15 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
                 float m[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) m[i] = (c0 + i <= r) ? x[i] : 0.f;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) Pf[r * LDM + c0 + i] = m[i];
+                st_row8(Pf + r * LDM + c0, m);
+                st_row8(Pf + r * LDM + c0 + 8, m + 8);
             });
             acc_rows2(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
                 float m[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) m[i] = -bt[c0 + i] * x[i];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) Tbf[r * LDM + c0 + i] = m[i];
+                st_row8(Tbf + r * LDM + c0, m);
+                st_row8(Tbf + r * LDM + c0 + 8, m + 8);
             });
             acc_rows(tb, kAK, Dv, [&](int r, int c0, const float (&x)[16]) {
                 float vv[16], y[16];
@@ -603,18 +615,28 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     sync_after_mma(&bar, phase, ok, epi);
     if (epi && ok) {
         acc_rows2(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
+            float m[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) Gkk[r * LDM + c0 + i] = rkv[r] * rkv[c0 + i] * x[i];
+            for (int i = 0; i < 16; ++i) m[i] = rkv[r] * rkv[c0 + i] * x[i];
+            st_row8(Gkk + r * LDM + c0, m);
+            st_row8(Gkk + r * LDM + c0 + 8, m + 8);
         });
         acc_rows2(tb, kS1, C, [&](int r, int c0, const float (&x)[16]) {
             float tt[16];
             ld_bf16x8(sm + L.Tt + tc::panel_off(c0, r, C), tt);
             ld_bf16x8(sm + L.Tt + tc::panel_off(c0 + 8, r, C), tt + 8);
+            float tb16[16], zp[16];
+            ld_row8(Tbf + r * LDM + c0, tb16);
+            ld_row8(Tbf + r * LDM + c0 + 8, tb16 + 8);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                Tbf[r * LDM + c0 + i] += bt[c0 + i] * gm[c0 + i] * rkv[c0 + i] * x[i];
-                ZP[r * LDM + c0 + i] = tt[i] * x[i];
+                tb16[i] += bt[c0 + i] * gm[c0 + i] * rkv[c0 + i] * x[i];
+                zp[i] = tt[i] * x[i];
             }
+            st_row8(Tbf + r * LDM + c0, tb16);
+            st_row8(Tbf + r * LDM + c0 + 8, tb16 + 8);
+            st_row8(ZP + r * LDM + c0, zp);
+            st_row8(ZP + r * LDM + c0 + 8, zp + 8);
         });
     }
     __syncthreads();
@@ -634,7 +656,9 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     // Tbar as a bf16 operand (x = j, y = i)
     for (int e = tid; e < C * (C / 8); e += blockDim.x) {
         const int i = e / (C / 8), j0 = (e % (C / 8)) * 8;
-        st_bf16x8(sm + L.Tbh + canon(j0, i, C), Tbf + i * LDM + j0);
+        float t8[8];
+        ld_row8(Tbf + i * LDM + j0, t8);
+        st_bf16x8(sm + L.Tbh + canon(j0, i, C), t8);
     }
     tc::fence_async_smem();
     cta_sync_tc();
@@ -651,8 +675,11 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             tile_put16(sm + L.Xh, C, c0, r, x);  // X row-major (x = l, y = j)
         });
         acc_rows2(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
+            float m[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) Gqk[r * LDM + c0 + i] = rqv[r] * rkv[c0 + i] * x[i];
+            for (int i = 0; i < 16; ++i) m[i] = rqv[r] * rkv[c0 + i] * x[i];
+            st_row8(Gqk + r * LDM + c0, m);
+            st_row8(Gqk + r * LDM + c0 + 8, m + 8);
         });
     }
     tc::fence_async_smem();
@@ -689,26 +716,31 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mv[i] = 0.f;
             }
+            float gk8[8], pf8[8], gq8[8];
+            ld_row8(Gkk + r * LDM + c0, gk8);
+            ld_row8(Pf + r * LDM + c0, pf8);
+            ld_row8(Gqk + r * LDM + c0, gq8);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int jj = c0 + i;
-                const int idx = r * LDM + jj;
                 const float m = mv[i];
                 const float ab = jj < r ? -x[i] : 0.f;
-                const float gk = Gkk[idx];
-                const float mb = ab * bt[r] * gk + Pf[idx] * Gqk[idx];
+                const float gk = gk8[i];
+                const float mb = ab * bt[r] * gk + pf8[i] * gq8[i];
                 sb = fmaf(ab * m, gk, sb);
                 const float mm = mb * m;
-                Gkk[idx] = mm;
-                Gqk[idx] = ab * bt[r] * m;
+                gk8[i] = mm;
+                gq8[i] = ab * bt[r] * m;
                 const float yk = mm - rc;
                 const float tk = rs + yk;
                 rc = (tk - rs) - yk;
                 rs = tk;
-                const float pm = Pf[idx] * m;
+                const float pm = pf8[i] * m;
                 pk[i] = pm * rkv[jj];
                 pq[i] = pm * rqv[r];
             }
+            st_row8(Gkk + r * LDM + c0, gk8);
+            st_row8(Gqk + r * LDM + c0, gq8);
             st_bf16x8(sm + L.PMk + canon(c0, r, C), pk);
             st_bf16x8(sm + L.PMq + canon(c0, r, C), pq);
             sbp[pi * C + r] += sb;  // two 8-column pieces per lane
@@ -719,10 +751,13 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     __syncthreads();
     // H = (Gb + Gb^T) diag(r_k) as a bf16 operand; column sums of Mbar o M (fp64)
     for (int e = tid; e < C * (C / 8); e += blockDim.x) {
-        const int i = e / (C / 8), j0 = (e % (C / 8)) * 8;
+        // lanes take consecutive rows i: the row-wise float4 reads and the
+        // transposed column reads both stay conflict-free
+        const int i = e % C, j0 = (e / C) * 8;
         float h8[8];
+        ld_row8(Gqk + i * LDM + j0, h8);
 #pragma unroll
-        for (int s = 0; s < 8; ++s) h8[s] = (Gqk[i * LDM + j0 + s] + Gqk[(j0 + s) * LDM + i]) * rkv[j0 + s];
+        for (int s = 0; s < 8; ++s) h8[s] = (h8[s] + Gqk[(j0 + s) * LDM + i]) * rkv[j0 + s];
         st_bf16x8(sm + L.Hk + canon(j0, i, C), h8);
     }
     if (epi) {
