@@ -460,7 +460,9 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             acc_rows2(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
                 float m[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) m[i] = -bt[c0 + i] * x[i];
+                for (int i = 0; i < 16; i += 8) ld_row8(bt + c0 + i, m + i);  // per-column vectors as float4
+#pragma unroll
+                for (int i = 0; i < 16; ++i) m[i] = -m[i] * x[i];
                 st_row8(Tbf + r * LDM + c0, m);
                 st_row8(Tbf + r * LDM + c0 + 8, m + 8);
             });
@@ -617,7 +619,9 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         acc_rows2(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
             float m[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) m[i] = rkv[r] * rkv[c0 + i] * x[i];
+            for (int i = 0; i < 16; i += 8) ld_row8(rkv + c0 + i, m + i);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) m[i] = rkv[r] * m[i] * x[i];
             st_row8(Gkk + r * LDM + c0, m);
             st_row8(Gkk + r * LDM + c0 + 8, m + 8);
         });
@@ -628,9 +632,16 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             float tb16[16], zp[16];
             ld_row8(Tbf + r * LDM + c0, tb16);
             ld_row8(Tbf + r * LDM + c0 + 8, tb16 + 8);
+            float cb[16], cg[16], ck[16];
+#pragma unroll
+            for (int i = 0; i < 16; i += 8) {
+                ld_row8(bt + c0 + i, cb + i);
+                ld_row8(gm + c0 + i, cg + i);
+                ld_row8(rkv + c0 + i, ck + i);
+            }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                tb16[i] += bt[c0 + i] * gm[c0 + i] * rkv[c0 + i] * x[i];
+                tb16[i] += cb[i] * cg[i] * ck[i] * x[i];
                 zp[i] = tt[i] * x[i];
             }
             st_row8(Tbf + r * LDM + c0, tb16);
@@ -677,7 +688,9 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         acc_rows2(tb, kS2, C, [&](int r, int c0, const float (&x)[16]) {
             float m[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) m[i] = rqv[r] * rkv[c0 + i] * x[i];
+            for (int i = 0; i < 16; i += 8) ld_row8(rkv + c0 + i, m + i);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) m[i] = rqv[r] * m[i] * x[i];
             st_row8(Gqk + r * LDM + c0, m);
             st_row8(Gqk + r * LDM + c0 + 8, m + 8);
         });
@@ -703,8 +716,9 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             const int J = c0 >> 4, I = r >> 4;
             if (J < I) {
                 const float u = uf[J * C + r];
+                ld_row8(wf + J * C + c0, mv);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mv[i] = u * wf[J * C + c0 + i];
+                for (int i = 0; i < 8; ++i) mv[i] *= u;
             } else if (J == I) {
                 const float ghr = Ghi[r], glr = Glo[r];
 #pragma unroll
@@ -716,7 +730,8 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mv[i] = 0.f;
             }
-            float gk8[8], pf8[8], gq8[8];
+            float gk8[8], pf8[8], gq8[8], kc8[8];
+            ld_row8(rkv + c0, kc8);
             ld_row8(Gkk + r * LDM + c0, gk8);
             ld_row8(Pf + r * LDM + c0, pf8);
             ld_row8(Gqk + r * LDM + c0, gq8);
@@ -736,7 +751,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
                 rc = (tk - rs) - yk;
                 rs = tk;
                 const float pm = pf8[i] * m;
-                pk[i] = pm * rkv[jj];
+                pk[i] = pm * kc8[i];
                 pq[i] = pm * rqv[r];
             }
             st_row8(Gkk + r * LDM + c0, gk8);
