@@ -651,11 +651,15 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         });
     }
     __syncthreads();
-    if (tid < C) {  // <Z_i, k_i> = sum_m T_mi (Wbar K^T)_mi, Z = T^T Wbar (fixed order)
+    if (epi) {  // <Z_i, k_i> = sum_m T_mi (Wbar K^T)_mi, Z = T^T Wbar: four 16-row partials
+        const int i = tid & (C - 1), qd = tid >> 6;
         float z = 0.f;
-        for (int m = 0; m < C; ++m) z += ZP[m * LDM + tid];
-        zk[tid] = z;
+#pragma unroll 4
+        for (int m = 16 * qd; m < 16 * qd + 16; ++m) z += ZP[m * LDM + i];
+        csp[qd * C + i] = z;  // scratch until the column sums of phase 2
     }
+    __syncthreads();
+    if (tid < C) zk[tid] = (csp[tid] + csp[C + tid]) + (csp[2 * C + tid] + csp[3 * C + tid]);
     __syncthreads();
     if (tid < C) {
         const int i = tid;
