@@ -123,7 +123,7 @@ __device__ __forceinline__ void scale_q(uint8_t* Q, const uint8_t* raw, int Dk) 
 __global__ void __launch_bounds__(kThreads + 32, 1)
     fwd_scan_ta_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm) {
     extern __shared__ __align__(1024) uint8_t sm[];
-    __shared__ uint64_t bar, barW, barQ, barK, barP, barU, barR[2];
+    __shared__ uint64_t bar, barW, barQ, barK, barP, barU, barR[2], barD[2];
     __shared__ uint32_t tmem_sh;
     const int tile = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
     const int j = h / (int)d.G;
@@ -221,6 +221,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::mbar_init(&barU, 1);
         tc::mbar_init(&barR[0], 1);
         tc::mbar_init(&barR[1], 1);
+        for (int i = 0; i < 2; ++i) tc::mbar_init(&barD[i], kThreads / 32);
         tc::fence_mbar_init();
     }
     __syncthreads();  // barriers initialised
@@ -339,7 +340,9 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
             phase ^= 1u;
             tc::tc_fence_after();
-            // step 3: Delta^T = U^T - acc -> A operands hi, lo and (diag(e r_k)) hi, lo
+            // step 3: Delta^T = U^T - acc -> A operands hi, lo and (diag(e r_k)) hi, lo,
+            // in two passes of 16 steps (32 g + 16 u2 .. + 15), each handed to the
+            // MMA issuer on its own barrier
             ok = tc::mbar_wait(&barU, (uint32_t)(c & 1), &g_err_scanta) && ok;
             float a[2][16];
             tc::tmem_ld16(tc::tmem_addr(tb, lb, TC.dacc + 32 * g), a[0]);
@@ -347,33 +350,37 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             tc::tmem_wait_ld();
             uint32_t dew[16], delw[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float dl[2], lo[2], de[2], dlo[2];
+            for (int u2 = 0; u2 < 2; ++u2) {
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int ti = 2 * i + u;  // step 32 g + ti
-                    dl[u] = Ub[(32 * g + ti) * DVT + r] - a[ti >> 4][ti & 15];
-                    lo[u] = dl[u] - __bfloat162float(__float2bfloat16_rn(dl[u]));
-                    de[u] = dl[u] * kev[32 * g + ti];
-                    dlo[u] = de[u] - __bfloat162float(__float2bfloat16_rn(de[u]));
+                for (int i = 8 * u2; i < 8 * u2 + 8; ++i) {
+                    float dl[2], lo[2], de[2], dlo[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int ti = 2 * i + u;  // step 32 g + ti
+                        dl[u] = Ub[(32 * g + ti) * DVT + r] - a[ti >> 4][ti & 15];
+                        lo[u] = dl[u] - __bfloat162float(__float2bfloat16_rn(dl[u]));
+                        de[u] = dl[u] * kev[32 * g + ti];
+                        dlo[u] = de[u] - __bfloat162float(__float2bfloat16_rn(de[u]));
+                    }
+                    hiw[i] = tc::pack_bf16(dl[0], dl[1]);
+                    low[i] = tc::pack_bf16(lo[0], lo[1]);
+                    dew[i] = tc::pack_bf16(de[0], de[1]);
+                    delw[i] = tc::pack_bf16(dlo[0], dlo[1]);
                 }
-                hiw[i] = tc::pack_bf16(dl[0], dl[1]);
-                low[i] = tc::pack_bf16(lo[0], lo[1]);
-                dew[i] = tc::pack_bf16(de[0], de[1]);
-                delw[i] = tc::pack_bf16(dlo[0], dlo[1]);
+                const uint32_t cc = 16 * g + 8 * u2;
+                tc::tmem_st8u(tc::tmem_addr(tb, lb, TC.aop + cc), hiw + 8 * u2);
+                tc::tmem_st8u(tc::tmem_addr(tb, lb, TC.aop + 32 + cc), low + 8 * u2);
+                tc::tmem_st8u(tc::tmem_addr(tb, lb, TC.aop + 64 + cc), dew + 8 * u2);
+                tc::tmem_st8u(tc::tmem_addr(tb, lb, TC.aop + 96 + cc), delw + 8 * u2);
+                tc::tmem_wait_st();
+                tc::warp_arrive_after_st(&barD[u2]);
             }
-            tc::tmem_st16u(tc::tmem_addr(tb, lb, TC.aop + 16 * g), hiw);
-            tc::tmem_st16u(tc::tmem_addr(tb, lb, TC.aop + 32 + 16 * g), low);
-            tc::tmem_st16u(tc::tmem_addr(tb, lb, TC.aop + 64 + 16 * g), dew);
-            tc::tmem_st16u(tc::tmem_addr(tb, lb, TC.aop + 96 + 16 * g), delw);
-            tc::tmem_wait_st();
+            if (storer) tc::bulk_wait_read_all();  // Delta staging of c - 1 read out
+            tc::named_sync(1, kThreads);
         }
-        if (storer) tc::bulk_wait_read_all();  // Delta staging of c - 1 read out
-        tc::tc_fence_before();
-        __syncthreads();  // (C)
-        tc::tc_fence_after();
         if (prod) {
-            // step 4: O^T += Delta^T P^T (hi, lo);  S^T += (Delta^T diag(e r_k)) K (hi, lo)
+            // step 4: O^T += Delta^T P^T (hi, lo);  S^T += (Delta^T diag(e r_k)) K (hi, lo);
+            // the steps of pass u2 (16-step slices u2 and 2 + u2) once it is handed over
             ok = tc::mbar_wait(&barP, (uint32_t)(c & 1), &g_err_scanta) && ok;
             ok = tc::mbar_wait(&barK, (uint32_t)(c & 1), &g_err_scanta) && ok;
             const uint32_t idp = tc::idesc_bf16(DVT, C, false, false);
@@ -381,11 +388,16 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             const uint64_t dp0 = tP.desc(0), ip = tP.desc_step();
             const uint64_t dk0 = tKmn.desc(0), ik = tKmn.desc_step();
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int k = (i & 3) * 16;
-                const uint32_t hl = (uint32_t)(i >> 2) * 32u;
-                tc::mma_bf16_ta(tb + ocol, tb + TC.aop + hl + k / 2, dp0 + (uint64_t)(i & 3) * ip, idp, 1u);
-                tc::mma_bf16_ta(tb, tb + TC.aop + 64 + hl + k / 2, dk0 + (uint64_t)(i & 3) * ik, idk, 1u);
+            for (int u2 = 0; u2 < 2; ++u2) {
+                ok = tc::mbar_wait(&barD[u2], (uint32_t)(c & 1), &g_err_scanta) && ok;
+                tc::tc_fence_after();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int ks = 2 * (i & 1) + u2;  // 16-step slice
+                    const uint32_t hl = (uint32_t)(i >> 1) * 32u;
+                    tc::mma_bf16_ta(tb + ocol, tb + TC.aop + hl + 8 * ks, dp0 + (uint64_t)ks * ip, idp, 1u);
+                    tc::mma_bf16_ta(tb, tb + TC.aop + 64 + hl + 8 * ks, dk0 + (uint64_t)ks * ik, idk, 1u);
+                }
             }
             tc::mma_commit(&bar);
             if (c + 1 < d.NC) load_u(c + 1);  // step 3 of chunk c has read U

@@ -342,6 +342,25 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[1
         "r"(v[15])
         : "memory");
 }
+// 32 lanes x 32 bits, 8 consecutive columns per thread, raw 32-bit words v[0 .. 7]
+__device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+        : "memory");
+}
+// One arrival on `bar` for the calling warp, once every lane's tcgen05.st have
+// completed (each lane has executed tcgen05.wait::st): the waiter may then
+// issue MMAs that read those TMEM columns.
+__device__ __forceinline__ void warp_arrive_after_st(uint64_t* bar) {
+    tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+// named barrier `id` (1 .. 15) over `count` threads of the CTA, a multiple of 32
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 __device__ __forceinline__ void tmem_ld16u(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
