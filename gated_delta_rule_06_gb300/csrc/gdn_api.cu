@@ -162,6 +162,7 @@ gdn_status cuda_status(cudaError_t e) {
 }  // namespace
 
 namespace gdn {
+int note_cuda_error(cudaError_t e) { return (int)cuda_status(e); }
 int sm_count() {
     constexpr int kMaxDev = 64;
     static std::atomic<int> cache[kMaxDev];

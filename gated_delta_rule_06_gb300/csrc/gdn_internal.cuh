@@ -179,6 +179,9 @@ cudaError_t launch_causal_conv1d_update(int64_t B, int64_t C, int64_t S, int K, 
                                         cudaStream_t s);
 // streaming multiprocessors of the current device (cached per device)
 int sm_count();
+// Records e as the library's last CUDA error (the text gdn_last_cuda_error
+// returns) and gives GDN_ERR_CUDA; cudaSuccess gives GDN_OK and records nothing.
+int note_cuda_error(cudaError_t e);
 unsigned int read_clear_error_decode();
 // tensor-core (tcgen05) variants for bf16 inputs
 bool bwd_chunk_tc_supported(const Dims& d);

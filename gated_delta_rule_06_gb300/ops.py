@@ -39,6 +39,16 @@ class GdnShape(ctypes.Structure):
                 ("dtype", ctypes.c_int32), ("has_mask", ctypes.c_int32)]
 
 
+class GdnHostInputs(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "a", "b", "A_log", "dt_bias",
+                                               "state0", "mask", "d_o", "d_state_T")]
+
+
+class GdnHostOutputs(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("o", "state_T", "dq", "dk", "dv", "da", "db",
+                                               "dA_log", "ddt_bias", "dstate0")]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -78,6 +88,17 @@ def load_library(path: str = LIB_PATH):
         lib.gdn_causal_conv1d_update.restype = i32
         lib.gdn_decode_conv.argtypes = [shp, i32, ctypes.c_int64] + [vp] * 13
         lib.gdn_decode_conv.restype = i32
+        lib.gdn_host_session_bytes.argtypes = [shp, i32, ctypes.POINTER(sz)]
+        lib.gdn_host_session_bytes.restype = i32
+        lib.gdn_host_session_create.argtypes = [shp, i32, i32, vp, sz, vp, ctypes.POINTER(vp)]
+        lib.gdn_host_session_create.restype = i32
+        lib.gdn_host_step.argtypes = [vp, ctypes.POINTER(GdnHostInputs),
+                                      ctypes.POINTER(GdnHostOutputs)]
+        lib.gdn_host_step.restype = i32
+        lib.gdn_host_session_sync.argtypes = [vp]
+        lib.gdn_host_session_sync.restype = i32
+        lib.gdn_host_session_destroy.argtypes = [vp]
+        lib.gdn_host_session_destroy.restype = i32
         _lib = lib
         return lib
 
@@ -448,3 +469,112 @@ def decode_conv(hidden, conv_state, conv_weight, state, *, a=None, b=None, A_log
         _p(state_out), _stream())
     _check(rc)
     return o, state_out, final_conv_state
+
+
+class HostSession:
+    """Steps on HOST tensors through gdn_host_step (include/gdn_host.h): the
+    library uploads each step's inputs, runs the forward (and the backward) and
+    downloads the results, overlapping one step's copies with the compute of
+    the steps next to it.  The device arena is a PyTorch allocation owned by
+    this object; compute runs on the current CUDA stream at construction.
+
+    ``step(inputs, outputs)`` takes dicts of contiguous CPU tensors (pinned for
+    asynchronous copies): inputs q, k, v, a, b (or log_decay, beta when
+    ``gates="lb"``), A_log, dt_bias, state0, mask, d_o, d_state_T; outputs o,
+    state_T and, for a backward session, dq, dk, dv, da, db (or d_log_decay,
+    d_beta), dA_log, ddt_bias, dstate0.  It only enqueues: the step's tensors
+    are kept alive here and must be left alone until ``sync()``."""
+
+    _IN = ("q", "k", "v", "a", "b", "A_log", "dt_bias", "state0", "mask", "d_o", "d_state_T")
+    _OUT = ("o", "state_T", "dq", "dk", "dv", "da", "db", "dA_log", "ddt_bias", "dstate0")
+    _ALIAS = {"log_decay": "a", "beta": "b", "d_log_decay": "da", "d_beta": "db"}
+
+    def __init__(self, B, T, Hk, Hv, Dk, Dv, dtype, *, has_mask=False, gates="ab",
+                 backward=True, device="cuda"):
+        if dtype not in _DTYPES:
+            raise GdnError(f"unsupported dtype {dtype}")
+        if gates not in ("ab", "lb"):
+            raise GdnError("gates must be 'ab' or 'lb'")
+        lib = load_library()
+        self._h = None
+        self.dtype, self.gates, self.backward = dtype, gates, bool(backward)
+        self.shape = GdnShape(B, T, Hk, Hv, Dk, Dv, _DTYPES[dtype], int(bool(has_mask)))
+        n = ctypes.c_size_t()
+        _check(lib.gdn_host_session_bytes(ctypes.byref(self.shape), int(self.backward),
+                                          ctypes.byref(n)))
+        self.arena_bytes = n.value
+        self._arena = torch.empty(n.value, dtype=torch.uint8, device=device)
+        h = ctypes.c_void_p()
+        _check(lib.gdn_host_session_create(
+            ctypes.byref(self.shape), 1 if gates == "lb" else 0, int(self.backward),
+            ctypes.c_void_p(self._arena.data_ptr()), n,
+            ctypes.c_void_p(torch.cuda.current_stream(self._arena.device).cuda_stream),
+            ctypes.byref(h)))
+        self._h = h
+        self._inflight = []
+        f32, dt = torch.float32, dtype
+        self._spec = {
+            "q": ((B, T, Hk, Dk), dt), "k": ((B, T, Hk, Dk), dt), "v": ((B, T, Hv, Dv), dt),
+            "a": ((B, T, Hv), dt), "b": ((B, T, Hv), dt), "A_log": ((Hv,), f32),
+            "dt_bias": ((Hv,), f32), "state0": ((B, Hv, Dk, Dv), f32), "mask": ((B, T), torch.uint8),
+            "d_o": ((B, T, Hv, Dv), dt), "d_state_T": ((B, Hv, Dk, Dv), f32),
+            "o": ((B, T, Hv, Dv), dt), "state_T": ((B, Hv, Dk, Dv), f32),
+            "dq": ((B, T, Hk, Dk), dt), "dk": ((B, T, Hk, Dk), dt), "dv": ((B, T, Hv, Dv), dt),
+            "da": ((B, T, Hv), dt), "db": ((B, T, Hv), dt), "dA_log": ((Hv,), f32),
+            "ddt_bias": ((Hv,), f32), "dstate0": ((B, Hv, Dk, Dv), f32)}
+
+    def _host(self, name, t):
+        shape, dt = self._spec[name]
+        if t.is_cuda or not t.is_contiguous() or t.dtype != dt or tuple(t.shape) != shape:
+            raise GdnError(f"{name}: expected a contiguous CPU tensor {dt} {shape}, got "
+                           f"{t.device} {t.dtype} {tuple(t.shape)}")
+        return ctypes.c_void_p(t.data_ptr())
+
+    def outputs(self, pin=True):
+        """Fresh host output tensors for one step (page-locked by default)."""
+        names = self._OUT if self.backward else ("o", "state_T")
+        rename = {}
+        if self.gates == "lb":
+            names = [n for n in names if n not in ("dA_log", "ddt_bias")]
+            rename = {"da": "d_log_decay", "db": "d_beta"}
+        return {rename.get(n, n): torch.empty(self._spec[n][0], dtype=self._spec[n][1],
+                                              pin_memory=pin) for n in names}
+
+    def step(self, inputs: dict, outputs: dict):
+        if self._h is None:
+            raise GdnError("session is closed")
+        ins, outs = GdnHostInputs(), GdnHostOutputs()
+        for k, t in inputs.items():
+            if t is None:
+                continue
+            n = "mask" if k == "mask" else self._ALIAS.get(k, k)
+            if n not in self._IN:
+                raise GdnError(f"unknown input {k}")
+            if n == "mask" and t.dtype != torch.uint8:
+                raise GdnError("mask: expected a uint8 host tensor")
+            setattr(ins, n, self._host(n, t))
+        for k, t in outputs.items():
+            n = self._ALIAS.get(k, k)
+            if n not in self._OUT:
+                raise GdnError(f"unknown output {k}")
+            setattr(outs, n, self._host(n, t))
+        _check(load_library().gdn_host_step(self._h, ctypes.byref(ins), ctypes.byref(outs)))
+        self._inflight.append((inputs, outputs))
+
+    def sync(self):
+        """Wait for every enqueued step; their output tensors are then complete."""
+        if self._h is not None:
+            _check(load_library().gdn_host_session_sync(self._h))
+        self._inflight.clear()
+
+    def close(self):
+        if self._h is not None:
+            h, self._h = self._h, None
+            _check(load_library().gdn_host_session_destroy(h))
+        self._inflight.clear()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

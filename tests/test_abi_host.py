@@ -150,3 +150,37 @@ def test_decode_conv_rejects_before_launch(lib):
     assert call(final=A) == 1                            # final conv state overlaps the input
     assert call(hidden=None) == 1
     assert call(hidden=vp(0x1004)) == 4                  # misaligned
+
+
+def test_host_session_sizing_and_rejections(lib):
+    """gdn_host_session_bytes / _create check everything before any CUDA call."""
+    s = _shape()
+    n_train, n_inf = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.gdn_host_session_bytes(ctypes.byref(s), 1, ctypes.byref(n_train)) == 0
+    assert lib.gdn_host_session_bytes(ctypes.byref(s), 0, ctypes.byref(n_inf)) == 0
+    assert n_train.value % 256 == 0 and n_inf.value % 256 == 0
+    # two slots of one step's tensors at least: q, k, v and o alone per slot
+    per_slot_min = (2 * 130 * 2 * 64 + 2 * 130 * 4 * 32) * 2
+    assert n_inf.value >= 2 * per_slot_min
+    assert n_train.value > n_inf.value
+    assert lib.gdn_host_session_bytes(ctypes.byref(s), 2, ctypes.byref(n_train)) == 1
+    assert lib.gdn_host_session_bytes(ctypes.byref(_shape(Hv=5)), 1, ctypes.byref(n_train)) == 2
+
+    vp = ctypes.c_void_p
+    h = vp()
+    need = n_inf.value
+
+    def create(arena=vp(0x10000000), nbytes=need, gates=0, backward=0, shape=s, out=True):
+        return lib.gdn_host_session_create(ctypes.byref(shape), gates, backward, arena,
+                                           nbytes, None, ctypes.byref(h) if out else None)
+
+    assert create(arena=None) == 1              # null arena
+    assert create(gates=2) == 1                 # gate form
+    assert create(backward=3) == 1
+    assert create(out=False) == 1               # nowhere to put the session
+    assert create(shape=_shape(Dk=12)) == 2
+    assert create(arena=vp(0x10000010)) == 4    # not 256-byte aligned
+    assert create(nbytes=need - 256) == 3       # arena too small
+    assert lib.gdn_host_step(None, None, None) == 1
+    assert lib.gdn_host_session_sync(None) == 1
+    assert lib.gdn_host_session_destroy(None) == 0
