@@ -438,11 +438,12 @@ __device__ __forceinline__ void st8(__nv_bfloat16* o, const float* v) {
     *reinterpret_cast<uint4*>(o) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// TI: input dtype; PT: dtype of the per-value-head partials
+// TI: input dtype; PT: dtype of the per-value-head partials; blk: this
+// block's index among the ceil(B T Hk / 8) blocks of this part
 template <typename TI, typename PT>
-__global__ void __launch_bounds__(256) bwd_qk_kernel(Dims d, Ptrs p) {
+__device__ __forceinline__ void bwd_qk_body(const Dims& d, const Ptrs& p, int64_t blk) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;  // over (b, t, j)
+    const int64_t row = blk * (blockDim.x >> 5) + warp;  // over (b, t, j)
     if (row >= d.B * d.T * d.Hk) return;
     const int64_t j = row % d.Hk;
     const int64_t t = (row / d.Hk) % d.T;
@@ -509,15 +510,14 @@ __global__ void __launch_bounds__(256) bwd_qk_kernel(Dims d, Ptrs p) {
     }
 }
 
-// da / db and per-(b, chunk, head) partial sums; grid (NC, B, ceil(Hv / 8)),
-// one warp per head in the sums
+// da / db and per-(b, chunk, head) partial sums of chunk c, batch bb, heads
+// 8 hz .. 8 hz + 7; one warp per head in the sums
 constexpr int kGateHeadsB = 8;
 template <typename TI>
-__global__ void __launch_bounds__(256) bwd_gate_kernel(Dims d, Ptrs p) {
+__device__ __forceinline__ void bwd_gate_body(const Dims& d, const Ptrs& p, int c, int bb, int hz) {
     __shared__ float sA[kChunk][kGateHeadsB + 1];
     __shared__ float sD[kChunk][kGateHeadsB + 1];
-    const int c = blockIdx.x, bb = blockIdx.y;
-    const int h0 = blockIdx.z * kGateHeadsB;
+    const int h0 = hz * kGateHeadsB;
     const int nh = (int)(d.Hv - h0 < kGateHeadsB ? d.Hv - h0 : kGateHeadsB);
     const int64_t t0 = (int64_t)c * kChunk;
     const TI* a = (const TI*)p.a;
@@ -576,17 +576,46 @@ __global__ void __launch_bounds__(256) bwd_gate_kernel(Dims d, Ptrs p) {
     }
 }
 
-// dA_log / ddt_bias: per head, sum of the partials in (b, chunk) order
-__global__ void bwd_head_sum_kernel(Dims d, Ptrs p) {
-    const int64_t h = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (h >= d.Hv) return;
-    float sA = 0.f, sD = 0.f;
-    for (int64_t r = 0; r < d.B * d.NC; ++r) {
-        sA += p.part[r * d.Hv + h];
-        sD += p.part[d.B * d.NC * d.Hv + r * d.Hv + h];
+// The two independent parts of the reduction in one launch: blocks
+// [0, NC B ceil(Hv / 8)) take the gate cotangents (first, so that they start
+// early: the per-head sum waits for them), the rest the q / k rows.
+template <typename TI, typename PT>
+__global__ void __launch_bounds__(256) bwd_reduce_kernel(Dims d, Ptrs p) {
+    const int64_t nhz = (d.Hv + kGateHeadsB - 1) / kGateHeadsB;
+    const int64_t ngate = d.NC * d.B * nhz;
+    const int64_t blk = blockIdx.x;
+    if (blk < ngate) {
+        const int c = (int)(blk % d.NC), bb = (int)((blk / d.NC) % d.B), hz = (int)(blk / (d.NC * d.B));
+        bwd_gate_body<TI>(d, p, c, bb, hz);
+    } else {
+        bwd_qk_body<TI, PT>(d, p, blk - ngate);
     }
-    p.dA_log[h] = sA;
-    p.ddt_bias[h] = sD;
+}
+
+// dA_log / ddt_bias: one warp per head.  Lane l sums the partials of rows
+// l, l + 32, ... in (b, chunk) order, then a fixed xor tree adds the lanes, so
+// the result does not depend on scheduling; the loads of a lane are independent
+// and go out together.
+__global__ void bwd_head_sum_kernel(Dims d, Ptrs p) {
+    const int64_t h = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (h >= d.Hv) return;
+    const int64_t rows = d.B * d.NC;
+    float sA = 0.f, sD = 0.f;
+#pragma unroll 4
+    for (int64_t r = lane; r < rows; r += 32) {
+        sA += p.part[r * d.Hv + h];
+        sD += p.part[rows * d.Hv + r * d.Hv + h];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        sA += __shfl_xor_sync(0xffffffffu, sA, off);
+        sD += __shfl_xor_sync(0xffffffffu, sD, off);
+    }
+    if (lane == 0) {
+        p.dA_log[h] = sA;
+        p.ddt_bias[h] = sD;
+    }
 }
 
 template <typename TI, int DVT>
@@ -619,18 +648,17 @@ cudaError_t launch_bchunk_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
 template <typename TI>
 cudaError_t launch_reduce_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
     const int64_t rows = d.B * d.T * d.Hk;
+    const int64_t nblk = (rows + 7) / 8 + d.NC * d.B * ((d.Hv + kGateHeadsB - 1) / kGateHeadsB);
     if (tc_path(d))
-        bwd_qk_kernel<TI, __nv_bfloat16><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(d, p);
+        bwd_reduce_kernel<TI, __nv_bfloat16><<<(unsigned)nblk, 256, 0, s>>>(d, p);
     else
-        bwd_qk_kernel<TI, float><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(d, p);
-    dim3 g((unsigned)d.NC, (unsigned)d.B, (unsigned)((d.Hv + kGateHeadsB - 1) / kGateHeadsB));
-    bwd_gate_kernel<TI><<<g, 256, 0, s>>>(d, p);
+        bwd_reduce_kernel<TI, float><<<(unsigned)nblk, 256, 0, s>>>(d, p);
     if (d.gates == 1) {  // log_decay / beta inputs: no per-head parameters to sum
-        count_launches(2);
+        count_launches(1);
         return cudaPeekAtLastError();
     }
-    bwd_head_sum_kernel<<<(unsigned)((d.Hv + 127) / 128), 128, 0, s>>>(d, p);
-    count_launches(3);
+    bwd_head_sum_kernel<<<(unsigned)((d.Hv + 7) / 8), 256, 0, s>>>(d, p);  // 8 heads per CTA
+    count_launches(2);
     return cudaPeekAtLastError();
 }
 

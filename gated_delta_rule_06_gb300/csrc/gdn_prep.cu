@@ -17,16 +17,15 @@ namespace {
 constexpr int kGateHeads = 8;  // heads per CTA of the gate kernel: one warp each, many CTAs
 
 template <typename TI>
-__global__ void __launch_bounds__(256) prep_gates_kernel(Dims d, const TI* __restrict__ a,
-                                                         const TI* __restrict__ b,
-                                                         const float* __restrict__ A_log,
-                                                         const float* __restrict__ dt_bias,
-                                                         const uint8_t* __restrict__ mask,
-                                                         double* __restrict__ gam,
-                                                         float* __restrict__ beta) {
+__device__ __forceinline__ void prep_gates_body(const Dims& d, const TI* __restrict__ a,
+                                                const TI* __restrict__ b,
+                                                const float* __restrict__ A_log,
+                                                const float* __restrict__ dt_bias,
+                                                const uint8_t* __restrict__ mask,
+                                                double* __restrict__ gam,
+                                                float* __restrict__ beta, int c, int bb, int hz) {
     __shared__ float lg[kChunk][kGateHeads + 1];
-    const int c = blockIdx.x, bb = blockIdx.y;
-    const int h0 = blockIdx.z * kGateHeads;
+    const int h0 = hz * kGateHeads;
     const int nh = (int)(d.Hv - h0 < kGateHeads ? d.Hv - h0 : kGateHeads);
     const int64_t t0 = (int64_t)c * kChunk;
     for (int idx = threadIdx.x; idx < kChunk * nh; idx += blockDim.x) {
@@ -110,14 +109,12 @@ __global__ void __launch_bounds__(256) prep_norms_kernel(Dims d, const TI* __res
 // the norms come from shared memory; each image leaves with contiguous stores.
 constexpr int kPanelPad = kChunk * 16 + 16;  // bytes per staged 64-row panel
 
-__global__ void __launch_bounds__(256) prep_norms_img_kernel(Dims d, const __nv_bfloat16* __restrict__ q,
-                                                             const __nv_bfloat16* __restrict__ k,
-                                                             float* __restrict__ rq,
-                                                             float* __restrict__ rk,
-                                                             uint8_t* __restrict__ qimg,
-                                                             uint8_t* __restrict__ kimg) {
+__device__ __forceinline__ void prep_norms_img_body(const Dims& d, const __nv_bfloat16* __restrict__ q,
+                                                    const __nv_bfloat16* __restrict__ k,
+                                                    float* __restrict__ rq, float* __restrict__ rk,
+                                                    uint8_t* __restrict__ qimg,
+                                                    uint8_t* __restrict__ kimg, int c, int j, int bb) {
     extern __shared__ __align__(16) uint8_t stage[];  // 2 * (Dk / 8) panels
-    const int c = blockIdx.x, j = blockIdx.y, bb = blockIdx.z;
     const int tid = threadIdx.x;
     const int ng = (int)(d.Dk / 8);  // 16-byte pieces per row
     uint8_t* sq = stage;
@@ -164,22 +161,46 @@ __global__ void __launch_bounds__(256) prep_norms_img_kernel(Dims d, const __nv_
 }
 
 template <typename TI>
+__global__ void __launch_bounds__(256) prep_gates_kernel(Dims d, Ptrs p) {
+    prep_gates_body<TI>(d, (const TI*)p.a, (const TI*)p.b, p.A_log, p.dt_bias, p.mask, p.gam,
+                        p.beta, blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
+// The tensor-core path's prep in one launch: blocks [0, NC B ceil(Hv / 8)) take
+// the gates, the rest the q / k norms and images (two independent parts).
+__global__ void __launch_bounds__(256) prep_tc_kernel(Dims d, Ptrs p) {
+    const int64_t ngate = d.NC * d.B * ((d.Hv + kGateHeads - 1) / kGateHeads);
+    const int64_t blk = blockIdx.x;
+    if (blk < ngate) {
+        prep_gates_body<__nv_bfloat16>(d, (const __nv_bfloat16*)p.a, (const __nv_bfloat16*)p.b,
+                                       p.A_log, p.dt_bias, p.mask, p.gam, p.beta,
+                                       (int)(blk % d.NC), (int)((blk / d.NC) % d.B),
+                                       (int)(blk / (d.NC * d.B)));
+    } else {
+        const int64_t r = blk - ngate;  // (chunk, key head, batch)
+        prep_norms_img_body(d, (const __nv_bfloat16*)p.q, (const __nv_bfloat16*)p.k, p.rq, p.rk,
+                            static_cast<uint8_t*>(p.qimg), static_cast<uint8_t*>(p.kimg),
+                            (int)(r % d.NC), (int)((r / d.NC) % d.Hk), (int)(r / (d.NC * d.Hk)));
+    }
+}
+
+template <typename TI>
 cudaError_t launch_prep_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
-    dim3 g1((unsigned)d.NC, (unsigned)d.B, (unsigned)((d.Hv + kGateHeads - 1) / kGateHeads));
-    prep_gates_kernel<TI><<<g1, 256, 0, s>>>(d, (const TI*)p.a, (const TI*)p.b, p.A_log,
-                                             p.dt_bias, p.mask, p.gam, p.beta);
-    const int64_t rows = d.B * d.Tp * d.Hk;
+    const int64_t ngate = d.NC * d.B * ((d.Hv + kGateHeads - 1) / kGateHeads);
     if (tc_path(d)) {
         const int smem = (int)(2 * (d.Dk / 8) * kPanelPad);
-        cudaError_t e = cudaFuncSetAttribute(prep_norms_img_kernel,
+        cudaError_t e = cudaFuncSetAttribute(prep_tc_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        prep_norms_img_kernel<<<dim3((unsigned)d.NC, (unsigned)d.Hk, (unsigned)d.B), 256, smem, s>>>(
-            d, (const __nv_bfloat16*)p.q, (const __nv_bfloat16*)p.k, p.rq, p.rk,
-            static_cast<uint8_t*>(p.qimg), static_cast<uint8_t*>(p.kimg));
-    } else
-        prep_norms_kernel<TI><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(d, (const TI*)p.q,
-                                                                         (const TI*)p.k, p.rq, p.rk);
+        prep_tc_kernel<<<(unsigned)(ngate + d.NC * d.Hk * d.B), 256, smem, s>>>(d, p);
+        count_launches(1);
+        return cudaPeekAtLastError();
+    }
+    dim3 g1((unsigned)d.NC, (unsigned)d.B, (unsigned)((d.Hv + kGateHeads - 1) / kGateHeads));
+    prep_gates_kernel<TI><<<g1, 256, 0, s>>>(d, p);
+    const int64_t rows = d.B * d.Tp * d.Hk;
+    prep_norms_kernel<TI><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(d, (const TI*)p.q,
+                                                                     (const TI*)p.k, p.rq, p.rk);
     count_launches(2);
     return cudaPeekAtLastError();
 }
