@@ -264,6 +264,8 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs 
     const int64_t ldv = d.Hv * Dv;
     const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(p.v);
 
+    // the v tile is first read by the U product: its copies stay in flight under
+    // the Grams, the A / P pass and the solve
     cpa_tile(sm + L.V, v + ((int64_t)bb * d.T + t0) * ldv + (int64_t)h * Dv, ldv, Dv, nvalid);
     tc::cp_async_commit();
     if (warp == 0) {
@@ -291,8 +293,6 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs 
         rqv[tid] = p.rq[rbase + tid] * rsqrtf((float)Dk);
         rkv[tid] = p.rk[rbase + tid];
     }
-    tc::cp_async_wait_all();
-    tc::fence_async_smem();
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -414,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs 
         st_bf16x8(sm + L.Tu + o, u8);
         st_bf16x8(sm + L.Tul + o, ul);
     }
+    tc::cp_async_wait_all();  // this thread's pieces of the v tile
     tc::fence_async_smem();
     tc::tc_fence_before();
     __syncthreads();
