@@ -110,6 +110,10 @@ def work_model(w, conv_k=0):
         bytes=qk + units * (2 * Dk * Dv * img + C * Dv * 4 + C * Dv * img + C * C * img
                             + 2 * C * Dv * es + 4 * C * 4
                             + 2 * C * Dk * img + C * Dv * es + 2 * C * 4))
+    # the reverse scan and the per-chunk gradients as one launch (the images the
+    # first writes and the second reads counted in both)
+    m["bwd_scan_chunk"] = dict(flops=m["bwd_scan"]["flops"] + m["bwd_chunk"]["flops"],
+                               bytes=m["bwd_scan"]["bytes"] + m["bwd_chunk"]["bytes"])
     m["bwd_reduce"] = dict(
         flops=0.0,
         bytes=2 * BH * T * Dk * img + 4 * BHk * T * Dk * es + 2 * BH * T * 4 + 4 * B * T * Hv * es)
@@ -512,7 +516,8 @@ def run_ours(args, w, world, rank, local):
     t_hbm = by / (peaks["hbm_gbs"] * 1e9)
     # bf16 workloads run the chunk contractions on the tensor cores (tcgen05);
     # fp32 workloads run them as FFMA on the CUDA cores
-    tensor = w.dtype == torch.bfloat16 and dom in ("fwd_chunk", "fwd_scan", "bwd_scan", "bwd_chunk")
+    tensor = w.dtype == torch.bfloat16 and dom in ("fwd_chunk", "fwd_scan", "bwd_scan", "bwd_chunk",
+                                                  "bwd_scan_chunk")
     cpeak = peaks["bf16_tflops"] if tensor else FP32_ALU_PEAK_TFLOPS
     t_cmp = fl / (cpeak * 1e12)
     traffic = measured_traffic(w.name, dom)

@@ -49,7 +49,7 @@ struct Layout {
     // byte offsets into the forward workspace
     size_t U, fwd_total;
     // byte offsets into the backward workspace
-    size_t dSck, Dbar, dqh, dkh, dl, dbeta, part, bwd_total;
+    size_t dSck, Dbar, dqh, dkh, dl, dbeta, part, sched, bwd_total;
 };
 
 bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -113,6 +113,7 @@ Layout make_layout(const gdn::Dims& d) {
     L.dl = o; o = align_up(o + perstep * 4);
     L.dbeta = o; o = align_up(o + perstep * 4);
     L.part = o; o = align_up(o + 2 * (size_t)d.B * d.NC * d.Hv * 4);
+    L.sched = o; o = align_up(o + (1 + (size_t)d.B * d.Hv) * 4);  // item counter, progress
     L.bwd_total = o;
     return L;
 }
@@ -377,14 +378,20 @@ gdn_status backward_impl(const gdn_shape* shape, int gates, const void* q, const
     p.dl = reinterpret_cast<float*>(w + L.dl);
     p.dbeta = reinterpret_cast<float*>(w + L.dbeta);
     p.part = reinterpret_cast<float*>(w + L.part);
+    p.sched = reinterpret_cast<unsigned int*>(w + L.sched);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     gdn::Tmaps maps;
     if (gdn::tc_path(d)) {
         if (!make_tmaps(d, v, d_o, nullptr, nullptr, &maps)) return tmap_error();
         p.tmaps = &maps;
     }
-    cudaError_t e = run_phase("bwd_scan", s, [&] { return gdn::launch_bwd_scan(d, p, s); });
-    if (e == cudaSuccess) e = run_phase("bwd_chunk", s, [&] { return gdn::launch_bwd_chunk(d, p, s); });
+    cudaError_t e;
+    if (p.tmaps && gdn::bwd_fused_tc_supported(d)) {
+        e = run_phase("bwd_scan_chunk", s, [&] { return gdn::launch_bwd_fused_tc(d, p, s); });
+    } else {
+        e = run_phase("bwd_scan", s, [&] { return gdn::launch_bwd_scan(d, p, s); });
+        if (e == cudaSuccess) e = run_phase("bwd_chunk", s, [&] { return gdn::launch_bwd_chunk(d, p, s); });
+    }
     if (e == cudaSuccess) e = run_phase("bwd_reduce", s, [&] { return gdn::launch_bwd_reduce(d, p, s); });
     return cuda_status(e);
 }

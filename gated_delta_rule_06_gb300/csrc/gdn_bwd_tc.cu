@@ -26,6 +26,7 @@
 // bulk copy, and the 64-wide Dk blocks of S / Sbar' stream through one buffer so the
 // next block streams in while the current block's epilogue runs.
 #include "gdn_internal.cuh"
+#include "gdn_scan_ta.cuh"
 #include "gdn_tc.cuh"
 
 namespace gdn {
@@ -259,8 +260,15 @@ __device__ __forceinline__ void cta_sync_tc() {
     tc::tc_fence_after();
 }
 
-__global__ void __launch_bounds__(kThreads + 32, 1)
-    bwd_chunk_tc_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm) {
+// Work items are (chunk, value head, batch) in order of decreasing chunk, the
+// (batch, value head) pairs of a chunk consecutive (the value heads of a key head
+// share their q / k images).  Each CTA takes its next item from the counter
+// *sched (zero before the launch).  progress (null: the inputs are all there):
+// the reverse scan's per-(b, h) count of finished chunks (ntiles value tiles per
+// head); item (c, h, b) waits until it reaches ntiles (NC - c).
+__device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, const Tmaps& tm,
+                                               unsigned int* sched, const unsigned int* progress,
+                                               int ntiles) {
     extern __shared__ __align__(1024) uint8_t sm[];
     // bar: MMA rounds outside phase 1; barM / barE: phase-1 products of block b
     // done / block b's epilogue done (two of each, by block parity); barMa: block
@@ -268,6 +276,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     // barOV, barL, barKQ, barSa / barSb (S / Sbar' halves of a block): arrivals
     __shared__ uint64_t bar, barOV, barL, barKQ, barSa, barSb, barMa, barG, barM[2], barE[2];
     __shared__ uint32_t tmem_base_sh;
+    __shared__ int next_item;
     const int Dk = (int)d.Dk, Dv = (int)d.Dv;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // warps 0-7: epilogues (row quarter warp % 4, column half g); warp 8: loads and MMA issue
@@ -306,9 +315,30 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     float* uf = gbl + C;        // [3][64]
     float* wf = uf + 3 * C;     // [3][64]
 
-    // Persistent: CTA k takes the work items (chunk, value head, batch) k, k + grid,
-    // ... (chunk fastest); the next item's operands load while the current one ends.
+    // Persistent: the next item's operands load while the current one ends.
     const int nitems = (int)(d.NC * d.Hv * d.B);
+    const int nbh = (int)(d.Hv * d.B);
+    auto item_c = [&](int it) { return (int)d.NC - 1 - it / nbh; };
+    auto item_h = [&](int it) { return (it % nbh) % (int)d.Hv; };
+    auto item_b = [&](int it) { return (it % nbh) / (int)d.Hv; };
+    // producer: the reverse scan has finished chunk c of this head (bounded wait)
+    auto wait_ready = [&](int it) -> bool {
+        if (progress == nullptr) return true;
+        const unsigned int* f = progress + (int64_t)item_b(it) * d.Hv + item_h(it);
+        const unsigned int need = (unsigned int)(ntiles * ((int)d.NC - item_c(it)));
+        if (tc::ld_acquire_gpu(f) < need) {
+            const uint64_t t0 = tc::globaltimer_ns();
+            for (uint32_t i = 1; tc::ld_acquire_gpu(f) < need; ++i) {
+                __nanosleep(64);
+                if ((i & 255u) == 0 && tc::globaltimer_ns() - t0 > 1000000000ull) {
+                    atomicOr(&g_err_bwdtc, tc::kErrWaitTimeout);
+                    return false;
+                }
+            }
+        }
+        tc::fence_async_global();  // the images it saw released, before the copies read them
+        return true;
+    };
     __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(p.dv);
     const int64_t ldv = d.Hv * Dv;
     const uint32_t tv = (uint32_t)(C * Dv * 2);         // one 64 x Dv bf16 tile
@@ -338,7 +368,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     // images and the first Sbar' block (its half of the block buffer is not used
     // by phase 0).
     auto issue_loads = [&](int it) {
-        const int c = it % (int)d.NC, h = (it / (int)d.NC) % (int)d.Hv, bb = it / (int)(d.NC * d.Hv);
+        const int c = item_c(it), h = item_h(it), bb = item_b(it);
         const int64_t ci = ((int64_t)bb * d.Hv + h) * d.NC + c;
         tc::mbar_arrive_expect_tx(&barOV, 2 * tv);
         tc::tma_load_5d(sm + L.O, &tm.dOf, 0, c * C, 0, h, bb, &barOV);
@@ -352,7 +382,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
                      C * C * 2, &barL);
     };
     auto issue_loads_kq = [&](int it) {
-        const int c = it % (int)d.NC, h = (it / (int)d.NC) % (int)d.Hv, bb = it / (int)(d.NC * d.Hv);
+        const int c = item_c(it), h = item_h(it), bb = item_b(it);
         const int j = h / (int)d.G;
         const int64_t ci = ((int64_t)bb * d.Hv + h) * d.NC + c;
         const int64_t kqi = ((int64_t)bb * d.Hk + j) * d.NC + c;  // q / k images of this chunk
@@ -379,7 +409,10 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             tc::mbar_init(&barE[i], kThreads);
         }
         tc::fence_mbar_init();
-        if ((int)blockIdx.x < nitems) issue_loads((int)blockIdx.x);
+        const int first = (int)atomicAdd(sched, 1u);
+        next_item = first;
+        if (first < nitems && !wait_ready(first)) next_item = nitems;  // gave up: no item
+        else if (first < nitems) issue_loads(first);
     }
     cta_sync_tc();
     const uint32_t tb = tmem_base_sh;
@@ -390,9 +423,9 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     // producer: an item whose operands are in flight but not yet waited for
     bool pending = false;
     uint32_t pend_pit = 0;
-    for (int it = (int)blockIdx.x; it < nitems; it += (int)gridDim.x, pit ^= 1u, B0 += (uint32_t)nblk) {
+    for (int it = next_item; it < nitems; it = next_item, pit ^= 1u, B0 += (uint32_t)nblk) {
     pending = false;
-    const int c = it % (int)d.NC, h = (it / (int)d.NC) % (int)d.Hv, bb = it / (int)(d.NC * d.Hv);
+    const int c = item_c(it), h = item_h(it), bb = item_b(it);
     const int j = h / (int)d.G;
     const int64_t t0 = (int64_t)c * C;
     const int nvalid = (int)(d.T - t0 < C ? d.T - t0 : C);
@@ -848,12 +881,16 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     // tile of this item is dead and the next item's loads go out, under the
     // final stores below
     sync_after_mma(&bar, phase, ok, epi || prod);
-    if (prod && ok) {
-        const int next = it + (int)gridDim.x;
-        if (next < nitems) {
-            issue_loads(next);
-            pending = true;
-            pend_pit = pit ^ 1u;
+    if (prod) {
+        const int next = (int)atomicAdd(sched, 1u);
+        next_item = next;
+        if (ok && next < nitems) {
+            ok = wait_ready(next);
+            if (ok) {
+                issue_loads(next);
+                pending = true;
+                pend_pit = pit ^ 1u;
+            }
         }
     }
     if (epi && ok) {
@@ -885,6 +922,36 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
 
+__global__ void __launch_bounds__(kThreads + 32, 1)
+    bwd_chunk_tc_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm) {
+    bwd_chunk_body(d, p, tm, p.sched, nullptr, 0);
+}
+
+// The reverse scan and the per-chunk gradients in one cooperative launch (one
+// CTA per SM, all resident at once).  CTAs [0, nscan) first run the reverse scan
+// of one value tile each, publishing every finished chunk; then every CTA takes
+// gradient items, each once the reverse scan has published its chunk for all
+// value tiles of its head.  The scan CTAs never wait on the gradient CTAs, so
+// every wait ends; the SMs the scan leaves idle run gradient items meanwhile.
+__global__ void __launch_bounds__(kThreads + 32, 1)
+    bwd_fused_tc_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm) {
+    const int ntiles = (int)(d.Dv / ta::DVT);
+    const int nscan = ntiles * (int)(d.Hv * d.B);
+    unsigned int* progress = p.sched + 1;
+    const int t = (int)blockIdx.x;
+    if (t < nscan) {
+        ta::bwd_scan_ta_body(d, p, tm, t % ntiles, (t / ntiles) % (int)d.Hv, t / (ntiles * (int)d.Hv),
+                             &g_err_bwdtc, progress, false);
+        __syncthreads();
+    }
+    bwd_chunk_body(d, p, tm, p.sched, progress, ntiles);
+}
+
+size_t fused_smem(const Dims& d) {
+    const uint32_t a = smem_plan((int)d.Dk, (int)d.Dv).total, b = ta::tb_plan((int)d.Dk).total;
+    return (size_t)(a > b ? a : b) + 1024;  // slack for the 1024-byte alignment of the base
+}
+
 }  // namespace
 
 bool bwd_chunk_tc_supported(const Dims& d) {
@@ -903,9 +970,45 @@ cudaError_t launch_bwd_chunk_tc(const Dims& d, const Ptrs& p, cudaStream_t s) {
     // persistent: one CTA per SM (the shared memory allows no second one)
     const int64_t nitems = d.NC * d.Hv * d.B;
     const int grid = (int)(nitems < sm_count() ? nitems : sm_count());
+    e = cudaMemsetAsync(p.sched, 0, sizeof(unsigned int), s);  // the item counter
+    if (e != cudaSuccess) return e;
     kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps);
     count_launches(1);
     return cudaPeekAtLastError();
+}
+
+bool bwd_fused_tc_supported(const Dims& d) {
+    if (!bwd_chunk_tc_supported(d) || !scan_ta_supported(d)) return false;
+    if (fused_smem(d) + 1024 > 227u * 1024u) return false;
+    // the reverse scan's CTAs leave SMs to the gradient items from the start
+    const int64_t nscan = (d.Dv / ta::DVT) * d.Hv * d.B;
+    int dev = 0, coop = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop)
+        return false;
+    return nscan + 8 <= sm_count();
+}
+
+cudaError_t launch_bwd_fused_tc(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    const size_t smem = fused_smem(d);
+    auto kern = bwd_fused_tc_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads + 32, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+    // the item counter and the per-(b, h) progress counts start at zero
+    e = cudaMemsetAsync(p.sched, 0, (size_t)(1 + d.B * d.Hv) * sizeof(unsigned int), s);
+    if (e != cudaSuccess) return e;
+    Dims dd = d;
+    Ptrs pp = p;
+    Tmaps tm = *p.tmaps;
+    void* args[] = {&dd, &pp, &tm};
+    e = cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)sm_count()),
+                                    dim3(kThreads + 32), args, smem, s);
+    count_launches(1);
+    return e;
 }
 
 }  // namespace gdn

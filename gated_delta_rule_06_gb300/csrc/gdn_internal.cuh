@@ -105,6 +105,8 @@ struct Ptrs {
     float* dl;     // [B, Hv, Tp] cotangent of the log-decay
     float* dbeta;  // [B, Hv, Tp]
     float* part;   // [2, B, NC, Hv] per-chunk partial sums for dA_log, ddt_bias
+    unsigned int* sched;  // tensor-core path: [1 + B Hv] the gradient kernel's item
+                          // counter, then the reverse scan's per-(b, h) progress
     // host copy of the tensor maps (tensor-core path; read by the launchers only)
     const Tmaps* tmaps;
 };
@@ -186,6 +188,10 @@ unsigned int read_clear_error_decode();
 // tensor-core (tcgen05) variants for bf16 inputs
 bool bwd_chunk_tc_supported(const Dims& d);
 cudaError_t launch_bwd_chunk_tc(const Dims& d, const Ptrs& p, cudaStream_t s);
+// the reverse scan and the gradient kernel in one cooperative launch (bf16,
+// shapes both tensor-core kernels take, fewer reverse-scan tiles than SMs)
+bool bwd_fused_tc_supported(const Dims& d);
+cudaError_t launch_bwd_fused_tc(const Dims& d, const Ptrs& p, cudaStream_t s);
 unsigned int read_clear_error_bwdtc();
 bool scan_tc_supported(const Dims& d);
 cudaError_t launch_fwd_scan_tc(const Dims& d, const Ptrs& p, cudaStream_t s);

@@ -188,6 +188,19 @@ __device__ __forceinline__ void bulk_wait_read_but1() {
 }
 // this thread's bulk stores are complete
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// load with acquire semantics at GPU scope (pairs with a release by another CTA)
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// ... all but the most recent committed group
+__device__ __forceinline__ void bulk_wait_but1() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }
+// global-memory accesses of the generic proxy (an acquire that saw another CTA's
+// release) ordered before this thread's later bulk / tensor copies
+__device__ __forceinline__ void fence_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 // ---- tensor (TMA) loads -----------------------------------------------------------
 // 5-d tiled load of the box at coordinates c0..c4 of the tensor map `map` (the
