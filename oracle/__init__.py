@@ -73,6 +73,10 @@ def _load():
         lib.gdn_oracle_forward_lb.restype = ctypes.c_int
         lib.gdn_oracle_backward_lb.argtypes = [i64] * 6 + [dp] * 15
         lib.gdn_oracle_backward_lb.restype = ctypes.c_int
+        lib.gdn_oracle_forward_kc.argtypes = [i64] * 6 + [dp] * 9
+        lib.gdn_oracle_forward_kc.restype = ctypes.c_int
+        lib.gdn_oracle_backward_kc.argtypes = [i64] * 6 + [dp] * 15
+        lib.gdn_oracle_backward_kc.restype = ctypes.c_int
         lib.gdn_oracle_causal_conv1d_update.argtypes = [i64] * 4 + [dp] * 5
         lib.gdn_oracle_causal_conv1d_update.restype = ctypes.c_int
         lib.gdn_oracle_threads.argtypes = []
@@ -204,6 +208,46 @@ def backward_lb(q, k, v, log_decay, beta, state0, mask, d_o, d_state_T=None):
 
 
 GRAD_NAMES_LB = ("dq", "dk", "dv", "d_log_decay", "d_beta", "dstate0")
+
+
+def forward_kc(q, k, v, log_decay, beta, state0=None, mask=None):
+    """Sequential recurrence with one decay per key channel (the mlx-lm page's
+    vectorised gating, g.ndim == 4): log_decay [B, T, Hv, Dk], beta [B, T, Hv].
+    An applied step scales row i of the state by exp(log_decay[..., i]).
+    Returns (o, state_T)."""
+    q, k, v, log_decay, beta, state0 = map(_f64, (q, k, v, log_decay, beta, state0))
+    mask = _u8(mask)
+    B, T, Hk, Hv, Dk, Dv = _dims(q, v)
+    o = np.zeros((B, T, Hv, Dv))
+    sT = np.zeros((B, Hv, Dk, Dv))
+    rc = _load().gdn_oracle_forward_kc(B, T, Hk, Hv, Dk, Dv, *map(_ptr, (
+        q, k, v, log_decay, beta, state0, mask, o, sT)))
+    if rc:
+        raise ValueError(f"oracle forward_kc rejected the shapes (code {rc})")
+    return o, sT
+
+
+def backward_kc(q, k, v, log_decay, beta, state0, mask, d_o, d_state_T=None):
+    """VJP of forward_kc.  Returns a dict with dq, dk, dv, d_log_decay
+    ([B, T, Hv, Dk]), d_beta ([B, T, Hv]) and dstate0; gate cotangents are zero
+    on masked steps."""
+    q, k, v, log_decay, beta, state0, d_o, d_state_T = map(
+        _f64, (q, k, v, log_decay, beta, state0, d_o, d_state_T))
+    mask = _u8(mask)
+    B, T, Hk, Hv, Dk, Dv = _dims(q, v)
+    out = dict(
+        dq=np.zeros(q.shape), dk=np.zeros(k.shape), dv=np.zeros(v.shape),
+        d_log_decay=np.zeros(log_decay.shape), d_beta=np.zeros(beta.shape),
+        dstate0=np.zeros((B, Hv, Dk, Dv)))
+    rc = _load().gdn_oracle_backward_kc(B, T, Hk, Hv, Dk, Dv, *map(_ptr, (
+        q, k, v, log_decay, beta, state0, mask, d_o, d_state_T,
+        out["dq"], out["dk"], out["dv"], out["d_log_decay"], out["d_beta"], out["dstate0"])))
+    if rc:
+        raise ValueError(f"oracle backward_kc rejected the shapes (code {rc})")
+    return out
+
+
+GRAD_NAMES_KC = GRAD_NAMES_LB
 
 
 def causal_conv1d_update(hidden, conv_state, weight):

@@ -357,6 +357,46 @@ int gdn_oracle_forward_chunked(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int
  *            db = betabar * beta (1 - beta);
  *            dA_log[h] = sum_{b,t} lbar * l;  ddt_bias[h] = sum_{b,t} da
  */
+/* After the per-(b, h) reverse passes: zero dv on masked steps, then the GQA
+ * sum and the L2-norm backward of q and k (see the comment above
+ * backward_core), per (b, t, key head) in a fixed order. */
+static void qk_finish(const dims_t* dd, const double* q, const double* k, const uint8_t* mask,
+                      const double* dqh, const double* dkh, double* dq, double* dk, double* dv) {
+    const dims_t d = *dd;
+    const int64_t B = d.B, T = d.T, Hk = d.Hk, Hv = d.Hv, Dk = d.Dk, Dv = d.Dv;
+    int64_t G = Hv / Hk;
+    /* v gradient is zero on masked steps */
+    if (mask)
+        for (int64_t bb = 0; bb < B; ++bb)
+            for (int64_t t = 0; t < T; ++t)
+                if (!mask[bb * T + t])
+                    for (int64_t h = 0; h < Hv; ++h)
+                        memset(dv + IV(&d, bb, t, h), 0, sizeof(double) * Dv);
+    /* GQA sum + L2-norm backward, per (b, t, key head) */
+    double* acc = malloc(sizeof(double) * Dk);
+    double sq = 1.0 / sqrt((double)Dk);
+    for (int64_t bb = 0; bb < B; ++bb)
+        for (int64_t t = 0; t < T; ++t)
+            for (int64_t j = 0; j < Hk; ++j) {
+                for (int pass = 0; pass < 2; ++pass) {
+                    const double* x = (pass == 0 ? q : k) + IQK(&d, bb, t, j);
+                    const double* src = pass == 0 ? dqh : dkh;
+                    double* dst = (pass == 0 ? dq : dk) + IQK(&d, bb, t, j);
+                    double s = pass == 0 ? sq : 1.0;
+                    for (int64_t r = 0; r < Dk; ++r) acc[r] = 0.0;
+                    for (int64_t h = j * G; h < (j + 1) * G; ++h) {
+                        const double* y = src + ((bb * T + t) * Hv + h) * Dk;
+                        for (int64_t r = 0; r < Dk; ++r) acc[r] += y[r];
+                    }
+                    double rn = inv_norm(x, Dk); /* 1/n */
+                    double uy = 0.0;
+                    for (int64_t r = 0; r < Dk; ++r) uy += x[r] * rn * acc[r];
+                    for (int64_t r = 0; r < Dk; ++r) dst[r] = s * rn * (acc[r] - x[r] * rn * uy);
+                }
+            }
+    free(acc);
+}
+
 /* The VJP up to the gates: dq, dk, dv, dstate0 and the per-step cotangents
  * dlg of l = log g and dbt of beta ([B, T, Hv], zero on masked steps). */
 static int backward_core(const dims_t* dd, const double* q, const double* k, const double* v,
@@ -365,8 +405,7 @@ static int backward_core(const dims_t* dd, const double* q, const double* k, con
                          double* dq, double* dk, double* dv, double* dlg, double* dbt,
                          double* dstate0) {
     const dims_t d = *dd;
-    const int64_t B = d.B, T = d.T, Hk = d.Hk, Hv = d.Hv, Dk = d.Dk, Dv = d.Dv;
-    int64_t G = Hv / Hk;
+    const int64_t B = d.B, T = d.T, Hv = d.Hv, Dk = d.Dk, Dv = d.Dv;
     int64_t SS = Dk * Dv;
     int64_t nseg = (T + SEGMENT - 1) / SEGMENT;
     /* per value head gradients of the normalised q / k */
@@ -498,36 +537,7 @@ static int backward_core(const dims_t* dd, const double* q, const double* k, con
         free(seg); free(hist); free(Sb); free(Sa); free(qh); free(kh);
         free(p); free(dl); free(dbar); free(pbar); free(S);
     }
-    /* v gradient is zero on masked steps */
-    if (mask)
-        for (int64_t bb = 0; bb < B; ++bb)
-            for (int64_t t = 0; t < T; ++t)
-                if (!mask[bb * T + t])
-                    for (int64_t h = 0; h < Hv; ++h)
-                        memset(dv + IV(&d, bb, t, h), 0, sizeof(double) * Dv);
-    /* GQA sum + L2-norm backward, per (b, t, key head) */
-    double* acc = malloc(sizeof(double) * Dk);
-    double sq = 1.0 / sqrt((double)Dk);
-    for (int64_t bb = 0; bb < B; ++bb)
-        for (int64_t t = 0; t < T; ++t)
-            for (int64_t j = 0; j < Hk; ++j) {
-                for (int pass = 0; pass < 2; ++pass) {
-                    const double* x = (pass == 0 ? q : k) + IQK(&d, bb, t, j);
-                    const double* src = pass == 0 ? dqh : dkh;
-                    double* dst = (pass == 0 ? dq : dk) + IQK(&d, bb, t, j);
-                    double s = pass == 0 ? sq : 1.0;
-                    for (int64_t r = 0; r < Dk; ++r) acc[r] = 0.0;
-                    for (int64_t h = j * G; h < (j + 1) * G; ++h) {
-                        const double* y = src + ((bb * T + t) * Hv + h) * Dk;
-                        for (int64_t r = 0; r < Dk; ++r) acc[r] += y[r];
-                    }
-                    double rn = inv_norm(x, Dk); /* 1/n */
-                    double uy = 0.0;
-                    for (int64_t r = 0; r < Dk; ++r) uy += x[r] * rn * acc[r];
-                    for (int64_t r = 0; r < Dk; ++r) dst[r] = s * rn * (acc[r] - x[r] * rn * uy);
-                }
-            }
-    free(acc);
+    qk_finish(&d, q, k, mask, dqh, dkh, dq, dk, dv);
     free(dqh); free(dkh);
     return 0;
 }
@@ -587,6 +597,202 @@ int gdn_oracle_backward_lb(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t
     if (rc) return rc;
     return backward_core(&d, q, k, v, log_decay_, beta, state0, mask, d_o, d_state_T, dq, dk,
                          dv, d_log_decay, d_beta, dstate0);
+}
+
+/* ---- per-key-channel gates ------------------------------------------------
+ * The vectorised gating the mlx-lm page lists (g.ndim == 4: one decay per key
+ * channel), in the op contract's log_decay form extended by the key-channel
+ * axis: log_decay [B, T, Hv, Dk] holds l_{t,i} = log g_{t,i}, beta [B, T, Hv].
+ * An applied step scales row i of S (key channel i) by g_{t,i}:
+ *     S_a = diag(g) S_prev,  p = S_a^T k,  delta = beta (v - p),  S = S_a + k delta^T,
+ * and its VJP is the scalar one above with diag(g) in place of g:
+ *     Sbar_prev = diag(g) Sbar_a,   lbar_i = g_i sum_c Sbar_a[i, c] S_prev[i, c].
+ * Written apart from the scalar path (not through it), so that with equal
+ * channels the two agree only through the mathematics. */
+#define IGK(d, b, t, h) ((((b) * (d)->T + (t)) * (d)->Hv + (h)) * (d)->Dk)
+
+static void apply_step_kc(int64_t Dk, int64_t Dv, double* S, const double* g, double beta,
+                          const double* kh, const double* v, double* p, double* dl) {
+    for (int64_t r = 0; r < Dk; ++r)
+        for (int64_t c = 0; c < Dv; ++c) S[r * Dv + c] *= g[r];
+    for (int64_t c = 0; c < Dv; ++c) p[c] = 0.0;
+    for (int64_t r = 0; r < Dk; ++r)
+        for (int64_t c = 0; c < Dv; ++c) p[c] += S[r * Dv + c] * kh[r];
+    for (int64_t c = 0; c < Dv; ++c) dl[c] = beta * (v[c] - p[c]);
+    for (int64_t r = 0; r < Dk; ++r)
+        for (int64_t c = 0; c < Dv; ++c) S[r * Dv + c] += kh[r] * dl[c];
+}
+
+int gdn_oracle_forward_kc(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk, int64_t Dv,
+                          const double* q, const double* k, const double* v,
+                          const double* log_decay_, const double* beta, const double* state0,
+                          const uint8_t* mask, double* o, double* state_T) {
+    dims_t d = {B, T, Hk, Hv, Dk, Dv};
+    int rc = check_dims(&d);
+    if (rc) return rc;
+    int64_t npairs = B * Hv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t pr = 0; pr < npairs; ++pr) {
+        int64_t bb = pr / Hv, h = pr % Hv;
+        double* S = state_T + IS(&d, bb, h);
+        if (state0)
+            memcpy(S, state0 + IS(&d, bb, h), sizeof(double) * Dk * Dv);
+        else
+            memset(S, 0, sizeof(double) * Dk * Dv);
+        double* qh = malloc(sizeof(double) * Dk);
+        double* kh = malloc(sizeof(double) * Dk);
+        double* g = malloc(sizeof(double) * Dk);
+        double* p = malloc(sizeof(double) * Dv);
+        double* dl = malloc(sizeof(double) * Dv);
+        for (int64_t t = 0; t < T; ++t) {
+            load_qk_hat(&d, q, k, bb, t, h, qh, kh);
+            int on = mask ? (mask[bb * T + t] != 0) : 1;
+            if (on) {
+                for (int64_t r = 0; r < Dk; ++r) g[r] = exp(log_decay_[IGK(&d, bb, t, h) + r]);
+                apply_step_kc(Dk, Dv, S, g, beta[IG(&d, bb, t, h)], kh, v + IV(&d, bb, t, h), p, dl);
+            }
+            read_out(Dk, Dv, S, qh, o + IV(&d, bb, t, h));
+        }
+        free(qh); free(kh); free(g); free(p); free(dl);
+    }
+    return 0;
+}
+
+/* d_log_decay [B, T, Hv, Dk] and d_beta [B, T, Hv] (zero on masked steps), with
+ * dq, dk, dv and dstate0 as in gdn_oracle_backward. */
+int gdn_oracle_backward_kc(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk, int64_t Dv,
+                           const double* q, const double* k, const double* v,
+                           const double* log_decay_, const double* beta_, const double* state0,
+                           const uint8_t* mask, const double* d_o, const double* d_state_T,
+                           double* dq, double* dk, double* dv, double* d_log_decay,
+                           double* d_beta, double* dstate0) {
+    dims_t d = {B, T, Hk, Hv, Dk, Dv};
+    int rc = check_dims(&d);
+    if (rc) return rc;
+    int64_t SS = Dk * Dv;
+    int64_t nseg = (T + SEGMENT - 1) / SEGMENT;
+    double* dqh = calloc((size_t)(B * T * Hv * Dk > 0 ? B * T * Hv * Dk : 1), sizeof(double));
+    double* dkh = calloc((size_t)(B * T * Hv * Dk > 0 ? B * T * Hv * Dk : 1), sizeof(double));
+    if (!dqh || !dkh) { free(dqh); free(dkh); return 3; }
+    memset(d_log_decay, 0, sizeof(double) * B * T * Hv * Dk);
+    memset(d_beta, 0, sizeof(double) * B * T * Hv);
+    int64_t npairs = B * Hv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t pr = 0; pr < npairs; ++pr) {
+        int64_t bb = pr / Hv, h = pr % Hv;
+        double* seg = malloc(sizeof(double) * SS * (nseg > 0 ? nseg : 1));
+        double* hist = malloc(sizeof(double) * SS * (SEGMENT + 1));
+        double* Sb = malloc(sizeof(double) * SS);
+        double* Sa = malloc(sizeof(double) * SS);
+        double* S = malloc(sizeof(double) * SS);
+        double* qh = malloc(sizeof(double) * Dk);
+        double* kh = malloc(sizeof(double) * Dk);
+        double* g = malloc(sizeof(double) * Dk);
+        double* p = malloc(sizeof(double) * Dv);
+        double* dl = malloc(sizeof(double) * Dv);
+        double* dbar = malloc(sizeof(double) * Dv);
+        double* pbar = malloc(sizeof(double) * Dv);
+        if (state0)
+            memcpy(S, state0 + IS(&d, bb, h), sizeof(double) * SS);
+        else
+            memset(S, 0, sizeof(double) * SS);
+        for (int64_t t = 0; t < T; ++t) {  /* segment-start states */
+            if (t % SEGMENT == 0) memcpy(seg + (t / SEGMENT) * SS, S, sizeof(double) * SS);
+            if (mask && !mask[bb * T + t]) continue;
+            load_qk_hat(&d, q, k, bb, t, h, qh, kh);
+            for (int64_t r = 0; r < Dk; ++r) g[r] = exp(log_decay_[IGK(&d, bb, t, h) + r]);
+            apply_step_kc(Dk, Dv, S, g, beta_[IG(&d, bb, t, h)], kh, v + IV(&d, bb, t, h), p, dl);
+        }
+        if (d_state_T)
+            memcpy(Sb, d_state_T + IS(&d, bb, h), sizeof(double) * SS);
+        else
+            memset(Sb, 0, sizeof(double) * SS);
+        for (int64_t sg = nseg - 1; sg >= 0; --sg) {
+            int64_t t0 = sg * SEGMENT;
+            int64_t L = (T - t0) < SEGMENT ? (T - t0) : SEGMENT;
+            memcpy(hist, seg + sg * SS, sizeof(double) * SS);
+            for (int64_t i = 0; i < L; ++i) {
+                int64_t t = t0 + i;
+                double* Sn = hist + (i + 1) * SS;
+                memcpy(Sn, hist + i * SS, sizeof(double) * SS);
+                if (mask && !mask[bb * T + t]) continue;
+                load_qk_hat(&d, q, k, bb, t, h, qh, kh);
+                for (int64_t r = 0; r < Dk; ++r) g[r] = exp(log_decay_[IGK(&d, bb, t, h) + r]);
+                apply_step_kc(Dk, Dv, Sn, g, beta_[IG(&d, bb, t, h)], kh, v + IV(&d, bb, t, h), p, dl);
+            }
+            for (int64_t i = L - 1; i >= 0; --i) {
+                int64_t t = t0 + i;
+                const double* Sprev = hist + i * SS;
+                const double* Scur = hist + (i + 1) * SS;
+                const double* ob = d_o + IV(&d, bb, t, h);
+                double* qbar = dqh + ((bb * T + t) * Hv + h) * Dk;
+                double* kbar = dkh + ((bb * T + t) * Hv + h) * Dk;
+                load_qk_hat(&d, q, k, bb, t, h, qh, kh);
+                for (int64_t r = 0; r < Dk; ++r) {  /* o = S^T q */
+                    double acc = 0.0;
+                    for (int64_t c = 0; c < Dv; ++c) {
+                        Sb[r * Dv + c] += qh[r] * ob[c];
+                        acc += Scur[r * Dv + c] * ob[c];
+                    }
+                    qbar[r] = acc;
+                }
+                if (mask && !mask[bb * T + t]) continue;
+                double beta = beta_[IG(&d, bb, t, h)];
+                const double* vt = v + IV(&d, bb, t, h);
+                for (int64_t r = 0; r < Dk; ++r) g[r] = exp(log_decay_[IGK(&d, bb, t, h) + r]);
+                /* S_a = diag(g) S_prev, p = S_a^T k, delta = beta (v - p) */
+                for (int64_t r = 0; r < Dk; ++r)
+                    for (int64_t c = 0; c < Dv; ++c) Sa[r * Dv + c] = g[r] * Sprev[r * Dv + c];
+                for (int64_t c = 0; c < Dv; ++c) p[c] = 0.0;
+                for (int64_t r = 0; r < Dk; ++r)
+                    for (int64_t c = 0; c < Dv; ++c) p[c] += Sa[r * Dv + c] * kh[r];
+                for (int64_t c = 0; c < Dv; ++c) dl[c] = beta * (vt[c] - p[c]);
+                /* S = S_a + k delta^T */
+                for (int64_t r = 0; r < Dk; ++r) {
+                    double acc = 0.0;
+                    for (int64_t c = 0; c < Dv; ++c) acc += Sb[r * Dv + c] * dl[c];
+                    kbar[r] = acc;
+                }
+                for (int64_t c = 0; c < Dv; ++c) {
+                    double acc = 0.0;
+                    for (int64_t r = 0; r < Dk; ++r) acc += Sb[r * Dv + c] * kh[r];
+                    dbar[c] = acc;
+                }
+                /* delta = beta (v - p) */
+                double betabar = 0.0;
+                double* vbar = dv + IV(&d, bb, t, h);
+                for (int64_t c = 0; c < Dv; ++c) {
+                    vbar[c] = beta * dbar[c];
+                    betabar += dbar[c] * (vt[c] - p[c]);
+                    pbar[c] = -beta * dbar[c];
+                }
+                /* p = S_a^T k */
+                for (int64_t r = 0; r < Dk; ++r) {
+                    double acc = 0.0;
+                    for (int64_t c = 0; c < Dv; ++c) {
+                        Sb[r * Dv + c] += kh[r] * pbar[c];
+                        acc += Sa[r * Dv + c] * pbar[c];
+                    }
+                    kbar[r] += acc;
+                }
+                /* S_a = diag(g) S_prev: one log-decay cotangent per key channel */
+                double* lbar = d_log_decay + IGK(&d, bb, t, h);
+                for (int64_t r = 0; r < Dk; ++r) {
+                    double gb = 0.0;
+                    for (int64_t c = 0; c < Dv; ++c) gb += Sb[r * Dv + c] * Sprev[r * Dv + c];
+                    lbar[r] = gb * g[r];
+                    for (int64_t c = 0; c < Dv; ++c) Sb[r * Dv + c] *= g[r];
+                }
+                d_beta[IG(&d, bb, t, h)] = betabar;
+            }
+        }
+        memcpy(dstate0 + IS(&d, bb, h), Sb, sizeof(double) * SS);
+        free(seg); free(hist); free(Sb); free(Sa); free(S); free(qh); free(kh); free(g);
+        free(p); free(dl); free(dbar); free(pbar);
+    }
+    qk_finish(&d, q, k, mask, dqh, dkh, dq, dk, dv);
+    free(dqh); free(dkh);
+    return 0;
 }
 
 /* ---- causal conv1d update ------------------------------------------------ */

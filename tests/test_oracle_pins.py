@@ -435,6 +435,90 @@ def test_lb_matches_gate_form_and_chain_rule():
         assert np.all(g2["d_log_decay"][off] == 0) and np.all(g2["d_beta"][off] == 0)
 
 
+# -- per-key-channel gates (the mlx-lm page's vectorised gating, g.ndim == 4) --
+
+def _kc_inputs(B, T, Hk, Hv, Dk, Dv, seed, masked=False):
+    x = _lb_inputs(B, T, Hk, Hv, Dk, Dv, seed, masked)
+    r = np.random.default_rng(seed + 1000)
+    x["log_decay"] = -r.uniform(0.0, 2.0, (B, T, Hv, Dk))
+    return x
+
+
+def _kc_loss(x):
+    o, sT = oracle.forward_kc(x["q"], x["k"], x["v"], x["log_decay"], x["beta"], x["state0"],
+                              x["mask"])
+    return float((o * x["d_o"]).sum() + (sT * x["d_state_T"]).sum())
+
+
+@pytest.mark.parametrize("masked", [False, True])
+def test_kc_fd_all_grads(masked):
+    """Central differences of L = <o, dO> + <S_T, dS_T> through the per-channel
+    form: every input, one log-decay cotangent per key channel (GQA G = 2,
+    T = 67 over two 64-step segments, optional mask)."""
+    x = _kc_inputs(2, 67, 1, 2, 6, 4, seed=61 + masked, masked=masked)
+    g = oracle.backward_kc(x["q"], x["k"], x["v"], x["log_decay"], x["beta"], x["state0"],
+                           x["mask"], x["d_o"], x["d_state_T"])
+    h = 2.0 ** -17
+    rng = np.random.default_rng(7)
+    names = dict(q="dq", k="dk", v="dv", log_decay="d_log_decay", beta="d_beta",
+                 state0="dstate0")
+    for name, gname in names.items():
+        flat = x[name].reshape(-1)
+        idx = rng.choice(flat.size, min(flat.size, 24), replace=False)
+        if masked and name in ("log_decay", "beta"):  # include masked steps
+            idx = np.concatenate([idx, [flat.size - 1, flat.size - 5]])
+        fd = np.zeros(len(idx))
+        for n, i in enumerate(idx):
+            old = flat[i]
+            flat[i] = old + h
+            lp = _kc_loss(x)
+            flat[i] = old - h
+            lm = _kc_loss(x)
+            flat[i] = old
+            fd[n] = (lp - lm) / (2 * h)
+        an = g[gname].reshape(-1)[idx]
+        assert np.abs(an - fd).max() <= 1e-7 * max(np.abs(fd).max(), 1.0), name
+    if masked:
+        off = x["mask"] == 0
+        assert np.all(g["d_log_decay"][off] == 0) and np.all(g["d_beta"][off] == 0)
+
+
+def test_kc_equal_channels_is_the_scalar_form():
+    """With the same log-decay on every key channel the per-channel recurrence is
+    the scalar one (written separately in the oracle): o, S_T, dq, dk, dv, d_beta
+    and dstate0 agree, and the per-channel log-decay cotangents sum to the
+    scalar one."""
+    x = _lb_inputs(2, 70, 2, 4, 5, 3, seed=71, masked=True)
+    lk = np.repeat(x["log_decay"][..., None], 5, axis=-1)
+    o1, s1 = oracle.forward_lb(x["q"], x["k"], x["v"], x["log_decay"], x["beta"], x["state0"],
+                               x["mask"])
+    o2, s2 = oracle.forward_kc(x["q"], x["k"], x["v"], lk, x["beta"], x["state0"], x["mask"])
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(s2, s1, rtol=0, atol=1e-12)
+    g1 = oracle.backward_lb(x["q"], x["k"], x["v"], x["log_decay"], x["beta"], x["state0"],
+                            x["mask"], x["d_o"], x["d_state_T"])
+    g2 = oracle.backward_kc(x["q"], x["k"], x["v"], lk, x["beta"], x["state0"], x["mask"],
+                            x["d_o"], x["d_state_T"])
+    for n in ("dq", "dk", "dv", "d_beta", "dstate0"):
+        np.testing.assert_allclose(g2[n], g1[n], rtol=0, atol=1e-10 * max(1.0, np.abs(g1[n]).max()))
+    np.testing.assert_allclose(g2["d_log_decay"].sum(-1), g1["d_log_decay"], rtol=0,
+                               atol=1e-10 * max(1.0, np.abs(g1["d_log_decay"]).max()))
+
+
+def test_kc_channel_reset_and_freeze_closed_forms():
+    """Key channel 0 with log_decay = -800 (g = 0 in fp64) and the others at 0
+    (g = 1), beta = 0: row 0 of the state is cleared at the first step and every
+    other row keeps its start value, S_T = diag(0, 1, ..., 1) S_0."""
+    x = _kc_inputs(1, 6, 1, 2, 4, 3, seed=81)
+    ld = np.zeros_like(x["log_decay"])
+    ld[..., 0] = -800.0
+    zero = np.zeros_like(x["beta"])
+    _, sT = oracle.forward_kc(x["q"], x["k"], x["v"], ld, zero, x["state0"])
+    want = x["state0"].copy()
+    want[:, :, 0, :] = 0.0
+    np.testing.assert_array_equal(sT, want)
+
+
 # -- the causal conv1d update (torch-to-nnef page, CausalConvUpdateReified) -----
 
 def _silu(x):
