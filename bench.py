@@ -68,7 +68,7 @@ def _peaks():
 # algorithmic work model (per launch of each phase)
 # ---------------------------------------------------------------------------
 
-def work_model(w, conv_k=0):
+def work_model(w, conv_k=0, gates="ab"):
     """Per-phase algorithmic flops and bytes of one fwd+bwd step, in the storage
     formats the kernels use: bf16 inputs keep the saved intermediates as bf16
     operand images (checkpoints, T, W, P, Delta as hi + lo, state cotangents,
@@ -137,6 +137,28 @@ def work_model(w, conv_k=0):
     m["_step"] = dict(bytes=io_fwd + io_bwd + ckpt,
                       flops=sum(m[k]["flops"] for k in ("fwd_chunk", "fwd_scan", "bwd_scan",
                                                         "bwd_chunk")))
+    if gates == "kc":
+        # per-key-channel gates: the CUDA-core recurrence.  Per (b, t, h): forward
+        # decay, prediction, update and read-out, 7 Dk Dv flops; backward: the
+        # segment recompute (5 Dk Dv) and the reverse step (~15 Dk Dv).  Bytes:
+        # fp32 states every 8 steps written and read back, and the per-16-column
+        # tile partials of the q / k / log-decay cotangents (fp32).
+        nt, NS = Dv // 16, (T + 7) // 8
+        tok = B * T * Hv
+        gin = B * T * Hv * (Dk + 1) * es  # log_decay [.., Dk] and beta
+        io_in = 2 * B * T * Hk * Dk * es + B * T * Hv * Dv * es + gin
+        ck = BH * NS * Dk * Dv * 4
+        part = BH * nt * Tp * (3 * Dk + 1) * 4
+        m["prep"] = dict(flops=0.0, bytes=2 * B * T * Hk * Dk * es + 2 * BHk * Tp * 4)
+        m["kc_fwd"] = dict(flops=7.0 * tok * Dk * Dv,
+                           bytes=io_in + B * T * Hv * Dv * es + 2 * BH * Dk * Dv * 4 + ck)
+        m["kc_bwd"] = dict(flops=20.0 * tok * Dk * Dv,
+                           bytes=io_in + 2 * B * T * Hv * Dv * es + ck + part
+                           + BH * nt * Tp * (Dk + 1) * 4 + gin + 2 * BH * Dk * Dv * 4)
+        m["bwd_reduce"] = dict(flops=0.0, bytes=2 * BH * nt * Tp * Dk * 4 + 4 * B * T * Hk * Dk * es)
+        m["_step"] = dict(bytes=2 * io_in + 2 * B * T * Hv * Dv * es + gin + 2 * ck
+                          + 4 * B * T * Hk * Dk * es + 4 * BH * Dk * Dv * 4,
+                          flops=m["kc_fwd"]["flops"] + m["kc_bwd"]["flops"])
     return m
 
 
@@ -251,8 +273,8 @@ def make_inputs(w, gates="ab"):
     per-step log_decay and beta (torch-to-nnef page, op contract) instead of
     a, b, A_log, dt_bias."""
     x = wl.make_inputs(w)
-    if gates == "lb":
-        x.update(wl.make_lb_gates(w))
+    if gates in ("lb", "kc"):
+        x.update(wl.make_lb_gates(w) if gates == "lb" else wl.make_kc_gates(w))
         for n in ("a", "b", "A_log", "dt_bias"):
             x.pop(n)
     return x
@@ -295,9 +317,10 @@ def run_oracle_step(sub, backward):
         oracle.causal_conv1d_update(sub["hidden"], sub["conv_state"], sub["conv_weight"])
     if "log_decay" in sub:
         args = [sub[n] for n in ("q", "k", "v", "log_decay", "beta", "state0", "mask")]
-        oracle.forward_lb(*args)
+        kc = sub["log_decay"].dim() == 4  # one decay per key channel
+        (oracle.forward_kc if kc else oracle.forward_lb)(*args)
         if backward:
-            oracle.backward_lb(*args, sub["d_o"], sub["d_state_T"])
+            (oracle.backward_kc if kc else oracle.backward_lb)(*args, sub["d_o"], sub["d_state_T"])
     else:
         args = [sub[n] for n in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "state0", "mask")]
         oracle.forward(*args)
@@ -364,6 +387,8 @@ def config_of(w, gates="ab", conv_k=0):
                      f"fwd (decode step, {conv_k}-tap short convolution fused in front)" if conv_k
                      else "fwd (decode step)"),
             "gates": ("log_decay, beta (gdn_forward_lb / gdn_backward_lb)" if gates == "lb"
+                      else "per-key-channel log_decay [B, T, Hv, Dk], beta (gdn_forward_kc / "
+                      "gdn_backward_kc, CUDA-core recurrence)" if gates == "kc"
                       else "a, b, A_log, dt_bias"),
             "l2": "flushed between timed steps (256 MiB write outside the events)",
             "phase_times": "a second pass over the same steps with per-phase CUDA events "
@@ -387,7 +412,8 @@ def run_ours(args, w, world, rank, local):
                     ("total_ms", ctypes.c_double)]
 
     dev = torch.device("cuda", local)
-    lb = args.gates == "lb"
+    lb = args.gates in ("lb", "kc")
+    kc = args.gates == "kc"
     x = make_inputs(w, args.gates)
     conv_k = args.fused_conv
     if conv_k:  # the mixed projection and its convolution replace q, k, v
@@ -411,9 +437,14 @@ def run_ours(args, w, world, rank, local):
     if conv_k:
         fo["final_conv_state"] = torch.empty_like(xd["conv_state"])
     if backward:
-        fo["saved"] = torch.empty(ops.saved_bytes(shape), dtype=torch.uint8, device=dev)
-        fo["ws"] = torch.empty(ops.workspace_bytes(shape, 0), dtype=torch.uint8, device=dev)
-        bo = {"ws": torch.empty(ops.workspace_bytes(shape, 1), dtype=torch.uint8, device=dev)}
+        if kc:
+            sv, wf, wb = ops._kc_sizes(shape)
+        else:
+            sv, wf, wb = ops.saved_bytes(shape), ops.workspace_bytes(shape, 0), \
+                ops.workspace_bytes(shape, 1)
+        fo["saved"] = torch.empty(sv, dtype=torch.uint8, device=dev)
+        fo["ws"] = torch.empty(wf, dtype=torch.uint8, device=dev)
+        bo = {"ws": torch.empty(wb, dtype=torch.uint8, device=dev)}
         gate_grads = ((("d_log_decay", xd["log_decay"]), ("d_beta", xd["beta"])) if lb else
                       (("da", xd["a"]), ("db", xd["b"])))
         for n, ref in (("dq", xd["q"]), ("dk", xd["k"]), ("dv", xd["v"])) + gate_grads:
@@ -431,6 +462,9 @@ def run_ours(args, w, world, rank, local):
             ops.decode_conv(inp["hidden"], inp["conv_state"], inp["conv_weight"], inp["state0"],
                             mask=inp["mask"], final_conv_state=fo["final_conv_state"],
                             state_out=fo["state_T"], o=fo["o"], **gates)
+        elif kc:
+            ops.forward_kc(inp["q"], inp["k"], inp["v"], inp["log_decay"], inp["beta"],
+                           inp["state0"], inp["mask"], keep_saved=keep_saved, out=fo)
         elif lb:
             ops.forward_lb(inp["q"], inp["k"], inp["v"], inp["log_decay"], inp["beta"],
                            inp["state0"], inp["mask"], keep_saved=keep_saved, out=fo)
@@ -443,7 +477,10 @@ def run_ours(args, w, world, rank, local):
         fwd_call(inp, True)
 
     def step_bwd(inp):
-        if lb:
+        if kc:
+            ops.backward_kc(inp["q"], inp["k"], inp["v"], inp["log_decay"], inp["beta"],
+                            inp["mask"], fo["saved"], inp["d_o"], inp["d_state_T"], out=bo)
+        elif lb:
             ops.backward_lb(inp["q"], inp["k"], inp["v"], inp["log_decay"], inp["beta"],
                             inp["mask"], fo["saved"], inp["d_o"], inp["d_state_T"], out=bo)
         else:
@@ -506,7 +543,7 @@ def run_ours(args, w, world, rank, local):
 
     # ---- per-phase roofline of the dominant kernel
     peaks = _peaks()
-    model = work_model(w, args.fused_conv)
+    model = work_model(w, args.fused_conv, args.gates)
     ph = {phases[i].name.decode(): (phases[i].launches, phases[i].total_ms)
           for i in range(cnt.value)}
     dom = max(ph, key=lambda k: ph[k][1])
@@ -547,7 +584,7 @@ def run_ours(args, w, world, rank, local):
     # ---- end to end through the C ABI with host buffers (pinned), copies timed
     if args.no_e2e:
         e2e = None
-    elif args.fused_conv:
+    elif args.fused_conv or args.gates == "kc":  # forms the host session does not take
         e2e = run_e2e(args, w, x, xd, fo, bo if backward else None, step, world)
     else:
         e2e = run_e2e_session(args, w, x, world)
@@ -735,9 +772,9 @@ def main():
     ap.add_argument("--fused-conv", type=int, default=0, metavar="K",
                     help="decode workloads: run the step with a K-tap short convolution "
                          "fused in front (gdn_decode_conv); 0 = plain decode")
-    ap.add_argument("--gates", choices=["ab", "lb"], default="ab",
-                    help="gate inputs: a, b, A_log, dt_bias (default) or the per-step "
-                         "log_decay and beta")
+    ap.add_argument("--gates", choices=["ab", "lb", "kc"], default="ab",
+                    help="gate inputs: a, b, A_log, dt_bias (default), the per-step "
+                         "log_decay and beta (lb), or one log_decay per key channel (kc)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

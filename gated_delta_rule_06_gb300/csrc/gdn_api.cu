@@ -440,6 +440,131 @@ gdn_status gdn_backward_lb(const gdn_shape* shape, const void* q, const void* k,
                          nullptr, dstate0, ws, ws_bytes, stream);
 }
 
+/* ---- per-key-channel gates ---------------------------------------------------- */
+namespace {
+struct KcLayout {
+    size_t ckpt, rq, rk, dqh, dkh, gpart, bpart, saved_total, fwd_total, bwd_total;
+};
+gdn_status kc_layout(const gdn_shape* shape, gdn::Dims* d, KcLayout* L) {
+    gdn_status st = validate_shape(shape, d);
+    if (st != GDN_OK) return st;
+    if (!gdn::kc_supported(*d)) return GDN_ERR_UNSUPPORTED_SHAPE;
+    const size_t nt = (size_t)gdn::kc_tiles(*d);
+    const size_t rows = (size_t)d->B * d->Hv * nt * d->Tp;  // per-tile partial rows
+    L->ckpt = 0;
+    L->saved_total = align_up((size_t)d->B * d->Hv * gdn::kc_segments(*d) * d->Dk * d->Dv * 4);
+    size_t o = 0;
+    L->rq = o; o = align_up(o + (size_t)d->B * d->Hk * d->Tp * 4);
+    L->rk = o; o = align_up(o + (size_t)d->B * d->Hk * d->Tp * 4);
+    L->fwd_total = o;
+    L->dqh = o; o = align_up(o + rows * d->Dk * 4);
+    L->dkh = o; o = align_up(o + rows * d->Dk * 4);
+    L->gpart = o; o = align_up(o + rows * d->Dk * 4);
+    L->bpart = o; o = align_up(o + rows * 4);
+    L->bwd_total = o;
+    return GDN_OK;
+}
+}  // namespace
+
+gdn_status gdn_kc_saved_bytes(const gdn_shape* shape, size_t* bytes) {
+    gdn::Dims d;
+    KcLayout L;
+    gdn_status st = kc_layout(shape, &d, &L);
+    if (st != GDN_OK) return st;
+    if (bytes == nullptr) return GDN_ERR_INVALID_ARG;
+    *bytes = L.saved_total;
+    return GDN_OK;
+}
+
+gdn_status gdn_kc_workspace_bytes(const gdn_shape* shape, int pass, size_t* bytes) {
+    gdn::Dims d;
+    KcLayout L;
+    gdn_status st = kc_layout(shape, &d, &L);
+    if (st != GDN_OK) return st;
+    if (bytes == nullptr || pass < 0 || pass > 1) return GDN_ERR_INVALID_ARG;
+    *bytes = pass == 0 ? L.fwd_total : L.bwd_total;
+    return GDN_OK;
+}
+
+gdn_status gdn_forward_kc(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                          const void* log_decay, const void* beta, const float* state0,
+                          const uint8_t* mask, void* o, float* state_T, void* saved,
+                          size_t saved_bytes, void* ws, size_t ws_bytes, void* stream) {
+    gdn::Dims d;
+    KcLayout L;
+    gdn_status st = kc_layout(shape, &d, &L);
+    if (st != GDN_OK) return st;
+    if (!q || !k || !v || !log_decay || !beta || !o || !state_T || !ws) return GDN_ERR_INVALID_ARG;
+    if (shape->has_mask && !mask) return GDN_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, log_decay, beta, state0, mask, o, state_T, saved, ws};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return GDN_ERR_MISALIGNED;
+    if ((saved && saved_bytes < L.saved_total) || ws_bytes < L.fwd_total)
+        return GDN_ERR_WORKSPACE_TOO_SMALL;
+    gdn::Ptrs p{};
+    p.q = q; p.k = k; p.v = v; p.state0 = state0;
+    p.mask = shape->has_mask ? mask : nullptr;
+    p.o = o; p.state_T = state_T;
+    char* w = static_cast<char*>(ws);
+    p.rq = reinterpret_cast<float*>(w + L.rq);
+    p.rk = reinterpret_cast<float*>(w + L.rk);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = run_phase("prep", s, [&] { return gdn::launch_prep_norms(d, p, s); });
+    if (e == cudaSuccess)
+        e = run_phase("kc_fwd", s, [&] {
+            return gdn::launch_kc_forward(d, p, log_decay, beta, static_cast<float*>(saved), s);
+        });
+    return cuda_status(e);
+}
+
+gdn_status gdn_backward_kc(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                           const void* log_decay, const void* beta, const uint8_t* mask,
+                           const void* saved, size_t saved_bytes, const void* d_o,
+                           const float* d_state_T, void* dq, void* dk, void* dv,
+                           void* d_log_decay, void* d_beta, float* dstate0, void* ws,
+                           size_t ws_bytes, void* stream) {
+    gdn::Dims d;
+    KcLayout L;
+    gdn_status st = kc_layout(shape, &d, &L);
+    if (st != GDN_OK) return st;
+    if (!q || !k || !v || !log_decay || !beta || !saved || !d_o || !dq || !dk || !dv ||
+        !d_log_decay || !d_beta || !dstate0 || !ws)
+        return GDN_ERR_INVALID_ARG;
+    if (shape->has_mask && !mask) return GDN_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, log_decay, beta, mask, saved, d_o, d_state_T, dq, dk, dv,
+                          d_log_decay, d_beta, dstate0, ws};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return GDN_ERR_MISALIGNED;
+    if (saved_bytes < L.saved_total || ws_bytes < L.bwd_total) return GDN_ERR_WORKSPACE_TOO_SMALL;
+    gdn::Ptrs p{};
+    p.q = q; p.k = k; p.v = v;
+    p.mask = shape->has_mask ? mask : nullptr;
+    p.d_o = d_o; p.d_state_T = d_state_T;
+    p.dq = dq; p.dk = dk; p.dv = dv; p.dstate0 = dstate0;
+    char* w = static_cast<char*>(ws);
+    p.rq = reinterpret_cast<float*>(w + L.rq);
+    p.rk = reinterpret_cast<float*>(w + L.rk);
+    p.dqh = reinterpret_cast<float*>(w + L.dqh);
+    p.dkh = reinterpret_cast<float*>(w + L.dkh);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = run_phase("prep", s, [&] { return gdn::launch_prep_norms(d, p, s); });
+    if (e == cudaSuccess)
+        e = run_phase("kc_bwd", s, [&] {
+            return gdn::launch_kc_backward(d, p, log_decay, beta, static_cast<const float*>(saved),
+                                           reinterpret_cast<float*>(w + L.gpart),
+                                           reinterpret_cast<float*>(w + L.bpart), d_log_decay,
+                                           d_beta, s);
+        });
+    if (e == cudaSuccess) {
+        // the tiles' partials as value heads of their own: G Dv / 16 per key head
+        gdn::Dims d2 = d;
+        d2.Hv = d.Hv * gdn::kc_tiles(d);
+        d2.G = d.G * gdn::kc_tiles(d);
+        e = run_phase("bwd_reduce", s, [&] { return gdn::launch_qk_reduce(d2, p, s); });
+    }
+    return cuda_status(e);
+}
+
 gdn_status gdn_causal_conv1d_update(int64_t B, int64_t C, int64_t S, int64_t K, int32_t dtype,
                                     const void* hidden, const void* conv_state,
                                     const void* weight, void* out, void* final_state,

@@ -592,6 +592,13 @@ __global__ void __launch_bounds__(256) bwd_reduce_kernel(Dims d, Ptrs p) {
     }
 }
 
+// the q / k part alone (fp32 per-head partials), for callers whose gate
+// cotangents come out elsewhere
+template <typename TI>
+__global__ void __launch_bounds__(256) bwd_qk_kernel(Dims d, Ptrs p) {
+    bwd_qk_body<TI, float>(d, p, blockIdx.x);
+}
+
 // dA_log / ddt_bias: one warp per head.  Lane l sums the partials of rows
 // l, l + 32, ... in (b, chunk) order, then a fixed xor tree adds the lanes, so
 // the result does not depend on scheduling; the loads of a lane are independent
@@ -676,6 +683,16 @@ cudaError_t launch_bwd_scan(const Dims& d, const Ptrs& p, cudaStream_t s) {
 cudaError_t launch_bwd_chunk(const Dims& d, const Ptrs& p, cudaStream_t s) {
     if (tc_path(d)) return launch_bwd_chunk_tc(d, p, s);
     return d.dtype == 1 ? launch_bchunk_t<__nv_bfloat16>(d, p, s) : launch_bchunk_t<float>(d, p, s);
+}
+
+cudaError_t launch_qk_reduce(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    const unsigned nblk = (unsigned)((d.B * d.T * d.Hk + 7) / 8);
+    if (d.dtype == 1)
+        bwd_qk_kernel<__nv_bfloat16><<<nblk, 256, 0, s>>>(d, p);
+    else
+        bwd_qk_kernel<float><<<nblk, 256, 0, s>>>(d, p);
+    count_launches(1);
+    return cudaPeekAtLastError();
 }
 
 cudaError_t launch_bwd_reduce(const Dims& d, const Ptrs& p, cudaStream_t s) {

@@ -181,6 +181,19 @@ cudaError_t launch_causal_conv1d_update(int64_t B, int64_t C, int64_t S, int K, 
                                         cudaStream_t s);
 // streaming multiprocessors of the current device (cached per device)
 int sm_count();
+// q / k row norms alone (rq, rk), and the q / k part of the reduction alone
+cudaError_t launch_prep_norms(const Dims& d, const Ptrs& p, cudaStream_t s);
+cudaError_t launch_qk_reduce(const Dims& d, const Ptrs& p, cudaStream_t s);
+// per-key-channel gates (gdn_kc.cu)
+bool kc_supported(const Dims& d);
+size_t kc_bwd_smem_bytes(const Dims& d);
+int64_t kc_tiles(const Dims& d);
+int64_t kc_segments(const Dims& d);
+cudaError_t launch_kc_forward(const Dims& d, const Ptrs& p, const void* log_decay,
+                              const void* beta, float* ckpt, cudaStream_t s);
+cudaError_t launch_kc_backward(const Dims& d, const Ptrs& p, const void* log_decay,
+                               const void* beta, const float* ckpt, float* gpart, float* bpart,
+                               void* d_log_decay, void* d_beta, cudaStream_t s);
 // Records e as the library's last CUDA error (the text gdn_last_cuda_error
 // returns) and gives GDN_ERR_CUDA; cudaSuccess gives GDN_OK and records nothing.
 int note_cuda_error(cudaError_t e);

@@ -207,6 +207,18 @@ cudaError_t launch_prep_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
 
 }  // namespace
 
+cudaError_t launch_prep_norms(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    const unsigned nblk = (unsigned)((d.B * d.Tp * d.Hk + 7) / 8);
+    if (d.dtype == 1)
+        prep_norms_kernel<__nv_bfloat16><<<nblk, 256, 0, s>>>(d, (const __nv_bfloat16*)p.q,
+                                                             (const __nv_bfloat16*)p.k, p.rq, p.rk);
+    else
+        prep_norms_kernel<float><<<nblk, 256, 0, s>>>(d, (const float*)p.q, (const float*)p.k,
+                                                     p.rq, p.rk);
+    count_launches(1);
+    return cudaPeekAtLastError();
+}
+
 cudaError_t launch_prep(const Dims& d, const Ptrs& p, cudaStream_t s) {
     return d.dtype == 1 ? launch_prep_t<__nv_bfloat16>(d, p, s) : launch_prep_t<float>(d, p, s);
 }

@@ -88,6 +88,14 @@ def load_library(path: str = LIB_PATH):
         lib.gdn_causal_conv1d_update.restype = i32
         lib.gdn_decode_conv.argtypes = [shp, i32, ctypes.c_int64] + [vp] * 13
         lib.gdn_decode_conv.restype = i32
+        lib.gdn_kc_saved_bytes.argtypes = [shp, ctypes.POINTER(sz)]
+        lib.gdn_kc_saved_bytes.restype = i32
+        lib.gdn_kc_workspace_bytes.argtypes = [shp, i32, ctypes.POINTER(sz)]
+        lib.gdn_kc_workspace_bytes.restype = i32
+        lib.gdn_forward_kc.argtypes = [shp] + [vp] * 9 + [vp, sz, vp, sz, vp]
+        lib.gdn_forward_kc.restype = i32
+        lib.gdn_backward_kc.argtypes = [shp] + [vp] * 7 + [sz] + [vp] * 8 + [vp, sz, vp]
+        lib.gdn_backward_kc.restype = i32
         lib.gdn_host_session_bytes.argtypes = [shp, i32, ctypes.POINTER(sz)]
         lib.gdn_host_session_bytes.restype = i32
         lib.gdn_host_session_create.argtypes = [shp, i32, i32, vp, sz, vp, ctypes.POINTER(vp)]
@@ -469,6 +477,82 @@ def decode_conv(hidden, conv_state, conv_weight, state, *, a=None, b=None, A_log
         _p(state_out), _stream())
     _check(rc)
     return o, state_out, final_conv_state
+
+
+def _kc_sizes(shape):
+    lib = load_library()
+    n = ctypes.c_size_t()
+    _check(lib.gdn_kc_saved_bytes(ctypes.byref(shape), ctypes.byref(n)))
+    saved = n.value
+    _check(lib.gdn_kc_workspace_bytes(ctypes.byref(shape), 0, ctypes.byref(n)))
+    wf = n.value
+    _check(lib.gdn_kc_workspace_bytes(ctypes.byref(shape), 1, ctypes.byref(n)))
+    return saved, wf, n.value
+
+
+def forward_kc(q, k, v, log_decay, beta, state0=None, mask=None, *, keep_saved=True,
+               out=None):
+    """gdn_forward_kc: one decay per key channel, log_decay [B, T, Hv, Dk] and
+    beta [B, T, Hv] in q's dtype.  Returns (o, state_T, saved) (saved None when
+    keep_saved is False).  ``out`` may pass preallocated dict(o=, state_T=,
+    saved=, ws=) buffers."""
+    dt = q.dtype
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (log_decay, "log_decay"), (beta, "beta")):
+        _cuda(t, n, dt)
+    _cuda(state0, "state0", torch.float32)
+    m = _mask_u8(mask)
+    shape = make_shape(q, v, m is not None)
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    saved_n, wf, _ = _kc_sizes(shape)
+    out = out or {}
+    o = out.get("o")
+    if o is None:
+        o = torch.empty((B, T, Hv, Dv), dtype=dt, device=q.device)
+    sT = out.get("state_T")
+    if sT is None:
+        sT = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=q.device)
+    saved = (out.get("saved") if out.get("saved") is not None else _buf(saved_n, q.device)) \
+        if keep_saved else None
+    ws = out.get("ws") if out.get("ws") is not None else _buf(wf, q.device)
+    rc = load_library().gdn_forward_kc(
+        ctypes.byref(shape), _p(q), _p(k), _p(v), _p(log_decay), _p(beta), _p(state0), _p(m),
+        _p(o), _p(sT), _p(saved), saved_n if keep_saved else 0, _p(ws), wf, _stream())
+    _check(rc)
+    return o, sT, saved
+
+
+def backward_kc(q, k, v, log_decay, beta, mask, saved, d_o, d_state_T=None, *, out=None):
+    """gdn_backward_kc.  Returns a dict with dq, dk, dv, d_log_decay, d_beta
+    (q's dtype) and dstate0 (fp32).  ``out`` may pass preallocated tensors of
+    those names and the workspace ``ws``."""
+    dt = q.dtype
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (log_decay, "log_decay"), (beta, "beta"),
+                 (d_o, "d_o")):
+        _cuda(t, n, dt)
+    _cuda(d_state_T, "d_state_T", torch.float32)
+    m = _mask_u8(mask)
+    shape = make_shape(q, v, m is not None)
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    saved_n, _, wb = _kc_sizes(shape)
+    out = out or {}
+    g = dict(dq=out.get("dq"), dk=out.get("dk"), dv=out.get("dv"),
+             d_log_decay=out.get("d_log_decay"), d_beta=out.get("d_beta"),
+             dstate0=out.get("dstate0"))
+    for n, ref in (("dq", q), ("dk", k), ("dv", v), ("d_log_decay", log_decay),
+                   ("d_beta", beta)):
+        if g[n] is None:
+            g[n] = torch.empty_like(ref)
+    if g["dstate0"] is None:
+        g["dstate0"] = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=q.device)
+    ws = out.get("ws") if out.get("ws") is not None else _buf(wb, q.device)
+    rc = load_library().gdn_backward_kc(
+        ctypes.byref(shape), _p(q), _p(k), _p(v), _p(log_decay), _p(beta), _p(m), _p(saved),
+        saved_n, _p(d_o), _p(d_state_T), _p(g["dq"]), _p(g["dk"]), _p(g["dv"]),
+        _p(g["d_log_decay"]), _p(g["d_beta"]), _p(g["dstate0"]), _p(ws), wb, _stream())
+    _check(rc)
+    return g
 
 
 class HostSession:

@@ -161,6 +161,20 @@ def make_lb_gates(w: Workload, seed: Optional[int] = None) -> dict:
     return {"log_decay": ld.to(w.dtype), "beta": beta.to(w.dtype)}
 
 
+def make_kc_gates(w: Workload, seed: Optional[int] = None) -> dict:
+    """Draw per-key-channel log_decay ([B, T, Hv, Dk]) and beta ([B, T, Hv]) in
+    the input dtype: log_decay = -exp(u), u ~ U(ln 0.01, ln 4) per channel, with
+    channel 0 of value head 0 at -50 (that channel is cleared every step);
+    beta ~ U(0, 1)."""
+    gen = torch.Generator().manual_seed((w.seed if seed is None else seed) + 104729)
+    u = torch.rand((w.B, w.T, w.Hv, w.Dk), generator=gen, dtype=torch.float64)
+    lo, hi = math.log(0.01), math.log(4.0)
+    ld = -torch.exp(lo + u * (hi - lo))
+    ld[:, :, 0, 0] = -50.0
+    beta = torch.rand((w.B, w.T, w.Hv), generator=gen, dtype=torch.float64)
+    return {"log_decay": ld.to(w.dtype), "beta": beta.to(w.dtype)}
+
+
 def make_conv_inputs(B: int, C: int, S: int, K: int, dtype: torch.dtype = torch.float32,
                      seed: int = 0) -> dict:
     """Inputs of the causal conv1d update: hidden [B, C, S] ~ N(0, 1), conv_state

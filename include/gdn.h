@@ -143,6 +143,40 @@ gdn_status gdn_backward_lb(const gdn_shape* shape, const void* q, const void* k,
                            void* dv, void* d_log_decay, void* d_beta, float* dstate0,
                            void* ws, size_t ws_bytes, void* stream);
 
+/* ---- per-key-channel gates ------------------------------------------------ */
+
+/* The vectorised gating the mlx-lm page lists (g.ndim == 4, "Scope and
+ * follow-ups": on its Python path only): one decay per key channel.  Taken in
+ * the op contract's log_decay form with a key-channel axis (torch-to-nnef
+ * "custom_extractors/gdn", op contract):
+ *   - log_decay, d_log_decay: [B, T, Hv, Dk]; beta, d_beta: [B, T, Hv]; both in
+ *     the shape's dtype.  l_{t,i} = log g_{t,i} <= 0 for key channel i.
+ *   - An applied step scales row i of the state by g_{t,i} before the delta
+ *     rule: S_a = diag(g_t) S, delta = beta_t (v_t - S_a^T kh_t),
+ *     S = S_a + kh_t delta^T, o_t = S^T qh_t.  Masking, norms, layouts of q, k,
+ *     v, o, the states and their cotangents are those of gdn_forward /
+ *     gdn_backward.
+ *   - The recurrence runs on the CUDA cores with an fp32 state (no chunked
+ *     tensor-core form): one CTA per 16 value columns of a (b, h), the state at
+ *     every 8th step kept in `saved` (gdn_kc_saved_bytes) for the backward.
+ *   - Requires Dk and Dv multiples of 16 (Dk <= 256) on top of gdn.h's set,
+ *     else GDN_ERR_UNSUPPORTED_SHAPE.
+ *   - saved may be NULL in gdn_forward_kc (inference).  ws must hold
+ *     gdn_kc_workspace_bytes(shape, 0) bytes for the forward and (shape, 1) for
+ *     the backward; every output is written in full. */
+gdn_status gdn_kc_saved_bytes(const gdn_shape* shape, size_t* bytes);
+gdn_status gdn_kc_workspace_bytes(const gdn_shape* shape, int pass, size_t* bytes);
+gdn_status gdn_forward_kc(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                          const void* log_decay, const void* beta, const float* state0,
+                          const uint8_t* mask, void* o, float* state_T, void* saved,
+                          size_t saved_bytes, void* ws, size_t ws_bytes, void* stream);
+gdn_status gdn_backward_kc(const gdn_shape* shape, const void* q, const void* k, const void* v,
+                           const void* log_decay, const void* beta, const uint8_t* mask,
+                           const void* saved, size_t saved_bytes, const void* d_o,
+                           const float* d_state_T, void* dq, void* dk, void* dv,
+                           void* d_log_decay, void* d_beta, float* dstate0, void* ws,
+                           size_t ws_bytes, void* stream);
+
 /* ---- causal conv1d update ------------------------------------------------- */
 
 /* Depthwise causal conv1d + SiLU with a K-sample carry state, the short
@@ -228,7 +262,9 @@ uint64_t gdn_launch_count(void);
  * `max` entries {phase name, launches, total milliseconds} in first-seen
  * order, sets *count, and switches recording off.  Returns GDN_ERR_CUDA if an
  * event failed.  Phases: "prep", "fwd_chunk", "fwd_scan", "bwd_scan",
- * "bwd_chunk", "bwd_reduce", "decode".  Not thread-safe: one caller at a time. */
+ * "bwd_chunk", "bwd_scan_chunk" (the reverse scan and the gradient kernel in one
+ * launch), "bwd_reduce", "decode", "kc_fwd", "kc_bwd".  Not thread-safe: one
+ * caller at a time. */
 typedef struct {
     const char* name;
     int64_t launches;
