@@ -31,7 +31,7 @@ namespace gdn {
 namespace {
 
 constexpr int KT = 16;             // value columns per CTA
-constexpr int KG = 16;             // row groups
+constexpr int KG = 16;             // Dk <= KG kMaxR
 constexpr int kThreads = KT * KG;  // 256
 constexpr int kSeg = 8;            // steps between checkpoints
 constexpr int kMaxR = 16;          // rows per thread (Dk <= 256)
@@ -45,25 +45,6 @@ struct KcArgs {
     void* d_lg;          // [B, T, Hv, Dk]
     void* d_beta;        // [B, T, Hv]
 };
-
-// sum over the 16 row groups of column jj: lanes l and l + 16 of a warp hold row
-// groups 2w and 2w + 1; the eight warp sums go through red[8][KT] in warp order
-__device__ __forceinline__ float col_sum(float x, float (*red)[KT], int warp, int lane, int jj) {
-    x += __shfl_xor_sync(0xffffffffu, x, 16);
-    if (lane < 16) red[warp][jj] = x;
-    __syncthreads();
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) s += red[w][jj];
-    return s;
-}
-
-// sum over the 16 columns of the tile (the 16 lanes of a half warp)
-__device__ __forceinline__ float row_sum(float x) {
-#pragma unroll
-    for (int off = 1; off < 16; off <<= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-    return x;
-}
 
 // Per-step vectors of steps t0 .. t0 + L - 1 of (b, h) into shared memory: the
 // normalised k and q rows, g per key channel, beta, the applied flag, the tile's
@@ -122,37 +103,49 @@ __device__ __forceinline__ void load_seg(const Dims& d, const Ptrs& p, const KcA
     }
 }
 
+// sum over the 32 lanes of a warp (fixed xor tree)
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+// Forward: warp w owns columns col0 + 2 w, + 1 of the tile; lane l owns rows
+// l, l + 32, ... (RR = Dk / 32 of them), so every per-step sum is a warp
+// shuffle and the steps need no CTA barrier (only the segment staging does).
 template <typename TI>
 __global__ void __launch_bounds__(kThreads) kc_fwd_kernel(Dims d, Ptrs p, KcArgs a) {
     extern __shared__ __align__(16) float kcf[];
-    const int Dk = (int)d.Dk, Dv = (int)d.Dv, R = Dk / KG;
+    const int Dk = (int)d.Dk, Dv = (int)d.Dv, RR = Dk / 32;
     float* kh = kcf;                  // [kSeg][Dk]
     float* qh = kh + kSeg * Dk;       // [kSeg][Dk]
     float* gv = qh + kSeg * Dk;       // [kSeg][Dk]
     float* vv = gv + kSeg * Dk;       // [kSeg][KT]
     float* bt = vv + kSeg * KT;       // [kSeg]
     int* on = reinterpret_cast<int*>(bt + kSeg);
-    __shared__ float red[2][kThreads / 32][KT];
     const int tile = blockIdx.x;
     const int64_t h = blockIdx.y, bb = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int jj = tid % KT, rg = tid / KT, r0 = rg * R;
-    const int col0 = tile * KT, col = col0 + jj;
+    const int col0 = tile * KT, c0 = 2 * warp;  // the warp's columns c0, c0 + 1 of the tile
     const int64_t bh = bb * d.Hv + h;
     const int64_t NS = (d.T + kSeg - 1) / kSeg;
-    int nred = 0;
-    float S[kMaxR];
+    float S[kMaxR / 2][2];
 #pragma unroll
-    for (int m = 0; m < kMaxR; ++m)
-        S[m] = (m < R && p.state0) ? p.state0[(bh * Dk + r0 + m) * Dv + col] : 0.f;
+    for (int m = 0; m < kMaxR / 2; ++m)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+            S[m][c] = (m < RR && p.state0) ? p.state0[(bh * Dk + lane + 32 * m) * Dv + col0 + c0 + c] : 0.f;
     for (int64_t sg = 0; sg < NS; ++sg) {
         const int64_t t0 = sg * kSeg;
         const int L = (int)(d.T - t0 < kSeg ? d.T - t0 : kSeg);
         if (a.ckpt) {  // the state at the start of this segment
-            float* ck = a.ckpt + ((bh * NS + sg) * Dk + r0) * Dv + col;
+            float* ck = a.ckpt + (bh * NS + sg) * Dk * Dv + col0 + c0;
 #pragma unroll
-            for (int m = 0; m < kMaxR; ++m)
-                if (m < R) ck[(int64_t)m * Dv] = S[m];
+            for (int m = 0; m < kMaxR / 2; ++m)
+                if (m < RR) {
+                    ck[(int64_t)(lane + 32 * m) * Dv] = S[m][0];
+                    ck[(int64_t)(lane + 32 * m) * Dv + 1] = S[m][1];
+                }
         }
         __syncthreads();  // the previous segment's vectors have been read
         load_seg<TI>(d, p, a, bb, h, t0, L, col0, kh, qh, gv, vv, nullptr, bt, on);
@@ -160,157 +153,223 @@ __global__ void __launch_bounds__(kThreads) kc_fwd_kernel(Dims d, Ptrs p, KcArgs
         for (int i = 0; i < L; ++i) {
             const float* kk = kh + i * Dk;
             const float* gg = gv + i * Dk;
-            float pp = 0.f;
+            const float* qq = qh + i * Dk;
+            float p0 = 0.f, p1 = 0.f;
 #pragma unroll
-            for (int m = 0; m < kMaxR; ++m)
-                if (m < R) pp = fmaf(gg[r0 + m] * S[m], kk[r0 + m], pp);
-            const float pc = col_sum(pp, red[nred], warp, lane, jj);
-            nred ^= 1;
+            for (int m = 0; m < kMaxR / 2; ++m)
+                if (m < RR) {
+                    const float gk = gg[lane + 32 * m] * kk[lane + 32 * m];
+                    p0 = fmaf(gk, S[m][0], p0);
+                    p1 = fmaf(gk, S[m][1], p1);
+                }
+            p0 = warp_sum(p0);
+            p1 = warp_sum(p1);
             if (on[i]) {
-                const float dl = bt[i] * (vv[i * KT + jj] - pc);
+                const float d0 = bt[i] * (vv[i * KT + c0] - p0), d1 = bt[i] * (vv[i * KT + c0 + 1] - p1);
 #pragma unroll
-                for (int m = 0; m < kMaxR; ++m)
-                    if (m < R) S[m] = fmaf(kk[r0 + m], dl, gg[r0 + m] * S[m]);
+                for (int m = 0; m < kMaxR / 2; ++m)
+                    if (m < RR) {
+                        const float gi = gg[lane + 32 * m], ki = kk[lane + 32 * m];
+                        S[m][0] = fmaf(ki, d0, gi * S[m][0]);
+                        S[m][1] = fmaf(ki, d1, gi * S[m][1]);
+                    }
             }
-            float po = 0.f;
+            float o0 = 0.f, o1 = 0.f;
 #pragma unroll
-            for (int m = 0; m < kMaxR; ++m)
-                if (m < R) po = fmaf(S[m], qh[i * Dk + r0 + m], po);
-            const float oc = col_sum(po, red[nred], warp, lane, jj);
-            nred ^= 1;
-            if (rg == 0) stf((TI*)p.o + ((bb * d.T + t0 + i) * d.Hv + h) * Dv + col, oc);
+            for (int m = 0; m < kMaxR / 2; ++m)
+                if (m < RR) {
+                    o0 = fmaf(S[m][0], qq[lane + 32 * m], o0);
+                    o1 = fmaf(S[m][1], qq[lane + 32 * m], o1);
+                }
+            o0 = warp_sum(o0);
+            o1 = warp_sum(o1);
+            if (lane < 2) stf((TI*)p.o + ((bb * d.T + t0 + i) * d.Hv + h) * Dv + col0 + c0 + lane,
+                              lane == 0 ? o0 : o1);
         }
     }
 #pragma unroll
-    for (int m = 0; m < kMaxR; ++m)
-        if (m < R) p.state_T[(bh * Dk + r0 + m) * Dv + col] = S[m];
+    for (int m = 0; m < kMaxR / 2; ++m)
+        if (m < RR) {
+            p.state_T[(bh * Dk + lane + 32 * m) * Dv + col0 + c0] = S[m][0];
+            p.state_T[(bh * Dk + lane + 32 * m) * Dv + col0 + c0 + 1] = S[m][1];
+        }
 }
 
-// Partials of the tile (b, h, tile) are written as if (h, tile) were value head
-// h nt + tile of B x (Hv nt) heads.
+// Backward, in the forward's decomposition (warp w: columns c0 = 2 w, + 1 of the
+// tile; lane l: rows l + 32 m).  Per segment (reverse order): the warp's states
+// of the segment are recomputed from its checkpoint into the warp's own slice
+// of shared memory, then walked back.  Column sums are warp shuffles; the row
+// sums over the tile's 16 columns (the q, k and log-decay cotangents) and the
+// beta cotangent are per-warp register sums, added over the 8 warps in warp
+// order through shared memory (double-buffered: one barrier per step).  The
+// tile's partials are written as if (h, tile) were value head h nt + tile of
+// B x (Hv nt) heads.
 template <typename TI>
 __global__ void __launch_bounds__(kThreads) kc_bwd_kernel(Dims d, Ptrs p, KcArgs a) {
     extern __shared__ __align__(16) float kcs[];
-    const int Dk = (int)d.Dk, Dv = (int)d.Dv, R = Dk / KG;
-    float* hist = kcs;                              // [kSeg + 1][Dk][KT] states of a segment
-    float* kh = hist + (kSeg + 1) * Dk * KT;        // [kSeg][Dk]
-    float* qh = kh + kSeg * Dk;                     // [kSeg][Dk]
-    float* gv = qh + kSeg * Dk;                     // [kSeg][Dk]
-    float* vv = gv + kSeg * Dk;                     // [kSeg][KT]
-    float* ob = vv + kSeg * KT;                     // [kSeg][KT] d_o
-    float* dlv = ob + kSeg * KT;                    // [kSeg][KT] delta
-    float* pvv = dlv + kSeg * KT;                   // [kSeg][KT] p
-    float* bt = pvv + kSeg * KT;                    // [kSeg]
-    int* on = reinterpret_cast<int*>(bt + kSeg);    // [kSeg]
-    __shared__ float red[2][kThreads / 32][KT];
+    const int Dk = (int)d.Dk, Dv = (int)d.Dv, RR = Dk / 32;
+    constexpr int NW = kThreads / 32;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float* hw = kcs + warp * (kSeg + 1) * 2 * Dk;     // this warp: [kSeg + 1][2][Dk] states
+    float* kh = kcs + NW * (kSeg + 1) * 2 * Dk;       // [kSeg][Dk]
+    float* qh = kh + kSeg * Dk;                       // [kSeg][Dk]
+    float* gv = qh + kSeg * Dk;                       // [kSeg][Dk]
+    float* vv = gv + kSeg * Dk;                       // [kSeg][KT]
+    float* ob = vv + kSeg * KT;                       // [kSeg][KT] d_o
+    float* bt = ob + kSeg * KT;                       // [kSeg]
+    float* rowp = bt + kSeg;                          // [2][NW][3 Dk + 1] per-warp row sums
+    int* on = reinterpret_cast<int*>(rowp + 2 * NW * (3 * Dk + 1));  // [kSeg]
+    const int RP = 3 * Dk + 1;
     const int tile = blockIdx.x;
     const int64_t h = blockIdx.y, bb = blockIdx.z;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int jj = tid % KT, rg = tid / KT, r0 = rg * R;
-    const int col0 = tile * KT, col = col0 + jj;
+    const int col0 = tile * KT, c0 = 2 * warp;
     const int nt = Dv / KT;
     const int64_t bh = bb * d.Hv + h;
     const int64_t hv2 = bb * d.Hv * nt + h * nt + tile;  // virtual head of the partials
     const int64_t NS = (d.T + kSeg - 1) / kSeg;
-    float* dqh = p.dqh;
-    float* dkh = p.dkh;
-    int nred = 0;
-    float Sb[kMaxR];
+    int nb = 0;
+    float Sb[kMaxR / 2][2];
 #pragma unroll
-    for (int m = 0; m < kMaxR; ++m)
-        Sb[m] = (m < R && p.d_state_T) ? p.d_state_T[(bh * Dk + r0 + m) * Dv + col] : 0.f;
+    for (int m = 0; m < kMaxR / 2; ++m)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+            Sb[m][c] = (m < RR && p.d_state_T) ? p.d_state_T[(bh * Dk + lane + 32 * m) * Dv + col0 + c0 + c] : 0.f;
     for (int64_t sg = NS - 1; sg >= 0; --sg) {
         const int64_t t0 = sg * kSeg;
         const int L = (int)(d.T - t0 < kSeg ? d.T - t0 : kSeg);
+        __syncthreads();  // the previous segment's shared memory is free
         load_seg<TI>(d, p, a, bb, h, t0, L, col0, kh, qh, gv, vv, ob, bt, on);
-        float S[kMaxR];
-        const float* ck = a.ckpt + ((bh * NS + sg) * Dk + r0) * Dv + col;
+        float S[kMaxR / 2][2];
+        const float* ck = a.ckpt + (bh * NS + sg) * Dk * Dv + col0 + c0;
 #pragma unroll
-        for (int m = 0; m < kMaxR; ++m)
-            if (m < R) {
-                S[m] = ck[(int64_t)m * Dv];
-                hist[(r0 + m) * KT + jj] = S[m];
+        for (int m = 0; m < kMaxR / 2; ++m)
+            if (m < RR) {
+                S[m][0] = ck[(int64_t)(lane + 32 * m) * Dv];
+                S[m][1] = ck[(int64_t)(lane + 32 * m) * Dv + 1];
+                hw[lane + 32 * m] = S[m][0];
+                hw[Dk + lane + 32 * m] = S[m][1];
             }
         __syncthreads();
         // the segment's states again, with delta and p of every step
-        for (int i = 0; i < L; ++i) {
-            float pp = 0.f;
+        float dls[kSeg][2], pcs[kSeg][2];
 #pragma unroll
-            for (int m = 0; m < kMaxR; ++m)
-                if (m < R) pp = fmaf(gv[i * Dk + r0 + m] * S[m], kh[i * Dk + r0 + m], pp);
-            const float pc = col_sum(pp, red[nred], warp, lane, jj);
-            nred ^= 1;
-            float dl = 0.f;
+        for (int i = 0; i < kSeg; ++i) {
+            dls[i][0] = dls[i][1] = pcs[i][0] = pcs[i][1] = 0.f;
+            if (i >= L) continue;
+            const float* kk = kh + i * Dk;
+            const float* gg = gv + i * Dk;
+            float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < kMaxR / 2; ++m)
+                if (m < RR) {
+                    const float gk = gg[lane + 32 * m] * kk[lane + 32 * m];
+                    p0 = fmaf(gk, S[m][0], p0);
+                    p1 = fmaf(gk, S[m][1], p1);
+                }
+            p0 = warp_sum(p0);
+            p1 = warp_sum(p1);
+            pcs[i][0] = p0;
+            pcs[i][1] = p1;
             if (on[i]) {
-                dl = bt[i] * (vv[i * KT + jj] - pc);
+                dls[i][0] = bt[i] * (vv[i * KT + c0] - p0);
+                dls[i][1] = bt[i] * (vv[i * KT + c0 + 1] - p1);
 #pragma unroll
-                for (int m = 0; m < kMaxR; ++m)
-                    if (m < R) S[m] = fmaf(kh[i * Dk + r0 + m], dl, gv[i * Dk + r0 + m] * S[m]);
+                for (int m = 0; m < kMaxR / 2; ++m)
+                    if (m < RR) {
+                        const float gi = gg[lane + 32 * m], ki = kk[lane + 32 * m];
+                        S[m][0] = fmaf(ki, dls[i][0], gi * S[m][0]);
+                        S[m][1] = fmaf(ki, dls[i][1], gi * S[m][1]);
+                    }
             }
-            if (rg == 0) {
-                dlv[i * KT + jj] = dl;
-                pvv[i * KT + jj] = pc;
-            }
+            float* hs = hw + (i + 1) * 2 * Dk;
 #pragma unroll
-            for (int m = 0; m < kMaxR; ++m)
-                if (m < R) hist[((i + 1) * Dk + r0 + m) * KT + jj] = S[m];
+            for (int m = 0; m < kMaxR / 2; ++m)
+                if (m < RR) {
+                    hs[lane + 32 * m] = S[m][0];
+                    hs[Dk + lane + 32 * m] = S[m][1];
+                }
         }
-        __syncthreads();
+        __syncwarp();  // the warp's own states (each lane rereads only its own rows)
         // reverse over the segment's steps
-        for (int i = L - 1; i >= 0; --i) {
-            const int64_t t = t0 + i;
-            const float* scur = hist + (i + 1) * Dk * KT;
-            const float* sprev = hist + i * Dk * KT;
-            const float oj = ob[i * KT + jj];
-            const int64_t prow = (hv2 * d.Tp + t) * Dk;
 #pragma unroll
-            for (int m = 0; m < kMaxR; ++m)
-                if (m < R) {
-                    Sb[m] = fmaf(qh[i * Dk + r0 + m], oj, Sb[m]);
-                    const float qb = row_sum(scur[(r0 + m) * KT + jj] * oj);
-                    if (jj == 0) dqh[prow + r0 + m] = qb;
+        for (int i = kSeg - 1; i >= 0; --i) {
+            if (i >= L) continue;
+            const int64_t t = t0 + i;
+            const float* scur = hw + (i + 1) * 2 * Dk;
+            const float* sprev = hw + i * 2 * Dk;
+            const float* kk = kh + i * Dk;
+            const float* gg = gv + i * Dk;
+            const float* qq = qh + i * Dk;
+            const float o0 = ob[i * KT + c0], o1 = ob[i * KT + c0 + 1];
+            float* rp = rowp + (nb * NW + warp) * RP;
+            float db0 = 0.f, db1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < kMaxR / 2; ++m)
+                if (m < RR) {
+                    const int r = lane + 32 * m;
+                    Sb[m][0] = fmaf(qq[r], o0, Sb[m][0]);
+                    Sb[m][1] = fmaf(qq[r], o1, Sb[m][1]);
+                    rp[r] = fmaf(scur[r], o0, scur[Dk + r] * o1);  // q cotangent, this warp's columns
+                    db0 = fmaf(Sb[m][0], kk[r], db0);
+                    db1 = fmaf(Sb[m][1], kk[r], db1);
                 }
             if (on[i]) {
-                const float dl = dlv[i * KT + jj], pc = pvv[i * KT + jj], beta = bt[i];
-                float db = 0.f;
+                db0 = warp_sum(db0);
+                db1 = warp_sum(db1);
+                const float beta = bt[i];
+                if (lane < 2)
+                    stf((TI*)p.dv + ((bb * d.T + t) * d.Hv + h) * Dv + col0 + c0 + lane,
+                        beta * (lane == 0 ? db0 : db1));
+                const float pb0 = -beta * db0, pb1 = -beta * db1;
+                const float d0 = dls[i][0], d1 = dls[i][1];
+                if (lane == 0)
+                    rp[3 * Dk] = fmaf(db0, vv[i * KT + c0] - pcs[i][0], db1 * (vv[i * KT + c0 + 1] - pcs[i][1]));
 #pragma unroll
-                for (int m = 0; m < kMaxR; ++m)
-                    if (m < R) db = fmaf(Sb[m], kh[i * Dk + r0 + m], db);
-                const float dbar = col_sum(db, red[nred], warp, lane, jj);
-                nred ^= 1;
-                if (rg == 0) stf((TI*)p.dv + ((bb * d.T + t) * d.Hv + h) * Dv + col, beta * dbar);
-                const float bsum = row_sum(dbar * (vv[i * KT + jj] - pc));
-                if (tid == 0) a.bpart[hv2 * d.Tp + t] = bsum;
-                const float pbar = -beta * dbar;
-#pragma unroll
-                for (int m = 0; m < kMaxR; ++m)
-                    if (m < R) {
-                        const float gi = gv[i * Dk + r0 + m], sp = sprev[(r0 + m) * KT + jj];
-                        const float kb = row_sum(fmaf(Sb[m], dl, gi * sp * pbar));
-                        Sb[m] = fmaf(kh[i * Dk + r0 + m], pbar, Sb[m]);  // Sbar_a
-                        const float gb = row_sum(Sb[m] * sp);
-                        Sb[m] *= gi;
-                        if (jj == 0) {
-                            dkh[prow + r0 + m] = kb;
-                            a.gpart[prow + r0 + m] = gb * gi;
-                        }
+                for (int m = 0; m < kMaxR / 2; ++m)
+                    if (m < RR) {
+                        const int r = lane + 32 * m;
+                        const float gi = gg[r], ki = kk[r];
+                        const float sp0 = sprev[r], sp1 = sprev[Dk + r];
+                        rp[Dk + r] = fmaf(Sb[m][0], d0, gi * sp0 * pb0) + fmaf(Sb[m][1], d1, gi * sp1 * pb1);
+                        Sb[m][0] = fmaf(ki, pb0, Sb[m][0]);  // Sbar_a
+                        Sb[m][1] = fmaf(ki, pb1, Sb[m][1]);
+                        rp[2 * Dk + r] = gi * fmaf(Sb[m][0], sp0, Sb[m][1] * sp1);
+                        Sb[m][0] *= gi;
+                        Sb[m][1] *= gi;
                     }
             } else {
-                if (rg == 0) stf((TI*)p.dv + ((bb * d.T + t) * d.Hv + h) * Dv + col, 0.f);
-                if (tid == 0) a.bpart[hv2 * d.Tp + t] = 0.f;
+                if (lane < 2)
+                    stf((TI*)p.dv + ((bb * d.T + t) * d.Hv + h) * Dv + col0 + c0 + lane, 0.f);
+                if (lane == 0) rp[3 * Dk] = 0.f;
 #pragma unroll
-                for (int m = 0; m < kMaxR; ++m)
-                    if (m < R && jj == 0) {
-                        dkh[prow + r0 + m] = 0.f;
-                        a.gpart[prow + r0 + m] = 0.f;
+                for (int m = 0; m < kMaxR / 2; ++m)
+                    if (m < RR) {
+                        rp[Dk + lane + 32 * m] = 0.f;
+                        rp[2 * Dk + lane + 32 * m] = 0.f;
                     }
             }
+            __syncthreads();
+            // the tile's row sums: the eight warps' in warp order
+            const int64_t prow = (hv2 * d.Tp + t) * Dk;
+            const float* rb = rowp + nb * NW * RP;
+            for (int e = tid; e < RP; e += kThreads) {
+                float x = 0.f;
+#pragma unroll
+                for (int w = 0; w < NW; ++w) x += rb[w * RP + e];
+                if (e < Dk) p.dqh[prow + e] = x;
+                else if (e < 2 * Dk) p.dkh[prow + e - Dk] = x;
+                else if (e < 3 * Dk) a.gpart[prow + e - 2 * Dk] = x;
+                else a.bpart[hv2 * d.Tp + t] = x;
+            }
+            nb ^= 1;
         }
-        __syncthreads();  // the segment's shared memory is free
     }
 #pragma unroll
-    for (int m = 0; m < kMaxR; ++m)
-        if (m < R) p.dstate0[(bh * Dk + r0 + m) * Dv + col] = Sb[m];
+    for (int m = 0; m < kMaxR / 2; ++m)
+        if (m < RR) {
+            p.dstate0[(bh * Dk + lane + 32 * m) * Dv + col0 + c0] = Sb[m][0];
+            p.dstate0[(bh * Dk + lane + 32 * m) * Dv + col0 + c0 + 1] = Sb[m][1];
+        }
 }
 
 // d_log_decay and d_beta: the tiles' partials in tile order
@@ -338,8 +397,10 @@ size_t fwd_smem(const Dims& d) {
 }
 
 size_t bwd_smem(const Dims& d) {
-    return sizeof(float) * ((size_t)(kSeg + 1) * d.Dk * KT + 3 * (size_t)kSeg * d.Dk +
-                            4 * (size_t)kSeg * KT + kSeg) + sizeof(int) * kSeg;
+    const size_t NW = kThreads / 32;
+    return sizeof(float) * (NW * (kSeg + 1) * 2 * (size_t)d.Dk + 3 * (size_t)kSeg * d.Dk +
+                            2 * (size_t)kSeg * KT + kSeg + 2 * NW * (3 * (size_t)d.Dk + 1)) +
+           sizeof(int) * kSeg;
 }
 
 template <typename TI>
@@ -367,7 +428,7 @@ cudaError_t launch_kc_bwd_t(const Dims& d, const Ptrs& p, const KcArgs& a, cudaS
 }  // namespace
 
 bool kc_supported(const Dims& d) {
-    return d.Dk % KG == 0 && d.Dk / KG <= kMaxR && d.Dv % KT == 0;
+    return d.Dk % 32 == 0 && d.Dk / KG <= kMaxR && d.Dv % KT == 0;
 }
 size_t kc_bwd_smem_bytes(const Dims& d) { return bwd_smem(d); }
 int64_t kc_tiles(const Dims& d) { return d.Dv / KT; }

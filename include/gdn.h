@@ -159,7 +159,7 @@ gdn_status gdn_backward_lb(const gdn_shape* shape, const void* q, const void* k,
  *   - The recurrence runs on the CUDA cores with an fp32 state (no chunked
  *     tensor-core form): one CTA per 16 value columns of a (b, h), the state at
  *     every 8th step kept in `saved` (gdn_kc_saved_bytes) for the backward.
- *   - Requires Dk and Dv multiples of 16 (Dk <= 256) on top of gdn.h's set,
+ *   - Requires Dk a multiple of 32 and Dv of 16 (Dk <= 256) on top of gdn.h's set,
  *     else GDN_ERR_UNSUPPORTED_SHAPE.
  *   - saved may be NULL in gdn_forward_kc (inference).  ws must hold
  *     gdn_kc_workspace_bytes(shape, 0) bytes for the forward and (shape, 1) for
