@@ -48,10 +48,10 @@ struct KcArgs {
 
 // Per-step vectors of steps t0 .. t0 + L - 1 of (b, h) into shared memory: the
 // normalised k and q rows, g per key channel, beta, the applied flag, the tile's
-// v columns and (ob non-null) its d_o columns.  Every global load of the
-// segment is issued before the first store, so the segment pays one load
-// latency, not one per step.
-template <typename TI>
+// v columns and (ob non-null) its d_o columns.  NB steps at a time, every global
+// load of a batch issued before its first store, so a batch pays one load
+// latency, not one per step (NB trades that against registers).
+template <typename TI, int NB>
 __device__ __forceinline__ void load_seg(const Dims& d, const Ptrs& p, const KcArgs& a,
                                          int64_t bb, int64_t h, int64_t t0, int L, int col0,
                                          float* kh, float* qh, float* g, float* v, float* ob,
@@ -59,46 +59,50 @@ __device__ __forceinline__ void load_seg(const Dims& d, const Ptrs& p, const KcA
     const int tid = threadIdx.x;
     const int64_t j = h / d.G;
     const int Dk = (int)d.Dk;
-    float xk[kSeg], xq[kSeg], xg[kSeg], nk[kSeg], nq[kSeg], xv[kSeg], xo[kSeg], xb[kSeg];
-    bool live[kSeg];
+#pragma unroll 1
+    for (int i0 = 0; i0 < L; i0 += NB) {
+        float xk[NB], xq[NB], xg[NB], nk[NB], nq[NB], xv[NB], xo[NB], xb[NB];
+        bool live[NB];
 #pragma unroll
-    for (int i = 0; i < kSeg; ++i) {
-        const int64_t t = t0 + i;
-        const bool in = i < L;
-        live[i] = in && (p.mask == nullptr || p.mask[bb * d.T + t] != 0);
-        xk[i] = xq[i] = nk[i] = nq[i] = xv[i] = xo[i] = xb[i] = 0.f;
-        xg[i] = 0.f;
-        if (in && tid < Dk) {
-            const int64_t xi = ((bb * d.T + t) * d.Hk + j) * Dk + tid;
-            const int64_t ri = (bb * d.Hk + j) * d.Tp + t;
-            xk[i] = ldf((const TI*)p.k + xi);
-            xq[i] = ldf((const TI*)p.q + xi);
-            nk[i] = p.rk[ri];
-            nq[i] = p.rq[ri];
-            xg[i] = ldf((const TI*)a.lg + ((bb * d.T + t) * d.Hv + h) * Dk + tid);
+        for (int u = 0; u < NB; ++u) {
+            const int i = i0 + u;
+            const int64_t t = t0 + i;
+            const bool in = i < L;
+            live[u] = in && (p.mask == nullptr || p.mask[bb * d.T + t] != 0);
+            xk[u] = xq[u] = nk[u] = nq[u] = xv[u] = xo[u] = xb[u] = xg[u] = 0.f;
+            if (in && tid < Dk) {
+                const int64_t xi = ((bb * d.T + t) * d.Hk + j) * Dk + tid;
+                const int64_t ri = (bb * d.Hk + j) * d.Tp + t;
+                xk[u] = ldf((const TI*)p.k + xi);
+                xq[u] = ldf((const TI*)p.q + xi);
+                nk[u] = p.rk[ri];
+                nq[u] = p.rq[ri];
+                xg[u] = ldf((const TI*)a.lg + ((bb * d.T + t) * d.Hv + h) * Dk + tid);
+            }
+            if (in && tid < KT) {
+                const int64_t vi = ((bb * d.T + t) * d.Hv + h) * d.Dv + col0 + tid;
+                xv[u] = ldf((const TI*)p.v + vi);
+                if (ob) xo[u] = ldf((const TI*)p.d_o + vi);
+            }
+            if (in && tid == 0) xb[u] = ldf((const TI*)a.beta + (bb * d.T + t) * d.Hv + h);
         }
-        if (in && tid < KT) {
-            const int64_t vi = ((bb * d.T + t) * d.Hv + h) * d.Dv + col0 + tid;
-            xv[i] = ldf((const TI*)p.v + vi);
-            if (ob) xo[i] = ldf((const TI*)p.d_o + vi);
-        }
-        if (in && tid == 0) xb[i] = ldf((const TI*)a.beta + (bb * d.T + t) * d.Hv + h);
-    }
 #pragma unroll
-    for (int i = 0; i < kSeg; ++i) {
-        if (i >= L) break;
-        if (tid < Dk) {
-            kh[i * Dk + tid] = xk[i] * nk[i];
-            qh[i * Dk + tid] = xq[i] * nq[i] * rsqrtf((float)Dk);
-            g[i * Dk + tid] = live[i] ? expf(xg[i]) : 1.f;
-        }
-        if (tid < KT) {
-            v[i * KT + tid] = xv[i];
-            if (ob) ob[i * KT + tid] = xo[i];
-        }
-        if (tid == 0) {
-            bt[i] = live[i] ? xb[i] : 0.f;
-            on[i] = live[i] ? 1 : 0;
+        for (int u = 0; u < NB; ++u) {
+            const int i = i0 + u;
+            if (i >= L) break;
+            if (tid < Dk) {
+                kh[i * Dk + tid] = xk[u] * nk[u];
+                qh[i * Dk + tid] = xq[u] * nq[u] * rsqrtf((float)Dk);
+                g[i * Dk + tid] = live[u] ? expf(xg[u]) : 1.f;
+            }
+            if (tid < KT) {
+                v[i * KT + tid] = xv[u];
+                if (ob) ob[i * KT + tid] = xo[u];
+            }
+            if (tid == 0) {
+                bt[i] = live[u] ? xb[u] : 0.f;
+                on[i] = live[u] ? 1 : 0;
+            }
         }
     }
 }
@@ -114,7 +118,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 // l, l + 32, ... (RR = Dk / 32 of them), so every per-step sum is a warp
 // shuffle and the steps need no CTA barrier (only the segment staging does).
 template <typename TI>
-__global__ void __launch_bounds__(kThreads) kc_fwd_kernel(Dims d, Ptrs p, KcArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) kc_fwd_kernel(Dims d, Ptrs p, KcArgs a) {
     extern __shared__ __align__(16) float kcf[];
     const int Dk = (int)d.Dk, Dv = (int)d.Dv, RR = Dk / 32;
     float* kh = kcf;                  // [kSeg][Dk]
@@ -148,7 +152,7 @@ __global__ void __launch_bounds__(kThreads) kc_fwd_kernel(Dims d, Ptrs p, KcArgs
                 }
         }
         __syncthreads();  // the previous segment's vectors have been read
-        load_seg<TI>(d, p, a, bb, h, t0, L, col0, kh, qh, gv, vv, nullptr, bt, on);
+        load_seg<TI, 2>(d, p, a, bb, h, t0, L, col0, kh, qh, gv, vv, nullptr, bt, on);
         __syncthreads();
         for (int i = 0; i < L; ++i) {
             const float* kk = kh + i * Dk;
@@ -238,7 +242,7 @@ __global__ void __launch_bounds__(kThreads) kc_bwd_kernel(Dims d, Ptrs p, KcArgs
         const int64_t t0 = sg * kSeg;
         const int L = (int)(d.T - t0 < kSeg ? d.T - t0 : kSeg);
         __syncthreads();  // the previous segment's shared memory is free
-        load_seg<TI>(d, p, a, bb, h, t0, L, col0, kh, qh, gv, vv, ob, bt, on);
+        load_seg<TI, kSeg>(d, p, a, bb, h, t0, L, col0, kh, qh, gv, vv, ob, bt, on);
         float S[kMaxR / 2][2];
         const float* ck = a.ckpt + (bh * NS + sg) * Dk * Dv + col0 + c0;
 #pragma unroll
