@@ -200,29 +200,32 @@ __global__ void __launch_bounds__(kThreads, 4) kc_fwd_kernel(Dims d, Ptrs p, KcA
 }
 
 // Backward, in the forward's decomposition (warp w: columns c0 = 2 w, + 1 of the
-// tile; lane l: rows l + 32 m).  Per segment (reverse order): the warp's states
-// of the segment are recomputed from its checkpoint into the warp's own slice
-// of shared memory, then walked back.  Column sums are warp shuffles; the row
-// sums over the tile's 16 columns (the q, k and log-decay cotangents) and the
-// beta cotangent are per-warp register sums, added over the 8 warps in warp
-// order through shared memory (double-buffered: one barrier per step).  The
-// tile's partials are written as if (h, tile) were value head h nt + tile of
-// B x (Hv nt) heads.
+// tile; lane l: rows l + 32 m).  Per segment (reverse order), in two halves of
+// kSub steps (the later half first): the warp's states of a half are recomputed
+// from the segment's checkpoint (the earlier half run through again for the
+// later one) into the warp's own slice of shared memory, then walked back.
+// Column sums are warp shuffles; the row sums over the tile's 16 columns (the
+// q, k and log-decay cotangents) and the beta cotangent are per-warp register
+// sums, added over the 8 warps in warp order through shared memory.  The tile's
+// partials are written as if (h, tile) were value head h nt + tile of
+// B x (Hv nt) heads.  Sized for two CTAs per SM.
+constexpr int kSub = kSeg / 2;
+
 template <typename TI>
-__global__ void __launch_bounds__(kThreads) kc_bwd_kernel(Dims d, Ptrs p, KcArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) kc_bwd_kernel(Dims d, Ptrs p, KcArgs a) {
     extern __shared__ __align__(16) float kcs[];
     const int Dk = (int)d.Dk, Dv = (int)d.Dv, RR = Dk / 32;
     constexpr int NW = kThreads / 32;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    float* hw = kcs + warp * (kSeg + 1) * 2 * Dk;     // this warp: [kSeg + 1][2][Dk] states
-    float* kh = kcs + NW * (kSeg + 1) * 2 * Dk;       // [kSeg][Dk]
+    float* hw = kcs + warp * (kSub + 1) * 2 * Dk;     // this warp: [kSub + 1][2][Dk] states
+    float* kh = kcs + NW * (kSub + 1) * 2 * Dk;       // [kSeg][Dk]
     float* qh = kh + kSeg * Dk;                       // [kSeg][Dk]
     float* gv = qh + kSeg * Dk;                       // [kSeg][Dk]
     float* vv = gv + kSeg * Dk;                       // [kSeg][KT]
     float* ob = vv + kSeg * KT;                       // [kSeg][KT] d_o
     float* bt = ob + kSeg * KT;                       // [kSeg]
-    float* rowp = bt + kSeg;                          // [2][NW][3 Dk + 1] per-warp row sums
-    int* on = reinterpret_cast<int*>(rowp + 2 * NW * (3 * Dk + 1));  // [kSeg]
+    float* rowp = bt + kSeg;                          // [NW][3 Dk + 1] per-warp row sums
+    int* on = reinterpret_cast<int*>(rowp + NW * (3 * Dk + 1));  // [kSeg]
     const int RP = 3 * Dk + 1;
     const int tile = blockIdx.x;
     const int64_t h = blockIdx.y, bb = blockIdx.z;
@@ -231,7 +234,6 @@ __global__ void __launch_bounds__(kThreads) kc_bwd_kernel(Dims d, Ptrs p, KcArgs
     const int64_t bh = bb * d.Hv + h;
     const int64_t hv2 = bb * d.Hv * nt + h * nt + tile;  // virtual head of the partials
     const int64_t NS = (d.T + kSeg - 1) / kSeg;
-    int nb = 0;
     float Sb[kMaxR / 2][2];
 #pragma unroll
     for (int m = 0; m < kMaxR / 2; ++m)
@@ -242,130 +244,150 @@ __global__ void __launch_bounds__(kThreads) kc_bwd_kernel(Dims d, Ptrs p, KcArgs
         const int64_t t0 = sg * kSeg;
         const int L = (int)(d.T - t0 < kSeg ? d.T - t0 : kSeg);
         __syncthreads();  // the previous segment's shared memory is free
-        load_seg<TI, kSeg>(d, p, a, bb, h, t0, L, col0, kh, qh, gv, vv, ob, bt, on);
-        float S[kMaxR / 2][2];
-        const float* ck = a.ckpt + (bh * NS + sg) * Dk * Dv + col0 + c0;
-#pragma unroll
-        for (int m = 0; m < kMaxR / 2; ++m)
-            if (m < RR) {
-                S[m][0] = ck[(int64_t)(lane + 32 * m) * Dv];
-                S[m][1] = ck[(int64_t)(lane + 32 * m) * Dv + 1];
-                hw[lane + 32 * m] = S[m][0];
-                hw[Dk + lane + 32 * m] = S[m][1];
-            }
+        load_seg<TI, 2>(d, p, a, bb, h, t0, L, col0, kh, qh, gv, vv, ob, bt, on);
         __syncthreads();
-        // the segment's states again, with delta and p of every step
-        float dls[kSeg][2], pcs[kSeg][2];
-#pragma unroll
-        for (int i = 0; i < kSeg; ++i) {
-            dls[i][0] = dls[i][1] = pcs[i][0] = pcs[i][1] = 0.f;
-            if (i >= L) continue;
-            const float* kk = kh + i * Dk;
-            const float* gg = gv + i * Dk;
-            float p0 = 0.f, p1 = 0.f;
+        const float* ck = a.ckpt + (bh * NS + sg) * Dk * Dv + col0 + c0;
+#pragma unroll 1
+        for (int half = 1; half >= 0; --half) {
+            const int h0 = half * kSub;
+            const int Lh = L - h0 < kSub ? L - h0 : kSub;
+            if (Lh <= 0) continue;
+            float S[kMaxR / 2][2];
 #pragma unroll
             for (int m = 0; m < kMaxR / 2; ++m)
                 if (m < RR) {
-                    const float gk = gg[lane + 32 * m] * kk[lane + 32 * m];
-                    p0 = fmaf(gk, S[m][0], p0);
-                    p1 = fmaf(gk, S[m][1], p1);
+                    S[m][0] = ck[(int64_t)(lane + 32 * m) * Dv];
+                    S[m][1] = ck[(int64_t)(lane + 32 * m) * Dv + 1];
                 }
-            p0 = warp_sum(p0);
-            p1 = warp_sum(p1);
-            pcs[i][0] = p0;
-            pcs[i][1] = p1;
-            if (on[i]) {
-                dls[i][0] = bt[i] * (vv[i * KT + c0] - p0);
-                dls[i][1] = bt[i] * (vv[i * KT + c0 + 1] - p1);
+            float dls[kSub][2], pcs[kSub][2];
+            // steps 0 .. h0 + Lh - 1 of the segment; the states of the half's steps kept
+#pragma unroll 1
+            for (int i = 0; i < h0 + Lh; ++i) {
+                const float* kk = kh + i * Dk;
+                const float* gg = gv + i * Dk;
+                if (i == h0) {
+#pragma unroll
+                    for (int m = 0; m < kMaxR / 2; ++m)
+                        if (m < RR) {
+                            hw[lane + 32 * m] = S[m][0];
+                            hw[Dk + lane + 32 * m] = S[m][1];
+                        }
+                }
+                float p0 = 0.f, p1 = 0.f;
 #pragma unroll
                 for (int m = 0; m < kMaxR / 2; ++m)
                     if (m < RR) {
-                        const float gi = gg[lane + 32 * m], ki = kk[lane + 32 * m];
-                        S[m][0] = fmaf(ki, dls[i][0], gi * S[m][0]);
-                        S[m][1] = fmaf(ki, dls[i][1], gi * S[m][1]);
+                        const float gk = gg[lane + 32 * m] * kk[lane + 32 * m];
+                        p0 = fmaf(gk, S[m][0], p0);
+                        p1 = fmaf(gk, S[m][1], p1);
                     }
+                p0 = warp_sum(p0);
+                p1 = warp_sum(p1);
+                float d0 = 0.f, d1 = 0.f;
+                if (on[i]) {
+                    d0 = bt[i] * (vv[i * KT + c0] - p0);
+                    d1 = bt[i] * (vv[i * KT + c0 + 1] - p1);
+#pragma unroll
+                    for (int m = 0; m < kMaxR / 2; ++m)
+                        if (m < RR) {
+                            const float gi = gg[lane + 32 * m], ki = kk[lane + 32 * m];
+                            S[m][0] = fmaf(ki, d0, gi * S[m][0]);
+                            S[m][1] = fmaf(ki, d1, gi * S[m][1]);
+                        }
+                }
+                if (i >= h0) {
+                    const int u = i - h0;
+#pragma unroll
+                    for (int uu = 0; uu < kSub; ++uu)
+                        if (uu == u) {
+                            dls[uu][0] = d0;
+                            dls[uu][1] = d1;
+                            pcs[uu][0] = p0;
+                            pcs[uu][1] = p1;
+                        }
+                    float* hs = hw + (u + 1) * 2 * Dk;
+#pragma unroll
+                    for (int m = 0; m < kMaxR / 2; ++m)
+                        if (m < RR) {
+                            hs[lane + 32 * m] = S[m][0];
+                            hs[Dk + lane + 32 * m] = S[m][1];
+                        }
+                }
             }
-            float* hs = hw + (i + 1) * 2 * Dk;
+            __syncwarp();  // the warp's own states (each lane rereads only its own rows)
+            // reverse over the half's steps
 #pragma unroll
-            for (int m = 0; m < kMaxR / 2; ++m)
-                if (m < RR) {
-                    hs[lane + 32 * m] = S[m][0];
-                    hs[Dk + lane + 32 * m] = S[m][1];
-                }
-        }
-        __syncwarp();  // the warp's own states (each lane rereads only its own rows)
-        // reverse over the segment's steps
-#pragma unroll
-        for (int i = kSeg - 1; i >= 0; --i) {
-            if (i >= L) continue;
-            const int64_t t = t0 + i;
-            const float* scur = hw + (i + 1) * 2 * Dk;
-            const float* sprev = hw + i * 2 * Dk;
-            const float* kk = kh + i * Dk;
-            const float* gg = gv + i * Dk;
-            const float* qq = qh + i * Dk;
-            const float o0 = ob[i * KT + c0], o1 = ob[i * KT + c0 + 1];
-            float* rp = rowp + (nb * NW + warp) * RP;
-            float db0 = 0.f, db1 = 0.f;
-#pragma unroll
-            for (int m = 0; m < kMaxR / 2; ++m)
-                if (m < RR) {
-                    const int r = lane + 32 * m;
-                    Sb[m][0] = fmaf(qq[r], o0, Sb[m][0]);
-                    Sb[m][1] = fmaf(qq[r], o1, Sb[m][1]);
-                    rp[r] = fmaf(scur[r], o0, scur[Dk + r] * o1);  // q cotangent, this warp's columns
-                    db0 = fmaf(Sb[m][0], kk[r], db0);
-                    db1 = fmaf(Sb[m][1], kk[r], db1);
-                }
-            if (on[i]) {
-                db0 = warp_sum(db0);
-                db1 = warp_sum(db1);
-                const float beta = bt[i];
-                if (lane < 2)
-                    stf((TI*)p.dv + ((bb * d.T + t) * d.Hv + h) * Dv + col0 + c0 + lane,
-                        beta * (lane == 0 ? db0 : db1));
-                const float pb0 = -beta * db0, pb1 = -beta * db1;
-                const float d0 = dls[i][0], d1 = dls[i][1];
-                if (lane == 0)
-                    rp[3 * Dk] = fmaf(db0, vv[i * KT + c0] - pcs[i][0], db1 * (vv[i * KT + c0 + 1] - pcs[i][1]));
+            for (int u = kSub - 1; u >= 0; --u) {
+                if (u >= Lh) continue;
+                const int i = h0 + u;
+                const int64_t t = t0 + i;
+                const float* scur = hw + (u + 1) * 2 * Dk;
+                const float* sprev = hw + u * 2 * Dk;
+                const float* kk = kh + i * Dk;
+                const float* gg = gv + i * Dk;
+                const float* qq = qh + i * Dk;
+                const float o0 = ob[i * KT + c0], o1 = ob[i * KT + c0 + 1];
+                float* rp = rowp + warp * RP;
+                float db0 = 0.f, db1 = 0.f;
 #pragma unroll
                 for (int m = 0; m < kMaxR / 2; ++m)
                     if (m < RR) {
                         const int r = lane + 32 * m;
-                        const float gi = gg[r], ki = kk[r];
-                        const float sp0 = sprev[r], sp1 = sprev[Dk + r];
-                        rp[Dk + r] = fmaf(Sb[m][0], d0, gi * sp0 * pb0) + fmaf(Sb[m][1], d1, gi * sp1 * pb1);
-                        Sb[m][0] = fmaf(ki, pb0, Sb[m][0]);  // Sbar_a
-                        Sb[m][1] = fmaf(ki, pb1, Sb[m][1]);
-                        rp[2 * Dk + r] = gi * fmaf(Sb[m][0], sp0, Sb[m][1] * sp1);
-                        Sb[m][0] *= gi;
-                        Sb[m][1] *= gi;
+                        Sb[m][0] = fmaf(qq[r], o0, Sb[m][0]);
+                        Sb[m][1] = fmaf(qq[r], o1, Sb[m][1]);
+                        rp[r] = fmaf(scur[r], o0, scur[Dk + r] * o1);  // q cotangent, this warp's columns
+                        db0 = fmaf(Sb[m][0], kk[r], db0);
+                        db1 = fmaf(Sb[m][1], kk[r], db1);
                     }
-            } else {
-                if (lane < 2)
-                    stf((TI*)p.dv + ((bb * d.T + t) * d.Hv + h) * Dv + col0 + c0 + lane, 0.f);
-                if (lane == 0) rp[3 * Dk] = 0.f;
+                if (on[i]) {
+                    db0 = warp_sum(db0);
+                    db1 = warp_sum(db1);
+                    const float beta = bt[i];
+                    if (lane < 2)
+                        stf((TI*)p.dv + ((bb * d.T + t) * d.Hv + h) * Dv + col0 + c0 + lane,
+                            beta * (lane == 0 ? db0 : db1));
+                    const float pb0 = -beta * db0, pb1 = -beta * db1;
+                    const float d0 = dls[u][0], d1 = dls[u][1];
+                    if (lane == 0)
+                        rp[3 * Dk] = fmaf(db0, vv[i * KT + c0] - pcs[u][0], db1 * (vv[i * KT + c0 + 1] - pcs[u][1]));
 #pragma unroll
-                for (int m = 0; m < kMaxR / 2; ++m)
-                    if (m < RR) {
-                        rp[Dk + lane + 32 * m] = 0.f;
-                        rp[2 * Dk + lane + 32 * m] = 0.f;
-                    }
-            }
-            __syncthreads();
-            // the tile's row sums: the eight warps' in warp order
-            const int64_t prow = (hv2 * d.Tp + t) * Dk;
-            const float* rb = rowp + nb * NW * RP;
-            for (int e = tid; e < RP; e += kThreads) {
-                float x = 0.f;
+                    for (int m = 0; m < kMaxR / 2; ++m)
+                        if (m < RR) {
+                            const int r = lane + 32 * m;
+                            const float gi = gg[r], ki = kk[r];
+                            const float sp0 = sprev[r], sp1 = sprev[Dk + r];
+                            rp[Dk + r] = fmaf(Sb[m][0], d0, gi * sp0 * pb0) + fmaf(Sb[m][1], d1, gi * sp1 * pb1);
+                            Sb[m][0] = fmaf(ki, pb0, Sb[m][0]);  // Sbar_a
+                            Sb[m][1] = fmaf(ki, pb1, Sb[m][1]);
+                            rp[2 * Dk + r] = gi * fmaf(Sb[m][0], sp0, Sb[m][1] * sp1);
+                            Sb[m][0] *= gi;
+                            Sb[m][1] *= gi;
+                        }
+                } else {
+                    if (lane < 2)
+                        stf((TI*)p.dv + ((bb * d.T + t) * d.Hv + h) * Dv + col0 + c0 + lane, 0.f);
+                    if (lane == 0) rp[3 * Dk] = 0.f;
 #pragma unroll
-                for (int w = 0; w < NW; ++w) x += rb[w * RP + e];
-                if (e < Dk) p.dqh[prow + e] = x;
-                else if (e < 2 * Dk) p.dkh[prow + e - Dk] = x;
-                else if (e < 3 * Dk) a.gpart[prow + e - 2 * Dk] = x;
-                else a.bpart[hv2 * d.Tp + t] = x;
+                    for (int m = 0; m < kMaxR / 2; ++m)
+                        if (m < RR) {
+                            rp[Dk + lane + 32 * m] = 0.f;
+                            rp[2 * Dk + lane + 32 * m] = 0.f;
+                        }
+                }
+                __syncthreads();
+                // the tile's row sums: the eight warps' in warp order
+                const int64_t prow = (hv2 * d.Tp + t) * Dk;
+                for (int e = tid; e < RP; e += kThreads) {
+                    float x = 0.f;
+#pragma unroll
+                    for (int w = 0; w < NW; ++w) x += rowp[w * RP + e];
+                    if (e < Dk) p.dqh[prow + e] = x;
+                    else if (e < 2 * Dk) p.dkh[prow + e - Dk] = x;
+                    else if (e < 3 * Dk) a.gpart[prow + e - 2 * Dk] = x;
+                    else a.bpart[hv2 * d.Tp + t] = x;
+                }
+                __syncthreads();  // rowp free for the next step
             }
-            nb ^= 1;
         }
     }
 #pragma unroll
@@ -402,8 +424,8 @@ size_t fwd_smem(const Dims& d) {
 
 size_t bwd_smem(const Dims& d) {
     const size_t NW = kThreads / 32;
-    return sizeof(float) * (NW * (kSeg + 1) * 2 * (size_t)d.Dk + 3 * (size_t)kSeg * d.Dk +
-                            2 * (size_t)kSeg * KT + kSeg + 2 * NW * (3 * (size_t)d.Dk + 1)) +
+    return sizeof(float) * (NW * (kSub + 1) * 2 * (size_t)d.Dk + 3 * (size_t)kSeg * d.Dk +
+                            2 * (size_t)kSeg * KT + kSeg + NW * (3 * (size_t)d.Dk + 1)) +
            sizeof(int) * kSeg;
 }
 
