@@ -68,7 +68,7 @@ def _peaks():
 # algorithmic work model (per launch of each phase)
 # ---------------------------------------------------------------------------
 
-def work_model(w, conv_k=0, gates="ab"):
+def work_model(w, conv_k=0, gates="ab", nseg=1):
     """Per-phase algorithmic flops and bytes of one fwd+bwd step, in the storage
     formats the kernels use: bf16 inputs keep the saved intermediates as bf16
     operand images (checkpoints, T, W, P, Delta as hi + lo, state cotangents,
@@ -98,6 +98,22 @@ def work_model(w, conv_k=0, gates="ab"):
         flops=units * (6 * C * Dk * Dv + 2 * C * C * Dv),
         bytes=qk + units * (C * Dk * es + C * C * es + C * Dv * 4 + Dk * Dv * img
                             + C * Dv * 4 + C * Dv * es) + 2 * BH * Dk * Dv * 4)
+    if nseg > 1:
+        # segmented scan: the maps scan segments 0 .. nseg - 2 over Wd = Dv + Dk
+        # (padded) columns (W, P, q, k images and U in, the maps out); the chain
+        # reads each map once and writes each start state; the scan proper then
+        # also reads the start states
+        L = -(-NC // nseg)
+        Wd = Dv + -(-Dk // 128) * 128
+        mu = BH * (nseg - 1) * L
+        m["fwd_seg_maps"] = dict(
+            flops=mu * (6 * C * Dk * Wd + 2 * C * C * Wd),
+            bytes=mu * (C * Dk * es + C * C * es + 2 * C * Dk * es + C * Dv * 4)
+            + BH * (nseg - 1) * Dk * Wd * 4)
+        m["fwd_seg_chain"] = dict(
+            flops=BH * (nseg - 1) * 2 * Dk * Dk * Dv,
+            bytes=BH * (nseg - 1) * Dk * (Wd + Dv) * 4)
+        m["fwd_scan"]["bytes"] += BH * (nseg - 1) * Dk * Dv * 4
     # dO, P, k, q, W in; chunk-end cotangent and -Dbar images out
     m["bwd_scan"] = dict(
         flops=units * (6 * C * Dk * Dv + 2 * C * C * Dv),
@@ -543,7 +559,8 @@ def run_ours(args, w, world, rank, local):
 
     # ---- per-phase roofline of the dominant kernel
     peaks = _peaks()
-    model = work_model(w, args.fused_conv, args.gates)
+    nseg = ops.segments_auto(shape) if shape is not None and args.gates != "kc" else 1
+    model = work_model(w, args.fused_conv, args.gates, nseg)
     ph = {phases[i].name.decode(): (phases[i].launches, phases[i].total_ms)
           for i in range(cnt.value)}
     dom = max(ph, key=lambda k: ph[k][1])
@@ -554,7 +571,7 @@ def run_ours(args, w, world, rank, local):
     # bf16 workloads run the chunk contractions on the tensor cores (tcgen05);
     # fp32 workloads run them as FFMA on the CUDA cores
     tensor = w.dtype == torch.bfloat16 and dom in ("fwd_chunk", "fwd_scan", "bwd_scan", "bwd_chunk",
-                                                  "bwd_scan_chunk")
+                                                  "bwd_scan_chunk", "fwd_seg_maps")
     cpeak = peaks["bf16_tflops"] if tensor else FP32_ALU_PEAK_TFLOPS
     t_cmp = fl / (cpeak * 1e12)
     traffic = measured_traffic(w.name, dom)

@@ -252,6 +252,65 @@ unsigned int read_clear_error_all() {
 }
 }  // namespace gdn
 
+namespace {
+// ---- segmented forward scan: sizing and the automatic segment count -------------
+bool seg_supported(const gdn::Dims& d) { return gdn::tc_path(d) && gdn::scan_ta_supported(d); }
+
+// segments actually formed from a requested count: len chunks each, none empty
+void seg_geometry(const gdn::Dims& d, int requested, int* nseg, int* len) {
+    int64_t r = requested < 1 ? 1 : requested;
+    if (r > d.NC) r = d.NC;
+    const int64_t l = (d.NC + r - 1) / r;
+    *len = (int)l;
+    *nseg = (int)((d.NC + l - 1) / l);
+}
+
+// extra forward workspace of nseg segments: the maps [nseg - 1][B][Hv][Dk][Wd] and
+// the chained start states [nseg - 1][B][Hv][Dk][Dv], fp32
+size_t seg_bytes(const gdn::Dims& d, int nseg) {
+    if (nseg <= 1) return 0;
+    const size_t n = (size_t)(nseg - 1) * d.B * d.Hv * d.Dk;
+    return align_up(n * gdn::seg_map_width(d) * 4) + align_up(n * d.Dv * 4);
+}
+
+// Segment count that minimises the modelled critical path, in units of one chunk
+// step of the scan: the plain scan takes waves(B Hv Dv/128) NC; with P segments of
+// L chunks, the maps take waves((P - 1) B Hv Wd/128) L, the chain (P - 1) steps of
+// about (Dk / 128)^2 chunk steps each (measured on GB300) and the scan proper
+// waves(P B Hv Dv/128) L, plus two launches (about one step each).
+int seg_auto(const gdn::Dims& d) {
+    if (!seg_supported(d)) return 1;
+    const int64_t sms = gdn::sm_count();
+    auto waves = [&](int64_t ctas) { return (double)((ctas + sms - 1) / sms); };
+    const int64_t tiles = d.B * d.Hv * (d.Dv / 128), mtiles = d.B * d.Hv * (gdn::seg_map_width(d) / 128);
+    double best = waves(tiles) * (double)d.NC;
+    const double chain = (double)(d.Dk * d.Dk) / (128.0 * 128.0);
+    int best_p = 1;
+    const int64_t pmax = d.NC < 4096 ? d.NC : 4096;
+    for (int64_t r = 2; r <= pmax; ++r) {
+        int nseg = 1, len = 1;
+        seg_geometry(d, (int)r, &nseg, &len);
+        if ((int64_t)nseg * d.B > 65535) break;
+        const double cost = (waves((nseg - 1) * mtiles) + waves(nseg * tiles)) * len + chain * (nseg - 1) + 2.0;
+        if (cost < best) {
+            best = cost;
+            best_p = nseg;
+        }
+    }
+    return best_p;
+}
+
+// segments and chunks per segment a request resolves to (0: the automatic count)
+int seg_resolve(const gdn::Dims& d, int requested, int* len) {
+    if (requested == 0) requested = seg_auto(d);
+    int nseg = 1;
+    *len = (int)d.NC;
+    if (requested > 1) seg_geometry(d, requested, &nseg, len);
+    return nseg;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* gdn_status_string(gdn_status status) {
@@ -274,9 +333,12 @@ gdn_status gdn_workspace_bytes(const gdn_shape* shape, int pass, size_t* bytes) 
     if (st != GDN_OK) return st;
     if (bytes == nullptr || pass < 0 || pass > 2) return GDN_ERR_INVALID_ARG;
     const Layout L = make_layout(d);
-    if (pass == 0) *bytes = L.fwd_total;
+    // the forward's segment buffers for the automatic segment count
+    int len = 0;
+    const size_t seg = pass == 1 ? 0 : seg_bytes(d, seg_resolve(d, 0, &len));
+    if (pass == 0) *bytes = L.fwd_total + seg;
     else if (pass == 1) *bytes = L.bwd_total;
-    else *bytes = L.fwd_total + L.saved_total;  // inference forward without a saved buffer
+    else *bytes = L.fwd_total + L.saved_total + seg;  // inference forward without a saved buffer
     return GDN_OK;
 }
 
@@ -296,11 +358,18 @@ gdn_status forward_impl(const gdn_shape* shape, int gates, const void* q, const 
                         const void* v, const void* a, const void* b, const float* A_log,
                         const float* dt_bias, const float* state0, const uint8_t* mask, void* o,
                         float* state_T, void* saved, size_t saved_bytes, void* ws,
-                        size_t ws_bytes, void* stream) {
+                        size_t ws_bytes, void* stream, int segments = 1) {
     gdn::Dims d;
     gdn_status st = validate_shape(shape, &d);
     if (st != GDN_OK) return st;
     d.gates = gates;
+    // segments of the scan (1: the plain sequential scan; 0: the automatic choice)
+    if (segments < 0) return GDN_ERR_INVALID_ARG;
+    if (segments > 1 && !seg_supported(d)) return GDN_ERR_UNSUPPORTED_SHAPE;
+    int len = 0;
+    const int nseg = seg_resolve(d, segments, &len);
+    if ((int64_t)nseg * d.B > 65535) return GDN_ERR_UNSUPPORTED_SHAPE;
+    const size_t sbytes = seg_bytes(d, nseg);
     if (!q || !k || !v || !a || !b || !o || !state_T) return GDN_ERR_INVALID_ARG;
     if (gates == 0 && (!A_log || !dt_bias)) return GDN_ERR_INVALID_ARG;
     if (shape->has_mask && !mask) return GDN_ERR_INVALID_ARG;
@@ -317,15 +386,17 @@ gdn_status forward_impl(const gdn_shape* shape, int gates, const void* q, const 
     if (saved == nullptr && d.T == 1 && gdn::decode_supported(d.Dk, d.Dv))
         return cuda_status(run_phase("decode", s, [&] { return gdn::launch_decode(d, p, s); }));
     char* wsb = static_cast<char*>(ws);
+    size_t used = L.fwd_total;  // the segment buffers follow the workspace proper
     if (saved != nullptr) {
         if (saved_bytes < L.saved_total) return GDN_ERR_WORKSPACE_TOO_SMALL;
         if (ws == nullptr) return GDN_ERR_INVALID_ARG;
-        if (ws_bytes < L.fwd_total) return GDN_ERR_WORKSPACE_TOO_SMALL;
+        if (ws_bytes < L.fwd_total + sbytes) return GDN_ERR_WORKSPACE_TOO_SMALL;
         carve_saved(L, saved, &p);
     } else {
         if (ws == nullptr) return GDN_ERR_INVALID_ARG;
-        if (ws_bytes < L.fwd_total + L.saved_total) return GDN_ERR_WORKSPACE_TOO_SMALL;
+        if (ws_bytes < L.fwd_total + L.saved_total + sbytes) return GDN_ERR_WORKSPACE_TOO_SMALL;
         carve_saved(L, wsb + L.fwd_total, &p);
+        used += L.saved_total;
     }
     p.U = reinterpret_cast<float*>(wsb + L.U);
     gdn::Tmaps maps;
@@ -335,7 +406,18 @@ gdn_status forward_impl(const gdn_shape* shape, int gates, const void* q, const 
     }
     cudaError_t e = run_phase("prep", s, [&] { return gdn::launch_prep(d, p, s); });
     if (e == cudaSuccess) e = run_phase("fwd_chunk", s, [&] { return gdn::launch_fwd_chunk(d, p, s); });
-    if (e == cudaSuccess) e = run_phase("fwd_scan", s, [&] { return gdn::launch_fwd_scan(d, p, s); });
+    if (e == cudaSuccess && nseg > 1) {
+        // segment maps, their chain, then every segment's scan at once
+        const size_t nmap = (size_t)(nseg - 1) * d.B * d.Hv * d.Dk;
+        gdn::ScanSeg sg{nseg, len, 1, reinterpret_cast<float*>(wsb + used + align_up(nmap * gdn::seg_map_width(d) * 4)),
+                        reinterpret_cast<float*>(wsb + used)};
+        e = run_phase("fwd_seg_maps", s, [&] { return gdn::launch_fwd_scan_ta_seg(d, p, sg, s); });
+        if (e == cudaSuccess) e = run_phase("fwd_seg_chain", s, [&] { return gdn::launch_seg_chain(d, p, sg, s); });
+        sg.mode = 0;
+        if (e == cudaSuccess) e = run_phase("fwd_scan", s, [&] { return gdn::launch_fwd_scan_ta_seg(d, p, sg, s); });
+    } else if (e == cudaSuccess) {
+        e = run_phase("fwd_scan", s, [&] { return gdn::launch_fwd_scan(d, p, s); });
+    }
     return cuda_status(e);
 }
 
@@ -407,7 +489,7 @@ gdn_status gdn_forward(const gdn_shape* shape, const void* q, const void* k, con
                        void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
                        void* stream) {
     return forward_impl(shape, 0, q, k, v, a, b, A_log, dt_bias, state0, mask, o, state_T, saved,
-                        saved_bytes, ws, ws_bytes, stream);
+                        saved_bytes, ws, ws_bytes, stream, 0);
 }
 
 gdn_status gdn_forward_lb(const gdn_shape* shape, const void* q, const void* k, const void* v,
@@ -415,7 +497,37 @@ gdn_status gdn_forward_lb(const gdn_shape* shape, const void* q, const void* k, 
                           const uint8_t* mask, void* o, float* state_T, void* saved,
                           size_t saved_bytes, void* ws, size_t ws_bytes, void* stream) {
     return forward_impl(shape, 1, q, k, v, log_decay, beta, nullptr, nullptr, state0, mask, o,
-                        state_T, saved, saved_bytes, ws, ws_bytes, stream);
+                        state_T, saved, saved_bytes, ws, ws_bytes, stream, 0);
+}
+
+gdn_status gdn_segments_auto(const gdn_shape* shape, int* segments) {
+    gdn::Dims d;
+    gdn_status st = validate_shape(shape, &d);
+    if (st != GDN_OK) return st;
+    if (segments == nullptr) return GDN_ERR_INVALID_ARG;
+    int len = 0;
+    *segments = seg_resolve(d, 0, &len);
+    return GDN_OK;
+}
+
+gdn_status gdn_segment_bytes(const gdn_shape* shape, int segments, size_t* bytes) {
+    gdn::Dims d;
+    gdn_status st = validate_shape(shape, &d);
+    if (st != GDN_OK) return st;
+    if (bytes == nullptr || segments < 0) return GDN_ERR_INVALID_ARG;
+    if (segments > 1 && !seg_supported(d)) return GDN_ERR_UNSUPPORTED_SHAPE;
+    int len = 0;
+    *bytes = seg_bytes(d, seg_resolve(d, segments, &len));
+    return GDN_OK;
+}
+
+gdn_status gdn_forward_segmented(const gdn_shape* shape, int segments, const void* q,
+                                 const void* k, const void* v, const void* a, const void* b,
+                                 const float* A_log, const float* dt_bias, const float* state0,
+                                 const uint8_t* mask, void* o, float* state_T, void* saved,
+                                 size_t saved_bytes, void* ws, size_t ws_bytes, void* stream) {
+    return forward_impl(shape, 0, q, k, v, a, b, A_log, dt_bias, state0, mask, o, state_T, saved,
+                        saved_bytes, ws, ws_bytes, stream, segments);
 }
 
 gdn_status gdn_backward(const gdn_shape* shape, const void* q, const void* k, const void* v,

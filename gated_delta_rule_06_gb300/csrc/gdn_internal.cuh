@@ -212,6 +212,26 @@ cudaError_t launch_bwd_scan_tc(const Dims& d, const Ptrs& p, cudaStream_t s);
 unsigned int read_clear_error_scantc();
 bool scan_ta_supported(const Dims& d);
 cudaError_t launch_fwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s);
+// Segmented forward scan.  The chunk transition S_{c+1} = A_c S_c + B_c is affine
+// in the state, so a run of chunks composes into one affine segment map.  The
+// chunks are cut into nseg segments of len chunks (the last may be shorter):
+//   mode 1 (maps): for segments 0 .. nseg - 2, the scan from the zero state (the
+//     offset B_s, value tiles of Dv) and, with U = 0, from the identity (the linear
+//     part A_s, value tiles over Dk padded to the tile width); the end states go to
+//     maps [nseg - 1][B][Hv][Dk][Wd], Wd = Dv + Dk padded, offset part first;
+//   the chain kernel: S_{s+1} = A_s S_s + B_s from S_0 = state0 into start
+//     [nseg - 1][B][Hv][Dk][Dv] (the start states of segments 1 ..);
+//   mode 0 (the scan proper): every segment from its start state at once, writing
+//     the checkpoints, Delta images and outputs of its chunks; the last segment
+//     writes the final state.
+struct ScanSeg {
+    int nseg, len, mode;
+    float* start;
+    float* maps;
+};
+int64_t seg_map_width(const Dims& d);  // Wd
+cudaError_t launch_fwd_scan_ta_seg(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s);
+cudaError_t launch_seg_chain(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s);
 cudaError_t launch_bwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s);
 unsigned int read_clear_error_scanta();
 bool fwd_chunk_tc_supported(const Dims& d);

@@ -69,6 +69,10 @@ __host__ __device__ inline TaCols ta_cols(int Dk) {
     return t;
 }
 
+// width of a segment map: the offset part (Dv columns), then the linear part (Dk
+// columns, padded to whole value tiles)
+__host__ __device__ inline int64_t seg_wd(int64_t Dk, int64_t Dv) { return Dv + (Dk + DVT - 1) / DVT * DVT; }
+
 // gam r_q / sqrt(Dk) of its step; each thread keeps one step
 __device__ __forceinline__ void scale_q(uint8_t* Q, const uint8_t* raw, int Dk) {
     const int t = threadIdx.x & (C - 1);
@@ -88,11 +92,12 @@ __device__ __forceinline__ void scale_q(uint8_t* Q, const uint8_t* raw, int Dk) 
 }
 
 __global__ void __launch_bounds__(kThreads + 32, 1)
-    fwd_scan_ta_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm) {
+    fwd_scan_ta_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm, ScanSeg sg) {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ uint64_t bar, barW, barQ, barK, barP, barU, barR[2], barD[2];
     __shared__ uint32_t tmem_sh;
-    const int tile = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
+    const int tile = blockIdx.x, h = blockIdx.y;
+    const int bb = (int)(blockIdx.z % d.B), sgi = (int)(blockIdx.z / d.B);  // batch, segment
     const int j = h / (int)d.G;
     const int Dk = (int)d.Dk, Dv = (int)d.Dv;
     const int n0 = tile * DVT;
@@ -106,6 +111,13 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     const TaSmem L = ta_plan(Dk);
     const TaCols TC = ta_cols(Dk);
     const int64_t bh = (int64_t)bb * d.Hv + h;
+    // chunks cb .. ce - 1 of segment sgi; barrier phases and double buffers count
+    // from cb (lp: the parity of a chunk within the segment)
+    const int64_t cb = (int64_t)sgi * sg.len;
+    const int64_t ce = cb + sg.len < d.NC ? cb + sg.len : d.NC;
+    auto lp = [&](int64_t c) { return (uint32_t)((c - cb) & 1); };
+    const bool maps = sg.mode != 0;       // segment maps: no checkpoints, Delta or outputs
+    const bool uz = maps && n0 >= Dv;     // linear part of a map: U = 0, identity start
     const uint32_t wbytes = (uint32_t)(C * Dk * 2), pbytes = (uint32_t)(C * C * 2);
     const uint8_t* Wimg = static_cast<const uint8_t*>(p.W);
     const uint8_t* Pimg = static_cast<const uint8_t*>(p.P);
@@ -133,7 +145,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::bulk_g2s(sm + L.K, static_cast<const uint8_t*>(p.kimg) + (kq * d.NC + c) * wbytes, wbytes, &barK);
     };
     auto load_raw = [&](int64_t c) {
-        const int s = (int)(c & 1);
+        const int s = (int)lp(c);
         uint8_t* dst = sm + L.raw + s * kRawBytes;
         tc::mbar_arrive_expect_tx(&barR[s], kRawBytes);
         tc::bulk_g2s(dst, p.gam + bh * d.Tp + c * C, C * 8, &barR[s]);
@@ -165,7 +177,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     // output rows of chunk c (buffer c & 1) -> staging
     auto step5 = [&](uint32_t tb, int64_t c) {
         float a[2][16];
-        const uint32_t col = TC.o0 + (uint32_t)(c & 1) * 64u + 32u * g;
+        const uint32_t col = TC.o0 + lp(c) * 64u + 32u * g;
         tc::tmem_ld16(tc::tmem_addr(tb, lb, col), a[0]);
         tc::tmem_ld16(tc::tmem_addr(tb, lb, col + 16), a[1]);
         tc::tmem_wait_ld();
@@ -193,26 +205,31 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     }
     __syncthreads();  // barriers initialised
     if (prod) {
-        load_w(0);
-        load_q(0);
-        load_k(0);
-        load_p(0);
-        load_u(0);
-        load_raw(0);
-        if (d.NC > 1) load_raw(1);
+        load_w(cb);
+        load_q(cb);
+        load_k(cb);
+        load_p(cb);
+        if (!uz) load_u(cb);
+        load_raw(cb);
+        if (ce - cb > 1) load_raw(cb + 1);
     }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tb = tmem_sh;
     const int halfk = Dk / 2;
-    const int64_t sbase = bh * Dk * Dv + n0;
+    // start state (rows dk, row stride Dv): state0 for the first segment, the
+    // chained start states for the others; zero / the identity for the maps
+    const float* sin = nullptr;
+    if (!maps && sgi == 0 && p.state0) sin = p.state0 + bh * Dk * Dv + n0;
+    if (!maps && sgi > 0) sin = sg.start + ((int64_t)(sgi - 1) * d.B * d.Hv + bh) * Dk * Dv + n0;
     bool ok = true;
     if (epi) {
         for (int cc = g * halfk; cc < (g + 1) * halfk; cc += 16) {  // initial state -> TMEM
             float v[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = p.state0 ? p.state0[sbase + (int64_t)(cc + i) * Dv + r] : 0.f;
+            for (int i = 0; i < 16; ++i)
+                v[i] = uz ? (cc + i == n0 - Dv + r ? 1.f : 0.f) : sin ? sin[(int64_t)(cc + i) * Dv + r] : 0.f;
             tc::tmem_st16(tc::tmem_addr(tb, lb, cc), v);
         }
         tc::tmem_wait_st();
@@ -232,13 +249,13 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     const tc::Tile tKmn = tc::panel_tile(sm + L.K, C, false);  // B = K: x = dk = N
     uint32_t phase = 0;
 
-    for (int64_t c = 0; c < d.NC; ++c) {
-        const float* vb = reinterpret_cast<const float*>(sm + L.vec) + (c & 1) * 4 * C;
+    for (int64_t c = cb; c < ce; ++c) {
+        const float* vb = reinterpret_cast<const float*>(sm + L.vec) + lp(c) * 4 * C;
         const float* kev = vb + 3 * C;
         const float gC = vb[C - 1];
-        const uint32_t ocol = TC.o0 + (uint32_t)(c & 1) * 64u;
+        const uint32_t ocol = TC.o0 + lp(c) * 64u;
         if (storer) {  // Delta images of chunk c - 1, staged before the barrier above
-            if (c > 0) store_delta(c - 1);
+            if (!maps && c > cb) store_delta(c - 1);
             tc::bulk_commit();
         }
         // step 1: S^T -> A operand (bf16 pairs in TMEM); S^T *= gam_63
@@ -273,7 +290,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         if (prod) {
             // step 2: Delta^T acc = S^T W^T and O^T = S^T Qs^T, two independent
             // accumulation chains interleaved
-            ok = tc::mbar_wait(&barW, (uint32_t)(c & 1), &g_err_scanta) && ok;
+            ok = tc::mbar_wait(&barW, lp(c), &g_err_scanta) && ok;
             const uint32_t id = tc::idesc_bf16(DVT, C, false, false);
             uint64_t dw = tW.desc(0), dq = tQ.desc(0);
             const uint64_t iw = tW.desc_step(), iq = tQ.desc_step();
@@ -286,7 +303,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             tc::mma_commit(&bar);
             ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
             phase ^= 1u;
-            if (c + 1 < d.NC) {
+            if (c + 1 < ce) {
                 load_w(c + 1);
                 load_q(c + 1);
             }
@@ -302,7 +319,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
                     *reinterpret_cast<uint4*>(sm + L.St + tc::panel_off(2 * cb + 8 * q4, r, DVT)) =
                         make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
             }
-            if (c > 0) step5(tb, c - 1);
+            if (!maps && c > cb) step5(tb, c - 1);
             tc::fence_async_smem();
             ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
             phase ^= 1u;
@@ -310,7 +327,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             // step 3: Delta^T = U^T - acc -> A operands hi, lo and (diag(e r_k)) hi, lo,
             // in two passes of 16 steps (32 g + 16 u2 .. + 15), each handed to the
             // MMA issuer on its own barrier
-            ok = tc::mbar_wait(&barU, (uint32_t)(c & 1), &g_err_scanta) && ok;
+            if (!uz) ok = tc::mbar_wait(&barU, lp(c), &g_err_scanta) && ok;
             float a[2][16];
             tc::tmem_ld16(tc::tmem_addr(tb, lb, TC.dacc + 32 * g), a[0]);
             tc::tmem_ld16(tc::tmem_addr(tb, lb, TC.dacc + 32 * g + 16), a[1]);
@@ -324,7 +341,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int ti = 2 * i + u;  // step 32 g + ti
-                        dl[u] = Ub[(32 * g + ti) * DVT + r] - a[ti >> 4][ti & 15];
+                        dl[u] = (uz ? 0.f : Ub[(32 * g + ti) * DVT + r]) - a[ti >> 4][ti & 15];
                         lo[u] = dl[u] - __bfloat162float(__float2bfloat16_rn(dl[u]));
                         de[u] = dl[u] * kev[32 * g + ti];
                         dlo[u] = de[u] - __bfloat162float(__float2bfloat16_rn(de[u]));
@@ -348,15 +365,15 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         if (prod) {
             // step 4: O^T += Delta^T P^T (hi, lo);  S^T += (Delta^T diag(e r_k)) K (hi, lo);
             // the steps of pass u2 (16-step slices u2 and 2 + u2) once it is handed over
-            ok = tc::mbar_wait(&barP, (uint32_t)(c & 1), &g_err_scanta) && ok;
-            ok = tc::mbar_wait(&barK, (uint32_t)(c & 1), &g_err_scanta) && ok;
+            ok = tc::mbar_wait(&barP, lp(c), &g_err_scanta) && ok;
+            ok = tc::mbar_wait(&barK, lp(c), &g_err_scanta) && ok;
             const uint32_t idp = tc::idesc_bf16(DVT, C, false, false);
             const uint32_t idk = tc::idesc_bf16(DVT, Dk, false, true);
             const uint64_t dp0 = tP.desc(0), ip = tP.desc_step();
             const uint64_t dk0 = tKmn.desc(0), ik = tKmn.desc_step();
 #pragma unroll
             for (int u2 = 0; u2 < 2; ++u2) {
-                ok = tc::mbar_wait(&barD[u2], (uint32_t)(c & 1), &g_err_scanta) && ok;
+                ok = tc::mbar_wait(&barD[u2], lp(c), &g_err_scanta) && ok;
                 tc::tc_fence_after();
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -367,18 +384,20 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
                 }
             }
             tc::mma_commit(&bar);
-            if (c + 1 < d.NC) load_u(c + 1);  // step 3 of chunk c has read U
+            if (!uz && c + 1 < ce) load_u(c + 1);  // step 3 of chunk c has read U
             ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
             phase ^= 1u;
-            if (c + 1 < d.NC) {
+            if (c + 1 < ce) {
                 load_k(c + 1);
                 load_p(c + 1);
             }
-            if (c + 2 < d.NC) load_raw(c + 2);
+            if (c + 2 < ce) load_raw(c + 2);
         } else if (epi) {
             if (storer) {
-                store_ck(c);
-                if (c > 0) store_o(c - 1);
+                if (!maps) {
+                    store_ck(c);
+                    if (c > cb) store_o(c - 1);
+                }
                 tc::bulk_commit();
             }
             // meanwhile: Delta image staging, U / vectors / scaled q of chunk c + 1
@@ -390,11 +409,12 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
                 *reinterpret_cast<uint4*>(sm + L.Dlo + off) =
                     make_uint4(low[4 * q4], low[4 * q4 + 1], low[4 * q4 + 2], low[4 * q4 + 3]);
             }
-            if (c + 1 < d.NC) {
-                const uint8_t* raw = sm + L.raw + ((c + 1) & 1) * kRawBytes;
-                ok = tc::mbar_wait(&barR[(c + 1) & 1], (uint32_t)(((c + 1) >> 1) & 1), &g_err_scanta) && ok;
-                vectors_from_raw(raw, reinterpret_cast<float*>(sm + L.vec) + ((c + 1) & 1) * 4 * C, Dk);
-                ok = tc::mbar_wait(&barQ, (uint32_t)((c + 1) & 1), &g_err_scanta) && ok;
+            if (c + 1 < ce) {
+                const int64_t l1 = c + 1 - cb;
+                const uint8_t* raw = sm + L.raw + (l1 & 1) * kRawBytes;
+                ok = tc::mbar_wait(&barR[l1 & 1], (uint32_t)((l1 >> 1) & 1), &g_err_scanta) && ok;
+                vectors_from_raw(raw, reinterpret_cast<float*>(sm + L.vec) + (l1 & 1) * 4 * C, Dk);
+                ok = tc::mbar_wait(&barQ, (uint32_t)(l1 & 1), &g_err_scanta) && ok;
                 scale_q(sm + L.Q, raw, Dk);
             }
             tc::fence_async_smem();
@@ -403,29 +423,38 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             tc::tc_fence_after();
         }
         // before the last chunk's output rows are staged: all stores have read out
-        if (storer && c + 1 == d.NC) tc::bulk_wait_read_all();
+        if (storer && c + 1 == ce) tc::bulk_wait_read_all();
         tc::tc_fence_before();
         __syncthreads();  // (A) of chunk c + 1
         tc::tc_fence_after();
     }
     // the last chunk's output rows and Delta images
-    if (epi) step5(tb, d.NC - 1);
+    if (epi && !maps) step5(tb, ce - 1);
     tc::fence_async_smem();
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (storer) {
-        store_delta(d.NC - 1);
-        store_o(d.NC - 1);
+    if (storer && !maps) {
+        store_delta(ce - 1);
+        store_o(ce - 1);
         tc::bulk_commit();
     }
-    if (epi) {
+    // end state: the final state (last segment) or the segment map's columns
+    float* sout = nullptr;
+    int64_t ostr = Dv;
+    if (maps) {
+        ostr = seg_wd(Dk, Dv);
+        sout = sg.maps + ((int64_t)sgi * d.B * d.Hv + bh) * Dk * ostr + n0;
+    } else if (sgi == sg.nseg - 1) {
+        sout = p.state_T + bh * Dk * Dv + n0;
+    }
+    if (epi && sout) {
         for (int cc = g * halfk; cc < (g + 1) * halfk; cc += 16) {
             float v[16];
             tc::tmem_ld16(tc::tmem_addr(tb, lb, cc), v);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) p.state_T[sbase + (int64_t)(cc + i) * Dv + r] = v[i];
+            for (int i = 0; i < 16; ++i) sout[(int64_t)(cc + i) * ostr + r] = v[i];
         }
     }
     if (storer) tc::bulk_wait_all();
@@ -452,9 +481,114 @@ cudaError_t launch_fwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);
-    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps);
+    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps, ScanSeg{1, (int)d.NC, 0, nullptr, nullptr});
     count_launches(1);
     return cudaPeekAtLastError();
+}
+
+int64_t seg_map_width(const Dims& d) { return seg_wd(d.Dk, d.Dv); }
+
+cudaError_t launch_fwd_scan_ta_seg(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s) {
+    const size_t smem = ta_plan((int)d.Dk).total + 1024;
+    auto kern = fwd_scan_ta_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int64_t nx = sg.mode == 0 ? d.Dv / DVT : seg_wd(d.Dk, d.Dv) / DVT;
+    const int64_t nz = (sg.mode == 0 ? sg.nseg : sg.nseg - 1) * d.B;
+    dim3 grid((unsigned)nx, (unsigned)d.Hv, (unsigned)nz);
+    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps, sg);
+    count_launches(1);
+    return cudaPeekAtLastError();
+}
+
+namespace {
+constexpr int kChainCols = 8;  // value columns of the state per chain CTA
+constexpr int kChainThreads = 256;
+constexpr int kChainRowGroups = kChainThreads / kChainCols;
+
+// S_{s+1} = A_s S_s + B_s for s = 0 .. nseg - 2 from S_0 = state0 (zero when
+// null), fp32 on the CUDA cores, each entry summed over k in ascending order.
+// One CTA per (8 value columns, value head, batch) keeps its columns of the
+// state in shared memory and stages each A_s there with asynchronous 16-byte
+// copies (all in flight at once); thread (row group rg, column n) forms rows rg + 32 j,
+// j < R = Dk / 32, as R independent sums.
+template <int R>
+__global__ void __launch_bounds__(kChainThreads)
+    seg_chain_kernel(Dims d, const float* __restrict__ state0, ScanSeg sg) {
+    constexpr int Dk = 32 * R;
+    // rows of A padded by 4 floats: the 4 rows a warp reads fall in distinct banks
+    constexpr int AS = Dk + 4;
+    extern __shared__ __align__(16) float cs[];  // A [Dk][AS], then S [2][Dk][8]
+    float* As = cs;
+    float* cur = cs + Dk * AS;
+    float* nxt = cur + Dk * kChainCols;
+    const int n0 = blockIdx.x * kChainCols, h = blockIdx.y, bb = blockIdx.z;
+    const int Dv = (int)d.Dv;
+    const int64_t bh = (int64_t)bb * d.Hv + h;
+    const int64_t Wd = seg_wd(Dk, Dv);
+    const int n = threadIdx.x % kChainCols, rg = threadIdx.x / kChainCols;
+    for (int i = threadIdx.x; i < Dk * kChainCols; i += kChainThreads)
+        cur[i] = state0 ? state0[(bh * Dk + i / kChainCols) * Dv + n0 + i % kChainCols] : 0.f;
+    for (int sgi = 0; sgi + 1 < sg.nseg; ++sgi) {
+        const float* M = sg.maps + ((int64_t)sgi * d.B * d.Hv + bh) * Dk * Wd;  // rows: [B_s | A_s]
+        __syncthreads();  // the previous step's reads of As are done
+        for (int e = threadIdx.x; e < Dk * Dk / 4; e += kChainThreads) {  // async copies, all in flight
+            const int i = e / (Dk / 4), k4 = e % (Dk / 4);
+            tc::cp_async16(tc::smem_u32(As + i * AS + 4 * k4), M + (int64_t)i * Wd + Dv + 4 * k4, 16);
+        }
+        tc::cp_async_commit();
+        float acc[R];
+#pragma unroll
+        for (int j = 0; j < R; ++j) acc[j] = M[(int64_t)(rg + kChainRowGroups * j) * Wd + n0 + n];
+        tc::cp_async_wait_all();
+        __syncthreads();  // As staged
+#pragma unroll 4
+        for (int k = 0; k < Dk; k += 4) {
+            const float s0 = cur[(k + 0) * kChainCols + n], s1 = cur[(k + 1) * kChainCols + n];
+            const float s2 = cur[(k + 2) * kChainCols + n], s3 = cur[(k + 3) * kChainCols + n];
+#pragma unroll
+            for (int j = 0; j < R; ++j) {
+                const float4 a = *reinterpret_cast<const float4*>(As + (rg + kChainRowGroups * j) * AS + k);
+                acc[j] = fmaf(a.x, s0, acc[j]);
+                acc[j] = fmaf(a.y, s1, acc[j]);
+                acc[j] = fmaf(a.z, s2, acc[j]);
+                acc[j] = fmaf(a.w, s3, acc[j]);
+            }
+        }
+        float* out = sg.start + ((int64_t)sgi * d.B * d.Hv + bh) * Dk * Dv + n0;
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const int i = rg + kChainRowGroups * j;
+            nxt[i * kChainCols + n] = acc[j];
+            out[(int64_t)i * Dv + n] = acc[j];
+        }
+        float* t = cur;
+        cur = nxt;
+        nxt = t;
+    }
+}
+
+template <int R>
+cudaError_t launch_chain_r(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s) {
+    constexpr int Dk = 32 * R;
+    const size_t smem = ((size_t)Dk * (Dk + 4) + 2 * (size_t)Dk * kChainCols) * sizeof(float);
+    auto kern = seg_chain_kernel<R>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)(d.Dv / kChainCols), (unsigned)d.Hv, (unsigned)d.B);
+    kern<<<grid, kChainThreads, smem, s>>>(d, p.state0, sg);
+    count_launches(1);
+    return cudaPeekAtLastError();
+}
+}  // namespace
+
+cudaError_t launch_seg_chain(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s) {
+    switch (d.Dk) {  // the tensor-core scan's key widths
+        case 64: return launch_chain_r<2>(d, p, sg, s);
+        case 128: return launch_chain_r<4>(d, p, sg, s);
+        case 192: return launch_chain_r<6>(d, p, sg, s);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace gdn

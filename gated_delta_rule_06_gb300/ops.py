@@ -82,6 +82,12 @@ def load_library(path: str = LIB_PATH):
         lib.gdn_backward.restype = i32
         lib.gdn_forward_lb.argtypes = [shp] + [vp] * 9 + [vp, sz, vp, sz, vp]
         lib.gdn_forward_lb.restype = i32
+        lib.gdn_forward_segmented.argtypes = [shp, i32] + [vp] * 11 + [vp, sz, vp, sz, vp]
+        lib.gdn_forward_segmented.restype = i32
+        lib.gdn_segment_bytes.argtypes = [shp, i32, ctypes.POINTER(sz)]
+        lib.gdn_segment_bytes.restype = i32
+        lib.gdn_segments_auto.argtypes = [shp, ctypes.POINTER(i32)]
+        lib.gdn_segments_auto.restype = i32
         lib.gdn_backward_lb.argtypes = [shp] + [vp] * 7 + [sz] + [vp] * 8 + [vp, sz, vp]
         lib.gdn_backward_lb.restype = i32
         lib.gdn_causal_conv1d_update.argtypes = [ctypes.c_int64] * 4 + [i32] + [vp] * 6
@@ -172,11 +178,27 @@ def _buf(nbytes: int, device) -> torch.Tensor:
     return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
 
 
+def segment_bytes(shape, segments: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().gdn_segment_bytes(ctypes.byref(shape), int(segments), ctypes.byref(n)))
+    return n.value
+
+
+def segments_auto(shape) -> int:
+    n = ctypes.c_int(0)
+    _check(load_library().gdn_segments_auto(ctypes.byref(shape), ctypes.byref(n)))
+    return n.value
+
+
 def forward(q, k, v, a, b, A_log, dt_bias, state0=None, mask=None, *, keep_saved=True,
-            out=None):
-    """Run gdn_forward.  Returns (o, state_T, saved) with saved=None when
+            out=None, segments=None):
+    """Run gdn_forward (the scan split into segments when the library's
+    automatic choice says so).  Returns (o, state_T, saved) with saved=None when
     keep_saved is False (inference).  ``out`` may pass preallocated
-    dict(o=, state_T=, saved=, ws=) buffers."""
+    dict(o=, state_T=, saved=, ws=) buffers.  An integer ``segments`` runs
+    gdn_forward_segmented with that count instead (1: the plain scan, 0: the
+    automatic count); its saved buffer is the same, and ws then also holds the
+    segment buffers of that count."""
     dt = q.dtype
     for n, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b)):
         _cuda(t, n, dt)
@@ -201,19 +223,25 @@ def forward(q, k, v, a, b, A_log, dt_bias, state0=None, mask=None, *, keep_saved
             saved = _buf(saved_bytes(shape), q.device)
         ws = out.get("ws")
         if ws is None:
-            ws = _buf(workspace_bytes(shape, 0), q.device)
+            extra = segment_bytes(shape, segments) if segments is not None else 0
+            ws = _buf(workspace_bytes(shape, 0) + extra, q.device)
     else:
         # T == 1 runs the single-step decode kernel, which needs no workspace
         # (it handles Dk * Dv <= 32768 with Dv % 4 == 0); otherwise the chunked
         # forward runs with its intermediates in an inference workspace.
         ws = out.get("ws")
         if ws is None and not (T == 1 and Dk * Dv <= 32768 and Dv % 4 == 0):
-            ws = _buf(workspace_bytes(shape, 2), q.device)
-    rc = load_library().gdn_forward(
-        ctypes.byref(shape), _p(q), _p(k), _p(v), _p(a), _p(b), _p(A_log), _p(dt_bias),
-        _p(state0), _p(m), _p(o), _p(sT), _p(saved),
-        ctypes.c_size_t(saved.numel() if saved is not None else 0), _p(ws),
-        ctypes.c_size_t(ws.numel() if ws is not None else 0), _stream())
+            extra = segment_bytes(shape, segments) if segments is not None else 0
+            ws = _buf(workspace_bytes(shape, 2) + extra, q.device)
+    lib = load_library()
+    args = (_p(q), _p(k), _p(v), _p(a), _p(b), _p(A_log), _p(dt_bias),
+            _p(state0), _p(m), _p(o), _p(sT), _p(saved),
+            ctypes.c_size_t(saved.numel() if saved is not None else 0), _p(ws),
+            ctypes.c_size_t(ws.numel() if ws is not None else 0), _stream())
+    if segments is None:
+        rc = lib.gdn_forward(ctypes.byref(shape), *args)
+    else:
+        rc = lib.gdn_forward_segmented(ctypes.byref(shape), int(segments), *args)
     _check(rc)
     return o, sT, saved
 

@@ -78,11 +78,16 @@ WORKLOADS = {
                                         seed=1003),
     "decode_B256_bf16": Workload("decode_B256_bf16", 256, 1, 16, 32, 128, 128, torch.bfloat16,
                                  "log_uniform_1_16", 0.02, False, backward=False, seed=1004),
+    # few (batch, head) pairs over a long sequence: the case the segmented scan is for
+    "long_B1_T65536_Hv8_bf16": Workload("long_B1_T65536_Hv8_bf16", 1, 65536, 4, 8, 128, 128,
+                                        torch.bfloat16, "log_uniform_1_16", 0.02, False,
+                                        seed=1005),
 }
 
 # index order used in docs and the bench: 0 toy, 1 mask, 2 9B layer, 3 batch, 4 decode
+# (then the long-sequence case of the segmented scan)
 WORKLOAD_ORDER = ["toy_fp32", "chunk_mask_fp32", "qwen35_9b_layer_T2048_bf16",
-                  "gqa_train_B4_T4096_bf16", "decode_B256_bf16"]
+                  "gqa_train_B4_T4096_bf16", "decode_B256_bf16", "long_B1_T65536_Hv8_bf16"]
 
 
 def custom(name: str, B: int, T: int, Hk: int, Hv: int, Dk: int, Dv: int,

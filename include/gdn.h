@@ -143,6 +143,48 @@ gdn_status gdn_backward_lb(const gdn_shape* shape, const void* q, const void* k,
                            void* dv, void* d_log_decay, void* d_beta, float* dstate0,
                            void* ws, size_t ws_bytes, void* stream);
 
+/* ---- segmented (associative) forward scan -------------------------------- */
+
+/* The state recurrence of one chunk is an affine map of the state,
+ * S_{c+1} = A_c S_c + B_c with A_c = gam_C I - K^T diag(e) W and
+ * B_c = K^T diag(e) U, and affine maps compose associatively (mlx-lm page,
+ * "Post-initial-submission extensions", Extension 5: the recurrence as an
+ * associative monoid, for scans that are not one sequential pass).
+ * gdn_forward_segmented cuts the chunks into `segments` runs of equal length
+ * (the last may be shorter), forms every run's composed map but the last in
+ * parallel (the scan from the zero state gives its offset, the scan from the
+ * identity with U = 0 its linear part), chains the run start states
+ * S_{s+1} = A_s S_s + B_s in fp32, and then scans every run from its start state
+ * at once.  Its results are those of gdn_forward up to rounding, and its saved
+ * buffer is the same (gdn_backward consumes it unchanged): it only shortens
+ * the sequential chain when B * Hv * (Dv / 128) leaves SMs idle and T is long.
+ *   - Arguments, layouts and saved-buffer rules as gdn_forward (a, b, A_log,
+ *     dt_bias gates).  ws must hold gdn_workspace_bytes(shape, 0) bytes
+ *     (gdn_workspace_bytes(shape, 2) when saved is NULL) plus
+ *     gdn_segment_bytes(shape, segments) bytes.
+ *   - segments = 1: the plain scan (as gdn_forward); 0: the count
+ *     gdn_segments_auto picks; above the number of chunks it is clamped.
+ *   - segments > 1 requires bf16 with Dv % 128 == 0 and Dk in {64, 128, 192}
+ *     (the tensor-core scan), and B * segments <= 65535; otherwise
+ *     GDN_ERR_UNSUPPORTED_SHAPE.  T == 1 with saved == NULL runs the decode
+ *     kernel as gdn_forward does. */
+gdn_status gdn_forward_segmented(const gdn_shape* shape, int segments, const void* q,
+                                 const void* k, const void* v, const void* a, const void* b,
+                                 const float* A_log, const float* dt_bias, const float* state0,
+                                 const uint8_t* mask, void* o, float* state_T, void* saved,
+                                 size_t saved_bytes, void* ws, size_t ws_bytes, void* stream);
+
+/* Extra workspace bytes of gdn_forward_segmented with `segments` (0 = automatic):
+ * the segment maps [segments - 1][B][Hv][Dk][Dv + Dk rounded up to 128] and the
+ * chained start states [segments - 1][B][Hv][Dk][Dv], fp32.  0 for one segment.
+ * Host-only. */
+gdn_status gdn_segment_bytes(const gdn_shape* shape, int segments, size_t* bytes);
+
+/* The segment count the automatic choice takes (1 = the plain scan): the count
+ * that minimises a model of the sequential chain, in waves of the GPU's SMs times
+ * chunks per run.  Reads the SM count of the current device. */
+gdn_status gdn_segments_auto(const gdn_shape* shape, int* segments);
+
 /* ---- per-key-channel gates ------------------------------------------------ */
 
 /* The vectorised gating the mlx-lm page lists (g.ndim == 4, "Scope and

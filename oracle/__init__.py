@@ -67,6 +67,8 @@ def _load():
         lib.gdn_oracle_forward.restype = ctypes.c_int
         lib.gdn_oracle_forward_chunked.argtypes = [i64] * 7 + [dp] * 11
         lib.gdn_oracle_forward_chunked.restype = ctypes.c_int
+        lib.gdn_oracle_forward_monoid.argtypes = [i64] * 7 + [dp] * 11
+        lib.gdn_oracle_forward_monoid.restype = ctypes.c_int
         lib.gdn_oracle_backward.argtypes = [i64] * 6 + [dp] * 19
         lib.gdn_oracle_backward.restype = ctypes.c_int
         lib.gdn_oracle_forward_lb.argtypes = [i64] * 6 + [dp] * 9
@@ -144,6 +146,24 @@ def forward_chunked(q, k, v, a, b, A_log, dt_bias, state0=None, mask=None, chunk
         q, k, v, a, b, A_log, dt_bias, state0, mask, o, sT)))
     if rc:
         raise ValueError(f"oracle chunked forward rejected the shapes (code {rc})")
+    return o, sT
+
+
+def forward_monoid(q, k, v, a, b, A_log, dt_bias, state0=None, mask=None, seg_len=64):
+    """The same recurrence evaluated through its associative form (mlx-lm page,
+    "Post-initial-submission extensions", Extension 5): per-step affine maps of
+    the state composed into runs of seg_len steps, an exclusive tree prefix over
+    the run maps for the run start states, each run replayed from its start.
+    Returns (o, state_T)."""
+    q, k, v, a, b, A_log, dt_bias, state0 = map(_f64, (q, k, v, a, b, A_log, dt_bias, state0))
+    mask = _u8(mask)
+    B, T, Hk, Hv, Dk, Dv = _dims(q, v)
+    o = np.zeros((B, T, Hv, Dv))
+    sT = np.zeros((B, Hv, Dk, Dv))
+    rc = _load().gdn_oracle_forward_monoid(B, T, Hk, Hv, Dk, Dv, int(seg_len), *map(_ptr, (
+        q, k, v, a, b, A_log, dt_bias, state0, mask, o, sT)))
+    if rc:
+        raise ValueError(f"oracle monoid forward rejected the arguments (code {rc})")
     return o, sT
 
 

@@ -50,6 +50,11 @@
  *    follow-ups": chunk-parallel rewrite through a lower-triangular solve):
  *    an independent fp64 forward in the WY/UT form, used only to check that
  *    chunked equals sequential up to rounding.
+ *  - Associative form (mlx-lm page, "Post-initial-submission extensions",
+ *    Extension 5: the recurrence as an associative monoid): each step as an
+ *    affine map of the state, runs of steps composed, a tree prefix over the
+ *    runs; used only to check that this evaluation order equals the
+ *    sequential recurrence up to rounding.
  *
  * Everything is fp64.  Parallelism: OpenMP over independent (b, h) pairs;
  * all cross-pair sums run afterwards in a fixed serial order.
@@ -333,6 +338,164 @@ int gdn_oracle_forward_chunked(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int
         free(U); free(W); free(Dl); free(Snew);
     }
     return 0;
+}
+
+/* ---- associative (monoid) form of the forward ------------------------------
+ *
+ * mlx-lm page, "Post-initial-submission extensions", Extension 5: the
+ * recurrence written as an associative monoid, so that it can be evaluated by a
+ * scan other than one sequential pass.  Written out, an applied step
+ *   S -> g S + k beta (v - (g S)^T k)^T
+ * is the affine map S -> A S + M with A = g (I - beta k k^T) (Dk x Dk) and
+ * M = beta k v^T (Dk x Dv); a masked step is the identity map (I, 0).  "First
+ * x, then y" is x (+) y = (A_y A_x, A_y M_x + M_y), which is associative with
+ * identity (I, 0).
+ *
+ * This form cuts the T steps into runs of seg_len, composes each run's map from
+ * its steps, takes the exclusive prefix of the run maps with a balanced tree
+ * (an up-sweep then a down-sweep over a power-of-two array padded with
+ * identities), applies each prefix to state0 for the run's start state, and
+ * replays each run from its start state for the outputs.  It exists only to
+ * check that this evaluation order gives the sequential recurrence.
+ */
+
+typedef struct {
+    double* A; /* Dk x Dk */
+    double* M; /* Dk x Dv */
+} amap_t;
+
+static void amap_identity(int64_t Dk, int64_t Dv, amap_t* m) {
+    memset(m->A, 0, sizeof(double) * Dk * Dk);
+    for (int64_t i = 0; i < Dk; ++i) m->A[i * Dk + i] = 1.0;
+    memset(m->M, 0, sizeof(double) * Dk * Dv);
+}
+
+/* X (Dk x n) <- g (X - beta k (k^T X)): the linear part of one step applied to X */
+static void step_linear(int64_t Dk, int64_t n, double* X, double g, double beta,
+                        const double* kh, double* tmp) {
+    for (int64_t c = 0; c < n; ++c) tmp[c] = 0.0;
+    for (int64_t r = 0; r < Dk; ++r)
+        for (int64_t c = 0; c < n; ++c) tmp[c] += kh[r] * X[r * n + c];
+    for (int64_t r = 0; r < Dk; ++r)
+        for (int64_t c = 0; c < n; ++c) X[r * n + c] = g * (X[r * n + c] - beta * kh[r] * tmp[c]);
+}
+
+/* out = x (+) y = (A_y A_x, A_y M_x + M_y); out may not alias x or y */
+static void amap_then(int64_t Dk, int64_t Dv, const amap_t* x, const amap_t* y, amap_t* out) {
+    for (int64_t i = 0; i < Dk; ++i) {
+        for (int64_t j = 0; j < Dk; ++j) {
+            double s = 0.0;
+            for (int64_t l = 0; l < Dk; ++l) s += y->A[i * Dk + l] * x->A[l * Dk + j];
+            out->A[i * Dk + j] = s;
+        }
+        for (int64_t j = 0; j < Dv; ++j) {
+            double s = y->M[i * Dv + j];
+            for (int64_t l = 0; l < Dk; ++l) s += y->A[i * Dk + l] * x->M[l * Dv + j];
+            out->M[i * Dv + j] = s;
+        }
+    }
+}
+
+static void amap_copy(int64_t Dk, int64_t Dv, const amap_t* x, amap_t* out) {
+    memcpy(out->A, x->A, sizeof(double) * Dk * Dk);
+    memcpy(out->M, x->M, sizeof(double) * Dk * Dv);
+}
+
+int gdn_oracle_forward_monoid(int64_t B, int64_t T, int64_t Hk, int64_t Hv, int64_t Dk,
+                              int64_t Dv, int64_t seg_len, const double* q, const double* k,
+                              const double* v, const double* a, const double* b,
+                              const double* A_log, const double* dt_bias, const double* state0,
+                              const uint8_t* mask, double* o, double* state_T) {
+    dims_t d = {B, T, Hk, Hv, Dk, Dv};
+    int rc = check_dims(&d);
+    if (rc) return rc;
+    if (seg_len < 1) return 1;
+    double *lg, *bt;
+    if (gates_ab(&d, a, b, A_log, dt_bias, &lg, &bt)) return 3;
+    const int64_t nseg = T > 0 ? (T + seg_len - 1) / seg_len : 0;
+    int64_t npad = 1;
+    while (npad < nseg) npad *= 2;
+    int fail = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t pr = 0; pr < B * Hv; ++pr) {
+        const int64_t bb = pr / Hv, h = pr % Hv;
+        amap_t* x = calloc((size_t)npad, sizeof(amap_t));
+        amap_t tmpm;
+        double* pool = malloc(sizeof(double) * (size_t)(npad + 1) * (Dk * Dk + Dk * Dv));
+        double* qh = malloc(sizeof(double) * Dk);
+        double* kh = malloc(sizeof(double) * Dk);
+        double* w = malloc(sizeof(double) * (Dk > Dv ? Dk : Dv));
+        double* p = malloc(sizeof(double) * Dv);
+        double* dl = malloc(sizeof(double) * Dv);
+        double* S = malloc(sizeof(double) * Dk * Dv);
+        if (!x || !pool || !qh || !kh || !w || !p || !dl || !S) {
+#pragma omp atomic write
+            fail = 3;
+        } else {
+            for (int64_t i = 0; i <= npad; ++i) {
+                amap_t* m = i < npad ? &x[i] : &tmpm;
+                m->A = pool + i * (Dk * Dk + Dk * Dv);
+                m->M = m->A + Dk * Dk;
+                amap_identity(Dk, Dv, m);
+            }
+            /* each run's map, composed step by step: (A, M) <- (A_t A, A_t M + M_t) */
+            for (int64_t s = 0; s < nseg; ++s) {
+                for (int64_t t = s * seg_len; t < T && t < (s + 1) * seg_len; ++t) {
+                    if (mask && !mask[bb * T + t]) continue;
+                    load_qk_hat(&d, q, k, bb, t, h, qh, kh);
+                    const double g = exp(lg[IG(&d, bb, t, h)]), beta = bt[IG(&d, bb, t, h)];
+                    step_linear(Dk, Dk, x[s].A, g, beta, kh, w);
+                    step_linear(Dk, Dv, x[s].M, g, beta, kh, w);
+                    const double* vt = v + IV(&d, bb, t, h);
+                    for (int64_t r = 0; r < Dk; ++r)
+                        for (int64_t c = 0; c < Dv; ++c) x[s].M[r * Dv + c] += beta * kh[r] * vt[c];
+                }
+            }
+            /* exclusive prefix: up-sweep, then down-sweep from the identity */
+            for (int64_t st = 1; st < npad; st *= 2)
+                for (int64_t i = 2 * st - 1; i < npad; i += 2 * st) {
+                    amap_then(Dk, Dv, &x[i - st], &x[i], &tmpm);
+                    amap_copy(Dk, Dv, &tmpm, &x[i]);
+                }
+            amap_identity(Dk, Dv, &x[npad - 1]);
+            for (int64_t st = npad / 2; st >= 1; st /= 2)
+                for (int64_t i = 2 * st - 1; i < npad; i += 2 * st) {
+                    /* left child <- the parent's prefix; right child <- the parent's
+                     * prefix followed by the left subtree's total */
+                    amap_then(Dk, Dv, &x[i], &x[i - st], &tmpm);
+                    amap_copy(Dk, Dv, &x[i], &x[i - st]);
+                    amap_copy(Dk, Dv, &tmpm, &x[i]);
+                }
+            /* replay each run from prefix(state0) */
+            const double* S0 = state0 ? state0 + IS(&d, bb, h) : NULL;
+            for (int64_t s = 0; s < nseg; ++s) {
+                for (int64_t r = 0; r < Dk; ++r)
+                    for (int64_t c = 0; c < Dv; ++c) {
+                        double acc = x[s].M[r * Dv + c];
+                        if (S0)
+                            for (int64_t l = 0; l < Dk; ++l) acc += x[s].A[r * Dk + l] * S0[l * Dv + c];
+                        S[r * Dv + c] = acc;
+                    }
+                for (int64_t t = s * seg_len; t < T && t < (s + 1) * seg_len; ++t) {
+                    load_qk_hat(&d, q, k, bb, t, h, qh, kh);
+                    if (!mask || mask[bb * T + t]) {
+                        const double g = exp(lg[IG(&d, bb, t, h)]), beta = bt[IG(&d, bb, t, h)];
+                        apply_step(Dk, Dv, S, g, beta, kh, v + IV(&d, bb, t, h), p, dl);
+                    }
+                    read_out(Dk, Dv, S, qh, o + IV(&d, bb, t, h));
+                }
+            }
+            if (nseg > 0)
+                memcpy(state_T + IS(&d, bb, h), S, sizeof(double) * Dk * Dv);
+            else if (S0)
+                memcpy(state_T + IS(&d, bb, h), S0, sizeof(double) * Dk * Dv);
+            else
+                memset(state_T + IS(&d, bb, h), 0, sizeof(double) * Dk * Dv);
+        }
+        free(x); free(pool); free(qh); free(kh); free(w); free(p); free(dl); free(S);
+    }
+    free(lg); free(bt);
+    return fail;
 }
 
 /* ---- sequential VJP ------------------------------------------------------ */

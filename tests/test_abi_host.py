@@ -184,3 +184,36 @@ def test_host_session_sizing_and_rejections(lib):
     assert lib.gdn_host_step(None, None, None) == 1
     assert lib.gdn_host_session_sync(None) == 1
     assert lib.gdn_host_session_destroy(None) == 0
+
+
+def test_segmented_forward_sizing_and_rejections(lib):
+    """gdn_forward_segmented: segment geometry in the extra workspace size, and
+    the host checks before any launch."""
+    n = ctypes.c_size_t()
+    s = _shape(B=2, T=64 * 10, Hk=2, Hv=4, Dk=192, Dv=128)  # NC = 10
+    assert lib.gdn_segment_bytes(ctypes.byref(s), 1, ctypes.byref(n)) == 0 and n.value == 0
+    # 4 requested: runs of 3 chunks, 4 segments, 3 maps / start states
+    wd = 128 + 256
+    assert lib.gdn_segment_bytes(ctypes.byref(s), 4, ctypes.byref(n)) == 0
+    assert n.value == 3 * 2 * 4 * 192 * (wd + 128) * 4
+    # above the chunk count: clamped to one chunk per segment
+    assert lib.gdn_segment_bytes(ctypes.byref(s), 100, ctypes.byref(n)) == 0
+    assert n.value == 9 * 2 * 4 * 192 * (wd + 128) * 4
+    assert lib.gdn_segment_bytes(ctypes.byref(s), -1, ctypes.byref(n)) == 1
+    a = ctypes.c_int()
+    assert lib.gdn_segments_auto(ctypes.byref(s), ctypes.byref(a)) == 0 and a.value >= 1
+    # fp32 has no tensor-core scan: more than one segment is unsupported
+    s32 = _shape(B=1, T=64 * 10, Dk=128, Dv=128, dtype=0)
+    assert lib.gdn_segment_bytes(ctypes.byref(s32), 4, ctypes.byref(n)) == 2
+    vp = ctypes.c_void_p
+    P = vp(0x1000)
+    big = ctypes.c_size_t(1 << 40)
+    fwd = [P] * 7 + [None, None, P, P, P, big, P, big, None]
+    assert lib.gdn_forward_segmented(ctypes.byref(s32), 4, *fwd) == 2
+    assert lib.gdn_forward_segmented(ctypes.byref(s), -2, *fwd) == 1
+    small = list(fwd)
+    small[14] = ctypes.c_size_t(16)
+    assert lib.gdn_forward_segmented(ctypes.byref(s), 4, *small) == 3
+    mis = list(fwd)
+    mis[0] = vp(0x1004)
+    assert lib.gdn_forward_segmented(ctypes.byref(s), 4, *mis) == 4

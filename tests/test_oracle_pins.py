@@ -325,6 +325,42 @@ def test_chunked_catches_planted_slip():
     assert np.abs(o1 - o2).max() > 1e-8
 
 
+@pytest.mark.parametrize("T,L", [(1, 1), (5, 1), (37, 37), (37, 100), (65, 64), (129, 16),
+                                 (200, 7)])
+def test_monoid_equals_sequential(T, L):
+    """mlx-lm page, "Post-initial-submission extensions", Extension 5: the recurrence
+    as an associative monoid of affine state maps, evaluated by a tree prefix over
+    runs of L steps (run counts 1, 5 padded to 8, 3, 9, 29), equals the sequential
+    recurrence up to rounding; masked batch, GQA, the clamp head, a nonzero
+    initial state.  Composing the non-commuting maps in the wrong order, or
+    dropping a run's offset, moves the result by far more than the bound."""
+    w = wl.custom("mo", 2, T, 2, 4, 12, 6, seed=70 + T, mask="half_second_batch",
+                  clamp_head=True)
+    x = _inputs(w)
+    args = ("q", "k", "v", "a", "b", "A_log", "dt_bias", "state0", "mask")
+    assert np.abs(x["state0"]).max() > 0
+    o1, s1 = oracle.forward(*[x[n] for n in args])
+    o2, s2 = oracle.forward_monoid(*[x[n] for n in args], seg_len=L)
+    assert np.abs(o1 - o2).max() <= 1e-12 * max(np.abs(o1).max(), 1.0)
+    assert np.abs(s1 - s2).max() <= 1e-12 * max(np.abs(s1).max(), 1.0)
+
+
+def test_monoid_run_maps_do_not_commute():
+    """Guard for the test above: two runs of steps give different results in the
+    two orders, so an order slip in the prefix would be seen.  Swapping the two
+    halves of the sequence (the same run maps, composed the other way round)
+    changes the final state."""
+    w = wl.custom("mo", 1, 16, 1, 1, 8, 4, seed=98)
+    x = _inputs(w)
+    args = ("q", "k", "v", "a", "b", "A_log", "dt_bias", "state0", "mask")
+    _, s1 = oracle.forward_monoid(*[x[n] for n in args], seg_len=8)
+    y = dict(x)
+    for n in ("q", "k", "v", "a", "b"):
+        y[n] = np.concatenate([x[n][:, 8:], x[n][:, :8]], axis=1)
+    _, s2 = oracle.forward_monoid(*[y[n] for n in args], seg_len=8)
+    assert np.abs(s1 - s2).max() > 1e-3 * np.abs(s1).max()
+
+
 # -- the log_decay / beta input form (torch-to-nnef page, op contract) ----------
 
 def _lb_inputs(B, T, Hk, Hv, Dk, Dv, seed, masked=False):
