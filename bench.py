@@ -68,7 +68,7 @@ def _peaks():
 # algorithmic work model (per launch of each phase)
 # ---------------------------------------------------------------------------
 
-def work_model(w, conv_k=0, gates="ab", nseg=1):
+def work_model(w, conv_k=0, gates="ab", nseg=1, nseg_bwd=1):
     """Per-phase algorithmic flops and bytes of one fwd+bwd step, in the storage
     formats the kernels use: bf16 inputs keep the saved intermediates as bf16
     operand images (checkpoints, T, W, P, Delta as hi + lo, state cotangents,
@@ -114,6 +114,18 @@ def work_model(w, conv_k=0, gates="ab", nseg=1):
             flops=BH * (nseg - 1) * 2 * Dk * Dk * Dv,
             bytes=BH * (nseg - 1) * Dk * (Wd + Dv) * 4)
         m["fwd_scan"]["bytes"] += BH * (nseg - 1) * Dk * Dv * 4
+    if nseg_bwd > 1:
+        # the reverse scan in segments: maps (dO, P, k, q, W in; maps out), the chain
+        Lb = -(-NC // nseg_bwd)
+        Wd = Dv + -(-Dk // 128) * 128
+        mb = BH * (nseg_bwd - 1) * Lb
+        m["bwd_seg_maps"] = dict(
+            flops=mb * (6 * C * Dk * Wd + 2 * C * C * Wd),
+            bytes=mb * (C * Dv * es + C * C * es + 3 * C * Dk * es)
+            + BH * (nseg_bwd - 1) * Dk * Wd * 4)
+        m["bwd_seg_chain"] = dict(
+            flops=BH * (nseg_bwd - 1) * 2 * Dk * Dk * Dv,
+            bytes=BH * (nseg_bwd - 1) * Dk * (Wd + Dv) * 4)
     # dO, P, k, q, W in; chunk-end cotangent and -Dbar images out
     m["bwd_scan"] = dict(
         flops=units * (6 * C * Dk * Dv + 2 * C * C * Dv),
@@ -559,8 +571,10 @@ def run_ours(args, w, world, rank, local):
 
     # ---- per-phase roofline of the dominant kernel
     peaks = _peaks()
-    nseg = ops.segments_auto(shape) if shape is not None and args.gates != "kc" else 1
-    model = work_model(w, args.fused_conv, args.gates, nseg)
+    seg_ok = shape is not None and args.gates != "kc"
+    nseg = ops.segments_auto(shape) if seg_ok else 1
+    nseg_bwd = ops.segments_auto(shape, backward=True) if seg_ok and backward else 1
+    model = work_model(w, args.fused_conv, args.gates, nseg, nseg_bwd)
     ph = {phases[i].name.decode(): (phases[i].launches, phases[i].total_ms)
           for i in range(cnt.value)}
     dom = max(ph, key=lambda k: ph[k][1])
@@ -571,7 +585,7 @@ def run_ours(args, w, world, rank, local):
     # bf16 workloads run the chunk contractions on the tensor cores (tcgen05);
     # fp32 workloads run them as FFMA on the CUDA cores
     tensor = w.dtype == torch.bfloat16 and dom in ("fwd_chunk", "fwd_scan", "bwd_scan", "bwd_chunk",
-                                                  "bwd_scan_chunk", "fwd_seg_maps")
+                                                  "bwd_scan_chunk", "fwd_seg_maps", "bwd_seg_maps")
     cpeak = peaks["bf16_tflops"] if tensor else FP32_ALU_PEAK_TFLOPS
     t_cmp = fl / (cpeak * 1e12)
     traffic = measured_traffic(w.name, dom)

@@ -2,6 +2,7 @@
 // of the `saved` and workspace buffers, and the launch sequence.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <cstring>
@@ -300,9 +301,42 @@ int seg_auto(const gdn::Dims& d) {
     return best_p;
 }
 
-// segments and chunks per segment a request resolves to (0: the automatic count)
-int seg_resolve(const gdn::Dims& d, int requested, int* len) {
-    if (requested == 0) requested = seg_auto(d);
+// The backward's segment count.  Same model for the reverse scan, plus the
+// per-chunk gradient items (about 7.8 Dk / 192 chunk steps of one SM each,
+// measured on GB300): with one segment they run in the fused launch beside the
+// scan (or after it when the scan's tiles fill the GPU); with several, after the
+// segmented scan on every SM.
+int seg_auto_bwd(const gdn::Dims& d) {
+    if (!seg_supported(d)) return 1;
+    const int64_t sms = gdn::sm_count();
+    auto waves = [&](int64_t ctas) { return (double)((ctas + sms - 1) / sms); };
+    const int64_t tiles = d.B * d.Hv * (d.Dv / 128), mtiles = d.B * d.Hv * (gdn::seg_map_width(d) / 128);
+    const double items = (double)(d.B * d.Hv * d.NC), item = 7.8 * (double)d.Dk / 192.0;
+    const double grads = waves(d.B * d.Hv * d.NC) * item;
+    double best = gdn::bwd_fused_tc_supported(d)
+                      ? std::max((double)d.NC, (items * item + (double)(tiles * d.NC)) / (double)sms)
+                      : waves(tiles) * (double)d.NC + grads;
+    int best_p = 1;
+    const double chain = (double)(d.Dk * d.Dk) / (128.0 * 128.0);
+    const int64_t pmax = d.NC < 4096 ? d.NC : 4096;
+    for (int64_t r = 2; r <= pmax; ++r) {
+        int nseg = 1, len = 1;
+        seg_geometry(d, (int)r, &nseg, &len);
+        if ((int64_t)nseg * d.B > 65535) break;
+        const double cost = (waves((nseg - 1) * mtiles) + waves(nseg * tiles)) * len + chain * (nseg - 1) +
+                            grads + 3.0;
+        if (cost < best) {
+            best = cost;
+            best_p = nseg;
+        }
+    }
+    return best_p;
+}
+
+// segments and chunks per segment a request resolves to (0: the automatic count
+// of the forward, or of the backward when bwd)
+int seg_resolve(const gdn::Dims& d, int requested, int* len, bool bwd = false) {
+    if (requested == 0) requested = bwd ? seg_auto_bwd(d) : seg_auto(d);
     int nseg = 1;
     *len = (int)d.NC;
     if (requested > 1) seg_geometry(d, requested, &nseg, len);
@@ -333,11 +367,11 @@ gdn_status gdn_workspace_bytes(const gdn_shape* shape, int pass, size_t* bytes) 
     if (st != GDN_OK) return st;
     if (bytes == nullptr || pass < 0 || pass > 2) return GDN_ERR_INVALID_ARG;
     const Layout L = make_layout(d);
-    // the forward's segment buffers for the automatic segment count
+    // the segment buffers of the pass's automatic segment count
     int len = 0;
-    const size_t seg = pass == 1 ? 0 : seg_bytes(d, seg_resolve(d, 0, &len));
+    const size_t seg = seg_bytes(d, seg_resolve(d, 0, &len, pass == 1));
     if (pass == 0) *bytes = L.fwd_total + seg;
-    else if (pass == 1) *bytes = L.bwd_total;
+    else if (pass == 1) *bytes = L.bwd_total + seg;
     else *bytes = L.fwd_total + L.saved_total + seg;  // inference forward without a saved buffer
     return GDN_OK;
 }
@@ -428,11 +462,19 @@ gdn_status backward_impl(const gdn_shape* shape, int gates, const void* q, const
                          const float* dt_bias, const uint8_t* mask, const void* saved,
                          size_t saved_bytes, const void* d_o, const float* d_state_T, void* dq,
                          void* dk, void* dv, void* da, void* db, float* dA_log, float* ddt_bias,
-                         float* dstate0, void* ws, size_t ws_bytes, void* stream) {
+                         float* dstate0, void* ws, size_t ws_bytes, void* stream, int segments = 0) {
     gdn::Dims d;
     gdn_status st = validate_shape(shape, &d);
     if (st != GDN_OK) return st;
     d.gates = gates;
+    // segments of the reverse scan (1: one pass, fused with the gradients when it
+    // fits; 0: the automatic choice)
+    if (segments < 0) return GDN_ERR_INVALID_ARG;
+    if (segments > 1 && !seg_supported(d)) return GDN_ERR_UNSUPPORTED_SHAPE;
+    int len = 0;
+    const int nseg = seg_resolve(d, segments, &len, true);
+    if ((int64_t)nseg * d.B > 65535) return GDN_ERR_UNSUPPORTED_SHAPE;
+    const size_t sbytes = seg_bytes(d, nseg);
     if (!q || !k || !v || !a || !b || !saved || !d_o || !dq || !dk || !dv || !da || !db ||
         !dstate0 || !ws)
         return GDN_ERR_INVALID_ARG;
@@ -443,7 +485,7 @@ gdn_status backward_impl(const gdn_shape* shape, int gates, const void* q, const
     for (const void* p : ptrs)
         if (!aligned16(p)) return GDN_ERR_MISALIGNED;
     const Layout L = make_layout(d);
-    if (saved_bytes < L.saved_total || ws_bytes < L.bwd_total) return GDN_ERR_WORKSPACE_TOO_SMALL;
+    if (saved_bytes < L.saved_total || ws_bytes < L.bwd_total + sbytes) return GDN_ERR_WORKSPACE_TOO_SMALL;
     gdn::Ptrs p{};
     p.q = q; p.k = k; p.v = v; p.a = a; p.b = b;
     p.A_log = A_log; p.dt_bias = dt_bias;
@@ -468,7 +510,20 @@ gdn_status backward_impl(const gdn_shape* shape, int gates, const void* q, const
         p.tmaps = &maps;
     }
     cudaError_t e;
-    if (p.tmaps && gdn::bwd_fused_tc_supported(d)) {
+    if (nseg > 1) {
+        // segment maps, their chain from d_state_T, every segment's reverse scan,
+        // then the per-chunk gradients on every SM
+        const size_t nmap = (size_t)(nseg - 1) * d.B * d.Hv * d.Dk;
+        gdn::ScanSeg sg{nseg, len, 1, reinterpret_cast<float*>(w + L.bwd_total + align_up(nmap * gdn::seg_map_width(d) * 4)),
+                        reinterpret_cast<float*>(w + L.bwd_total)};
+        gdn::Ptrs pc = p;
+        pc.state0 = d_state_T;
+        e = run_phase("bwd_seg_maps", s, [&] { return gdn::launch_bwd_scan_ta_seg(d, p, sg, s); });
+        if (e == cudaSuccess) e = run_phase("bwd_seg_chain", s, [&] { return gdn::launch_seg_chain(d, pc, sg, s); });
+        sg.mode = 0;
+        if (e == cudaSuccess) e = run_phase("bwd_scan", s, [&] { return gdn::launch_bwd_scan_ta_seg(d, p, sg, s); });
+        if (e == cudaSuccess) e = run_phase("bwd_chunk", s, [&] { return gdn::launch_bwd_chunk(d, p, s); });
+    } else if (p.tmaps && gdn::bwd_fused_tc_supported(d)) {
         e = run_phase("bwd_scan_chunk", s, [&] { return gdn::launch_bwd_fused_tc(d, p, s); });
     } else {
         e = run_phase("bwd_scan", s, [&] { return gdn::launch_bwd_scan(d, p, s); });
@@ -510,6 +565,16 @@ gdn_status gdn_segments_auto(const gdn_shape* shape, int* segments) {
     return GDN_OK;
 }
 
+gdn_status gdn_backward_segments_auto(const gdn_shape* shape, int* segments) {
+    gdn::Dims d;
+    gdn_status st = validate_shape(shape, &d);
+    if (st != GDN_OK) return st;
+    if (segments == nullptr) return GDN_ERR_INVALID_ARG;
+    int len = 0;
+    *segments = seg_resolve(d, 0, &len, true);
+    return GDN_OK;
+}
+
 gdn_status gdn_segment_bytes(const gdn_shape* shape, int segments, size_t* bytes) {
     gdn::Dims d;
     gdn_status st = validate_shape(shape, &d);
@@ -539,6 +604,18 @@ gdn_status gdn_backward(const gdn_shape* shape, const void* q, const void* k, co
     return backward_impl(shape, 0, q, k, v, a, b, A_log, dt_bias, mask, saved, saved_bytes, d_o,
                          d_state_T, dq, dk, dv, da, db, dA_log, ddt_bias, dstate0, ws, ws_bytes,
                          stream);
+}
+
+gdn_status gdn_backward_segmented(const gdn_shape* shape, int segments, const void* q,
+                                  const void* k, const void* v, const void* a, const void* b,
+                                  const float* A_log, const float* dt_bias, const uint8_t* mask,
+                                  const void* saved, size_t saved_bytes, const void* d_o,
+                                  const float* d_state_T, void* dq, void* dk, void* dv, void* da,
+                                  void* db, float* dA_log, float* ddt_bias, float* dstate0,
+                                  void* ws, size_t ws_bytes, void* stream) {
+    return backward_impl(shape, 0, q, k, v, a, b, A_log, dt_bias, mask, saved, saved_bytes, d_o,
+                         d_state_T, dq, dk, dv, da, db, dA_log, ddt_bias, dstate0, ws, ws_bytes,
+                         stream, segments);
 }
 
 gdn_status gdn_backward_lb(const gdn_shape* shape, const void* q, const void* k,

@@ -232,6 +232,11 @@ struct ScanSeg {
 int64_t seg_map_width(const Dims& d);  // Wd
 cudaError_t launch_fwd_scan_ta_seg(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s);
 cudaError_t launch_seg_chain(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s);
+// The same three passes for the reverse scan of the backward (segment t counted
+// from the top, the bottom one possibly shorter): the maps of segments 0 .. nseg - 2
+// (mode 1), the chain from d_state_T (launch_seg_chain with state0 = d_state_T),
+// then every segment (mode 0); the per-chunk gradients follow as their own launch.
+cudaError_t launch_bwd_scan_ta_seg(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s);
 cudaError_t launch_bwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s);
 unsigned int read_clear_error_scanta();
 bool fwd_chunk_tc_supported(const Dims& d);

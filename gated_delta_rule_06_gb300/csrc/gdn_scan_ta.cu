@@ -69,10 +69,6 @@ __host__ __device__ inline TaCols ta_cols(int Dk) {
     return t;
 }
 
-// width of a segment map: the offset part (Dv columns), then the linear part (Dk
-// columns, padded to whole value tiles)
-__host__ __device__ inline int64_t seg_wd(int64_t Dk, int64_t Dv) { return Dv + (Dk + DVT - 1) / DVT * DVT; }
-
 // gam r_q / sqrt(Dk) of its step; each thread keeps one step
 __device__ __forceinline__ void scale_q(uint8_t* Q, const uint8_t* raw, int Dk) {
     const int t = threadIdx.x & (C - 1);
@@ -464,8 +460,9 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
 }
 
 __global__ void __launch_bounds__(kThreads + 32, 1)
-    bwd_scan_ta_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm) {
-    bwd_scan_ta_body(d, p, tm, blockIdx.x, blockIdx.y, blockIdx.z, &g_err_scanta, nullptr, true);
+    bwd_scan_ta_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm, ScanSeg sg) {
+    bwd_scan_ta_body(d, p, tm, blockIdx.x, blockIdx.y, (int)(blockIdx.z % d.B), sg,
+                     (int)(blockIdx.z / d.B), &g_err_scanta, nullptr, true);
 }
 
 }  // namespace
@@ -600,7 +597,20 @@ cudaError_t launch_bwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);
-    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps);
+    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps, ScanSeg{1, (int)d.NC, 0, nullptr, nullptr});
+    count_launches(1);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_bwd_scan_ta_seg(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s) {
+    const size_t smem = tb_plan((int)d.Dk).total + 1024;
+    auto kern = bwd_scan_ta_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int64_t nx = sg.mode == 0 ? d.Dv / DVT : seg_wd(d.Dk, d.Dv) / DVT;
+    const int64_t nz = (sg.mode == 0 ? sg.nseg : sg.nseg - 1) * d.B;
+    dim3 grid((unsigned)nx, (unsigned)d.Hv, (unsigned)nz);
+    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps, sg);
     count_launches(1);
     return cudaPeekAtLastError();
 }

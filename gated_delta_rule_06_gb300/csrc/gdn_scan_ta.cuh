@@ -104,6 +104,10 @@ __device__ __forceinline__ void build_os(const uint8_t* O, uint8_t* Os, uint8_t*
     }
 }
 
+// width of a segment map: the offset part (Dv columns), then the linear part (Dk
+// columns, padded to whole value tiles)
+__host__ __device__ inline int64_t seg_wd(int64_t Dk, int64_t Dv) { return Dv + (Dk + DVT - 1) / DVT * DVT; }
+
 // The reverse scan of value tile `tile` of (batch bb, value head h), run by a
 // CTA of kThreads + 32 threads with tb_plan(Dk).total + 1024 bytes of dynamic
 // shared memory and all 512 TMEM columns.  err: the caller's error word for
@@ -113,9 +117,17 @@ __device__ __forceinline__ void build_os(const uint8_t* O, uint8_t* Os, uint8_t*
 // may read the images of chunk c of this tile once the count reaches NC - c.
 // relinquish: give up the CTA's TMEM allocation permit after the allocation
 // (false when the CTA allocates again after this body).
+// Segments (sg.nseg > 1; progress null): segment t counts from the top, chunks
+// hi - sg.len .. hi - 1 with hi = NC - t sg.len (the bottom one may be shorter).
+// Mode 0 scans segment t from d_state_T (t = 0) or from the chained start state
+// sg.start[t - 1], storing its images; the bottom segment writes dstate0.  Mode 1
+// (maps, t < nseg - 1) scans it from zero (offset part, the Dv value tiles) and,
+// with Obar = 0, from the identity (linear part, tiles over Dk padded), storing
+// only the end states, into sg.maps[t] with rows of seg_wd(Dk, Dv).
 __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, const Tmaps& tm,
-                                                 int tile, int h, int bb, unsigned int* err,
-                                                 unsigned int* progress, bool relinquish) {
+                                                 int tile, int h, int bb, const ScanSeg& sg, int t,
+                                                 unsigned int* err, unsigned int* progress,
+                                                 bool relinquish) {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ uint64_t bar, barW, barQ, barK, barP, barO[2], barR[2];
     __shared__ uint32_t tmem_sh;
@@ -139,8 +151,13 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
     uint8_t* dsimg = reinterpret_cast<uint8_t*>(p.dSck);
     uint8_t* dbimg = reinterpret_cast<uint8_t*>(p.Dbar);
     const int64_t NC = d.NC;
+    // chunks lo .. hi - 1 of segment t, walked downwards
+    const int64_t hi = NC - (int64_t)t * sg.len;
+    const int64_t lo = hi - sg.len > 0 ? hi - sg.len : 0;
+    const bool maps = sg.mode != 0;    // segment maps: no images, no progress
+    const bool oz = maps && n0 >= Dv;  // linear part of a map: Obar = 0, identity start
 
-    // m = NC - 1 - c counts processed chunks: ring slots and mbarrier parities follow it
+    // m = hi - 1 - c counts processed chunks: ring slots and mbarrier parities follow it
     auto load_w = [&](int64_t c) {
         tc::mbar_arrive_expect_tx(&barW, kbytes);
         tc::bulk_g2s(sm + L.W, Wimg + (bh * NC + c) * kbytes, kbytes, &barW);
@@ -156,23 +173,23 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
         tc::mbar_arrive_expect_tx(&barQ, kbytes);
         tc::bulk_g2s(sm + L.Q, static_cast<const uint8_t*>(p.qimg) + (kq * NC + c) * kbytes, kbytes, &barQ);
     };
-    // Obar tile of chunk c -> buffer (NC - 1 - c) & 1
-    auto obuf = [&](int64_t c) { return sm + L.O + ((NC - 1 - c) & 1) * obytes; };
+    // Obar tile of chunk c -> buffer (hi - 1 - c) & 1
+    auto obuf = [&](int64_t c) { return sm + L.O + ((hi - 1 - c) & 1) * obytes; };
     auto load_o = [&](int64_t c) {
-        uint64_t* b = &barO[(NC - 1 - c) & 1];
+        uint64_t* b = &barO[(hi - 1 - c) & 1];
         tc::mbar_arrive_expect_tx(b, obytes);
         tc::tma_load_5d(obuf(c), &tm.dO, 0, (int)(c * C), n0 / 8, h, bb, b);
     };
     auto load_raw = [&](int64_t c) {
-        const int s = (int)((NC - 1 - c) & 1);
+        const int s = (int)((hi - 1 - c) & 1);
         uint8_t* dst = sm + L.raw + s * kRawBytes;
         tc::mbar_arrive_expect_tx(&barR[s], kRawBytes);
         tc::bulk_g2s(dst, p.gam + bh * d.Tp + c * C, C * 8, &barR[s]);
         tc::bulk_g2s(dst + C * 8, p.rq + ((int64_t)bb * d.Hk + j) * d.Tp + c * C, C * 4, &barR[s]);
         tc::bulk_g2s(dst + C * 12, p.rk + ((int64_t)bb * d.Hk + j) * d.Tp + c * C, C * 4, &barR[s]);
     };
-    // -Dbar^T tile of chunk c (and its image source) -> buffer (NC - 1 - c) & 1
-    auto ndbuf = [&](int64_t c) { return sm + L.ND + ((NC - 1 - c) & 1) * (uint32_t)(DVT * C * 2); };
+    // -Dbar^T tile of chunk c (and its image source) -> buffer (hi - 1 - c) & 1
+    auto ndbuf = [&](int64_t c) { return sm + L.ND + ((hi - 1 - c) & 1) * (uint32_t)(DVT * C * 2); };
     auto store_dbar = [&](int64_t c) {  // storer; the caller commits
         tc::bulk_s2g(dbimg + (bh * NC + c) * (int64_t)C * Dv * 2 + (int64_t)n0 * 128, ndbuf(c),
                      (uint32_t)(DVT * 128));
@@ -196,33 +213,42 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
     }
     __syncthreads();  // barriers initialised
     if (prod) {
-        load_w(NC - 1);
-        load_kq(NC - 1);
-        load_p(NC - 1);
-        load_o(NC - 1);
-        if (NC > 1) load_o(NC - 2);
-        load_raw(NC - 1);
-        if (NC > 1) load_raw(NC - 2);
+        load_w(hi - 1);
+        load_kq(hi - 1);
+        load_p(hi - 1);
+        if (!oz) {
+            load_o(hi - 1);
+            if (hi - lo > 1) load_o(hi - 2);
+        }
+        load_raw(hi - 1);
+        if (hi - lo > 1) load_raw(hi - 2);
     }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tb = tmem_sh;
     const int halfk = Dk / 2;
-    const int64_t sbase = bh * Dk * Dv + n0;
+    // cotangent entering the segment (rows dk, row stride Dv): d_state_T for the
+    // top segment, the chained one below it; zero / the identity for the maps
+    const float* sin = nullptr;
+    if (!maps && t == 0 && p.d_state_T) sin = p.d_state_T + bh * Dk * Dv + n0;
+    if (!maps && t > 0) sin = sg.start + ((int64_t)(t - 1) * d.B * d.Hv + bh) * Dk * Dv + n0;
     bool ok = true;
     if (epi) {
         for (int cc = g * halfk; cc < (g + 1) * halfk; cc += 16) {  // final cotangent -> TMEM
             float v[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = p.d_state_T ? p.d_state_T[sbase + (int64_t)(cc + i) * Dv + r] : 0.f;
+            for (int i = 0; i < 16; ++i)
+                v[i] = oz ? (cc + i == n0 - Dv + r ? 1.f : 0.f) : sin ? sin[(int64_t)(cc + i) * Dv + r] : 0.f;
             tc::tmem_st16(tc::tmem_addr(tb, lb, cc), v);
         }
         tc::tmem_wait_st();
         ok = tc::mbar_wait(&barR[0], 0, err);
-        ok = tc::mbar_wait(&barO[0], 0, err) && ok;
         vectors_from_raw(sm + L.raw, reinterpret_cast<float*>(sm + L.vec), Dk);
-        build_os(obuf(NC - 1), sm + L.Os, sm + L.Oslo, sm + L.raw, Dk);
+        if (!oz) {
+            ok = tc::mbar_wait(&barO[0], 0, err) && ok;
+            build_os(obuf(hi - 1), sm + L.Os, sm + L.Oslo, sm + L.raw, Dk);
+        }
         tc::fence_async_smem();
     }
     tc::tc_fence_before();
@@ -242,8 +268,8 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
     tND.k_major = true;
     uint32_t phase = 0;
 
-    for (int64_t c = NC - 1; c >= 0; --c) {
-        const int64_t m = NC - 1 - c;
+    for (int64_t c = hi - 1; c >= lo; --c) {
+        const int64_t m = hi - 1 - c;
         if (progress && m >= 2 && epi) {
             // chunk c + 2 is complete in global memory: its Sbar'^T image went out
             // by generic stores in its step 2, its -Dbar^T image by the bulk store
@@ -309,7 +335,7 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
             for (int k = 0; k < Dk; k += 16) {
                 tc::mma_bf16_ta(tb + kA2, tb + aop + k / 2, dK, id2, k > 0);
                 dK += iK;
-                if (k < C) {
+                if (k < C && !oz) {
                     tc::mma_bf16(tb + kA1, dO, dP, id64, k > 0);
                     tc::mma_bf16(tb, dOs, dQ, idq, 1u);
                     tc::mma_bf16(tb, dOl, dQ, idq, 1u);
@@ -319,8 +345,8 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
             tc::mma_commit(&bar);
             ok = tc::mbar_wait(&bar, phase, err) && ok;
             phase ^= 1u;
-            if (c > 0) {  // P, K, Q tiles (and this chunk's Obar buffer) are free
-                if (c > 1) load_o(c - 2);
+            if (c > lo) {  // P, K, Q tiles (and this chunk's Obar buffer) are free
+                if (!oz && c > lo + 1) load_o(c - 2);
                 load_p(c - 1);
                 load_kq(c - 1);
             }
@@ -328,7 +354,7 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
             // meanwhile: the Sbar'^T image, straight from the A operand to global
             // memory (each warp store covers 32 consecutive 16-byte rows of a panel)
             uint8_t* img = dsimg + (bh * NC + c) * (int64_t)Dk * Dv * 2;
-            for (int cb = g * (Dk / 4); cb < (g + 1) * (Dk / 4); cb += 16) {
+            for (int cb = g * (Dk / 4); !maps && cb < (g + 1) * (Dk / 4); cb += 16) {
                 uint32_t w[16];
                 tc::tmem_ld16u(tc::tmem_addr(tb, lb, aop + cb), w);
                 tc::tmem_wait_ld();
@@ -342,8 +368,13 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
             tc::tc_fence_after();
             // step 3: -Dbar^T = -(A1 + A2 diag(e r_k)) -> operand / image tile
             float a1[2][16], a2[2][16];
-            tc::tmem_ld16(tc::tmem_addr(tb, lb, kA1 + 32 * g), a1[0]);
-            tc::tmem_ld16(tc::tmem_addr(tb, lb, kA1 + 32 * g + 16), a1[1]);
+            if (oz) {  // no Obar: A1 was not formed (its TMEM columns are not read)
+#pragma unroll
+                for (int i = 0; i < 16; ++i) a1[0][i] = a1[1][i] = 0.f;
+            } else {
+                tc::tmem_ld16(tc::tmem_addr(tb, lb, kA1 + 32 * g), a1[0]);
+                tc::tmem_ld16(tc::tmem_addr(tb, lb, kA1 + 32 * g + 16), a1[1]);
+            }
             tc::tmem_ld16(tc::tmem_addr(tb, lb, kA2 + 32 * g), a2[0]);
             tc::tmem_ld16(tc::tmem_addr(tb, lb, kA2 + 32 * g + 16), a2[1]);
             tc::tmem_wait_ld();
@@ -372,19 +403,21 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
             tc::mma_commit(&bar);
             ok = tc::mbar_wait(&bar, phase, err) && ok;
             phase ^= 1u;
-            if (c > 0) load_w(c - 1);
-            if (c > 1) load_raw(c - 2);
+            if (c > lo) load_w(c - 1);
+            if (c > lo + 1) load_raw(c - 2);
         } else if (epi) {
             if (storer) {
-                store_dbar(c);
+                if (!maps) store_dbar(c);
                 tc::bulk_commit();
             }
-            if (c > 0) {  // vectors and the scaled Obar operands of chunk c - 1
+            if (c > lo) {  // vectors and the scaled Obar operands of chunk c - 1
                 const uint8_t* raw = sm + L.raw + ((m + 1) & 1) * kRawBytes;
                 ok = tc::mbar_wait(&barR[(m + 1) & 1], (uint32_t)(((m + 1) >> 1) & 1), err) && ok;
                 vectors_from_raw(raw, reinterpret_cast<float*>(sm + L.vec) + ((m + 1) & 1) * 4 * C, Dk);
-                ok = tc::mbar_wait(&barO[(m + 1) & 1], (uint32_t)(((m + 1) >> 1) & 1), err) && ok;
-                build_os(obuf(c - 1), sm + L.Os, sm + L.Oslo, raw, Dk);
+                if (!oz) {
+                    ok = tc::mbar_wait(&barO[(m + 1) & 1], (uint32_t)(((m + 1) >> 1) & 1), err) && ok;
+                    build_os(obuf(c - 1), sm + L.Os, sm + L.Oslo, raw, Dk);
+                }
                 tc::fence_async_smem();
             }
             ok = tc::mbar_wait(&bar, phase, err) && ok;
@@ -395,13 +428,22 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
         __syncthreads();  // (A) of chunk c - 1
         tc::tc_fence_after();
     }
-    if (epi) {
+    // cotangent leaving the segment: dstate0 (bottom segment) or the map's columns
+    float* sout = nullptr;
+    int64_t ostr = Dv;
+    if (maps) {
+        ostr = seg_wd(Dk, Dv);
+        sout = sg.maps + ((int64_t)t * d.B * d.Hv + bh) * Dk * ostr + n0;
+    } else if (t == sg.nseg - 1) {
+        sout = p.dstate0 + bh * Dk * Dv + n0;
+    }
+    if (epi && sout) {
         for (int cc = g * halfk; cc < (g + 1) * halfk; cc += 16) {
             float v[16];
             tc::tmem_ld16(tc::tmem_addr(tb, lb, cc), v);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) p.dstate0[sbase + (int64_t)(cc + i) * Dv + r] = v[i];
+            for (int i = 0; i < 16; ++i) sout[(int64_t)(cc + i) * ostr + r] = v[i];
         }
     }
     if (storer) tc::bulk_wait_all();
@@ -413,7 +455,7 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
     __syncthreads();
     if (progress && storer) {  // the last (up to) two chunks
         __threadfence();
-        atomicAdd(progress + (int64_t)bb * d.Hv + h, (unsigned int)(NC < 2 ? NC : 2));
+        atomicAdd(progress + (int64_t)bb * d.Hv + h, (unsigned int)(hi - lo < 2 ? hi - lo : 2));
     }
     if (warp == 0) tc::tmem_dealloc(tb, 512);
 }

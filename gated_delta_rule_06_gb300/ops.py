@@ -84,10 +84,14 @@ def load_library(path: str = LIB_PATH):
         lib.gdn_forward_lb.restype = i32
         lib.gdn_forward_segmented.argtypes = [shp, i32] + [vp] * 11 + [vp, sz, vp, sz, vp]
         lib.gdn_forward_segmented.restype = i32
+        lib.gdn_backward_segmented.argtypes = [shp, i32] + [vp] * 9 + [sz] + [vp] * 10 + [vp, sz, vp]
+        lib.gdn_backward_segmented.restype = i32
         lib.gdn_segment_bytes.argtypes = [shp, i32, ctypes.POINTER(sz)]
         lib.gdn_segment_bytes.restype = i32
         lib.gdn_segments_auto.argtypes = [shp, ctypes.POINTER(i32)]
         lib.gdn_segments_auto.restype = i32
+        lib.gdn_backward_segments_auto.argtypes = [shp, ctypes.POINTER(i32)]
+        lib.gdn_backward_segments_auto.restype = i32
         lib.gdn_backward_lb.argtypes = [shp] + [vp] * 7 + [sz] + [vp] * 8 + [vp, sz, vp]
         lib.gdn_backward_lb.restype = i32
         lib.gdn_causal_conv1d_update.argtypes = [ctypes.c_int64] * 4 + [i32] + [vp] * 6
@@ -184,9 +188,11 @@ def segment_bytes(shape, segments: int) -> int:
     return n.value
 
 
-def segments_auto(shape) -> int:
+def segments_auto(shape, backward: bool = False) -> int:
     n = ctypes.c_int(0)
-    _check(load_library().gdn_segments_auto(ctypes.byref(shape), ctypes.byref(n)))
+    lib = load_library()
+    fn = lib.gdn_backward_segments_auto if backward else lib.gdn_segments_auto
+    _check(fn(ctypes.byref(shape), ctypes.byref(n)))
     return n.value
 
 
@@ -256,8 +262,12 @@ def decode(q, k, v, a, b, A_log, dt_bias, state, mask=None, *, state_out=None, o
     return o, sT
 
 
-def backward(q, k, v, a, b, A_log, dt_bias, mask, saved, d_o, d_state_T=None, *, out=None):
-    """Run gdn_backward.  Returns dict(dq, dk, dv, da, db, dA_log, ddt_bias, dstate0)."""
+def backward(q, k, v, a, b, A_log, dt_bias, mask, saved, d_o, d_state_T=None, *, out=None,
+             segments=None):
+    """Run gdn_backward.  Returns dict(dq, dk, dv, da, db, dA_log, ddt_bias, dstate0).
+    An integer ``segments`` runs gdn_backward_segmented with that count instead
+    (1: one reverse pass, 0: the automatic count); ws then also holds the
+    segment buffers of that count."""
     dt = q.dtype
     _cuda(d_o, "d_o", dt)
     _cuda(d_state_T, "d_state_T", torch.float32)
@@ -291,12 +301,17 @@ def backward(q, k, v, a, b, A_log, dt_bias, mask, saved, d_o, d_state_T=None, *,
         g["dstate0"] = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=dev)
     ws = out.get("ws")
     if ws is None:
-        ws = _buf(workspace_bytes(shape, 1), dev)
-    rc = load_library().gdn_backward(
-        ctypes.byref(shape), _p(q), _p(k), _p(v), _p(a), _p(b), _p(A_log), _p(dt_bias),
-        _p(m), _p(saved), ctypes.c_size_t(saved.numel()), _p(d_o), _p(d_state_T),
-        _p(g["dq"]), _p(g["dk"]), _p(g["dv"]), _p(g["da"]), _p(g["db"]), _p(g["dA_log"]),
-        _p(g["ddt_bias"]), _p(g["dstate0"]), _p(ws), ctypes.c_size_t(ws.numel()), _stream())
+        extra = segment_bytes(shape, segments) if segments is not None else 0
+        ws = _buf(workspace_bytes(shape, 1) + extra, dev)
+    lib = load_library()
+    args = (_p(q), _p(k), _p(v), _p(a), _p(b), _p(A_log), _p(dt_bias),
+            _p(m), _p(saved), ctypes.c_size_t(saved.numel()), _p(d_o), _p(d_state_T),
+            _p(g["dq"]), _p(g["dk"]), _p(g["dv"]), _p(g["da"]), _p(g["db"]), _p(g["dA_log"]),
+            _p(g["ddt_bias"]), _p(g["dstate0"]), _p(ws), ctypes.c_size_t(ws.numel()), _stream())
+    if segments is None:
+        rc = lib.gdn_backward(ctypes.byref(shape), *args)
+    else:
+        rc = lib.gdn_backward_segmented(ctypes.byref(shape), int(segments), *args)
     _check(rc)
     return g
 

@@ -174,16 +174,44 @@ gdn_status gdn_forward_segmented(const gdn_shape* shape, int segments, const voi
                                  const uint8_t* mask, void* o, float* state_T, void* saved,
                                  size_t saved_bytes, void* ws, size_t ws_bytes, void* stream);
 
-/* Extra workspace bytes of gdn_forward_segmented with `segments` (0 = automatic):
- * the segment maps [segments - 1][B][Hv][Dk][Dv + Dk rounded up to 128] and the
- * chained start states [segments - 1][B][Hv][Dk][Dv], fp32.  0 for one segment.
- * Host-only. */
+/* The reverse scan of the backward is affine in the state cotangent too, with
+ * the transposed chunk transition as its linear part, so gdn_backward_segmented
+ * runs it in the same three passes (segments counted from the end of the
+ * sequence, the first one possibly shorter): the maps, the chain from
+ * d_state_T, every segment's reverse scan; the per-chunk gradients then run as
+ * their own launch on every SM instead of beside a single scan.  gdn_backward
+ * takes the automatic count of a model that weighs that against the single
+ * fused launch (one segment at the benched 9B layer shape).
+ *   - Arguments as gdn_backward.  ws must hold gdn_workspace_bytes(shape, 1)
+ *     plus gdn_segment_bytes(shape, segments) bytes.
+ *   - segments = 1: one reverse pass (as gdn_backward picks it for one
+ *     segment); 0: the automatic count; requirements as gdn_forward_segmented.
+ *   - Any saved buffer of gdn_forward / gdn_forward_segmented of the same
+ *     inputs is accepted: the segment counts of the two need not agree. */
+gdn_status gdn_backward_segmented(const gdn_shape* shape, int segments, const void* q,
+                                  const void* k, const void* v, const void* a, const void* b,
+                                  const float* A_log, const float* dt_bias, const uint8_t* mask,
+                                  const void* saved, size_t saved_bytes, const void* d_o,
+                                  const float* d_state_T, void* dq, void* dk, void* dv, void* da,
+                                  void* db, float* dA_log, float* ddt_bias, float* dstate0,
+                                  void* ws, size_t ws_bytes, void* stream);
+
+/* Extra workspace bytes of gdn_forward_segmented / gdn_backward_segmented with
+ * `segments` segments (0: the forward's automatic count): the segment maps
+ * [segments - 1][B][Hv][Dk][Dv + Dk rounded up to 128] and the chained states
+ * [segments - 1][B][Hv][Dk][Dv], fp32.  0 for one segment.  gdn_workspace_bytes
+ * already includes the buffers of the automatic counts.  Host-only. */
 gdn_status gdn_segment_bytes(const gdn_shape* shape, int segments, size_t* bytes);
 
 /* The segment count the automatic choice takes (1 = the plain scan): the count
  * that minimises a model of the sequential chain, in waves of the GPU's SMs times
  * chunks per run.  Reads the SM count of the current device. */
 gdn_status gdn_segments_auto(const gdn_shape* shape, int* segments);
+
+/* The backward's automatic segment count (1 = one reverse pass, fused with the
+ * per-chunk gradients where that fits).  Reads the SM count of the current
+ * device. */
+gdn_status gdn_backward_segments_auto(const gdn_shape* shape, int* segments);
 
 /* ---- per-key-channel gates ------------------------------------------------ */
 
