@@ -217,3 +217,28 @@ def test_segmented_forward_sizing_and_rejections(lib):
     mis = list(fwd)
     mis[0] = vp(0x1004)
     assert lib.gdn_forward_segmented(ctypes.byref(s), 4, *mis) == 4
+
+
+def test_segmented_backward_rejections(lib):
+    """gdn_backward_segmented: the host checks before any launch."""
+    s = _shape(B=2, T=64 * 10, Hk=2, Hv=4, Dk=128, Dv=128)
+    s32 = _shape(B=1, T=64 * 10, Dk=128, Dv=128, dtype=0)
+    a = ctypes.c_int()
+    assert lib.gdn_backward_segments_auto(ctypes.byref(s), ctypes.byref(a)) == 0 and a.value >= 1
+    assert lib.gdn_backward_segments_auto(ctypes.byref(s), None) == 1
+    vp = ctypes.c_void_p
+    P = vp(0x1000)
+    big = ctypes.c_size_t(1 << 40)
+    bwd = [P] * 9 + [big] + [P] * 10 + [P, big, None]
+    assert lib.gdn_backward_segmented(ctypes.byref(s32), 4, *bwd) == 2      # no tensor-core scan
+    assert lib.gdn_backward_segmented(ctypes.byref(s), -1, *bwd) == 1       # bad count
+    small = list(bwd)
+    small[21] = ctypes.c_size_t(16)
+    assert lib.gdn_backward_segmented(ctypes.byref(s), 4, *small) == 3      # ws too small
+    mis = list(bwd)
+    mis[0] = vp(0x1004)
+    assert lib.gdn_backward_segmented(ctypes.byref(s), 4, *mis) == 4        # misaligned
+    # the backward's workspace covers its automatic count's segment buffers
+    n0, n1 = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.gdn_workspace_bytes(ctypes.byref(s), 1, ctypes.byref(n1)) == 0
+    assert lib.gdn_segment_bytes(ctypes.byref(s), 4, ctypes.byref(n0)) == 0 and n0.value > 0
