@@ -166,3 +166,16 @@ def test_segmented_backward_deterministic_and_automatic():
     gr = oracle_backward(x)
     for name in oracle.GRAD_NAMES:
         check(name, g3[name], gr[name], TOL[w.dtype])
+
+
+def test_automatic_counts_on_this_gpu():
+    """The cost models keep the single-pass scans (and the fused backward) at the
+    9B layer shape, and split both scans for few heads over a long sequence."""
+    ops = _ops()
+    nine = ops.GdnShape(1, 2048, 16, 64, 192, 128, 1, 0)
+    assert ops.segments_auto(nine) == 1 and ops.segments_auto(nine, backward=True) == 1
+    long_ = ops.GdnShape(1, 65536, 4, 8, 128, 128, 1, 0)
+    assert ops.segments_auto(long_) > 1 and ops.segments_auto(long_, backward=True) > 1
+    n = ctypes.c_size_t()
+    lib = ops.load_library()
+    assert lib.gdn_segment_bytes(ctypes.byref(nine), 0, ctypes.byref(n)) == 0 and n.value == 0
