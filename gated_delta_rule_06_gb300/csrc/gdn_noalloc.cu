@@ -54,16 +54,23 @@ extern "C" gdn_status gdn_forward_noalloc(const gdn_shape* shape, const void* q,
                                           const float* A_log, const float* dt_bias,
                                           const float* state0, const uint8_t* mask, void* o,
                                           float* state_T, void* stream) {
-    size_t need = 0;
+    size_t need = 0, seg = 0;
     gdn_status st = gdn_workspace_bytes(shape, 2, &need);
+    if (st == GDN_OK) st = gdn_segment_bytes(shape, 0, &seg);
     if (st != GDN_OK) return st;
-    if (need > kNoAllocScratchBytes) return GDN_ERR_WORKSPACE_TOO_SMALL;
+    // the automatic segment count's buffers are part of `need`; when only the
+    // single-pass scan fits, that runs instead
+    const bool fits = need <= kNoAllocScratchBytes;
+    if (!fits && need - seg > kNoAllocScratchBytes) return GDN_ERR_WORKSPACE_TOO_SMALL;
     cudaError_t err = cudaSuccess;
     void* scratch = scratch_on_current_device(&err);
     if (scratch == nullptr) return GDN_ERR_CUDA;
     // Nothing in the scratch has to start at zero: every intermediate is
     // written before it is read.  The previous call's contents are simply
     // overwritten.
-    return gdn_forward(shape, q, k, v, a, b, A_log, dt_bias, state0, mask, o, state_T, nullptr, 0,
-                       scratch, kNoAllocScratchBytes, stream);
+    if (fits)
+        return gdn_forward(shape, q, k, v, a, b, A_log, dt_bias, state0, mask, o, state_T, nullptr,
+                           0, scratch, kNoAllocScratchBytes, stream);
+    return gdn_forward_segmented(shape, 1, q, k, v, a, b, A_log, dt_bias, state0, mask, o, state_T,
+                                 nullptr, 0, scratch, kNoAllocScratchBytes, stream);
 }

@@ -307,8 +307,11 @@ gdn_status gdn_decode_conv(const gdn_shape* shape, int32_t gates, int64_t K, con
  *     saved = NULL; the caller passes only inputs and outputs.
  *   - The scratch is a static device array of gdn_noalloc_scratch_bytes()
  *     bytes (64 MiB) that every GPU which loads the library holds until the
- *     process exits.  Shapes whose gdn_workspace_bytes(shape, 2) exceeds it are
- *     rejected with GDN_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ *     process exits.  When gdn_workspace_bytes(shape, 2) exceeds it but the
+ *     same less gdn_segment_bytes(shape, 0) fits, the single-pass scan runs
+ *     (as gdn_forward_segmented with one segment); shapes for which that does
+ *     not fit either are rejected with GDN_ERR_WORKSPACE_TOO_SMALL before
+ *     anything is launched.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
  *   - All calls share the one array and leave their intermediates in it:
