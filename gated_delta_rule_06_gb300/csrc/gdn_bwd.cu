@@ -438,19 +438,36 @@ __device__ __forceinline__ void st8(__nv_bfloat16* o, const float* v) {
     *reinterpret_cast<uint4*>(o) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// TI: input dtype; PT: dtype of the per-value-head partials; blk: this
-// block's index among the ceil(B T Hk / 8) blocks of this part
-template <typename TI, typename PT>
+// lanes that share one (b, t, key head) row: 8 columns each, the smallest
+// power of two that covers Dk (a warp takes 32 / qk_lanes rows)
+__host__ __device__ inline int qk_lanes(int64_t Dk) { return Dk > 128 ? 32 : Dk > 64 ? 16 : 8; }
+// blocks of the q / k part: 8 warps each
+inline int64_t qk_blocks(const Dims& d) {
+    const int64_t rows_per_blk = 8 * (32 / qk_lanes(d.Dk));
+    return (d.B * d.T * d.Hk + rows_per_blk - 1) / rows_per_blk;
+}
+
+// TI: input dtype; PT: dtype of the per-value-head partials; W: 32 (one row
+// per warp, Dk > 128) or 0 (qk_lanes(Dk) taken at run time: measured faster for
+// the narrower rows than the unrolled constant); blk: this block's index among
+// the qk_blocks(d) blocks of this part
+template <typename TI, typename PT, int W>
 __device__ __forceinline__ void bwd_qk_body(const Dims& d, const Ptrs& p, int64_t blk) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t row = blk * (blockDim.x >> 5) + warp;  // over (b, t, j)
-    if (row >= d.B * d.T * d.Hk) return;
-    const int64_t j = row % d.Hk;
-    const int64_t t = (row / d.Hk) % d.T;
-    const int64_t bb = row / (d.Hk * d.T);
     const int Dk = (int)d.Dk, G = (int)d.G;
-    const bool act = 8 * lane < Dk;
-    const int c0 = act ? 8 * lane : 0;
+    const int LPR = W ? W : qk_lanes(Dk);
+    const int sub = lane % LPR;
+    // over (b, t, j); a lane group past the last row computes zeros and stores
+    // nothing, but takes part in the warp's shuffles (a whole warp past it leaves)
+    const int64_t row = (blk * (blockDim.x >> 5) + warp) * (32 / LPR) + lane / LPR;
+    const bool valid = row < d.B * d.T * d.Hk;
+    if (W == 32 && !valid) return;
+    const int64_t rr = valid ? row : 0;
+    const int64_t j = rr % d.Hk;
+    const int64_t t = (rr / d.Hk) % d.T;
+    const int64_t bb = rr / (d.Hk * d.T);
+    const bool act = valid && 8 * sub < Dk;
+    const int c0 = act ? 8 * sub : 0;
     const int64_t xoff = ((bb * d.T + t) * d.Hk + j) * Dk + c0;
     const int64_t hstride = d.Tp * Dk;  // next value head of the group
     const int64_t off0 = ((bb * d.Hv + j * d.G) * d.Tp + t) * Dk + c0;
@@ -499,8 +516,7 @@ __device__ __forceinline__ void bwd_qk_body(const Dims& d, const Ptrs& p, int64_
             u[ps][c] *= r;
             dot = fmaf(u[ps][c], y[ps][c], dot);
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+        for (int off = LPR / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
         if (act) {
             float o[8];
 #pragma unroll
@@ -579,7 +595,7 @@ __device__ __forceinline__ void bwd_gate_body(const Dims& d, const Ptrs& p, int 
 // The two independent parts of the reduction in one launch: blocks
 // [0, NC B ceil(Hv / 8)) take the gate cotangents (first, so that they start
 // early: the per-head sum waits for them), the rest the q / k rows.
-template <typename TI, typename PT>
+template <typename TI, typename PT, int W>
 __global__ void __launch_bounds__(256) bwd_reduce_kernel(Dims d, Ptrs p) {
     const int64_t nhz = (d.Hv + kGateHeadsB - 1) / kGateHeadsB;
     const int64_t ngate = d.NC * d.B * nhz;
@@ -588,15 +604,15 @@ __global__ void __launch_bounds__(256) bwd_reduce_kernel(Dims d, Ptrs p) {
         const int c = (int)(blk % d.NC), bb = (int)((blk / d.NC) % d.B), hz = (int)(blk / (d.NC * d.B));
         bwd_gate_body<TI>(d, p, c, bb, hz);
     } else {
-        bwd_qk_body<TI, PT>(d, p, blk - ngate);
+        bwd_qk_body<TI, PT, W>(d, p, blk - ngate);
     }
 }
 
 // the q / k part alone (fp32 per-head partials), for callers whose gate
 // cotangents come out elsewhere
-template <typename TI>
+template <typename TI, int W>
 __global__ void __launch_bounds__(256) bwd_qk_kernel(Dims d, Ptrs p) {
-    bwd_qk_body<TI, float>(d, p, blockIdx.x);
+    bwd_qk_body<TI, float, W>(d, p, blockIdx.x);
 }
 
 // dA_log / ddt_bias: one warp per head.  Lane l sums the partials of rows
@@ -654,12 +670,17 @@ cudaError_t launch_bchunk_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
 
 template <typename TI>
 cudaError_t launch_reduce_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
-    const int64_t rows = d.B * d.T * d.Hk;
-    const int64_t nblk = (rows + 7) / 8 + d.NC * d.B * ((d.Hv + kGateHeadsB - 1) / kGateHeadsB);
+    const int64_t nblk = qk_blocks(d) + d.NC * d.B * ((d.Hv + kGateHeadsB - 1) / kGateHeadsB);
+    const int lpr = qk_lanes(d.Dk);
+    auto go = [&](auto pt) {
+        using PT = decltype(pt);
+        if (lpr == 32) bwd_reduce_kernel<TI, PT, 32><<<(unsigned)nblk, 256, 0, s>>>(d, p);
+        else bwd_reduce_kernel<TI, PT, 0><<<(unsigned)nblk, 256, 0, s>>>(d, p);
+    };
     if (tc_path(d))
-        bwd_reduce_kernel<TI, __nv_bfloat16><<<(unsigned)nblk, 256, 0, s>>>(d, p);
+        go(__nv_bfloat16());
     else
-        bwd_reduce_kernel<TI, float><<<(unsigned)nblk, 256, 0, s>>>(d, p);
+        go(float());
     if (d.gates == 1) {  // log_decay / beta inputs: no per-head parameters to sum
         count_launches(1);
         return cudaPeekAtLastError();
@@ -686,11 +707,17 @@ cudaError_t launch_bwd_chunk(const Dims& d, const Ptrs& p, cudaStream_t s) {
 }
 
 cudaError_t launch_qk_reduce(const Dims& d, const Ptrs& p, cudaStream_t s) {
-    const unsigned nblk = (unsigned)((d.B * d.T * d.Hk + 7) / 8);
+    const unsigned nblk = (unsigned)qk_blocks(d);
+    const int lpr = qk_lanes(d.Dk);
+    auto go = [&](auto ti) {
+        using TI = decltype(ti);
+        if (lpr == 32) bwd_qk_kernel<TI, 32><<<nblk, 256, 0, s>>>(d, p);
+        else bwd_qk_kernel<TI, 0><<<nblk, 256, 0, s>>>(d, p);
+    };
     if (d.dtype == 1)
-        bwd_qk_kernel<__nv_bfloat16><<<nblk, 256, 0, s>>>(d, p);
+        go(__nv_bfloat16());
     else
-        bwd_qk_kernel<float><<<nblk, 256, 0, s>>>(d, p);
+        go(float());
     count_launches(1);
     return cudaPeekAtLastError();
 }
