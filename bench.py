@@ -65,15 +65,98 @@ def _peaks():
 
 
 # ---------------------------------------------------------------------------
-# algorithmic work model (per launch of each phase)
+# algorithmic work (the method's own bytes and flops, per phase)
 # ---------------------------------------------------------------------------
 
-def work_model(w, conv_k=0, gates="ab", nseg=1, nseg_bwd=1):
-    """Per-phase algorithmic flops and bytes of one fwd+bwd step, in the storage
-    formats the kernels use: bf16 inputs keep the saved intermediates as bf16
-    operand images (checkpoints, T, W, P, Delta as hi + lo, state cotangents,
-    -Dbar, the q / k rows of each chunk) and the per-value-head q / k
-    cotangents in bf16, fp32 inputs all of them as fp32 arrays."""
+def method_model(w, gates="ab", nseg=1, nseg_bwd=1, conv_k=0):
+    """The method's own bytes and flops, per phase and per step.
+
+    Bytes count only the method's tensors: the primal inputs and outputs, the
+    cotangents, and one fp32 state checkpoint per (b, h, chunk), which the
+    forward writes once and the backward reads once.  A phase is charged for
+    each of those tensors it reads or writes itself; intermediates the
+    implementation keeps between its kernels (gate sums, WY images, state
+    cotangent images, per-value-head q / k cotangents) count nothing.  Flops
+    per token and value head (C the chunk, G the GQA group, Grams shared by a
+    key head's G value heads): forward 2C(3Dk + 2Dv) + C^2/3 for the
+    chunk-local products and 6 Dk Dv for the scan; backward
+    18C Dk + 10C Dv + 14 Dk Dv + 4C^2, of which 6 Dk Dv + 2C Dv is the
+    reverse scan; each less (1 - 1/G) 4C Dk for the shared Grams.  The step
+    counts every method tensor once per pass plus the checkpoints written and
+    read: 673 MB and 110.8 GFLOP at B1 T2048 Hk16 Hv64 Dk192 Dv128 bf16."""
+    es = 2 if w.dtype == torch.bfloat16 else 4
+    B, T, Hk, Hv, Dk, Dv = w.B, w.T, w.Hk, w.Hv, w.Dk, w.Dv
+    G = Hv // Hk
+    NC = (T + C - 1) // C
+    BH = B * Hv
+    th = B * T * Hv  # (token, value head) pairs
+    qk = 2 * B * T * Hk * Dk * es  # q and k
+    vv = B * T * Hv * Dv * es  # v, o, dO, dv each
+    ab = 2 * B * T * Hv * es  # a and b (or log_decay and beta); da and db
+    st = BH * Dk * Dv * 4  # one fp32 state tensor
+    ckpt = BH * NC * Dk * Dv * 4  # the fp32 chunk checkpoints
+    shared = (1 - 1 / G) * 4 * C * Dk
+    f_chunk = th * (2 * C * (3 * Dk + 2 * Dv) + C * C / 3 - shared)
+    f_scan = th * 6 * Dk * Dv
+    f_bwd = th * (18 * C * Dk + 10 * C * Dv + 14 * Dk * Dv + 4 * C * C - shared)
+    f_bscan = th * (6 * Dk * Dv + 2 * C * Dv)
+    m = {
+        "prep": dict(flops=0.0, bytes=qk + ab),
+        "fwd_chunk": dict(flops=f_chunk, bytes=qk + vv),
+        "fwd_scan": dict(flops=f_scan, bytes=qk + st + vv + st + ckpt),
+        "bwd_scan": dict(flops=f_bscan, bytes=qk + vv + st + st),
+        "bwd_chunk": dict(flops=f_bwd - f_bscan, bytes=qk + 2 * vv + ckpt + vv),
+        "bwd_scan_chunk": dict(flops=f_bwd, bytes=qk + 2 * vv + st + ckpt + vv + st),
+        "bwd_reduce": dict(flops=0.0, bytes=qk + ab + qk + ab + 2 * Hv * 4),
+        "decode": dict(flops=BH * (4 * Dk * Dv + 2 * Dk),
+                       bytes=2 * st + B * Hk * 2 * Dk * es + B * Hv * 2 * Dv * es + B * Hv * 2 * es),
+    }
+    Wd = Dv + -(-Dk // 128) * 128
+    if nseg > 1:
+        # the associative form's own work: per-segment maps over Wd columns and
+        # the chain of segment start states
+        L = -(-NC // nseg)
+        mu = B * Hv * (nseg - 1) * L * C
+        m["fwd_seg_maps"] = dict(flops=mu * (6 * Dk * Wd + 2 * C * Wd), bytes=qk)
+        m["fwd_seg_chain"] = dict(flops=BH * (nseg - 1) * 2 * Dk * Dk * Dv, bytes=st)
+    if nseg_bwd > 1:
+        Lb = -(-NC // nseg_bwd)
+        mb = B * Hv * (nseg_bwd - 1) * Lb * C
+        m["bwd_seg_maps"] = dict(flops=mb * (6 * Dk * Wd + 2 * C * Wd), bytes=qk + vv)
+        m["bwd_seg_chain"] = dict(flops=BH * (nseg_bwd - 1) * 2 * Dk * Dk * Dv, bytes=st)
+    if conv_k:
+        # fused short convolution: the mixed projection, the carried windows in
+        # and out and the taps replace the q / k / v reads
+        Cm = 2 * Hk * Dk + Hv * Dv
+        m["decode"]["flops"] += B * Cm * 2 * conv_k
+        m["decode"]["bytes"] += (B * Cm * (1 + 2 * conv_k) + Cm * conv_k) * es \
+            - (B * Hk * 2 * Dk + BH * Dv) * es
+    io_fwd = qk + vv + ab + vv + 2 * st
+    io_bwd = qk + 2 * vv + ab + st + qk + vv + ab + st
+    m["_step"] = dict(bytes=io_fwd + io_bwd + 2 * ckpt, flops=f_chunk + f_scan + f_bwd)
+    if gates == "kc":
+        # per-key-channel gates: the recurrence per step, forward decay,
+        # prediction, update and read-out (7 Dk Dv); backward the recompute and
+        # the reverse step (20 Dk Dv).  Gate inputs log_decay [B, T, Hv, Dk] and
+        # beta; checkpoints per 64-step chunk as for the scalar gates.
+        gin = B * T * Hv * (Dk + 1) * es
+        m["prep"] = dict(flops=0.0, bytes=qk)
+        m["kc_fwd"] = dict(flops=7.0 * th * Dk * Dv, bytes=qk + vv + gin + vv + 2 * st + ckpt)
+        m["kc_bwd"] = dict(flops=20.0 * th * Dk * Dv,
+                           bytes=qk + 2 * vv + gin + st + ckpt + vv + gin + st)
+        m["bwd_reduce"] = dict(flops=0.0, bytes=2 * qk)
+        m["_step"] = dict(bytes=(qk + 2 * vv + gin + 2 * st) + (2 * qk + 3 * vv + 2 * gin + 2 * st)
+                          + 2 * ckpt, flops=27.0 * th * Dk * Dv)
+    return m
+
+
+def design_model(w, conv_k=0, gates="ab", nseg=1, nseg_bwd=1):
+    """Per-phase bytes this implementation has to move at the least, in the
+    storage formats its kernels use (not the method's algorithmic bytes): bf16
+    inputs keep the saved intermediates as bf16 operand images (checkpoints,
+    T, W, P, Delta as hi + lo, state cotangents, -Dbar, the q / k rows of each
+    chunk) and the per-value-head q / k cotangents in bf16, fp32 inputs all of
+    them as fp32 arrays.  Reported beside the roofline as design_bytes."""
     es = 2 if w.dtype == torch.bfloat16 else 4
     img = 2 if w.dtype == torch.bfloat16 else 4  # checkpoint / T / cotangent images
     B, T, Hk, Hv, Dk, Dv = w.B, w.T, w.Hk, w.Hv, w.Dk, w.Dv
@@ -357,12 +440,27 @@ def run_oracle_step(sub, backward):
     return time.perf_counter() - t0
 
 
+# fp64 work of one sample step: the whole 9B layer (B1 T2048 Hv64 Dk192 Dv128,
+# about 2 s of fwd+bwd on 16 host cores); larger workloads run on as many of
+# their key-head groups as fit in the same budget
+ORACLE_SAMPLE_BUDGET = 1 * 2048 * 64 * 192 * 128
+
+
 def sample_key_heads(w):
-    # a quarter of the key-head groups: a few seconds of fp64 work per step
-    return max(1, w.Hk // 4)
+    per_group = w.B * w.T * w.G * w.Dk * w.Dv
+    return max(1, min(w.Hk, ORACLE_SAMPLE_BUDGET // per_group))
 
 
-def cpu_baseline(w, backward, reps=1, gates="ab", conv_k=0):
+def _sample_text(w, kh, frac, backward):
+    if kh == w.Hk:
+        return (f"the whole workload ({w.B}x{w.T} tokens, {w.Hv} value heads), fp64 "
+                f"{'fwd+bwd' if backward else 'fwd'}")
+    return (f"{kh} of {w.Hk} key-head groups ({int(round(frac * w.Hv))} of {w.Hv} value heads), "
+            f"all {w.B}x{w.T} tokens, fp64 {'fwd+bwd' if backward else 'fwd'}; tokens/s scaled "
+            f"by the head fraction")
+
+
+def cpu_baseline(w, backward, reps=3, gates="ab", conv_k=0):
     import oracle
 
     kh = sample_key_heads(w)
@@ -372,9 +470,7 @@ def cpu_baseline(w, backward, reps=1, gates="ab", conv_k=0):
     tokens = w.B * w.T
     return {"value": tokens * frac / t, "unit": "tokens/s", "cores": oracle.threads(),
             "kind": "oracle",
-            "sample": f"{kh} of {w.Hk} key-head groups ({int(frac * w.Hv)} of {w.Hv} value heads), "
-                      f"all {w.B}x{w.T} tokens, fp64 {'fwd+bwd' if backward else 'fwd'}, "
-                      f"median of {reps}; scaled by the head fraction"}
+            "sample": _sample_text(w, kh, frac, backward) + f", median of {reps}"}
 
 
 def run_reference(args, w, world, rank):
@@ -400,8 +496,8 @@ def run_reference(args, w, world, rank):
         "config": config_of(w, args.gates, args.fused_conv),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(),
                          "kind": "oracle",
-                         "sample": f"{kh} of {w.Hk} key-head groups per step, all "
-                                   f"{w.B}x{w.T} tokens, scaled by the head fraction"},
+                         "sample": _sample_text(w, kh, frac, backward)
+                         + f", mean of {args.steps} steps"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -574,7 +670,8 @@ def run_ours(args, w, world, rank, local):
     seg_ok = shape is not None and args.gates != "kc"
     nseg = ops.segments_auto(shape) if seg_ok else 1
     nseg_bwd = ops.segments_auto(shape, backward=True) if seg_ok and backward else 1
-    model = work_model(w, args.fused_conv, args.gates, nseg, nseg_bwd)
+    model = method_model(w, args.gates, nseg, nseg_bwd, args.fused_conv)
+    design = design_model(w, args.fused_conv, args.gates, nseg, nseg_bwd)
     ph = {phases[i].name.decode(): (phases[i].launches, phases[i].total_ms)
           for i in range(cnt.value)}
     dom = max(ph, key=lambda k: ph[k][1])
@@ -601,16 +698,24 @@ def run_ours(args, w, world, rank, local):
     roof["traffic"] = traffic
     roof["algorithmic_bytes"] = by
     roof["algorithmic_flops"] = fl
+    roof["bytes_basis"] = ("the method's tensors this kernel reads or writes (inputs, outputs, "
+                           "cotangents, fp32 chunk checkpoints); no intermediates")
+    roof["traffic_over_algorithmic"] = (traffic / by) if traffic else None
+    roof["design_bytes"] = design[dom]["bytes"] if dom in design else None
     roof["achieved_tflops"] = fl / avg_s / 1e12
     roof["achieved_gbs"] = by / avg_s / 1e9
     roof["avg_launch_ms"] = avg_s * 1e3
     roof["share"] = dms / sum(v[1] for v in ph.values())
 
     step_bytes = model["_step"]["bytes"] if backward else model["decode"]["bytes"]
-    step_roof = {"algorithmic_bytes": step_bytes,
+    step_flops = model["_step"]["flops"] if backward else model["decode"]["flops"]
+    t_roof = max(step_bytes / (peaks["hbm_gbs"] * 1e9),
+                 step_flops / (peaks["bf16_tflops"] * 1e12) if w.dtype == torch.bfloat16 else 0.0)
+    step_roof = {"algorithmic_bytes": step_bytes, "algorithmic_flops": step_flops,
                  "achieved_gbs": step_bytes / (ms / 1e3) / 1e9,
                  "frac_of_hbm": step_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
-                 "peak_source": f"{peaks['source']} hbm_gbs"}
+                 "roofline_ms": t_roof * 1e3, "frac": t_roof / (ms / 1e3),
+                 "peak_source": f"{peaks['source']} hbm_gbs, bf16_tflops"}
 
     # ---- end to end through the C ABI with host buffers (pinned), copies timed
     if args.no_e2e:

@@ -457,11 +457,14 @@ __device__ __forceinline__ void bwd_qk_body(const Dims& d, const Ptrs& p, int64_
     const int Dk = (int)d.Dk, G = (int)d.G;
     const int LPR = W ? W : qk_lanes(Dk);
     const int sub = lane % LPR;
-    // over (b, t, j); a lane group past the last row computes zeros and stores
-    // nothing, but takes part in the warp's shuffles (a whole warp past it leaves)
-    const int64_t row = (blk * (blockDim.x >> 5) + warp) * (32 / LPR) + lane / LPR;
+    // over (b, t, j).  A warp whose first row is past the last one leaves at
+    // once (the test is uniform over the warp); in the last warp, a lane group
+    // past the last row computes zeros and stores nothing, but takes part in
+    // the warp's shuffles
+    const int64_t warp_row0 = (blk * (blockDim.x >> 5) + warp) * (32 / LPR);
+    if (warp_row0 >= d.B * d.T * d.Hk) return;
+    const int64_t row = warp_row0 + lane / LPR;
     const bool valid = row < d.B * d.T * d.Hk;
-    if (W == 32 && !valid) return;
     const int64_t rr = valid ? row : 0;
     const int64_t j = rr % d.Hk;
     const int64_t t = (rr / d.Hk) % d.T;

@@ -168,6 +168,25 @@ def test_segmented_backward_deterministic_and_automatic():
         check(name, g3[name], gr[name], TOL[w.dtype])
 
 
+def test_segmented_long_runs():
+    """Runs of 33 chunks (NC = 97, three segments forward and backward), the
+    length the automatic counts pick for long sequences: the bf16 maps are
+    composed over dozens of chunks before the chain uses them."""
+    w = wl.custom("seglong", 1, 64 * 96 + 17, 2, 4, 128, 128, dtype=torch.bfloat16, seed=781,
+                  state_sigma=0.02)
+    x = wl.make_inputs(w)
+    xd = to_dev(x)
+    o, sT, saved = _fwd(xd, 3)
+    g = _bwd(xd, saved, 3)
+    torch.cuda.synchronize()
+    o_r, s_r = oracle_forward(x)
+    check("o", o, o_r, TOL[w.dtype])
+    check("state_T", sT, s_r, TOL[w.dtype])
+    gr = oracle_backward(x)
+    for name in oracle.GRAD_NAMES:
+        check(name, g[name], gr[name], TOL[w.dtype])
+
+
 def test_automatic_counts_on_this_gpu():
     """The cost models keep the single-pass scans (and the fused backward) at the
     9B layer shape, and split both scans for few heads over a long sequence."""
