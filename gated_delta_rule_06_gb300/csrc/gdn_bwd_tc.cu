@@ -326,16 +326,7 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
         if (progress == nullptr) return true;
         const unsigned int* f = progress + (int64_t)item_b(it) * d.Hv + item_h(it);
         const unsigned int need = (unsigned int)(ntiles * ((int)d.NC - item_c(it)));
-        if (tc::ld_acquire_gpu(f) < need) {
-            const uint64_t t0 = tc::globaltimer_ns();
-            for (uint32_t i = 1; tc::ld_acquire_gpu(f) < need; ++i) {
-                __nanosleep(64);
-                if ((i & 255u) == 0 && tc::globaltimer_ns() - t0 > 1000000000ull) {
-                    atomicOr(&g_err_bwdtc, tc::kErrWaitTimeout);
-                    return false;
-                }
-            }
-        }
+        if (!tc::poll_geq(f, need, &g_err_bwdtc, tc::kWaitLimitNs)) return false;
         tc::fence_async_global();  // the images it saw released, before the copies read them
         return true;
     };

@@ -221,6 +221,70 @@ extern "C" gdn_status gdn_selftest_tma_tile(int64_t B, int64_t T, int64_t H, int
     return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+namespace gdn {
+namespace {
+
+// A bounded wait that nobody ends: the CTA takes TMEM as the tensor-core
+// kernels do, then waits for an mbarrier phase no thread completes (mode 0)
+// or for a global word the host left below 1 (mode 1, the form of the fused
+// backward's progress poll), with a limit of limit_ns.  On timeout the wait
+// sets the error word; the CTA then frees its TMEM, records out[0] = 1 if the
+// wait succeeded (0 if it gave up) and out[1] = 1 once the TMEM is freed, and
+// returns.
+__global__ void __launch_bounds__(128) selftest_wait_timeout_kernel(int mode, uint64_t limit_ns,
+                                                                    const unsigned int* word,
+                                                                    unsigned int* out) {
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tmem_base;
+    __shared__ int waited;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    if (warp == 0) {
+        tc::tmem_alloc(&tmem_base, 32);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        tc::mbar_init(&bar, 1);  // one arrival expected; none comes
+        tc::fence_mbar_init();
+        waited = 1;
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tbase = tmem_base;
+    bool ok = true;
+    if (mode == 0) {
+        ok = tc::mbar_wait_for(&bar, 0, &g_err_selftest, limit_ns);
+    } else if (tid == 0) {
+        ok = tc::poll_geq(word, 1u, &g_err_selftest, limit_ns);
+    }
+    if (!ok) waited = 0;  // benign: every writer stores 0
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc::tmem_dealloc(tbase, 32);
+        if (tid == 0) {
+            out[0] = (unsigned int)waited;
+            __threadfence();
+            out[1] = 1u;
+        }
+    }
+}
+
+}  // namespace
+}  // namespace gdn
+
+extern "C" gdn_status gdn_selftest_wait_timeout(int mode, uint64_t limit_ns,
+                                                const unsigned int* word, unsigned int* out,
+                                                void* stream) {
+    if (!out || (mode == 1 && !word)) return GDN_ERR_INVALID_ARG;
+    if ((mode != 0 && mode != 1) || limit_ns < 1000ull || limit_ns > gdn::tc::kWaitLimitNs)
+        return GDN_ERR_INVALID_ARG;
+    gdn::selftest_wait_timeout_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+        mode, limit_ns, word, out);
+    gdn::count_launches(1);
+    return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
 extern "C" gdn_status gdn_device_error(unsigned int* flag) {
     if (!flag) return GDN_ERR_INVALID_ARG;
     const unsigned int v = gdn::read_clear_error_all();

@@ -60,18 +60,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait (about one second of wall time).  On timeout it records
-// kErrWaitTimeout in *err and returns false; callers then skip work.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err) {
+// Every wait on another agent gives up after this much wall time.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
+
+// Bounded wait on an mbarrier phase.  On timeout it records kErrWaitTimeout in
+// *err and returns false; callers then skip work.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, unsigned int* err,
+                                              uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && globaltimer_ns() - t0 > 1000000000ull) {
+        if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) {
             atomicOr(err, kErrWaitTimeout);
             return false;
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err) {
+    return mbar_wait_for(bar, parity, err, kWaitLimitNs);
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -193,6 +200,22 @@ __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
     unsigned int v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+// Bounded poll until the global word *f (written by other CTAs with release
+// semantics) reaches `need`; acquire ordering on success.  On timeout it
+// records kErrWaitTimeout in *err and returns false.
+__device__ __forceinline__ bool poll_geq(const unsigned int* f, unsigned int need, unsigned int* err,
+                                         uint64_t limit_ns) {
+    if (ld_acquire_gpu(f) >= need) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1; ld_acquire_gpu(f) < need; ++i) {
+        __nanosleep(64);
+        if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) {
+            atomicOr(err, kErrWaitTimeout);
+            return false;
+        }
+    }
+    return true;
 }
 // ... all but the most recent committed group
 __device__ __forceinline__ void bulk_wait_but1() { asm volatile("cp.async.bulk.wait_group 1;" ::: "memory"); }

@@ -49,6 +49,20 @@ gdn_status gdn_selftest_tma_tile(int64_t B, int64_t T, int64_t H, int64_t D, int
                                  int t0, int h, int xg0, const void* src, void* out,
                                  void* stream);
 
+/* Failure detection check: one CTA takes tensor memory as the tensor-core
+ * kernels do, then waits on something nothing will complete, bounded by
+ * limit_ns (1 us .. 1 s; the kernels use 1 s):
+ *   mode 0: an mbarrier phase that no thread arrives at;
+ *   mode 1: the device word *word reaching 1 (pass a word holding 0), polled
+ *           with acquire loads as the fused backward polls its progress words.
+ * When the wait gives up, the kernel sets the timeout bit (1) of the device
+ * error word (read it with gdn_device_error), frees its tensor memory, writes
+ * out[0] = 0 (1 had the wait succeeded) and then out[1] = 1, and returns; the
+ * context stays usable.  out: device, 2 words.  Enqueued on `stream`; returns
+ * GDN_ERR_INVALID_ARG for a bad mode, limit or pointer. */
+gdn_status gdn_selftest_wait_timeout(int mode, uint64_t limit_ns, const unsigned int* word,
+                                     unsigned int* out, void* stream);
+
 /* Reads and clears the library's device error word (nonzero after a bounded
  * wait inside a kernel gave up).  Synchronises the device. */
 gdn_status gdn_device_error(unsigned int* flag);

@@ -3,6 +3,9 @@ import sys
 
 import pytest
 
+# deterministic cuBLAS for the reference products some GPU tests take with torch
+os.environ.setdefault("CUBLAS_WORKSPACE_CONFIG", ":4096:8")
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)

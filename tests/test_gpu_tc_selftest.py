@@ -106,3 +106,57 @@ def test_no_wait_timeouts(lib):
     flag = ctypes.c_uint(123)
     assert lib.gdn_device_error(ctypes.byref(flag)) == 0
     assert flag.value == 0
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_bounded_wait_gives_up_and_reports(lib, mode):
+    """A wait that nothing completes (mode 0: an mbarrier phase; mode 1: a
+    progress word left at 0) gives up after its limit (1 ms here): the kernel
+    returns, the timeout bit of the device error word is set and then cleared
+    by reading it, the kernel freed its tensor memory before returning, and the
+    next launches run normally."""
+    import time
+
+    from gated_delta_rule_06_gb300 import workloads as wl
+    from parity_util import TOL, check, gpu_backward, gpu_forward, oracle_backward, \
+        oracle_forward, to_dev
+
+    lib.gdn_selftest_wait_timeout.argtypes = [ctypes.c_int, ctypes.c_uint64, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_void_p]
+    lib.gdn_selftest_wait_timeout.restype = ctypes.c_int
+    flag = ctypes.c_uint(123)
+    assert lib.gdn_device_error(ctypes.byref(flag)) == 0 and flag.value == 0
+    word = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    rc = lib.gdn_selftest_wait_timeout(mode, 1_000_000, ctypes.c_void_p(word.data_ptr()),
+                                       ctypes.c_void_p(out.data_ptr()), stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert elapsed < 0.5, elapsed  # 1 ms limit (plus launch): far below the kernels' 1 s
+    assert out.tolist() == [0, 1]  # gave up; tensor memory freed before returning
+    assert lib.gdn_device_error(ctypes.byref(flag)) == 0
+    assert flag.value & 1, flag.value
+    assert lib.gdn_device_error(ctypes.byref(flag)) == 0 and flag.value == 0  # cleared
+    # bad arguments are refused before any launch
+    assert lib.gdn_selftest_wait_timeout(2, 1_000_000, None, ctypes.c_void_p(out.data_ptr()),
+                                         stream) != 0
+    assert lib.gdn_selftest_wait_timeout(0, 10 ** 10, None, ctypes.c_void_p(out.data_ptr()),
+                                         stream) != 0
+    # the context is intact: the tensor-core self-check and a forward + backward pass
+    D, ref = _run(lib, 128, 64, 64, 0, 0, seed=5)
+    torch.testing.assert_close(D, ref, rtol=1e-5, atol=1e-4)
+    w = wl.custom("after_timeout", 1, 130, 2, 4, 64, 64, dtype=torch.bfloat16, seed=41)
+    x = wl.make_inputs(w)
+    xd = to_dev(x)
+    o, sT, saved = gpu_forward(xd)
+    g = gpu_backward(xd, saved)
+    torch.cuda.synchronize()
+    o_r, _ = oracle_forward(x)
+    check("o", o, o_r, TOL[torch.bfloat16])
+    gr = oracle_backward(x)
+    check("dk", g["dk"], gr["dk"], TOL[torch.bfloat16])
+    assert lib.gdn_device_error(ctypes.byref(flag)) == 0 and flag.value == 0
