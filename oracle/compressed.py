@@ -25,10 +25,17 @@ Readings where the page is silent (each one is listed in the design notes):
   1e-12 of its own norm (it lies in the span of the earlier ones, to
   rounding) is set to zero, so a state of rank below r keeps its whole range
   and nothing else.
-* The VJP holds each boundary's basis fixed: the truncation is the linear
-  map S -> P S with P = Q Q^T, so its cotangent is P S_bar (P is symmetric).
-  The basis' own dependence on S is not differentiated (a stop-gradient on
-  Q).
+* The VJP passes the state cotangent straight through each boundary: the
+  backward is the chunked VJP evaluated along the compressed trajectory (each
+  chunk from its truncated start state), with the truncation's own
+  derivative taken as the identity.  It is the exact gradient of the forward
+  in which each boundary adds the fixed offset P S - S (a stop-gradient on
+  the truncation error).  Differentiating the truncation itself is
+  ill-conditioned wherever the state's spectrum has no gap at r (its
+  derivative divides by sigma_r^2 - sigma_{r+1}^2), which is the common case
+  for states that decay over a chunk, and even with the basis held fixed the
+  projected cotangent P S_bar changes by O(|S_bar|) with the choice of basis
+  inside a numerically null part of the state's range.
 
 The chunk recurrence itself is the pinned sequential oracle (`oracle.forward`
 / `oracle.backward`) run one chunk at a time from the truncated chunk state;
@@ -96,48 +103,54 @@ def _sl(x, t0, t1):
 
 
 def forward_compressed(q, k, v, a, b, A_log, dt_bias, state0, mask, omega, iters=3,
-                       bases=None):
+                       offsets=None):
     """Forward with the state truncated at every chunk boundary.
 
-    Returns (o, state_T, chunk_states, bases): chunk_states[c] is the state
-    chunk c starts from ([B, Hv, Dk, Dv]: state0 for c = 0, the truncated
-    state for c >= 1), bases[c] the basis Q of boundary c ([B, Hv, Dk, r],
-    None for c = 0).  Passing `bases` holds every boundary's basis fixed at the
-    given values instead of computing it (used to check the VJP by finite
-    differences)."""
+    Returns (o, state_T, chunk_states, bases, offsets): chunk_states[c] is the
+    state chunk c starts from ([B, Hv, Dk, Dv]: state0 for c = 0, the
+    truncated state for c >= 1), bases[c] the basis Q of boundary c
+    ([B, Hv, Dk, r]) and offsets[c] the truncation's change P S - S there
+    (both None for c = 0).  Passing `offsets` adds those fixed offsets at the
+    boundaries instead of truncating (the function whose exact gradient the
+    straight-through VJP is; used to check it by finite differences)."""
     q, k, v, a, b, A_log, dt_bias, state0, omega = map(
         _f64, (q, k, v, a, b, A_log, dt_bias, state0, omega))
     mask = _o._u8(mask)
     B, T, Hk, Hv, Dk, Dv = _o._dims(q, v)
     S = np.zeros((B, Hv, Dk, Dv)) if state0 is None else state0.copy()
     o = np.zeros((B, T, Hv, Dv))
-    states, used = [], []
+    states, bases, offs = [], [], []
     spans = _chunks(T)
     for c, (t0, t1) in enumerate(spans):
-        if c > 0:
+        if c > 0 and offsets is not None:
+            bases.append(None)
+            offs.append(offsets[c])
+            S = S + offsets[c]
+        elif c > 0:
             Qc = np.zeros((B, Hv, Dk, omega.shape[1]))
             St = np.zeros_like(S)
             for bb in range(B):
                 for h in range(Hv):
-                    if bases is None:
-                        Qc[bb, h] = subspace_basis(S[bb, h], omega, iters)
-                    else:
-                        Qc[bb, h] = bases[c][bb, h]
+                    Qc[bb, h] = subspace_basis(S[bb, h], omega, iters)
                     St[bb, h] = Qc[bb, h] @ (Qc[bb, h].T @ S[bb, h])
+            bases.append(Qc)
+            offs.append(St - S)
             S = St
-            used.append(Qc)
         else:
-            used.append(None)
+            bases.append(None)
+            offs.append(None)
         states.append(S.copy())
         oc, S = _o.forward(_sl(q, t0, t1), _sl(k, t0, t1), _sl(v, t0, t1), _sl(a, t0, t1),
                            _sl(b, t0, t1), A_log, dt_bias, S, _sl(mask, t0, t1))
         o[:, t0:t1] = oc
-    return o, S, states, used
+    return o, S, states, bases, offs
 
 
 def backward_compressed(q, k, v, a, b, A_log, dt_bias, state0, mask, d_o, d_state_T, omega,
                         iters=3):
-    """VJP of forward_compressed with every boundary's basis held fixed.
+    """VJP of forward_compressed, the state cotangent passed straight through
+    every boundary: chunk by chunk in reverse, the VJP of the recurrence from
+    that chunk's (truncated) start state.
 
     Returns a dict with dq, dk, dv, da, db, dA_log, ddt_bias, dstate0 (the
     names and shapes of oracle.backward)."""
@@ -145,8 +158,8 @@ def backward_compressed(q, k, v, a, b, A_log, dt_bias, state0, mask, d_o, d_stat
         _f64, (q, k, v, a, b, A_log, dt_bias, state0, d_o, d_state_T, omega))
     mask = _o._u8(mask)
     B, T, Hk, Hv, Dk, Dv = _o._dims(q, v)
-    _, _, states, bases = forward_compressed(q, k, v, a, b, A_log, dt_bias, state0, mask,
-                                             omega, iters)
+    _, _, states, _, _ = forward_compressed(q, k, v, a, b, A_log, dt_bias, state0, mask,
+                                            omega, iters)
     out = dict(dq=np.zeros(q.shape), dk=np.zeros(k.shape), dv=np.zeros(v.shape),
                da=np.zeros(a.shape), db=np.zeros(b.shape), dA_log=np.zeros(Hv),
                ddt_bias=np.zeros(Hv), dstate0=None)
@@ -161,10 +174,7 @@ def backward_compressed(q, k, v, a, b, A_log, dt_bias, state0, mask, d_o, d_stat
             out[n][:, t0:t1] = g[n]
         out["dA_log"] += g["dA_log"]
         out["ddt_bias"] += g["ddt_bias"]
-        Sb = g["dstate0"]  # cotangent of the state chunk c starts from
-        if c > 0:  # through the truncation at boundary c: P S_bar
-            Qc = bases[c]
-            Sb = np.einsum("bhir,bhjr,bhjv->bhiv", Qc, Qc, Sb)
+        Sb = g["dstate0"]  # cotangent of the state chunk c starts from, passed on
     out["dstate0"] = Sb
     return out
 

@@ -9,8 +9,9 @@ numpy's SVD truncated; the result is a projection, so applying it twice
 changes nothing; no rank-r matrix is closer to S than the SVD truncation).
 The recurrence with truncation is pinned by its special cases (one chunk has
 no boundary and equals the plain recurrence; a rank equal to the key width
-makes every truncation the identity) and its VJP by central differences with
-the boundary bases held fixed, which is the reading of the VJP.
+makes every truncation the identity) and its straight-through VJP by central
+differences of the forward in which every boundary adds its truncation
+offset P S - S held fixed, the function whose exact gradient that VJP is.
 """
 
 import numpy as np
@@ -112,7 +113,7 @@ def test_one_chunk_has_no_boundary():
     w = wl.custom("c1", 2, 60, 2, 4, 16, 12, seed=11, mask="half_second_batch")
     x = _inputs(w)
     om = _omega(12, 2)
-    o, sT, _, _ = oc.forward_compressed(*_args(x), om, 3)
+    o, sT, _, _, _ = oc.forward_compressed(*_args(x), om, 3)
     o_p, s_p = oracle.forward(*_args(x))
     assert np.array_equal(o, o_p) and np.array_equal(sT, s_p)
     g = oc.backward_compressed(*_args(x), x["d_o"], x["d_state_T"], om, 3)
@@ -131,7 +132,7 @@ def test_rank_equal_to_key_width_is_the_plain_recurrence():
     x = _inputs(w)
     x["a"][:] = -20.0
     om = _omega(12, 8, seed=6)
-    o, sT, _, _ = oc.forward_compressed(*_args(x), om, 3)
+    o, sT, _, _, _ = oc.forward_compressed(*_args(x), om, 3)
     o_p, s_p = oracle.forward(*_args(x))
     assert _rel(o, o_p) <= 1e-12 and _rel(sT, s_p) <= 1e-12
     g = oc.backward_compressed(*_args(x), x["d_o"], x["d_state_T"], om, 3)
@@ -147,7 +148,7 @@ def test_truncation_applies_at_boundaries_only():
     w = wl.custom("cb", 1, 150, 1, 2, 16, 12, seed=17)
     x = _inputs(w)
     om = _omega(12, 2, seed=8)
-    o, _, states, bases = oc.forward_compressed(*_args(x), om, 3)
+    o, _, states, bases, _ = oc.forward_compressed(*_args(x), om, 3)
     o_p, _ = oracle.forward(*_args(x))
     assert np.array_equal(o[:, :64], o_p[:, :64])
     assert _rel(o[:, 64:], o_p[:, 64:]) > 1e-3
@@ -168,19 +169,20 @@ GRAD_OF = dict(q="dq", k="dk", v="dv", a="da", b="db", A_log="dA_log", dt_bias="
                state0="dstate0")
 
 
-def test_vjp_with_fixed_bases_matches_central_differences():
-    """L = <o, dO> + <S_T, dS_T> of the forward with every boundary's basis held
-    at its value at the unperturbed inputs: fp64 central differences of every
-    input against backward_compressed (3 boundaries, GQA, a masked tail, the
-    clamp head)."""
+def test_straight_through_vjp_matches_central_differences():
+    """L = <o, dO> + <S_T, dS_T> of the forward in which every boundary adds its
+    truncation offset P S - S, held at its value at the unperturbed inputs:
+    fp64 central differences of every input against backward_compressed (3
+    boundaries, GQA, a masked tail, the clamp head)."""
     w = wl.custom("cfd", 2, 200, 1, 2, 8, 6, seed=19, mask="half_second_batch", clamp_head=True)
     x = _inputs(w)
     om = _omega(6, 3, seed=9)
-    _, _, _, bases = oc.forward_compressed(*_args(x), om, 3)
+    _, _, _, _, offs = oc.forward_compressed(*_args(x), om, 3)
+    assert max(np.abs(d).max() for d in offs[1:]) > 1e-3  # the truncation does act
     g = oc.backward_compressed(*_args(x), x["d_o"], x["d_state_T"], om, 3)
 
     def loss():
-        o, sT, _, _ = oc.forward_compressed(*_args(x), om, 3, bases=bases)
+        o, sT, _, _, _ = oc.forward_compressed(*_args(x), om, 3, offsets=offs)
         return float((o * x["d_o"]).sum() + (sT * x["d_state_T"]).sum())
 
     h = 2.0 ** -17
@@ -201,30 +203,16 @@ def test_vjp_with_fixed_bases_matches_central_differences():
         assert np.abs(an - fd).max() <= 1e-7 * max(np.abs(fd).max(), 1.0), name
 
 
-def test_straight_through_would_be_caught():
-    """A VJP that skipped the projection (the cotangent passed straight through
-    each boundary) gives other input cotangents in the chunks below a
-    boundary than the fixed-basis VJP, on a truncating rank."""
-    w = wl.custom("cst", 1, 140, 1, 1, 8, 6, seed=23)
+def test_offsets_reproduce_the_truncated_forward():
+    """Adding the recorded offsets instead of truncating reproduces the
+    compressed forward (so the finite differences above differentiate the
+    compressed trajectory itself)."""
+    w = wl.custom("coff", 1, 150, 1, 2, 16, 12, seed=29)
     x = _inputs(w)
-    x["a"][:] = -20.0  # slow decay: the boundary's effect reaches far into the chunk below
-    om = _omega(6, 2, seed=10)
-    g = oc.backward_compressed(*_args(x), x["d_o"], x["d_state_T"], om, 3)
-    _, _, states, _ = oc.forward_compressed(*_args(x), om, 3)
-    Sb = x["d_state_T"]
-    st = {}
-    for c, (t0, t1) in reversed(list(enumerate([(0, 64), (64, 128), (128, 140)]))):
-        sl = lambda z: None if z is None else z[:, t0:t1]  # noqa: E731
-        gc = oracle.backward(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["a"]), sl(x["b"]),
-                             x["A_log"], x["dt_bias"], states[c], sl(x["mask"]),
-                             sl(x["d_o"]), Sb)
-        st[c] = gc
-        Sb = gc["dstate0"]  # no projection
-    # chunk 1 sees boundary 2, chunk 0 sees boundary 1 (through its last steps)
-    assert _rel(st[1]["dv"], g["dv"][:, 64:128]) > 1e-3
-    assert _rel(st[0]["dk"], g["dk"][:, :64]) > 1e-3
-    # chunk 2 has no boundary above it: the same in both
-    assert _rel(st[2]["dv"], g["dv"][:, 128:]) <= 1e-14
+    om = _omega(12, 3, seed=12)
+    o, sT, _, _, offs = oc.forward_compressed(*_args(x), om, 3)
+    o2, s2, _, _, _ = oc.forward_compressed(*_args(x), om, 3, offsets=offs)
+    assert _rel(o2, o) <= 1e-13 and _rel(s2, sT) <= 1e-13
 
 
 def test_checkpoint_values():
