@@ -134,6 +134,45 @@ void carve_saved(const Layout& L, void* saved, gdn::Ptrs* p) {
     p->qimg = s + L.qimg;
 }
 
+// Compressed chunk states (rank-r factors in place of the checkpoint images).
+// saved: the other saved regions of make_layout moved down to offset 0, then the
+// initial state (fp32) and the factors Q [B][Hv][NC][Dk][r], R [B][Hv][NC][r][Dv]
+// (fp32; slot 0 unused).  Forward workspace: make_layout's, then the checkpoint
+// images the scan writes (not kept) and two fp32 state buffers (the chunk-end
+// state and the truncated one).  Backward workspace: make_layout's and the
+// segment buffers of its automatic count, then the images rebuilt from the
+// factors.
+struct CLayout {
+    Layout L;  // saved offsets moved down (ckpt unused)
+    size_t S0f, Qf, Rf, saved_total;
+    size_t img, stA, stB, fwd_total;
+    size_t bimg, bwd_total;
+};
+
+CLayout make_clayout(const gdn::Dims& d, int rank, size_t bwd_seg_bytes) {
+    CLayout C{};
+    C.L = make_layout(d);
+    Layout& L = C.L;
+    const size_t sh = L.gam;  // the checkpoint images come first
+    L.ckpt = 0;
+    for (size_t* o : {&L.gam, &L.beta, &L.rq, &L.rk, &L.Tinv, &L.W, &L.P, &L.Delta, &L.kimg, &L.qimg})
+        *o -= sh;
+    const size_t BH = (size_t)d.B * d.Hv;
+    const size_t st = BH * d.Dk * d.Dv * 4;
+    const size_t imgb = BH * d.NC * d.Dk * d.Dv * 2;
+    C.S0f = L.saved_total - sh;
+    C.Qf = align_up(C.S0f + st);
+    C.Rf = align_up(C.Qf + BH * d.NC * d.Dk * rank * 4);
+    C.saved_total = align_up(C.Rf + BH * d.NC * rank * d.Dv * 4);
+    C.img = L.fwd_total;
+    C.stA = align_up(C.img + imgb);
+    C.stB = align_up(C.stA + st);
+    C.fwd_total = align_up(C.stB + st);
+    C.bimg = align_up(L.bwd_total + bwd_seg_bytes);
+    C.bwd_total = align_up(C.bimg + imgb);
+    return C;
+}
+
 // tensor maps of v (and dO, o, U) for the tensor-core kernels: full-width
 // 64-row tiles, dO in tiles of at most 128 columns (the scans' value tile)
 bool make_tmaps(const gdn::Dims& d, const void* v, const void* dO, const void* o, const void* U,
@@ -462,11 +501,17 @@ gdn_status backward_impl(const gdn_shape* shape, int gates, const void* q, const
                          const float* dt_bias, const uint8_t* mask, const void* saved,
                          size_t saved_bytes, const void* d_o, const float* d_state_T, void* dq,
                          void* dk, void* dv, void* da, void* db, float* dA_log, float* ddt_bias,
-                         float* dstate0, void* ws, size_t ws_bytes, void* stream, int segments = 0) {
+                         float* dstate0, void* ws, size_t ws_bytes, void* stream, int segments = 0,
+                         int rank = 0) {
     gdn::Dims d;
     gdn_status st = validate_shape(shape, &d);
     if (st != GDN_OK) return st;
     d.gates = gates;
+    // rank > 0: the saved buffer of gdn_forward_compressed (factors in place of
+    // the checkpoint images; the images are rebuilt into the workspace first)
+    if (rank > 0 && (gates != 0 || !gdn::tc_path(d) || !seg_supported(d) ||
+                     !gdn::compress_supported(d, rank, 0)))
+        return GDN_ERR_UNSUPPORTED_SHAPE;
     // segments of the reverse scan (1: one pass, fused with the gradients when it
     // fits; 0: the automatic choice)
     if (segments < 0) return GDN_ERR_INVALID_ARG;
@@ -485,12 +530,18 @@ gdn_status backward_impl(const gdn_shape* shape, int gates, const void* q, const
     for (const void* p : ptrs)
         if (!aligned16(p)) return GDN_ERR_MISALIGNED;
     const Layout L = make_layout(d);
-    if (saved_bytes < L.saved_total || ws_bytes < L.bwd_total + sbytes) return GDN_ERR_WORKSPACE_TOO_SMALL;
+    const CLayout C = make_clayout(d, rank > 0 ? rank : 1, sbytes);
+    if (rank > 0) {
+        if (saved_bytes < C.saved_total || ws_bytes < C.bwd_total) return GDN_ERR_WORKSPACE_TOO_SMALL;
+    } else if (saved_bytes < L.saved_total || ws_bytes < L.bwd_total + sbytes) {
+        return GDN_ERR_WORKSPACE_TOO_SMALL;
+    }
     gdn::Ptrs p{};
     p.q = q; p.k = k; p.v = v; p.a = a; p.b = b;
     p.A_log = A_log; p.dt_bias = dt_bias;
     p.mask = shape->has_mask ? mask : nullptr;
-    carve_saved(L, const_cast<void*>(saved), &p);
+    carve_saved(rank > 0 ? C.L : L, const_cast<void*>(saved), &p);
+    if (rank > 0) p.ckpt = reinterpret_cast<float*>(static_cast<char*>(ws) + C.bimg);
     p.d_o = d_o; p.d_state_T = d_state_T;
     p.dq = dq; p.dk = dk; p.dv = dv; p.da = da; p.db = db;
     p.dA_log = dA_log; p.ddt_bias = ddt_bias; p.dstate0 = dstate0;
@@ -509,8 +560,17 @@ gdn_status backward_impl(const gdn_shape* shape, int gates, const void* q, const
         if (!make_tmaps(d, v, d_o, nullptr, nullptr, &maps)) return tmap_error();
         p.tmaps = &maps;
     }
-    cudaError_t e;
-    if (nseg > 1) {
+    cudaError_t e = cudaSuccess;
+    if (rank > 0) {
+        const char* sv = static_cast<const char*>(saved);
+        e = run_phase("expand", s, [&] {
+            return gdn::launch_expand_ckpt(d, reinterpret_cast<const float*>(sv + C.S0f),
+                                           reinterpret_cast<const float*>(sv + C.Qf),
+                                           reinterpret_cast<const float*>(sv + C.Rf), rank, p.ckpt, s);
+        });
+    }
+    if (e != cudaSuccess) {
+    } else if (nseg > 1) {
         // segment maps, their chain from d_state_T, every segment's reverse scan,
         // then the per-chunk gradients on every SM
         const size_t nmap = (size_t)(nseg - 1) * d.B * d.Hv * d.Dk;
@@ -530,6 +590,67 @@ gdn_status backward_impl(const gdn_shape* shape, int gates, const void* q, const
         if (e == cudaSuccess) e = run_phase("bwd_chunk", s, [&] { return gdn::launch_bwd_chunk(d, p, s); });
     }
     if (e == cudaSuccess) e = run_phase("bwd_reduce", s, [&] { return gdn::launch_bwd_reduce(d, p, s); });
+    return cuda_status(e);
+}
+
+// gdn_forward_compressed: prep and the chunk-local products as in forward_impl,
+// then the scan one chunk at a time, the state truncated to rank r between
+// chunks (the truncated state is the next chunk's start state; its factors are
+// saved)
+gdn_status forward_compressed_impl(const gdn_shape* shape, int rank, int iters, const float* omega,
+                                   const void* q, const void* k, const void* v, const void* a,
+                                   const void* b, const float* A_log, const float* dt_bias,
+                                   const float* state0, const uint8_t* mask, void* o,
+                                   float* state_T, void* saved, size_t saved_bytes, void* ws,
+                                   size_t ws_bytes, void* stream) {
+    gdn::Dims d;
+    gdn_status st = validate_shape(shape, &d);
+    if (st != GDN_OK) return st;
+    if (!gdn::tc_path(d) || !seg_supported(d) || !gdn::compress_supported(d, rank, iters))
+        return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (!q || !k || !v || !a || !b || !A_log || !dt_bias || !o || !state_T || !saved || !ws || !omega)
+        return GDN_ERR_INVALID_ARG;
+    if (shape->has_mask && !mask) return GDN_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, a, b, A_log, dt_bias, state0, mask, o, state_T, saved, ws, omega};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return GDN_ERR_MISALIGNED;
+    const CLayout C = make_clayout(d, rank, 0);
+    if (saved_bytes < C.saved_total || ws_bytes < C.fwd_total) return GDN_ERR_WORKSPACE_TOO_SMALL;
+    gdn::Ptrs p{};
+    p.q = q; p.k = k; p.v = v; p.a = a; p.b = b;
+    p.A_log = A_log; p.dt_bias = dt_bias; p.state0 = state0;
+    p.mask = shape->has_mask ? mask : nullptr;
+    p.o = o; p.state_T = state_T;
+    carve_saved(C.L, saved, &p);
+    char* wsb = static_cast<char*>(ws);
+    char* sv = static_cast<char*>(saved);
+    p.ckpt = reinterpret_cast<float*>(wsb + C.img);
+    p.U = reinterpret_cast<float*>(wsb + C.L.U);
+    float* S0f = reinterpret_cast<float*>(sv + C.S0f);
+    float* Qf = reinterpret_cast<float*>(sv + C.Qf);
+    float* Rf = reinterpret_cast<float*>(sv + C.Rf);
+    float* stA = reinterpret_cast<float*>(wsb + C.stA);  // truncated state: next chunk's start
+    float* stB = reinterpret_cast<float*>(wsb + C.stB);  // chunk-end state
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    gdn::Tmaps maps;
+    if (!make_tmaps(d, v, nullptr, o, p.U, &maps)) return tmap_error();
+    p.tmaps = &maps;
+    const size_t stbytes = (size_t)d.B * d.Hv * d.Dk * d.Dv * 4;
+    cudaError_t e = state0 ? cudaMemcpyAsync(S0f, state0, stbytes, cudaMemcpyDeviceToDevice, s)
+                           : cudaMemsetAsync(S0f, 0, stbytes, s);
+    if (e == cudaSuccess) e = run_phase("prep", s, [&] { return gdn::launch_prep(d, p, s); });
+    if (e == cudaSuccess) e = run_phase("fwd_chunk", s, [&] { return gdn::launch_fwd_chunk(d, p, s); });
+    for (int64_t c = 0; c < d.NC && e == cudaSuccess; ++c) {
+        gdn::ScanSeg sg{(int)d.NC, 1, 0, nullptr, nullptr};
+        sg.first = (int)c;
+        sg.sin = c > 0 ? stA : nullptr;            // chunk 0 starts from state0
+        sg.sout = c + 1 < d.NC ? stB : nullptr;    // the last chunk writes state_T
+        e = run_phase("fwd_scan", s, [&] { return gdn::launch_fwd_scan_ta_one(d, p, sg, s); });
+        if (e == cudaSuccess && c + 1 < d.NC)
+            e = run_phase("compress", s, [&] {
+                return gdn::launch_trunc(d, stB, omega, rank, iters, stA, Qf, Rf, c + 1, s);
+            });
+    }
     return cuda_status(e);
 }
 }  // namespace
@@ -616,6 +737,45 @@ gdn_status gdn_backward_segmented(const gdn_shape* shape, int segments, const vo
     return backward_impl(shape, 0, q, k, v, a, b, A_log, dt_bias, mask, saved, saved_bytes, d_o,
                          d_state_T, dq, dk, dv, da, db, dA_log, ddt_bias, dstate0, ws, ws_bytes,
                          stream, segments);
+}
+
+gdn_status gdn_compressed_bytes(const gdn_shape* shape, int rank, size_t* saved_bytes,
+                                size_t* fwd_ws_bytes, size_t* bwd_ws_bytes) {
+    gdn::Dims d;
+    gdn_status st = validate_shape(shape, &d);
+    if (st != GDN_OK) return st;
+    if (!saved_bytes || !fwd_ws_bytes || !bwd_ws_bytes) return GDN_ERR_INVALID_ARG;
+    if (!gdn::tc_path(d) || !seg_supported(d) || !gdn::compress_supported(d, rank, 0))
+        return GDN_ERR_UNSUPPORTED_SHAPE;
+    int len = 0;
+    const CLayout C = make_clayout(d, rank, seg_bytes(d, seg_resolve(d, 0, &len, true)));
+    *saved_bytes = C.saved_total;
+    *fwd_ws_bytes = C.fwd_total;
+    *bwd_ws_bytes = C.bwd_total;
+    return GDN_OK;
+}
+
+gdn_status gdn_forward_compressed(const gdn_shape* shape, int rank, int iters, const float* omega,
+                                  const void* q, const void* k, const void* v, const void* a,
+                                  const void* b, const float* A_log, const float* dt_bias,
+                                  const float* state0, const uint8_t* mask, void* o, float* state_T,
+                                  void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
+                                  void* stream) {
+    return forward_compressed_impl(shape, rank, iters, omega, q, k, v, a, b, A_log, dt_bias, state0,
+                                   mask, o, state_T, saved, saved_bytes, ws, ws_bytes, stream);
+}
+
+gdn_status gdn_backward_compressed(const gdn_shape* shape, int rank, const void* q, const void* k,
+                                   const void* v, const void* a, const void* b, const float* A_log,
+                                   const float* dt_bias, const uint8_t* mask, const void* saved,
+                                   size_t saved_bytes, const void* d_o, const float* d_state_T,
+                                   void* dq, void* dk, void* dv, void* da, void* db, float* dA_log,
+                                   float* ddt_bias, float* dstate0, void* ws, size_t ws_bytes,
+                                   void* stream) {
+    if (rank < 1) return GDN_ERR_INVALID_ARG;
+    return backward_impl(shape, 0, q, k, v, a, b, A_log, dt_bias, mask, saved, saved_bytes, d_o,
+                         d_state_T, dq, dk, dv, da, db, dA_log, ddt_bias, dstate0, ws, ws_bytes,
+                         stream, 0, rank);
 }
 
 gdn_status gdn_backward_lb(const gdn_shape* shape, const void* q, const void* k,

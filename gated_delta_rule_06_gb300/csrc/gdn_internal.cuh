@@ -224,10 +224,17 @@ cudaError_t launch_fwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s);
 //   mode 0 (the scan proper): every segment from its start state at once, writing
 //     the checkpoints, Delta images and outputs of its chunks; the last segment
 //     writes the final state.
+// A launch may also cover segment `first` alone (grid z = B) with its start
+// state read from `sin` and its end state written to `sout` ([B][Hv][Dk][Dv]
+// fp32 each, null: the rules above): the chunk-by-chunk scans of the compressed
+// forward and backward, which change the state between two chunks.
 struct ScanSeg {
     int nseg, len, mode;
     float* start;
     float* maps;
+    int first = 0;
+    const float* sin = nullptr;
+    float* sout = nullptr;
 };
 int64_t seg_map_width(const Dims& d);  // Wd
 cudaError_t launch_fwd_scan_ta_seg(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s);
@@ -238,10 +245,23 @@ cudaError_t launch_seg_chain(const Dims& d, const Ptrs& p, const ScanSeg& sg, cu
 // then every segment (mode 0); the per-chunk gradients follow as their own launch.
 cudaError_t launch_bwd_scan_ta_seg(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s);
 cudaError_t launch_bwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s);
+// segment sg.first alone (mode 0, grid z = B), forward and reverse
+cudaError_t launch_fwd_scan_ta_one(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s);
+cudaError_t launch_bwd_scan_ta_one(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s);
 unsigned int read_clear_error_scanta();
 bool fwd_chunk_tc_supported(const Dims& d);
 cudaError_t launch_fwd_chunk_tc(const Dims& d, const Ptrs& p, cudaStream_t s);
 unsigned int read_clear_error_fwdtc();
+// rank-r compressed chunk states: the truncation at boundary c of every (b, h)
+// (chunk-end states S_end in, truncated states S_tr out, factors into slot c of
+// Qf [B][Hv][NC][Dk][r] and Rf [B][Hv][NC][r][Dv], fp32), and the bf16
+// checkpoint images of every chunk start state rebuilt from them (chunk 0 from
+// S0f [B][Hv][Dk][Dv])
+bool compress_supported(const Dims& d, int rank, int iters);
+cudaError_t launch_trunc(const Dims& d, const float* S_end, const float* omega, int rank, int iters,
+                         float* S_tr, float* Qf, float* Rf, int64_t c, cudaStream_t s);
+cudaError_t launch_expand_ckpt(const Dims& d, const float* S0f, const float* Qf, const float* Rf,
+                               int rank, void* img, cudaStream_t s);
 // bf16 inputs whose shape every tensor-core kernel supports: the whole forward
 // and backward run on the tensor-core kernels with the image formats above
 bool tc_path(const Dims& d);

@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     __shared__ uint64_t bar, barW, barQ, barK, barP, barU, barR[2], barD[2];
     __shared__ uint32_t tmem_sh;
     const int tile = blockIdx.x, h = blockIdx.y;
-    const int bb = (int)(blockIdx.z % d.B), sgi = (int)(blockIdx.z / d.B);  // batch, segment
+    const int bb = (int)(blockIdx.z % d.B), sgi = sg.first + (int)(blockIdx.z / d.B);  // batch, segment
     const int j = h / (int)d.G;
     const int Dk = (int)d.Dk, Dv = (int)d.Dv;
     const int n0 = tile * DVT;
@@ -218,7 +218,8 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     // chained start states for the others; zero / the identity for the maps
     const float* sin = nullptr;
     if (!maps && sgi == 0 && p.state0) sin = p.state0 + bh * Dk * Dv + n0;
-    if (!maps && sgi > 0) sin = sg.start + ((int64_t)(sgi - 1) * d.B * d.Hv + bh) * Dk * Dv + n0;
+    if (!maps && sgi > 0 && sg.start) sin = sg.start + ((int64_t)(sgi - 1) * d.B * d.Hv + bh) * Dk * Dv + n0;
+    if (!maps && sg.sin) sin = sg.sin + bh * Dk * Dv + n0;
     bool ok = true;
     if (epi) {
         for (int cc = g * halfk; cc < (g + 1) * halfk; cc += 16) {  // initial state -> TMEM
@@ -441,6 +442,8 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     if (maps) {
         ostr = seg_wd(Dk, Dv);
         sout = sg.maps + ((int64_t)sgi * d.B * d.Hv + bh) * Dk * ostr + n0;
+    } else if (sg.sout) {
+        sout = sg.sout + bh * Dk * Dv + n0;
     } else if (sgi == sg.nseg - 1) {
         sout = p.state_T + bh * Dk * Dv + n0;
     }
@@ -462,7 +465,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
 __global__ void __launch_bounds__(kThreads + 32, 1)
     bwd_scan_ta_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm, ScanSeg sg) {
     bwd_scan_ta_body(d, p, tm, blockIdx.x, blockIdx.y, (int)(blockIdx.z % d.B), sg,
-                     (int)(blockIdx.z / d.B), &g_err_scanta, nullptr, true);
+                     sg.first + (int)(blockIdx.z / d.B), &g_err_scanta, nullptr, true);
 }
 
 }  // namespace
@@ -493,6 +496,18 @@ cudaError_t launch_fwd_scan_ta_seg(const Dims& d, const Ptrs& p, const ScanSeg& 
     const int64_t nx = sg.mode == 0 ? d.Dv / DVT : seg_wd(d.Dk, d.Dv) / DVT;
     const int64_t nz = (sg.mode == 0 ? sg.nseg : sg.nseg - 1) * d.B;
     dim3 grid((unsigned)nx, (unsigned)d.Hv, (unsigned)nz);
+    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps, sg);
+    count_launches(1);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_fwd_scan_ta_one(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s) {
+    if (sg.mode != 0) return cudaErrorInvalidValue;
+    const size_t smem = ta_plan((int)d.Dk).total + 1024;
+    auto kern = fwd_scan_ta_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);
     kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps, sg);
     count_launches(1);
     return cudaPeekAtLastError();
@@ -610,6 +625,18 @@ cudaError_t launch_bwd_scan_ta_seg(const Dims& d, const Ptrs& p, const ScanSeg& 
     const int64_t nx = sg.mode == 0 ? d.Dv / DVT : seg_wd(d.Dk, d.Dv) / DVT;
     const int64_t nz = (sg.mode == 0 ? sg.nseg : sg.nseg - 1) * d.B;
     dim3 grid((unsigned)nx, (unsigned)d.Hv, (unsigned)nz);
+    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps, sg);
+    count_launches(1);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_bwd_scan_ta_one(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s) {
+    if (sg.mode != 0) return cudaErrorInvalidValue;
+    const size_t smem = tb_plan((int)d.Dk).total + 1024;
+    auto kern = bwd_scan_ta_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);
     kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps, sg);
     count_launches(1);
     return cudaPeekAtLastError();

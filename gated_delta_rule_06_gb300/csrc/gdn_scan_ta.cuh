@@ -232,7 +232,8 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
     // top segment, the chained one below it; zero / the identity for the maps
     const float* sin = nullptr;
     if (!maps && t == 0 && p.d_state_T) sin = p.d_state_T + bh * Dk * Dv + n0;
-    if (!maps && t > 0) sin = sg.start + ((int64_t)(t - 1) * d.B * d.Hv + bh) * Dk * Dv + n0;
+    if (!maps && t > 0 && sg.start) sin = sg.start + ((int64_t)(t - 1) * d.B * d.Hv + bh) * Dk * Dv + n0;
+    if (!maps && sg.sin) sin = sg.sin + bh * Dk * Dv + n0;
     bool ok = true;
     if (epi) {
         for (int cc = g * halfk; cc < (g + 1) * halfk; cc += 16) {  // final cotangent -> TMEM
@@ -434,6 +435,8 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
     if (maps) {
         ostr = seg_wd(Dk, Dv);
         sout = sg.maps + ((int64_t)t * d.B * d.Hv + bh) * Dk * ostr + n0;
+    } else if (sg.sout) {
+        sout = sg.sout + bh * Dk * Dv + n0;
     } else if (t == sg.nseg - 1) {
         sout = p.dstate0 + bh * Dk * Dv + n0;
     }

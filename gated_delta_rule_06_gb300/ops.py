@@ -106,6 +106,12 @@ def load_library(path: str = LIB_PATH):
         lib.gdn_forward_kc.restype = i32
         lib.gdn_backward_kc.argtypes = [shp] + [vp] * 7 + [sz] + [vp] * 8 + [vp, sz, vp]
         lib.gdn_backward_kc.restype = i32
+        lib.gdn_compressed_bytes.argtypes = [shp, i32] + [ctypes.POINTER(sz)] * 3
+        lib.gdn_compressed_bytes.restype = i32
+        lib.gdn_forward_compressed.argtypes = [shp, i32, i32, vp] + [vp] * 11 + [vp, sz, vp, sz, vp]
+        lib.gdn_forward_compressed.restype = i32
+        lib.gdn_backward_compressed.argtypes = [shp, i32] + [vp] * 9 + [sz] + [vp] * 10 + [vp, sz, vp]
+        lib.gdn_backward_compressed.restype = i32
         lib.gdn_host_session_bytes.argtypes = [shp, i32, ctypes.POINTER(sz)]
         lib.gdn_host_session_bytes.restype = i32
         lib.gdn_host_session_create.argtypes = [shp, i32, i32, vp, sz, vp, ctypes.POINTER(vp)]
@@ -312,6 +318,92 @@ def backward(q, k, v, a, b, A_log, dt_bias, mask, saved, d_o, d_state_T=None, *,
         rc = lib.gdn_backward(ctypes.byref(shape), *args)
     else:
         rc = lib.gdn_backward_segmented(ctypes.byref(shape), int(segments), *args)
+    _check(rc)
+    return g
+
+
+# ---- rank-r compressed chunk states --------------------------------------------
+
+def compressed_sizes(shape, rank: int):
+    """(saved, forward workspace, backward workspace) bytes of the compressed form."""
+    n = [ctypes.c_size_t(0) for _ in range(3)]
+    _check(load_library().gdn_compressed_bytes(ctypes.byref(shape), int(rank),
+                                               *[ctypes.byref(x) for x in n]))
+    return tuple(x.value for x in n)
+
+
+def forward_compressed(q, k, v, a, b, A_log, dt_bias, state0=None, mask=None, *, omega, rank,
+                       iters=3, out=None):
+    """Run gdn_forward_compressed: the state truncated to rank `rank` by `iters`
+    power iterations from the start block omega ([Dv, rank] fp32) at every
+    chunk boundary.  Returns (o, state_T, saved); saved holds rank-r factors
+    in place of the chunk states.  ``out`` may pass dict(o=, state_T=, saved=,
+    ws=)."""
+    dt = q.dtype
+    for n, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b)):
+        _cuda(t, n, dt)
+    _cuda(A_log, "A_log", torch.float32)
+    _cuda(dt_bias, "dt_bias", torch.float32)
+    _cuda(state0, "state0", torch.float32)
+    _cuda(omega, "omega", torch.float32)
+    m = _mask_u8(mask)
+    shape = make_shape(q, v, m is not None)
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    if tuple(omega.shape) != (Dv, rank):
+        raise GdnError(f"omega must be [{Dv}, {rank}], got {tuple(omega.shape)}")
+    sv, wf, _ = compressed_sizes(shape, rank)
+    out = out or {}
+    o = out.get("o")
+    if o is None:
+        o = torch.empty((B, T, Hv, Dv), dtype=dt, device=q.device)
+    sT = out.get("state_T")
+    if sT is None:
+        sT = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=q.device)
+    saved = out.get("saved")
+    if saved is None:
+        saved = _buf(sv, q.device)
+    ws = out.get("ws")
+    if ws is None:
+        ws = _buf(wf, q.device)
+    rc = load_library().gdn_forward_compressed(
+        ctypes.byref(shape), int(rank), int(iters), _p(omega), _p(q), _p(k), _p(v), _p(a), _p(b),
+        _p(A_log), _p(dt_bias), _p(state0), _p(m), _p(o), _p(sT), _p(saved),
+        ctypes.c_size_t(saved.numel()), _p(ws), ctypes.c_size_t(ws.numel()), _stream())
+    _check(rc)
+    return o, sT, saved
+
+
+def backward_compressed(q, k, v, a, b, A_log, dt_bias, mask, saved, d_o, d_state_T=None, *, rank,
+                        out=None):
+    """Run gdn_backward_compressed on the saved buffer of forward_compressed
+    (same rank).  Returns dict(dq, dk, dv, da, db, dA_log, ddt_bias, dstate0)."""
+    dt = q.dtype
+    _cuda(d_o, "d_o", dt)
+    _cuda(d_state_T, "d_state_T", torch.float32)
+    m = _mask_u8(mask)
+    shape = make_shape(q, v, m is not None)
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    out = dict(out or {})
+    dev = q.device
+    g = {n: out.get(n) for n in ("dq", "dk", "dv", "da", "db", "dA_log", "ddt_bias", "dstate0")}
+    for n, ref in (("dq", q), ("dk", k), ("dv", v), ("da", a), ("db", b)):
+        if g[n] is None:
+            g[n] = torch.empty_like(ref)
+    for n in ("dA_log", "ddt_bias"):
+        if g[n] is None:
+            g[n] = torch.empty((Hv,), dtype=torch.float32, device=dev)
+    if g["dstate0"] is None:
+        g["dstate0"] = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=dev)
+    ws = out.get("ws")
+    if ws is None:
+        ws = _buf(compressed_sizes(shape, rank)[2], dev)
+    rc = load_library().gdn_backward_compressed(
+        ctypes.byref(shape), int(rank), _p(q), _p(k), _p(v), _p(a), _p(b), _p(A_log), _p(dt_bias),
+        _p(m), _p(saved), ctypes.c_size_t(saved.numel()), _p(d_o), _p(d_state_T), _p(g["dq"]),
+        _p(g["dk"]), _p(g["dv"]), _p(g["da"]), _p(g["db"]), _p(g["dA_log"]), _p(g["ddt_bias"]),
+        _p(g["dstate0"]), _p(ws), ctypes.c_size_t(ws.numel()), _stream())
     _check(rc)
     return g
 

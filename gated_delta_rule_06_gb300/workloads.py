@@ -189,3 +189,10 @@ def make_conv_inputs(B: int, C: int, S: int, K: int, dtype: torch.dtype = torch.
     return {"hidden": _normal(gen, (B, C, S), dtype),
             "conv_state": _normal(gen, (B, C, K), dtype),
             "weight": _normal(gen, (C, K), dtype, sigma=1.0 / math.sqrt(K))}
+
+
+def make_omega(Dv: int, rank: int, seed: int = 0) -> torch.Tensor:
+    """The start block of the compressed form's power iteration: [Dv, rank]
+    fp32, standard normal, seeded (a random draw of the method, passed in)."""
+    gen = torch.Generator().manual_seed(10_000 + seed)
+    return torch.randn((Dv, rank), generator=gen, dtype=torch.float32)

@@ -247,6 +247,53 @@ gdn_status gdn_backward_kc(const gdn_shape* shape, const void* q, const void* k,
                            void* d_log_decay, void* d_beta, float* dstate0, void* ws,
                            size_t ws_bytes, void* stream);
 
+/* ---- rank-r compressed chunk states ---------------------------------------- */
+
+/* Compression-aware training (mlx-lm page, "Post-initial-submission
+ * extensions", Extension 1: power-iteration rank-r truncation of the state at
+ * every chunk boundary; three iterations there, ranks of at most 16 per
+ * Extension 6).  Only rank-r factors of each chunk state are kept between the
+ * forward and the backward.
+ *   - Boundaries: between consecutive 64-step chunks.  The state S (Dk x Dv)
+ *     reached at the end of a chunk is replaced, before the next chunk starts,
+ *     by Q R: Y = S omega, Q = orth(Y), then `iters` times Y = S (S^T Q),
+ *     Q = orth(Y); R = Q^T S.  orth is Gram-Schmidt with one reorthogonalisation
+ *     pass; a column in the span of the earlier ones (to fp32 rounding) becomes
+ *     zero.  state0 enters chunk 0 as given and state_T, after the last chunk, is
+ *     not truncated.  Masking does not change where the truncation applies.
+ *   - omega: device fp32 [Dv][rank] row-major, the start block of the power
+ *     iteration, drawn by the caller (any fixed full-rank block; a Gaussian one is
+ *     usual).  rank: 1 .. 16; iters: 0 .. 16.
+ *   - The backward passes the state cotangent straight through each boundary:
+ *     it is the chunked VJP along the compressed trajectory (each chunk from its
+ *     truncated start state), with the truncation's derivative taken as the
+ *     identity.
+ *   - bf16 inputs whose shape runs every tensor-core kernel with 128-column
+ *     value tiles (Dk in {64, 128, 192}, Dv = 128), a and b gates (A_log,
+ *     dt_bias), else GDN_ERR_UNSUPPORTED_SHAPE.
+ *   - gdn_compressed_bytes gives the saved buffer (the other saved
+ *     intermediates, state0 in fp32 and the factors Q [B][Hv][NC][Dk][rank],
+ *     R [B][Hv][NC][rank][Dv] in fp32) and the forward and backward workspaces;
+ *     gdn_backward_compressed takes the saved buffer of gdn_forward_compressed
+ *     with the same rank.  Buffers, streams and errors are as for gdn_forward /
+ *     gdn_backward; the forward enqueues 2 NC + 1 launches and one device copy
+ *     (or memset) of state0. */
+gdn_status gdn_compressed_bytes(const gdn_shape* shape, int rank, size_t* saved_bytes,
+                                size_t* fwd_ws_bytes, size_t* bwd_ws_bytes);
+gdn_status gdn_forward_compressed(const gdn_shape* shape, int rank, int iters, const float* omega,
+                                  const void* q, const void* k, const void* v, const void* a,
+                                  const void* b, const float* A_log, const float* dt_bias,
+                                  const float* state0, const uint8_t* mask, void* o, float* state_T,
+                                  void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
+                                  void* stream);
+gdn_status gdn_backward_compressed(const gdn_shape* shape, int rank, const void* q, const void* k,
+                                   const void* v, const void* a, const void* b, const float* A_log,
+                                   const float* dt_bias, const uint8_t* mask, const void* saved,
+                                   size_t saved_bytes, const void* d_o, const float* d_state_T,
+                                   void* dq, void* dk, void* dv, void* da, void* db, float* dA_log,
+                                   float* ddt_bias, float* dstate0, void* ws, size_t ws_bytes,
+                                   void* stream);
+
 /* ---- causal conv1d update ------------------------------------------------- */
 
 /* Depthwise causal conv1d + SiLU with a K-sample carry state, the short

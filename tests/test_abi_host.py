@@ -242,3 +242,35 @@ def test_segmented_backward_rejections(lib):
     n0, n1 = ctypes.c_size_t(), ctypes.c_size_t()
     assert lib.gdn_workspace_bytes(ctypes.byref(s), 1, ctypes.byref(n1)) == 0
     assert lib.gdn_segment_bytes(ctypes.byref(s), 4, ctypes.byref(n0)) == 0 and n0.value > 0
+
+
+def test_compressed_sizes_and_rejections(lib):
+    """The compressed-state form (gdn_forward_compressed / _backward_compressed):
+    a smaller saved buffer than the plain form at the 9B layer, and shapes or
+    ranks outside its range refused."""
+    n = [ctypes.c_size_t(0) for _ in range(3)]
+    ref = [ctypes.byref(v) for v in n]
+    nine = _shape(1, 2048, 16, 64, 192, 128)
+    assert lib.gdn_compressed_bytes(ctypes.byref(nine), 16, *ref) == 0
+    plain = ctypes.c_size_t()
+    assert lib.gdn_saved_bytes(ctypes.byref(nine), ctypes.byref(plain)) == 0
+    # the bf16 checkpoint images (64 x 32 x 192 x 128 x 2 bytes) give way to the
+    # initial state and rank-16 factors of 31 boundaries (fp32)
+    assert plain.value - n[0].value == 64 * 32 * 192 * 128 * 2 - 4 * 64 * (192 * 128 + 32 * 320 * 16)
+    for rank in (0, 17):
+        assert lib.gdn_compressed_bytes(ctypes.byref(nine), rank, *ref) == 2
+    for bad in (_shape(Dk=128, Dv=128, dtype=0), _shape(Dk=128, Dv=64), _shape(Dk=96, Dv=128)):
+        assert lib.gdn_compressed_bytes(ctypes.byref(bad), 8, *ref) == 2
+    vp = ctypes.c_void_p
+    dummy = vp(256)
+    ok = _shape(Dk=128, Dv=128)
+    lib.gdn_forward_compressed.argtypes = [ctypes.POINTER(ops.GdnShape), ctypes.c_int, ctypes.c_int] + \
+        [vp] * 12 + [vp, ctypes.c_size_t, vp, ctypes.c_size_t, vp]
+    # no omega -> invalid argument; too small a saved buffer -> workspace too small
+    args = [dummy] * 5 + [dummy, dummy, None, None, dummy, dummy]
+    assert lib.gdn_forward_compressed(ctypes.byref(ok), 8, 3, None, *args, dummy, 1 << 40,
+                                      dummy, 1 << 40, None) == 1
+    assert lib.gdn_forward_compressed(ctypes.byref(ok), 8, 3, dummy, *args, dummy, 16,
+                                      dummy, 1 << 40, None) == 3
+    assert lib.gdn_forward_compressed(ctypes.byref(ok), 8, 17, dummy, *args, dummy, 1 << 40,
+                                      dummy, 1 << 40, None) == 2
