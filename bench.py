@@ -6,7 +6,8 @@ page's performance table (B=1, T=2048, Hk=16, Hv=64, Dk=192, Dv=128, bf16
 inputs, fp32 state), forward + full backward per step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--gates ab|lb] [--fused-conv K]
+                  [--workload NAME] [--gates ab|lb|kc] [--fused-conv K]
+                  [--compress-rank R [--compress-iters N]]
 
 One process per GPU (torchrun for N > 1); every rank runs its own replica
 of the workload (weak scaling, no collective on the data path).  Timing:
@@ -68,7 +69,7 @@ def _peaks():
 # algorithmic work (the method's own bytes and flops, per phase)
 # ---------------------------------------------------------------------------
 
-def method_model(w, gates="ab", nseg=1, nseg_bwd=1, conv_k=0):
+def method_model(w, gates="ab", nseg=1, nseg_bwd=1, conv_k=0, rank=0, iters=3):
     """The method's own bytes and flops, per phase and per step.
 
     Bytes count only the method's tensors: the primal inputs and outputs, the
@@ -134,6 +135,20 @@ def method_model(w, gates="ab", nseg=1, nseg_bwd=1, conv_k=0):
     io_fwd = qk + vv + ab + vv + 2 * st
     io_bwd = qk + 2 * vv + ab + st + qk + vv + ab + st
     m["_step"] = dict(bytes=io_fwd + io_bwd + 2 * ckpt, flops=f_chunk + f_scan + f_bwd)
+    if rank:
+        # compressed chunk states: the initial state and rank-r factors of the
+        # NC - 1 boundaries (fp32) take the checkpoints' place; the truncation
+        # at a boundary costs 2 Dk Dv r flops for S Omega, each of `iters`
+        # iterations two such products, then R = Q^T S
+        fac = BH * (Dk * Dv + (NC - 1) * (Dk + Dv) * rank) * 4
+        m["compress"] = dict(flops=BH * (NC - 1) * (2 * iters + 2) * 2 * Dk * Dv * rank,
+                             bytes=fac - st)
+        m["expand"] = dict(flops=BH * (NC - 1) * 2 * Dk * Dv * rank, bytes=fac)
+        m["fwd_scan"]["bytes"] -= ckpt
+        m["bwd_scan_chunk"]["bytes"] -= ckpt
+        m["bwd_chunk"]["bytes"] -= ckpt
+        m["_step"] = dict(bytes=io_fwd + io_bwd + 2 * fac,
+                          flops=m["_step"]["flops"] + m["compress"]["flops"] + m["expand"]["flops"])
     if gates == "kc":
         # per-key-channel gates: the recurrence per step, forward decay,
         # prediction, update and read-out (7 Dk Dv); backward the recompute and
@@ -420,10 +435,20 @@ def oracle_sample(w, key_heads, gates="ab", conv_k=0):
     return sub, nh / w.Hv
 
 
-def run_oracle_step(sub, backward):
+def run_oracle_step(sub, backward, rank=0, iters=3):
     import oracle
 
     t0 = time.perf_counter()
+    if rank:  # rank-r compressed chunk states
+        from oracle import compressed as oc
+
+        args = [sub[n] for n in ("q", "k", "v", "a", "b", "A_log", "dt_bias", "state0", "mask")]
+        om = wl.make_omega(sub["v"].shape[3], rank)
+        if backward:  # the backward reruns the forward for its chunk states
+            oc.backward_compressed(*args, sub["d_o"], sub["d_state_T"], om, iters)
+        else:
+            oc.forward_compressed(*args, om, iters)
+        return time.perf_counter() - t0
     if "hidden" in sub:  # the fused decode's convolution (all channels)
         oracle.causal_conv1d_update(sub["hidden"], sub["conv_state"], sub["conv_weight"])
     if "log_decay" in sub:
@@ -446,9 +471,11 @@ def run_oracle_step(sub, backward):
 ORACLE_SAMPLE_BUDGET = 1 * 2048 * 64 * 192 * 128
 
 
-def sample_key_heads(w):
+def sample_key_heads(w, rank=0):
     per_group = w.B * w.T * w.G * w.Dk * w.Dv
-    return max(1, min(w.Hk, ORACLE_SAMPLE_BUDGET // per_group))
+    # the compressed-state oracle's truncations run in numpy: a quarter of the budget
+    budget = ORACLE_SAMPLE_BUDGET // (4 if rank else 1)
+    return max(1, min(w.Hk, budget // per_group))
 
 
 def _sample_text(w, kh, frac, backward):
@@ -460,12 +487,12 @@ def _sample_text(w, kh, frac, backward):
             f"by the head fraction")
 
 
-def cpu_baseline(w, backward, reps=3, gates="ab", conv_k=0):
+def cpu_baseline(w, backward, reps=3, gates="ab", conv_k=0, rank=0, iters=3):
     import oracle
 
-    kh = sample_key_heads(w)
+    kh = sample_key_heads(w, rank)
     sub, frac = oracle_sample(w, kh, gates, conv_k)
-    times = [run_oracle_step(sub, backward) for _ in range(reps)]
+    times = [run_oracle_step(sub, backward, rank, iters) for _ in range(reps)]
     t = statistics.median(times)
     tokens = w.B * w.T
     return {"value": tokens * frac / t, "unit": "tokens/s", "cores": oracle.threads(),
@@ -480,11 +507,12 @@ def run_reference(args, w, world, rank):
 
     oracle.build()
     backward = w.backward
-    kh = sample_key_heads(w)
+    kh = sample_key_heads(w, args.compress_rank)
     sub, frac = oracle_sample(w, kh, args.gates, args.fused_conv)
     for _ in range(args.warmup):
-        run_oracle_step(sub, backward)
-    times = [run_oracle_step(sub, backward) for _ in range(args.steps)]
+        run_oracle_step(sub, backward, args.compress_rank, args.compress_iters)
+    times = [run_oracle_step(sub, backward, args.compress_rank, args.compress_iters)
+             for _ in range(args.steps)]
     t = sum(times) / len(times)
     tokens = w.B * w.T
     value = tokens * frac / t
@@ -493,7 +521,8 @@ def run_reference(args, w, world, rank):
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t * 1e3 / frac, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w, args.gates, args.fused_conv),
+        "config": config_of(w, args.gates, args.fused_conv, args.compress_rank,
+                            args.compress_iters),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(),
                          "kind": "oracle",
                          "sample": _sample_text(w, kh, frac, backward)
@@ -504,7 +533,15 @@ def run_reference(args, w, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def config_of(w, gates="ab", conv_k=0):
+def config_of(w, gates="ab", conv_k=0, rank=0, iters=3):
+    cfg = _config_of(w, gates, conv_k)
+    if rank:
+        cfg["compressed_states"] = (f"rank {rank}, {iters} power iterations at every chunk "
+                                    "boundary (gdn_forward_compressed / gdn_backward_compressed)")
+    return cfg
+
+
+def _config_of(w, gates="ab", conv_k=0):
     return {"workload": w.name, "B": w.B, "T": w.T, "Hk": w.Hk, "Hv": w.Hv, "Dk": w.Dk,
             "Dv": w.Dv, "chunk": C, "state": "fp32",
             "pass": ("fwd+bwd" if w.backward else
@@ -560,9 +597,13 @@ def run_ours(args, w, world, rank, local):
           "state_T": torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=dev)}
     if conv_k:
         fo["final_conv_state"] = torch.empty_like(xd["conv_state"])
+    cr, ci = args.compress_rank, args.compress_iters
+    omega = wl.make_omega(Dv, cr).to(dev) if cr else None
     if backward:
         if kc:
             sv, wf, wb = ops._kc_sizes(shape)
+        elif cr:
+            sv, wf, wb = ops.compressed_sizes(shape, cr)
         else:
             sv, wf, wb = ops.saved_bytes(shape), ops.workspace_bytes(shape, 0), \
                 ops.workspace_bytes(shape, 1)
@@ -592,6 +633,10 @@ def run_ours(args, w, world, rank, local):
         elif lb:
             ops.forward_lb(inp["q"], inp["k"], inp["v"], inp["log_decay"], inp["beta"],
                            inp["state0"], inp["mask"], keep_saved=keep_saved, out=fo)
+        elif cr:
+            ops.forward_compressed(inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], inp["A_log"],
+                                   inp["dt_bias"], inp["state0"], inp["mask"], omega=omega,
+                                   rank=cr, iters=ci, out=fo)
         else:
             ops.forward(inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], inp["A_log"],
                         inp["dt_bias"], inp["state0"], inp["mask"], keep_saved=keep_saved,
@@ -607,6 +652,10 @@ def run_ours(args, w, world, rank, local):
         elif lb:
             ops.backward_lb(inp["q"], inp["k"], inp["v"], inp["log_decay"], inp["beta"],
                             inp["mask"], fo["saved"], inp["d_o"], inp["d_state_T"], out=bo)
+        elif cr:
+            ops.backward_compressed(inp["q"], inp["k"], inp["v"], inp["a"], inp["b"],
+                                    inp["A_log"], inp["dt_bias"], inp["mask"], fo["saved"],
+                                    inp["d_o"], inp["d_state_T"], rank=cr, out=bo)
         else:
             ops.backward(inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], inp["A_log"],
                          inp["dt_bias"], inp["mask"], fo["saved"], inp["d_o"],
@@ -667,10 +716,12 @@ def run_ours(args, w, world, rank, local):
 
     # ---- per-phase roofline of the dominant kernel
     peaks = _peaks()
-    seg_ok = shape is not None and args.gates != "kc"
+    seg_ok = shape is not None and args.gates != "kc" and not cr
     nseg = ops.segments_auto(shape) if seg_ok else 1
     nseg_bwd = ops.segments_auto(shape, backward=True) if seg_ok and backward else 1
-    model = method_model(w, args.gates, nseg, nseg_bwd, args.fused_conv)
+    if cr:  # the compressed backward picks its own reverse-scan segment count
+        nseg_bwd = ops.segments_auto(shape, backward=True)
+    model = method_model(w, args.gates, nseg, nseg_bwd, args.fused_conv, cr, ci)
     design = design_model(w, args.fused_conv, args.gates, nseg, nseg_bwd)
     ph = {phases[i].name.decode(): (phases[i].launches, phases[i].total_ms)
           for i in range(cnt.value)}
@@ -720,7 +771,7 @@ def run_ours(args, w, world, rank, local):
     # ---- end to end through the C ABI with host buffers (pinned), copies timed
     if args.no_e2e:
         e2e = None
-    elif args.fused_conv or args.gates == "kc":  # forms the host session does not take
+    elif args.fused_conv or args.gates == "kc" or cr:  # forms the host session does not take
         e2e = run_e2e(args, w, x, xd, fo, bo if backward else None, step, world)
     else:
         e2e = run_e2e_session(args, w, x, world)
@@ -733,7 +784,7 @@ def run_ours(args, w, world, rank, local):
         "vs_baseline": (value / PAGE_TOKENS_PER_S[w.name]) if w.name in PAGE_TOKENS_PER_S else None,
         "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded, shapes and distributions of the workload)",
-        "config": config_of(w, args.gates, args.fused_conv),
+        "config": config_of(w, args.gates, args.fused_conv, cr, ci),
         "clocks": clocks,
         "gpu_launches": launches,
         "roofline": roof,
@@ -743,12 +794,22 @@ def run_ours(args, w, world, rank, local):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if cr:
+        kept = ops.compressed_sizes(shape, cr)[0]
+        plain = ops.saved_bytes(shape)
+        img = B * Hv * ((T + C - 1) // C) * Dk * Dv * 2
+        line["compressed_states"] = {
+            "rank": cr, "iters": ci, "saved_bytes": kept, "saved_bytes_uncompressed": plain,
+            "checkpoint_bytes": kept - (plain - img), "checkpoint_bytes_uncompressed": img,
+            "checkpoint_bytes_fp32_states": 2 * img,
+            "note": ("checkpoints: the initial state and rank-r factors of each boundary (fp32) "
+                     "against one bf16 image per chunk state (and against fp32 states)")}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
 
         oracle.build()
         line["cpu_baseline"] = cpu_baseline(w, backward, gates=args.gates,
-                                            conv_k=args.fused_conv)
+                                            conv_k=args.fused_conv, rank=cr, iters=ci)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -911,7 +972,16 @@ def main():
     ap.add_argument("--gates", choices=["ab", "lb", "kc"], default="ab",
                     help="gate inputs: a, b, A_log, dt_bias (default), the per-step "
                          "log_decay and beta (lb), or one log_decay per key channel (kc)")
+    ap.add_argument("--compress-rank", type=int, default=0, metavar="R",
+                    help="fwd+bwd workloads: truncate the state to rank R (1 .. 16) at every "
+                         "chunk boundary and keep rank-R factors in place of the chunk states "
+                         "(gdn_forward_compressed / gdn_backward_compressed); 0 = off")
+    ap.add_argument("--compress-iters", type=int, default=3, metavar="N",
+                    help="power iterations of the truncation (default 3)")
     args = ap.parse_args()
+    if args.compress_rank and (not wl.WORKLOADS[args.workload].backward or args.gates != "ab"
+                               or args.fused_conv or not 1 <= args.compress_rank <= 16):
+        ap.error("--compress-rank R takes 1 <= R <= 16, a fwd+bwd workload and the a / b gates")
     if args.warmup < 3:
         args.warmup = 3
     if args.fused_conv and (wl.WORKLOADS[args.workload].backward or not 1 <= args.fused_conv <= 16):
