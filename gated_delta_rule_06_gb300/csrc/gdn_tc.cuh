@@ -60,6 +60,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// try_wait with a suspend-time hint: a thread whose phase is not complete is
+// suspended until the phase completes or hint_ns pass, instead of returning at
+// once and spinning
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+constexpr uint32_t kWaitSleepNs = 10000;  // suspend-time hint of one try_wait
 // Every wait on another agent gives up after this much wall time.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
 
@@ -69,9 +84,9 @@ __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, un
                                               uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) {
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) {
             atomicOr(err, kErrWaitTimeout);
             return false;
         }
