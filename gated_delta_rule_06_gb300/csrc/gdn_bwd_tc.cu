@@ -270,11 +270,13 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
                                                unsigned int* sched, const unsigned int* progress,
                                                int ntiles) {
     extern __shared__ __align__(1024) uint8_t sm[];
-    // bar: MMA rounds outside phase 1; barM / barE: phase-1 products of block b
-    // done / block b's epilogue done (two of each, by block parity); barMa: block
-    // b's products with Sbar' done; barG: block b's tiles read by the <S, Sbar'> sums;
-    // barOV, barL, barKQ, barSa / barSb (S / Sbar' halves of a block): arrivals
-    __shared__ uint64_t bar, barOV, barL, barKQ, barSa, barSb, barMa, barG, barM[2], barE[2];
+    // bar: MMA rounds outside phase 1; barOV, barL, barKQ: arrivals of an item's
+    // operands.  Phase 1 (one of each per Dk block b, completing once per item):
+    // barMa1[b] the block's Delta Sbar'^T products done, barM2[b] its Obar S^T and
+    // -Dbar S^T products done, barG2[b] its tiles read by the <S, Sbar'> sums,
+    // barE2[b] its epilogue done (Wbar scratch free); barT[s]: arrivals of the
+    // tiles of slot s (several per item)
+    __shared__ uint64_t bar, barOV, barL, barKQ, barT[4], barMa1[4], barM2[4], barG2[4], barE2[4];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int next_item;
     const int Dk = (int)d.Dk, Dv = (int)d.Dv;
@@ -336,21 +338,29 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
     const uint32_t tk = (uint32_t)(C * Dk * 2);         // one 64 x Dk bf16 tile
     const uint32_t blk = (uint32_t)(kBlkK * Dv * 2);    // one full Dk block of S (or Sbar')
     // Dk block b of S / Sbar' (panels 8b .. 8b + nk(b) / 8 - 1 of the images of
-    // chunk image ci, one buffer in the space of the V tile, free once phase 0 is
-    // done): the S half at L.V, the Sbar' half one full block further
+    // chunk image ci) goes to one of four tile slots of a block each: slot 0 in
+    // the space of the V tile (free once phase 0 is done), slot 1 right after it
+    // (never used by phase 0), slots 2 and 3 in the space of the Delta hi / lo
+    // tiles (free once the Delta Sbar'^T products are done).  Phase 1 walks the
+    // blocks twice: first Delta Sbar'^T (Sbar' blocks in slots 1, 0, 1, ...),
+    // then Obar S^T and -Dbar S^T with the <S, Sbar'> sums (S and Sbar' of block
+    // b in slots 0 / 1 for even b, 2 / 3 for odd b), so both walks double-buffer
+    // their tiles.  Per item, slot 0 takes nblk tiles, slot 1 2 ceil(nblk / 2),
+    // slots 2 and 3 floor(nblk / 2); a wait on slot s for its occ-th tile of the
+    // item uses parity (iord * uses(s) + occ) & 1.
     const int nblk = (Dk + kBlkK - 1) / kBlkK;
     auto nkb = [&](int b) { return Dk - b * kBlkK < kBlkK ? Dk - b * kBlkK : kBlkK; };
-    auto load_s = [&](int64_t ci, int b) {
-        const uint32_t bytes = (uint32_t)(nkb(b) * Dv * 2);
-        tc::mbar_arrive_expect_tx(&barSa, bytes);
-        tc::bulk_g2s(sm + L.V, reinterpret_cast<const uint8_t*>(p.ckpt) + ci * (int64_t)Dk * Dv * 2 + (int64_t)b * blk,
-                     bytes, &barSa);
+    auto slot_ptr = [&](int sl) -> uint8_t* {
+        return sm + (sl == 0 ? L.V : sl == 1 ? L.V + blk : sl == 2 ? L.D : L.Dlo);
     };
-    auto load_sp = [&](int64_t ci, int b) {
+    auto slot_uses = [&](int sl) -> uint32_t {
+        return sl == 0 ? (uint32_t)nblk : sl == 1 ? 2u * (uint32_t)((nblk + 1) / 2) : (uint32_t)(nblk / 2);
+    };
+    auto load_tile = [&](const void* img, int64_t ci, int b, int sl) {
         const uint32_t bytes = (uint32_t)(nkb(b) * Dv * 2);
-        tc::mbar_arrive_expect_tx(&barSb, bytes);
-        tc::bulk_g2s(sm + L.V + blk, reinterpret_cast<const uint8_t*>(p.dSck) + ci * (int64_t)Dk * Dv * 2 + (int64_t)b * blk,
-                     bytes, &barSb);
+        tc::mbar_arrive_expect_tx(&barT[sl], bytes);
+        tc::bulk_g2s(slot_ptr(sl), static_cast<const uint8_t*>(img) + ci * (int64_t)Dk * Dv * 2 + (int64_t)b * blk,
+                     bytes, &barT[sl]);
     };
     // ---- operands of item it, all issued by the producer, in two groups.  Phase 0:
     // raw dO, v by TMA in the panel layout, Delta (hi + lo), -Dbar and T by bulk
@@ -380,7 +390,7 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
         tc::mbar_arrive_expect_tx(&barKQ, 2 * tk);
         tc::bulk_g2s(sm + L.K, static_cast<const uint8_t*>(p.kimg) + kqi * tk, tk, &barKQ);
         tc::bulk_g2s(sm + L.Q, static_cast<const uint8_t*>(p.qimg) + kqi * tk, tk, &barKQ);
-        load_sp(ci, 0);
+        load_tile(p.dSck, ci, 0, 1);
     };
     if (warp == 0) {
         tc::tmem_alloc(&tmem_base_sh, 512);
@@ -391,13 +401,12 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
         tc::mbar_init(&barOV, 1);
         tc::mbar_init(&barL, 1);
         tc::mbar_init(&barKQ, 1);
-        tc::mbar_init(&barSa, 1);
-        tc::mbar_init(&barSb, 1);
-        tc::mbar_init(&barMa, 1);
-        tc::mbar_init(&barG, kThreads);
-        for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&barM[i], 1);
-            tc::mbar_init(&barE[i], kThreads);
+        for (int i = 0; i < 4; ++i) {
+            tc::mbar_init(&barT[i], 1);
+            tc::mbar_init(&barMa1[i], 1);
+            tc::mbar_init(&barM2[i], 1);
+            tc::mbar_init(&barG2[i], kThreads);
+            tc::mbar_init(&barE2[i], kThreads);
         }
         tc::fence_mbar_init();
         const int first = (int)atomicAdd(sched, 1u);
@@ -409,12 +418,12 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
     const uint32_t tb = tmem_base_sh;
     uint32_t phase = 0;        // parity of the next completion of bar (MMA rounds)
     uint32_t pit = 0;          // parity of the per-item arrivals (barOV, barL, barKQ)
-    uint32_t B0 = 0;           // Dk blocks of the earlier items (parities of the block barriers)
+    uint32_t iord = 0;         // items this CTA has run before (parities of the phase-1 barriers)
     bool ok = true;
     // producer: an item whose operands are in flight but not yet waited for
     bool pending = false;
     uint32_t pend_pit = 0;
-    for (int it = next_item; it < nitems; it = next_item, pit ^= 1u, B0 += (uint32_t)nblk) {
+    for (int it = next_item; it < nitems; it = next_item, pit ^= 1u, ++iord) {
     pending = false;
     const int c = item_c(it), h = item_h(it), bb = item_b(it);
     const int j = h / (int)d.G;
@@ -511,100 +520,141 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
     }
     cta_sync_tc();  // phase-0 reads of TMEM and of the V tile are done
 
-    // ---- phase 1: state products per kBlkK-wide block of Dk through one buffer
-    // of two halves, S and Sbar'.  The producer issues block b's products with
-    // Sbar' (Delta Sbar'^T) as soon as its half has landed, then those with S
-    // (Obar S^T, -Dbar S^T) once the S half has landed and the epilogue of block
-    // b - 2 has released its Wbar scratch (S1 for even, S2 for odd blocks); each
-    // half of block b + 1 loads as soon as the products (and the <S, Sbar'> sums)
-    // that read it are done, so the loads overlap the other half's products and
-    // the epilogues.  The first Sbar' half arrives with the phase-0 operands.
-    // Obar S^T and Delta Sbar'^T land in the dq / dk accumulators, rescaled there
-    // by gam and e.
+    // ---- phase 1: state products per kBlkK-wide block of Dk, in two walks over
+    // the blocks (slots: see load_tile above).  Walk 1: Delta Sbar'^T (hi + lo)
+    // into the dk accumulator, each Sbar' block loading while the previous
+    // block's products run; the epilogue rescales dk by e and forms <dk, k> per
+    // row.  Walk 2, once every walk-1 product is done (all four slots free):
+    // Obar S^T into the dq accumulator and -Dbar S^T into the Wbar scratch (S1 for
+    // even, S2 for odd blocks, reused once the epilogue of block b - 2 released
+    // it), the S / Sbar' pair of block b + 2 loading once block b's products and
+    // its <S, Sbar'> sums are done; the epilogue rescales dq by gam, forms
+    // <dq, q> per row and stages Wbar as a bf16 tile.  The first Sbar' block
+    // arrives with the phase-0 operands.
     float gcb = 0.f;
+    const uint32_t ip = iord & 1u;  // parity of the per-block barriers in this item
+    auto slot_par = [&](int sl, int occ) { return (iord * slot_uses(sl) + (uint32_t)occ) & 1u; };
     if (prod) {
-        load_s(ci, 0);
-        for (int b = 0; b < nblk; ++b) {
-            const int dk0 = b * kBlkK, nk = nkb(b);
-            const uint32_t B = B0 + (uint32_t)b, par = B & 1u;
-            const tc::Tile tS = tc::panel_tile(sm + L.V, Dv, false);
-            const tc::Tile tSp = tc::panel_tile(sm + L.V + blk, Dv, false);
-            const uint32_t wcol = (b & 1) ? kS2 : kS1;
-            ok = tc::mbar_wait(&barSb, par, &g_err_bwdtc) && ok;
+        if (nblk >= 2) load_tile(p.dSck, ci, 1, 0);  // the V tile is dead: phase 0 is done
+        for (int b = 0; b < nblk; ++b) {  // walk 1
+            const int dk0 = b * kBlkK, nk = nkb(b), sl = (b & 1) ? 0 : 1;
+            ok = tc::mbar_wait(&barT[sl], slot_par(sl, b >> 1), &g_err_bwdtc) && ok;
+            const tc::Tile tSp = tc::panel_tile(slot_ptr(sl), Dv, false);
             tc::mma_tile(tb + kAK + dk0, tDmn, tSp, C, nk, Dv, false);
             tc::mma_tile(tb + kAK + dk0, tDlomn, tSp, C, nk, Dv, true);
-            tc::mma_commit(&barMa);
-            ok = tc::mbar_wait(&barSa, par, &g_err_bwdtc) && ok;
-            if (b >= 2) ok = tc::mbar_wait(&barE[B & 1], ((B - 2) >> 1) & 1u, &g_err_bwdtc) && ok;
+            tc::mma_commit(&barMa1[b]);
+            if (b + 2 < nblk) {
+                ok = tc::mbar_wait(&barMa1[b], ip, &g_err_bwdtc) && ok;
+                load_tile(p.dSck, ci, b + 2, sl);
+            }
+        }
+        ok = tc::mbar_wait(&barMa1[nblk - 1], ip, &g_err_bwdtc) && ok;  // every walk-1 product done
+        load_tile(p.ckpt, ci, 0, 0);
+        load_tile(p.dSck, ci, 0, 1);
+        if (nblk >= 2) {
+            load_tile(p.ckpt, ci, 1, 2);
+            load_tile(p.dSck, ci, 1, 3);
+        }
+        for (int b = 0; b < nblk; ++b) {  // walk 2
+            const int dk0 = b * kBlkK, nk = nkb(b);
+            const int sS = (b & 1) ? 2 : 0, sP = sS + 1;
+            const int occS = (b & 1) ? (b >> 1) : (nblk / 2 + (b >> 1));
+            ok = tc::mbar_wait(&barT[sS], slot_par(sS, occS), &g_err_bwdtc) && ok;
+            if (b >= 2) ok = tc::mbar_wait(&barE2[b - 2], ip, &g_err_bwdtc) && ok;
+            const uint32_t wcol = (b & 1) ? kS2 : kS1;
+            const tc::Tile tS = tc::panel_tile(slot_ptr(sS), Dv, false);
             tc::mma_tile(tb + kAQ + dk0, tO, tS, C, nk, Dv, false);
             tc::mma_tile(tb + wcol, tNBmn, tS, C, nk, Dv, false);
-            tc::mma_commit(&barM[B & 1]);
-            if (b + 1 < nblk) {
-                ok = tc::mbar_wait(&barMa, par, &g_err_bwdtc) && ok;
-                ok = tc::mbar_wait(&barG, par, &g_err_bwdtc) && ok;
-                load_sp(ci, b + 1);
-                ok = tc::mbar_wait(&barM[B & 1], (B >> 1) & 1u, &g_err_bwdtc) && ok;
-                load_s(ci, b + 1);
+            tc::mma_commit(&barM2[b]);
+            if (b + 2 < nblk) {
+                ok = tc::mbar_wait(&barM2[b], ip, &g_err_bwdtc) && ok;
+                ok = tc::mbar_wait(&barG2[b], ip, &g_err_bwdtc) && ok;
+                load_tile(p.ckpt, ci, b + 2, sS);
+                load_tile(p.dSck, ci, b + 2, sP);
             }
         }
     } else if (epi) {
         ok = tc::mbar_wait(&barKQ, pit, &g_err_bwdtc) && ok;
         const int sp = warp & 3;
-        for (int b = 0; b < nblk; ++b) {
+        // warp columns g nk / 2 .. + nk / 2 of a block in one or two 16-column pieces
+        for (int b = 0; b < nblk; ++b) {  // walk 1: dk *= e, <dk, k> per row
             const int dk0 = b * kBlkK, nk = nkb(b);
-            const uint32_t B = B0 + (uint32_t)b;
-            ok = tc::mbar_wait(&barSa, B & 1u, &g_err_bwdtc) && ok;
-            ok = tc::mbar_wait(&barSb, B & 1u, &g_err_bwdtc) && ok;
-            const uint8_t* sS = sm + L.V;
-            const int bytes = nk * Dv * 2;
-            for (int e = tid; e < bytes / 16; e += kThreads) {
-                float a8[8], b8[8];
-                ld_bf16x8(sS + 16 * e, a8);
-                ld_bf16x8(sS + blk + 16 * e, b8);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) gcb = fmaf(a8[i], b8[i], gcb);
-            }
-            tc::mbar_arrive(&barG);
-            ok = tc::mbar_wait(&barM[B & 1], (B >> 1) & 1u, &g_err_bwdtc) && ok;
+            ok = tc::mbar_wait(&barMa1[b], ip, &g_err_bwdtc) && ok;
             tc::tc_fence_after();
             if (ok) {
-                // warp columns g nk / 2 .. + nk / 2 in one or two 16-column pieces; the
-                // three accumulators of a piece in one batch of TMEM loads
                 const int half = nk / 2, np = half / 16;
-                const uint32_t wcol = (b & 1) ? kS2 : kS1;
                 for (int u = 0; u < np; ++u) {
                     const int cc = g * half + 16 * u;
-                    float aq[16], wv[16], ak[16];
-                    tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, kAQ + dk0 + cc), aq);
-                    tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, wcol + cc), wv);
+                    float ak[16];
                     tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, kAK + dk0 + cc), ak);
                     tc::tmem_wait_ld();
                     if (lane < 16) {
                         const int r = 16 * sp + lane;
-                        float qq[16], kk[16];
-                        panel_row16(sm + L.Q, dk0 + cc, r, qq);
+                        float kk[16];
                         panel_row16(sm + L.K, dk0 + cc, r, kk);
-                        float sq = 0.f, sk = 0.f;
+                        float sk = 0.f;
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            aq[i] *= gm[r];
-                            sq = fmaf(aq[i], qq[i], sq);
                             ak[i] *= ev[r];
                             sk = fmaf(ak[i], kk[i], sk);
                         }
-                        gq[g * C + r] += sq;
                         ee[g * C + r] += sk;
-                        tile_put16(sm + L.W, Dk, dk0 + cc, r, wv);
                     }
                     // rescaled values back in place (lanes 16..31 write TMEM lanes
                     // that an M = 64 accumulator does not use)
-                    tc::tmem_st16(tc::tmem_addr(tb, 32 * sp, kAQ + dk0 + cc), aq);
                     tc::tmem_st16(tc::tmem_addr(tb, 32 * sp, kAK + dk0 + cc), ak);
                 }
                 tc::tmem_wait_st();
             }
+        }
+        for (int b = 0; b < nblk; ++b) {  // walk 2: <S, Sbar'>, dq *= gam, <dq, q>, Wbar tile
+            const int dk0 = b * kBlkK, nk = nkb(b);
+            const int sS = (b & 1) ? 2 : 0, sP = sS + 1;
+            const int occS = (b & 1) ? (b >> 1) : (nblk / 2 + (b >> 1));
+            const int occP = (b & 1) ? (b >> 1) : ((nblk + 1) / 2 + (b >> 1));
+            ok = tc::mbar_wait(&barT[sS], slot_par(sS, occS), &g_err_bwdtc) && ok;
+            ok = tc::mbar_wait(&barT[sP], slot_par(sP, occP), &g_err_bwdtc) && ok;
+            const uint8_t* tSs = slot_ptr(sS);
+            const uint8_t* tSps = slot_ptr(sP);
+            const int bytes = nk * Dv * 2;
+            for (int e = tid; e < bytes / 16; e += kThreads) {
+                float a8[8], b8[8];
+                ld_bf16x8(tSs + 16 * e, a8);
+                ld_bf16x8(tSps + 16 * e, b8);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) gcb = fmaf(a8[i], b8[i], gcb);
+            }
+            tc::mbar_arrive(&barG2[b]);
+            ok = tc::mbar_wait(&barM2[b], ip, &g_err_bwdtc) && ok;
+            tc::tc_fence_after();
+            if (ok) {
+                const int half = nk / 2, np = half / 16;
+                const uint32_t wcol = (b & 1) ? kS2 : kS1;
+                for (int u = 0; u < np; ++u) {
+                    const int cc = g * half + 16 * u;
+                    float aq[16], wv[16];
+                    tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, kAQ + dk0 + cc), aq);
+                    tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, wcol + cc), wv);
+                    tc::tmem_wait_ld();
+                    if (lane < 16) {
+                        const int r = 16 * sp + lane;
+                        float qq[16];
+                        panel_row16(sm + L.Q, dk0 + cc, r, qq);
+                        float sq = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            aq[i] *= gm[r];
+                            sq = fmaf(aq[i], qq[i], sq);
+                        }
+                        gq[g * C + r] += sq;
+                        tile_put16(sm + L.W, Dk, dk0 + cc, r, wv);
+                    }
+                    tc::tmem_st16(tc::tmem_addr(tb, 32 * sp, kAQ + dk0 + cc), aq);
+                }
+                tc::tmem_wait_st();
+            }
             tc::tc_fence_before();
-            tc::mbar_arrive(&barE[B & 1]);
+            tc::mbar_arrive(&barE2[b]);
         }
         // <S, Sbar'> of this CTA: warp sums by a fixed shuffle tree, then in warp order
 #pragma unroll
