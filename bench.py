@@ -150,18 +150,31 @@ def method_model(w, gates="ab", nseg=1, nseg_bwd=1, conv_k=0, rank=0, iters=3):
         m["_step"] = dict(bytes=io_fwd + io_bwd + 2 * fac,
                           flops=m["_step"]["flops"] + m["compress"]["flops"] + m["expand"]["flops"])
     if gates == "kc":
-        # per-key-channel gates: the recurrence per step, forward decay,
-        # prediction, update and read-out (7 Dk Dv); backward the recompute and
-        # the reverse step (20 Dk Dv).  Gate inputs log_decay [B, T, Hv, Dk] and
-        # beta; checkpoints per 64-step chunk as for the scalar gates.
+        # per-key-channel gates.  Gate inputs log_decay [B, T, Hv, Dk] and beta;
+        # checkpoints per 64-step chunk as for the scalar gates.  The chunked
+        # form (bf16 at the tensor-core scans' shapes): the scalar form's flops
+        # with no Gram shared between value heads (each has its own decays);
+        # the gradient phase split into its Dv-long products (the three state
+        # products, Pbar, Dbar V^T, T^T Dbar: 6 Dk Dv + 6 C Dv) and the rest.
+        # The recurrent form (other shapes): per step forward decay, prediction,
+        # update and read-out (7 Dk Dv), backward the recompute and the reverse
+        # step (20 Dk Dv).
         gin = B * T * Hv * (Dk + 1) * es
+        fk_chunk = th * (2 * C * (3 * Dk + 2 * Dv) + C * C / 3)
+        fk_bwd = th * (18 * C * Dk + 10 * C * Dv + 14 * Dk * Dv + 4 * C * C)
+        fk_prod = th * (6 * Dk * Dv + 6 * C * Dv)
         m["prep"] = dict(flops=0.0, bytes=qk)
+        m["kc_chunk"] = dict(flops=fk_chunk, bytes=qk + vv + gin)
+        m["kc_scan"] = dict(flops=f_scan, bytes=st + vv + st + ckpt)
+        m["kc_bwd_scan"] = dict(flops=f_bscan, bytes=vv + st + st)
+        m["kc_bwd_prod"] = dict(flops=fk_prod, bytes=ckpt + 3 * vv)
+        m["kc_bwd_local"] = dict(flops=fk_bwd - f_bscan - fk_prod, bytes=qk + 2 * gin)
         m["kc_fwd"] = dict(flops=7.0 * th * Dk * Dv, bytes=qk + vv + gin + vv + 2 * st + ckpt)
         m["kc_bwd"] = dict(flops=20.0 * th * Dk * Dv,
                            bytes=qk + 2 * vv + gin + st + ckpt + vv + gin + st)
         m["bwd_reduce"] = dict(flops=0.0, bytes=2 * qk)
         m["_step"] = dict(bytes=(qk + 2 * vv + gin + 2 * st) + (2 * qk + 3 * vv + 2 * gin + 2 * st)
-                          + 2 * ckpt, flops=27.0 * th * Dk * Dv)
+                          + 2 * ckpt, flops=fk_chunk + f_scan + fk_bwd)
     return m
 
 
@@ -264,27 +277,50 @@ def design_model(w, conv_k=0, gates="ab", nseg=1, nseg_bwd=1):
                       flops=sum(m[k]["flops"] for k in ("fwd_chunk", "fwd_scan", "bwd_scan",
                                                         "bwd_chunk")))
     if gates == "kc":
-        # per-key-channel gates: the CUDA-core recurrence.  Per (b, t, h): forward
-        # decay, prediction, update and read-out, 7 Dk Dv flops; backward: the
-        # segment recompute (5 Dk Dv) and the reverse step (~15 Dk Dv).  Bytes:
-        # fp32 states every 8 steps written and read back, and the per-16-column
-        # tile partials of the q / k / log-decay cotangents (fp32).
-        nt, NS = Dv // 16, (T + 7) // 8
-        tok = B * T * Hv
         gin = B * T * Hv * (Dk + 1) * es  # log_decay [.., Dk] and beta
         io_in = 2 * B * T * Hk * Dk * es + B * T * Hv * Dv * es + gin
+        tok = B * T * Hv
+        m["prep"] = dict(flops=0.0, bytes=2 * B * T * Hk * Dk * es + 2 * BHk * Tp * 4)
+        # chunked form: per (b, h, chunk) the Q_r, K_d and W images, P and T
+        # images, U (fp32), e_C and the decayed Gram (fp32) out of the chunk
+        # kernel; the scans read them as the scalar scans do; the tensor-core
+        # gradient pass writes Kbar_d, Qbar_r, Wbar (fp32 rows), Pbar and M1
+        # (fp32), which the CUDA-core pass reads with q, k, the gates, T and G
+        # and turns into fp32 per-value-head q / k cotangents
+        m["kc_chunk"] = dict(
+            flops=units * (6 * C * C * Dk + 2 * C * C * Dv + C ** 3 / 3),
+            bytes=io_in + units * (3 * C * Dk * es + 2 * C * C * es + C * Dv * 4 + Dk * 4 + C * C * 4))
+        m["kc_scan"] = dict(
+            flops=units * (6 * C * Dk * Dv + 2 * C * C * Dv),
+            bytes=units * (3 * C * Dk * es + C * C * es + C * Dv * 4 + Dk * 4 + Dk * Dv * img
+                           + C * Dv * 4 + C * Dv * es) + 2 * BH * Dk * Dv * 4)
+        m["kc_bwd_scan"] = dict(
+            flops=units * (6 * C * Dk * Dv + 2 * C * C * Dv),
+            bytes=units * (C * Dv * es + C * C * es + 3 * C * Dk * es + Dk * 4 + Dk * Dv * img
+                           + C * Dv * img) + 2 * BH * Dk * Dv * 4)
+        m["kc_bwd_prod"] = dict(
+            flops=units * (6 * C * Dk * Dv + 6 * C * C * Dv),
+            bytes=units * (2 * C * Dv * es + C * Dv * 4 + C * Dv * img + C * C * img + 2 * Dk * Dv * img
+                           + 2 * C * C * 4 + C * Dv * es + 3 * C * Dk * 4 + Dk * 4))
+        m["kc_bwd_local"] = dict(
+            flops=units * (8 * C * C * Dk + 2 * C * C * Dk + 4 * C ** 3),
+            bytes=io_in - B * T * Hv * Dv * es + units * (C * C * img + 3 * C * C * 4 + 4 * C * Dk * 4
+                                                          + Dk * 4 + 2 * C * Dk * 4) + gin)
+        # recurrent form: fp32 states every 8 steps written and read back, and
+        # the per-16-column tile partials of the q / k / log-decay cotangents
+        nt, NS = Dv // 16, (T + 7) // 8
         ck = BH * NS * Dk * Dv * 4
         part = BH * nt * Tp * (3 * Dk + 1) * 4
-        m["prep"] = dict(flops=0.0, bytes=2 * B * T * Hk * Dk * es + 2 * BHk * Tp * 4)
         m["kc_fwd"] = dict(flops=7.0 * tok * Dk * Dv,
                            bytes=io_in + B * T * Hv * Dv * es + 2 * BH * Dk * Dv * 4 + ck)
         m["kc_bwd"] = dict(flops=20.0 * tok * Dk * Dv,
                            bytes=io_in + 2 * B * T * Hv * Dv * es + ck + part
                            + BH * nt * Tp * (Dk + 1) * 4 + gin + 2 * BH * Dk * Dv * 4)
-        m["bwd_reduce"] = dict(flops=0.0, bytes=2 * BH * nt * Tp * Dk * 4 + 4 * B * T * Hk * Dk * es)
-        m["_step"] = dict(bytes=2 * io_in + 2 * B * T * Hv * Dv * es + gin + 2 * ck
+        m["bwd_reduce"] = dict(flops=0.0, bytes=2 * BH * Tp * Dk * 4 + 4 * B * T * Hk * Dk * es)
+        m["_step"] = dict(bytes=2 * io_in + 2 * B * T * Hv * Dv * es + gin + 2 * units * Dk * Dv * img
                           + 4 * B * T * Hk * Dk * es + 4 * BH * Dk * Dv * 4,
-                          flops=m["kc_fwd"]["flops"] + m["kc_bwd"]["flops"])
+                          flops=sum(m[k]["flops"] for k in ("kc_chunk", "kc_scan", "kc_bwd_scan",
+                                                            "kc_bwd_prod", "kc_bwd_local")))
     return m
 
 
@@ -549,7 +585,8 @@ def _config_of(w, gates="ab", conv_k=0):
                      else "fwd (decode step)"),
             "gates": ("log_decay, beta (gdn_forward_lb / gdn_backward_lb)" if gates == "lb"
                       else "per-key-channel log_decay [B, T, Hv, Dk], beta (gdn_forward_kc / "
-                      "gdn_backward_kc, CUDA-core recurrence)" if gates == "kc"
+                      "gdn_backward_kc: the chunked form at bf16, Dk 64 / 128 / 192, Dv 128, "
+                      "else the CUDA-core recurrence)" if gates == "kc"
                       else "a, b, A_log, dt_bias"),
             "l2": "flushed between timed steps (256 MiB write outside the events)",
             "phase_times": "a second pass over the same steps with per-phase CUDA events "
@@ -736,7 +773,8 @@ def run_ours(args, w, world, rank, local):
     # bf16 workloads run the chunk contractions on the tensor cores (tcgen05);
     # fp32 workloads run them as FFMA on the CUDA cores
     tensor = w.dtype == torch.bfloat16 and dom in ("fwd_chunk", "fwd_scan", "bwd_scan", "bwd_chunk",
-                                                  "bwd_scan_chunk", "fwd_seg_maps", "bwd_seg_maps")
+                                                  "bwd_scan_chunk", "fwd_seg_maps", "bwd_seg_maps",
+                                                  "kc_scan", "kc_bwd_scan", "kc_bwd_prod")
     cpeak = peaks["bf16_tflops"] if tensor else FP32_ALU_PEAK_TFLOPS
     t_cmp = fl / (cpeak * 1e12)
     traffic = measured_traffic(w.name, dom)

@@ -282,7 +282,8 @@ void count_launches(int n) { g_launches.fetch_add((uint64_t)n); }
 unsigned int read_clear_error_all() {
     const unsigned int words[] = {read_clear_error_selftest(), read_clear_error_bwdtc(),
                                   read_clear_error_scantc(), read_clear_error_fwdtc(),
-                                  read_clear_error_scanta(), read_clear_error_decode()};
+                                  read_clear_error_scanta(), read_clear_error_decode(),
+                                  read_clear_error_kctc()};
     unsigned int v = 0;
     for (unsigned int w : words) {
         if (w == ~0u) return ~0u;
@@ -791,12 +792,62 @@ gdn_status gdn_backward_lb(const gdn_shape* shape, const void* q, const void* k,
 
 /* ---- per-key-channel gates ---------------------------------------------------- */
 namespace {
+// Two forms.  The chunked form (bf16, shapes of the tensor-core scans, Dv = 128)
+// keeps per-chunk images like the scalar tensor-core path; the recurrent form
+// (everything else) keeps the state at every 8th step.
 struct KcLayout {
-    size_t ckpt, rq, rk, dqh, dkh, gpart, bpart, saved_total, fwd_total, bwd_total;
+    bool chunked;
+    // recurrent form
+    size_t ckpt, rq, rk, dqh, dkh, gpart, bpart;
+    // chunked form, saved: checkpoints, Delta, W, P, T, Q_r, K_d images, e_C, the
+    // decayed k Gram (and rq, rk above); forward workspace: U, then room for the
+    // saved tensors when the caller keeps none; backward workspace: the reverse
+    // scan's images, the q / k partials, the tensor-core pass's products
+    size_t Delta, W, P, Tinv, qimg, kimg, ecd, gram, U, fwd_saved;
+    size_t dSck, Dbar, kdb, qrb, wb, pbm, m1, ecb;
+    size_t saved_total, fwd_total, bwd_total;
 };
 gdn_status kc_layout(const gdn_shape* shape, gdn::Dims* d, KcLayout* L) {
     gdn_status st = validate_shape(shape, d);
     if (st != GDN_OK) return st;
+    *L = KcLayout{};
+    if (gdn::kc_chunked_supported(*d)) {
+        L->chunked = true;
+        const size_t BH = (size_t)d->B * d->Hv, C = gdn::kChunk;
+        const size_t img = BH * d->NC * d->Dk * d->Dv * 2;
+        const size_t rowsk = BH * d->Tp * d->Dk, rowsv = BH * d->Tp * d->Dv;
+        const size_t mat = BH * d->NC * C * C;
+        size_t o = 0;
+        L->ckpt = o; o = align_up(o + img);
+        L->Delta = o; o = align_up(o + rowsv * 4);
+        L->W = o; o = align_up(o + rowsk * 2);
+        L->P = o; o = align_up(o + mat * 2);
+        L->Tinv = o; o = align_up(o + mat * 2);
+        L->qimg = o; o = align_up(o + rowsk * 2);
+        L->kimg = o; o = align_up(o + rowsk * 2);
+        L->ecd = o; o = align_up(o + BH * d->NC * d->Dk * 4);
+        L->gram = o; o = align_up(o + mat * 4);
+        L->rq = o; o = align_up(o + (size_t)d->B * d->Hk * d->Tp * 4);
+        L->rk = o; o = align_up(o + (size_t)d->B * d->Hk * d->Tp * 4);
+        L->saved_total = o;
+        o = 0;
+        L->U = o; o = align_up(o + rowsv * 4);
+        L->fwd_saved = o; o = align_up(o + L->saved_total);
+        L->fwd_total = o;
+        o = 0;
+        L->dSck = o; o = align_up(o + img);
+        L->Dbar = o; o = align_up(o + rowsv * 2);
+        L->dqh = o; o = align_up(o + rowsk * 4);
+        L->dkh = o; o = align_up(o + rowsk * 4);
+        L->kdb = o; o = align_up(o + rowsk * 4);
+        L->qrb = o; o = align_up(o + rowsk * 4);
+        L->wb = o; o = align_up(o + rowsk * 4);
+        L->pbm = o; o = align_up(o + mat * 4);
+        L->m1 = o; o = align_up(o + mat * 4);
+        L->ecb = o; o = align_up(o + BH * d->NC * d->Dk * 4);
+        L->bwd_total = o;
+        return GDN_OK;
+    }
     if (!gdn::kc_supported(*d)) return GDN_ERR_UNSUPPORTED_SHAPE;
     const size_t nt = (size_t)gdn::kc_tiles(*d);
     const size_t rows = (size_t)d->B * d->Hv * nt * d->Tp;  // per-tile partial rows
@@ -812,6 +863,21 @@ gdn_status kc_layout(const gdn_shape* shape, gdn::Dims* d, KcLayout* L) {
     L->bpart = o; o = align_up(o + rows * 4);
     L->bwd_total = o;
     return GDN_OK;
+}
+
+void carve_kc_saved(const KcLayout& L, void* saved, gdn::Ptrs* p) {
+    char* s = static_cast<char*>(saved);
+    p->ckpt = reinterpret_cast<float*>(s + L.ckpt);
+    p->Delta = reinterpret_cast<float*>(s + L.Delta);
+    p->W = s + L.W;
+    p->P = s + L.P;
+    p->Tinv = reinterpret_cast<float*>(s + L.Tinv);
+    p->qimg = s + L.qimg;
+    p->kimg = s + L.kimg;
+    p->ecd = reinterpret_cast<float*>(s + L.ecd);
+    p->gram = reinterpret_cast<float*>(s + L.gram);
+    p->rq = reinterpret_cast<float*>(s + L.rq);
+    p->rk = reinterpret_cast<float*>(s + L.rk);
 }
 }  // namespace
 
@@ -852,12 +918,24 @@ gdn_status gdn_forward_kc(const gdn_shape* shape, const void* q, const void* k, 
         return GDN_ERR_WORKSPACE_TOO_SMALL;
     gdn::Ptrs p{};
     p.q = q; p.k = k; p.v = v; p.state0 = state0;
+    p.a = log_decay; p.b = beta;
     p.mask = shape->has_mask ? mask : nullptr;
     p.o = o; p.state_T = state_T;
     char* w = static_cast<char*>(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (L.chunked) {
+        carve_kc_saved(L, saved ? saved : w + L.fwd_saved, &p);
+        p.U = reinterpret_cast<float*>(w + L.U);
+        gdn::Tmaps maps;
+        if (!make_tmaps(d, v, nullptr, o, p.U, &maps)) return tmap_error();
+        p.tmaps = &maps;
+        cudaError_t e = run_phase("prep", s, [&] { return gdn::launch_prep_norms(d, p, s); });
+        if (e == cudaSuccess) e = run_phase("kc_chunk", s, [&] { return gdn::launch_kc_chunk(d, p, s); });
+        if (e == cudaSuccess) e = run_phase("kc_scan", s, [&] { return gdn::launch_fwd_scan_kc(d, p, s); });
+        return cuda_status(e);
+    }
     p.rq = reinterpret_cast<float*>(w + L.rq);
     p.rk = reinterpret_cast<float*>(w + L.rk);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = run_phase("prep", s, [&] { return gdn::launch_prep_norms(d, p, s); });
     if (e == cudaSuccess)
         e = run_phase("kc_fwd", s, [&] {
@@ -887,15 +965,36 @@ gdn_status gdn_backward_kc(const gdn_shape* shape, const void* q, const void* k,
     if (saved_bytes < L.saved_total || ws_bytes < L.bwd_total) return GDN_ERR_WORKSPACE_TOO_SMALL;
     gdn::Ptrs p{};
     p.q = q; p.k = k; p.v = v;
+    p.a = log_decay; p.b = beta;
     p.mask = shape->has_mask ? mask : nullptr;
     p.d_o = d_o; p.d_state_T = d_state_T;
     p.dq = dq; p.dk = dk; p.dv = dv; p.dstate0 = dstate0;
+    p.da = d_log_decay; p.db = d_beta;
     char* w = static_cast<char*>(ws);
-    p.rq = reinterpret_cast<float*>(w + L.rq);
-    p.rk = reinterpret_cast<float*>(w + L.rk);
     p.dqh = reinterpret_cast<float*>(w + L.dqh);
     p.dkh = reinterpret_cast<float*>(w + L.dkh);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (L.chunked) {
+        carve_kc_saved(L, const_cast<void*>(saved), &p);
+        p.dSck = reinterpret_cast<float*>(w + L.dSck);
+        p.Dbar = reinterpret_cast<float*>(w + L.Dbar);
+        p.kdb = reinterpret_cast<float*>(w + L.kdb);
+        p.qrb = reinterpret_cast<float*>(w + L.qrb);
+        p.wb = reinterpret_cast<float*>(w + L.wb);
+        p.pbm = reinterpret_cast<float*>(w + L.pbm);
+        p.m1 = reinterpret_cast<float*>(w + L.m1);
+        p.ecb = reinterpret_cast<float*>(w + L.ecb);
+        gdn::Tmaps maps;
+        if (!make_tmaps(d, v, d_o, nullptr, nullptr, &maps)) return tmap_error();
+        p.tmaps = &maps;
+        cudaError_t e = run_phase("kc_bwd_scan", s, [&] { return gdn::launch_bwd_scan_kc(d, p, s); });
+        if (e == cudaSuccess) e = run_phase("kc_bwd_prod", s, [&] { return gdn::launch_kc_bwd_prod(d, p, s); });
+        if (e == cudaSuccess) e = run_phase("kc_bwd_local", s, [&] { return gdn::launch_kc_bwd_local(d, p, s); });
+        if (e == cudaSuccess) e = run_phase("bwd_reduce", s, [&] { return gdn::launch_qk_reduce(d, p, s); });
+        return cuda_status(e);
+    }
+    p.rq = reinterpret_cast<float*>(w + L.rq);
+    p.rk = reinterpret_cast<float*>(w + L.rk);
     cudaError_t e = run_phase("prep", s, [&] { return gdn::launch_prep_norms(d, p, s); });
     if (e == cudaSuccess)
         e = run_phase("kc_bwd", s, [&] {

@@ -982,7 +982,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     const int t = (int)blockIdx.x;
     if (t < nscan) {
         const ScanSeg whole{1, (int)d.NC, 0, nullptr, nullptr};
-        ta::bwd_scan_ta_body(d, p, tm, t % ntiles, (t / ntiles) % (int)d.Hv, t / (ntiles * (int)d.Hv),
+        ta::bwd_scan_ta_body<false>(d, p, tm, t % ntiles, (t / ntiles) % (int)d.Hv, t / (ntiles * (int)d.Hv),
                              whole, 0, &g_err_bwdtc, progress, false);
         __syncthreads();
     }

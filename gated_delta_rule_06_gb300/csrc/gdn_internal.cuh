@@ -105,6 +105,17 @@ struct Ptrs {
     float* dl;     // [B, Hv, Tp] cotangent of the log-decay
     float* dbeta;  // [B, Hv, Tp]
     float* part;   // [2, B, NC, Hv] per-chunk partial sums for dA_log, ddt_bias
+    float* ecd;    // per-key-channel chunked form: [B, Hv, NC, Dk] exp(Gamma_63, i) of
+                   // each chunk and key channel i (the state's per-chunk decay)
+    float* gram;   // per-key-channel chunked form: [B, Hv, NC, 64, 64] the decayed
+                   // Gram sum_i kh_ti kh_si exp(Gamma_ti - Gamma_si), s < t (fp32)
+    // per-key-channel chunked backward: per-chunk products of the tensor-core pass
+    float* kdb;    // [B, Hv, Tp, Dk] Delta Sbar'^T       (cotangent of K_d)
+    float* qrb;    // [B, Hv, Tp, Dk] Obar S^T             (cotangent of Q_r)
+    float* wb;     // [B, Hv, Tp, Dk] -Dbar S^T            (cotangent of W)
+    float* pbm;    // [B, Hv, NC, 64, 64] Obar Delta^T, lower incl. diagonal
+    float* m1;     // [B, Hv, NC, 64, 64] Dbar V^T
+    float* ecb;    // [B, Hv, NC, Dk] <Sbar'_i, S_i> per key channel i
     unsigned int* sched;  // tensor-core path: [1 + B Hv] the gradient kernel's item
                           // counter, then the reverse scan's per-(b, h) progress
     // host copy of the tensor maps (tensor-core path; read by the launchers only)
@@ -249,6 +260,16 @@ cudaError_t launch_bwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s);
 cudaError_t launch_fwd_scan_ta_one(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s);
 cudaError_t launch_bwd_scan_ta_one(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s);
 unsigned int read_clear_error_scanta();
+// per-key-channel gates, chunked form: the scans with the chunk kernel's
+// per-value-head Q_r / K_d images (p.qimg / p.kimg) and per-channel decays (p.ecd)
+cudaError_t launch_fwd_scan_kc(const Dims& d, const Ptrs& p, cudaStream_t s);
+cudaError_t launch_bwd_scan_kc(const Dims& d, const Ptrs& p, cudaStream_t s);
+// the chunk-local products of the chunked per-key-channel form (gdn_kc_tc.cu)
+bool kc_chunked_supported(const Dims& d);
+cudaError_t launch_kc_chunk(const Dims& d, const Ptrs& p, cudaStream_t s);
+cudaError_t launch_kc_bwd_prod(const Dims& d, const Ptrs& p, cudaStream_t s);
+cudaError_t launch_kc_bwd_local(const Dims& d, const Ptrs& p, cudaStream_t s);
+unsigned int read_clear_error_kctc();
 bool fwd_chunk_tc_supported(const Dims& d);
 cudaError_t launch_fwd_chunk_tc(const Dims& d, const Ptrs& p, cudaStream_t s);
 unsigned int read_clear_error_fwdtc();

@@ -87,6 +87,12 @@ __device__ __forceinline__ void scale_q(uint8_t* Q, const uint8_t* raw, int Dk) 
     }
 }
 
+// KC: per-key-channel gates.  W, P and U as above (from the per-channel chunk
+// kernel); the B operands Qs and K are the per-value-head images Q_r = qh o
+// exp(Gamma) and K_d = kh o exp(Gamma_63 - Gamma) (qimg, kimg indexed by
+// (b, value head)) with no per-step factor, and S^T decays column by column by
+// the chunk's exp(Gamma_63, i) (p.ecd).
+template <bool KC>
 __global__ void __launch_bounds__(kThreads + 32, 1)
     fwd_scan_ta_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm, ScanSeg sg) {
     extern __shared__ __align__(1024) uint8_t sm[];
@@ -131,7 +137,8 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::mbar_arrive_expect_tx(&barP, pbytes);
         tc::bulk_g2s(sm + L.P, Pimg + (bh * d.NC + c) * pbytes, pbytes, &barP);
     };
-    const int64_t kq = (int64_t)bb * d.Hk + j;  // (b, key head): q / k images of its chunks
+    // (b, key head): q / k images of its chunks; (b, value head) with KC
+    const int64_t kq = KC ? bh : (int64_t)bb * d.Hk + j;
     auto load_q = [&](int64_t c) {
         tc::mbar_arrive_expect_tx(&barQ, wbytes);
         tc::bulk_g2s(sm + L.Q, static_cast<const uint8_t*>(p.qimg) + (kq * d.NC + c) * wbytes, wbytes, &barQ);
@@ -143,6 +150,11 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     auto load_raw = [&](int64_t c) {
         const int s = (int)lp(c);
         uint8_t* dst = sm + L.raw + s * kRawBytes;
+        if constexpr (KC) {
+            tc::mbar_arrive_expect_tx(&barR[s], (uint32_t)(Dk * 4));
+            tc::bulk_g2s(dst, p.ecd + (bh * d.NC + c) * Dk, (uint32_t)(Dk * 4), &barR[s]);
+            return;
+        }
         tc::mbar_arrive_expect_tx(&barR[s], kRawBytes);
         tc::bulk_g2s(dst, p.gam + bh * d.Tp + c * C, C * 8, &barR[s]);
         tc::bulk_g2s(dst + C * 8, p.rq + ((int64_t)bb * d.Hk + j) * d.Tp + c * C, C * 4, &barR[s]);
@@ -232,8 +244,8 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::tmem_wait_st();
         ok = tc::mbar_wait(&barR[0], 0, &g_err_scanta);
         ok = tc::mbar_wait(&barQ, 0, &g_err_scanta) && ok;
-        vectors_from_raw(sm + L.raw, reinterpret_cast<float*>(sm + L.vec), Dk);
-        scale_q(sm + L.Q, sm + L.raw, Dk);
+        vectors_from_raw<KC>(sm + L.raw, reinterpret_cast<float*>(sm + L.vec), Dk);
+        if (!KC) scale_q(sm + L.Q, sm + L.raw, Dk);
         tc::fence_async_smem();
     }
     tc::tc_fence_before();
@@ -271,8 +283,8 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
                 tc::tmem_st16u(tc::tmem_addr(tb, lb, TC.aop + cb / 2), w);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    v[0][i] *= gC;
-                    v[1][i] *= gC;
+                    v[0][i] *= KC ? vb[cb + i] : gC;
+                    v[1][i] *= KC ? vb[cb + 16 + i] : gC;
                 }
                 tc::tmem_st16(tc::tmem_addr(tb, lb, cb), v[0]);
                 tc::tmem_st16(tc::tmem_addr(tb, lb, cb + 16), v[1]);
@@ -288,6 +300,8 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             // step 2: Delta^T acc = S^T W^T and O^T = S^T Qs^T, two independent
             // accumulation chains interleaved
             ok = tc::mbar_wait(&barW, lp(c), &g_err_scanta) && ok;
+            // (the epilogue waits for q and scales it before (B); KC has no scaling)
+            if (KC) ok = tc::mbar_wait(&barQ, lp(c), &g_err_scanta) && ok;
             const uint32_t id = tc::idesc_bf16(DVT, C, false, false);
             uint64_t dw = tW.desc(0), dq = tQ.desc(0);
             const uint64_t iw = tW.desc_step(), iq = tQ.desc_step();
@@ -340,7 +354,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
                         const int ti = 2 * i + u;  // step 32 g + ti
                         dl[u] = (uz ? 0.f : Ub[(32 * g + ti) * DVT + r]) - a[ti >> 4][ti & 15];
                         lo[u] = dl[u] - __bfloat162float(__float2bfloat16_rn(dl[u]));
-                        de[u] = dl[u] * kev[32 * g + ti];
+                        de[u] = KC ? dl[u] : dl[u] * kev[32 * g + ti];
                         dlo[u] = de[u] - __bfloat162float(__float2bfloat16_rn(de[u]));
                     }
                     hiw[i] = tc::pack_bf16(dl[0], dl[1]);
@@ -410,9 +424,11 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
                 const int64_t l1 = c + 1 - cb;
                 const uint8_t* raw = sm + L.raw + (l1 & 1) * kRawBytes;
                 ok = tc::mbar_wait(&barR[l1 & 1], (uint32_t)((l1 >> 1) & 1), &g_err_scanta) && ok;
-                vectors_from_raw(raw, reinterpret_cast<float*>(sm + L.vec) + (l1 & 1) * 4 * C, Dk);
-                ok = tc::mbar_wait(&barQ, (uint32_t)(l1 & 1), &g_err_scanta) && ok;
-                scale_q(sm + L.Q, raw, Dk);
+                vectors_from_raw<KC>(raw, reinterpret_cast<float*>(sm + L.vec) + (l1 & 1) * 4 * C, Dk);
+                if (!KC) {
+                    ok = tc::mbar_wait(&barQ, (uint32_t)(l1 & 1), &g_err_scanta) && ok;
+                    scale_q(sm + L.Q, raw, Dk);
+                }
             }
             tc::fence_async_smem();
             ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
@@ -462,9 +478,10 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
 
+template <bool KC>
 __global__ void __launch_bounds__(kThreads + 32, 1)
     bwd_scan_ta_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm, ScanSeg sg) {
-    bwd_scan_ta_body(d, p, tm, blockIdx.x, blockIdx.y, (int)(blockIdx.z % d.B), sg,
+    bwd_scan_ta_body<KC>(d, p, tm, blockIdx.x, blockIdx.y, (int)(blockIdx.z % d.B), sg,
                      sg.first + (int)(blockIdx.z / d.B), &g_err_scanta, nullptr, true);
 }
 
@@ -477,7 +494,7 @@ bool scan_ta_supported(const Dims& d) {
 
 cudaError_t launch_fwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s) {
     const size_t smem = ta_plan((int)d.Dk).total + 1024;
-    auto kern = fwd_scan_ta_kernel;
+    auto kern = fwd_scan_ta_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);
@@ -490,7 +507,7 @@ int64_t seg_map_width(const Dims& d) { return seg_wd(d.Dk, d.Dv); }
 
 cudaError_t launch_fwd_scan_ta_seg(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s) {
     const size_t smem = ta_plan((int)d.Dk).total + 1024;
-    auto kern = fwd_scan_ta_kernel;
+    auto kern = fwd_scan_ta_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t nx = sg.mode == 0 ? d.Dv / DVT : seg_wd(d.Dk, d.Dv) / DVT;
@@ -504,7 +521,7 @@ cudaError_t launch_fwd_scan_ta_seg(const Dims& d, const Ptrs& p, const ScanSeg& 
 cudaError_t launch_fwd_scan_ta_one(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s) {
     if (sg.mode != 0) return cudaErrorInvalidValue;
     const size_t smem = ta_plan((int)d.Dk).total + 1024;
-    auto kern = fwd_scan_ta_kernel;
+    auto kern = fwd_scan_ta_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);
@@ -608,7 +625,7 @@ cudaError_t launch_seg_chain(const Dims& d, const Ptrs& p, const ScanSeg& sg, cu
 namespace gdn {
 cudaError_t launch_bwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s) {
     const size_t smem = tb_plan((int)d.Dk).total + 1024;
-    auto kern = bwd_scan_ta_kernel;
+    auto kern = bwd_scan_ta_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);
@@ -619,7 +636,7 @@ cudaError_t launch_bwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s) {
 
 cudaError_t launch_bwd_scan_ta_seg(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s) {
     const size_t smem = tb_plan((int)d.Dk).total + 1024;
-    auto kern = bwd_scan_ta_kernel;
+    auto kern = bwd_scan_ta_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t nx = sg.mode == 0 ? d.Dv / DVT : seg_wd(d.Dk, d.Dv) / DVT;
@@ -630,10 +647,34 @@ cudaError_t launch_bwd_scan_ta_seg(const Dims& d, const Ptrs& p, const ScanSeg& 
     return cudaPeekAtLastError();
 }
 
+// per-key-channel gates: the forward and reverse scans over all chunks (grid as
+// launch_fwd_scan_ta / launch_bwd_scan_ta)
+cudaError_t launch_fwd_scan_kc(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    const size_t smem = ta_plan((int)d.Dk).total + 1024;
+    auto kern = fwd_scan_ta_kernel<true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);
+    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps, ScanSeg{1, (int)d.NC, 0, nullptr, nullptr});
+    count_launches(1);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_bwd_scan_kc(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    const size_t smem = tb_plan((int)d.Dk).total + 1024;
+    auto kern = bwd_scan_ta_kernel<true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);
+    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps, ScanSeg{1, (int)d.NC, 0, nullptr, nullptr});
+    count_launches(1);
+    return cudaPeekAtLastError();
+}
+
 cudaError_t launch_bwd_scan_ta_one(const Dims& d, const Ptrs& p, const ScanSeg& sg, cudaStream_t s) {
     if (sg.mode != 0) return cudaErrorInvalidValue;
     const size_t smem = tb_plan((int)d.Dk).total + 1024;
-    auto kern = bwd_scan_ta_kernel;
+    auto kern = bwd_scan_ta_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);

@@ -33,10 +33,15 @@ __device__ __forceinline__ uint32_t canon(int x, int y, int ncols) {
            (uint32_t)(y & 7) * 16u + (uint32_t)(x & 7) * 2u;
 }
 
-// gam, e, gam r_q / sqrt(Dk), e r_k of one chunk from its raw block
+// gam, e, gam r_q / sqrt(Dk), e r_k of one chunk from its raw block; with
+// per-key-channel gates (KC) the raw block is the chunk's decay exp(Gamma_63,i)
+// of each key channel i, copied to v[0 .. Dk)
+template <bool KC>
 __device__ __forceinline__ void vectors_from_raw(const uint8_t* raw, float* v, int Dk) {
     const int i = threadIdx.x;
-    if (i < C) {
+    if constexpr (KC) {
+        for (int c = i; c < Dk; c += kThreads) v[c] = reinterpret_cast<const float*>(raw)[c];
+    } else if (i < C) {
         const double* G = reinterpret_cast<const double*>(raw);
         const float* rq = reinterpret_cast<const float*>(raw + C * 8);
         const float* rk = reinterpret_cast<const float*>(raw + C * 12);
@@ -78,13 +83,15 @@ __host__ __device__ inline TbSmem tb_plan(int Dk) {
 }
 
 // Obar tile (panel layout, chunk e holds step e % 64) -> Os, Oslo: the tile
-// scaled by gam r_q / sqrt(Dk) of its step, as hi + lo bf16
+// scaled by gam r_q / sqrt(Dk) of its step, as hi + lo bf16 (KC: the per-step
+// factors are in the Q operand already, so Os = Obar and Oslo = 0)
+template <bool KC>
 __device__ __forceinline__ void build_os(const uint8_t* O, uint8_t* Os, uint8_t* Oslo,
                                          const uint8_t* raw, int Dk) {
     const int t = threadIdx.x & (C - 1);
     const double* G = reinterpret_cast<const double*>(raw);
     const float* rq = reinterpret_cast<const float*>(raw + C * 8);
-    const float s = expf((float)G[t]) * rq[t] * rsqrtf((float)Dk);
+    const float s = KC ? 1.f : expf((float)G[t]) * rq[t] * rsqrtf((float)Dk);
     for (int e = threadIdx.x; e < C * DVT / 8; e += kThreads) {
         uint4 u = reinterpret_cast<const uint4*>(O)[e];
         const uint32_t* w = reinterpret_cast<const uint32_t*>(&u);
@@ -124,6 +131,11 @@ __host__ __device__ inline int64_t seg_wd(int64_t Dk, int64_t Dv) { return Dv + 
 // (maps, t < nseg - 1) scans it from zero (offset part, the Dv value tiles) and,
 // with Obar = 0, from the identity (linear part, tiles over Dk padded), storing
 // only the end states, into sg.maps[t] with rows of seg_wd(Dk, Dv).
+// KC: per-key-channel gates.  The Q and K operands are then the per-value-head
+// images Q_r = qh o exp(Gamma) and K_d = kh o exp(Gamma_63 - Gamma) (qimg, kimg
+// indexed by (b, value head)), the state cotangent decays column by column by
+// the chunk's exp(Gamma_63, i) (p.ecd), and no per-step factor scales Obar or A2.
+template <bool KC>
 __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, const Tmaps& tm,
                                                  int tile, int h, int bb, const ScanSeg& sg, int t,
                                                  unsigned int* err, unsigned int* progress,
@@ -166,7 +178,8 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
         tc::mbar_arrive_expect_tx(&barP, pbytes);
         tc::bulk_g2s(sm + L.P, Pimg + (bh * NC + c) * pbytes, pbytes, &barP);
     };
-    const int64_t kq = (int64_t)bb * d.Hk + j;  // (b, key head): q / k images of its chunks
+    // (b, key head): q / k images of its chunks; (b, value head) with KC
+    const int64_t kq = KC ? bh : (int64_t)bb * d.Hk + j;
     auto load_kq = [&](int64_t c) {
         tc::mbar_arrive_expect_tx(&barK, kbytes);
         tc::bulk_g2s(sm + L.K, static_cast<const uint8_t*>(p.kimg) + (kq * NC + c) * kbytes, kbytes, &barK);
@@ -183,6 +196,11 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
     auto load_raw = [&](int64_t c) {
         const int s = (int)((hi - 1 - c) & 1);
         uint8_t* dst = sm + L.raw + s * kRawBytes;
+        if constexpr (KC) {
+            tc::mbar_arrive_expect_tx(&barR[s], (uint32_t)(Dk * 4));
+            tc::bulk_g2s(dst, p.ecd + (bh * NC + c) * Dk, (uint32_t)(Dk * 4), &barR[s]);
+            return;
+        }
         tc::mbar_arrive_expect_tx(&barR[s], kRawBytes);
         tc::bulk_g2s(dst, p.gam + bh * d.Tp + c * C, C * 8, &barR[s]);
         tc::bulk_g2s(dst + C * 8, p.rq + ((int64_t)bb * d.Hk + j) * d.Tp + c * C, C * 4, &barR[s]);
@@ -245,10 +263,10 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
         }
         tc::tmem_wait_st();
         ok = tc::mbar_wait(&barR[0], 0, err);
-        vectors_from_raw(sm + L.raw, reinterpret_cast<float*>(sm + L.vec), Dk);
+        vectors_from_raw<KC>(sm + L.raw, reinterpret_cast<float*>(sm + L.vec), Dk);
         if (!oz) {
             ok = tc::mbar_wait(&barO[0], 0, err) && ok;
-            build_os(obuf(hi - 1), sm + L.Os, sm + L.Oslo, sm + L.raw, Dk);
+            build_os<KC>(obuf(hi - 1), sm + L.Os, sm + L.Oslo, sm + L.raw, Dk);
         }
         tc::fence_async_smem();
     }
@@ -306,8 +324,8 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
                 tc::tmem_st16u(tc::tmem_addr(tb, lb, aop + cb / 2), w);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    v[0][i] *= gC;
-                    v[1][i] *= gC;
+                    v[0][i] *= KC ? vb[cb + i] : gC;
+                    v[1][i] *= KC ? vb[cb + 16 + i] : gC;
                 }
                 tc::tmem_st16(tc::tmem_addr(tb, lb, cb), v[0]);
                 tc::tmem_st16(tc::tmem_addr(tb, lb, cb + 16), v[1]);
@@ -383,9 +401,10 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int t0 = 32 * g + 2 * i;
-                const float x = -(a1[(2 * i) >> 4][(2 * i) & 15] + kev[t0] * a2[(2 * i) >> 4][(2 * i) & 15]);
+                const float e0 = KC ? 1.f : kev[t0], e1 = KC ? 1.f : kev[t0 + 1];
+                const float x = -(a1[(2 * i) >> 4][(2 * i) & 15] + e0 * a2[(2 * i) >> 4][(2 * i) & 15]);
                 const float y = -(a1[(2 * i + 1) >> 4][(2 * i + 1) & 15] +
-                                  kev[t0 + 1] * a2[(2 * i + 1) >> 4][(2 * i + 1) & 15]);
+                                  e1 * a2[(2 * i + 1) >> 4][(2 * i + 1) & 15]);
                 nd[i] = tc::pack_bf16(x, y);
             }
 #pragma unroll
@@ -414,10 +433,10 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
             if (c > lo) {  // vectors and the scaled Obar operands of chunk c - 1
                 const uint8_t* raw = sm + L.raw + ((m + 1) & 1) * kRawBytes;
                 ok = tc::mbar_wait(&barR[(m + 1) & 1], (uint32_t)(((m + 1) >> 1) & 1), err) && ok;
-                vectors_from_raw(raw, reinterpret_cast<float*>(sm + L.vec) + ((m + 1) & 1) * 4 * C, Dk);
+                vectors_from_raw<KC>(raw, reinterpret_cast<float*>(sm + L.vec) + ((m + 1) & 1) * 4 * C, Dk);
                 if (!oz) {
                     ok = tc::mbar_wait(&barO[(m + 1) & 1], (uint32_t)(((m + 1) >> 1) & 1), err) && ok;
-                    build_os(obuf(c - 1), sm + L.Os, sm + L.Oslo, raw, Dk);
+                    build_os<KC>(obuf(c - 1), sm + L.Os, sm + L.Oslo, raw, Dk);
                 }
                 tc::fence_async_smem();
             }
