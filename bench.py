@@ -168,7 +168,10 @@ def method_model(w, gates="ab", nseg=1, nseg_bwd=1, conv_k=0, rank=0, iters=3):
         m["kc_scan"] = dict(flops=f_scan, bytes=st + vv + st + ckpt)
         m["kc_bwd_scan"] = dict(flops=f_bscan, bytes=vv + st + st)
         m["kc_bwd_prod"] = dict(flops=fk_prod, bytes=ckpt + 3 * vv)
-        m["kc_bwd_local"] = dict(flops=fk_bwd - f_bscan - fk_prod, bytes=qk + 2 * gin)
+        fk_gate = th * (3 * C * Dk + 2 * C * C)
+        m["kc_bwd_gate"] = dict(flops=fk_gate, bytes=qk / 2 + gin + B * T * Hv * es)
+        m["kc_bwd_chan"] = dict(flops=fk_bwd - f_bscan - fk_prod - fk_gate,
+                                bytes=qk + gin + B * T * Hv * Dk * es)
         m["kc_fwd"] = dict(flops=7.0 * th * Dk * Dv, bytes=qk + vv + gin + vv + 2 * st + ckpt)
         m["kc_bwd"] = dict(flops=20.0 * th * Dk * Dv,
                            bytes=qk + 2 * vv + gin + st + ckpt + vv + gin + st)
@@ -302,10 +305,18 @@ def design_model(w, conv_k=0, gates="ab", nseg=1, nseg_bwd=1):
             flops=units * (6 * C * Dk * Dv + 6 * C * C * Dv),
             bytes=units * (2 * C * Dv * es + C * Dv * 4 + C * Dv * img + C * C * img + 2 * Dk * Dv * img
                            + 2 * C * C * 4 + C * Dv * es + 3 * C * Dk * 4 + Dk * 4))
-        m["kc_bwd_local"] = dict(
-            flops=units * (8 * C * C * Dk + 2 * C * C * Dk + 4 * C ** 3),
-            bytes=io_in - B * T * Hv * Dv * es + units * (C * C * img + 3 * C * C * 4 + 4 * C * Dk * 4
-                                                          + Dk * 4 + 2 * C * Dk * 4) + gin)
+        # the gate pass reads k, the gates, T, M1, G and Wbar and writes Kbar_r
+        # over Wbar, Gbar over M1 and the beta cotangent; the channel pass reads
+        # q, k, the gates, Pbar, Gbar, Qbar_r, Kbar_d, Kbar_r, ebar and writes the
+        # fp32 per-value-head q / k cotangents and the log-decay cotangent
+        m["kc_bwd_gate"] = dict(
+            flops=units * (3 * C * C * Dk + 4 * C ** 3 / 3),
+            bytes=B * T * Hk * Dk * es + gin + units * (C * C * img + 3 * C * C * 4 + 2 * C * Dk * 4)
+            + B * T * Hv * es)
+        m["kc_bwd_chan"] = dict(
+            flops=units * 10 * C * C * Dk,
+            bytes=2 * B * T * Hk * Dk * es + gin + units * (2 * C * C * 4 + 5 * C * Dk * 4 + Dk * 4)
+            + B * T * Hv * Dk * es)
         # recurrent form: fp32 states every 8 steps written and read back, and
         # the per-16-column tile partials of the q / k / log-decay cotangents
         nt, NS = Dv // 16, (T + 7) // 8
@@ -320,7 +331,7 @@ def design_model(w, conv_k=0, gates="ab", nseg=1, nseg_bwd=1):
         m["_step"] = dict(bytes=2 * io_in + 2 * B * T * Hv * Dv * es + gin + 2 * units * Dk * Dv * img
                           + 4 * B * T * Hk * Dk * es + 4 * BH * Dk * Dv * 4,
                           flops=sum(m[k]["flops"] for k in ("kc_chunk", "kc_scan", "kc_bwd_scan",
-                                                            "kc_bwd_prod", "kc_bwd_local")))
+                                                            "kc_bwd_prod", "kc_bwd_gate", "kc_bwd_chan")))
     return m
 
 

@@ -989,7 +989,8 @@ gdn_status gdn_backward_kc(const gdn_shape* shape, const void* q, const void* k,
         p.tmaps = &maps;
         cudaError_t e = run_phase("kc_bwd_scan", s, [&] { return gdn::launch_bwd_scan_kc(d, p, s); });
         if (e == cudaSuccess) e = run_phase("kc_bwd_prod", s, [&] { return gdn::launch_kc_bwd_prod(d, p, s); });
-        if (e == cudaSuccess) e = run_phase("kc_bwd_local", s, [&] { return gdn::launch_kc_bwd_local(d, p, s); });
+        if (e == cudaSuccess) e = run_phase("kc_bwd_gate", s, [&] { return gdn::launch_kc_bwd_gate(d, p, s); });
+        if (e == cudaSuccess) e = run_phase("kc_bwd_chan", s, [&] { return gdn::launch_kc_bwd_chan(d, p, s); });
         if (e == cudaSuccess) e = run_phase("bwd_reduce", s, [&] { return gdn::launch_qk_reduce(d, p, s); });
         return cuda_status(e);
     }

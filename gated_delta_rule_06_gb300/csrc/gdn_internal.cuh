@@ -268,7 +268,8 @@ cudaError_t launch_bwd_scan_kc(const Dims& d, const Ptrs& p, cudaStream_t s);
 bool kc_chunked_supported(const Dims& d);
 cudaError_t launch_kc_chunk(const Dims& d, const Ptrs& p, cudaStream_t s);
 cudaError_t launch_kc_bwd_prod(const Dims& d, const Ptrs& p, cudaStream_t s);
-cudaError_t launch_kc_bwd_local(const Dims& d, const Ptrs& p, cudaStream_t s);
+cudaError_t launch_kc_bwd_gate(const Dims& d, const Ptrs& p, cudaStream_t s);
+cudaError_t launch_kc_bwd_chan(const Dims& d, const Ptrs& p, cudaStream_t s);
 unsigned int read_clear_error_kctc();
 bool fwd_chunk_tc_supported(const Dims& d);
 cudaError_t launch_fwd_chunk_tc(const Dims& d, const Ptrs& p, cudaStream_t s);

@@ -58,14 +58,17 @@ __device__ __forceinline__ void ld_bf16x8(const void* src, float* v) {
 // ---- forward: chunk-local products ------------------------------------------
 
 // Shared memory of the chunk kernel, byte offsets.  q, k and Gamma rows are fp32
-// with an odd row stride (Dk + 1 floats): threads on consecutive rows of one
-// column fall in distinct banks.  Region q later holds T and the solve's scratch,
-// region R the rows kh_s exp(Gamma_b - Gamma_s) of blocks 0..2, then beta V.
+// with rows of Dk + 4 floats (16-byte aligned, so four channels move as one
+// float4; consecutive rows four banks apart).  Region q later holds T and the
+// solve's scratch; region R the right factors kh_s exp(Gamma_b - Gamma_s) of
+// the steps s < 48 channel-major ([Dk][52]: one pivot block's 8 or 16 factors
+// of a channel are contiguous), then beta V.
+constexpr int kRS = 52;
 struct KfSmem {
     uint32_t q, k, G, R, A, P, vec, total;
 };
 __host__ __device__ inline KfSmem kf_plan(int Dk, int Dv) {
-    const uint32_t LD = (uint32_t)Dk + 1;
+    const uint32_t LD = (uint32_t)Dk + 4;
     KfSmem s{};
     uint32_t o = 0;
     auto take = [&](uint32_t bytes) {
@@ -74,7 +77,7 @@ __host__ __device__ inline KfSmem kf_plan(int Dk, int Dv) {
         return r;
     };
     const uint32_t rows = C * LD * 4, mat = C * LDT * 4;
-    const uint32_t rR = 48 * LD * 4, rV = C * ((uint32_t)Dv + 1) * 4;
+    const uint32_t rR = (uint32_t)Dk * kRS * 4, rV = C * ((uint32_t)Dv + 4) * 4;
     s.q = take(rows > 2 * mat ? rows : 2 * mat);
     s.k = take(rows);
     s.G = take(rows);
@@ -86,14 +89,20 @@ __host__ __device__ inline KfSmem kf_plan(int Dk, int Dv) {
     return s;
 }
 
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void st4(float* p, float a, float b, float c, float e) {
+    *reinterpret_cast<float4*>(p) = make_float4(a, b, c, e);
+}
+
 // One CTA per (chunk, value head, batch).  p.a = log_decay [B, T, Hv, Dk], p.b =
 // beta [B, T, Hv] (bf16); rq, rk from prep.  Writes the panel images of Q_r, K_d
-// (p.qimg, p.kimg, per value head), P, T, W, the fp32 rows of U, and e_C (p.ecd).
+// (p.qimg, p.kimg, per value head), P, T, W, the fp32 rows of U, e_C (p.ecd) and
+// the decayed Gram of the k rows (p.gram, for the beta cotangent).
 __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
     extern __shared__ __align__(16) uint8_t ksm[];
     const int c = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
     const int j = h / (int)d.G;
-    const int Dk = (int)d.Dk, Dv = (int)d.Dv, LD = Dk + 1, LV = Dv + 1;
+    const int Dk = (int)d.Dk, Dv = (int)d.Dv, LD = Dk + 4, LV = Dv + 4;
     const int tid = threadIdx.x;
     const KfSmem L = kf_plan(Dk, Dv);
     float* qf = reinterpret_cast<float*>(ksm + L.q);
@@ -141,11 +150,12 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
 #pragma unroll
             for (int u = 0; u < 8; ++u) xq[u] = xk[u] = xl[u] = 0.f;
         }
+        const float rq = rqs[t], rk = rks[t], o = on[t];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            qf[t * LD + i0 + u] = xq[u] * rqs[t];
-            kf[t * LD + i0 + u] = xk[u] * rks[t];
-            Gf[t * LD + i0 + u] = on[t] != 0.f ? xl[u] : 0.f;
+        for (int u = 0; u < 8; u += 4) {
+            st4(qf + t * LD + i0 + u, xq[u] * rq, xq[u + 1] * rq, xq[u + 2] * rq, xq[u + 3] * rq);
+            st4(kf + t * LD + i0 + u, xk[u] * rk, xk[u + 1] * rk, xk[u + 2] * rk, xk[u + 3] * rk);
+            st4(Gf + t * LD + i0 + u, xl[u] * o, xl[u + 1] * o, xl[u + 2] * o, xl[u + 3] * o);
         }
     }
     __syncthreads();
@@ -166,10 +176,17 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
         const int t = e % C, i0 = (e / C) * 8;
         float a[8], b[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const float g = Gf[t * LD + i0 + u];
-            a[u] = qf[t * LD + i0 + u] * expf(g);
-            b[u] = kf[t * LD + i0 + u] * expf(Gf[(C - 1) * LD + i0 + u] - g);
+        for (int u = 0; u < 8; u += 4) {
+            const float4 g = ld4(Gf + t * LD + i0 + u), gl = ld4(Gf + (C - 1) * LD + i0 + u);
+            const float4 qq = ld4(qf + t * LD + i0 + u), kk = ld4(kf + t * LD + i0 + u);
+            a[u] = qq.x * expf(g.x);
+            a[u + 1] = qq.y * expf(g.y);
+            a[u + 2] = qq.z * expf(g.z);
+            a[u + 3] = qq.w * expf(g.w);
+            b[u] = kk.x * expf(gl.x - g.x);
+            b[u + 1] = kk.y * expf(gl.y - g.y);
+            b[u + 2] = kk.z * expf(gl.z - g.z);
+            b[u + 3] = kk.w * expf(gl.w - g.w);
         }
         st_bf16x8(qr_img + 16 * e, a);
         st_bf16x8(kd_img + 16 * e, b);
@@ -177,13 +194,12 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
     for (int i = tid; i < Dk; i += kThreads) p.ecd[ci * Dk + i] = expf(Gf[(C - 1) * LD + i]);
     for (int e = tid; e < 48 * Dk; e += kThreads) {
         const int s = e / Dk, i = e % Dk, b = s | 15;
-        Rt[s * LD + i] = kf[s * LD + i] * expf(Gf[b * LD + i] - Gf[s * LD + i]);
+        Rt[i * kRS + s] = kf[s * LD + i] * expf(Gf[b * LD + i] - Gf[s * LD + i]);
     }
     __syncthreads();
 
-    // A and P.  Threads 0..191: the off-diagonal blocks, one row t and eight
-    // columns s of a pivot block J each; threads 192..255: the diagonal blocks,
-    // one (t, s) pair at a time
+    // A and P off the diagonal blocks: threads 0..191, one row t and eight
+    // columns s of a pivot block J each; four channels per step
     if (tid < 192) {
         const int half = tid / 96, r = tid % 96;
         const int J = r < 48 ? 0 : r < 80 ? 1 : 2;
@@ -192,19 +208,21 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
         float a8[8], p8[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) a8[x] = p8[x] = 0.f;
-        const float* kt = kf + t * LD;
-        const float* qt = qf + t * LD;
-        const float* Gt = Gf + t * LD;
-        const float* Gb = Gf + b * LD;
-        const float* Rs = Rt + s0 * LD;
-        for (int i = 0; i < Dk; ++i) {
-            const float u = expf(Gt[i] - Gb[i]);
-            const float ka = kt[i] * u, qa = qt[i] * u;
+        for (int i = 0; i < Dk; i += 4) {
+            const float4 kt = ld4(kf + t * LD + i), qt = ld4(qf + t * LD + i);
+            const float4 gt = ld4(Gf + t * LD + i), gb = ld4(Gf + b * LD + i);
+            const float u[4] = {expf(gt.x - gb.x), expf(gt.y - gb.y), expf(gt.z - gb.z), expf(gt.w - gb.w)};
+            const float ka[4] = {kt.x * u[0], kt.y * u[1], kt.z * u[2], kt.w * u[3]};
+            const float qa[4] = {qt.x * u[0], qt.y * u[1], qt.z * u[2], qt.w * u[3]};
 #pragma unroll
-            for (int x = 0; x < 8; ++x) {
-                const float rr = Rs[x * LD + i];
-                a8[x] = fmaf(ka, rr, a8[x]);
-                p8[x] = fmaf(qa, rr, p8[x]);
+            for (int x = 0; x < 4; ++x) {
+                const float4 r0 = ld4(Rt + (i + x) * kRS + s0), r1 = ld4(Rt + (i + x) * kRS + s0 + 4);
+                const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+                for (int y = 0; y < 8; ++y) {
+                    a8[y] = fmaf(ka[x], rr[y], a8[y]);
+                    p8[y] = fmaf(qa[x], rr[y], p8[y]);
+                }
             }
         }
 #pragma unroll
@@ -215,22 +233,47 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
         float* gr = p.gram + (ci * C + t) * C + s0;
         reinterpret_cast<float4*>(gr)[0] = make_float4(a8[0], a8[1], a8[2], a8[3]);
         reinterpret_cast<float4*>(gr)[1] = make_float4(a8[4], a8[5], a8[6], a8[7]);
-    } else {
-        for (int e = tid - 192; e < 4 * 136; e += kThreads - 192) {
-            const int I = e / 136, pi = e % 136;
-            int tt = (int)((sqrtf(8.f * pi + 1.f) - 1.f) * 0.5f);
-            while ((tt + 1) * (tt + 2) / 2 <= pi) ++tt;
-            while (tt * (tt + 1) / 2 > pi) --tt;
-            const int t = 16 * I + tt, s = 16 * I + (pi - tt * (tt + 1) / 2);
-            float a = 0.f, pp = 0.f;
-            for (int i = 0; i < Dk; ++i) {
-                const float ks = kf[s * LD + i] * expf(Gf[t * LD + i] - Gf[s * LD + i]);
-                a = fmaf(kf[t * LD + i], ks, a);
-                pp = fmaf(qf[t * LD + i], ks, pp);
+    }
+    // the diagonal blocks: thread (row t, channel quarter qq) forms row t against
+    // every s = 16 I .. t of its block over its quarter of the channels, each term
+    // with its own exponential; the quarters' sums meet by shuffles
+    {
+        const int t = tid >> 2, qq = tid & 3, I = t >> 4, n = t - 16 * I;  // s = 16 I + 0 .. n
+        const int qw = Dk / 4;
+        float ad[16], pd[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) ad[x] = pd[x] = 0.f;
+        for (int i = qq * qw; i < (qq + 1) * qw; i += 4) {
+            const float4 kt = ld4(kf + t * LD + i), qt = ld4(qf + t * LD + i), gt = ld4(Gf + t * LD + i);
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+                if (x <= n) {
+                    const int sr = 16 * I + x;
+                    const float4 ks = ld4(kf + sr * LD + i), gs = ld4(Gf + sr * LD + i);
+                    const float e0 = ks.x * expf(gt.x - gs.x), e1 = ks.y * expf(gt.y - gs.y);
+                    const float e2 = ks.z * expf(gt.z - gs.z), e3 = ks.w * expf(gt.w - gs.w);
+                    ad[x] = fmaf(kt.x, e0, fmaf(kt.y, e1, fmaf(kt.z, e2, fmaf(kt.w, e3, ad[x]))));
+                    pd[x] = fmaf(qt.x, e0, fmaf(qt.y, e1, fmaf(qt.z, e2, fmaf(qt.w, e3, pd[x]))));
+                }
             }
-            A[t * LDT + s] = s < t ? bt[t] * a : 0.f;
-            Pm[t * LDT + s] = pp;
-            if (s < t) p.gram[(ci * C + t) * C + s] = a;
+        }
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+            ad[x] += __shfl_xor_sync(0xffffffffu, ad[x], 1);
+            ad[x] += __shfl_xor_sync(0xffffffffu, ad[x], 2);
+            pd[x] += __shfl_xor_sync(0xffffffffu, pd[x], 1);
+            pd[x] += __shfl_xor_sync(0xffffffffu, pd[x], 2);
+        }
+        if (qq == 0) {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+                if (x <= n) {
+                    const int sr = 16 * I + x;
+                    A[t * LDT + sr] = x < n ? bt[t] * ad[x] : 0.f;
+                    Pm[t * LDT + sr] = pd[x];
+                    if (x < n) p.gram[(ci * C + t) * C + sr] = ad[x];
+                }
+            }
         }
     }
     __syncthreads();
@@ -270,8 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
 #pragma unroll
             for (int u = 0; u < 8; ++u) x[u] = 0.f;
         }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) Vb[t * LV + c0 + u] = bt[t] * x[u];
+        const float bs = bt[t];
+        st4(Vb + t * LV + c0, bs * x[0], bs * x[1], bs * x[2], bs * x[3]);
+        st4(Vb + t * LV + c0 + 4, bs * x[4], bs * x[5], bs * x[6], bs * x[7]);
     }
     __syncthreads();
 
@@ -291,11 +335,11 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
 #pragma unroll
             for (int x = 0; x < 4; ++x) acc[r][x] = 0.f;
         for (int s = 0; s <= tq + 3; ++s) {
-            float tv[4], bv[4];
+            float tv[4];
 #pragma unroll
             for (int r = 0; r < 4; ++r) tv[r] = Tm[(tq + r) * LDT + s];
-#pragma unroll
-            for (int x = 0; x < 4; ++x) bv[x] = Bm[s * ldb + x];
+            const float4 b4 = ld4(Bm + s * ldb);
+            const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
             for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -316,7 +360,6 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
         }
     }
 }
-
 
 // ---- backward: per-chunk gradients ------------------------------------------
 //
@@ -556,51 +599,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) tc::tmem_dealloc(tb, 256);
 }
 
-constexpr int CB = 32;       // key channels per block of kernel 2
-constexpr int LB = CB + 1;   // row stride of its per-block arrays (odd: conflict-free columns)
-
-struct KlSmem {
-    uint32_t T, Pb, M, X, q, k, G, W, F, R, Gb, vec, total;
-};
-__host__ __device__ inline KlSmem kl_plan() {
-    KlSmem s{};
-    uint32_t o = 0;
-    auto take = [&](uint32_t bytes) {
-        const uint32_t r = o;
-        o += (bytes + 127u) & ~127u;
-        return r;
-    };
-    const uint32_t mat = C * LDT * 4, blk = C * LB * 4;
-    s.T = take(mat);
-    s.Pb = take(mat);
-    s.M = take(mat);
-    s.X = take(mat);
-    s.q = take(blk);
-    s.k = take(blk);
-    s.G = take(blk);
-    s.W = take(blk);
-    s.F = take(96 * LB * 4);
-    s.R = take(48 * LB * 4);
-    s.Gb = take(blk);
-    s.vec = take(6 * C * 4 + 8 * CB * 4);
-    s.total = o;
-    return s;
-}
+constexpr int CB = 32;       // key channels per block of kernels 2 and 3
+constexpr int LB = CB + 1;   // row stride of their per-block arrays (odd: conflict-free columns)
+constexpr int kBlkMat = C * LDT * 4, kBlkArr = C * LB * 4;
 
 // rows of the pivot factors exp(Gamma_t - Gamma_b), b = 16 J + 15, t > b: J-major
 __device__ __forceinline__ int frow(int J, int t) { return J == 0 ? t - 16 : J == 1 ? 48 + t - 32 : 80 + t - 48; }
 
-// normalised q, k rows and Gamma of key channels cb0 .. cb0 + 31 (256 threads:
-// thread = (row, 8 channels)); ends synchronised
+// normalised k (and, WITH_Q, q) rows and Gamma of key channels cb0 .. cb0 + 31
+// (256 threads: thread = (row, 8 channels)); Gamma by a two-level running sum,
+// warp w over rows 8 w .. 8 w + 7 of channel `lane`, then the offsets of the
+// pieces above (part: [8][CB] scratch).  Ends synchronised.
+template <bool WITH_Q>
 __device__ __forceinline__ void load_block(const Dims& d, const Ptrs& p, int bb, int h, int j, int64_t t0,
                                            int nvalid, int cb0, const float* on, const float* rqs,
-                                           const float* rks, float* qb, float* kb, float* Gm) {
+                                           const float* rks, float* qb, float* kb, float* Gm, float* part) {
     const int tid = threadIdx.x, t = tid >> 2, i0 = (tid & 3) * 8;
     const int Dk = (int)d.Dk;
     float xq[8], xk[8], xl[8];
     if (t < nvalid) {
         const int64_t qi = (((int64_t)bb * d.T + t0 + t) * d.Hk + j) * Dk + cb0 + i0;
-        ld_bf16x8(static_cast<const __nv_bfloat16*>(p.q) + qi, xq);
+        if (WITH_Q) ld_bf16x8(static_cast<const __nv_bfloat16*>(p.q) + qi, xq);
         ld_bf16x8(static_cast<const __nv_bfloat16*>(p.k) + qi, xk);
         ld_bf16x8(static_cast<const __nv_bfloat16*>(p.a) + (((int64_t)bb * d.T + t0 + t) * d.Hv + h) * Dk + cb0 + i0,
                   xl);
@@ -610,59 +629,68 @@ __device__ __forceinline__ void load_block(const Dims& d, const Ptrs& p, int bb,
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-        qb[t * LB + i0 + u] = xq[u] * rqs[t];
+        if (WITH_Q) qb[t * LB + i0 + u] = xq[u] * rqs[t];
         kb[t * LB + i0 + u] = xk[u] * rks[t];
         Gm[t * LB + i0 + u] = on[t] != 0.f ? xl[u] : 0.f;
     }
     __syncthreads();
-    if (tid < CB) {
-        float g = 0.f;
-        for (int s = 0; s < C; ++s) {
-            g += Gm[s * LB + tid];
-            Gm[s * LB + tid] = g;
-        }
+    const int w = tid >> 5, i = tid & 31;
+    float sacc = 0.f;
+    for (int r = 8 * w; r < 8 * w + 8; ++r) {
+        sacc += Gm[r * LB + i];
+        Gm[r * LB + i] = sacc;
     }
+    part[w * CB + i] = sacc;
+    __syncthreads();
+    float off = 0.f;
+    for (int w2 = 0; w2 < w; ++w2) off += part[w2 * CB + i];
+    for (int r = 8 * w; r < 8 * w + 8; ++r) Gm[r * LB + i] += off;
     __syncthreads();
 }
 
+// per-step vectors of a chunk: beta, applied flag, r_q / sqrt(Dk), r_k
+__device__ __forceinline__ void chunk_vectors(const Dims& d, const Ptrs& p, int bb, int h, int j, int64_t t0,
+                                              int nvalid, float* bt, float* on, float* rqs, float* rks) {
+    const int tid = threadIdx.x;
+    if (tid < C) {
+        step_gate(d, p, bb, h, t0, nvalid, tid, &bt[tid], &on[tid]);
+        const int64_t ri = ((int64_t)bb * d.Hk + j) * d.Tp + t0 + tid;
+        rqs[tid] = tid < nvalid ? p.rq[ri] * rsqrtf((float)d.Dk) : 0.f;
+        rks[tid] = tid < nvalid ? p.rk[ri] : 0.f;
+    }
+}
+
 // Kernel 2: one CTA per (chunk, value head, batch), 256 threads, CUDA cores.
-__global__ void __launch_bounds__(kThreads, 1) kc_bwd_local_kernel(Dims d, Ptrs p) {
+// M = M1 + Wbar (kh o E)^T and Kbar_r = diag(beta) T^T Wbar over the channel
+// blocks (Kbar_r overwrites Wbar in p.wb), then betabar (p.db) and Gbar (into
+// p.m1, over M1).
+__global__ void __launch_bounds__(kThreads, 2) kc_bwd_gate_kernel(Dims d, Ptrs p) {
     extern __shared__ __align__(16) uint8_t lsm[];
     const int c = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
     const int j = h / (int)d.G;
     const int Dk = (int)d.Dk;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const KlSmem L = kl_plan();
-    float* Tm = reinterpret_cast<float*>(lsm + L.T);
-    float* Pb = reinterpret_cast<float*>(lsm + L.Pb);
-    float* Mm = reinterpret_cast<float*>(lsm + L.M);
-    float* Xm = reinterpret_cast<float*>(lsm + L.X);
-    float* qb = reinterpret_cast<float*>(lsm + L.q);
-    float* kb = reinterpret_cast<float*>(lsm + L.k);
-    float* Gm = reinterpret_cast<float*>(lsm + L.G);
-    float* Wk = reinterpret_cast<float*>(lsm + L.W);
-    float* Fm = reinterpret_cast<float*>(lsm + L.F);
-    float* Rm = reinterpret_cast<float*>(lsm + L.R);
-    float* Gb = reinterpret_cast<float*>(lsm + L.Gb);
-    float* bt = reinterpret_cast<float*>(lsm + L.vec);
+    float* Tm = reinterpret_cast<float*>(lsm);
+    float* Mm = Tm + C * LDT;
+    float* Xm = Mm + C * LDT;
+    float* kb = Xm + C * LDT;
+    float* Gm = kb + C * LB;
+    float* Wk = Gm + C * LB;
+    float* Kr = Wk + C * LB;
+    float* part = Kr + C * LB;  // [8][CB]
+    float* bt = part + 8 * CB;
     float* on = bt + C;
     float* rqs = on + C;
     float* rks = rqs + C;
     float* bbar = rks + C;
-    float* red = bbar + 2 * C;  // [8][CB]
     const int64_t t0 = (int64_t)c * C;
     const int nvalid = (int)(d.T - t0 < C ? d.T - t0 : C);
     const int64_t bh = (int64_t)bb * d.Hv + h;
     const int64_t ci = bh * d.NC + c;
     const int64_t rowbase = bh * d.Tp + t0;
 
-    if (tid < C) {
-        step_gate(d, p, bb, h, t0, nvalid, tid, &bt[tid], &on[tid]);
-        const int64_t ri = ((int64_t)bb * d.Hk + j) * d.Tp + t0 + tid;
-        rqs[tid] = tid < nvalid ? p.rq[ri] * rsqrtf((float)Dk) : 0.f;
-        rks[tid] = tid < nvalid ? p.rk[ri] : 0.f;
-    }
-    {  // T (from its bf16 panel image), Pbar and M1
+    chunk_vectors(d, p, bb, h, j, t0, nvalid, bt, on, rqs, rks);
+    {  // T (from its bf16 panel image) and M1
         const uint8_t* Timg = reinterpret_cast<const uint8_t*>(p.Tinv) + ci * C * C * 2;
         for (int e = tid; e < C * (C / 8); e += kThreads) {
             float x[8];
@@ -671,19 +699,16 @@ __global__ void __launch_bounds__(kThreads, 1) kc_bwd_local_kernel(Dims d, Ptrs 
 #pragma unroll
             for (int u = 0; u < 8; ++u) Tm[t * LDT + s0 + u] = x[u];
         }
-        const float* pg = p.pbm + ci * C * C;
         const float* mg = p.m1 + ci * C * C;
         for (int e = tid; e < C * C / 4; e += kThreads) {
             const int t = e / (C / 4), s0 = (e % (C / 4)) * 4;
-            *reinterpret_cast<float4*>(Pb + t * LDT + s0) = reinterpret_cast<const float4*>(pg)[e];
             *reinterpret_cast<float4*>(Mm + t * LDT + s0) = reinterpret_cast<const float4*>(mg)[e];
         }
     }
     __syncthreads();
 
-    // pass 1: M += Wbar (kh o E)^T over the channel blocks
     for (int cb0 = 0; cb0 < Dk; cb0 += CB) {
-        load_block(d, p, bb, h, j, t0, nvalid, cb0, on, rqs, rks, qb, kb, Gm);
+        load_block<false>(d, p, bb, h, j, t0, nvalid, cb0, on, rqs, rks, nullptr, kb, Gm, part);
         {
             const int t = tid >> 2, i0 = (tid & 3) * 8;
             const float* src = p.wb + (rowbase + t) * Dk + cb0 + i0;
@@ -692,11 +717,11 @@ __global__ void __launch_bounds__(kThreads, 1) kc_bwd_local_kernel(Dims d, Ptrs 
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 Wk[t * LB + i0 + u] = w8[u];
-                Fm[t * LB + i0 + u] = kb[t * LB + i0 + u] * expf(Gm[t * LB + i0 + u]);
+                Kr[t * LB + i0 + u] = kb[t * LB + i0 + u] * expf(Gm[t * LB + i0 + u]);
             }
         }
         __syncthreads();
-        {
+        {  // M += Wbar (kh o E)^T over this block's channels: 4 x 4 tiles
             const int tq = 4 * (tid >> 4), sq = 4 * (tid & 15);
             float acc[4][4];
 #pragma unroll
@@ -708,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1) kc_bwd_local_kernel(Dims d, Ptrs 
 #pragma unroll
                 for (int r = 0; r < 4; ++r) wv[r] = Wk[(tq + r) * LB + i];
 #pragma unroll
-                for (int x = 0; x < 4; ++x) kv[x] = Fm[(sq + x) * LB + i];
+                for (int x = 0; x < 4; ++x) kv[x] = Kr[(sq + x) * LB + i];
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -718,6 +743,22 @@ __global__ void __launch_bounds__(kThreads, 1) kc_bwd_local_kernel(Dims d, Ptrs 
             for (int r = 0; r < 4; ++r)
 #pragma unroll
                 for (int x = 0; x < 4; ++x) Mm[(tq + r) * LDT + sq + x] += acc[r][x];
+        }
+        // Kbar_r = diag(beta) T^T Wbar: four rows r0 .. r0 + 3 and channel `lane` per
+        // item (T zero above the diagonal, so u starts at r0)
+        for (int it = 0; it < 2; ++it) {
+            const int r0 = 4 * (warp + 8 * it), i = lane;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int u = r0; u < C; ++u) {
+                const float4 t4 = *reinterpret_cast<const float4*>(Tm + u * LDT + r0);
+                const float wv = Wk[u * LB + i];
+                acc[0] = fmaf(t4.x, wv, acc[0]);
+                acc[1] = fmaf(t4.y, wv, acc[1]);
+                acc[2] = fmaf(t4.z, wv, acc[2]);
+                acc[3] = fmaf(t4.w, wv, acc[3]);
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a) p.wb[(rowbase + r0 + a) * Dk + cb0 + i] = bt[r0 + a] * acc[a];
         }
         __syncthreads();
     }
@@ -782,8 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1) kc_bwd_local_kernel(Dims d, Ptrs 
             for (int x = 0; x < 4; ++x) Mm[(tq + r) * LDT + sq + x] = sq + x < tq + r ? -acc[r][x] : 0.f;
     }
     __syncthreads();
-    // the decayed Gram G of the forward (into X), betabar += sum_s Abar G, Gbar = diag(beta) Abar
-    {
+    {  // the forward's decayed Gram G (into X)
         const float* gg = p.gram + ci * C * C;
         for (int e = tid; e < C * C; e += kThreads) {
             const int t = e / C, s = e % C;
@@ -791,124 +831,208 @@ __global__ void __launch_bounds__(kThreads, 1) kc_bwd_local_kernel(Dims d, Ptrs 
         }
     }
     __syncthreads();
-    if (tid < C) {
+    if (tid < C) {  // betabar += sum_s Abar G
         float sacc = bbar[tid];
         for (int s = 0; s < tid; ++s) sacc = fmaf(Mm[tid * LDT + s], Xm[tid * LDT + s], sacc);
         if (tid < nvalid)
             static_cast<__nv_bfloat16*>(p.db)[((int64_t)bb * d.T + t0 + tid) * d.Hv + h] =
                 __float2bfloat16_rn(on[tid] != 0.f ? sacc : 0.f);
     }
-    __syncthreads();
-    for (int e = tid; e < C * C; e += kThreads) {
-        const int t = e / C, s = e % C;
-        Mm[t * LDT + s] *= bt[t];
-    }
-    __syncthreads();
-    const float* Gbar = Mm;
-
-    // pass 2, per channel block: lane = channel, warp w = rows w, w + 8, ..
-    __nv_bfloat16* dlg = static_cast<__nv_bfloat16*>(p.da);
-    for (int cb0 = 0; cb0 < Dk; cb0 += CB) {
-        load_block(d, p, bb, h, j, t0, nvalid, cb0, on, rqs, rks, qb, kb, Gm);
-        {
-            const int t = tid >> 2, i0 = (tid & 3) * 8;
-            const float* src = p.wb + (rowbase + t) * Dk + cb0 + i0;
-            const float4 a = reinterpret_cast<const float4*>(src)[0], b = reinterpret_cast<const float4*>(src)[1];
-            const float w8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-            for (int u = 0; u < 8; ++u) Wk[t * LB + i0 + u] = w8[u];
+    {  // Gbar = diag(beta) Abar over M1's place
+        float* gb = p.m1 + ci * C * C;
+        for (int e = tid; e < C * C; e += kThreads) {
+            const int t = e / C, s = e % C;
+            gb[e] = bt[t] * Mm[t * LDT + s];
         }
-        for (int e = tid; e < 96 * CB; e += kThreads) {
-            const int row = e / CB, i = e % CB;
-            const int J = row < 48 ? 0 : row < 80 ? 1 : 2;
-            const int t = J == 0 ? 16 + row : J == 1 ? 32 + (row - 48) : 48 + (row - 80);
-            Fm[row * LB + i] = expf(Gm[t * LB + i] - Gm[(16 * J + 15) * LB + i]);
-        }
-        for (int e = tid; e < 48 * CB; e += kThreads) {
-            const int s = e / CB, i = e % CB, b = s | 15;
-            Rm[s * LB + i] = kb[s * LB + i] * expf(Gm[b * LB + i] - Gm[s * LB + i]);
-        }
-        __syncthreads();
-        const int i = lane;
-        float colK = 0.f;
-        for (int rr = 0; rr < 8; ++rr) {
-            const int r = warp + 8 * rr, I = r >> 4;
-            const float g_r = Gm[r * LB + i], k_r = kb[r * LB + i], q_r = qb[r * LB + i];
-            float kr = 0.f;
-            for (int u = r; u < C; ++u) kr = fmaf(Tm[u * LDT + r], Wk[u * LB + i], kr);
-            kr *= bt[r];
-            // left sums: off-diagonal blocks through the pivots, then the diagonal block
-            float LG = 0.f, LP = 0.f;
-            for (int J = 0; J < I; ++J) {
-                float sG = 0.f, sP = 0.f;
-#pragma unroll 4
-                for (int s = 16 * J; s < 16 * J + 16; ++s) {
-                    const float rs = Rm[s * LB + i];
-                    sG = fmaf(Gbar[r * LDT + s], rs, sG);
-                    sP = fmaf(Pb[r * LDT + s], rs, sP);
-                }
-                const float fo = Fm[frow(J, r) * LB + i];
-                LG = fmaf(fo, sG, LG);
-                LP = fmaf(fo, sP, LP);
-            }
-            for (int s = 16 * I; s <= r; ++s) {
-                const float ks = kb[s * LB + i] * expf(g_r - Gm[s * LB + i]);
-                if (s < r) LG = fmaf(Gbar[r * LDT + s], ks, LG);
-                LP = fmaf(Pb[r * LDT + s], ks, LP);
-            }
-            // right sums (r as the column)
-            float RG = 0.f, RP = 0.f;
-            if (I < 3) {
-                const int b = 16 * I + 15;
-                float sG = 0.f, sP = 0.f;
-                for (int t = b + 1; t < C; ++t) {
-                    const float ft = Fm[frow(I, t) * LB + i];
-                    sG = fmaf(Gbar[t * LDT + r], kb[t * LB + i] * ft, sG);
-                    sP = fmaf(Pb[t * LDT + r], qb[t * LB + i] * ft, sP);
-                }
-                const float fr = expf(Gm[b * LB + i] - g_r);
-                RG = fr * sG;
-                RP = fr * sP;
-            }
-            for (int t = r; t < 16 * I + 16; ++t) {
-                const float e = expf(Gm[t * LB + i] - g_r);
-                if (t > r) RG = fmaf(Gbar[t * LDT + r], kb[t * LB + i] * e, RG);
-                RP = fmaf(Pb[t * LDT + r], qb[t * LB + i] * e, RP);
-            }
-            const float E = expf(g_r), ed = expf(Gm[(C - 1) * LB + i] - g_r);
-            const int64_t gi = (rowbase + r) * Dk + cb0 + i;
-            const float qrb = p.qrb[gi], kdb = p.kdb[gi];
-            const float Kd = k_r * ed;
-            p.dqh[gi] = fmaf(qrb, E, LP);
-            p.dkh[gi] = kr * E + kdb * ed + LG + RG + RP;
-            Gb[r * LB + i] = qrb * q_r * E + kr * k_r * E - kdb * Kd + q_r * LP + k_r * (LG - RG - RP);
-            colK = fmaf(kdb, Kd, colK);
-        }
-        red[warp * CB + i] = colK;
-        __syncthreads();
-        if (tid < CB) {  // Gammabar_63: the K_d column sums (warp order) and the state decay
-            float tot = 0.f;
-            for (int w = 0; w < kThreads / 32; ++w) tot += red[w * CB + tid];
-            Gb[(C - 1) * LB + tid] += tot + p.ecb[ci * Dk + cb0 + tid] * expf(Gm[(C - 1) * LB + tid]);
-        }
-        __syncthreads();
-        {  // lbar: sums of Gammabar from the end of the chunk; warp w takes rows 8 w .. 8 w + 7
-            float part = 0.f;
-            for (int t = 8 * warp; t < 8 * warp + 8; ++t) part += Gb[t * LB + i];
-            red[warp * CB + i] = part;
-            __syncthreads();
-            float acc = 0.f;
-            for (int w = kThreads / 32 - 1; w > warp; --w) acc += red[w * CB + i];
-            for (int t = 8 * warp + 7; t >= 8 * warp; --t) {
-                acc += Gb[t * LB + i];
-                if (t < nvalid)
-                    dlg[(((int64_t)bb * d.T + t0 + t) * d.Hv + h) * Dk + cb0 + i] =
-                        __float2bfloat16_rn(on[t] != 0.f ? acc : 0.f);
-            }
-        }
-        __syncthreads();
     }
 }
+
+// Kernel 3: one CTA per (chunk, 32-channel block, value head, batch), 256
+// threads, CUDA cores, two CTAs per SM.  Thread (warp w, lane i) takes channel
+// i of the row quads w and w + 8: the four rows share every load of a column
+// value, and the rows of Gbar / Pbar come as 16-byte loads.
+__global__ void __launch_bounds__(kThreads, 2) kc_bwd_chan_kernel(Dims d, Ptrs p) {
+    extern __shared__ __align__(16) uint8_t lsm[];
+    const int nblk = (int)d.Dk / CB;
+    const int c = blockIdx.x / nblk, cb0 = (blockIdx.x % nblk) * CB;
+    const int h = blockIdx.y, bb = blockIdx.z;
+    const int j = h / (int)d.G;
+    const int Dk = (int)d.Dk;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    float* Pb = reinterpret_cast<float*>(lsm);
+    float* Gg = Pb + C * LDT;
+    float* qb = Gg + C * LDT;
+    float* kb = qb + C * LB;
+    float* Gm = kb + C * LB;
+    float* Gb = Gm + C * LB;
+    float* Fm = Gb + C * LB;   // [96][LB]
+    float* Rm = Fm + 96 * LB;  // [48][LB]
+    float* part = Rm + 48 * LB;  // [8][CB]
+    float* bt = part + 8 * CB;
+    float* on = bt + C;
+    float* rqs = on + C;
+    float* rks = rqs + C;
+    const int64_t t0 = (int64_t)c * C;
+    const int nvalid = (int)(d.T - t0 < C ? d.T - t0 : C);
+    const int64_t bh = (int64_t)bb * d.Hv + h;
+    const int64_t ci = bh * d.NC + c;
+    const int64_t rowbase = bh * d.Tp + t0;
+
+    chunk_vectors(d, p, bb, h, j, t0, nvalid, bt, on, rqs, rks);
+    {
+        const float* pg = p.pbm + ci * C * C;
+        const float* gg = p.m1 + ci * C * C;
+        for (int e = tid; e < C * C / 4; e += kThreads) {
+            const int t = e / (C / 4), s0 = (e % (C / 4)) * 4;
+            *reinterpret_cast<float4*>(Pb + t * LDT + s0) = reinterpret_cast<const float4*>(pg)[e];
+            *reinterpret_cast<float4*>(Gg + t * LDT + s0) = reinterpret_cast<const float4*>(gg)[e];
+        }
+    }
+    __syncthreads();
+    load_block<true>(d, p, bb, h, j, t0, nvalid, cb0, on, rqs, rks, qb, kb, Gm, part);
+    for (int e = tid; e < 96 * CB; e += kThreads) {
+        const int row = e / CB, i = e % CB;
+        const int J = row < 48 ? 0 : row < 80 ? 1 : 2;
+        const int t = J == 0 ? 16 + row : J == 1 ? 32 + (row - 48) : 48 + (row - 80);
+        Fm[row * LB + i] = expf(Gm[t * LB + i] - Gm[(16 * J + 15) * LB + i]);
+    }
+    for (int e = tid; e < 48 * CB; e += kThreads) {
+        const int s = e / CB, i = e % CB, b = s | 15;
+        Rm[s * LB + i] = kb[s * LB + i] * expf(Gm[b * LB + i] - Gm[s * LB + i]);
+    }
+    __syncthreads();
+
+    const int i = lane;
+    float colK = 0.f;
+    for (int it = 0; it < 2; ++it) {
+        const int g = warp + 8 * it, r0 = 4 * g, I = g >> 2;
+        float gr[4], qrb[4], kdb[4], krb[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int64_t gi = (rowbase + r0 + a) * Dk + cb0 + i;
+            qrb[a] = p.qrb[gi];
+            kdb[a] = p.kdb[gi];
+            krb[a] = p.wb[gi];
+            gr[a] = Gm[(r0 + a) * LB + i];
+        }
+        float LG[4] = {0.f, 0.f, 0.f, 0.f}, LP[4] = {0.f, 0.f, 0.f, 0.f};
+        float RG[4] = {0.f, 0.f, 0.f, 0.f}, RP[4] = {0.f, 0.f, 0.f, 0.f};
+        // left sums, off the diagonal block: per pivot block J < I
+        for (int J = 0; J < I; ++J) {
+            float sG[4] = {0.f, 0.f, 0.f, 0.f}, sP[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int s = 16 * J; s < 16 * J + 16; s += 4) {
+                const float rs[4] = {Rm[s * LB + i], Rm[(s + 1) * LB + i], Rm[(s + 2) * LB + i],
+                                     Rm[(s + 3) * LB + i]};
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    const float4 g4 = *reinterpret_cast<const float4*>(Gg + (r0 + a) * LDT + s);
+                    const float4 p4 = *reinterpret_cast<const float4*>(Pb + (r0 + a) * LDT + s);
+                    sG[a] = fmaf(g4.x, rs[0], fmaf(g4.y, rs[1], fmaf(g4.z, rs[2], fmaf(g4.w, rs[3], sG[a]))));
+                    sP[a] = fmaf(p4.x, rs[0], fmaf(p4.y, rs[1], fmaf(p4.z, rs[2], fmaf(p4.w, rs[3], sP[a]))));
+                }
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const float fo = Fm[frow(J, r0 + a) * LB + i];
+                LG[a] = fmaf(fo, sG[a], LG[a]);
+                LP[a] = fmaf(fo, sP[a], LP[a]);
+            }
+        }
+        // left sums on the diagonal block
+        for (int s = 16 * I; s <= r0 + 3; ++s) {
+            const float ks0 = kb[s * LB + i], gs = Gm[s * LB + i];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                if (s <= r0 + a) {
+                    const float ks = ks0 * expf(gr[a] - gs);
+                    if (s < r0 + a) LG[a] = fmaf(Gg[(r0 + a) * LDT + s], ks, LG[a]);
+                    LP[a] = fmaf(Pb[(r0 + a) * LDT + s], ks, LP[a]);
+                }
+            }
+        }
+        // right sums (the rows as columns s), off the diagonal block
+        if (I < 3) {
+            const int b = 16 * I + 15;
+            float sG[4] = {0.f, 0.f, 0.f, 0.f}, sP[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int t = b + 1; t < C; ++t) {
+                const float ft = Fm[frow(I, t) * LB + i];
+                const float kt = kb[t * LB + i] * ft, qt = qb[t * LB + i] * ft;
+                const float4 g4 = *reinterpret_cast<const float4*>(Gg + t * LDT + r0);
+                const float4 p4 = *reinterpret_cast<const float4*>(Pb + t * LDT + r0);
+                sG[0] = fmaf(g4.x, kt, sG[0]);
+                sG[1] = fmaf(g4.y, kt, sG[1]);
+                sG[2] = fmaf(g4.z, kt, sG[2]);
+                sG[3] = fmaf(g4.w, kt, sG[3]);
+                sP[0] = fmaf(p4.x, qt, sP[0]);
+                sP[1] = fmaf(p4.y, qt, sP[1]);
+                sP[2] = fmaf(p4.z, qt, sP[2]);
+                sP[3] = fmaf(p4.w, qt, sP[3]);
+            }
+            const float gb = Gm[b * LB + i];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const float fr = expf(gb - gr[a]);
+                RG[a] = fr * sG[a];
+                RP[a] = fr * sP[a];
+            }
+        }
+        // right sums on the diagonal block
+        for (int t = r0; t < 16 * I + 16; ++t) {
+            const float gt = Gm[t * LB + i], kt0 = kb[t * LB + i], qt0 = qb[t * LB + i];
+            const float4 g4 = *reinterpret_cast<const float4*>(Gg + t * LDT + r0);
+            const float4 p4 = *reinterpret_cast<const float4*>(Pb + t * LDT + r0);
+            const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, pv[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                if (t >= r0 + a) {
+                    const float e = expf(gt - gr[a]);
+                    if (t > r0 + a) RG[a] = fmaf(gv[a], kt0 * e, RG[a]);
+                    RP[a] = fmaf(pv[a], qt0 * e, RP[a]);
+                }
+            }
+        }
+        const float g63 = Gm[(C - 1) * LB + i];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int r = r0 + a;
+            const float k_r = kb[r * LB + i], q_r = qb[r * LB + i];
+            const float E = expf(gr[a]), ed = expf(g63 - gr[a]);
+            const int64_t gi = (rowbase + r) * Dk + cb0 + i;
+            const float Kd = k_r * ed;
+            p.dqh[gi] = fmaf(qrb[a], E, LP[a]);
+            p.dkh[gi] = krb[a] * E + kdb[a] * ed + LG[a] + RG[a] + RP[a];
+            Gb[r * LB + i] = qrb[a] * q_r * E + krb[a] * k_r * E - kdb[a] * Kd + q_r * LP[a] +
+                             k_r * (LG[a] - RG[a] - RP[a]);
+            colK = fmaf(kdb[a], Kd, colK);
+        }
+    }
+    part[warp * CB + i] = colK;
+    __syncthreads();
+    if (tid < CB) {  // Gammabar_63: the K_d column sums (warp order) and the state decay
+        float tot = 0.f;
+        for (int w = 0; w < kThreads / 32; ++w) tot += part[w * CB + tid];
+        Gb[(C - 1) * LB + tid] += tot + p.ecb[ci * Dk + cb0 + tid] * expf(Gm[(C - 1) * LB + tid]);
+    }
+    __syncthreads();
+    // lbar: sums of Gammabar from the end of the chunk; warp w takes rows 8 w .. 8 w + 7
+    float piece = 0.f;
+    for (int t = 8 * warp; t < 8 * warp + 8; ++t) piece += Gb[t * LB + i];
+    part[warp * CB + i] = piece;
+    __syncthreads();
+    float acc = 0.f;
+    for (int w = kThreads / 32 - 1; w > warp; --w) acc += part[w * CB + i];
+    __nv_bfloat16* dlg = static_cast<__nv_bfloat16*>(p.da);
+    for (int t = 8 * warp + 7; t >= 8 * warp; --t) {
+        acc += Gb[t * LB + i];
+        if (t < nvalid)
+            dlg[(((int64_t)bb * d.T + t0 + t) * d.Hv + h) * Dk + cb0 + i] = __float2bfloat16_rn(on[t] != 0.f ? acc : 0.f);
+    }
+}
+
+inline size_t kc_gate_smem() { return 3 * kBlkMat + 4 * kBlkArr + (8 * CB + 5 * C) * 4; }
+inline size_t kc_chan_smem() { return 2 * kBlkMat + 4 * kBlkArr + (96 + 48) * LB * 4 + (8 * CB + 4 * C) * 4; }
+
 }  // namespace
 
 bool kc_chunked_supported(const Dims& d) {
@@ -927,13 +1051,20 @@ cudaError_t launch_kc_bwd_prod(const Dims& d, const Ptrs& p, cudaStream_t s) {
     return cudaPeekAtLastError();
 }
 
-cudaError_t launch_kc_bwd_local(const Dims& d, const Ptrs& p, cudaStream_t s) {
-    const size_t smem = kl_plan().total;
-    auto kern = kc_bwd_local_kernel;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+cudaError_t launch_kc_bwd_gate(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    auto kern = kc_bwd_gate_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kc_gate_smem());
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)d.NC, (unsigned)d.Hv, (unsigned)d.B);
-    kern<<<grid, kThreads, smem, s>>>(d, p);
+    kern<<<dim3((unsigned)d.NC, (unsigned)d.Hv, (unsigned)d.B), kThreads, kc_gate_smem(), s>>>(d, p);
+    count_launches(1);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_kc_bwd_chan(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    auto kern = kc_bwd_chan_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kc_chan_smem());
+    if (e != cudaSuccess) return e;
+    kern<<<dim3((unsigned)(d.NC * (d.Dk / CB)), (unsigned)d.Hv, (unsigned)d.B), kThreads, kc_chan_smem(), s>>>(d, p);
     count_launches(1);
     return cudaPeekAtLastError();
 }

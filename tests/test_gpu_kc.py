@@ -121,7 +121,7 @@ def test_kc_chunked_form(B, T, Hk, Hv, Dk, mask):
     w = wl.custom("kcch", B, T, Hk, Hv, Dk, 128, dtype=torch.bfloat16, seed=650 + T + Dk,
                   mask=mask)
     phases = _parity(w, seed=651 + T + Dk)
-    for name in ("kc_chunk", "kc_scan", "kc_bwd_scan", "kc_bwd_prod", "kc_bwd_local"):
+    for name in ("kc_chunk", "kc_scan", "kc_bwd_scan", "kc_bwd_prod", "kc_bwd_gate", "kc_bwd_chan"):
         assert name in phases
     assert "kc_fwd" not in phases and "kc_bwd" not in phases
 
