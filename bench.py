@@ -154,22 +154,24 @@ def method_model(w, gates="ab", nseg=1, nseg_bwd=1, conv_k=0, rank=0, iters=3):
         # checkpoints per 64-step chunk as for the scalar gates.  The chunked
         # form (bf16 at the tensor-core scans' shapes): the scalar form's flops
         # with no Gram shared between value heads (each has its own decays);
-        # the gradient phase split into its Dv-long products (the three state
-        # products, Pbar, Dbar V^T, T^T Dbar: 6 Dk Dv + 6 C Dv) and the rest.
+        # the gradient phase split into the tensor-core products (the three state
+        # products, Pbar, Dbar V^T, T^T Dbar, Wbar K_r^T, T^T Wbar:
+        # 6 Dk Dv + 6 C Dv + 3 C Dk), the 64 x 64 gate products (2 C^2) and the
+        # decayed-Gram sums (the rest).
         # The recurrent form (other shapes): per step forward decay, prediction,
         # update and read-out (7 Dk Dv), backward the recompute and the reverse
         # step (20 Dk Dv).
         gin = B * T * Hv * (Dk + 1) * es
         fk_chunk = th * (2 * C * (3 * Dk + 2 * Dv) + C * C / 3)
         fk_bwd = th * (18 * C * Dk + 10 * C * Dv + 14 * Dk * Dv + 4 * C * C)
-        fk_prod = th * (6 * Dk * Dv + 6 * C * Dv)
+        fk_prod = th * (6 * Dk * Dv + 6 * C * Dv + 3 * C * Dk)
         m["prep"] = dict(flops=0.0, bytes=qk)
         m["kc_chunk"] = dict(flops=fk_chunk, bytes=qk + vv + gin)
         m["kc_scan"] = dict(flops=f_scan, bytes=st + vv + st + ckpt)
         m["kc_bwd_scan"] = dict(flops=f_bscan, bytes=vv + st + st)
         m["kc_bwd_prod"] = dict(flops=fk_prod, bytes=ckpt + 3 * vv)
-        fk_gate = th * (3 * C * Dk + 2 * C * C)
-        m["kc_bwd_gate"] = dict(flops=fk_gate, bytes=qk / 2 + gin + B * T * Hv * es)
+        fk_gate = th * 2 * C * C
+        m["kc_bwd_gate"] = dict(flops=fk_gate, bytes=2 * B * T * Hv * es)
         m["kc_bwd_chan"] = dict(flops=fk_bwd - f_bscan - fk_prod - fk_gate,
                                 bytes=qk + gin + B * T * Hv * Dk * es)
         m["kc_fwd"] = dict(flops=7.0 * th * Dk * Dv, bytes=qk + vv + gin + vv + 2 * st + ckpt)
@@ -284,7 +286,7 @@ def design_model(w, conv_k=0, gates="ab", nseg=1, nseg_bwd=1):
         io_in = 2 * B * T * Hk * Dk * es + B * T * Hv * Dv * es + gin
         tok = B * T * Hv
         m["prep"] = dict(flops=0.0, bytes=2 * B * T * Hk * Dk * es + 2 * BHk * Tp * 4)
-        # chunked form: per (b, h, chunk) the Q_r, K_d and W images, P and T
+        # chunked form: per (b, h, chunk) the Q_r, K_d, K_r and W images, P and T
         # images, U (fp32), e_C and the decayed Gram (fp32) out of the chunk
         # kernel; the scans read them as the scalar scans do; the tensor-core
         # gradient pass writes Kbar_d, Qbar_r, Wbar (fp32 rows), Pbar and M1
@@ -292,7 +294,7 @@ def design_model(w, conv_k=0, gates="ab", nseg=1, nseg_bwd=1):
         # and turns into fp32 per-value-head q / k cotangents
         m["kc_chunk"] = dict(
             flops=units * (6 * C * C * Dk + 2 * C * C * Dv + C ** 3 / 3),
-            bytes=io_in + units * (3 * C * Dk * es + 2 * C * C * es + C * Dv * 4 + Dk * 4 + C * C * 4))
+            bytes=io_in + units * (4 * C * Dk * es + 2 * C * C * es + C * Dv * 4 + Dk * 4 + C * C * 4))
         m["kc_scan"] = dict(
             flops=units * (6 * C * Dk * Dv + 2 * C * C * Dv),
             bytes=units * (3 * C * Dk * es + C * C * es + C * Dv * 4 + Dk * 4 + Dk * Dv * img
@@ -302,17 +304,16 @@ def design_model(w, conv_k=0, gates="ab", nseg=1, nseg_bwd=1):
             bytes=units * (C * Dv * es + C * C * es + 3 * C * Dk * es + Dk * 4 + Dk * Dv * img
                            + C * Dv * img) + 2 * BH * Dk * Dv * 4)
         m["kc_bwd_prod"] = dict(
-            flops=units * (6 * C * Dk * Dv + 6 * C * C * Dv),
+            flops=units * (6 * C * Dk * Dv + 6 * C * C * Dv + 3 * C * C * Dk),
             bytes=units * (2 * C * Dv * es + C * Dv * 4 + C * Dv * img + C * C * img + 2 * Dk * Dv * img
-                           + 2 * C * C * 4 + C * Dv * es + 3 * C * Dk * 4 + Dk * 4))
-        # the gate pass reads k, the gates, T, M1, G and Wbar and writes Kbar_r
-        # over Wbar, Gbar over M1 and the beta cotangent; the channel pass reads
-        # q, k, the gates, Pbar, Gbar, Qbar_r, Kbar_d, Kbar_r, ebar and writes the
-        # fp32 per-value-head q / k cotangents and the log-decay cotangent
+                           + C * Dk * es + 3 * C * C * 4 + C * Dv * es + 3 * C * Dk * 4 + Dk * 4))
+        # the gate pass reads beta, T, M and G and writes Gbar over M and the
+        # beta cotangent; the channel pass reads q, k, the gates, Pbar, Gbar,
+        # Qbar_r, Kbar_d, Kbar_r, ebar and writes the fp32 per-value-head q / k
+        # cotangents and the log-decay cotangent
         m["kc_bwd_gate"] = dict(
-            flops=units * (3 * C * C * Dk + 4 * C ** 3 / 3),
-            bytes=B * T * Hk * Dk * es + gin + units * (C * C * img + 3 * C * C * 4 + 2 * C * Dk * 4)
-            + B * T * Hv * es)
+            flops=units * 4 * C ** 3 / 3,
+            bytes=2 * B * T * Hv * es + units * (C * C * img + 3 * C * C * 4))
         m["kc_bwd_chan"] = dict(
             flops=units * 10 * C * C * Dk,
             bytes=2 * B * T * Hk * Dk * es + gin + units * (2 * C * C * 4 + 5 * C * Dk * 4 + Dk * 4)

@@ -799,11 +799,11 @@ struct KcLayout {
     bool chunked;
     // recurrent form
     size_t ckpt, rq, rk, dqh, dkh, gpart, bpart;
-    // chunked form, saved: checkpoints, Delta, W, P, T, Q_r, K_d images, e_C, the
+    // chunked form, saved: checkpoints, Delta, W, P, T, Q_r, K_d, K_r images, e_C, the
     // decayed k Gram (and rq, rk above); forward workspace: U, then room for the
     // saved tensors when the caller keeps none; backward workspace: the reverse
     // scan's images, the q / k partials, the tensor-core pass's products
-    size_t Delta, W, P, Tinv, qimg, kimg, ecd, gram, U, fwd_saved;
+    size_t Delta, W, P, Tinv, qimg, kimg, krimg, ecd, gram, U, fwd_saved;
     size_t dSck, Dbar, kdb, qrb, wb, pbm, m1, ecb;
     size_t saved_total, fwd_total, bwd_total;
 };
@@ -825,6 +825,7 @@ gdn_status kc_layout(const gdn_shape* shape, gdn::Dims* d, KcLayout* L) {
         L->Tinv = o; o = align_up(o + mat * 2);
         L->qimg = o; o = align_up(o + rowsk * 2);
         L->kimg = o; o = align_up(o + rowsk * 2);
+        L->krimg = o; o = align_up(o + rowsk * 2);
         L->ecd = o; o = align_up(o + BH * d->NC * d->Dk * 4);
         L->gram = o; o = align_up(o + mat * 4);
         L->rq = o; o = align_up(o + (size_t)d->B * d->Hk * d->Tp * 4);
@@ -874,6 +875,7 @@ void carve_kc_saved(const KcLayout& L, void* saved, gdn::Ptrs* p) {
     p->Tinv = reinterpret_cast<float*>(s + L.Tinv);
     p->qimg = s + L.qimg;
     p->kimg = s + L.kimg;
+    p->krimg = s + L.krimg;
     p->ecd = reinterpret_cast<float*>(s + L.ecd);
     p->gram = reinterpret_cast<float*>(s + L.gram);
     p->rq = reinterpret_cast<float*>(s + L.rq);

@@ -107,14 +107,16 @@ struct Ptrs {
     float* part;   // [2, B, NC, Hv] per-chunk partial sums for dA_log, ddt_bias
     float* ecd;    // per-key-channel chunked form: [B, Hv, NC, Dk] exp(Gamma_63, i) of
                    // each chunk and key channel i (the state's per-chunk decay)
+    void* krimg;   // per-key-channel chunked form: [B, Hv, NC] panel images of
+                   // K_r = kh o exp(Gamma) (64 rows x Dk), bf16
     float* gram;   // per-key-channel chunked form: [B, Hv, NC, 64, 64] the decayed
                    // Gram sum_i kh_ti kh_si exp(Gamma_ti - Gamma_si), s < t (fp32)
     // per-key-channel chunked backward: per-chunk products of the tensor-core pass
     float* kdb;    // [B, Hv, Tp, Dk] Delta Sbar'^T       (cotangent of K_d)
     float* qrb;    // [B, Hv, Tp, Dk] Obar S^T             (cotangent of Q_r)
-    float* wb;     // [B, Hv, Tp, Dk] -Dbar S^T            (cotangent of W)
+    float* wb;     // [B, Hv, Tp, Dk] diag(beta) T^T Wbar  (cotangent of K_r)
     float* pbm;    // [B, Hv, NC, 64, 64] Obar Delta^T, lower incl. diagonal
-    float* m1;     // [B, Hv, NC, 64, 64] Dbar V^T
+    float* m1;     // [B, Hv, NC, 64, 64] Dbar V^T + Wbar K_r^T, then Gbar
     float* ecb;    // [B, Hv, NC, Dk] <Sbar'_i, S_i> per key channel i
     unsigned int* sched;  // tensor-core path: [1 + B Hv] the gradient kernel's item
                           // counter, then the reverse scan's per-(b, h) progress

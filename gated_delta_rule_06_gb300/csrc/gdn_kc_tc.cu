@@ -17,7 +17,8 @@
 // over- or underflows for strong decays.  Off the diagonal 16 x 16 blocks it is
 // the product of exp(Gamma_ti - Gamma_bi) and exp(Gamma_bi - Gamma_si) through
 // the last step b of the block of s, both in (0, 1]; on the diagonal blocks
-// every term takes its own exponential.
+// every term takes its own exponential.  Exponentials use the fast intrinsic
+// (a few ulp; the arguments are never positive).
 //
 // This file: the chunk-local forward products (CUDA cores, fp32), then the
 // per-chunk gradients (see the backward section below).  The scans are the KC
@@ -96,8 +97,9 @@ __device__ __forceinline__ void st4(float* p, float a, float b, float c, float e
 
 // One CTA per (chunk, value head, batch).  p.a = log_decay [B, T, Hv, Dk], p.b =
 // beta [B, T, Hv] (bf16); rq, rk from prep.  Writes the panel images of Q_r, K_d
-// (p.qimg, p.kimg, per value head), P, T, W, the fp32 rows of U, e_C (p.ecd) and
-// the decayed Gram of the k rows (p.gram, for the beta cotangent).
+// (p.qimg, p.kimg, per value head), K_r = kh o E (p.krimg), P, T, W, the fp32
+// rows of U, e_C (p.ecd) and the decayed Gram of the k rows (p.gram, for the
+// beta cotangent).
 __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
     extern __shared__ __align__(16) uint8_t ksm[];
     const int c = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
@@ -172,29 +174,35 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
     // and the right factors kh_s exp(Gamma_b - Gamma_s) of the off-diagonal blocks
     uint8_t* qr_img = static_cast<uint8_t*>(p.qimg) + ci * C * Dk * 2;
     uint8_t* kd_img = static_cast<uint8_t*>(p.kimg) + ci * C * Dk * 2;
+    uint8_t* kr_img = static_cast<uint8_t*>(p.krimg) + ci * C * Dk * 2;
     for (int e = tid; e < C * cpr; e += kThreads) {
         const int t = e % C, i0 = (e / C) * 8;
-        float a[8], b[8];
+        float a[8], b[8], kr[8];
 #pragma unroll
         for (int u = 0; u < 8; u += 4) {
             const float4 g = ld4(Gf + t * LD + i0 + u), gl = ld4(Gf + (C - 1) * LD + i0 + u);
             const float4 qq = ld4(qf + t * LD + i0 + u), kk = ld4(kf + t * LD + i0 + u);
-            a[u] = qq.x * expf(g.x);
-            a[u + 1] = qq.y * expf(g.y);
-            a[u + 2] = qq.z * expf(g.z);
-            a[u + 3] = qq.w * expf(g.w);
-            b[u] = kk.x * expf(gl.x - g.x);
-            b[u + 1] = kk.y * expf(gl.y - g.y);
-            b[u + 2] = kk.z * expf(gl.z - g.z);
-            b[u + 3] = kk.w * expf(gl.w - g.w);
+            a[u] = qq.x * __expf(g.x);
+            a[u + 1] = qq.y * __expf(g.y);
+            a[u + 2] = qq.z * __expf(g.z);
+            a[u + 3] = qq.w * __expf(g.w);
+            b[u] = kk.x * __expf(gl.x - g.x);
+            b[u + 1] = kk.y * __expf(gl.y - g.y);
+            b[u + 2] = kk.z * __expf(gl.z - g.z);
+            b[u + 3] = kk.w * __expf(gl.w - g.w);
+            kr[u] = kk.x * __expf(g.x);
+            kr[u + 1] = kk.y * __expf(g.y);
+            kr[u + 2] = kk.z * __expf(g.z);
+            kr[u + 3] = kk.w * __expf(g.w);
         }
         st_bf16x8(qr_img + 16 * e, a);
         st_bf16x8(kd_img + 16 * e, b);
+        st_bf16x8(kr_img + 16 * e, kr);
     }
-    for (int i = tid; i < Dk; i += kThreads) p.ecd[ci * Dk + i] = expf(Gf[(C - 1) * LD + i]);
+    for (int i = tid; i < Dk; i += kThreads) p.ecd[ci * Dk + i] = __expf(Gf[(C - 1) * LD + i]);
     for (int e = tid; e < 48 * Dk; e += kThreads) {
         const int s = e / Dk, i = e % Dk, b = s | 15;
-        Rt[i * kRS + s] = kf[s * LD + i] * expf(Gf[b * LD + i] - Gf[s * LD + i]);
+        Rt[i * kRS + s] = kf[s * LD + i] * __expf(Gf[b * LD + i] - Gf[s * LD + i]);
     }
     __syncthreads();
 
@@ -211,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
         for (int i = 0; i < Dk; i += 4) {
             const float4 kt = ld4(kf + t * LD + i), qt = ld4(qf + t * LD + i);
             const float4 gt = ld4(Gf + t * LD + i), gb = ld4(Gf + b * LD + i);
-            const float u[4] = {expf(gt.x - gb.x), expf(gt.y - gb.y), expf(gt.z - gb.z), expf(gt.w - gb.w)};
+            const float u[4] = {__expf(gt.x - gb.x), __expf(gt.y - gb.y), __expf(gt.z - gb.z), __expf(gt.w - gb.w)};
             const float ka[4] = {kt.x * u[0], kt.y * u[1], kt.z * u[2], kt.w * u[3]};
             const float qa[4] = {qt.x * u[0], qt.y * u[1], qt.z * u[2], qt.w * u[3]};
 #pragma unroll
@@ -250,8 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
                 if (x <= n) {
                     const int sr = 16 * I + x;
                     const float4 ks = ld4(kf + sr * LD + i), gs = ld4(Gf + sr * LD + i);
-                    const float e0 = ks.x * expf(gt.x - gs.x), e1 = ks.y * expf(gt.y - gs.y);
-                    const float e2 = ks.z * expf(gt.z - gs.z), e3 = ks.w * expf(gt.w - gs.w);
+                    const float e0 = ks.x * __expf(gt.x - gs.x), e1 = ks.y * __expf(gt.y - gs.y);
+                    const float e2 = ks.z * __expf(gt.z - gs.z), e3 = ks.w * __expf(gt.w - gs.w);
                     ad[x] = fmaf(kt.x, e0, fmaf(kt.y, e1, fmaf(kt.z, e2, fmaf(kt.w, e3, ad[x]))));
                     pd[x] = fmaf(qt.x, e0, fmaf(qt.y, e1, fmaf(qt.z, e2, fmaf(qt.w, e3, pd[x]))));
                 }
@@ -301,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
     // beta (kh o E) in place of kh, beta V in region R
     for (int e = tid; e < C * Dk; e += kThreads) {
         const int s = e / Dk, i = e % Dk;
-        kf[s * LD + i] *= bt[s] * expf(Gf[s * LD + i]);
+        kf[s * LD + i] *= bt[s] * __expf(Gf[s * LD + i]);
     }
     float* Vb = Rt;
     for (int e = tid; e < C * (Dv / 8); e += kThreads) {
@@ -368,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
 // cotangent of Delta), Delta (hi + lo images) and Obar:
 //   Kbar_d = Delta Sbar'^T,  Qbar_r = Obar S^T,  Wbar = -Dbar S^T,
 //   ebar_i = <Sbar'_i, S_i>,  Pbar = Obar Delta^T (s <= t),  M1 = Dbar V^T,
-//   dv = diag(beta) T^T Dbar,  M2 = Wbar (kh o E)^T,  Tbar = (M1 + M2) diag(beta),
+//   dv = diag(beta) T^T Dbar,  M2 = Wbar K_r^T (K_r = kh o E),  Tbar = (M1 + M2) diag(beta),
 //   Abar = -T^T Tbar T^T (s < t),  Gbar = diag(beta) Abar,  Kbar_r = diag(beta) T^T Wbar,
 //   betabar_t = sum_u T_ut (M1 + M2)_ut + sum_{s < t} Abar_ts G_ts,
 // then, per key channel with e_ts = exp(Gamma_t - Gamma_s), the sums through
@@ -383,10 +391,12 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
 //   Gammabar_63 += sum_t Kbar_d o K_d + ebar o e_C,
 //   lbar_t = sum_{u >= t} Gammabar_u  (applied steps; 0 elsewhere).
 // Kernel 1 (tensor cores) forms the products whose sums run over the Dv value
-// columns; kernel 2 (CUDA cores, fp32) the rest, 32 key channels at a time.
+// columns, and M2 and Kbar_r (Wbar staged as a bf16 operand); kernel 2 (CUDA
+// cores, fp32) Abar, Gbar and the beta cotangent per chunk; kernel 3 (CUDA
+// cores, fp32) the decayed-Gram sums, 32 key channels at a time.
 
 struct KpSmem {
-    uint32_t O, V, D, Dlo, ND, Tt, S, Sp, total;
+    uint32_t O, V, D, Dlo, ND, Tt, S, Sp, Kr, Wt, total;
 };
 __host__ __device__ inline KpSmem kp_plan(int Dv) {
     KpSmem s{};
@@ -405,6 +415,8 @@ __host__ __device__ inline KpSmem kp_plan(int Dv) {
     s.Tt = take(C * C * 2);
     s.S = take(tv);   // one 64-channel block of the S^T image (Dv rows)
     s.Sp = take(tv);  // and of the Sbar'^T image
+    s.Kr = take(C * 64 * 2);  // the block's 64 channels of the K_r image (panel, 64 rows)
+    s.Wt = take(C * 64 * 2);  // Wbar of the block as a bf16 operand (canonical, x = channel)
     s.total = o;
     return s;
 }
@@ -457,10 +469,12 @@ __device__ __forceinline__ void step_gate(const Dims& d, const Ptrs& p, int bb, 
     *on = live ? 1.f : 0.f;
 }
 
-// Kernel 1: one CTA per (chunk, value head, batch), 256 threads, 256 TMEM
+// Kernel 1: one CTA per (chunk, value head, batch), 256 threads, all 512 TMEM
 // columns.  Products: Pbar (cols 0..63), -M1 (64..127), -T^T Dbar (128..) from
-// dO, v (TMA tiles), Delta, -Dbar and T images; then per 64-channel block of S
-// and Sbar': Kbar_d (0..63), Qbar_r (64..127), Wbar (128..191), and ebar.
+// dO, v (TMA tiles), Delta, -Dbar and T images; then per 64-channel block of S,
+// Sbar' and K_r: Kbar_d (0..63), Qbar_r (64..127), Wbar (128..191) and ebar;
+// Wbar as a bf16 tile, then Kbar_r = T^T Wbar (192..255, times beta on the way
+// out) and M2 += Wbar K_r^T (256..319); M = M1 + M2 at the end.
 __global__ void __launch_bounds__(kThreads, 1)
     kc_bwd_prod_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm) {
     extern __shared__ __align__(1024) uint8_t sm[];
@@ -484,9 +498,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         step_gate(d, p, bb, h, t0, nvalid, tid, &bt[tid], &o);
     }
     if (warp == 0) {
-        tc::tmem_alloc(&tmem_sh, 256);
+        tc::tmem_alloc(&tmem_sh, 512);
         tc::tmem_relinquish();
     }
+    const uint8_t* krimg = static_cast<const uint8_t*>(p.krimg) + ci * (int64_t)C * Dk * 2;
+    const uint32_t kblk = (uint32_t)(C * 64 * 2);
     if (tid == 0) {
         tc::mbar_init(&bar, 1);
         tc::mbar_init(&barL, 1);
@@ -500,9 +516,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::bulk_g2s(sm + L.Dlo, dl + tv, tv, &barL);
         tc::bulk_g2s(sm + L.ND, reinterpret_cast<const uint8_t*>(p.Dbar) + ci * (int64_t)tv, tv, &barL);
         tc::bulk_g2s(sm + L.Tt, reinterpret_cast<const uint8_t*>(p.Tinv) + ci * C * C * 2, C * C * 2, &barL);
-        tc::mbar_arrive_expect_tx(&barS, 2 * blk);
+        tc::mbar_arrive_expect_tx(&barS, 2 * blk + kblk);
         tc::bulk_g2s(sm + L.S, ckimg, blk, &barS);
         tc::bulk_g2s(sm + L.Sp, dsimg, blk, &barS);
+        tc::bulk_g2s(sm + L.Kr, krimg, kblk, &barS);
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -516,6 +533,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const tc::Tile tNB = canon_tile(sm, L.ND, C, true), tNBmn = canon_tile(sm, L.ND, C, false);
     const tc::Tile tTmn = tc::panel_tile(sm + L.Tt, C, false);
     const tc::Tile tS = tc::panel_tile(sm + L.S, Dv, false), tSp = tc::panel_tile(sm + L.Sp, Dv, false);
+    const tc::Tile tKr = tc::panel_tile(sm + L.Kr, C, true);  // B = K_r^T: x = channel = K
+    const tc::Tile tWk = canon_tile(sm, L.Wt, 64, true);       // A = Wbar: x = channel = K
+    const tc::Tile tWmn = canon_tile(sm, L.Wt, 64, false);     // B = Wbar: x = channel = N
     if (tid == 0) {
         tc::mma_tile(tb + 0, tO, tDmn, C, C, Dv, false);     // Obar Delta^T (hi + lo)
         tc::mma_tile(tb + 0, tO, tDlomn, C, C, Dv, true);
@@ -579,24 +599,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = tc::mbar_wait(&bar, phase, &g_err_kctc) && ok;
         phase ^= 1u;
         tc::tc_fence_after();
+        const int64_t cb0 = 64 * b;
+        if (ok) {  // Wbar as a bf16 operand tile, then Kbar_d and Qbar_r out
+            acc_walk(tb, 128, 64, [&](int r, int c0, const float* x) {
+                st_bf16x8(sm + L.Wt + (c0 >> 3) * 128 + (r >> 3) * 1024 + (r & 7) * 16, x);
+            });
+        }
+        tc::fence_async_smem();
+        tc::tc_fence_before();
+        __syncthreads();  // Wbar tile written
+        tc::tc_fence_after();
+        if (tid == 0) {
+            tc::mma_tile(tb + 192, tTmn, tWmn, C, 64, C, false);  // T^T Wbar
+            tc::mma_tile(tb + 256, tWk, tKr, C, C, 64, b > 0);    // M2 += Wbar K_r^T
+            tc::mma_commit(&bar);
+        }
         if (ok) {
-            const int64_t cb0 = 64 * b;
             acc_walk(tb, 0, 64, [&](int r, int c0, const float* x) { st_f32x8(p.kdb + (rowbase + r) * Dk + cb0 + c0, x); });
             acc_walk(tb, 64, 64, [&](int r, int c0, const float* x) { st_f32x8(p.qrb + (rowbase + r) * Dk + cb0 + c0, x); });
-            acc_walk(tb, 128, 64, [&](int r, int c0, const float* x) { st_f32x8(p.wb + (rowbase + r) * Dk + cb0 + c0, x); });
+        }
+        ok = tc::mbar_wait(&bar, phase, &g_err_kctc) && ok;
+        phase ^= 1u;
+        tc::tc_fence_after();
+        if (ok) {
+            acc_walk(tb, 192, 64, [&](int r, int c0, const float* x) {
+                float y[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) y[i] = bt[r] * x[i];
+                st_f32x8(p.wb + (rowbase + r) * Dk + cb0 + c0, y);
+            });
         }
         tc::tc_fence_before();
-        __syncthreads();  // accumulators read, S / Sbar' tiles read
+        __syncthreads();  // accumulators read; S, Sbar', K_r and Wbar tiles read
         tc::tc_fence_after();
         if (tid == 0 && b + 1 < nblk) {
-            tc::mbar_arrive_expect_tx(&barS, 2 * blk);
+            tc::mbar_arrive_expect_tx(&barS, 2 * blk + kblk);
             tc::bulk_g2s(sm + L.S, ckimg + (int64_t)(b + 1) * blk, blk, &barS);
             tc::bulk_g2s(sm + L.Sp, dsimg + (int64_t)(b + 1) * blk, blk, &barS);
+            tc::bulk_g2s(sm + L.Kr, krimg + (int64_t)(b + 1) * kblk, kblk, &barS);
         }
+    }
+    if (ok) {  // M = M1 + M2 (M1 written by this CTA before the block loop)
+        float* M1 = p.m1 + ci * C * C;
+        acc_walk(tb, 256, C, [&](int r, int c0, const float* x) {
+            float m[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m[i] = M1[r * C + c0 + i] + x[i];
+            st_f32x8(M1 + r * C + c0, m);
+        });
     }
     tc::tc_fence_before();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tb, 256);
+    if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
 
 constexpr int CB = 32;       // key channels per block of kernels 2 and 3
@@ -660,37 +714,25 @@ __device__ __forceinline__ void chunk_vectors(const Dims& d, const Ptrs& p, int 
     }
 }
 
-// Kernel 2: one CTA per (chunk, value head, batch), 256 threads, CUDA cores.
-// M = M1 + Wbar (kh o E)^T and Kbar_r = diag(beta) T^T Wbar over the channel
-// blocks (Kbar_r overwrites Wbar in p.wb), then betabar (p.db) and Gbar (into
-// p.m1, over M1).
-__global__ void __launch_bounds__(kThreads, 2) kc_bwd_gate_kernel(Dims d, Ptrs p) {
+// Kernel 2: one CTA per (chunk, value head, batch), 256 threads, CUDA cores:
+// betabar (p.db) and Gbar (into p.m1, over M) from T, M = M1 + M2 and G.
+__global__ void __launch_bounds__(kThreads, 3) kc_bwd_gate_kernel(Dims d, Ptrs p) {
     extern __shared__ __align__(16) uint8_t lsm[];
     const int c = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
-    const int j = h / (int)d.G;
-    const int Dk = (int)d.Dk;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x;
     float* Tm = reinterpret_cast<float*>(lsm);
     float* Mm = Tm + C * LDT;
     float* Xm = Mm + C * LDT;
-    float* kb = Xm + C * LDT;
-    float* Gm = kb + C * LB;
-    float* Wk = Gm + C * LB;
-    float* Kr = Wk + C * LB;
-    float* part = Kr + C * LB;  // [8][CB]
-    float* bt = part + 8 * CB;
+    float* bt = Xm + C * LDT;
     float* on = bt + C;
-    float* rqs = on + C;
-    float* rks = rqs + C;
-    float* bbar = rks + C;
+    float* bbar = on + C;
     const int64_t t0 = (int64_t)c * C;
     const int nvalid = (int)(d.T - t0 < C ? d.T - t0 : C);
     const int64_t bh = (int64_t)bb * d.Hv + h;
     const int64_t ci = bh * d.NC + c;
-    const int64_t rowbase = bh * d.Tp + t0;
 
-    chunk_vectors(d, p, bb, h, j, t0, nvalid, bt, on, rqs, rks);
-    {  // T (from its bf16 panel image) and M1
+    if (tid < C) step_gate(d, p, bb, h, t0, nvalid, tid, &bt[tid], &on[tid]);
+    {  // T (from its bf16 panel image) and M
         const uint8_t* Timg = reinterpret_cast<const uint8_t*>(p.Tinv) + ci * C * C * 2;
         for (int e = tid; e < C * (C / 8); e += kThreads) {
             float x[8];
@@ -706,62 +748,6 @@ __global__ void __launch_bounds__(kThreads, 2) kc_bwd_gate_kernel(Dims d, Ptrs p
         }
     }
     __syncthreads();
-
-    for (int cb0 = 0; cb0 < Dk; cb0 += CB) {
-        load_block<false>(d, p, bb, h, j, t0, nvalid, cb0, on, rqs, rks, nullptr, kb, Gm, part);
-        {
-            const int t = tid >> 2, i0 = (tid & 3) * 8;
-            const float* src = p.wb + (rowbase + t) * Dk + cb0 + i0;
-            const float4 a = reinterpret_cast<const float4*>(src)[0], b = reinterpret_cast<const float4*>(src)[1];
-            const float w8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                Wk[t * LB + i0 + u] = w8[u];
-                Kr[t * LB + i0 + u] = kb[t * LB + i0 + u] * expf(Gm[t * LB + i0 + u]);
-            }
-        }
-        __syncthreads();
-        {  // M += Wbar (kh o E)^T over this block's channels: 4 x 4 tiles
-            const int tq = 4 * (tid >> 4), sq = 4 * (tid & 15);
-            float acc[4][4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int x = 0; x < 4; ++x) acc[r][x] = 0.f;
-            for (int i = 0; i < CB; ++i) {
-                float wv[4], kv[4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) wv[r] = Wk[(tq + r) * LB + i];
-#pragma unroll
-                for (int x = 0; x < 4; ++x) kv[x] = Kr[(sq + x) * LB + i];
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) acc[r][x] = fmaf(wv[r], kv[x], acc[r][x]);
-            }
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int x = 0; x < 4; ++x) Mm[(tq + r) * LDT + sq + x] += acc[r][x];
-        }
-        // Kbar_r = diag(beta) T^T Wbar: four rows r0 .. r0 + 3 and channel `lane` per
-        // item (T zero above the diagonal, so u starts at r0)
-        for (int it = 0; it < 2; ++it) {
-            const int r0 = 4 * (warp + 8 * it), i = lane;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int u = r0; u < C; ++u) {
-                const float4 t4 = *reinterpret_cast<const float4*>(Tm + u * LDT + r0);
-                const float wv = Wk[u * LB + i];
-                acc[0] = fmaf(t4.x, wv, acc[0]);
-                acc[1] = fmaf(t4.y, wv, acc[1]);
-                acc[2] = fmaf(t4.z, wv, acc[2]);
-                acc[3] = fmaf(t4.w, wv, acc[3]);
-            }
-#pragma unroll
-            for (int a = 0; a < 4; ++a) p.wb[(rowbase + r0 + a) * Dk + cb0 + i] = bt[r0 + a] * acc[a];
-        }
-        __syncthreads();
-    }
 
     // betabar (T o M column sums), Tbar = M diag(beta), X = Tbar T^T, Abar = -T^T X
     if (tid < C) {
@@ -894,11 +880,11 @@ __global__ void __launch_bounds__(kThreads, 2) kc_bwd_chan_kernel(Dims d, Ptrs p
         const int row = e / CB, i = e % CB;
         const int J = row < 48 ? 0 : row < 80 ? 1 : 2;
         const int t = J == 0 ? 16 + row : J == 1 ? 32 + (row - 48) : 48 + (row - 80);
-        Fm[row * LB + i] = expf(Gm[t * LB + i] - Gm[(16 * J + 15) * LB + i]);
+        Fm[row * LB + i] = __expf(Gm[t * LB + i] - Gm[(16 * J + 15) * LB + i]);
     }
     for (int e = tid; e < 48 * CB; e += kThreads) {
         const int s = e / CB, i = e % CB, b = s | 15;
-        Rm[s * LB + i] = kb[s * LB + i] * expf(Gm[b * LB + i] - Gm[s * LB + i]);
+        Rm[s * LB + i] = kb[s * LB + i] * __expf(Gm[b * LB + i] - Gm[s * LB + i]);
     }
     __syncthreads();
 
@@ -945,7 +931,7 @@ __global__ void __launch_bounds__(kThreads, 2) kc_bwd_chan_kernel(Dims d, Ptrs p
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
                 if (s <= r0 + a) {
-                    const float ks = ks0 * expf(gr[a] - gs);
+                    const float ks = ks0 * __expf(gr[a] - gs);
                     if (s < r0 + a) LG[a] = fmaf(Gg[(r0 + a) * LDT + s], ks, LG[a]);
                     LP[a] = fmaf(Pb[(r0 + a) * LDT + s], ks, LP[a]);
                 }
@@ -972,7 +958,7 @@ __global__ void __launch_bounds__(kThreads, 2) kc_bwd_chan_kernel(Dims d, Ptrs p
             const float gb = Gm[b * LB + i];
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
-                const float fr = expf(gb - gr[a]);
+                const float fr = __expf(gb - gr[a]);
                 RG[a] = fr * sG[a];
                 RP[a] = fr * sP[a];
             }
@@ -986,7 +972,7 @@ __global__ void __launch_bounds__(kThreads, 2) kc_bwd_chan_kernel(Dims d, Ptrs p
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
                 if (t >= r0 + a) {
-                    const float e = expf(gt - gr[a]);
+                    const float e = __expf(gt - gr[a]);
                     if (t > r0 + a) RG[a] = fmaf(gv[a], kt0 * e, RG[a]);
                     RP[a] = fmaf(pv[a], qt0 * e, RP[a]);
                 }
@@ -997,7 +983,7 @@ __global__ void __launch_bounds__(kThreads, 2) kc_bwd_chan_kernel(Dims d, Ptrs p
         for (int a = 0; a < 4; ++a) {
             const int r = r0 + a;
             const float k_r = kb[r * LB + i], q_r = qb[r * LB + i];
-            const float E = expf(gr[a]), ed = expf(g63 - gr[a]);
+            const float E = __expf(gr[a]), ed = __expf(g63 - gr[a]);
             const int64_t gi = (rowbase + r) * Dk + cb0 + i;
             const float Kd = k_r * ed;
             p.dqh[gi] = fmaf(qrb[a], E, LP[a]);
@@ -1012,7 +998,7 @@ __global__ void __launch_bounds__(kThreads, 2) kc_bwd_chan_kernel(Dims d, Ptrs p
     if (tid < CB) {  // Gammabar_63: the K_d column sums (warp order) and the state decay
         float tot = 0.f;
         for (int w = 0; w < kThreads / 32; ++w) tot += part[w * CB + tid];
-        Gb[(C - 1) * LB + tid] += tot + p.ecb[ci * Dk + cb0 + tid] * expf(Gm[(C - 1) * LB + tid]);
+        Gb[(C - 1) * LB + tid] += tot + p.ecb[ci * Dk + cb0 + tid] * __expf(Gm[(C - 1) * LB + tid]);
     }
     __syncthreads();
     // lbar: sums of Gammabar from the end of the chunk; warp w takes rows 8 w .. 8 w + 7
@@ -1030,7 +1016,7 @@ __global__ void __launch_bounds__(kThreads, 2) kc_bwd_chan_kernel(Dims d, Ptrs p
     }
 }
 
-inline size_t kc_gate_smem() { return 3 * kBlkMat + 4 * kBlkArr + (8 * CB + 5 * C) * 4; }
+inline size_t kc_gate_smem() { return 3 * kBlkMat + 3 * C * 4; }
 inline size_t kc_chan_smem() { return 2 * kBlkMat + 4 * kBlkArr + (96 + 48) * LB * 4 + (8 * CB + 4 * C) * 4; }
 
 }  // namespace
