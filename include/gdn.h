@@ -226,11 +226,18 @@ gdn_status gdn_backward_segments_auto(const gdn_shape* shape, int* segments);
  *     S = S_a + kh_t delta^T, o_t = S^T qh_t.  Masking, norms, layouts of q, k,
  *     v, o, the states and their cotangents are those of gdn_forward /
  *     gdn_backward.
- *   - The recurrence runs on the CUDA cores with an fp32 state (no chunked
- *     tensor-core form): one CTA per 16 value columns of a (b, h), the state at
- *     every 8th step kept in `saved` (gdn_kc_saved_bytes) for the backward.
+ *   - Two forms, chosen by the shape.  bf16 inputs with Dk 64, 128 or 192 and
+ *     Dv 128 take the chunked form: per 64-step chunk the decayed key products
+ *     (exp(Gamma_t,i - Gamma_s,i) through 16-step pivots, every factor <= 1, so
+ *     any l <= 0 is safe) and the WY/UT solve on the CUDA cores in fp32, the
+ *     scans and the value-long gradient products on the tensor cores; `saved`
+ *     holds per-chunk bf16 images (checkpoints, Delta, W, P, T, Q_r, K_d, K_r)
+ *     and fp32 decays and Grams.  Every other shape takes the recurrence on the
+ *     CUDA cores with an fp32 state: one CTA per 16 value columns of a (b, h),
+ *     the state at every 8th step kept in `saved` for the backward.
  *   - Requires Dk a multiple of 32 and Dv of 16 (Dk <= 256) on top of gdn.h's set,
- *     else GDN_ERR_UNSUPPORTED_SHAPE.
+ *     else GDN_ERR_UNSUPPORTED_SHAPE.  gdn_kc_saved_bytes and
+ *     gdn_kc_workspace_bytes size the form the shape takes.
  *   - saved may be NULL in gdn_forward_kc (inference).  ws must hold
  *     gdn_kc_workspace_bytes(shape, 0) bytes for the forward and (shape, 1) for
  *     the backward; every output is written in full. */
@@ -383,7 +390,9 @@ uint64_t gdn_launch_count(void);
  * order, sets *count, and switches recording off.  Returns GDN_ERR_CUDA if an
  * event failed.  Phases: "prep", "fwd_chunk", "fwd_scan", "bwd_scan",
  * "bwd_chunk", "bwd_scan_chunk" (the reverse scan and the gradient kernel in one
- * launch), "bwd_reduce", "decode", "kc_fwd", "kc_bwd".  Not thread-safe: one
+ * launch), "bwd_reduce", "decode", "kc_fwd", "kc_bwd" (the recurrent
+ * per-key-channel form), "kc_chunk", "kc_scan", "kc_bwd_scan", "kc_bwd_prod",
+ * "kc_bwd_gate", "kc_bwd_chan" (its chunked form).  Not thread-safe: one
  * caller at a time. */
 typedef struct {
     const char* name;
