@@ -95,12 +95,13 @@ __device__ __forceinline__ void st4(float* p, float a, float b, float c, float e
     *reinterpret_cast<float4*>(p) = make_float4(a, b, c, e);
 }
 
-// One CTA per (chunk, value head, batch).  p.a = log_decay [B, T, Hv, Dk], p.b =
+// One 512-thread CTA per (chunk, value head, batch).  p.a = log_decay [B, T, Hv, Dk], p.b =
 // beta [B, T, Hv] (bf16); rq, rk from prep.  Writes the panel images of Q_r, K_d
 // (p.qimg, p.kimg, per value head), K_r = kh o E (p.krimg), P, T, W, the fp32
 // rows of U, e_C (p.ecd) and the decayed Gram of the k rows (p.gram, for the
 // beta cotangent).
-__global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
+constexpr int kChunkThreads = 512;
+__global__ void __launch_bounds__(kChunkThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
     extern __shared__ __align__(16) uint8_t ksm[];
     const int c = blockIdx.x, h = blockIdx.y, bb = blockIdx.z;
     const int j = h / (int)d.G;
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
     __syncthreads();
     // normalised q, k rows and the log-decays (zero off the applied steps)
     const int cpr = Dk / 8;
-    for (int e = tid; e < C * cpr; e += kThreads) {
+    for (int e = tid; e < C * cpr; e += kChunkThreads) {
         const int t = e / cpr, i0 = (e % cpr) * 8;
         float xq[8], xk[8], xl[8];
         if (t < nvalid) {
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
         }
     }
     __syncthreads();
-    for (int i = tid; i < Dk; i += kThreads) {  // Gamma: running sums down each key channel
+    for (int i = tid; i < Dk; i += kChunkThreads) {  // Gamma: running sums down each key channel
         float g = 0.f;
         for (int t = 0; t < C; ++t) {
             g += Gf[t * LD + i];
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
     uint8_t* qr_img = static_cast<uint8_t*>(p.qimg) + ci * C * Dk * 2;
     uint8_t* kd_img = static_cast<uint8_t*>(p.kimg) + ci * C * Dk * 2;
     uint8_t* kr_img = static_cast<uint8_t*>(p.krimg) + ci * C * Dk * 2;
-    for (int e = tid; e < C * cpr; e += kThreads) {
+    for (int e = tid; e < C * cpr; e += kChunkThreads) {
         const int t = e % C, i0 = (e / C) * 8;
         float a[8], b[8], kr[8];
 #pragma unroll
@@ -199,15 +200,16 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
         st_bf16x8(kd_img + 16 * e, b);
         st_bf16x8(kr_img + 16 * e, kr);
     }
-    for (int i = tid; i < Dk; i += kThreads) p.ecd[ci * Dk + i] = __expf(Gf[(C - 1) * LD + i]);
-    for (int e = tid; e < 48 * Dk; e += kThreads) {
+    for (int i = tid; i < Dk; i += kChunkThreads) p.ecd[ci * Dk + i] = __expf(Gf[(C - 1) * LD + i]);
+    for (int e = tid; e < 48 * Dk; e += kChunkThreads) {
         const int s = e / Dk, i = e % Dk, b = s | 15;
         Rt[i * kRS + s] = kf[s * LD + i] * __expf(Gf[b * LD + i] - Gf[s * LD + i]);
     }
     __syncthreads();
 
-    // A and P off the diagonal blocks: threads 0..191, one row t and eight
-    // columns s of a pivot block J each; four channels per step
+    // A and P off the diagonal blocks (warps 0-5: one row t and eight columns s
+    // of a pivot block J per thread, four channels per step) and on the
+    // diagonal blocks (warps 6-13), side by side
     if (tid < 192) {
         const int half = tid / 96, r = tid % 96;
         const int J = r < 48 ? 0 : r < 80 ? 1 : 2;
@@ -245,8 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
     // the diagonal blocks: thread (row t, channel quarter qq) forms row t against
     // every s = 16 I .. t of its block over its quarter of the channels, each term
     // with its own exponential; the quarters' sums meet by shuffles
-    {
-        const int t = tid >> 2, qq = tid & 3, I = t >> 4, n = t - 16 * I;  // s = 16 I + 0 .. n
+    else if (tid < 448) {
+        const int t = (tid - 192) >> 2, qq = tid & 3, I = t >> 4, n = t - 16 * I;  // s = 16 I + 0 .. n
         const int qw = Dk / 4;
         float ad[16], pd[16];
 #pragma unroll
@@ -288,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
 
     // P image (zero above the diagonal), then T = (I + A)^-1 into region q
     uint8_t* Pimg = static_cast<uint8_t*>(p.P) + ci * C * C * 2;
-    for (int e = tid; e < C * (C / 8); e += kThreads) {
+    for (int e = tid; e < C * (C / 8); e += kChunkThreads) {
         const int t = e % C, s0 = (e / C) * 8;
         float v8[8];
 #pragma unroll
@@ -299,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
     float* X = qf + C * LDT;
     tri::tri_inverse64(A, Tm, X);  // ends synchronised
     uint8_t* Timg = reinterpret_cast<uint8_t*>(p.Tinv) + ci * C * C * 2;
-    for (int e = tid; e < C * (C / 8); e += kThreads) {
+    for (int e = tid; e < C * (C / 8); e += kChunkThreads) {
         const int t = e % C, s0 = (e / C) * 8;
         float v8[8];
 #pragma unroll
@@ -307,12 +309,12 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
         st_bf16x8(Timg + 16 * e, v8);
     }
     // beta (kh o E) in place of kh, beta V in region R
-    for (int e = tid; e < C * Dk; e += kThreads) {
+    for (int e = tid; e < C * Dk; e += kChunkThreads) {
         const int s = e / Dk, i = e % Dk;
         kf[s * LD + i] *= bt[s] * __expf(Gf[s * LD + i]);
     }
     float* Vb = Rt;
-    for (int e = tid; e < C * (Dv / 8); e += kThreads) {
+    for (int e = tid; e < C * (Dv / 8); e += kChunkThreads) {
         const int t = e / (Dv / 8), c0 = (e % (Dv / 8)) * 8;
         float x[8];
         if (t < nvalid) {
@@ -332,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) kc_chunk_kernel(Dims d, Ptrs p) {
     uint8_t* Wimg = static_cast<uint8_t*>(p.W) + ci * C * Dk * 2;
     float* U = p.U + (bh * d.Tp + t0) * Dv;
     const int ncq = (Dk + Dv) / 4;
-    for (int e = tid; e < 16 * ncq; e += kThreads) {
+    for (int e = tid; e < 16 * ncq; e += kChunkThreads) {
         const int tq = 4 * (e / ncq), c0 = 4 * (e % ncq);
         const bool isW = c0 < Dk;
         const float* Bm = isW ? kf + c0 : Vb + (c0 - Dk);
@@ -1061,7 +1063,7 @@ cudaError_t launch_kc_chunk(const Dims& d, const Ptrs& p, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)d.NC, (unsigned)d.Hv, (unsigned)d.B);
-    kern<<<grid, kThreads, smem, s>>>(d, p);
+    kern<<<grid, kChunkThreads, smem, s>>>(d, p);
     count_launches(1);
     return cudaPeekAtLastError();
 }
