@@ -154,57 +154,58 @@ __device__ __forceinline__ tc::Tile mnmaj(uint8_t* smem, uint32_t off, int ncols
     return t;
 }
 
-// Walk an M = 64 accumulator of `ncols` columns at TMEM column col0: eight warps,
-// warp w reads rows 16 (w % 4) .. +15 and half (w / 4) of the columns.
+// Walk an M = 64 accumulator of `ncols` columns (a multiple of 32) at TMEM
+// column col0 with every thread of the eight warps busy: 32-column pieces,
+// taken in turn by the two warp groups g = warp / 4; in a piece at column c,
+// thread l < 16 of warp w holds row 16 (w % 4) + l at columns c .. c + 15 and
+// thread l + 16 the same row at columns c + 16 .. c + 31 (the 16x32bx2 TMEM
+// shape).  f(row, first column, 16 values) is called by all 32 lanes; a
+// per-row sum adds its two lane halves with row_pair_sum.
 template <typename F>
-__device__ __forceinline__ void acc_rows(uint32_t tbase, uint32_t col0, int ncols, F&& f) {
+__device__ __forceinline__ void acc_rows1(uint32_t tbase, uint32_t col0, int ncols, F&& f) {
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    const int sp = w & 3, g = w >> 2;
-    const int half = ncols / 2;
-    for (int c = g * half; c < (g + 1) * half; c += 16) {
+    const int sp = w & 3, g = w >> 2, hl = l >> 4;
+    for (int c = 32 * g; c < ncols; c += 64) {
         float v[16];
-        tc::tmem_ld16(tc::tmem_addr(tbase, 32 * sp, col0 + c), v);
+        tc::tmem_ld16x2<16>(tc::tmem_addr(tbase, 32 * sp, col0 + c), v);
         tc::tmem_wait_ld();
-        if (l < 16) f(16 * sp + l, c, v);
+        f(16 * sp + (l & 15), c + 16 * hl, v);
     }
 }
-
-// As acc_rows, and the (modified) values are written back in place.  Lanes
-// 16..31 write TMEM lanes that an M = 64 accumulator does not use.
+// As acc_rows1 with two pieces in flight per wait
 template <typename F>
-__device__ __forceinline__ void acc_rows_rw(uint32_t tbase, uint32_t col0, int ncols, F&& f) {
+__device__ __forceinline__ void acc_rows2(uint32_t tbase, uint32_t col0, int ncols, F&& f) {
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    const int sp = w & 3, g = w >> 2;
-    const int half = ncols / 2;
-    for (int c = g * half; c < (g + 1) * half; c += 16) {
-        float v[16];
-        const uint32_t ta = tc::tmem_addr(tbase, 32 * sp, col0 + c);
-        tc::tmem_ld16(ta, v);
+    const int sp = w & 3, g = w >> 2, hl = l >> 4;
+    for (int c = 32 * g; c < ncols; c += 128) {
+        float v[2][16];
+        const bool two = c + 64 < ncols;  // warp-uniform
+        tc::tmem_ld16x2<16>(tc::tmem_addr(tbase, 32 * sp, col0 + c), v[0]);
+        if (two) tc::tmem_ld16x2<16>(tc::tmem_addr(tbase, 32 * sp, col0 + c + 64), v[1]);
         tc::tmem_wait_ld();
-        if (l < 16) f(16 * sp + l, c, v);
-        tc::tmem_st16(ta, v);
+        f(16 * sp + (l & 15), c + 16 * hl, v[0]);
+        if (two) f(16 * sp + (l & 15), c + 64 + 16 * hl, v[1]);
     }
-    tc::tmem_wait_st();
 }
-// M = 64 accumulator walk with all 32 lanes: lane l < 16 takes columns c .. c + 7
-// of row 16 (w % 4) + l, lane l + 16 columns c + 8 .. c + 15 of the same row
-// (handed over by shuffles); f(row, first column, 8 values, lane half)
+// A row's two lane halves (lanes l and l + 16) summed; every lane gets the total
+__device__ __forceinline__ float row_pair_sum(float s) { return s + __shfl_xor_sync(0xffffffffu, s, 16); }
+// As acc_rows1, handing each lane's 16 columns to f in two 8-column runs:
+// f(row, first column, 8 values, lane half)
 template <typename F>
 __device__ __forceinline__ void acc_rows_all(uint32_t tbase, uint32_t col0, int ncols, F&& f) {
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
     const int sp = w & 3, g = w >> 2, hl = l >> 4;
-    const int half = ncols / 2;
-    for (int c = g * half; c < (g + 1) * half; c += 16) {
+    for (int c = 32 * g; c < ncols; c += 64) {
         float v[16];
-        tc::tmem_ld16(tc::tmem_addr(tbase, 32 * sp, col0 + c), v);
+        tc::tmem_ld16x2<16>(tc::tmem_addr(tbase, 32 * sp, col0 + c), v);
         tc::tmem_wait_ld();
         float x[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float up = __shfl_sync(0xffffffffu, v[8 + i], l & 15);
-            x[i] = hl ? up : v[i];
-        }
-        f(16 * sp + (l & 15), c + 8 * hl, x, hl);
+        for (int i = 0; i < 8; ++i) x[i] = v[i];
+        f(16 * sp + (l & 15), c + 16 * hl, x, hl);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = v[8 + i];
+        f(16 * sp + (l & 15), c + 16 * hl + 8, x, hl);
     }
 }
 
@@ -223,26 +224,6 @@ __device__ __forceinline__ f2 f2_add(f2 x, f2 y) {
     const float lo = s.lo + (x.lo + y.lo);
     const float h = s.hi + lo;
     return {h, lo - (h - s.hi)};
-}
-
-// As acc_rows with two 16-column loads in flight per wait
-template <typename F>
-__device__ __forceinline__ void acc_rows2(uint32_t tbase, uint32_t col0, int ncols, F&& f) {
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    const int sp = w & 3, g = w >> 2;
-    const int half = ncols / 2, end = (g + 1) * half;
-    for (int cb = g * half; cb < end; cb += 32) {
-        float v[2][16];
-#pragma unroll
-        for (int u = 0; u < 2; ++u)
-            if (cb + 16 * u < end) tc::tmem_ld16(tc::tmem_addr(tbase, 32 * sp, col0 + cb + 16 * u), v[u]);
-        tc::tmem_wait_ld();
-        if (l < 16) {
-#pragma unroll
-            for (int u = 0; u < 2; ++u)
-                if (cb + 16 * u < end) f(16 * sp + l, cb + 16 * u, v[u]);
-        }
-    }
 }
 
 // Completion of an MMA round on `bar`: waiting threads wait for it; every thread
@@ -499,7 +480,7 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
                 st_row8(Tbf + r * LDM + c0, m);
                 st_row8(Tbf + r * LDM + c0 + 8, m + 8);
             });
-            acc_rows(tb, kAK, Dv, [&](int r, int c0, const float (&x)[16]) {
+            acc_rows1(tb, kAK, Dv, [&](int r, int c0, const float (&x)[16]) {
                 float vv[16], y[16];
                 panel_row16(sm + L.V, c0, r, vv);
                 float s = 0.f;
@@ -508,7 +489,8 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
                     s = fmaf(-x[i], vv[i], s);
                     y[i] = -bt[r] * x[i];
                 }
-                bb0[g * C + r] += s;
+                s = row_pair_sum(s);
+                if (lane < 16) bb0[g * C + r] += s;
                 if (r < nvalid) {
                     uint8_t* dst = reinterpret_cast<uint8_t*>(dv + ((int64_t)bb * d.T + t0 + r) * ldv +
                                                               (int64_t)h * Dv + c0);
@@ -575,34 +557,31 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
         }
     } else if (epi) {
         ok = tc::mbar_wait(&barKQ, pit, &g_err_bwdtc) && ok;
-        const int sp = warp & 3;
-        // warp columns g nk / 2 .. + nk / 2 of a block in one or two 16-column pieces
+        const int sp = warp & 3, hl = lane >> 4;
+        const int r = 16 * sp + (lane & 15);  // the accumulator row of this lane
+        // a block's 32-column pieces (nk is 64 or 32) go to the warp groups in
+        // turn; lanes l and l + 16 take columns 16 (l / 16) .. + 15 of a piece
         for (int b = 0; b < nblk; ++b) {  // walk 1: dk *= e, <dk, k> per row
             const int dk0 = b * kBlkK, nk = nkb(b);
             ok = tc::mbar_wait(&barMa1[b], ip, &g_err_bwdtc) && ok;
             tc::tc_fence_after();
             if (ok) {
-                const int half = nk / 2, np = half / 16;
-                for (int u = 0; u < np; ++u) {
-                    const int cc = g * half + 16 * u;
+                for (int cc = 32 * g; cc < nk; cc += 64) {
                     float ak[16];
-                    tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, kAK + dk0 + cc), ak);
+                    const uint32_t ta = tc::tmem_addr(tb, 32 * sp, kAK + dk0 + cc);
+                    tc::tmem_ld16x2<16>(ta, ak);
                     tc::tmem_wait_ld();
-                    if (lane < 16) {
-                        const int r = 16 * sp + lane;
-                        float kk[16];
-                        panel_row16(sm + L.K, dk0 + cc, r, kk);
-                        float sk = 0.f;
+                    float kk[16];
+                    panel_row16(sm + L.K, dk0 + cc + 16 * hl, r, kk);
+                    float sk = 0.f;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            ak[i] *= ev[r];
-                            sk = fmaf(ak[i], kk[i], sk);
-                        }
-                        ee[g * C + r] += sk;
+                    for (int i = 0; i < 16; ++i) {
+                        ak[i] *= ev[r];
+                        sk = fmaf(ak[i], kk[i], sk);
                     }
-                    // rescaled values back in place (lanes 16..31 write TMEM lanes
-                    // that an M = 64 accumulator does not use)
-                    tc::tmem_st16(tc::tmem_addr(tb, 32 * sp, kAK + dk0 + cc), ak);
+                    sk = row_pair_sum(sk);
+                    if (lane < 16) ee[g * C + r] += sk;
+                    tc::tmem_st16x2<16>(ta, ak);  // rescaled values back in place
                 }
                 tc::tmem_wait_st();
             }
@@ -628,28 +607,26 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
             ok = tc::mbar_wait(&barM2[b], ip, &g_err_bwdtc) && ok;
             tc::tc_fence_after();
             if (ok) {
-                const int half = nk / 2, np = half / 16;
                 const uint32_t wcol = (b & 1) ? kS2 : kS1;
-                for (int u = 0; u < np; ++u) {
-                    const int cc = g * half + 16 * u;
+                for (int cc = 32 * g; cc < nk; cc += 64) {
                     float aq[16], wv[16];
-                    tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, kAQ + dk0 + cc), aq);
-                    tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, wcol + cc), wv);
+                    const uint32_t ta = tc::tmem_addr(tb, 32 * sp, kAQ + dk0 + cc);
+                    tc::tmem_ld16x2<16>(ta, aq);
+                    tc::tmem_ld16x2<16>(tc::tmem_addr(tb, 32 * sp, wcol + cc), wv);
                     tc::tmem_wait_ld();
-                    if (lane < 16) {
-                        const int r = 16 * sp + lane;
-                        float qq[16];
-                        panel_row16(sm + L.Q, dk0 + cc, r, qq);
-                        float sq = 0.f;
+                    const int c0 = dk0 + cc + 16 * hl;
+                    float qq[16];
+                    panel_row16(sm + L.Q, c0, r, qq);
+                    float sq = 0.f;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            aq[i] *= gm[r];
-                            sq = fmaf(aq[i], qq[i], sq);
-                        }
-                        gq[g * C + r] += sq;
-                        tile_put16(sm + L.W, Dk, dk0 + cc, r, wv);
+                    for (int i = 0; i < 16; ++i) {
+                        aq[i] *= gm[r];
+                        sq = fmaf(aq[i], qq[i], sq);
                     }
-                    tc::tmem_st16(tc::tmem_addr(tb, 32 * sp, kAQ + dk0 + cc), aq);
+                    sq = row_pair_sum(sq);
+                    if (lane < 16) gq[g * C + r] += sq;
+                    tile_put16(sm + L.W, Dk, c0, r, wv);
+                    tc::tmem_st16x2<16>(ta, aq);
                 }
                 tc::tmem_wait_st();
             }

@@ -13,7 +13,7 @@ namespace {
 __global__ void __launch_bounds__(128) selftest_mma_kernel(int M, int N, int K, int a_mn, int b_mn,
                                                            const __nv_bfloat16* __restrict__ A,
                                                            const __nv_bfloat16* __restrict__ B,
-                                                           float* __restrict__ D) {
+                                                           float* __restrict__ D, int rows16x2) {
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ uint64_t bar;
     __shared__ uint32_t tmem_base;
@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(128) selftest_mma_kernel(int M, int N, int K, 
     }
     const bool ok = tc::mbar_wait(&bar, 0, &g_err_selftest);
     tc::tc_fence_after();
-    if (ok) {
+    if (ok && !rows16x2) {
         for (int c0 = 0; c0 < N; c0 += 16) {
             float v[16];
             tc::tmem_ld16(tc::tmem_addr(tbase, 32 * (warp & 3), c0), v);
@@ -69,6 +69,26 @@ __global__ void __launch_bounds__(128) selftest_mma_kernel(int M, int N, int K, 
             const int row = 32 * (warp & 3) + (tid & 31);
 #pragma unroll
             for (int i = 0; i < 16; ++i) D[row * N + c0 + i] = v[i];
+        }
+    } else if (ok) {
+        // M = 64 rows through the 16x32bx2 shape: load, negate, store back with
+        // the same shape, load again; D is [64][N] (row 16 (warp % 4) + lane % 16)
+        const int l = tid & 31;
+        const int row = 16 * (warp & 3) + (l & 15);
+        for (int c0 = 0; c0 < N; c0 += 32) {
+            const uint32_t ta = tc::tmem_addr(tbase, 32 * (warp & 3), c0);
+            float v[16];
+            tc::tmem_ld16x2<16>(ta, v);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = -v[i];
+            tc::tmem_st16x2<16>(ta, v);
+            tc::tmem_wait_st();
+            tc::tmem_ld16x2<16>(ta, v);
+            tc::tmem_wait_ld();
+            const int col = c0 + 16 * (l >> 4);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) D[row * N + col + i] = v[i];
         }
     }
     tc::tc_fence_before();
@@ -184,7 +204,21 @@ extern "C" gdn_status gdn_selftest_mma(int M, int N, int K, int a_mn_major, int 
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     kern<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(
         M, N, K, a_mn_major, b_mn_major, static_cast<const __nv_bfloat16*>(A),
-        static_cast<const __nv_bfloat16*>(B), D_raw);
+        static_cast<const __nv_bfloat16*>(B), D_raw, 0);
+    gdn::count_launches(1);
+    return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+extern "C" gdn_status gdn_selftest_mma_m64_rows(int N, int K, const void* A, const void* B,
+                                                float* D, void* stream) {
+    if (N < 32 || N > 256 || N % 32 || K < 16 || K > 256 || K % 16) return GDN_ERR_UNSUPPORTED_SHAPE;
+    if (!A || !B || !D) return GDN_ERR_INVALID_ARG;
+    const size_t smem = (size_t)128 * 256 * 2 + (size_t)256 * 256 * 2;
+    auto kern = gdn::selftest_mma_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    kern<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(
+        64, N, K, 0, 0, static_cast<const __nv_bfloat16*>(A), static_cast<const __nv_bfloat16*>(B), D, 1);
     gdn::count_launches(1);
     return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -28,6 +28,17 @@ extern "C" {
 gdn_status gdn_selftest_mma(int M, int N, int K, int a_mn_major, int b_mn_major, const void* A,
                             const void* B, float* D_raw, void* stream);
 
+/* The rows of an M = 64 accumulator read through the 16x32bx2 TMEM shape (every
+ * thread of a warp on accumulator data; the form the gradient kernel's
+ * epilogues use): D = -(A * B) after one load, a negated store back with the
+ * same shape and a second load.
+ *   A: device bf16 [64][K] row-major, B: device bf16 [K][N] row-major, both
+ *   staged K-major.  N in 32..256 (multiple of 32); K in 16..256 (multiple of 16).
+ *   D: device fp32 [64][N].
+ * Enqueued on `stream`; returns GDN_ERR_UNSUPPORTED_SHAPE for other sizes. */
+gdn_status gdn_selftest_mma_m64_rows(int N, int K, const void* A, const void* B, float* D,
+                                     void* stream);
+
 /* D = A * B on one CTA with tcgen05.mma taking A from tensor memory (the form
  * the scans use for the state operand), M = 128.
  *   A: device bf16 [128][K] row-major, written by its 128 threads into TMEM

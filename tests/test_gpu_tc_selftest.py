@@ -19,6 +19,8 @@ def lib():
     L = ops.load_library()
     L.gdn_selftest_mma.argtypes = [ctypes.c_int] * 5 + [ctypes.c_void_p] * 4
     L.gdn_selftest_mma.restype = ctypes.c_int
+    L.gdn_selftest_mma_m64_rows.argtypes = [ctypes.c_int] * 2 + [ctypes.c_void_p] * 4
+    L.gdn_selftest_mma_m64_rows.restype = ctypes.c_int
     L.gdn_selftest_mma_tmem_a.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p] * 4
     L.gdn_selftest_mma_tmem_a.restype = ctypes.c_int
     L.gdn_selftest_tma_tile.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int] * 5 + [ctypes.c_void_p] * 3
@@ -62,6 +64,22 @@ def test_m64_lane_placement(lib, amn, bmn, N, K):
     D, ref = _run(lib, 64, N, K, amn, bmn)
     got = D[_lanes_m64().cuda()]
     torch.testing.assert_close(got, ref, rtol=1e-5, atol=1e-4)
+
+
+@pytest.mark.parametrize("N,K", [(32, 16), (64, 64), (192, 128), (256, 32)])
+def test_m64_rows_16x32bx2(lib, N, K):
+    # thread t < 16 of warp w holds row 16 (w % 4) + t, columns c .. c + 15;
+    # thread t + 16 the same row at columns c + 16 .. c + 31
+    g = torch.Generator().manual_seed(3 + N + K)
+    A = torch.randn((64, K), generator=g).to(torch.bfloat16).cuda()
+    B = torch.randn((K, N), generator=g).to(torch.bfloat16).cuda()
+    D = torch.full((64, N), float("nan"), device="cuda")
+    rc = lib.gdn_selftest_mma_m64_rows(N, K, ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
+                                       ctypes.c_void_p(D.data_ptr()),
+                                       ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 0
+    torch.cuda.synchronize()
+    torch.testing.assert_close(D, -(A.float() @ B.float()), rtol=1e-5, atol=1e-4)
 
 
 @pytest.mark.parametrize("bmn", [0, 1])
