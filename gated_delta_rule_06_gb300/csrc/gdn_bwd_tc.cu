@@ -262,9 +262,13 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
     __shared__ int next_item;
     const int Dk = (int)d.Dk, Dv = (int)d.Dv;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // warps 0-7: epilogues (row quarter warp % 4, column half g); warp 8: loads and MMA issue
+    // warps 0-7: epilogues (row quarter warp % 4, column half g); warp 8: loads and MMA
+    // issue; warp 9: MMA issue of the second of two independent product chains.  One
+    // thread issues a tcgen05.mma about every 80 cycles whatever its size, so small
+    // products from two issuing warps run side by side on the tensor core.
     const bool epi = tid < kThreads;
     const bool prod = tid == kThreads;
+    const bool prod2 = tid == kThreads + 32;
     const int g = (warp >> 2) & 1;
     const Smem L = smem_plan(Dk, Dv);
     float* vec = reinterpret_cast<float*>(sm + L.vec);
@@ -362,6 +366,11 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
         tc::bulk_g2s(sm + L.NB, reinterpret_cast<const uint8_t*>(p.Dbar) + ci * (int64_t)tv, tv, &barL);
         tc::bulk_g2s(sm + L.Tt, reinterpret_cast<const uint8_t*>(p.Tinv) + ci * (int64_t)C * C * 2,
                      C * C * 2, &barL);
+        // the state and state-cotangent images that phase 1 streams through its
+        // slots, into L2 now: a slot's copy then waits for L2, not for DRAM
+        const uint32_t sbytes = (uint32_t)(Dk * Dv * 2);
+        tc::bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(p.dSck) + ci * (int64_t)sbytes, sbytes);
+        tc::bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(p.ckpt) + ci * (int64_t)sbytes, sbytes);
     };
     auto issue_loads_kq = [&](int it) {
         const int c = item_c(it), h = item_h(it), bb = item_b(it);
@@ -378,14 +387,14 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
         tc::tmem_relinquish();
     }
     if (prod) {
-        tc::mbar_init(&bar, 1);
+        tc::mbar_init(&bar, 2);  // every MMA round: one commit (or arrival) from each issuer
         tc::mbar_init(&barOV, 1);
         tc::mbar_init(&barL, 1);
         tc::mbar_init(&barKQ, 1);
         for (int i = 0; i < 4; ++i) {
             tc::mbar_init(&barT[i], 1);
             tc::mbar_init(&barMa1[i], 1);
-            tc::mbar_init(&barM2[i], 1);
+            tc::mbar_init(&barM2[i], 2);
             tc::mbar_init(&barG2[i], kThreads);
             tc::mbar_init(&barE2[i], kThreads);
         }
@@ -454,10 +463,12 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
     if (prod) {
         tc::mma_tile(tb + kS1, tO, tDmn, C, C, Dv, false);
         tc::mma_tile(tb + kS1, tO, tDlomn, C, C, Dv, true);
+        tc::mma_commit(&bar);
+        issue_loads_kq(it);
+    } else if (prod2) {
         tc::mma_tile(tb + kS2, tNBmn, tV, C, C, Dv, false);
         tc::mma_tile(tb + kAK, tTmn, tNB, C, Dv, C, false);
         tc::mma_commit(&bar);
-        issue_loads_kq(it);
     }
     float* Pf = reinterpret_cast<float*>(sm + L.Pf);
     float* Tbf = reinterpret_cast<float*>(sm + L.Tbf);
@@ -516,21 +527,28 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
     float gcb = 0.f;
     const uint32_t ip = iord & 1u;  // parity of the per-block barriers in this item
     auto slot_par = [&](int sl, int occ) { return (iord * slot_uses(sl) + (uint32_t)occ) & 1u; };
+    // walk 1: the producer issues the blocks in slot 1 (even b), the second issuer
+    // those in slot 0 (odd b); walk 2: the producer Obar S^T, the second issuer
+    // -Dbar S^T of every block
+    auto walk1_block = [&](int b) {
+        const int dk0 = b * kBlkK, nk = nkb(b), sl = (b & 1) ? 0 : 1;
+        ok = tc::mbar_wait(&barT[sl], slot_par(sl, b >> 1), &g_err_bwdtc) && ok;
+        const tc::Tile tSp = tc::panel_tile(slot_ptr(sl), Dv, false);
+        tc::mma_tile(tb + kAK + dk0, tDmn, tSp, C, nk, Dv, false);
+        tc::mma_tile(tb + kAK + dk0, tDlomn, tSp, C, nk, Dv, true);
+        tc::mma_commit(&barMa1[b]);
+    };
     if (prod) {
         if (nblk >= 2) load_tile(p.dSck, ci, 1, 0);  // the V tile is dead: phase 0 is done
-        for (int b = 0; b < nblk; ++b) {  // walk 1
-            const int dk0 = b * kBlkK, nk = nkb(b), sl = (b & 1) ? 0 : 1;
-            ok = tc::mbar_wait(&barT[sl], slot_par(sl, b >> 1), &g_err_bwdtc) && ok;
-            const tc::Tile tSp = tc::panel_tile(slot_ptr(sl), Dv, false);
-            tc::mma_tile(tb + kAK + dk0, tDmn, tSp, C, nk, Dv, false);
-            tc::mma_tile(tb + kAK + dk0, tDlomn, tSp, C, nk, Dv, true);
-            tc::mma_commit(&barMa1[b]);
+        for (int b = 0; b < nblk; b += 2) {  // walk 1, even blocks (slot 1)
+            walk1_block(b);
             if (b + 2 < nblk) {
                 ok = tc::mbar_wait(&barMa1[b], ip, &g_err_bwdtc) && ok;
-                load_tile(p.dSck, ci, b + 2, sl);
+                load_tile(p.dSck, ci, b + 2, 1);
             }
         }
-        ok = tc::mbar_wait(&barMa1[nblk - 1], ip, &g_err_bwdtc) && ok;  // every walk-1 product done
+        for (int b = 0; b < nblk; ++b)  // every walk-1 product done
+            ok = tc::mbar_wait(&barMa1[b], ip, &g_err_bwdtc) && ok;
         load_tile(p.ckpt, ci, 0, 0);
         load_tile(p.dSck, ci, 0, 1);
         if (nblk >= 2) {
@@ -542,11 +560,8 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
             const int sS = (b & 1) ? 2 : 0, sP = sS + 1;
             const int occS = (b & 1) ? (b >> 1) : (nblk / 2 + (b >> 1));
             ok = tc::mbar_wait(&barT[sS], slot_par(sS, occS), &g_err_bwdtc) && ok;
-            if (b >= 2) ok = tc::mbar_wait(&barE2[b - 2], ip, &g_err_bwdtc) && ok;
-            const uint32_t wcol = (b & 1) ? kS2 : kS1;
             const tc::Tile tS = tc::panel_tile(slot_ptr(sS), Dv, false);
             tc::mma_tile(tb + kAQ + dk0, tO, tS, C, nk, Dv, false);
-            tc::mma_tile(tb + wcol, tNBmn, tS, C, nk, Dv, false);
             tc::mma_commit(&barM2[b]);
             if (b + 2 < nblk) {
                 ok = tc::mbar_wait(&barM2[b], ip, &g_err_bwdtc) && ok;
@@ -554,6 +569,19 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
                 load_tile(p.ckpt, ci, b + 2, sS);
                 load_tile(p.dSck, ci, b + 2, sP);
             }
+        }
+    } else if (prod2) {
+        for (int b = 1; b < nblk; b += 2) walk1_block(b);  // walk 1, odd blocks (slot 0)
+        for (int b = 0; b < nblk; ++b) {                     // walk 2: -Dbar S^T
+            const int nk = nkb(b);
+            const int sS = (b & 1) ? 2 : 0;
+            const int occS = (b & 1) ? (b >> 1) : (nblk / 2 + (b >> 1));
+            ok = tc::mbar_wait(&barT[sS], slot_par(sS, occS), &g_err_bwdtc) && ok;
+            if (b >= 2) ok = tc::mbar_wait(&barE2[b - 2], ip, &g_err_bwdtc) && ok;
+            const uint32_t wcol = (b & 1) ? kS2 : kS1;
+            const tc::Tile tS = tc::panel_tile(slot_ptr(sS), Dv, false);
+            tc::mma_tile(tb + wcol, tNBmn, tS, C, nk, Dv, false);
+            tc::mma_commit(&barM2[b]);
         }
     } else if (epi) {
         ok = tc::mbar_wait(&barKQ, pit, &g_err_bwdtc) && ok;
@@ -656,6 +684,9 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
         ok = tc::mbar_wait(&barKQ, pit, &g_err_bwdtc) && ok;
         tc::mma_tile(tb + kS1, tW, tK, C, C, Dk, false);
         tc::mma_tile(tb + kAK, tc::panel_tile(sm + L.Tsc, C, false), tWmn, C, Dk, C, true);
+        tc::mma_commit(&bar);
+    } else if (prod2) {
+        ok = tc::mbar_wait(&barKQ, pit, &g_err_bwdtc) && ok;
         tc::mma_tile(tb + kS2, tK, tK, C, C, Dk, false);
         tc::mma_commit(&bar);
     }
@@ -732,6 +763,8 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
     // ---- phase 2: X = Tbar T^T | Q K^T, then Abar' = T^T X (Abar = -Abar')
     if (prod) {
         tc::mma_tile(tb + kS1, kmaj(sm, L.Tbh, C), tTt, C, C, C, false);
+        tc::mma_commit(&bar);
+    } else if (prod2) {
         tc::mma_tile(tb + kS2, tQ, tK, C, C, Dk, false);
         tc::mma_commit(&bar);
     }
@@ -755,6 +788,8 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
     if (prod) {
         tc::mma_tile(tb + kS1, tTmn, mnmaj(sm, L.Xh, C), C, C, C, false);
         tc::mma_commit(&bar);
+    } else if (prod2) {
+        tc::mbar_arrive(&bar);  // nothing to issue in this round
     }
     sync_after_mma(&bar, phase, ok, epi);
     if (epi && ok) {
@@ -848,6 +883,8 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
     // ---- phase 3: dq += (Pbar o M) K;  dk += (Pbar o M)^T Q + (Gb + Gb^T) K
     if (prod) {
         tc::mma_tile(tb + kAQ, kmaj(sm, L.PMk, C), tKmn, C, Dk, C, true);
+        tc::mma_commit(&bar);
+    } else if (prod2) {
         tc::mma_tile(tb + kAK, mnmaj(sm, L.PMq, C), tQmn, C, Dk, C, true);
         tc::mma_tile(tb + kAK, kmaj(sm, L.Hk, C), tKmn, C, Dk, C, true);
         tc::mma_commit(&bar);
@@ -940,7 +977,7 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
     if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
 
-__global__ void __launch_bounds__(kThreads + 32, 1)
+__global__ void __launch_bounds__(kThreads + 64, 1)
     bwd_chunk_tc_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm) {
     bwd_chunk_body(d, p, tm, p.sched, nullptr, 0);
 }
@@ -951,7 +988,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
 // gradient items, each once the reverse scan has published its chunk for all
 // value tiles of its head.  The scan CTAs never wait on the gradient CTAs, so
 // every wait ends; the SMs the scan leaves idle run gradient items meanwhile.
-__global__ void __launch_bounds__(kThreads + 32, 1)
+__global__ void __launch_bounds__(kThreads + 64, 1)
     bwd_fused_tc_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm) {
     const int ntiles = (int)(d.Dv / ta::DVT);
     const int nscan = ntiles * (int)(d.Hv * d.B);
@@ -991,7 +1028,7 @@ cudaError_t launch_bwd_chunk_tc(const Dims& d, const Ptrs& p, cudaStream_t s) {
     const int grid = (int)(nitems < sm_count() ? nitems : sm_count());
     e = cudaMemsetAsync(p.sched, 0, sizeof(unsigned int), s);  // the item counter
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps);
+    kern<<<grid, kThreads + 64, smem, s>>>(d, p, *p.tmaps);
     count_launches(1);
     return cudaPeekAtLastError();
 }
@@ -1014,7 +1051,7 @@ cudaError_t launch_bwd_fused_tc(const Dims& d, const Ptrs& p, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads + 32, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads + 64, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
     // the item counter and the per-(b, h) progress counts start at zero
@@ -1025,7 +1062,7 @@ cudaError_t launch_bwd_fused_tc(const Dims& d, const Ptrs& p, cudaStream_t s) {
     Tmaps tm = *p.tmaps;
     void* args[] = {&dd, &pp, &tm};
     e = cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)sm_count()),
-                                    dim3(kThreads + 32), args, smem, s);
+                                    dim3(kThreads + 64), args, smem, s);
     count_launches(1);
     return e;
 }

@@ -67,26 +67,26 @@ __device__ __forceinline__ tc::Tile tile_of(uint8_t* p, int ncols, bool k_major)
     return t;
 }
 
-// M = 64 accumulator walk (rows 16 (w % 4) .. +15 in warp w, column half w / 4)
-// with all 32 lanes: lane l < 16 takes columns c .. c + 7 of row
-// 16 (w % 4) + l, lane l + 16 columns c + 8 .. c + 15 of that row (handed over
-// by shuffles); f(row, first column, 8 values)
+// M = 64 accumulator walk with every lane busy: 32-column pieces taken in turn
+// by the two warp groups g = w / 4; in a piece at column c, lane l < 16 of warp
+// w reads row 16 (w % 4) + l at columns c .. c + 15 and lane l + 16 the same row
+// at columns c + 16 .. c + 31 (the 16x32bx2 TMEM shape); f(row, first column,
+// 8 values) takes each lane's 16 columns as two runs of 8
 template <typename F>
 __device__ __forceinline__ void acc_rows_all(uint32_t tbase, uint32_t col0, int ncols, F&& f) {
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
     const int sp = w & 3, g = w >> 2, hl = l >> 4;
-    const int half = ncols / 2;
-    for (int c = g * half; c < (g + 1) * half; c += 16) {
+    for (int c = 32 * g; c < ncols; c += 64) {
         float v[16];
-        tc::tmem_ld16(tc::tmem_addr(tbase, 32 * sp, col0 + c), v);
+        tc::tmem_ld16x2<16>(tc::tmem_addr(tbase, 32 * sp, col0 + c), v);
         tc::tmem_wait_ld();
         float x[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float up = __shfl_sync(0xffffffffu, v[8 + i], l & 15);
-            x[i] = hl ? up : v[i];
-        }
-        f(16 * sp + (l & 15), c + 8 * hl, x);
+        for (int i = 0; i < 8; ++i) x[i] = v[i];
+        f(16 * sp + (l & 15), c + 16 * hl, x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = v[8 + i];
+        f(16 * sp + (l & 15), c + 16 * hl + 8, x);
     }
 }
 
@@ -218,26 +218,27 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs 
     tc::tc_fence_after();
     uint8_t* Pimg = static_cast<uint8_t*>(p.P) + (bh * d.NC + c) * C * C * 2;
     if (ok) {
-        // A and P in one pass over both Grams, all 32 lanes: row r, 8 columns from
-        // c0.  The 16-column block J of a piece and the row block of a warp are
-        // warp-uniform, so is the choice between the factored and the direct decay.
+        // A and P in one pass over both Grams, all 32 lanes (16x32bx2 loads): warp
+        // group g takes columns 32 g .. 32 g + 31 of row r, lane half hl the 16 of
+        // them from 32 g + 16 hl, in two runs of 8 from c0.  The 16-column block J
+        // of a run is uniform over each half-warp, so is the choice between the
+        // factored and the direct decay.
         const int l = tid & 31, sp = warp & 3, g = warp >> 2, hl = l >> 4;
         const int r = 16 * sp + (l & 15);
         const float ra = bt[r] * rkv[r], rp = rqv[r], ghr = Ghi[r], glr = Glo[r];
-        for (int cp = 32 * g; cp < 32 * g + 32; cp += 16) {
-            float va[16], vp[16];
-            tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, cp), va);
-            tc::tmem_ld16(tc::tmem_addr(tb, 32 * sp, 64 + cp), vp);
-            tc::tmem_wait_ld();
+        float va[16], vp[16];
+        tc::tmem_ld16x2<16>(tc::tmem_addr(tb, 32 * sp, 32 * g), va);
+        tc::tmem_ld16x2<16>(tc::tmem_addr(tb, 32 * sp, 64 + 32 * g), vp);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int run = 0; run < 2; ++run) {
             float xa[8], xp[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const float ua = __shfl_sync(0xffffffffu, va[8 + i], l & 15);
-                const float up = __shfl_sync(0xffffffffu, vp[8 + i], l & 15);
-                xa[i] = hl ? ua : va[i];
-                xp[i] = hl ? up : vp[i];
+                xa[i] = va[8 * run + i];
+                xp[i] = vp[8 * run + i];
             }
-            const int c0 = cp + 8 * hl, J = cp >> 4;
+            const int c0 = 32 * g + 16 * hl + 8 * run, J = c0 >> 4;
             float m[8];
             if (J < sp) {
                 const float u = uf[J * C + r];

@@ -287,6 +287,12 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const void* map, int c0, 
         : "memory");
 }
 
+// L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned global
+// address: no shared memory, no completion to wait for
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 2-d tiled load (coordinates c0 = innermost, c1) into shared memory
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int c0, int c1, uint64_t* bar) {
     asm volatile(
