@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs 
         tc::tmem_relinquish();
     }
     if (tid == 0) {
-        tc::mbar_init(&bar, 1);
+        tc::mbar_init(&bar, 2);  // each MMA round: one commit (or arrival) per issuer
         tc::mbar_init(&barKQ, 1);
         tc::fence_mbar_init();
         // raw k and q rows of this chunk: panel images written by prep
@@ -200,9 +200,13 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs 
     const tc::Tile tK = tc::panel_tile(sm + L.K, C, true), tQ = tc::panel_tile(sm + L.Q, C, true);
     const tc::Tile tKmn = tc::panel_tile(sm + L.K, C, false), tVmn = tile_of(sm + L.V, Dv, false);
 
-    // ---- Grams of the raw rows
+    // ---- Grams of the raw rows.  Threads 0 and 32 (two warps) issue one product
+    // chain each: one thread issues a tcgen05.mma about every 80 cycles whatever its
+    // size, so the two chains run side by side.
     if (tid == 0) {
         tc::mma_tile(tb + 0, tK, tK, C, C, Dk, false);
+        tc::mma_commit(&bar);
+    } else if (tid == 32) {
         tc::mma_tile(tb + 64, tQ, tK, C, C, Dk, false);
         tc::mma_commit(&bar);
     }
@@ -327,11 +331,15 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs 
     if (tid == 0) {
         tc::mma_tile(tb + 0, tTw, tKmn, C, Dk, C, false);
         tc::mma_tile(tb + 0, tTwl, tKmn, C, Dk, C, true);
+        tc::mma_commit(&bar);
+    } else if (tid == 32) {
         if (one_round) {
             tc::mma_tile(tb + Dk, tTu, tVmn, C, Dv, C, false);
             tc::mma_tile(tb + Dk, tTul, tVmn, C, Dv, C, true);
+            tc::mma_commit(&bar);
+        } else {
+            tc::mbar_arrive(&bar);
         }
-        tc::mma_commit(&bar);
     }
     ok = tc::mbar_wait(&bar, phase, &g_err_fwdtc) && ok;
     phase ^= 1u;
@@ -351,6 +359,8 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs 
             tc::mma_tile(tb + 0, tTu, tVmn, C, Dv, C, false);
             tc::mma_tile(tb + 0, tTul, tVmn, C, Dv, C, true);
             tc::mma_commit(&bar);
+        } else if (tid == 32) {
+            tc::mbar_arrive(&bar);
         }
         ok = tc::mbar_wait(&bar, phase, &g_err_fwdtc) && ok;
         phase ^= 1u;

@@ -93,7 +93,7 @@ __device__ __forceinline__ void scale_q(uint8_t* Q, const uint8_t* raw, int Dk) 
 // (b, value head)) with no per-step factor, and S^T decays column by column by
 // the chunk's exp(Gamma_63, i) (p.ecd).
 template <bool KC>
-__global__ void __launch_bounds__(kThreads + 32, 1)
+__global__ void __launch_bounds__(kThreads + 64, 1)
     fwd_scan_ta_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm, ScanSeg sg) {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ uint64_t bar, barW, barQ, barK, barP, barU, barR[2], barD[2];
@@ -104,9 +104,12 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
     const int Dk = (int)d.Dk, Dv = (int)d.Dv;
     const int n0 = tile * DVT;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // warps 0-7: epilogues (accumulator row r, column half g); warp 8: loads and MMA issue
+    // warps 0-7: epilogues (accumulator row r, column half g); warp 8: loads and MMA
+    // issue; warp 9: MMA issue of the second chain of steps 2 and 4 (one thread issues
+    // a tcgen05.mma about every 80 cycles, so two issuing warps overlap the chains)
     const bool epi = tid < kThreads;
     const bool prod = warp == kThreads / 32 && lane == 0;
+    const bool prod2 = warp == kThreads / 32 + 1 && lane == 0;
     const int r = 32 * (warp & 3) + lane;
     const int g = (tid >> 7) & 1;
     const uint32_t lb = 32u * (uint32_t)(warp & 3);
@@ -200,7 +203,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::tmem_relinquish();
     }
     if (prod) {
-        tc::mbar_init(&bar, 1);
+        tc::mbar_init(&bar, 2);  // one commit from each issuer per MMA round
         tc::mbar_init(&barW, 1);
         tc::mbar_init(&barQ, 1);
         tc::mbar_init(&barK, 1);
@@ -297,27 +300,35 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
         tc::tc_fence_after();
         uint32_t hiw[16], low[16];
         if (prod) {
-            // step 2: Delta^T acc = S^T W^T and O^T = S^T Qs^T, two independent
-            // accumulation chains interleaved
+            // step 2: Delta^T acc = S^T W^T here and O^T = S^T Qs^T by the second
+            // issuer, two independent accumulation chains
             ok = tc::mbar_wait(&barW, lp(c), &g_err_scanta) && ok;
-            // (the epilogue waits for q and scales it before (B); KC has no scaling)
-            if (KC) ok = tc::mbar_wait(&barQ, lp(c), &g_err_scanta) && ok;
             const uint32_t id = tc::idesc_bf16(DVT, C, false, false);
-            uint64_t dw = tW.desc(0), dq = tQ.desc(0);
-            const uint64_t iw = tW.desc_step(), iq = tQ.desc_step();
+            uint64_t dw = tW.desc(0);
+            const uint64_t iw = tW.desc_step();
             for (int k = 0; k < Dk; k += 16) {
                 tc::mma_bf16_ta(tb + TC.dacc, tb + TC.aop + k / 2, dw, id, k > 0);
-                tc::mma_bf16_ta(tb + ocol, tb + TC.aop + k / 2, dq, id, k > 0);
                 dw += iw;
-                dq += iq;
             }
             tc::mma_commit(&bar);
-            ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
+            ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;  // both chains
             phase ^= 1u;
             if (c + 1 < ce) {
                 load_w(c + 1);
                 load_q(c + 1);
             }
+        } else if (prod2) {
+            // (the epilogue waits for q and scales it before (B); KC has no scaling)
+            if (KC) ok = tc::mbar_wait(&barQ, lp(c), &g_err_scanta) && ok;
+            const uint32_t id = tc::idesc_bf16(DVT, C, false, false);
+            uint64_t dq = tQ.desc(0);
+            const uint64_t iq = tQ.desc_step();
+            for (int k = 0; k < Dk; k += 16) {
+                tc::mma_bf16_ta(tb + ocol, tb + TC.aop + k / 2, dq, id, k > 0);
+                dq += iq;
+            }
+            tc::mma_commit(&bar);
+            phase ^= 1u;
         } else if (epi) {
             // meanwhile: the checkpoint image (S^T bf16, from the A operand) and
             // the output rows of chunk c - 1
@@ -373,11 +384,12 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
             if (storer) tc::bulk_wait_read_all();  // Delta staging of c - 1 read out
             tc::named_sync(1, kThreads);
         }
-        if (prod) {
-            // step 4: O^T += Delta^T P^T (hi, lo);  S^T += (Delta^T diag(e r_k)) K (hi, lo);
-            // the steps of pass u2 (16-step slices u2 and 2 + u2) once it is handed over
-            ok = tc::mbar_wait(&barP, lp(c), &g_err_scanta) && ok;
-            ok = tc::mbar_wait(&barK, lp(c), &g_err_scanta) && ok;
+        if (prod || prod2) {
+            // step 4: O^T += Delta^T P^T (hi, lo) here and S^T += (Delta^T diag(e r_k)) K
+            // (hi, lo) by the second issuer; the steps of pass u2 (16-step slices u2 and
+            // 2 + u2) once it is handed over
+            if (prod) ok = tc::mbar_wait(&barP, lp(c), &g_err_scanta) && ok;
+            else ok = tc::mbar_wait(&barK, lp(c), &g_err_scanta) && ok;
             const uint32_t idp = tc::idesc_bf16(DVT, C, false, false);
             const uint32_t idk = tc::idesc_bf16(DVT, Dk, false, true);
             const uint64_t dp0 = tP.desc(0), ip = tP.desc_step();
@@ -390,11 +402,17 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
                 for (int i = 0; i < 4; ++i) {
                     const int ks = 2 * (i & 1) + u2;  // 16-step slice
                     const uint32_t hl = (uint32_t)(i >> 1) * 32u;
-                    tc::mma_bf16_ta(tb + ocol, tb + TC.aop + hl + 8 * ks, dp0 + (uint64_t)ks * ip, idp, 1u);
-                    tc::mma_bf16_ta(tb, tb + TC.aop + 64 + hl + 8 * ks, dk0 + (uint64_t)ks * ik, idk, 1u);
+                    if (prod)
+                        tc::mma_bf16_ta(tb + ocol, tb + TC.aop + hl + 8 * ks, dp0 + (uint64_t)ks * ip, idp, 1u);
+                    else
+                        tc::mma_bf16_ta(tb, tb + TC.aop + 64 + hl + 8 * ks, dk0 + (uint64_t)ks * ik, idk, 1u);
                 }
             }
             tc::mma_commit(&bar);
+        }
+        if (prod2) {
+            phase ^= 1u;
+        } else if (prod) {
             if (!uz && c + 1 < ce) load_u(c + 1);  // step 3 of chunk c has read U
             ok = tc::mbar_wait(&bar, phase, &g_err_scanta) && ok;
             phase ^= 1u;
@@ -479,7 +497,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
 }
 
 template <bool KC>
-__global__ void __launch_bounds__(kThreads + 32, 1)
+__global__ void __launch_bounds__(kThreads + 64, 1)
     bwd_scan_ta_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm, ScanSeg sg) {
     bwd_scan_ta_body<KC>(d, p, tm, blockIdx.x, blockIdx.y, (int)(blockIdx.z % d.B), sg,
                      sg.first + (int)(blockIdx.z / d.B), &g_err_scanta, nullptr, true);
@@ -498,7 +516,7 @@ cudaError_t launch_fwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);
-    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps, ScanSeg{1, (int)d.NC, 0, nullptr, nullptr});
+    kern<<<grid, kThreads + 64, smem, s>>>(d, p, *p.tmaps, ScanSeg{1, (int)d.NC, 0, nullptr, nullptr});
     count_launches(1);
     return cudaPeekAtLastError();
 }
@@ -513,7 +531,7 @@ cudaError_t launch_fwd_scan_ta_seg(const Dims& d, const Ptrs& p, const ScanSeg& 
     const int64_t nx = sg.mode == 0 ? d.Dv / DVT : seg_wd(d.Dk, d.Dv) / DVT;
     const int64_t nz = (sg.mode == 0 ? sg.nseg : sg.nseg - 1) * d.B;
     dim3 grid((unsigned)nx, (unsigned)d.Hv, (unsigned)nz);
-    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps, sg);
+    kern<<<grid, kThreads + 64, smem, s>>>(d, p, *p.tmaps, sg);
     count_launches(1);
     return cudaPeekAtLastError();
 }
@@ -525,7 +543,7 @@ cudaError_t launch_fwd_scan_ta_one(const Dims& d, const Ptrs& p, const ScanSeg& 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);
-    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps, sg);
+    kern<<<grid, kThreads + 64, smem, s>>>(d, p, *p.tmaps, sg);
     count_launches(1);
     return cudaPeekAtLastError();
 }
@@ -629,7 +647,7 @@ cudaError_t launch_bwd_scan_ta(const Dims& d, const Ptrs& p, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);
-    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps, ScanSeg{1, (int)d.NC, 0, nullptr, nullptr});
+    kern<<<grid, kThreads + 64, smem, s>>>(d, p, *p.tmaps, ScanSeg{1, (int)d.NC, 0, nullptr, nullptr});
     count_launches(1);
     return cudaPeekAtLastError();
 }
@@ -642,7 +660,7 @@ cudaError_t launch_bwd_scan_ta_seg(const Dims& d, const Ptrs& p, const ScanSeg& 
     const int64_t nx = sg.mode == 0 ? d.Dv / DVT : seg_wd(d.Dk, d.Dv) / DVT;
     const int64_t nz = (sg.mode == 0 ? sg.nseg : sg.nseg - 1) * d.B;
     dim3 grid((unsigned)nx, (unsigned)d.Hv, (unsigned)nz);
-    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps, sg);
+    kern<<<grid, kThreads + 64, smem, s>>>(d, p, *p.tmaps, sg);
     count_launches(1);
     return cudaPeekAtLastError();
 }
@@ -655,7 +673,7 @@ cudaError_t launch_fwd_scan_kc(const Dims& d, const Ptrs& p, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);
-    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps, ScanSeg{1, (int)d.NC, 0, nullptr, nullptr});
+    kern<<<grid, kThreads + 64, smem, s>>>(d, p, *p.tmaps, ScanSeg{1, (int)d.NC, 0, nullptr, nullptr});
     count_launches(1);
     return cudaPeekAtLastError();
 }
@@ -666,7 +684,7 @@ cudaError_t launch_bwd_scan_kc(const Dims& d, const Ptrs& p, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);
-    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps, ScanSeg{1, (int)d.NC, 0, nullptr, nullptr});
+    kern<<<grid, kThreads + 64, smem, s>>>(d, p, *p.tmaps, ScanSeg{1, (int)d.NC, 0, nullptr, nullptr});
     count_launches(1);
     return cudaPeekAtLastError();
 }
@@ -678,7 +696,7 @@ cudaError_t launch_bwd_scan_ta_one(const Dims& d, const Ptrs& p, const ScanSeg& 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(d.Dv / DVT), (unsigned)d.Hv, (unsigned)d.B);
-    kern<<<grid, kThreads + 32, smem, s>>>(d, p, *p.tmaps, sg);
+    kern<<<grid, kThreads + 64, smem, s>>>(d, p, *p.tmaps, sg);
     count_launches(1);
     return cudaPeekAtLastError();
 }

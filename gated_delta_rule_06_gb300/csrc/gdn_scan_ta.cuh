@@ -116,7 +116,7 @@ __device__ __forceinline__ void build_os(const uint8_t* O, uint8_t* Os, uint8_t*
 __host__ __device__ inline int64_t seg_wd(int64_t Dk, int64_t Dv) { return Dv + (Dk + DVT - 1) / DVT * DVT; }
 
 // The reverse scan of value tile `tile` of (batch bb, value head h), run by a
-// CTA of kThreads + 32 threads with tb_plan(Dk).total + 1024 bytes of dynamic
+// CTA of kThreads + 64 threads with tb_plan(Dk).total + 1024 bytes of dynamic
 // shared memory and all 512 TMEM columns.  err: the caller's error word for
 // bounded waits.  progress (may be null): after the -Dbar^T and Sbar'^T images
 // of a chunk are complete in global memory, progress[b Hv + h] goes up by one
@@ -149,6 +149,9 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool epi = tid < kThreads;
     const bool prod = warp == kThreads / 32 && lane == 0;
+    // warp 9 issues the second MMA chain of step 2 (one thread issues a tcgen05.mma
+    // about every 80 cycles, so two issuing warps overlap the chains)
+    const bool prod2 = warp == kThreads / 32 + 1 && lane == 0;
     const bool storer = warp == kStoreWarp && lane == 0;
     const int r = 32 * (warp & 3) + lane;
     const int g = (tid >> 7) & 1;
@@ -218,7 +221,7 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
         if (relinquish) tc::tmem_relinquish();
     }
     if (prod) {
-        tc::mbar_init(&bar, 1);
+        tc::mbar_init(&bar, 2);  // one commit (or arrival) from each issuer per MMA round
         tc::mbar_init(&barW, 1);
         tc::mbar_init(&barQ, 1);
         tc::mbar_init(&barK, 1);
@@ -338,28 +341,41 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
         tc::tc_fence_after();
         const tc::Tile tOmn = tc::panel_tile(obuf(c), C, false);
         tND.base = tc::smem_u32(ndbuf(c));
-        if (prod) {
-            // step 2: A1 = Obar^T P, A2 = Sbar^T K^T, Sbar^T += Os Q + Oslo Q, with the
-            // three accumulation chains interleaved
+        if (prod2) {
+            // step 2, second issuer: A1 = Obar^T P and Sbar^T += Os Q + Oslo Q, two
+            // chains interleaved.  The P and Q copies are waited for even when they
+            // are not read (a map's linear part): the producer's next copy into the
+            // buffer re-arms the barrier, which it may only do once this phase is
+            // complete.
             ok = tc::mbar_wait(&barP, (uint32_t)(m & 1), err) && ok;
-            ok = tc::mbar_wait(&barK, (uint32_t)(m & 1), err) && ok;
             ok = tc::mbar_wait(&barQ, (uint32_t)(m & 1), err) && ok;
-            const uint32_t id64 = tc::idesc_bf16(DVT, C, true, true);
-            const uint32_t id2 = tc::idesc_bf16(DVT, C, false, false);
-            const uint32_t idq = tc::idesc_bf16(DVT, Dk, true, true);
-            uint64_t dK = tK.desc(0), dO = tOmn.desc(0), dP = tPmn.desc(0), dOs = tOsmn.desc(0),
-                     dQ = tQmn.desc(0), dOl = tOslomn.desc(0);
-            const uint64_t iK = tK.desc_step(), iO = tOmn.desc_step(), iP = tPmn.desc_step(),
-                           iOs = tOsmn.desc_step(), iQ = tQmn.desc_step(), iOl = tOslomn.desc_step();
-            for (int k = 0; k < Dk; k += 16) {
-                tc::mma_bf16_ta(tb + kA2, tb + aop + k / 2, dK, id2, k > 0);
-                dK += iK;
-                if (k < C && !oz) {
+            if (!oz) {
+                const uint32_t id64 = tc::idesc_bf16(DVT, C, true, true);
+                const uint32_t idq = tc::idesc_bf16(DVT, Dk, true, true);
+                uint64_t dO = tOmn.desc(0), dP = tPmn.desc(0), dOs = tOsmn.desc(0), dQ = tQmn.desc(0),
+                         dOl = tOslomn.desc(0);
+                const uint64_t iO = tOmn.desc_step(), iP = tPmn.desc_step(), iOs = tOsmn.desc_step(),
+                               iQ = tQmn.desc_step(), iOl = tOslomn.desc_step();
+                for (int k = 0; k < C; k += 16) {
                     tc::mma_bf16(tb + kA1, dO, dP, id64, k > 0);
                     tc::mma_bf16(tb, dOs, dQ, idq, 1u);
                     tc::mma_bf16(tb, dOl, dQ, idq, 1u);
                     dO += iO; dP += iP; dOs += iOs; dQ += iQ; dOl += iOl;
                 }
+                tc::mma_commit(&bar);
+            } else {
+                tc::mbar_arrive(&bar);  // nothing to issue in this round
+            }
+            phase ^= 1u;
+        } else if (prod) {
+            // step 2: A2 = Sbar^T K^T (A1 and the state update by the second issuer)
+            ok = tc::mbar_wait(&barK, (uint32_t)(m & 1), err) && ok;
+            const uint32_t id2 = tc::idesc_bf16(DVT, C, false, false);
+            uint64_t dK = tK.desc(0);
+            const uint64_t iK = tK.desc_step();
+            for (int k = 0; k < Dk; k += 16) {
+                tc::mma_bf16_ta(tb + kA2, tb + aop + k / 2, dK, id2, k > 0);
+                dK += iK;
             }
             tc::mma_commit(&bar);
             ok = tc::mbar_wait(&bar, phase, err) && ok;
@@ -416,7 +432,10 @@ __device__ __forceinline__ void bwd_scan_ta_body(const Dims& d, const Ptrs& p, c
         tc::tc_fence_before();
         __syncthreads();  // (C)
         tc::tc_fence_after();
-        if (prod) {
+        if (prod2) {
+            tc::mbar_arrive(&bar);  // step 4 has one chain: nothing to issue here
+            phase ^= 1u;
+        } else if (prod) {
             // step 4: Sbar^T += (-Dbar^T) W
             ok = tc::mbar_wait(&barW, (uint32_t)(m & 1), err) && ok;
             tc::mma_tile(tb, tND, tWmn, DVT, Dk, C, true);
