@@ -257,7 +257,7 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
     // -Dbar S^T products done, barG2[b] its tiles read by the <S, Sbar'> sums,
     // barE2[b] its epilogue done (Wbar scratch free); barT[s]: arrivals of the
     // tiles of slot s (several per item)
-    __shared__ uint64_t bar, barOV, barL, barKQ, barT[4], barMa1[4], barM2[4], barG2[4], barE2[4];
+    __shared__ uint64_t bar, barOV, barL, barKQ, barT[5], barMa1[4], barM2[4], barG2[4], barE2[4];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int next_item;
     const int Dk = (int)d.Dk, Dv = (int)d.Dv;
@@ -323,24 +323,34 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
     const uint32_t tk = (uint32_t)(C * Dk * 2);         // one 64 x Dk bf16 tile
     const uint32_t blk = (uint32_t)(kBlkK * Dv * 2);    // one full Dk block of S (or Sbar')
     // Dk block b of S / Sbar' (panels 8b .. 8b + nk(b) / 8 - 1 of the images of
-    // chunk image ci) goes to one of four tile slots of a block each: slot 0 in
-    // the space of the V tile (free once phase 0 is done), slot 1 right after it
-    // (never used by phase 0), slots 2 and 3 in the space of the Delta hi / lo
-    // tiles (free once the Delta Sbar'^T products are done).  Phase 1 walks the
-    // blocks twice: first Delta Sbar'^T (Sbar' blocks in slots 1, 0, 1, ...),
-    // then Obar S^T and -Dbar S^T with the <S, Sbar'> sums (S and Sbar' of block
-    // b in slots 0 / 1 for even b, 2 / 3 for odd b), so both walks double-buffer
-    // their tiles.  Per item, slot 0 takes nblk tiles, slot 1 2 ceil(nblk / 2),
-    // slots 2 and 3 floor(nblk / 2); a wait on slot s for its occ-th tile of the
-    // item uses parity (iord * uses(s) + occ) & 1.
-    const int nblk = (Dk + kBlkK - 1) / kBlkK;
+    // chunk image ci) goes to one of five tile slots: slot 0 in the space of the V
+    // tile (free once phase 0 is done), slot 1 right after it (never used by phase
+    // 0), slots 2 and 3 in the space of the Delta hi / lo tiles (free once the
+    // Delta Sbar'^T products are done), slot 4 in the Wbar staging tile (free until
+    // walk 2's epilogues write Wbar).  Walk 1 (Delta Sbar'^T) with three blocks
+    // reads Sbar' block 1 from slot 1 and block 2 from slot 4, both loaded with the
+    // phase-1 group of copies, and block 0 from slot 0, loaded once phase 0 is
+    // done, so that blocks 0 and 1 lie side by side and go through one 128-wide
+    // product while the second issuer takes block 2; with fewer blocks, block 0
+    // comes early in slot 1 and block 1 in slot 0, one per issuer.  The blocks stay
+    // there for the <S, Sbar'> sums of walk 2, which so loads only S: walk-2
+    // position p takes block w2_blk(p) (order 2, 0, 1 for three blocks, so that
+    // the Wbar of block 2 is written first, beside Sbar' block 2) from slot 2
+    // (even p) or 3 (odd p), the third position once the first is done.  Per item,
+    // slot 0 takes one tile when nblk > 1, slot 1 one, slot 2 ceil(nblk / 2), slot 3
+    // floor(nblk / 2), slot 4 one when nblk = 3; a wait on slot s for its occ-th tile
+    // of the item uses parity (iord * uses(s) + occ) & 1.
+    const int nblk = (Dk + kBlkK - 1) / kBlkK;  // 1 .. 3 (Dk <= 192)
     auto nkb = [&](int b) { return Dk - b * kBlkK < kBlkK ? Dk - b * kBlkK : kBlkK; };
     auto slot_ptr = [&](int sl) -> uint8_t* {
-        return sm + (sl == 0 ? L.V : sl == 1 ? L.V + blk : sl == 2 ? L.D : L.Dlo);
+        return sm + (sl == 0 ? L.V : sl == 1 ? L.V + blk : sl == 2 ? L.D : sl == 3 ? L.Dlo : L.W);
     };
     auto slot_uses = [&](int sl) -> uint32_t {
-        return sl == 0 ? (uint32_t)nblk : sl == 1 ? 2u * (uint32_t)((nblk + 1) / 2) : (uint32_t)(nblk / 2);
+        return sl == 0 ? (uint32_t)(nblk > 1) : sl == 1 ? 1u : sl == 2 ? (uint32_t)((nblk + 1) / 2)
+               : sl == 3 ? (uint32_t)(nblk / 2) : (uint32_t)(nblk == 3);
     };
+    auto sbar_slot = [&](int b) { return b == 2 ? 4 : (nblk == 3) == (b == 1) ? 1 : 0; };
+    auto w2_blk = [&](int p) { return nblk == 3 ? (p == 0 ? 2 : p - 1) : p; };
     auto load_tile = [&](const void* img, int64_t ci, int b, int sl) {
         const uint32_t bytes = (uint32_t)(nkb(b) * Dv * 2);
         tc::mbar_arrive_expect_tx(&barT[sl], bytes);
@@ -380,7 +390,8 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
         tc::mbar_arrive_expect_tx(&barKQ, 2 * tk);
         tc::bulk_g2s(sm + L.K, static_cast<const uint8_t*>(p.kimg) + kqi * tk, tk, &barKQ);
         tc::bulk_g2s(sm + L.Q, static_cast<const uint8_t*>(p.qimg) + kqi * tk, tk, &barKQ);
-        load_tile(p.dSck, ci, 0, 1);
+        load_tile(p.dSck, ci, nblk == 3 ? 1 : 0, 1);
+        if (nblk == 3) load_tile(p.dSck, ci, 2, 4);
     };
     if (warp == 0) {
         tc::tmem_alloc(&tmem_base_sh, 512);
@@ -391,6 +402,7 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
         tc::mbar_init(&barOV, 1);
         tc::mbar_init(&barL, 1);
         tc::mbar_init(&barKQ, 1);
+        tc::mbar_init(&barT[4], 1);
         for (int i = 0; i < 4; ++i) {
             tc::mbar_init(&barT[i], 1);
             tc::mbar_init(&barMa1[i], 1);
@@ -448,7 +460,7 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
     // k, q, dO, v tiles: panel layout (x = column, 64 rows); Wbar tile: canonical
     const tc::Tile tK = tc::panel_tile(sm + L.K, C, true), tQ = tc::panel_tile(sm + L.Q, C, true);
     const tc::Tile tKmn = tc::panel_tile(sm + L.K, C, false), tQmn = tc::panel_tile(sm + L.Q, C, false);
-    const tc::Tile tW = kmaj(sm, L.W, Dk), tWmn = mnmaj(sm, L.W, Dk);
+    const tc::Tile tW = tc::panel_tile(sm + L.W, C, true), tWmn = tc::panel_tile(sm + L.W, C, false);
     const tc::Tile tO = tc::panel_tile(sm + L.O, C, true), tV = tc::panel_tile(sm + L.V, C, true);
     // Delta / -Dbar images: x = step t (canonical, 8-row groups of Dv 1024 bytes apart)
     const tc::Tile tDmn = mnmaj(sm, L.D, C), tDlomn = mnmaj(sm, L.Dlo, C);
@@ -515,73 +527,60 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
 
     // ---- phase 1: state products per kBlkK-wide block of Dk, in two walks over
     // the blocks (slots: see load_tile above).  Walk 1: Delta Sbar'^T (hi + lo)
-    // into the dk accumulator, each Sbar' block loading while the previous
-    // block's products run; the epilogue rescales dk by e and forms <dk, k> per
-    // row.  Walk 2, once every walk-1 product is done (all four slots free):
-    // Obar S^T into the dq accumulator and -Dbar S^T into the Wbar scratch (S1 for
-    // even, S2 for odd blocks, reused once the epilogue of block b - 2 released
-    // it), the S / Sbar' pair of block b + 2 loading once block b's products and
-    // its <S, Sbar'> sums are done; the epilogue rescales dq by gam, forms
-    // <dq, q> per row and stages Wbar as a bf16 tile.  The first Sbar' block
-    // arrives with the phase-0 operands.
+    // into the dk accumulator, the blocks' products issued as their Sbar' tiles
+    // arrive (block 1 by the second issuer); the epilogue rescales dk by e and
+    // forms <dk, k> per row.  Walk 2, once every walk-1 product is done (slots 2
+    // and 3 free): per position p, Obar S^T into the dq accumulator (producer) and
+    // -Dbar S^T into the Wbar scratch (second issuer; S1 for even, S2 for odd p,
+    // reused once the epilogue of position p - 2 released it); the epilogue forms
+    // <S, Sbar'> from the S tile and the Sbar' tile of walk 1, rescales dq by gam,
+    // forms <dq, q> per row and stages Wbar as a bf16 panel tile.
     float gcb = 0.f;
     const uint32_t ip = iord & 1u;  // parity of the per-block barriers in this item
     auto slot_par = [&](int sl, int occ) { return (iord * slot_uses(sl) + (uint32_t)occ) & 1u; };
-    // walk 1: the producer issues the blocks in slot 1 (even b), the second issuer
-    // those in slot 0 (odd b); walk 2: the producer Obar S^T, the second issuer
-    // -Dbar S^T of every block
-    auto walk1_block = [&](int b) {
-        const int dk0 = b * kBlkK, nk = nkb(b), sl = (b & 1) ? 0 : 1;
-        ok = tc::mbar_wait(&barT[sl], slot_par(sl, b >> 1), &g_err_bwdtc) && ok;
+    // walk-1 products of blocks b0 .. b0 + nb - 1 (one or two adjacent tiles from
+    // slot sbar_slot(b0)), committed to each block's barrier
+    auto walk1_blocks = [&](int b0, int nb) {
+        const int sl = sbar_slot(b0);
+        int nk = 0;
+        for (int b = b0; b < b0 + nb; ++b) {
+            ok = tc::mbar_wait(&barT[sbar_slot(b)], slot_par(sbar_slot(b), 0), &g_err_bwdtc) && ok;
+            nk += nkb(b);
+        }
         const tc::Tile tSp = tc::panel_tile(slot_ptr(sl), Dv, false);
-        tc::mma_tile(tb + kAK + dk0, tDmn, tSp, C, nk, Dv, false);
-        tc::mma_tile(tb + kAK + dk0, tDlomn, tSp, C, nk, Dv, true);
-        tc::mma_commit(&barMa1[b]);
+        tc::mma_tile(tb + kAK + b0 * kBlkK, tDmn, tSp, C, nk, Dv, false);
+        tc::mma_tile(tb + kAK + b0 * kBlkK, tDlomn, tSp, C, nk, Dv, true);
+        for (int b = b0; b < b0 + nb; ++b) tc::mma_commit(&barMa1[b]);
     };
     if (prod) {
-        if (nblk >= 2) load_tile(p.dSck, ci, 1, 0);  // the V tile is dead: phase 0 is done
-        for (int b = 0; b < nblk; b += 2) {  // walk 1, even blocks (slot 1)
-            walk1_block(b);
-            if (b + 2 < nblk) {
-                ok = tc::mbar_wait(&barMa1[b], ip, &g_err_bwdtc) && ok;
-                load_tile(p.dSck, ci, b + 2, 1);
-            }
-        }
-        for (int b = 0; b < nblk; ++b)  // every walk-1 product done
+        if (nblk >= 2) load_tile(p.dSck, ci, nblk == 3 ? 0 : 1, 0);  // the V tile is dead: phase 0 is done
+        walk1_blocks(0, nblk == 3 ? 2 : 1);
+        for (int b = 0; b < nblk; ++b)  // every walk-1 product done: slots 2, 3 free
             ok = tc::mbar_wait(&barMa1[b], ip, &g_err_bwdtc) && ok;
-        load_tile(p.ckpt, ci, 0, 0);
-        load_tile(p.dSck, ci, 0, 1);
-        if (nblk >= 2) {
-            load_tile(p.ckpt, ci, 1, 2);
-            load_tile(p.dSck, ci, 1, 3);
-        }
-        for (int b = 0; b < nblk; ++b) {  // walk 2
-            const int dk0 = b * kBlkK, nk = nkb(b);
-            const int sS = (b & 1) ? 2 : 0, sP = sS + 1;
-            const int occS = (b & 1) ? (b >> 1) : (nblk / 2 + (b >> 1));
-            ok = tc::mbar_wait(&barT[sS], slot_par(sS, occS), &g_err_bwdtc) && ok;
-            const tc::Tile tS = tc::panel_tile(slot_ptr(sS), Dv, false);
-            tc::mma_tile(tb + kAQ + dk0, tO, tS, C, nk, Dv, false);
-            tc::mma_commit(&barM2[b]);
-            if (b + 2 < nblk) {
-                ok = tc::mbar_wait(&barM2[b], ip, &g_err_bwdtc) && ok;
-                ok = tc::mbar_wait(&barG2[b], ip, &g_err_bwdtc) && ok;
-                load_tile(p.ckpt, ci, b + 2, sS);
-                load_tile(p.dSck, ci, b + 2, sP);
+        load_tile(p.ckpt, ci, w2_blk(0), 2);
+        if (nblk >= 2) load_tile(p.ckpt, ci, w2_blk(1), 3);
+        for (int q = 0; q < nblk; ++q) {  // walk 2: Obar S^T
+            const int b = w2_blk(q), sS = (q & 1) ? 3 : 2;
+            if (q == 2) {  // slot 2 again, once position 0's products and sums are done
+                ok = tc::mbar_wait(&barM2[0], ip, &g_err_bwdtc) && ok;
+                ok = tc::mbar_wait(&barG2[0], ip, &g_err_bwdtc) && ok;
+                load_tile(p.ckpt, ci, w2_blk(2), 2);
             }
+            ok = tc::mbar_wait(&barT[sS], slot_par(sS, q >> 1), &g_err_bwdtc) && ok;
+            const tc::Tile tS = tc::panel_tile(slot_ptr(sS), Dv, false);
+            tc::mma_tile(tb + kAQ + b * kBlkK, tO, tS, C, nkb(b), Dv, false);
+            tc::mma_commit(&barM2[q]);
         }
     } else if (prod2) {
-        for (int b = 1; b < nblk; b += 2) walk1_block(b);  // walk 1, odd blocks (slot 0)
-        for (int b = 0; b < nblk; ++b) {                     // walk 2: -Dbar S^T
-            const int nk = nkb(b);
-            const int sS = (b & 1) ? 2 : 0;
-            const int occS = (b & 1) ? (b >> 1) : (nblk / 2 + (b >> 1));
-            ok = tc::mbar_wait(&barT[sS], slot_par(sS, occS), &g_err_bwdtc) && ok;
-            if (b >= 2) ok = tc::mbar_wait(&barE2[b - 2], ip, &g_err_bwdtc) && ok;
-            const uint32_t wcol = (b & 1) ? kS2 : kS1;
+        if (nblk >= 2) walk1_blocks(nblk == 3 ? 2 : 1, 1);
+        for (int q = 0; q < nblk; ++q) {  // walk 2: -Dbar S^T
+            const int b = w2_blk(q), sS = (q & 1) ? 3 : 2;
+            ok = tc::mbar_wait(&barT[sS], slot_par(sS, q >> 1), &g_err_bwdtc) && ok;
+            if (q >= 2) ok = tc::mbar_wait(&barE2[q - 2], ip, &g_err_bwdtc) && ok;
+            const uint32_t wcol = (q & 1) ? kS2 : kS1;
             const tc::Tile tS = tc::panel_tile(slot_ptr(sS), Dv, false);
-            tc::mma_tile(tb + wcol, tNBmn, tS, C, nk, Dv, false);
-            tc::mma_commit(&barM2[b]);
+            tc::mma_tile(tb + wcol, tNBmn, tS, C, nkb(b), Dv, false);
+            tc::mma_commit(&barM2[q]);
         }
     } else if (epi) {
         ok = tc::mbar_wait(&barKQ, pit, &g_err_bwdtc) && ok;
@@ -614,13 +613,11 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
                 tc::tmem_wait_st();
             }
         }
-        for (int b = 0; b < nblk; ++b) {  // walk 2: <S, Sbar'>, dq *= gam, <dq, q>, Wbar tile
-            const int dk0 = b * kBlkK, nk = nkb(b);
-            const int sS = (b & 1) ? 2 : 0, sP = sS + 1;
-            const int occS = (b & 1) ? (b >> 1) : (nblk / 2 + (b >> 1));
-            const int occP = (b & 1) ? (b >> 1) : ((nblk + 1) / 2 + (b >> 1));
-            ok = tc::mbar_wait(&barT[sS], slot_par(sS, occS), &g_err_bwdtc) && ok;
-            ok = tc::mbar_wait(&barT[sP], slot_par(sP, occP), &g_err_bwdtc) && ok;
+        for (int q = 0; q < nblk; ++q) {  // walk 2: <S, Sbar'>, dq *= gam, <dq, q>, Wbar tile
+            const int b = w2_blk(q), dk0 = b * kBlkK, nk = nkb(b);
+            const int sS = (q & 1) ? 3 : 2, sP = sbar_slot(b);
+            ok = tc::mbar_wait(&barT[sS], slot_par(sS, q >> 1), &g_err_bwdtc) && ok;
+            ok = tc::mbar_wait(&barT[sP], slot_par(sP, 0), &g_err_bwdtc) && ok;
             const uint8_t* tSs = slot_ptr(sS);
             const uint8_t* tSps = slot_ptr(sP);
             const int bytes = nk * Dv * 2;
@@ -631,11 +628,14 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
 #pragma unroll
                 for (int i = 0; i < 8; ++i) gcb = fmaf(a8[i], b8[i], gcb);
             }
-            tc::mbar_arrive(&barG2[b]);
-            ok = tc::mbar_wait(&barM2[b], ip, &g_err_bwdtc) && ok;
+            tc::mbar_arrive(&barG2[q]);
+            ok = tc::mbar_wait(&barM2[q], ip, &g_err_bwdtc) && ok;
+            // Wbar of blocks 0 and 1 overwrites Sbar' block 2 in slot 4: every
+            // thread's sums over it (position 0) are done first
+            if (nblk == 3 && q >= 1) ok = tc::mbar_wait(&barG2[0], ip, &g_err_bwdtc) && ok;
             tc::tc_fence_after();
             if (ok) {
-                const uint32_t wcol = (b & 1) ? kS2 : kS1;
+                const uint32_t wcol = (q & 1) ? kS2 : kS1;
                 for (int cc = 32 * g; cc < nk; cc += 64) {
                     float aq[16], wv[16];
                     const uint32_t ta = tc::tmem_addr(tb, 32 * sp, kAQ + dk0 + cc);
@@ -653,13 +653,14 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
                     }
                     sq = row_pair_sum(sq);
                     if (lane < 16) gq[g * C + r] += sq;
-                    tile_put16(sm + L.W, Dk, c0, r, wv);
+                    st_bf16x8(sm + L.W + tc::panel_off(c0, r, C), wv);  // Wbar: panel tile
+                    st_bf16x8(sm + L.W + tc::panel_off(c0 + 8, r, C), wv + 8);
                     tc::tmem_st16x2<16>(ta, aq);
                 }
                 tc::tmem_wait_st();
             }
             tc::tc_fence_before();
-            tc::mbar_arrive(&barE2[b]);
+            tc::mbar_arrive(&barE2[q]);
         }
         // <S, Sbar'> of this CTA: warp sums by a fixed shuffle tree, then in warp order
 #pragma unroll
@@ -1014,6 +1015,8 @@ bool bwd_chunk_tc_supported(const Dims& d) {
     if (d.dtype != 1) return false;
     // TMEM: scratch 64 + dk and dq accumulators 2 Dk + scratch 64 <= 512
     if (d.Dk % 32 || d.Dv % 32 || d.Dk > 192 || d.Dv > 256) return false;
+    // the third Dk block of Sbar' sits in the Wbar tile ahead of that block's Wbar
+    if (d.Dk > 128 && (d.Dk - 128) * d.Dv * 2 > 16 * C * 16) return false;
     return smem_plan((int)d.Dk, (int)d.Dv).total + 2048 <= 227u * 1024u;
 }
 
