@@ -922,8 +922,12 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
         f2 suf = tot;  // inclusive suffix over lanes >= lane
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const f2 y{__shfl_down_sync(0xffffffffu, suf.hi, off), __shfl_down_sync(0xffffffffu, suf.lo, off)};
-            if (lane + off < 32) suf = f2_add(suf, y);
+            // every lane adds (zero past the last lane: the sum is unchanged, and no
+            // lane branches between the shuffles)
+            const float yh = __shfl_down_sync(0xffffffffu, suf.hi, off);
+            const float yl = __shfl_down_sync(0xffffffffu, suf.lo, off);
+            const bool in = lane + off < 32;
+            suf = f2_add(suf, f2{in ? yh : 0.f, in ? yl : 0.f});
         }
         const f2 after = f2_add(suf, f2{-tot.hi, -tot.lo});  // lanes > lane
         const f2 d1 = f2_add(x1, after);
