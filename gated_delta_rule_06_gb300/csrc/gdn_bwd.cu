@@ -472,8 +472,12 @@ __device__ __forceinline__ void bwd_qk_body(const Dims& d, const Ptrs& p, int64_
     const bool act = valid && 8 * sub < Dk;
     const int c0 = act ? 8 * sub : 0;
     const int64_t xoff = ((bb * d.T + t) * d.Hk + j) * Dk + c0;
-    const int64_t hstride = d.Tp * Dk;  // next value head of the group
-    const int64_t off0 = ((bb * d.Hv + j * d.G) * d.Tp + t) * Dk + c0;
+    // partials: fp32 [B, Hv, Tp, Dk] from the CUDA-core kernels, bf16 [B, Tp, Hv, Dk]
+    // from the tensor-core kernel (a group's rows of one step side by side)
+    constexpr bool kStepMajor = sizeof(PT) == 2;
+    const int64_t hstride = kStepMajor ? (int64_t)Dk : d.Tp * Dk;  // next value head of the group
+    const int64_t off0 = kStepMajor ? ((bb * d.Tp + t) * d.Hv + j * d.G) * Dk + c0
+                                    : ((bb * d.Hv + j * d.G) * d.Tp + t) * Dk + c0;
     const PT* dqh = reinterpret_cast<const PT*>(p.dqh) + off0;
     const PT* dkh = reinterpret_cast<const PT*>(p.dkh) + off0;
     float u[2][8], y[2][8];

@@ -954,16 +954,20 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
         }
     }
     if (epi && ok) {
-        // per-value-head partials as bf16 (summed over the group and normalised in fp32)
-        uint8_t* dqh = reinterpret_cast<uint8_t*>(p.dqh) + (gbase * Dk) * 2;
-        uint8_t* dkh = reinterpret_cast<uint8_t*>(p.dkh) + (gbase * Dk) * 2;
+        // per-value-head partials as bf16 [B, Tp, Hv, Dk] (summed over the group
+        // and normalised in fp32; a group's rows of one step are then contiguous
+        // for the reduction)
+        const int64_t prow = d.Hv * Dk;  // elements from one step's rows to the next
+        const int64_t pbase = (((int64_t)bb * d.Tp + t0) * d.Hv + h) * Dk;
+        uint8_t* dqh = reinterpret_cast<uint8_t*>(p.dqh) + pbase * 2;
+        uint8_t* dkh = reinterpret_cast<uint8_t*>(p.dkh) + pbase * 2;
         acc_rows2(tb, kAQ, Dk, [&](int r, int c0, const float (&x)[16]) {
-            st_bf16x8(dqh + ((int64_t)r * Dk + c0) * 2, x);
-            st_bf16x8(dqh + ((int64_t)r * Dk + c0 + 8) * 2, x + 8);
+            st_bf16x8(dqh + ((int64_t)r * prow + c0) * 2, x);
+            st_bf16x8(dqh + ((int64_t)r * prow + c0 + 8) * 2, x + 8);
         });
         acc_rows2(tb, kAK, Dk, [&](int r, int c0, const float (&x)[16]) {
-            st_bf16x8(dkh + ((int64_t)r * Dk + c0) * 2, x);
-            st_bf16x8(dkh + ((int64_t)r * Dk + c0 + 8) * 2, x + 8);
+            st_bf16x8(dkh + ((int64_t)r * prow + c0) * 2, x);
+            st_bf16x8(dkh + ((int64_t)r * prow + c0 + 8) * 2, x + 8);
         });
     }
     tc::tc_fence_before();

@@ -101,7 +101,7 @@ struct Ptrs {
     float* dSck;   // [B, Hv, NC, Dk, Dv] state cotangent at each chunk END
     float* Dbar;   // [B, Hv, Tp, Dv] cotangent of Delta
     float* dqh;    // [B, Hv, Tp, Dk] cotangent of the normalised q, per value head
-    float* dkh;    // [B, Hv, Tp, Dk]  (both bf16 on the tensor-core path)
+    float* dkh;    // [B, Hv, Tp, Dk]  (both bf16 [B, Tp, Hv, Dk] on the tensor-core path)
     float* dl;     // [B, Hv, Tp] cotangent of the log-decay
     float* dbeta;  // [B, Hv, Tp]
     float* part;   // [2, B, NC, Hv] per-chunk partial sums for dA_log, ddt_bias
