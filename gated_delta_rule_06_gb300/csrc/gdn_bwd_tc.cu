@@ -257,7 +257,7 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
     // -Dbar S^T products done, barG2[b] its tiles read by the <S, Sbar'> sums,
     // barE2[b] its epilogue done (Wbar scratch free); barT[s]: arrivals of the
     // tiles of slot s (several per item)
-    __shared__ uint64_t bar, barOV, barL, barKQ, barT[5], barMa1[4], barM2[4], barG2[4], barE2[4];
+    __shared__ uint64_t bar, barOV, barL, barKQ, barAQ, barT[5], barMa1[4], barM2[4], barG2[4], barE2[4];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int next_item;
     const int Dk = (int)d.Dk, Dv = (int)d.Dv;
@@ -402,6 +402,7 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
         tc::mbar_init(&barOV, 1);
         tc::mbar_init(&barL, 1);
         tc::mbar_init(&barKQ, 1);
+        tc::mbar_init(&barAQ, 1);  // the producer's phase-3 chain (dq complete), once per item
         tc::mbar_init(&barT[4], 1);
         for (int i = 0; i < 4; ++i) {
             tc::mbar_init(&barT[i], 1);
@@ -885,6 +886,7 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
     if (prod) {
         tc::mma_tile(tb + kAQ, kmaj(sm, L.PMk, C), tKmn, C, Dk, C, true);
         tc::mma_commit(&bar);
+        tc::mma_commit(&barAQ);
     } else if (prod2) {
         tc::mma_tile(tb + kAK, mnmaj(sm, L.PMq, C), tQmn, C, Dk, C, true);
         tc::mma_tile(tb + kAK, kmaj(sm, L.Hk, C), tKmn, C, Dk, C, true);
@@ -937,6 +939,21 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
         p.dbeta[gbase + 2 * lane] = betab[2 * lane];
         p.dbeta[gbase + 2 * lane + 1] = betab[2 * lane + 1];
     }
+    // dq is complete once the producer's phase-3 chain is: its partials go out
+    // while the second issuer's dk products still run
+    const int64_t prow = d.Hv * Dk;  // partials [B, Tp, Hv, Dk]: elements from one step's rows to the next
+    const int64_t pbase = (((int64_t)bb * d.Tp + t0) * d.Hv + h) * Dk;
+    if (epi) {
+        ok = tc::mbar_wait(&barAQ, ip, &g_err_bwdtc) && ok;
+        tc::tc_fence_after();
+        if (ok) {
+            uint8_t* dqh = reinterpret_cast<uint8_t*>(p.dqh) + pbase * 2;
+            acc_rows2(tb, kAQ, Dk, [&](int r, int c0, const float (&x)[16]) {
+                st_bf16x8(dqh + ((int64_t)r * prow + c0) * 2, x);
+                st_bf16x8(dqh + ((int64_t)r * prow + c0 + 8) * 2, x + 8);
+            });
+        }
+    }
     // the producer waits too: once the phase-3 products are done, every operand
     // tile of this item is dead and the next item's loads go out, under the
     // final stores below
@@ -957,14 +974,7 @@ __device__ __forceinline__ void bwd_chunk_body(const Dims& d, const Ptrs& p, con
         // per-value-head partials as bf16 [B, Tp, Hv, Dk] (summed over the group
         // and normalised in fp32; a group's rows of one step are then contiguous
         // for the reduction)
-        const int64_t prow = d.Hv * Dk;  // elements from one step's rows to the next
-        const int64_t pbase = (((int64_t)bb * d.Tp + t0) * d.Hv + h) * Dk;
-        uint8_t* dqh = reinterpret_cast<uint8_t*>(p.dqh) + pbase * 2;
         uint8_t* dkh = reinterpret_cast<uint8_t*>(p.dkh) + pbase * 2;
-        acc_rows2(tb, kAQ, Dk, [&](int r, int c0, const float (&x)[16]) {
-            st_bf16x8(dqh + ((int64_t)r * prow + c0) * 2, x);
-            st_bf16x8(dqh + ((int64_t)r * prow + c0 + 8) * 2, x + 8);
-        });
         acc_rows2(tb, kAK, Dk, [&](int r, int c0, const float (&x)[16]) {
             st_bf16x8(dkh + ((int64_t)r * prow + c0) * 2, x);
             st_bf16x8(dkh + ((int64_t)r * prow + c0 + 8) * 2, x + 8);
