@@ -185,6 +185,7 @@ bool make_tmaps(const gdn::Dims& d, const void* v, const void* dO, const void* o
              gdn::encode_row_tile_map(&m->dOf, dO, d.B, d.T, d.Hv, d.Dv, (int)d.Dv);
     if (ok && o) ok = gdn::encode_row_major_map(&m->o, o, d.B, d.T, d.Hv * d.Dv, vt);
     if (ok && U) ok = gdn::encode_f32_rows_map(&m->U, U, d.B * d.Hv * d.Tp, d.Dv, vt);
+    if (ok && U && d.Dv % 32 == 0) ok = gdn::encode_f32_rows_map_sw128(&m->Us, U, d.B * d.Hv * d.Tp, d.Dv);
     return ok;
 }
 
@@ -271,6 +272,18 @@ bool encode_f32_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t
     const cuuint32_t unit[2] = {1, 1};
     return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
                   unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_f32_rows_map_sw128(CUtensorMap* m, const void* base, int64_t rows, int64_t cols_total) {
+    const auto encode = tensor_map_encoder();
+    if (encode == nullptr || cols_total % 32) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols_total, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(cols_total * 4)};
+    const cuuint32_t box[2] = {32, (cuuint32_t)kChunk};
+    const cuuint32_t unit[2] = {1, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+                  unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -124,7 +124,10 @@ __host__ __device__ inline F1Smem f1_plan(int Dk, int Dv) {
     return s;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs p) {
+// u_tma: U leaves by TMA stores of swizzled 64 x 32 boxes staged in the A / X
+// space (dead once the W / U products are done) instead of per-thread stores
+__global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs p, const __grid_constant__ Tmaps tm,
+                                                                 int u_tma) {
     extern __shared__ __align__(1024) uint8_t sm[];
     __shared__ uint64_t bar, barKQ;
     __shared__ uint32_t tmem_sh;
@@ -367,16 +370,36 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_chunk_tc_kernel(Dims d, Ptrs 
         tc::tc_fence_after();
         ucol = 0;
     }
-    if (ok) {
+    if (ok && !u_tma) {
         float* U = p.U + gbase * Dv;
         acc_rows_all(tb, ucol, Dv, [&](int r, int c0, const float (&x)[8]) {
             float4* dst = reinterpret_cast<float4*>(U + (int64_t)r * Dv + c0);
             dst[0] = make_float4(x[0], x[1], x[2], x[3]);
             dst[1] = make_float4(x[4], x[5], x[6], x[7]);
         });
+    } else if (ok) {
+        // box b (columns 32 b .. 32 b + 31) 8 KB after the box before it, from the
+        // first 1024-byte aligned shared address in the A / X space (the swizzle
+        // follows the address bits): row r's 16-byte piece j at r * 128 +
+        // ((j ^ (r % 8)) * 16), the layout of the 128-byte swizzle
+        uint8_t* stage = sm + L.A + ((1024u - (tc::smem_u32(sm + L.A) & 1023u)) & 1023u);
+        acc_rows_all(tb, ucol, Dv, [&](int r, int c0, const float (&x)[8]) {
+            uint8_t* box = stage + (c0 >> 5) * (C * 128) + r * 128;
+            const int j = (c0 & 31) >> 2;
+            *reinterpret_cast<float4*>(box + (((j) ^ (r & 7)) << 4)) = make_float4(x[0], x[1], x[2], x[3]);
+            *reinterpret_cast<float4*>(box + (((j + 1) ^ (r & 7)) << 4)) = make_float4(x[4], x[5], x[6], x[7]);
+        });
+        tc::fence_async_smem();  // generic-proxy writes -> the TMA store reads them
     }
     tc::tc_fence_before();
     __syncthreads();
+    if (ok && u_tma && tid == 0) {
+        const uint8_t* stage = sm + L.A + ((1024u - (tc::smem_u32(sm + L.A) & 1023u)) & 1023u);
+        for (int bx = 0; bx < Dv / 32; ++bx)
+            tc::tma_store_2d(&tm.Us, stage + bx * (C * 128), 32 * bx, (int)gbase);
+        tc::bulk_commit();
+        tc::bulk_wait_all();  // the stores have read the staging space and are done
+    }
     if (warp == 0) tc::tmem_dealloc(tb, kTmemCols);
 }
 
@@ -394,7 +417,12 @@ cudaError_t launch_fwd_chunk_tc(const Dims& d, const Ptrs& p, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)d.NC, (unsigned)d.Hv, (unsigned)d.B);
-    kern<<<grid, kThreads, smem, s>>>(d, p);
+    // the U staging needs 64 Dv fp32 (plus up to 1 KB of alignment) in the A / X
+    // space (two padded 64 x 64 fp32 matrices) and a 32-column box grid
+    const int u_tma = p.tmaps != nullptr && d.Dv % 32 == 0 &&
+                      (uint32_t)(C * d.Dv * 4) + 1024u <= 2u * (uint32_t)(C * LDT * 4);
+    Tmaps tmz{};
+    kern<<<grid, kThreads, smem, s>>>(d, p, u_tma ? *p.tmaps : tmz, u_tma);
     count_launches(1);
     return cudaPeekAtLastError();
 }

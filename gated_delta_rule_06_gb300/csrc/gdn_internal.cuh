@@ -41,6 +41,8 @@ struct Dims {
 // min(Dv, 128) columns (row-major), for the forward scan.
 struct Tmaps {
     CUtensorMap v, dO, dOf, o, U;  // dO: boxes min(Dv, 128) wide; dOf: Dv wide
+    // U again for the chunk kernel's stores: boxes of 64 rows x 32 fp32, 128-byte swizzle
+    CUtensorMap Us;
 };
 // box `cols` columns wide (multiple of 8, <= 256); false if the driver refuses
 bool encode_row_tile_map(CUtensorMap* m, const void* base, int64_t B, int64_t T, int64_t H,
@@ -49,6 +51,9 @@ bool encode_row_major_map(CUtensorMap* m, const void* base, int64_t B, int64_t T
                           int cols);
 // fp32 [rows, cols_total] row-major, box of 64 rows x `cols` columns
 bool encode_f32_rows_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols_total, int cols);
+// the same rows in boxes of 64 rows x 32 columns with the 128-byte swizzle: the
+// 16-byte piece j of box row r sits at r * 128 + ((j ^ (r % 8)) * 16)
+bool encode_f32_rows_map_sw128(CUtensorMap* m, const void* base, int64_t rows, int64_t cols_total);
 
 // Every device buffer the kernels touch.  Inputs/outputs come from the
 // caller; the rest are carved out of the caller's `saved` and `ws` buffers.

@@ -311,6 +311,15 @@ __device__ __forceinline__ void tma_store_3d(const void* map, const void* src, i
                  : "memory");
 }
 
+// 2-d tiled store of a box from shared memory at coordinates c0 (innermost), c1
+// (non-negative), tracked in this thread's bulk groups
+__device__ __forceinline__ void tma_store_2d(const void* map, const void* src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(smem_u32(src))
+                 : "memory");
+}
+
 // ---- descriptors -------------------------------------------------------------------
 // shared-memory matrix descriptor, no swizzle, sm_100 version field = 1
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
