@@ -120,17 +120,34 @@ __device__ __forceinline__ void prep_norms_img_body(const Dims& d, const __nv_bf
     uint8_t* sq = stage;
     uint8_t* sk = stage + ng * kPanelPad;
     const int64_t t0 = (int64_t)c * kChunk;
-    for (int e = tid; e < kChunk * ng; e += blockDim.x) {  // row r = e / ng, piece g = e % ng
-        const int r = e / ng, g = e - (e / ng) * ng;
-        const int64_t t = t0 + r;
-        uint4 uq = make_uint4(0u, 0u, 0u, 0u), uk = uq;
-        if (t < d.T) {
-            const int64_t base = (((int64_t)bb * d.T + t) * d.Hk + j) * d.Dk + 8 * g;
-            uq = *reinterpret_cast<const uint4*>(q + base);
-            uk = *reinterpret_cast<const uint4*>(k + base);
+    // a thread's row pieces go in rounds of 4 of q and 4 of k, each round's loads
+    // issued before its stores so that they are in flight together
+    constexpr int kPer = 4;
+    for (int e0 = tid; e0 < kChunk * ng; e0 += kPer * 256) {
+        uint4 uq[kPer], uk[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {  // row r = e / ng, piece g = e % ng
+            const int e = e0 + u * 256;
+            uq[u] = uk[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (e < kChunk * ng) {
+                const int r = e / ng, g = e - (e / ng) * ng;
+                const int64_t t = t0 + r;
+                if (t < d.T) {
+                    const int64_t base = (((int64_t)bb * d.T + t) * d.Hk + j) * d.Dk + 8 * g;
+                    uq[u] = *reinterpret_cast<const uint4*>(q + base);
+                    uk[u] = *reinterpret_cast<const uint4*>(k + base);
+                }
+            }
         }
-        *reinterpret_cast<uint4*>(sq + g * kPanelPad + r * 16) = uq;
-        *reinterpret_cast<uint4*>(sk + g * kPanelPad + r * 16) = uk;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int e = e0 + u * 256;
+            if (e < kChunk * ng) {
+                const int r = e / ng, g = e - (e / ng) * ng;
+                *reinterpret_cast<uint4*>(sq + g * kPanelPad + r * 16) = uq[u];
+                *reinterpret_cast<uint4*>(sk + g * kPanelPad + r * 16) = uk[u];
+            }
+        }
     }
     __syncthreads();
     if (tid < 2 * kChunk) {  // thread r: row r of q; thread 64 + r: row r of k
