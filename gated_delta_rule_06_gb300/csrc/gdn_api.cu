@@ -292,11 +292,12 @@ bool tc_path(const Dims& d) {
            bwd_chunk_tc_supported(d);
 }
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n); }
+unsigned int read_clear_error_bwdr();  // the streamed q / k reduction (gdn_bwd.cu)
 unsigned int read_clear_error_all() {
     const unsigned int words[] = {read_clear_error_selftest(), read_clear_error_bwdtc(),
                                   read_clear_error_scantc(), read_clear_error_fwdtc(),
                                   read_clear_error_scanta(), read_clear_error_decode(),
-                                  read_clear_error_kctc()};
+                                  read_clear_error_kctc(), read_clear_error_bwdr()};
     unsigned int v = 0;
     for (unsigned int w : words) {
         if (w == ~0u) return ~0u;

@@ -24,8 +24,12 @@
 //       backward and the per-head sums for dA_log / ddt_bias as fixed-order
 //       two-stage sums (mlx-lm page, "Design notes": no atomics, deterministic).
 #include "gdn_internal.cuh"
+#include "gdn_tc.cuh"
 
 namespace gdn {
+
+GDN_ERROR_WORD(bwdr)
+
 namespace {
 
 // ---------------------------------------------------------------------------
@@ -534,56 +538,85 @@ __device__ __forceinline__ void bwd_qk_body(const Dims& d, const Ptrs& p, int64_
 }
 
 // da / db and per-(b, chunk, head) partial sums of chunk c, batch bb, heads
-// 8 hz .. 8 hz + 7; one warp per head in the sums
+// 8 hz .. 8 hz + 7.  The element-wise part: threads idx0, idx0 + step, ... of
+// the 64 x nh (step, head) pairs; each writes its da / db and its two summands
+// into sA / sD.
 constexpr int kGateHeadsB = 8;
 template <typename TI>
-__device__ __forceinline__ void bwd_gate_body(const Dims& d, const Ptrs& p, int c, int bb, int hz) {
-    __shared__ float sA[kChunk][kGateHeadsB + 1];
-    __shared__ float sD[kChunk][kGateHeadsB + 1];
+__device__ __forceinline__ void bwd_gate_elems(const Dims& d, const Ptrs& p, int c, int bb, int hz,
+                                               int idx0, int step, float (*sA)[kGateHeadsB + 1],
+                                               float (*sD)[kGateHeadsB + 1]) {
     const int h0 = hz * kGateHeadsB;
     const int nh = (int)(d.Hv - h0 < kGateHeadsB ? d.Hv - h0 : kGateHeadsB);
     const int64_t t0 = (int64_t)c * kChunk;
     const TI* a = (const TI*)p.a;
     TI* da = (TI*)p.da;
     TI* db = (TI*)p.db;
-    for (int idx = threadIdx.x; idx < kChunk * nh; idx += blockDim.x) {
-        const int i = idx / nh, hh = idx % nh, h = h0 + hh;
-        const int64_t t = t0 + i;
-        float vA = 0.f, vD = 0.f;
-        if (t < d.T) {
-            const int64_t ix = ((int64_t)bb * d.T + t) * d.Hv + h;
-            float ga = 0.f, gb = 0.f;
-            if (d.gates == 1) {  // cotangents of the given log_decay and beta
-                if (p.mask == nullptr || p.mask[bb * d.T + t] != 0) {
-                    const int64_t gx = ((int64_t)bb * d.Hv + h) * d.Tp + t;
-                    ga = p.dl[gx];
-                    gb = p.dbeta[gx];
-                }
-            } else if (p.mask == nullptr || p.mask[bb * d.T + t] != 0) {
+    // kGrp pairs at a time: every load of the group goes out before the first use
+    constexpr int kGrp = 4;
+    for (int base = idx0; base < kChunk * nh; base += kGrp * step) {
+        float lb[kGrp], xa[kGrp], be[kGrp], dbe[kGrp];
+        bool on[kGrp], live[kGrp];
+#pragma unroll
+        for (int e = 0; e < kGrp; ++e) {
+            const int idx = base + e * step;
+            const int i = idx / nh, h = h0 + idx % nh;
+            const int64_t t = t0 + i;
+            live[e] = idx < kChunk * nh && t < d.T;
+            on[e] = live[e] && (p.mask == nullptr || p.mask[bb * d.T + t] != 0);
+            lb[e] = xa[e] = be[e] = dbe[e] = 0.f;
+            if (on[e]) {
                 const int64_t gx = ((int64_t)bb * d.Hv + h) * d.Tp + t;
-                const float lb = p.dl[gx];
-                const float x = ldf(a + ix) + p.dt_bias[h];
-                const float xc = fminf(x, kSoftplusClamp);
-                const float eA = expf(p.A_log[h]);
-                const float l = -eA * log1pf(expf(xc));
-                const float sg = x <= kSoftplusClamp ? 1.f / (1.f + expf(-xc)) : 0.f;
-                ga = lb * (-eA) * sg;
-                const float be = p.beta[gx];
-                gb = p.dbeta[gx] * be * (1.f - be);
-                vA = lb * l;
-                vD = ga;
+                lb[e] = p.dl[gx];
+                dbe[e] = p.dbeta[gx];
+                if (d.gates != 1) {
+                    xa[e] = ldf(a + ((int64_t)bb * d.T + t) * d.Hv + h) + p.dt_bias[h];
+                    be[e] = p.beta[gx];
+                }
             }
-            stf(da + ix, ga);
-            stf(db + ix, gb);
         }
-        sA[i][hh] = vA;
-        sD[i][hh] = vD;
+#pragma unroll
+        for (int e = 0; e < kGrp; ++e) {
+            const int idx = base + e * step;
+            if (idx >= kChunk * nh) break;
+            const int i = idx / nh, hh = idx % nh, h = h0 + hh;
+            float vA = 0.f, vD = 0.f;
+            if (live[e]) {
+                const int64_t ix = ((int64_t)bb * d.T + t0 + i) * d.Hv + h;
+                float ga = 0.f, gb = 0.f;
+                if (d.gates == 1) {  // cotangents of the given log_decay and beta
+                    ga = lb[e];
+                    gb = dbe[e];
+                } else if (on[e]) {
+                    const float x = xa[e];
+                    const float xc = fminf(x, kSoftplusClamp);
+                    const float eA = expf(p.A_log[h]);
+                    const float l = -eA * log1pf(expf(xc));
+                    const float sg = x <= kSoftplusClamp ? 1.f / (1.f + expf(-xc)) : 0.f;
+                    ga = lb[e] * (-eA) * sg;
+                    gb = dbe[e] * be[e] * (1.f - be[e]);
+                    vA = lb[e] * l;
+                    vD = ga;
+                }
+                stf(da + ix, ga);
+                stf(db + ix, gb);
+            }
+            sA[i][hh] = vA;
+            sD[i][hh] = vD;
+        }
     }
-    if (d.gates == 1) return;  // no per-head gate parameters
-    __syncthreads();
-    // fixed-order sum over the 64 steps: one warp per head, pairwise tree
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int hh = warp; hh < nh; hh += blockDim.x >> 5) {
+}
+
+// The fixed-order sums over the chunk's 64 steps (after bwd_gate_elems, once
+// its writes to sA / sD are visible): warps w0, w0 + nw, ... take one head
+// each, pairwise then an xor tree over the lanes.
+__device__ __forceinline__ void bwd_gate_sums(const Dims& d, const Ptrs& p, int c, int bb, int hz,
+                                              int w0, int nw, float (*sA)[kGateHeadsB + 1],
+                                              float (*sD)[kGateHeadsB + 1]) {
+    const int h0 = hz * kGateHeadsB;
+    const int nh = (int)(d.Hv - h0 < kGateHeadsB ? d.Hv - h0 : kGateHeadsB);
+    const int lane = threadIdx.x & 31;
+    for (int hh = w0; hh < nh; hh += nw) {
         float x = sA[2 * lane][hh] + sA[2 * lane + 1][hh];
         float y = sD[2 * lane][hh] + sD[2 * lane + 1][hh];
 #pragma unroll
@@ -597,6 +630,17 @@ __device__ __forceinline__ void bwd_gate_body(const Dims& d, const Ptrs& p, int 
             p.part[d.B * d.NC * d.Hv + pi] = y;
         }
     }
+}
+
+// one gate unit by a whole CTA
+template <typename TI>
+__device__ __forceinline__ void bwd_gate_body(const Dims& d, const Ptrs& p, int c, int bb, int hz) {
+    __shared__ float sA[kChunk][kGateHeadsB + 1];
+    __shared__ float sD[kChunk][kGateHeadsB + 1];
+    bwd_gate_elems<TI>(d, p, c, bb, hz, threadIdx.x, blockDim.x, sA, sD);
+    if (d.gates == 1) return;  // no per-head gate parameters
+    __syncthreads();
+    bwd_gate_sums(d, p, c, bb, hz, threadIdx.x >> 5, blockDim.x >> 5, sA, sD);
 }
 
 // The two independent parts of the reduction in one launch: blocks
@@ -620,6 +664,265 @@ __global__ void __launch_bounds__(256) bwd_reduce_kernel(Dims d, Ptrs p) {
 template <typename TI, int W>
 __global__ void __launch_bounds__(256) bwd_qk_kernel(Dims d, Ptrs p) {
     bwd_qk_body<TI, float, W>(d, p, blockIdx.x);
+}
+
+// ---------------------------------------------------------------------------
+// bwd_reduce, streamed form (bf16 step-major partials of the tensor-core path)
+// ---------------------------------------------------------------------------
+// A unit is a run of n consecutive steps of one batch, or one step's key heads
+// j0 .. j0 + nj - 1 (nj < Hk when a step's rows alone pass the stage size).
+// Its q and k rows ([B, T, Hk, Dk]) and its per-value-head q / k cotangent
+// partials ([B, Tp, Hv, Dk], value heads j G .. j G + G - 1 of key head j) are
+// each one contiguous run, so one thread brings a unit into a shared-memory
+// stage with four bulk copies; kQkStages units are in flight per CTA while
+// eight warps reduce the rows of the oldest from shared memory, with the same
+// arithmetic in the same order as bwd_qk_body.  A ninth warp takes the gate
+// units (da / db and the per-chunk head partials) meanwhile.
+constexpr int kQkStages = 3;
+constexpr uint32_t kQkStageTarget = 32 * 1024;  // bytes of one stage at the most, where a key head fits
+constexpr int kQkWarps = 8;
+
+struct QkRun {
+    int n, nj, ks;    // steps per unit, key heads per unit, units per step (Hk / nj)
+    uint32_t stage;   // bytes of one full unit: q, k rows then dq, dk partials
+};
+
+constexpr int kQkPasses = 2;  // row passes of the 8 warps a unit takes at the most
+
+// rows a unit may hold: kQkPasses passes of 8 warps x (32 / lanes per row)
+int qk_max_rows(const Dims& d) { return kQkPasses * kQkWarps * (32 / qk_lanes(d.Dk)); }
+
+QkRun qk_run(const Dims& d) {
+    const int64_t per_kh = 4 * (1 + d.G) * d.Dk;  // one (step, key head): 2 rows + 2 G partial rows, bf16
+    const int64_t maxr = qk_max_rows(d);
+    QkRun r{1, (int)d.Hk, 1, 0};
+    if (per_kh * d.Hk <= kQkStageTarget && d.Hk <= maxr) {
+        r.n = (int)(kQkStageTarget / (per_kh * d.Hk));
+        if (r.n > maxr / d.Hk) r.n = (int)(maxr / d.Hk);
+        if (r.n > d.T) r.n = (int)d.T;
+    } else {
+        r.ks = (int)d.Hk;  // one key head per unit unless a larger divisor of Hk fits
+        for (int ks = 2; ks < d.Hk; ++ks)
+            if (d.Hk % ks == 0 && per_kh * (d.Hk / ks) <= kQkStageTarget && d.Hk / ks <= maxr) {
+                r.ks = ks;
+                break;
+            }
+        r.nj = (int)(d.Hk / r.ks);
+    }
+    r.stage = (uint32_t)(per_kh * r.n * r.nj);
+    return r;
+}
+
+// the streamed form applies: bf16 tensor-core partials, and three stages fit
+// twice per SM
+bool qk_stream_ok(const Dims& d) {
+    if (!tc_path(d) || d.Dk % 8 || d.Dk > 256) return false;
+    const QkRun r = qk_run(d);
+    if ((int64_t)r.n * r.nj > qk_max_rows(d)) return false;
+    if (d.B * ((d.T + r.n - 1) / r.n) * r.ks >= (int64_t)1 << 31) return false;  // 32-bit unit indices
+    return (size_t)kQkStages * r.stage <= 100u * 1024u;
+}
+
+// eight bf16 at a shared-memory address, as fp32
+__device__ __forceinline__ void lds8(uint32_t a, float* v) {
+    uint32_t w[4];
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                 : "r"(a));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+template <int LPR>
+__global__ void __launch_bounds__(kQkWarps * 32 + 32, 2)
+    bwd_reduce_stream_kernel(Dims d, Ptrs p, QkRun ru) {
+    extern __shared__ __align__(128) uint8_t smq[];
+    __shared__ uint64_t full[kQkStages];
+    __shared__ int s_fail;
+    __shared__ float gA[kChunk][kGateHeadsB + 1];
+    __shared__ float gD[kChunk][kGateHeadsB + 1];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < kQkStages; ++s) tc::mbar_init(&full[s], 1);
+        tc::fence_mbar_init();
+        s_fail = 0;
+    }
+    __syncthreads();
+    if (warp == kQkWarps) {
+        // gate units, as the gate blocks of bwd_reduce_kernel take them
+        const int64_t nhz = (d.Hv + kGateHeadsB - 1) / kGateHeadsB;
+        const int64_t ngate = d.NC * d.B * nhz;
+        for (int64_t g = blockIdx.x; g < ngate; g += gridDim.x) {
+            const int c = (int)(g % d.NC), bb = (int)((g / d.NC) % d.B), hz = (int)(g / (d.NC * d.B));
+            bwd_gate_elems<__nv_bfloat16>(d, p, c, bb, hz, lane, 32, gA, gD);
+            __syncwarp();
+            if (d.gates != 1) bwd_gate_sums(d, p, c, bb, hz, 0, 1, gA, gD);
+            __syncwarp();
+        }
+        return;
+    }
+    const int Dk = (int)d.Dk, G = (int)d.G;
+    const int64_t nt = (d.T + ru.n - 1) / ru.n;  // units per batch and key-head range
+    const int64_t nunits = d.B * nt * ru.ks;
+    const uint32_t qb = (uint32_t)(ru.n * ru.nj * Dk * 2);  // bytes of the q (and k) rows of a full unit
+    const uint32_t hb = qb * (uint32_t)G;                   // bytes of the dq (and dk) partials
+    struct Unit {
+        int bb, ne, j0;
+        int64_t t0;
+    };
+    // unit counts stay below 2^31 (checked on the host): 32-bit divisions
+    const uint32_t per_b = (uint32_t)(nt * ru.ks);
+    auto unit = [&](int64_t u) {
+        Unit x;
+        const uint32_t u32 = (uint32_t)u;
+        x.bb = (int)(u32 / per_b);
+        const uint32_t rem = u32 - (uint32_t)x.bb * per_b;
+        const uint32_t tq = rem / (uint32_t)ru.ks;
+        x.t0 = (int64_t)tq * ru.n;
+        x.j0 = (int)(rem - tq * (uint32_t)ru.ks) * ru.nj;
+        x.ne = (int)(d.T - x.t0 < ru.n ? d.T - x.t0 : ru.n);
+        return x;
+    };
+    const __nv_bfloat16* q = (const __nv_bfloat16*)p.q;
+    const __nv_bfloat16* k = (const __nv_bfloat16*)p.k;
+    const __nv_bfloat16* dqh = (const __nv_bfloat16*)p.dqh;
+    const __nv_bfloat16* dkh = (const __nv_bfloat16*)p.dkh;
+    auto issue = [&](int64_t u, int s) {
+        const Unit x = unit(u);
+        uint8_t* st = smq + (size_t)s * ru.stage;
+        const uint32_t b1 = (uint32_t)(x.ne * ru.nj * Dk * 2), bh = b1 * (uint32_t)G;
+        const int64_t xo = ((x.bb * d.T + x.t0) * d.Hk + x.j0) * Dk;
+        const int64_t ho = ((x.bb * d.Tp + x.t0) * d.Hv + (int64_t)x.j0 * G) * Dk;
+        tc::mbar_arrive_expect_tx(&full[s], 2 * b1 + 2 * bh);
+        tc::bulk_g2s(st, q + xo, b1, &full[s]);
+        tc::bulk_g2s(st + qb, k + xo, b1, &full[s]);
+        tc::bulk_g2s(st + 2 * qb, dqh + ho, bh, &full[s]);
+        tc::bulk_g2s(st + 2 * qb + hb, dkh + ho, bh, &full[s]);
+    };
+    const int64_t first = blockIdx.x, stride = gridDim.x;
+    int64_t issued = 0;  // thread 0: units of this CTA issued so far
+    if (tid == 0)
+        for (int s = 0; s < kQkStages && first + s * stride < nunits; ++s, ++issued) issue(first + s * stride, s);
+    const int sub = lane % LPR;
+    const int c0 = 8 * sub;
+    const bool colact = c0 < Dk;
+    const float sq = rsqrtf((float)Dk);
+    constexpr int kPass = kQkWarps * (32 / LPR);
+    constexpr int kMaxPass = kQkPasses;
+    // passes of the row loop a unit needs (uniform over the CTA)
+    const int npass = (ru.n * ru.nj + kPass - 1) / kPass;
+    // this thread's row of pass ps: key head j0 + rj[ps] of step t0 + rt[ps]
+    int rj[kMaxPass], rt[kMaxPass];
+#pragma unroll
+    for (int ps = 0; ps < kMaxPass; ++ps) {
+        const int r = ps * kPass + warp * (32 / LPR) + lane / LPR;
+        rj[ps] = r % ru.nj;
+        rt[ps] = r / ru.nj;
+    }
+    // the per-row norms of a unit (plain loads), taken one unit ahead
+    auto norms = [&](Unit x, int R, float (&rqv)[kMaxPass], float (&rkv)[kMaxPass]) {
+#pragma unroll
+        for (int ps = 0; ps < kMaxPass; ++ps) {
+            if (ps >= npass) break;
+            const int r = ps * kPass + warp * (32 / LPR) + lane / LPR;
+            rqv[ps] = rkv[ps] = 0.f;
+            if (r < R) {
+                const int64_t o = ((int64_t)x.bb * d.Hk + x.j0 + rj[ps]) * d.Tp + x.t0 + rt[ps];
+                rqv[ps] = p.rq[o];
+                rkv[ps] = p.rk[o];
+            }
+        }
+    };
+    float rqv[kMaxPass], rkv[kMaxPass];
+    Unit x = unit(first < nunits ? first : 0);
+    norms(x, first < nunits ? x.ne * ru.nj : 0, rqv, rkv);
+    int64_t it = 0;
+    int s = 0;
+    uint32_t par = 0;
+    bool failed = false;
+    for (int64_t u = first; u < nunits; u += stride, ++it) {
+        const int R = x.ne * ru.nj;  // rows of this unit
+        const uint8_t* st = smq + (size_t)s * ru.stage;
+        const bool more = u + stride < nunits;
+        const Unit xn = unit(more ? u + stride : u);
+        float nrq[kMaxPass], nrk[kMaxPass];
+        norms(xn, more ? xn.ne * ru.nj : 0, nrq, nrk);
+        if (!tc::mbar_wait(&full[s], par, &g_err_bwdr)) s_fail = 1;
+        const int64_t xo = ((x.bb * d.T + x.t0) * d.Hk + x.j0) * Dk;
+        const uint32_t sqr = tc::smem_u32(st), skr = sqr + qb, sdq = skr + qb, sdk = sdq + hb;
+#pragma unroll
+        for (int ps = 0; ps < kMaxPass; ++ps) {
+            const int rbase = ps * kPass + warp * (32 / LPR);  // uniform over the warp
+            if (rbase >= R) break;
+            const int r = rbase + lane / LPR;
+            const bool act = r < R && colact;
+            float u2[2][8], y[2][8];
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) u2[0][cc] = u2[1][cc] = y[0][cc] = y[1][cc] = 0.f;
+            if (act) {
+                lds8(sqr + 2u * (r * Dk + c0), u2[0]);
+                lds8(skr + 2u * (r * Dk + c0), u2[1]);
+                for (int e = 0; e < G; ++e) {
+                    float a8[8], b8[8];
+                    lds8(sdq + 2u * ((r * G + e) * Dk + c0), a8);
+                    lds8(sdk + 2u * ((r * G + e) * Dk + c0), b8);
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        y[0][cc] += a8[cc];
+                        y[1][cc] += b8[cc];
+                    }
+                }
+            }
+#pragma unroll
+            for (int pq = 0; pq < 2; ++pq) {
+                const float rn = pq == 0 ? rqv[ps] : rkv[ps];
+                const float sc = pq == 0 ? sq : 1.f;
+                float dot = 0.f;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    u2[pq][cc] *= rn;
+                    dot = fmaf(u2[pq][cc], y[pq][cc], dot);
+                }
+#pragma unroll
+                for (int off = LPR / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+                if (act) {
+                    float o[8];
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) o[cc] = sc * rn * (y[pq][cc] - u2[pq][cc] * dot);
+                    st8((__nv_bfloat16*)(pq == 0 ? p.dq : p.dk) + xo + r * Dk + c0, o);
+                }
+            }
+        }
+        // every row warp is done with stage s: it takes the unit kQkStages ahead
+        tc::named_sync(1, kQkWarps * 32);
+        if (s_fail) {
+            failed = true;
+            break;
+        }
+        if (tid == 0 && u + kQkStages * stride < nunits) {
+            issue(u + kQkStages * stride, s);
+            ++issued;
+        }
+        x = xn;
+#pragma unroll
+        for (int ps = 0; ps < kMaxPass; ++ps) {
+            rqv[ps] = nrq[ps];
+            rkv[ps] = nrk[ps];
+        }
+        if (++s == kQkStages) {
+            s = 0;
+            par ^= 1u;
+        }
+    }
+    if (failed && tid == 0) {
+        // a bounded wait gave up: the copies still in flight land before the CTA
+        // exits (each wait bounded)
+        for (int64_t i = it; i < issued; ++i)
+            tc::mbar_wait(&full[i % kQkStages], (uint32_t)((i / kQkStages) & 1), &g_err_bwdr);
+    }
 }
 
 // dA_log / ddt_bias: one warp per head.  Lane l sums the partials of rows
@@ -675,6 +978,22 @@ cudaError_t launch_bchunk_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
     return cudaPeekAtLastError();
 }
 
+template <int LPR>
+cudaError_t launch_reduce_stream(const Dims& d, const Ptrs& p, cudaStream_t s) {
+    const QkRun ru = qk_run(d);
+    const size_t smem = (size_t)kQkStages * ru.stage;
+    auto kern = bwd_reduce_stream_kernel<LPR>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int64_t nunits = d.B * ((d.T + ru.n - 1) / ru.n) * ru.ks;
+    const int64_t ngate = d.NC * d.B * ((d.Hv + kGateHeadsB - 1) / kGateHeadsB);
+    int64_t grid = 2 * (int64_t)sm_count();  // two CTAs per SM, each looping over units
+    const int64_t need = nunits > ngate ? nunits : ngate;
+    if (need < grid) grid = need > 0 ? need : 1;
+    kern<<<(unsigned)grid, kQkWarps * 32 + 32, smem, s>>>(d, p, ru);
+    return cudaPeekAtLastError();
+}
+
 template <typename TI>
 cudaError_t launch_reduce_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
     const int64_t nblk = qk_blocks(d) + d.NC * d.B * ((d.Hv + kGateHeadsB - 1) / kGateHeadsB);
@@ -684,10 +1003,16 @@ cudaError_t launch_reduce_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
         if (lpr == 32) bwd_reduce_kernel<TI, PT, 32><<<(unsigned)nblk, 256, 0, s>>>(d, p);
         else bwd_reduce_kernel<TI, PT, 0><<<(unsigned)nblk, 256, 0, s>>>(d, p);
     };
-    if (tc_path(d))
+    if (qk_stream_ok(d)) {
+        const cudaError_t e = lpr == 32 ? launch_reduce_stream<32>(d, p, s)
+                              : lpr == 16 ? launch_reduce_stream<16>(d, p, s)
+                                          : launch_reduce_stream<8>(d, p, s);
+        if (e != cudaSuccess) return e;
+    } else if (tc_path(d)) {
         go(__nv_bfloat16());
-    else
+    } else {
         go(float());
+    }
     if (d.gates == 1) {  // log_decay / beta inputs: no per-head parameters to sum
         count_launches(1);
         return cudaPeekAtLastError();
