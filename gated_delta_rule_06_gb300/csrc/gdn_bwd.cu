@@ -736,22 +736,28 @@ __device__ __forceinline__ void lds8(uint32_t a, float* v) {
     }
 }
 
+// Warps: kQkWarps row warps, then one producer warp (lane 0 issues the copies
+// of a stage once every row warp has released it), then the gate warp.
+constexpr int kQkThreads = kQkWarps * 32 + 64;
+
 template <int LPR>
-__global__ void __launch_bounds__(kQkWarps * 32 + 32, 2)
-    bwd_reduce_stream_kernel(Dims d, Ptrs p, QkRun ru) {
+__global__ void __launch_bounds__(kQkThreads, 2) bwd_reduce_stream_kernel(Dims d, Ptrs p, QkRun ru) {
     extern __shared__ __align__(128) uint8_t smq[];
-    __shared__ uint64_t full[kQkStages];
-    __shared__ int s_fail;
+    __shared__ uint64_t full[kQkStages], empty[kQkStages];
+    __shared__ volatile int s_stop;  // units the producer issued, once it gave up (else -1)
     __shared__ float gA[kChunk][kGateHeadsB + 1];
     __shared__ float gD[kChunk][kGateHeadsB + 1];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
-        for (int s = 0; s < kQkStages; ++s) tc::mbar_init(&full[s], 1);
+        for (int s = 0; s < kQkStages; ++s) {
+            tc::mbar_init(&full[s], 1);          // the producer's arrival with the byte count
+            tc::mbar_init(&empty[s], kQkWarps);  // one arrival per row warp
+        }
         tc::fence_mbar_init();
-        s_fail = 0;
+        s_stop = -1;
     }
     __syncthreads();
-    if (warp == kQkWarps) {
+    if (warp == kQkWarps + 1) {
         // gate units, as the gate blocks of bwd_reduce_kernel take them
         const int64_t nhz = (d.Hv + kGateHeadsB - 1) / kGateHeadsB;
         const int64_t ngate = d.NC * d.B * nhz;
@@ -786,34 +792,46 @@ __global__ void __launch_bounds__(kQkWarps * 32 + 32, 2)
         x.ne = (int)(d.T - x.t0 < ru.n ? d.T - x.t0 : ru.n);
         return x;
     };
-    const __nv_bfloat16* q = (const __nv_bfloat16*)p.q;
-    const __nv_bfloat16* k = (const __nv_bfloat16*)p.k;
-    const __nv_bfloat16* dqh = (const __nv_bfloat16*)p.dqh;
-    const __nv_bfloat16* dkh = (const __nv_bfloat16*)p.dkh;
-    auto issue = [&](int64_t u, int s) {
-        const Unit x = unit(u);
-        uint8_t* st = smq + (size_t)s * ru.stage;
-        const uint32_t b1 = (uint32_t)(x.ne * ru.nj * Dk * 2), bh = b1 * (uint32_t)G;
-        const int64_t xo = ((x.bb * d.T + x.t0) * d.Hk + x.j0) * Dk;
-        const int64_t ho = ((x.bb * d.Tp + x.t0) * d.Hv + (int64_t)x.j0 * G) * Dk;
-        tc::mbar_arrive_expect_tx(&full[s], 2 * b1 + 2 * bh);
-        tc::bulk_g2s(st, q + xo, b1, &full[s]);
-        tc::bulk_g2s(st + qb, k + xo, b1, &full[s]);
-        tc::bulk_g2s(st + 2 * qb, dqh + ho, bh, &full[s]);
-        tc::bulk_g2s(st + 2 * qb + hb, dkh + ho, bh, &full[s]);
-    };
+    // this CTA's units: first, first + stride, ...
     const int64_t first = blockIdx.x, stride = gridDim.x;
-    int64_t issued = 0;  // thread 0: units of this CTA issued so far
-    if (tid == 0)
-        for (int s = 0; s < kQkStages && first + s * stride < nunits; ++s, ++issued) issue(first + s * stride, s);
+    const int mine = first < nunits ? (int)((nunits - 1 - first) / stride + 1) : 0;
+    if (warp == kQkWarps) {
+        if (lane == 0) {
+            const __nv_bfloat16* q = (const __nv_bfloat16*)p.q;
+            const __nv_bfloat16* k = (const __nv_bfloat16*)p.k;
+            const __nv_bfloat16* dqh = (const __nv_bfloat16*)p.dqh;
+            const __nv_bfloat16* dkh = (const __nv_bfloat16*)p.dkh;
+            int s = 0;
+            uint32_t par = 0;  // parity of the empty phase to wait for, from the second round on
+            for (int i = 0; i < mine; ++i) {
+                if (i >= kQkStages && !tc::mbar_wait(&empty[s], par, &g_err_bwdr)) {
+                    s_stop = i;  // a bounded wait gave up: no more copies
+                    break;
+                }
+                const Unit x = unit(first + (int64_t)i * stride);
+                uint8_t* st = smq + (size_t)s * ru.stage;
+                const uint32_t b1 = (uint32_t)(x.ne * ru.nj * Dk * 2), bh = b1 * (uint32_t)G;
+                const int64_t xo = ((x.bb * d.T + x.t0) * d.Hk + x.j0) * Dk;
+                const int64_t ho = ((x.bb * d.Tp + x.t0) * d.Hv + (int64_t)x.j0 * G) * Dk;
+                tc::mbar_arrive_expect_tx(&full[s], 2 * b1 + 2 * bh);
+                tc::bulk_g2s(st, q + xo, b1, &full[s]);
+                tc::bulk_g2s(st + qb, k + xo, b1, &full[s]);
+                tc::bulk_g2s(st + 2 * qb, dqh + ho, bh, &full[s]);
+                tc::bulk_g2s(st + 2 * qb + hb, dkh + ho, bh, &full[s]);
+                if (++s == kQkStages) {
+                    s = 0;
+                    if (i >= kQkStages) par ^= 1u;
+                }
+            }
+        }
+        return;
+    }
     const int sub = lane % LPR;
     const int c0 = 8 * sub;
     const bool colact = c0 < Dk;
     const float sq = rsqrtf((float)Dk);
     constexpr int kPass = kQkWarps * (32 / LPR);
     constexpr int kMaxPass = kQkPasses;
-    // passes of the row loop a unit needs (uniform over the CTA)
-    const int npass = (ru.n * ru.nj + kPass - 1) / kPass;
     // this thread's row of pass ps: key head j0 + rj[ps] of step t0 + rt[ps]
     int rj[kMaxPass], rt[kMaxPass];
 #pragma unroll
@@ -826,7 +844,6 @@ __global__ void __launch_bounds__(kQkWarps * 32 + 32, 2)
     auto norms = [&](Unit x, int R, float (&rqv)[kMaxPass], float (&rkv)[kMaxPass]) {
 #pragma unroll
         for (int ps = 0; ps < kMaxPass; ++ps) {
-            if (ps >= npass) break;
             const int r = ps * kPass + warp * (32 / LPR) + lane / LPR;
             rqv[ps] = rkv[ps] = 0.f;
             if (r < R) {
@@ -837,26 +854,27 @@ __global__ void __launch_bounds__(kQkWarps * 32 + 32, 2)
         }
     };
     float rqv[kMaxPass], rkv[kMaxPass];
-    Unit x = unit(first < nunits ? first : 0);
-    norms(x, first < nunits ? x.ne * ru.nj : 0, rqv, rkv);
-    int64_t it = 0;
+    Unit x = unit(mine > 0 ? first : 0);
+    norms(x, mine > 0 ? x.ne * ru.nj : 0, rqv, rkv);
     int s = 0;
     uint32_t par = 0;
-    bool failed = false;
-    for (int64_t u = first; u < nunits; u += stride, ++it) {
+    bool ok = true;
+    for (int i = 0; i < mine; ++i) {
+        // a producer that gave up issued units [0, s_stop) only
+        if (s_stop >= 0 && i >= s_stop) break;
         const int R = x.ne * ru.nj;  // rows of this unit
         const uint8_t* st = smq + (size_t)s * ru.stage;
-        const bool more = u + stride < nunits;
-        const Unit xn = unit(more ? u + stride : u);
+        const bool more = i + 1 < mine;
+        const Unit xn = unit(more ? first + (int64_t)(i + 1) * stride : first);
         float nrq[kMaxPass], nrk[kMaxPass];
         norms(xn, more ? xn.ne * ru.nj : 0, nrq, nrk);
-        if (!tc::mbar_wait(&full[s], par, &g_err_bwdr)) s_fail = 1;
+        ok = tc::mbar_wait(&full[s], par, &g_err_bwdr) && ok;
         const int64_t xo = ((x.bb * d.T + x.t0) * d.Hk + x.j0) * Dk;
         const uint32_t sqr = tc::smem_u32(st), skr = sqr + qb, sdq = skr + qb, sdk = sdq + hb;
 #pragma unroll
         for (int ps = 0; ps < kMaxPass; ++ps) {
             const int rbase = ps * kPass + warp * (32 / LPR);  // uniform over the warp
-            if (rbase >= R) break;
+            if (rbase >= R || !ok) break;
             const int r = rbase + lane / LPR;
             const bool act = r < R && colact;
             float u2[2][8], y[2][8];
@@ -896,16 +914,9 @@ __global__ void __launch_bounds__(kQkWarps * 32 + 32, 2)
                 }
             }
         }
-        // every row warp is done with stage s: it takes the unit kQkStages ahead
-        tc::named_sync(1, kQkWarps * 32);
-        if (s_fail) {
-            failed = true;
-            break;
-        }
-        if (tid == 0 && u + kQkStages * stride < nunits) {
-            issue(u + kQkStages * stride, s);
-            ++issued;
-        }
+        // this warp is done with stage s (its shared-memory reads are complete)
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&empty[s]);
         x = xn;
 #pragma unroll
         for (int ps = 0; ps < kMaxPass; ++ps) {
@@ -916,12 +927,6 @@ __global__ void __launch_bounds__(kQkWarps * 32 + 32, 2)
             s = 0;
             par ^= 1u;
         }
-    }
-    if (failed && tid == 0) {
-        // a bounded wait gave up: the copies still in flight land before the CTA
-        // exits (each wait bounded)
-        for (int64_t i = it; i < issued; ++i)
-            tc::mbar_wait(&full[i % kQkStages], (uint32_t)((i / kQkStages) & 1), &g_err_bwdr);
     }
 }
 
@@ -990,7 +995,7 @@ cudaError_t launch_reduce_stream(const Dims& d, const Ptrs& p, cudaStream_t s) {
     int64_t grid = 2 * (int64_t)sm_count();  // two CTAs per SM, each looping over units
     const int64_t need = nunits > ngate ? nunits : ngate;
     if (need < grid) grid = need > 0 ? need : 1;
-    kern<<<(unsigned)grid, kQkWarps * 32 + 32, smem, s>>>(d, p, ru);
+    kern<<<(unsigned)grid, kQkThreads, smem, s>>>(d, p, ru);
     return cudaPeekAtLastError();
 }
 
