@@ -924,7 +924,7 @@ def run_e2e_session(args, w, x, world):
     return {"value": w.B * w.T * world / (ms / 1e3), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
             "api": "gdn_host_step (C ABI, host buffers)",
-            "overlap": ("across steps: two device slots; a step's uploads run under the "
+            "overlap": ("across steps: three device slots; a step's uploads run under the "
                         "previous step's compute, its downloads under the next step's"),
             "timing": "host clock between device-wide synchronisations"}
 

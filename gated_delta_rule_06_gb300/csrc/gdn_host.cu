@@ -1,10 +1,10 @@
 // gdn_host.cu -- training (or inference) steps on HOST buffers.
 //
 // A session owns no device memory: the caller hands it one device arena
-// (gdn_host_session_bytes) that holds two slots of step inputs and outputs,
-// the saved buffer and the workspace.  Each gdn_host_step enqueues, for step n
-// in slot n % 2:
-//   up stream       wait until step n - 2 has finished with the slot;
+// (gdn_host_session_bytes) that holds kSlots = 3 slots of step inputs and
+// outputs, the saved buffer and the workspace.  Each gdn_host_step enqueues, for
+// step n in slot n % 3:
+//   up stream       wait until step n - 3 has finished with the slot;
 //                   host -> device copies of the forward inputs, then of the
 //                   backward-only inputs (d_o, d_state_T)
 //   compute stream  forward, then backward (the caller's stream)
@@ -12,7 +12,11 @@
 //                   forward is done, of the gradients once the backward is
 //                   done; then the slot is released
 // so the copies of a step run under the compute of its neighbours while each
-// step still moves all of its own inputs and results.  The forward and backward
+// step still moves all of its own inputs and results.  A slot's turn (its
+// uploads, its compute, its downloads) is longer than a step when the copies
+// take about as long as the compute; with two slots the next step but one
+// waited for it, with three the uploads of step n + 3 wait only for step n's
+// downloads.  The forward and backward
 // are gdn_forward / gdn_backward (or the log_decay / beta form) on the slot's
 // device buffers; the saved buffer and the workspace are shared by all steps,
 // whose compute is serialised on the one compute stream.
@@ -55,6 +59,8 @@ struct Slot {
     void *o, *dq, *dk, *dv, *da, *db;
     float *state_T, *dA_log, *ddt_bias, *dstate0;
 };
+
+constexpr int kSlots = 3;
 
 struct Plan {
     size_t slot_bytes, saved, ws, total;
@@ -113,7 +119,7 @@ gdn_status make_plan(const gdn_shape* s, int backward, Plan* p) {
     p->slot_bytes = carve_slot(*s, backward, nullptr, nullptr);
     p->saved = align_up(saved);
     p->ws = align_up(ws);
-    p->total = 2 * p->slot_bytes + p->saved + p->ws;
+    p->total = kSlots * p->slot_bytes + p->saved + p->ws;
     return GDN_OK;
 }
 
@@ -123,8 +129,8 @@ struct gdn_host_session {
     gdn_shape shape;
     int gates, backward;
     cudaStream_t compute, up, down;
-    cudaEvent_t ev_in[2], ev_in_b[2], ev_fwd[2], ev_bwd[2], ev_free[2];
-    Slot slot[2];
+    cudaEvent_t ev_in[kSlots], ev_in_b[kSlots], ev_fwd[kSlots], ev_bwd[kSlots], ev_free[kSlots];
+    Slot slot[kSlots];
     void *saved, *ws;
     size_t saved_bytes, ws_bytes;
     int64_t step;
@@ -133,7 +139,7 @@ struct gdn_host_session {
 namespace {
 
 void release(gdn_host_session* s) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSlots; ++i) {
         cudaEvent_t* evs[] = {&s->ev_in[i], &s->ev_in_b[i], &s->ev_fwd[i], &s->ev_bwd[i],
                               &s->ev_free[i]};
         for (cudaEvent_t* e : evs)
@@ -176,15 +182,14 @@ gdn_status gdn_host_session_create(const gdn_shape* shape, int32_t gates, int32_
     s->backward = backward;
     s->compute = static_cast<cudaStream_t>(stream);
     uint8_t* base = static_cast<uint8_t*>(arena);
-    carve_slot(*shape, backward, base, &s->slot[0]);
-    carve_slot(*shape, backward, base + p.slot_bytes, &s->slot[1]);
-    s->saved = backward ? base + 2 * p.slot_bytes : nullptr;
+    for (int i = 0; i < kSlots; ++i) carve_slot(*shape, backward, base + i * p.slot_bytes, &s->slot[i]);
+    s->saved = backward ? base + kSlots * p.slot_bytes : nullptr;
     s->saved_bytes = backward ? p.saved : 0;
-    s->ws = base + 2 * p.slot_bytes + p.saved;
+    s->ws = base + kSlots * p.slot_bytes + p.saved;
     s->ws_bytes = p.ws;
     cudaError_t e = cudaStreamCreateWithFlags(&s->up, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s->down, cudaStreamNonBlocking);
-    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+    for (int i = 0; i < kSlots && e == cudaSuccess; ++i) {
         cudaEvent_t* evs[] = {&s->ev_in[i], &s->ev_in_b[i], &s->ev_fwd[i], &s->ev_bwd[i],
                               &s->ev_free[i]};
         for (cudaEvent_t* ev : evs)
@@ -212,14 +217,14 @@ gdn_status gdn_host_step(gdn_host_session* s, const gdn_host_inputs* in,
             return GDN_ERR_INVALID_ARG;
         if (g0 && (!out->dA_log || !out->ddt_bias)) return GDN_ERR_INVALID_ARG;
     }
-    const int sl = (int)(s->step & 1);
+    const int sl = (int)(s->step % kSlots);
     const Slot& d = s->slot[sl];
     const Sizes z = sizes_of(sh);
     const uint8_t* mask = sh.has_mask ? d.mask : nullptr;
     const float* state0 = in->state0 ? d.state0 : nullptr;
     const float* dST = (s->backward && in->d_state_T) ? d.d_state_T : nullptr;
 
-    // up: the slot's previous step (n - 2) must have released it (an event that
+    // up: the slot's previous step (n - 3) must have released it (an event that
     // was never recorded counts as complete)
     cudaError_t e = cudaStreamWaitEvent(s->up, s->ev_free[sl], 0);
     auto h2d = [&](void* dst, const void* src, size_t n) {

@@ -9,15 +9,15 @@
  * serving loop calls with its tensors in host memory.
  *
  * A session moves each step's inputs from host to device memory, runs the
- * forward (and the backward), and moves the results back.  It keeps two slots
- * of device buffers and three streams (the caller's `stream` for compute, and an
- * upload and a download stream of its own), so the copies of one step run
- * under the compute of the steps next to it.
+ * forward (and the backward), and moves the results back.  It keeps three
+ * slots of device buffers and three streams (the caller's `stream` for compute,
+ * and an upload and a download stream of its own), so the copies of one step
+ * run under the compute of the steps next to it.
  *
  *   - The session allocates no device memory.  The caller passes one device
  *     arena of gdn_host_session_bytes() bytes, 256-byte aligned, that it owns
  *     and keeps alive until gdn_host_session_destroy returns.
- *   - The session creates two CUDA streams and ten events on the current device
+ *   - The session creates two CUDA streams and fifteen events on the current device
  *     and destroys them in gdn_host_session_destroy.
  *   - gdn_host_step only enqueues.  The caller must leave that step's host
  *     input buffers unchanged and must not read its host output buffers until
@@ -84,7 +84,7 @@ typedef struct {
     float* dstate0;
 } gdn_host_outputs;
 
-/* Bytes of the device arena a session of this shape needs: two slots of one
+/* Bytes of the device arena a session of this shape needs: three slots of one
  * step's inputs and outputs, plus (backward = 1) the saved buffer and the
  * larger of the two workspaces, or (backward = 0) the inference workspace.
  * Host-only. */

@@ -2,8 +2,8 @@
 oracle, element by element, at the parity tolerances of the device entry
 points (per tensor max|x - y| / max|y|: 1e-4 for fp32 inputs, 2e-2 for bf16).
 
-Each session runs several steps on different seeded inputs, so both device
-slots are used and a step whose copies or compute touched its neighbour's slot
+Each session runs several steps on different seeded inputs, so every device
+slot is used and a step whose copies or compute touched its neighbour's slot
 would fail its own comparison.  A plumbing check also asks that a session step
 give bit-for-bit the results of gdn_forward / gdn_backward on the same inputs
 (the session only moves data around those calls).
@@ -57,12 +57,12 @@ def _oracle_ab(x, backward=True):
 @pytest.mark.parametrize("dtype,Dk,Dv", [(torch.bfloat16, 64, 64), (torch.bfloat16, 192, 128),
                                          (torch.float32, 32, 16)])
 def test_training_steps_match_oracle(dtype, Dk, Dv):
-    """Three training steps in a row (slots 0, 1, 0), each on its own inputs."""
+    """Four training steps in a row (slots 0, 1, 2, 0), each on its own inputs."""
     w = wl.custom("hs", 2, 130, 2, 4, Dk, Dv, dtype=dtype, seed=301 + Dk,
                   mask="half_second_batch")
     sess = _session(w)
     steps = []
-    for i in range(3):
+    for i in range(4):
         x = _pinned(wl.make_inputs(w, seed=311 + 7 * i))
         out = sess.outputs()
         sess.step(x, out)
