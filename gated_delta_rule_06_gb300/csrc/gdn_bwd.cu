@@ -673,11 +673,12 @@ __global__ void __launch_bounds__(256) bwd_qk_kernel(Dims d, Ptrs p) {
 // j0 .. j0 + nj - 1 (nj < Hk when a step's rows alone pass the stage size).
 // Its q and k rows ([B, T, Hk, Dk]) and its per-value-head q / k cotangent
 // partials ([B, Tp, Hv, Dk], value heads j G .. j G + G - 1 of key head j) are
-// each one contiguous run, so one thread brings a unit into a shared-memory
-// stage with four bulk copies; kQkStages units are in flight per CTA while
-// eight warps reduce the rows of the oldest from shared memory, with the same
-// arithmetic in the same order as bwd_qk_body.  A ninth warp takes the gate
-// units (da / db and the per-chunk head partials) meanwhile.
+// each one contiguous run, so a producer warp brings a unit into a
+// shared-memory stage with four bulk copies; kQkStages units are in flight per
+// CTA (per-stage full / empty barriers) while eight row warps reduce the rows of
+// the oldest from shared memory, with the same arithmetic in the same order as
+// bwd_qk_body (the rows' norms loaded one unit ahead).  A tenth warp takes the
+// gate units (da / db and the per-chunk head partials) meanwhile.
 constexpr int kQkStages = 3;
 constexpr uint32_t kQkStageTarget = 32 * 1024;  // bytes of one stage at the most, where a key head fits
 constexpr int kQkWarps = 8;
@@ -700,6 +701,7 @@ QkRun qk_run(const Dims& d) {
         r.n = (int)(kQkStageTarget / (per_kh * d.Hk));
         if (r.n > maxr / d.Hk) r.n = (int)(maxr / d.Hk);
         if (r.n > d.T) r.n = (int)d.T;
+        if (r.n < 1) r.n = 1;
     } else {
         r.ks = (int)d.Hk;  // one key head per unit unless a larger divisor of Hk fits
         for (int ks = 2; ks < d.Hk; ++ks)
