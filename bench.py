@@ -7,13 +7,14 @@ inputs, fp32 state), forward + full backward per step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--gates ab|lb|kc] [--fused-conv K]
-                  [--compress-rank R [--compress-iters N]]
+                  [--compress-rank R [--compress-iters N]] [--eager]
 
 One process per GPU (torchrun for N > 1); every rank runs its own replica
 of the workload (weak scaling, no collective on the data path).  Timing:
-W untimed warm-up steps, then K steps each bracketed by CUDA events on the
-launching stream; L2 is flushed (256 MiB write) between timed steps outside
-the events; barrier + synchronize around the timed region; the max over
+W untimed warm-up steps, then one step's C-ABI calls captured into a CUDA
+graph (eager launches with --eager, or where capture is refused), then K
+replays each bracketed by CUDA events on the launching stream; L2 is flushed
+(256 MiB write) between timed steps outside the events; barrier + synchronize around the timed region; the max over
 ranks is reported.  ``value`` = tokens of all ranks / time.  The per-phase
 kernel times behind the roofline come from a second pass over the same K
 steps with the library's phase events (the timed steps carry none).
@@ -723,6 +724,31 @@ def run_ours(args, w, world, rank, local):
     for _ in range(args.warmup):
         step(xd)
     torch.cuda.synchronize()
+    # One CUDA graph per step: the step's C-ABI calls (the same kernels on the
+    # same buffers) captured once and replayed, so the host's gaps between the
+    # launches drop out of the step.  Eager launches where capture is refused.
+    graph, per_step = None, None
+    launch_mode = "eager launches (--eager)"
+    if not args.eager:
+        try:
+            n_c = lib.gdn_launch_count()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step(xd)
+            per_step = int(lib.gdn_launch_count() - n_c)
+            g.replay()
+            torch.cuda.synchronize()
+            graph = g
+            launch_mode = "one CUDA graph per step (the step's C-ABI calls, captured once, replayed)"
+        except Exception as ex:  # capture refused: the eager loop below times the same calls
+            torch.cuda.synchronize()
+            launch_mode = f"eager launches (graph capture refused: {type(ex).__name__})"
+
+    def run_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step(xd)
 
     # ---- timed region (device time, CUDA events on the launching stream).  The
     # step time carries no per-phase events: recording them between the kernels
@@ -740,11 +766,11 @@ def run_ours(args, w, world, rank, local):
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
         starts[i].record(stream)
-        step(xd)
+        run_step()
         ends[i].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
-    launches = int(lib.gdn_launch_count() - n0)
+    launches = per_step * args.steps if graph is not None else int(lib.gdn_launch_count() - n0)
     barrier(world)
     # phase pass
     lib.gdn_timing_begin()
@@ -838,7 +864,7 @@ def run_ours(args, w, world, rank, local):
         "vs_baseline": (value / PAGE_TOKENS_PER_S[w.name]) if w.name in PAGE_TOKENS_PER_S else None,
         "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded, shapes and distributions of the workload)",
-        "config": config_of(w, args.gates, args.fused_conv, cr, ci),
+        "config": dict(config_of(w, args.gates, args.fused_conv, cr, ci), launch=launch_mode),
         "clocks": clocks,
         "gpu_launches": launches,
         "roofline": roof,
@@ -1019,6 +1045,8 @@ def main():
     ap.add_argument("--workload", default="qwen35_9b_layer_T2048_bf16",
                     choices=[n for n in wl.WORKLOAD_ORDER])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="time eager launches instead of one CUDA graph per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fused-conv", type=int, default=0, metavar="K",
                     help="decode workloads: run the step with a K-tap short convolution "
