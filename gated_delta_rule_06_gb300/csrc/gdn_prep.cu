@@ -183,33 +183,32 @@ __global__ void __launch_bounds__(256) prep_gates_kernel(Dims d, Ptrs p) {
                         p.beta, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
-// The tensor-core path's prep in one launch: blocks [0, NC B ceil(Hv / 8)) take
-// the gates, the rest the q / k norms and images (two independent parts).
+// The tensor-core path's prep in one launch: one CTA per (chunk, key head j,
+// batch) takes the q / k norms and images of its chunk and the gate blocks
+// (chunk, batch, value heads 8 hz .. 8 hz + 7) for hz = j, j + Hk, ...  Every
+// CTA of the launch reserves the images' staging, so the gates ride along in
+// the image CTAs instead of taking CTAs (and staging) of their own.
 __global__ void __launch_bounds__(256) prep_tc_kernel(Dims d, Ptrs p) {
-    const int64_t ngate = d.NC * d.B * ((d.Hv + kGateHeads - 1) / kGateHeads);
-    const int64_t blk = blockIdx.x;
-    if (blk < ngate) {
+    const int64_t r = blockIdx.x;  // (chunk, key head, batch)
+    const int c = (int)(r % d.NC), j = (int)((r / d.NC) % d.Hk), bb = (int)(r / (d.NC * d.Hk));
+    const int nhz = (int)((d.Hv + kGateHeads - 1) / kGateHeads);
+    for (int hz = j; hz < nhz; hz += (int)d.Hk) {
         prep_gates_body<__nv_bfloat16>(d, (const __nv_bfloat16*)p.a, (const __nv_bfloat16*)p.b,
-                                       p.A_log, p.dt_bias, p.mask, p.gam, p.beta,
-                                       (int)(blk % d.NC), (int)((blk / d.NC) % d.B),
-                                       (int)(blk / (d.NC * d.B)));
-    } else {
-        const int64_t r = blk - ngate;  // (chunk, key head, batch)
-        prep_norms_img_body(d, (const __nv_bfloat16*)p.q, (const __nv_bfloat16*)p.k, p.rq, p.rk,
-                            static_cast<uint8_t*>(p.qimg), static_cast<uint8_t*>(p.kimg),
-                            (int)(r % d.NC), (int)((r / d.NC) % d.Hk), (int)(r / (d.NC * d.Hk)));
+                                       p.A_log, p.dt_bias, p.mask, p.gam, p.beta, c, bb, hz);
+        __syncthreads();  // the gate body's shared sums are reused
     }
+    prep_norms_img_body(d, (const __nv_bfloat16*)p.q, (const __nv_bfloat16*)p.k, p.rq, p.rk,
+                        static_cast<uint8_t*>(p.qimg), static_cast<uint8_t*>(p.kimg), c, j, bb);
 }
 
 template <typename TI>
 cudaError_t launch_prep_t(const Dims& d, const Ptrs& p, cudaStream_t s) {
-    const int64_t ngate = d.NC * d.B * ((d.Hv + kGateHeads - 1) / kGateHeads);
     if (tc_path(d)) {
         const int smem = (int)(2 * (d.Dk / 8) * kPanelPad);
         cudaError_t e = cudaFuncSetAttribute(prep_tc_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        prep_tc_kernel<<<(unsigned)(ngate + d.NC * d.Hk * d.B), 256, smem, s>>>(d, p);
+        prep_tc_kernel<<<(unsigned)(d.NC * d.Hk * d.B), 256, smem, s>>>(d, p);
         count_launches(1);
         return cudaPeekAtLastError();
     }
